@@ -1,0 +1,182 @@
+"""GB300 (sm_103a) split-KV grouped-query decode attention.
+
+Thin ctypes binding over ``libattn_decode.so`` (declared in
+``include/attn_decode.h``). Every function here has the name and argument order
+of the C entry point it calls and does argument marshalling only: pointers may
+be given as integers or as tensors (their ``data_ptr()`` is passed), streams as
+integers, ``torch.cuda.Stream`` objects or ``None`` (the current torch stream).
+All arithmetic runs in the library's CUDA kernels; if the library has not been
+built, every call raises ``RuntimeError`` -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "AttnError", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_WORKSPACE",
+    "ATTN_ERR_CUDA", "ATTN_DEVERR_POSITION_CLAMPED", "ATTN_DEVERR_PIPELINE_TIMEOUT",
+    "ATTN_VARIANT_AUTO", "ATTN_VARIANT_SIMT", "ATTN_VARIANT_TC", "library_path", "load",
+    "attn_decode", "attn_decode_ex", "attn_decode_partial", "attn_decode_combine",
+    "attn_split_heuristic", "attn_workspace_size",
+    "attn_read_device_error", "attn_status_string", "attn_last_cuda_error", "attn_version",
+]
+
+ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE, ATTN_ERR_CUDA = range(5)
+ATTN_DEVERR_POSITION_CLAMPED = 0x1
+ATTN_DEVERR_PIPELINE_TIMEOUT = 0x2
+ATTN_VARIANT_AUTO, ATTN_VARIANT_SIMT, ATTN_VARIANT_TC = 0, 1, 2
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        name = attn_status_string(status)
+        extra = ""
+        if status == ATTN_ERR_CUDA:
+            extra = " (cudaError %d)" % attn_last_cuda_error()
+        super().__init__("%s returned %s%s" % (where, name, extra))
+
+
+def library_path() -> str:
+    return os.path.join(_PKG, "libattn_decode.so")
+
+
+def load():
+    """Load the library (once). Raises RuntimeError if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError("libattn_decode.so is not built (%s); run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`" % path)
+        lib = ctypes.CDLL(path)
+        vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        lib.attn_decode.restype = i32
+        lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, vp]
+        lib.attn_decode_ex.restype = i32
+        lib.attn_decode_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i64, i32, i32,
+                                       i32, vp, sz, vp]
+        lib.attn_decode_partial.restype = i32
+        lib.attn_decode_partial.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, i64, i32, i32,
+                                            i32, vp, sz, vp]
+        lib.attn_decode_combine.restype = i32
+        lib.attn_decode_combine.argtypes = [vp, sz, vp, i32, i32, i32, i32, vp]
+        lib.attn_split_heuristic.restype = i32
+        lib.attn_split_heuristic.argtypes = [i32, i32, i32, i32, i64, i32]
+        lib.attn_workspace_size.restype = sz
+        lib.attn_workspace_size.argtypes = [i32, i32, i32, i32]
+        lib.attn_read_device_error.restype = i32
+        lib.attn_read_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_status_string.argtypes = [i32]
+        lib.attn_last_cuda_error.restype = i32
+        lib.attn_last_cuda_error.argtypes = []
+        lib.attn_version.restype = i32
+        lib.attn_version.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    raise TypeError("expected an int address or a tensor, got %r" % type(x))
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    if hasattr(s, "cuda_stream"):
+        return s.cuda_stream
+    raise TypeError("expected a stream handle, torch.cuda.Stream or None")
+
+
+def _check(status: int, where: str):
+    if status != ATTN_OK:
+        raise AttnError(status, where)
+
+
+def attn_decode(q, k_cache, v_cache, positions, out, n_seq, n_head, n_kv_head, head_dim, scale,
+                stream=None):
+    """o = softmax(q·Kᵀ·scale)·V for one sequence (see include/attn_decode.h)."""
+    _check(load().attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(positions), _ptr(out),
+                              n_seq, n_head, n_kv_head, head_dim, scale, _stream(stream)),
+           "attn_decode")
+
+
+def attn_decode_ex(q, k_cache, v_cache, positions, out, n_seq, n_head, n_kv_head, head_dim, scale,
+                   cap, n_splits=0, split_len=0, variant=ATTN_VARIANT_AUTO, workspace=None,
+                   workspace_bytes=0, stream=None):
+    """Several sequences, explicit capacity, split and workspace control."""
+    if workspace is not None and not workspace_bytes and hasattr(workspace, "nbytes"):
+        workspace_bytes = workspace.nbytes
+    _check(load().attn_decode_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(positions), _ptr(out),
+                                 n_seq, n_head, n_kv_head, head_dim, scale, cap, n_splits,
+                                 split_len, variant, _ptr(workspace), workspace_bytes,
+                                 _stream(stream)),
+           "attn_decode_ex")
+
+
+def attn_decode_partial(q, k_cache, v_cache, positions, n_seq, n_head, n_kv_head, head_dim,
+                        scale, cap, n_splits, split_len=0, variant=ATTN_VARIANT_AUTO,
+                        workspace=None, workspace_bytes=0, stream=None):
+    """Stage one (partials into `workspace`); see include/attn_decode.h."""
+    if workspace is not None and not workspace_bytes and hasattr(workspace, "nbytes"):
+        workspace_bytes = workspace.nbytes
+    _check(load().attn_decode_partial(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(positions),
+                                      n_seq, n_head, n_kv_head, head_dim, scale, cap, n_splits,
+                                      split_len, variant, _ptr(workspace), workspace_bytes,
+                                      _stream(stream)),
+           "attn_decode_partial")
+
+
+def attn_decode_combine(workspace, workspace_bytes, out, n_seq, n_head, head_dim, n_splits,
+                        stream=None):
+    """Stage two (combine the partials in `workspace` into `out`)."""
+    if not workspace_bytes and hasattr(workspace, "nbytes"):
+        workspace_bytes = workspace.nbytes
+    _check(load().attn_decode_combine(_ptr(workspace), workspace_bytes, _ptr(out), n_seq, n_head,
+                                      head_dim, n_splits, _stream(stream)),
+           "attn_decode_combine")
+
+
+def attn_split_heuristic(n_seq, n_head, n_kv_head, head_dim, cap, sm_count) -> int:
+    return load().attn_split_heuristic(n_seq, n_head, n_kv_head, head_dim, cap, sm_count)
+
+
+def attn_workspace_size(n_seq, n_head, head_dim, n_splits) -> int:
+    return load().attn_workspace_size(n_seq, n_head, head_dim, n_splits)
+
+
+def attn_read_device_error(stream=None) -> int:
+    flags = ctypes.c_uint(0)
+    _check(load().attn_read_device_error(_stream(stream), ctypes.byref(flags)),
+           "attn_read_device_error")
+    return flags.value
+
+
+def attn_status_string(status) -> str:
+    return load().attn_status_string(status).decode()
+
+
+def attn_last_cuda_error() -> int:
+    return load().attn_last_cuda_error()
+
+
+def attn_version() -> int:
+    return load().attn_version()

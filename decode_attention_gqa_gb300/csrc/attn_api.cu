@@ -1,0 +1,408 @@
+// attn_api.cu -- the C ABI of include/attn_decode.h: argument validation, the
+// split-count heuristic, workspace sizing and ownership, tensor-map encoding,
+// the device error word, and dispatch to the per-head_dim kernel units.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "attn_decode.h"
+#include "attn_launch.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxSplits = 4096;                  // combine keeps P weights in shared memory
+constexpr int64_t kMaxFlatRows = (int64_t)1 << 31; // TMA row coordinates are int32
+constexpr int64_t kUnknownCap = kMaxFlatRows - 1024;
+
+thread_local int t_last_cuda_error = 0;
+
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::set<std::pair<const void *, int>> g_smem_done;
+
+struct DeviceState {
+    bool ready = false;
+    int sm_count = 0;
+    unsigned *err_word = nullptr;                 // device address of g_attn_error_word
+    void *ws = nullptr;                           // library-owned workspace
+    size_t ws_bytes = 0;
+};
+DeviceState g_dev[kMaxDevices];
+
+} // namespace
+
+// One sticky error word per device, set by the kernels with atomicOr.
+__device__ unsigned g_attn_error_word;
+
+namespace {
+
+attn_status cuda_fail(cudaError_t e)
+{
+    t_last_cuda_error = (int)e;
+    return ATTN_ERR_CUDA;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Per-device state; called with g_mu held and the device current.
+cudaError_t device_state(int dev, DeviceState **out)
+{
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    DeviceState &d = g_dev[dev];
+    if (!d.ready) {
+        cudaError_t e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_attn_error_word);
+        if (e != cudaSuccess) return e;
+        d.err_word = static_cast<unsigned *>(p);
+        d.ready = true;
+    }
+    *out = &d;
+    return cudaSuccess;
+}
+
+attn::KernelInfo kernel_info(int head_dim, int group, int variant)
+{
+    switch (head_dim) {
+    case 8: return attn::kernel_info_hd8(group, variant);
+    case 64: return attn::kernel_info_hd64(group, variant);
+    case 128: return attn::kernel_info_hd128(group, variant);
+    case 256: return attn::kernel_info_hd256(group, variant);
+    default: return attn::KernelInfo{0, 0, false};
+    }
+}
+
+bool head_dim_supported(int hd) { return hd == 8 || hd == 64 || hd == 128 || hd == 256; }
+
+// ATTN_VARIANT_AUTO: the CUDA-core kernel.
+int resolve_variant(int variant, int head_dim, int group)
+{
+    (void)head_dim;
+    (void)group;
+    if (variant == ATTN_VARIANT_AUTO) return attn::kVariantSimt;
+    return variant;
+}
+
+int heuristic(int n_seq, int n_kv_head, int64_t cap, int sm_count, const attn::KernelInfo &ki)
+{
+    const int64_t units = (int64_t)n_seq * n_kv_head;
+    const int64_t slots = (int64_t)sm_count * (ki.blocks_per_sm > 0 ? ki.blocks_per_sm : 1);
+    int64_t P = slots / (units > 0 ? units : 1);      // one full wave of blocks
+    if (P < 1) P = 1;
+    if (cap > 0) {
+        const int64_t most = (cap + attn::kSplitGranule - 1) / attn::kSplitGranule;
+        if (P > most) P = most;                       // no split shorter than one granule at full cap
+    }
+    if (P > kMaxSplits) P = kMaxSplits;
+    return (int)P;
+}
+
+attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache,
+                        const int32_t *positions, float *out, int n_seq, int n_head,
+                        int n_kv_head, int head_dim, float scale, int64_t cap, bool cap_known,
+                        int n_splits, int split_len, int variant, void *workspace,
+                        size_t workspace_bytes, int stages, cudaStream_t stream)
+{
+    // ---- synchronous argument checks, nothing launched yet ----
+    if (n_seq < 0 || n_head <= 0 || n_kv_head <= 0 || head_dim <= 0) return ATTN_ERR_INVALID_ARG;
+    if (n_head % n_kv_head != 0) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (cap < 1) return ATTN_ERR_INVALID_ARG;
+    if (n_splits < 0 || n_splits > kMaxSplits || split_len < 0) return ATTN_ERR_INVALID_ARG;
+    if (variant != ATTN_VARIANT_AUTO && variant != ATTN_VARIANT_SIMT && variant != ATTN_VARIANT_TC)
+        return ATTN_ERR_INVALID_ARG;
+    if (n_seq > 0 && (!q || !k_cache || !v_cache || !positions)) return ATTN_ERR_INVALID_ARG;
+    if (n_seq > 0 && (stages & attn::kStageCombine) && !out) return ATTN_ERR_INVALID_ARG;
+    if (n_seq > 65535 || n_kv_head > 65535) return ATTN_ERR_INVALID_ARG;   // grid y / z limits
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(positions) ||
+        !aligned16(out))
+        return ATTN_ERR_INVALID_ARG;
+    if ((int64_t)n_seq * cap > kMaxFlatRows - 1024) return ATTN_ERR_INVALID_ARG;
+    const int group = n_head / n_kv_head;
+    if (!head_dim_supported(head_dim) || group > 8) return ATTN_ERR_UNSUPPORTED;
+    const int v = resolve_variant(variant, head_dim, group);
+    const attn::KernelInfo ki = kernel_info(head_dim, group, v);
+    if (!ki.available) return ATTN_ERR_UNSUPPORTED;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return ATTN_ERR_INVALID_ARG;
+    if (n_seq == 0) return ATTN_OK;
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+
+    std::unique_lock<std::mutex> lock(g_mu);
+    DeviceState *ds = nullptr;
+    e = device_state(dev, &ds);
+    if (e != cudaSuccess) return cuda_fail(e);
+
+    const int P = n_splits > 0 ? n_splits
+                               : heuristic(n_seq, n_kv_head, cap_known ? cap : 0, ds->sm_count, ki);
+    if (split_len > 0 && (int64_t)P * split_len < cap) return ATTN_ERR_INVALID_ARG;
+    const size_t need = attn_workspace_size(n_seq, n_head, head_dim, P);
+
+    if (!workspace) {
+        if (stages != (attn::kStagePartial | attn::kStageCombine)) return ATTN_ERR_INVALID_ARG;
+        if (ds->ws_bytes < need) {
+            cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+            e = cudaStreamIsCapturing(stream, &cs);
+            if (e != cudaSuccess) return cuda_fail(e);
+            if (cs != cudaStreamCaptureStatusNone) return ATTN_ERR_WORKSPACE;
+            if (ds->ws) {
+                e = cudaFree(ds->ws);                 // synchronises with work using it
+                ds->ws = nullptr;
+                ds->ws_bytes = 0;
+                if (e != cudaSuccess) return cuda_fail(e);
+            }
+            e = cudaMalloc(&ds->ws, need);
+            if (e != cudaSuccess) return cuda_fail(e);
+            ds->ws_bytes = need;
+        }
+        workspace = ds->ws;
+    } else if (workspace_bytes < need) {
+        return ATTN_ERR_WORKSPACE;
+    }
+    unsigned *err_word = ds->err_word;
+    lock.unlock();
+
+    attn::LaunchRequest r{};
+    r.pa.q = q;
+    r.pa.k = static_cast<const __half *>(k_cache);
+    r.pa.v = static_cast<const __half *>(v_cache);
+    r.pa.positions = positions;
+    const size_t o_bytes = align256((size_t)n_seq * n_head * P * head_dim * sizeof(float));
+    r.pa.ws_o = static_cast<float *>(workspace);
+    r.pa.ws_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) + o_bytes);
+    r.pa.err = err_word;
+    r.pa.n_head = n_head;
+    r.pa.n_kv_head = n_kv_head;
+    r.pa.n_splits = P;
+    r.pa.split_len = split_len;
+    r.pa.cap = cap;
+    r.pa.qscale = (float)((double)scale * 1.4426950408889634);
+    r.k_cache = k_cache;
+    r.v_cache = v_cache;
+    r.out = out;
+    r.n_seq = n_seq;
+    r.head_dim = head_dim;
+    r.group = group;
+    r.variant = v;
+    r.stages = stages;
+    r.stream = stream;
+
+    switch (head_dim) {
+    case 8: e = attn::launch_hd8(r); break;
+    case 64: e = attn::launch_hd64(r); break;
+    case 128: e = attn::launch_hd128(r); break;
+    case 256: e = attn::launch_hd256(r); break;
+    default: return ATTN_ERR_UNSUPPORTED;
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    return ATTN_OK;
+}
+
+} // namespace
+
+// ---------------------------------------------------------------------------
+// Internal helpers used by the kernel translation units.
+// ---------------------------------------------------------------------------
+namespace attn {
+
+cudaError_t encode_kv_map(CUtensorMap *map, const void *base, int64_t rows, int n_kv_head,
+                          int head_dim, int box_x, int box_rows)
+{
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!g_encode) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult qr;
+            cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                             cudaEnableDefault, &qr);
+            if (e != cudaSuccess) return e;
+            if (qr != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+    }
+    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)n_kv_head, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)n_kv_head * head_dim * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)box_x, 1u, (cuuint32_t)box_rows};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUtensorMapSwizzle sw = (box_x * 2 == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims,
+                                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t ensure_smem_attr(const void *func, int bytes)
+{
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_smem_done.count({func, dev})) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) g_smem_done.insert({func, dev});
+    return e;
+}
+
+cudaError_t launch_pdl(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       void **args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, func, args);
+}
+
+} // namespace attn
+
+// ---------------------------------------------------------------------------
+// Public C ABI.
+// ---------------------------------------------------------------------------
+extern "C" {
+
+attn_status attn_decode(const float *q, const void *k_cache, const void *v_cache,
+                        const int32_t *positions, float *out, int n_seq, int n_head,
+                        int n_kv_head, int head_dim, float scale, attn_stream_t stream)
+{
+    if (n_seq != 1) return ATTN_ERR_INVALID_ARG;
+    return decode_impl(q, k_cache, v_cache, positions, out, n_seq, n_head, n_kv_head, head_dim,
+                       scale, kUnknownCap, false, 0, 0, ATTN_VARIANT_AUTO, nullptr, 0,
+                       attn::kStagePartial | attn::kStageCombine,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_decode_ex(const float *q, const void *k_cache, const void *v_cache,
+                           const int32_t *positions, float *out, int n_seq, int n_head,
+                           int n_kv_head, int head_dim, float scale, int64_t cap,
+                           int n_splits, int split_len, int variant, void *workspace,
+                           size_t workspace_bytes, attn_stream_t stream)
+{
+    return decode_impl(q, k_cache, v_cache, positions, out, n_seq, n_head, n_kv_head, head_dim,
+                       scale, cap, true, n_splits, split_len, variant, workspace, workspace_bytes,
+                       attn::kStagePartial | attn::kStageCombine,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_decode_partial(const float *q, const void *k_cache, const void *v_cache,
+                                const int32_t *positions, int n_seq, int n_head, int n_kv_head,
+                                int head_dim, float scale, int64_t cap, int n_splits,
+                                int split_len, int variant, void *workspace,
+                                size_t workspace_bytes, attn_stream_t stream)
+{
+    if (n_splits <= 0 || !workspace) return ATTN_ERR_INVALID_ARG;
+    return decode_impl(q, k_cache, v_cache, positions, nullptr, n_seq, n_head, n_kv_head,
+                       head_dim, scale, cap, true, n_splits, split_len, variant, workspace,
+                       workspace_bytes, attn::kStagePartial, reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_decode_combine(const void *workspace, size_t workspace_bytes, float *out,
+                                int n_seq, int n_head, int head_dim, int n_splits,
+                                attn_stream_t stream)
+{
+    if (n_seq < 0 || n_head <= 0 || n_splits <= 0 || n_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+    if (n_seq > 65535) return ATTN_ERR_INVALID_ARG;
+    if (!head_dim_supported(head_dim)) return ATTN_ERR_UNSUPPORTED;
+    if (n_seq == 0) return ATTN_OK;
+    if (!workspace || !out || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return ATTN_ERR_INVALID_ARG;
+    if (workspace_bytes < attn_workspace_size(n_seq, n_head, head_dim, n_splits))
+        return ATTN_ERR_WORKSPACE;
+    attn::LaunchRequest r{};
+    const size_t o_bytes = align256((size_t)n_seq * n_head * n_splits * head_dim * sizeof(float));
+    r.pa.ws_o = static_cast<float *>(const_cast<void *>(workspace));
+    r.pa.ws_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(const_cast<void *>(workspace)) + o_bytes);
+    r.pa.n_head = n_head;
+    r.pa.n_splits = n_splits;
+    r.out = out;
+    r.n_seq = n_seq;
+    r.head_dim = head_dim;
+    r.group = 1;
+    r.variant = attn::kVariantSimt;
+    r.stages = attn::kStageCombine;
+    r.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    switch (head_dim) {
+    case 8: e = attn::launch_hd8(r); break;
+    case 64: e = attn::launch_hd64(r); break;
+    case 128: e = attn::launch_hd128(r); break;
+    case 256: e = attn::launch_hd256(r); break;
+    default: return ATTN_ERR_UNSUPPORTED;
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    return ATTN_OK;
+}
+
+int attn_split_heuristic(int n_seq, int n_head, int n_kv_head, int head_dim, int64_t cap,
+                         int sm_count)
+{
+    if (n_seq <= 0 || n_head <= 0 || n_kv_head <= 0 || n_head % n_kv_head != 0) return 0;
+    const int group = n_head / n_kv_head;
+    if (!head_dim_supported(head_dim) || group > 8) return 0;
+    if (sm_count <= 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+        if (cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+    }
+    const int v = resolve_variant(ATTN_VARIANT_AUTO, head_dim, group);
+    return heuristic(n_seq, n_kv_head, cap, sm_count, kernel_info(head_dim, group, v));
+}
+
+size_t attn_workspace_size(int n_seq, int n_head, int head_dim, int n_splits)
+{
+    if (n_seq <= 0 || n_head <= 0 || head_dim <= 0 || n_splits <= 0) return 0;
+    const size_t slots = (size_t)n_seq * n_head * n_splits;
+    return align256(slots * head_dim * sizeof(float)) + align256(slots * 2 * sizeof(float));
+}
+
+attn_status attn_read_device_error(attn_stream_t stream, unsigned int *flags)
+{
+    if (!flags) return ATTN_ERR_INVALID_ARG;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    unsigned v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_attn_error_word, sizeof(v));
+    if (e != cudaSuccess) return cuda_fail(e);
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_attn_error_word, &zero, sizeof(zero));
+    if (e != cudaSuccess) return cuda_fail(e);
+    *flags = v;
+    return ATTN_OK;
+}
+
+const char *attn_status_string(attn_status status)
+{
+    switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    default: return "ATTN_ERR_UNKNOWN";
+    }
+}
+
+int attn_last_cuda_error(void) { return t_last_cuda_error; }
+
+int attn_version(void) { return 10000; }
+
+} // extern "C"

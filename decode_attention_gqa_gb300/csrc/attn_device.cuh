@@ -1,0 +1,218 @@
+// attn_device.cuh -- device-side helpers shared by the decode-attention kernels:
+// the argument block, the split rule, mbarriers with bounded waits, TMA tile
+// loads, programmatic-dependent-launch controls and small math wrappers.
+// sm_103a only (inline PTX for mbarrier, cp.async.bulk.tensor, griddepcontrol,
+// redux.sync.f32, ex2.approx).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace attn {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Error bits, the same values as ATTN_DEVERR_* in include/attn_decode.h.
+constexpr unsigned kErrPositionClamped = 0x1u;
+constexpr unsigned kErrPipelineTimeout = 0x2u;
+
+// A bounded wait gives up after this many nanoseconds of %globaltimer.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+// Rows are handed to splits in multiples of this (count mode).
+constexpr int kSplitGranule = 16;
+
+struct PartialArgs {
+    const float *q;           // [n_seq][n_head][HD] f32
+    const __half *k;          // [n_seq][cap][n_kv_head][HD] f16 (tail tiles are read directly)
+    const __half *v;
+    const int32_t *positions; // [n_seq]
+    float *ws_o;              // [n_seq][n_head][P][HD]   unnormalised partial accumulators
+    float2 *ws_ml;            // [n_seq][n_head][P]       (mx, S), mx in log2 units
+    unsigned *err;            // sticky device error word
+    int n_head;
+    int n_kv_head;
+    int n_splits;             // P
+    int split_len;            // 0 = by count
+    int64_t cap;              // cache rows per sequence
+    float qscale;             // scale * log2(e): scores come out in log2 units
+};
+
+struct CombineArgs {
+    const float *ws_o;
+    const float2 *ws_ml;
+    float *out;               // [n_seq][n_head][HD]
+    int n_head;
+    int n_splits;
+};
+
+// ---------------------------------------------------------------------------
+// a1: rows attended and the split's row range. nkv = positions[s] + 1 clamped
+// to [0, cap] ("10 · R4" §2.2). By count: chunk = ceil(nkv / P) rounded up to
+// kSplitGranule rows; by block (Red Lite dev35 "Change"): chunk = split_len.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int64_t rows_attended(const PartialArgs &a, int s, bool report)
+{
+    int64_t n = (int64_t)__ldg(a.positions + s) + 1;
+    if (n < 0 || n > a.cap) {
+        if (report) atomicOr(a.err, kErrPositionClamped);
+        n = n < 0 ? 0 : a.cap;
+    }
+    return n;
+}
+
+__device__ __forceinline__ void split_range(int64_t nkv, int sp, int n_splits, int split_len,
+                                            int64_t &lo, int64_t &hi)
+{
+    int64_t chunk;
+    if (split_len > 0) {
+        chunk = split_len;
+    } else {
+        chunk = (nkv + n_splits - 1) / n_splits;
+        chunk = (chunk + kSplitGranule - 1) / kSplitGranule * kSplitGranule;
+    }
+    lo = (int64_t)sp * chunk;
+    hi = lo + chunk < nkv ? lo + chunk : nkv;
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// Shared-memory addresses and mbarriers.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}"
+                 :: "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, unsigned bytes)
+{
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+                 :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity)
+{
+    unsigned ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase with the given parity to complete. Gives up after
+// kWaitLimitNs and returns false; never spins forever.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, unsigned parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// TMA: one 3-D tile (x = element within the row, y = KV head, z = cache row)
+// into shared memory, completion counted on an mbarrier.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y, int z)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z),
+           "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Math.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float warp_max(float x)
+{
+    float y;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float warp_sum(float x)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+// Eight f16 (one 16-byte unit) to f32.
+__device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8])
+{
+    const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 t = __half22float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory tile layout written by TMA. A tile of R rows x HD f16 is stored
+// as HD/64 column chunks; chunk c is R rows of 128 bytes, with the 16-byte
+// units of row r permuted by r & 7 (the 128-byte swizzle). head_dim 8 rows
+// (16 bytes) are stored densely. Returns the byte offset of 16-byte unit U of
+// row r.
+// ---------------------------------------------------------------------------
+template <int HD, int R>
+__device__ __forceinline__ uint32_t tile_unit_offset(int r, int U)
+{
+    if constexpr (HD >= 64) {
+        const int c = U >> 3, u = U & 7;
+        return (uint32_t)(c * R * 128 + r * 128 + ((u ^ (r & 7)) << 4));
+    } else {
+        return (uint32_t)(r * (HD * 2) + U * 16);
+    }
+}
+
+} // namespace attn

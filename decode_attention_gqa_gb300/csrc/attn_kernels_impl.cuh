@@ -1,0 +1,104 @@
+// attn_kernels_impl.cuh -- per-head_dim kernel instantiation and launch.
+// Each attn_kernels_hd<N>.cu includes this once with its own head_dim, so the
+// instantiations compile in parallel.
+#pragma once
+
+#include "attn_combine.cuh"
+#include "attn_launch.h"
+#include "attn_partial.cuh"
+
+namespace attn {
+
+// Pipeline shape of the CUDA-core partial kernel per head_dim: compute warps
+// and stages, sized so the stage ring fits the 227 KB shared-memory budget.
+template <int HD> struct SimtShape;
+template <> struct SimtShape<8>   { static constexpr int NWC = 4, S = 4; };
+template <> struct SimtShape<64>  { static constexpr int NWC = 4, S = 3; };
+template <> struct SimtShape<128> { static constexpr int NWC = 4, S = 3; };
+template <> struct SimtShape<256> { static constexpr int NWC = 2, S = 3; };
+
+template <int HD, int G>
+using SimtCfg = PartialCfg<HD, G, SimtWarp, SimtShape<HD>::NWC, SimtShape<HD>::S>;
+
+template <class Cfg, int HD, int G>
+cudaError_t launch_partial(const LaunchRequest &r)
+{
+    alignas(64) CUtensorMap kmap, vmap;
+    const int64_t rows = (int64_t)r.n_seq * r.pa.cap;
+    cudaError_t e = encode_kv_map(&kmap, r.k_cache, rows, r.pa.n_kv_head, HD, Cfg::BOX_X, Cfg::TILE);
+    if (e != cudaSuccess) return e;
+    e = encode_kv_map(&vmap, r.v_cache, rows, r.pa.n_kv_head, HD, Cfg::BOX_X, Cfg::TILE);
+    if (e != cudaSuccess) return e;
+    const void *fn = reinterpret_cast<const void *>(&attn_split_partial<Cfg, HD, G>);
+    e = ensure_smem_attr(fn, (int)Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    PartialArgs pa = r.pa;
+    void *args[] = {&kmap, &vmap, &pa};
+    return launch_pdl(fn, dim3(pa.n_splits, pa.n_kv_head, r.n_seq), dim3(Cfg::THREADS),
+                      Cfg::SMEM_BYTES, r.stream, args);
+}
+
+template <int HD>
+cudaError_t launch_combine(const LaunchRequest &r)
+{
+    CombineArgs ca;
+    ca.ws_o = r.pa.ws_o;
+    ca.ws_ml = r.pa.ws_ml;
+    ca.out = r.out;
+    ca.n_head = r.pa.n_head;
+    ca.n_splits = r.pa.n_splits;
+    const void *fn = reinterpret_cast<const void *>(&attn_combine<HD>);
+    const size_t smem = combine_smem_bytes<HD>(ca.n_splits);
+    cudaError_t e = ensure_smem_attr(fn, (int)smem);
+    if (e != cudaSuccess) return e;
+    void *args[] = {&ca};
+    return launch_pdl(fn, dim3(ca.n_head, r.n_seq), dim3(CombineCfg<HD>::THREADS), smem, r.stream, args);
+}
+
+template <int HD, int G>
+cudaError_t launch_group(const LaunchRequest &r)
+{
+    cudaError_t e = cudaSuccess;
+    if (r.stages & kStagePartial) {
+        switch (r.variant) {
+        case kVariantSimt: e = launch_partial<SimtCfg<HD, G>, HD, G>(r); break;
+        default: return cudaErrorInvalidValue;
+        }
+        if (e != cudaSuccess) return e;
+    }
+    if (r.stages & kStageCombine) e = launch_combine<HD>(r);
+    return e;
+}
+
+template <int HD>
+cudaError_t launch_for_hd(const LaunchRequest &r)
+{
+    switch (r.group) {
+    case 1: return launch_group<HD, 1>(r);
+    case 2: return launch_group<HD, 2>(r);
+    case 3: return launch_group<HD, 3>(r);
+    case 4: return launch_group<HD, 4>(r);
+    case 5: return launch_group<HD, 5>(r);
+    case 6: return launch_group<HD, 6>(r);
+    case 7: return launch_group<HD, 7>(r);
+    case 8: return launch_group<HD, 8>(r);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int HD>
+KernelInfo kernel_info_for_hd(int group, int variant)
+{
+    KernelInfo k{0, 0, false};
+    if (group < 1 || group > 8) return k;
+    if (variant == kVariantSimt) {
+        using C = SimtCfg<HD, 8>;     // the largest group sets the shared-memory need
+        k.tile_rows = C::TILE;
+        k.blocks_per_sm = (int)(227u * 1024u / C::SMEM_BYTES);
+        if (k.blocks_per_sm < 1) k.blocks_per_sm = 1;
+        k.available = true;
+    }
+    return k;
+}
+
+} // namespace attn

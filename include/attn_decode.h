@@ -1,0 +1,174 @@
+/*
+ * attn_decode.h -- C ABI of the GB300 (sm_103a) split-KV grouped-query decode
+ * attention library, libattn_decode.so.
+ *
+ * The operation (minfer "10 · R4 -- decode split-attention dim-parallel rewrite",
+ * §2.1): for every sequence s and query head h, with one new query row per
+ * sequence (decode, nt == 1),
+ *
+ *     o[s][h] = softmax(q[s][h] · K[s][0:nkv][hk]ᵀ · scale) · V[s][0:nkv][hk]
+ *
+ * where hk = h / (n_head / n_kv_head) is the KV head shared by the contiguous
+ * group of query heads h, and nkv = positions[s] + 1 is read on the device
+ * (§2.2), so one launch configuration serves every context length and the call
+ * can be captured in a CUDA graph and replayed while positions[] advances.
+ *
+ * It runs as two kernels (§2.1): a partial kernel with one block per
+ * (split, KV head, sequence) that runs the online softmax over its row range
+ * [lo, hi) for every query head of the group from a single K/V read and writes
+ * the triple (mx, S, oc); and a combine kernel that takes gmx = max mx over the
+ * splits, reweights each split by exp(mx - gmx) and writes o = acc / S (0 when
+ * every split is empty).
+ *
+ * Conventions for every entry point below
+ *  - Device pointers are caller-owned device memory; the library never frees,
+ *    reallocates or synchronises them, and never synchronises the stream except
+ *    in attn_read_device_error().
+ *  - Layouts are dense row-major:
+ *        q, out      float  [n_seq][n_head][head_dim]
+ *        k_cache,    f16    [n_seq][cap][n_kv_head][head_dim]   (IEEE binary16)
+ *        v_cache     f16    [n_seq][cap][n_kv_head][head_dim]
+ *        positions   int32  [n_seq]      (device memory; nkv_s = positions[s] + 1)
+ *    so row j of sequence s, KV head hk starts at element
+ *    ((s * cap + j) * n_kv_head + hk) * head_dim.
+ *  - All pointers must be 16-byte aligned.
+ *  - Supported shapes: head_dim in {8, 64, 128, 256}; 1 <= n_head / n_kv_head <= 8;
+ *    n_head % n_kv_head == 0. Anything else returns ATTN_ERR_UNSUPPORTED; there
+ *    is no fallback path.
+ *  - Rows [0, nkv_s) are read; rows >= nkv_s are never used. A positions[s]
+ *    outside [-1, cap - 1] is clamped (nkv_s to [0, cap]) and sets
+ *    ATTN_DEVERR_POSITION_CLAMPED in the device error word.
+ *  - Argument errors are returned synchronously, before anything is launched.
+ *    Launch failures return ATTN_ERR_CUDA. No entry point aborts the process.
+ *  - Thread safety: entry points may be called from several host threads.
+ */
+#ifndef ATTN_DECODE_H
+#define ATTN_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers. */
+typedef struct CUstream_st *attn_stream_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, n_head % n_kv_head != 0 */
+    ATTN_ERR_UNSUPPORTED = 2,  /* head_dim or group size outside the compiled set */
+    ATTN_ERR_WORKSPACE = 3,    /* workspace too small (or needed growth while capturing) */
+    ATTN_ERR_CUDA = 4          /* a CUDA runtime/driver call failed; see attn_last_cuda_error */
+} attn_status;
+
+/* Bits of the sticky device error word (attn_read_device_error). */
+#define ATTN_DEVERR_POSITION_CLAMPED 0x1u  /* some positions[s] fell outside [-1, cap-1] */
+#define ATTN_DEVERR_PIPELINE_TIMEOUT 0x2u  /* a bounded in-kernel wait gave up (block skipped) */
+
+/* Kernel variants for attn_decode_ex. */
+#define ATTN_VARIANT_AUTO 0   /* the library picks per (head_dim, group) */
+#define ATTN_VARIANT_SIMT 1   /* CUDA-core f32 partial kernel */
+#define ATTN_VARIANT_TC   2   /* tensor-core (mma, f16 hi/lo split of q and p) partial kernel */
+
+/*
+ * attn_decode -- one layer call, single sequence, library-owned workspace.
+ *
+ * The argument list of the operation itself. n_seq must be 1 (several
+ * sequences need their per-sequence row stride: use attn_decode_ex). The cache
+ * must hold at least positions[0] + 1 rows; with no capacity argument the
+ * library cannot clamp positions[0], so this is the caller's guarantee.
+ * The split count comes from attn_split_heuristic(). The workspace is a
+ * per-device buffer owned by the library; it grows (cudaMalloc) only outside
+ * stream capture, so make one uncaptured call with the largest shape before
+ * capturing. Calls that may run concurrently on different streams must use
+ * attn_decode_ex with their own workspaces.
+ * scale multiplies q·k (1/sqrt(head_dim) for standard attention).
+ */
+attn_status attn_decode(const float *q, const void *k_cache, const void *v_cache,
+                        const int32_t *positions, float *out, int n_seq, int n_head,
+                        int n_kv_head, int head_dim, float scale, attn_stream_t stream);
+
+/*
+ * attn_decode_ex -- full control.
+ *   cap             cache rows per sequence (>= 1); nkv_s is clamped to cap.
+ *   n_splits        splits P per (sequence, KV head); 0 = attn_split_heuristic().
+ *   split_len       0: split by count, chunk = ceil(nkv / P) rounded up to the
+ *                   kernel tile (minfer R4 §2.2); > 0: fixed block of split_len
+ *                   rows per split (Red Lite dev35 "Change"), which needs
+ *                   P * split_len >= cap, else ATTN_ERR_INVALID_ARG.
+ *   variant         ATTN_VARIANT_*.
+ *   workspace       device buffer of at least attn_workspace_size(...) bytes,
+ *                   256-byte aligned; NULL selects the library-owned buffer as in
+ *                   attn_decode. Its contents on entry do not matter.
+ */
+attn_status attn_decode_ex(const float *q, const void *k_cache, const void *v_cache,
+                           const int32_t *positions, float *out, int n_seq, int n_head,
+                           int n_kv_head, int head_dim, float scale, int64_t cap,
+                           int n_splits, int split_len, int variant, void *workspace,
+                           size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * attn_decode_partial / attn_decode_combine -- the two stages of attn_decode_ex
+ * as separate calls (same arguments, same validation), for callers that time
+ * the stages apart or merge partials produced elsewhere before combining.
+ *
+ * attn_decode_partial runs steps a1-a6 ("10 · R4" §2.1 partial kernel) and
+ * leaves the partial triples in `workspace`; n_splits must be given (> 0) and
+ * workspace must be non-NULL, since both calls have to agree on them.
+ * attn_decode_combine runs step a7 (the combine kernel) on a workspace filled
+ * by attn_decode_partial with the same n_seq, n_head, head_dim and n_splits,
+ * and writes `out`. Workspace layout (all f32, both regions 256-byte aligned):
+ *     oc  at byte 0:                      [n_seq][n_head][n_splits][head_dim]
+ *     ml  at byte round_up(4 * n_seq * n_head * n_splits * head_dim, 256):
+ *                                         [n_seq][n_head][n_splits][2] = (mx, S)
+ * where oc is the unnormalised weighted V sum of the split, S its softmax
+ * denominator and mx its running maximum, all relative to exp2(scores *
+ * log2 e) (mx is in log2 units). An empty split has mx = -inf, S = 0 and its
+ * oc is never read.
+ */
+attn_status attn_decode_partial(const float *q, const void *k_cache, const void *v_cache,
+                                const int32_t *positions, int n_seq, int n_head, int n_kv_head,
+                                int head_dim, float scale, int64_t cap, int n_splits,
+                                int split_len, int variant, void *workspace,
+                                size_t workspace_bytes, attn_stream_t stream);
+
+attn_status attn_decode_combine(const void *workspace, size_t workspace_bytes, float *out,
+                                int n_seq, int n_head, int head_dim, int n_splits,
+                                attn_stream_t stream);
+
+/*
+ * attn_split_heuristic -- host-only, static split count P for a launch.
+ * Chooses P from the shape and the static capacity (never from nkv, which lives
+ * on the device) so that (P x n_kv_head x n_seq) blocks fill about two waves of
+ * sm_count SMs while each split keeps at least one kernel tile of rows at full
+ * capacity. cap <= 0 means "unknown". sm_count <= 0 queries the current device
+ * (and returns 0 with no device).
+ */
+int attn_split_heuristic(int n_seq, int n_head, int n_kv_head, int head_dim, int64_t cap,
+                         int sm_count);
+
+/* attn_workspace_size -- bytes of workspace attn_decode_ex needs (host-only). */
+size_t attn_workspace_size(int n_seq, int n_head, int head_dim, int n_splits);
+
+/*
+ * attn_read_device_error -- synchronises `stream`, returns the sticky device
+ * error word (ATTN_DEVERR_* bits) of the current device in *flags and clears it.
+ */
+attn_status attn_read_device_error(attn_stream_t stream, unsigned int *flags);
+
+/* Human-readable name of a status code (static storage). */
+const char *attn_status_string(attn_status status);
+
+/* Last CUDA error seen by the calling thread (cudaError_t value; 0 = none). */
+int attn_last_cuda_error(void);
+
+/* Library version, MAJOR*10000 + MINOR*100 + PATCH. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_DECODE_H */

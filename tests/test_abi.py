@@ -1,0 +1,120 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point
+declared in include/*.h, and its host-only logic (argument validation, split
+heuristic, workspace sizing, status strings) behaves as documented. Nothing
+here launches a kernel."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import decode_attention_gqa_gb300 as pkg
+from decode_attention_gqa_gb300 import build as cuda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return pkg.load()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(attn_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("attn_decode", "attn_decode_ex", "attn_split_heuristic", "attn_workspace_size",
+                 "attn_read_device_error", "attn_status_string"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(pkg.library_path())
+    for name in declared_functions():
+        assert hasattr(raw, name), "missing export %s" % name
+
+
+def test_version_and_status_strings(lib):
+    assert pkg.attn_version() == 10000
+    assert pkg.attn_status_string(pkg.ATTN_OK) == "ATTN_OK"
+    assert pkg.attn_status_string(pkg.ATTN_ERR_WORKSPACE) == "ATTN_ERR_WORKSPACE"
+    assert pkg.attn_status_string(99) == "ATTN_ERR_UNKNOWN"
+
+
+def test_workspace_size(lib):
+    # partial accumulators [n_seq][n_head][P][hd] f32 + (mx, S) pairs, each 256-aligned
+    assert pkg.attn_workspace_size(1, 28, 128, 38) == 28 * 38 * 128 * 4 + ((28 * 38 * 8 + 255) // 256 * 256)
+    assert pkg.attn_workspace_size(0, 28, 128, 38) == 0
+    assert pkg.attn_workspace_size(1, 28, 128, 0) == 0
+
+
+def test_split_heuristic_host_only(lib):
+    # an explicit SM count never touches the device
+    P = pkg.attn_split_heuristic(1, 28, 4, 128, 8192, 152)
+    assert 1 <= P <= 8192 // 16
+    # more independent (sequence, KV head) units -> fewer splits each
+    assert pkg.attn_split_heuristic(32, 32, 8, 128, 32768, 152) <= P
+    # tiny capacity caps the split count at one 16-row granule per split
+    assert pkg.attn_split_heuristic(1, 8, 2, 128, 40, 152) == 3
+    # rejected shapes
+    assert pkg.attn_split_heuristic(1, 28, 5, 128, 8192, 152) == 0
+    assert pkg.attn_split_heuristic(1, 18, 2, 128, 8192, 152) == 0      # group 9
+    assert pkg.attn_split_heuristic(1, 8, 2, 96, 8192, 152) == 0        # head_dim 96
+
+
+def _ex(lib, **kw):
+    a = dict(q=16, k=16, v=16, pos=16, out=16, n_seq=1, n_head=8, n_kv=2, hd=128, scale=0.1,
+             cap=64, P=0, blk=0, variant=0, ws=None, ws_bytes=0)
+    a.update(kw)
+    return lib.attn_decode_ex(a["q"], a["k"], a["v"], a["pos"], a["out"], a["n_seq"], a["n_head"],
+                              a["n_kv"], a["hd"], a["scale"], a["cap"], a["P"], a["blk"],
+                              a["variant"], a["ws"], a["ws_bytes"], None)
+
+
+def test_argument_validation_is_synchronous(lib):
+    # Every case below is rejected on the host before any CUDA call.
+    assert _ex(lib, n_head=8, n_kv=3) == pkg.ATTN_ERR_INVALID_ARG          # 8 % 3 != 0
+    assert _ex(lib, n_kv=0) == pkg.ATTN_ERR_INVALID_ARG
+    assert _ex(lib, q=None) == pkg.ATTN_ERR_INVALID_ARG
+    assert _ex(lib, k=8) == pkg.ATTN_ERR_INVALID_ARG                        # misaligned
+    assert _ex(lib, out=4) == pkg.ATTN_ERR_INVALID_ARG
+    assert _ex(lib, cap=0) == pkg.ATTN_ERR_INVALID_ARG
+    assert _ex(lib, P=-1) == pkg.ATTN_ERR_INVALID_ARG
+    assert _ex(lib, P=5000) == pkg.ATTN_ERR_INVALID_ARG
+    assert _ex(lib, blk=-3) == pkg.ATTN_ERR_INVALID_ARG
+    assert _ex(lib, variant=7) == pkg.ATTN_ERR_INVALID_ARG
+    assert _ex(lib, scale=float("nan")) == pkg.ATTN_ERR_INVALID_ARG
+    assert _ex(lib, scale=float("inf")) == pkg.ATTN_ERR_INVALID_ARG
+    assert _ex(lib, n_seq=-1) == pkg.ATTN_ERR_INVALID_ARG
+    assert _ex(lib, ws=16) == pkg.ATTN_ERR_INVALID_ARG                      # not 256-aligned
+    assert _ex(lib, n_seq=2, cap=2 ** 30) == pkg.ATTN_ERR_INVALID_ARG       # rows past int32
+    assert _ex(lib, hd=96) == pkg.ATTN_ERR_UNSUPPORTED
+    assert _ex(lib, hd=32) == pkg.ATTN_ERR_UNSUPPORTED
+    assert _ex(lib, n_head=18, n_kv=2) == pkg.ATTN_ERR_UNSUPPORTED          # group 9
+    # nothing to do: no launch, no CUDA call
+    assert _ex(lib, n_seq=0, q=None, k=None, v=None, pos=None, out=None) == pkg.ATTN_OK
+    # the single-sequence entry point
+    assert lib.attn_decode(16, 16, 16, 16, 16, 2, 8, 2, 128, 0.1, None) == pkg.ATTN_ERR_INVALID_ARG
+
+
+def test_binding_raises_attn_error(lib):
+    with pytest.raises(pkg.AttnError) as ei:
+        pkg.attn_decode_ex(16, 16, 16, 16, 16, 1, 8, 3, 128, 0.1, 64, stream=0)
+    assert ei.value.status == pkg.ATTN_ERR_INVALID_ARG
+
+
+def test_ptxas_reports_no_spills(lib):
+    rep = cuda_build.spill_report()
+    assert rep, "no ptxas report found"
+    for fn, r in rep.items():
+        assert r["spill_stores"] == 0 and r["spill_loads"] == 0 and r["stack"] == 0, fn
