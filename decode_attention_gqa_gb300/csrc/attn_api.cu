@@ -84,25 +84,38 @@ attn::KernelInfo kernel_info(int head_dim, int group, int variant)
 
 bool head_dim_supported(int hd) { return hd == 8 || hd == 64 || hd == 128 || hd == 256; }
 
-// ATTN_VARIANT_AUTO: the CUDA-core kernel.
+// ATTN_VARIANT_AUTO: the tensor-core kernel wherever it is compiled
+// (head_dim % 16 == 0); it was measured faster than the CUDA-core kernel for
+// every group size. head_dim 8 runs on CUDA cores.
 int resolve_variant(int variant, int head_dim, int group)
 {
-    (void)head_dim;
     (void)group;
-    if (variant == ATTN_VARIANT_AUTO) return attn::kVariantSimt;
+    if (variant == ATTN_VARIANT_AUTO)
+        return head_dim % 16 == 0 ? attn::kVariantTc : attn::kVariantSimt;
     return variant;
 }
 
+// Static split count P (the host never sees nkv). With the capacity known,
+// size the chunk so that at full capacity the (sequence, KV head) units fill
+// `waves` waves of resident blocks -- one wave for a single sequence, eight for
+// a batch whose lengths may be ragged, so blocks of unequal work still balance
+// -- round it up to the kernel's row granule and take P = ceil(cap / chunk).
+// Without it: one wave.
 int heuristic(int n_seq, int n_kv_head, int64_t cap, int sm_count, const attn::KernelInfo &ki)
 {
     const int64_t units = (int64_t)n_seq * n_kv_head;
     const int64_t slots = (int64_t)sm_count * (ki.blocks_per_sm > 0 ? ki.blocks_per_sm : 1);
-    int64_t P = slots / (units > 0 ? units : 1);      // one full wave of blocks
-    if (P < 1) P = 1;
+    const int64_t gran = ki.granule > 0 ? ki.granule : attn::kSplitGranule;
+    int64_t P;
     if (cap > 0) {
-        const int64_t most = (cap + attn::kSplitGranule - 1) / attn::kSplitGranule;
-        if (P > most) P = most;                       // no split shorter than one granule at full cap
+        const int64_t waves = n_seq > 1 ? 8 : 1;
+        int64_t chunk = (cap * units + waves * slots - 1) / (waves * slots);
+        chunk = (chunk + gran - 1) / gran * gran;
+        P = (cap + chunk - 1) / chunk;
+    } else {
+        P = slots / (units > 0 ? units : 1);
     }
+    if (P < 1) P = 1;
     if (P > kMaxSplits) P = kMaxSplits;
     return (int)P;
 }

@@ -20,7 +20,7 @@ constexpr unsigned kErrPipelineTimeout = 0x2u;
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
-// Rows are handed to splits in multiples of this (count mode).
+// The host heuristic never makes a split shorter than this at full capacity.
 constexpr int kSplitGranule = 16;
 
 struct PartialArgs {
@@ -62,15 +62,17 @@ __device__ __forceinline__ int64_t rows_attended(const PartialArgs &a, int s, bo
     return n;
 }
 
+// By count the chunk is rounded up to a whole number of the kernel's tiles
+// (`tile` rows), so that only the last split of a sequence ends in a partial tile.
 __device__ __forceinline__ void split_range(int64_t nkv, int sp, int n_splits, int split_len,
-                                            int64_t &lo, int64_t &hi)
+                                            int tile, int64_t &lo, int64_t &hi)
 {
     int64_t chunk;
     if (split_len > 0) {
         chunk = split_len;
     } else {
         chunk = (nkv + n_splits - 1) / n_splits;
-        chunk = (chunk + kSplitGranule - 1) / kSplitGranule * kSplitGranule;
+        chunk = (chunk + tile - 1) / tile * tile;
     }
     lo = (int64_t)sp * chunk;
     hi = lo + chunk < nkv ? lo + chunk : nkv;
@@ -159,6 +161,47 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// cp.async (16 bytes, zero-filled when src_bytes == 0) with completion tracked
+// by an mbarrier: the arrive below fires once every cp.async this thread has
+// issued so far has landed, without changing the phase's expected count.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, unsigned src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                 :: "r"(smem_u32(dst)), "l"(src), "r"(src_bytes) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" :: "r"(smem_u32(bar)) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Warp-level tensor-core primitives (16x8x16 f16 MMA with f32 accumulation,
+// 8x8 matrix loads from shared memory).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void *p)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+                 "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 // ---------------------------------------------------------------------------

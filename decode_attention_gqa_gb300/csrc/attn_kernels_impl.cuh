@@ -9,16 +9,31 @@
 
 namespace attn {
 
-// Pipeline shape of the CUDA-core partial kernel per head_dim: compute warps
-// and stages, sized so the stage ring fits the 227 KB shared-memory budget.
+// Pipeline shape per (policy, head_dim): compute warps and stages, sized so
+// the stage ring fits the 227 KB shared-memory budget with enough bytes in
+// flight per SM (about two stages ahead of the compute warps).
 template <int HD> struct SimtShape;
 template <> struct SimtShape<8>   { static constexpr int NWC = 4, S = 4; };
 template <> struct SimtShape<64>  { static constexpr int NWC = 4, S = 3; };
 template <> struct SimtShape<128> { static constexpr int NWC = 4, S = 3; };
 template <> struct SimtShape<256> { static constexpr int NWC = 2, S = 3; };
 
+template <int HD> struct TcShape { static constexpr int NWC = 4, S = 3; };
+template <> struct TcShape<64>    { static constexpr int NWC = 4, S = 4; };
+
 template <int HD, int G>
 using SimtCfg = PartialCfg<HD, G, SimtWarp, SimtShape<HD>::NWC, SimtShape<HD>::S>;
+template <int HD, int G>
+using TcCfg = PartialCfg<HD, G, TcWarp, TcShape<HD>::NWC, TcShape<HD>::S>;
+
+// Resident blocks per SM for a configuration: 228 KB of shared memory per SM
+// with 1 KB reserved per block, 64 K registers, at most 32 blocks.
+template <class Cfg>
+constexpr int blocks_per_sm()
+{
+    const int by_smem = (int)(233472u / (Cfg::SMEM_BYTES + 1024u));
+    return by_smem < 1 ? 1 : (by_smem > 32 ? 32 : by_smem);
+}
 
 template <class Cfg, int HD, int G>
 cudaError_t launch_partial(const LaunchRequest &r)
@@ -48,11 +63,8 @@ cudaError_t launch_combine(const LaunchRequest &r)
     ca.n_head = r.pa.n_head;
     ca.n_splits = r.pa.n_splits;
     const void *fn = reinterpret_cast<const void *>(&attn_combine<HD>);
-    const size_t smem = combine_smem_bytes<HD>(ca.n_splits);
-    cudaError_t e = ensure_smem_attr(fn, (int)smem);
-    if (e != cudaSuccess) return e;
     void *args[] = {&ca};
-    return launch_pdl(fn, dim3(ca.n_head, r.n_seq), dim3(CombineCfg<HD>::THREADS), smem, r.stream, args);
+    return launch_pdl(fn, dim3(ca.n_head, r.n_seq), dim3(CombineCfg<HD>::THREADS), 0, r.stream, args);
 }
 
 template <int HD, int G>
@@ -60,9 +72,12 @@ cudaError_t launch_group(const LaunchRequest &r)
 {
     cudaError_t e = cudaSuccess;
     if (r.stages & kStagePartial) {
-        switch (r.variant) {
-        case kVariantSimt: e = launch_partial<SimtCfg<HD, G>, HD, G>(r); break;
-        default: return cudaErrorInvalidValue;
+        if constexpr (HD % 16 == 0) {
+            if (r.variant == kVariantTc) e = launch_partial<TcCfg<HD, G>, HD, G>(r);
+            else e = launch_partial<SimtCfg<HD, G>, HD, G>(r);
+        } else {
+            if (r.variant != kVariantSimt) return cudaErrorInvalidValue;
+            e = launch_partial<SimtCfg<HD, G>, HD, G>(r);
         }
         if (e != cudaSuccess) return e;
     }
@@ -89,14 +104,22 @@ cudaError_t launch_for_hd(const LaunchRequest &r)
 template <int HD>
 KernelInfo kernel_info_for_hd(int group, int variant)
 {
-    KernelInfo k{0, 0, false};
+    KernelInfo k{0, 0, 0, false};
     if (group < 1 || group > 8) return k;
     if (variant == kVariantSimt) {
         using C = SimtCfg<HD, 8>;     // the largest group sets the shared-memory need
         k.tile_rows = C::TILE;
-        k.blocks_per_sm = (int)(227u * 1024u / C::SMEM_BYTES);
-        if (k.blocks_per_sm < 1) k.blocks_per_sm = 1;
+        k.granule = C::WR;
+        k.blocks_per_sm = blocks_per_sm<C>();
         k.available = true;
+    } else if (variant == kVariantTc) {
+        if constexpr (HD % 16 == 0) {
+            using C = TcCfg<HD, 8>;
+            k.tile_rows = C::TILE;
+            k.granule = C::WR;
+            k.blocks_per_sm = blocks_per_sm<C>();
+            k.available = true;
+        }
     }
     return k;
 }

@@ -32,6 +32,7 @@ struct LaunchRequest {
 // Static properties of the partial kernel chosen for (head_dim, variant).
 struct KernelInfo {
     int tile_rows;           // rows per pipeline stage
+    int granule;             // split chunks (by count) are rounded up to this many rows
     int blocks_per_sm;       // resident blocks per SM (from its shared-memory need)
     bool available;          // compiled for this (head_dim, group)
 };

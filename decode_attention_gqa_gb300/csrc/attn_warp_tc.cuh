@@ -1,0 +1,214 @@
+// attn_warp_tc.cuh -- tensor-core per-warp arithmetic of the partial kernel:
+// steps a3-a5 for one warp's 16-row slice of a shared-memory tile, with
+// 16x8x16 f16 MMAs accumulating in f32.
+//
+// The dotLLM #199 design (§2) pads the single query row to a 16-row MMA tile
+// and wastes 15 rows. Here the 16 rows carry the whole query-head group twice:
+// rows 0..7 hold hi = f16(x) and rows 8..15 hold lo = f16(x - hi) for the G <= 8
+// heads, so q·k = hi·k + lo·k keeps about 22 significant bits of q (f16
+// products are exact in the f32 accumulator) instead of the 11 bits of a plain
+// f16 cast (the precision risk of "Option B", #199 §0). The softmax weights p
+// get the same hi/lo treatment for p·V, and the C fragment of q·Kᵀ is exactly
+// the A fragment layout of p·V, so no data moves between lanes.
+//
+//   scores  C[16 x 8 rows]  = Q[16 x hd] · K[8 rows x hd]ᵀ     (two n-tiles per slice)
+//   values  O[16 x hd]     += P[16 x 16 rows] · V[16 rows x hd]
+//
+// Lane l owns head g = l / 4 and rows {2t, 2t+1, 8+2t, 9+2t} (t = l % 4) of the
+// slice's scores, and dims {8n + 2t, 8n + 2t + 1} of head g's accumulator.
+//
+// q is scaled per head by a power of two (exact) so its largest element lies in
+// [2^14, 2^15): no f16 overflow for any finite q and the lo part stays normal.
+// Rescaling of the accumulator is lazy: the reference max only moves when a new
+// score exceeds it by more than TAU (log2 units), so p <= 2^(TAU + OFF) and the
+// final o = acc / S is unchanged (both use the same reference).
+#pragma once
+
+#include "attn_device.cuh"
+
+namespace attn {
+
+template <int HD, int G, int NWC>
+struct TcWarp {
+    static_assert(HD % 16 == 0, "tensor-core path needs head_dim % 16 == 0");
+    static constexpr int WR = 16;                     // rows per warp slice
+    static constexpr int KSTEPS = HD / 16;            // k-steps of q·Kᵀ
+    static constexpr int NTD = HD / 8;                // n-tiles of p·V
+    static constexpr bool Q_REGS = HD <= 128;         // keep q fragments in registers
+    static constexpr float TAU = 8.f;                 // lazy-rescale threshold
+    static constexpr float OFF = 7.f;                 // p headroom: max p in [2^OFF, 2^(OFF+TAU)]
+    static constexpr uint32_t QT_BYTES = 16u * HD * 2;  // Q tile, f16, swizzled like K
+    static constexpr uint32_t EXTRA_BYTES = QT_BYTES + 8 * 4;
+
+    uint32_t qa[Q_REGS ? KSTEPS : 1][4];
+    float o[NTD][4];
+    float m_ref, l, inv_sc;
+
+    // a2: Q tile rows g (hi) and 8 + g (lo) for g < G, zero rows for g >= G,
+    // and the per-head power-of-two scale. One warp per head.
+    static __device__ __forceinline__ void prepare(uint8_t *extra, const float *qg, float qscale,
+                                                   int tid, int nthreads)
+    {
+        float *inv = reinterpret_cast<float *>(extra + QT_BYTES);
+        const int warp = tid >> 5, lane = tid & 31, nwarps = nthreads >> 5;
+        for (int g = warp; g < 8; g += nwarps) {
+            constexpr int PER = (HD + 31) / 32;
+            float x[PER];
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int d = lane + 32 * i;
+                x[i] = (g < G && d < HD) ? __ldg(qg + g * HD + d) * qscale : 0.f;
+                amax = fmaxf(amax, fabsf(x[i]));
+            }
+            amax = warp_max(amax);
+            int e = 0;
+            float sc = 1.f;
+            if (amax > 0.f) {
+                (void)frexpf(amax, &e);               // amax in [2^(e-1), 2^e)
+                sc = ldexpf(1.f, 15 - e);             // scaled max in [2^14, 2^15)
+            }
+            if (lane == 0) inv[g] = amax > 0.f ? ldexpf(1.f, e - 15) : 1.f;
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int d = lane + 32 * i;
+                if (d < HD) {
+                    const float v = x[i] * sc;
+                    const __half hi = __float2half_rn(v);
+                    const __half lo = __float2half_rn(v - __half2float(hi));
+                    const uint32_t off = tile_unit_offset<HD, 16>(g, d >> 3) + (d & 7) * 2;
+                    const uint32_t offl = tile_unit_offset<HD, 16>(8 + g, d >> 3) + (d & 7) * 2;
+                    *reinterpret_cast<__half *>(extra + off) = hi;
+                    *reinterpret_cast<__half *>(extra + offl) = lo;
+                }
+            }
+        }
+    }
+
+    // A fragment (16 x 16) of Q for k-step kk: matrices (hi, d 0-7), (lo, d 0-7),
+    // (hi, d 8-15), (lo, d 8-15).
+    static __device__ __forceinline__ void load_q(uint32_t (&a)[4], const uint8_t *extra, int kk,
+                                                  int lane)
+    {
+        const int i = lane >> 3;
+        const int row = (i & 1) * 8 + (lane & 7);
+        ldsm_x4(a, extra + tile_unit_offset<HD, 16>(row, 2 * kk + (i >> 1)));
+    }
+
+    __device__ __forceinline__ void init(const uint8_t *extra, int, int lane)
+    {
+        if constexpr (Q_REGS) {
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) load_q(qa[kk], extra, kk, lane);
+        }
+#pragma unroll
+        for (int n = 0; n < NTD; ++n)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[n][i] = 0.f;
+        m_ref = -INFINITY;
+        l = 0.f;
+        inv_sc = reinterpret_cast<const float *>(extra + QT_BYTES)[lane >> 2];
+    }
+
+    // Rows [r0 + ra, r0 + 16) of a TILE-row stage are in range (0 <= ra < 16);
+    // rows before ra hold finite data (zeros or rows already attended).
+    template <int TILE>
+    __device__ __forceinline__ void process(const uint8_t *ks, const uint8_t *vs, int r0, int ra,
+                                            uint8_t *extra, int, int lane)
+    {
+        // a3: scores of the slice's 16 rows for all heads
+        float c[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c[n][i] = 0.f;
+        const int i8 = lane >> 3;
+        const int krow = r0 + (i8 >> 1) * 8 + (lane & 7);
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS; ++kk) {
+            uint32_t a[4];
+            if constexpr (Q_REGS) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) a[i] = qa[kk][i];
+            } else {
+                load_q(a, extra, kk, lane);
+            }
+            uint32_t b[4];        // (rows 0-7, d lo8), (rows 0-7, d hi8), (rows 8-15, lo8), (8-15, hi8)
+            ldsm_x4(b, ks + tile_unit_offset<HD, TILE>(krow, 2 * kk + (i8 & 1)));
+            mma_16816(c[0], a, b[0], b[1]);
+            mma_16816(c[1], a, b[2], b[3]);
+        }
+        const int t = lane & 3;
+        float s[4];
+        s[0] = (c[0][0] + c[0][2]) * inv_sc;      // row 2t
+        s[1] = (c[0][1] + c[0][3]) * inv_sc;      // row 2t + 1
+        s[2] = (c[1][0] + c[1][2]) * inv_sc;      // row 8 + 2t
+        s[3] = (c[1][1] + c[1][3]) * inv_sc;      // row 9 + 2t
+        if (2 * t < ra) s[0] = -INFINITY;
+        if (2 * t + 1 < ra) s[1] = -INFINITY;
+        if (8 + 2 * t < ra) s[2] = -INFINITY;
+        if (9 + 2 * t < ra) s[3] = -INFINITY;
+        // a4: slice max of head g (the four lanes of the group), lazy rescale
+        float mt = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+        const bool need = mt > m_ref + TAU;
+        if (__any_sync(0xffffffffu, need)) {
+            const float nr = need ? mt : m_ref;
+            const float corr = ex2(m_ref - nr);  // 0 on the first slice (m_ref = -inf)
+#pragma unroll
+            for (int n = 0; n < NTD; ++n)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) o[n][i] *= corr;
+            l *= corr;
+            m_ref = nr;
+        }
+        const float base = m_ref - OFF;
+        float p[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) p[i] = ex2(s[i] - base);
+        l += (p[0] + p[1]) + (p[2] + p[3]);
+        // p as the A fragment of p·V: hi parts in rows 0-7, lo parts in rows 8-15
+        uint32_t pa[4];
+        {
+            const __half2 h01 = __floats2half2_rn(p[0], p[1]);
+            const __half2 h23 = __floats2half2_rn(p[2], p[3]);
+            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+            const __half2 l01 = __floats2half2_rn(p[0] - f01.x, p[1] - f01.y);
+            const __half2 l23 = __floats2half2_rn(p[2] - f23.x, p[3] - f23.y);
+            pa[0] = *reinterpret_cast<const uint32_t *>(&h01);
+            pa[1] = *reinterpret_cast<const uint32_t *>(&l01);
+            pa[2] = *reinterpret_cast<const uint32_t *>(&h23);
+            pa[3] = *reinterpret_cast<const uint32_t *>(&l23);
+        }
+        // a5: O += P · V over the slice's 16 rows
+        const int vrow = r0 + (i8 & 1) * 8 + (lane & 7);
+#pragma unroll
+        for (int n = 0; n < NTD; n += 2) {
+            uint32_t b[4];        // (rows 0-7, dims n), (rows 8-15, dims n), (0-7, n+1), (8-15, n+1)
+            ldsm_x4_trans(b, vs + tile_unit_offset<HD, TILE>(vrow, n + (i8 >> 1)));
+            mma_16816(o[n], pa, b[0], b[1]);
+            mma_16816(o[n + 1], pa, b[2], b[3]);
+        }
+    }
+
+    // mm[g] = (mx, S) in the partial's convention (mx is the reference the p's
+    // were taken against), mo[g * HD + d] = oc.
+    __device__ __forceinline__ void publish(float2 *mm, float *mo, int lane)
+    {
+        float lt = l;
+        lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+        lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+        const int g = lane >> 2, t = lane & 3;
+        if (g < G) {
+            if (t == 0) mm[g] = make_float2(m_ref - OFF, lt);
+#pragma unroll
+            for (int n = 0; n < NTD; ++n) {
+                mo[g * HD + n * 8 + 2 * t] = o[n][0] + o[n][2];
+                mo[g * HD + n * 8 + 2 * t + 1] = o[n][1] + o[n][3];
+            }
+        }
+    }
+};
+
+} // namespace attn

@@ -68,9 +68,11 @@ typedef enum {
 #define ATTN_DEVERR_PIPELINE_TIMEOUT 0x2u  /* a bounded in-kernel wait gave up (block skipped) */
 
 /* Kernel variants for attn_decode_ex. */
-#define ATTN_VARIANT_AUTO 0   /* the library picks per (head_dim, group) */
-#define ATTN_VARIANT_SIMT 1   /* CUDA-core f32 partial kernel */
-#define ATTN_VARIANT_TC   2   /* tensor-core (mma, f16 hi/lo split of q and p) partial kernel */
+#define ATTN_VARIANT_AUTO 0   /* tensor cores where compiled (head_dim % 16 == 0), else CUDA cores */
+#define ATTN_VARIANT_SIMT 1   /* CUDA-core f32 partial kernel (every head_dim) */
+#define ATTN_VARIANT_TC   2   /* tensor-core partial kernel: 16x8x16 f16 MMA, f32 accumulate, q and
+                                 p each carried as an f16 hi + lo pair (about 22 significant bits);
+                                 head_dim 64, 128, 256 only (ATTN_ERR_UNSUPPORTED otherwise) */
 
 /*
  * attn_decode -- one layer call, single sequence, library-owned workspace.
@@ -95,7 +97,8 @@ attn_status attn_decode(const float *q, const void *k_cache, const void *v_cache
  *   cap             cache rows per sequence (>= 1); nkv_s is clamped to cap.
  *   n_splits        splits P per (sequence, KV head); 0 = attn_split_heuristic().
  *   split_len       0: split by count, chunk = ceil(nkv / P) rounded up to the
- *                   kernel tile (minfer R4 §2.2); > 0: fixed block of split_len
+ *                   kernel's row granule, 16 rows (tensor cores) or 32 rows
+ *                   (CUDA cores) (minfer R4 §2.2); > 0: fixed block of split_len
  *                   rows per split (Red Lite dev35 "Change"), which needs
  *                   P * split_len >= cap, else ATTN_ERR_INVALID_ARG.
  *   variant         ATTN_VARIANT_*.

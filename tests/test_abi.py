@@ -64,8 +64,14 @@ def test_split_heuristic_host_only(lib):
     assert 1 <= P <= 8192 // 16
     # more independent (sequence, KV head) units -> fewer splits each
     assert pkg.attn_split_heuristic(32, 32, 8, 128, 32768, 152) <= P
-    # tiny capacity caps the split count at one 16-row granule per split
+    # no split is shorter than the kernel's 16-row granule: 40 rows -> 3 splits
     assert pkg.attn_split_heuristic(1, 8, 2, 128, 40, 152) == 3
+    # one sequence fills one wave: 28/4 heads at 8192 rows -> 4 x 74 blocks of 112 rows
+    assert pkg.attn_split_heuristic(1, 28, 4, 128, 8192, 152) == 74
+    # a batch aims at eight waves so ragged lengths still balance
+    assert pkg.attn_split_heuristic(32, 32, 8, 128, 32768, 152) == 10
+    # unknown capacity: one wave of blocks over the (sequence, KV head) units
+    assert pkg.attn_split_heuristic(1, 28, 4, 128, 0, 152) >= 152 // 4
     # rejected shapes
     assert pkg.attn_split_heuristic(1, 28, 5, 128, 8192, 152) == 0
     assert pkg.attn_split_heuristic(1, 18, 2, 128, 8192, 152) == 0      # group 9

@@ -19,7 +19,7 @@ from harness import assert_close, make_case, run_decode, to_device
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = [1]          # ATTN_VARIANT_SIMT
+VARIANTS = [1, 2]       # ATTN_VARIANT_SIMT (CUDA cores), ATTN_VARIANT_TC (tensor cores)
 
 
 @pytest.fixture(scope="module")
@@ -68,6 +68,8 @@ def test_smallhead_fixture(pkg):
 @pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("hd", [8, 64, 128, 256])
 def test_all_groups_and_head_dims(pkg, hd, variant):
+    if variant == 2 and hd % 16:
+        pytest.skip("the tensor-core kernel needs head_dim % 16 == 0")
     for G in range(1, 9):
         n_kv = 2
         n_head = G * n_kv
@@ -166,12 +168,27 @@ def test_large_score_spread_and_planted_row(pkg, variant):
         assert_close(got[0, h], want, "planted row head %d" % h)
 
 
-def test_single_row_is_that_v_row(pkg):
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_single_row_is_that_v_row(pkg, variant):
     n_head, n_kv, hd, cap = 8, 2, 128, 64
     case = make_case(12, 1, n_head, n_kv, hd, cap, (1,))
-    got = run_decode(pkg, to_device(case), n_head, n_kv, hd, cap, 0.3).cpu().numpy()
+    got = run_decode(pkg, to_device(case), n_head, n_kv, hd, cap, 0.3,
+                     variant=variant).cpu().numpy()
     for h in range(n_head):
         np.testing.assert_array_equal(got[0, h], case["v"][0, 0, h // 4].astype(np.float32))
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_extreme_query_magnitudes(pkg, variant):
+    """q rows scaled by 1e-30 .. 1e4 (outside f16 range): the tensor-core kernel's
+    per-head power-of-two scaling keeps them finite and accurate."""
+    n_head, n_kv, hd, cap = 8, 2, 128, 300
+    case = make_case(13, 1, n_head, n_kv, hd, cap, (300,))
+    case["q"][0, 0] *= 1e-30
+    case["q"][0, 1] *= 1e-3
+    case["q"][0, 2] *= 30.0
+    case["q"][0, 5, :64] *= 1e4
+    _check(pkg, case, n_head, n_kv, hd, cap, 1 / math.sqrt(hd), "extreme q", variant=variant)
 
 
 # ------------------------------------------ full-size workloads, bench config
@@ -183,19 +200,22 @@ def _full_workload(pkg, name, sample_pairs=None, threads=16):
     kw = {}
     if w.split_len:
         kw = dict(n_splits=-(-w.cap // w.split_len), split_len=w.split_len)
-    got = run_decode(pkg, dev, w.n_head, w.n_kv_head, w.head_dim, w.cap, w.scale, **kw)
-    got = got.cpu().numpy()
+    gots = {}
+    for variant in (0,) + tuple(VARIANTS):
+        gots[variant] = run_decode(pkg, dev, w.n_head, w.n_kv_head, w.head_dim, w.cap, w.scale,
+                                   variant=variant, **kw).cpu().numpy()
     del dev
     if sample_pairs is None:
         ref = oracle.attn_decode(lay["q"], lay["k"], lay["v"], lay["positions"], w.n_head,
                                  w.n_kv_head, w.head_dim, w.cap, w.scale, n_threads=threads)
-        return assert_close(got, ref, name)
-    worst = 0.0
+        for variant, got in gots.items():
+            assert_close(got, ref, "%s variant %d" % (name, variant))
+        return
     for (s, h) in sample_pairs:
         ref = oracle.attn_decode_one(lay["q"], lay["k"], lay["v"], lay["positions"], w.n_head,
                                      w.n_kv_head, w.head_dim, w.cap, w.scale, s, h)
-        worst = max(worst, assert_close(got[s, h], ref, "%s s=%d h=%d" % (name, s, h)))
-    return worst
+        for variant, got in gots.items():
+            assert_close(got[s, h], ref, "%s variant %d s=%d h=%d" % (name, variant, s, h))
 
 
 def test_full_7b_all_contexts(pkg):
@@ -203,11 +223,13 @@ def test_full_7b_all_contexts(pkg):
     for ctx in syn.CTX_SWEEP_7B:
         wc = w.with_ctx(ctx)
         lay = syn.make_layer(wc)
-        got = run_decode(pkg, to_device(lay), wc.n_head, wc.n_kv_head, wc.head_dim, wc.cap,
-                         wc.scale).cpu().numpy()
+        dev = to_device(lay)
         ref = oracle.attn_decode(lay["q"], lay["k"], lay["v"], lay["positions"], wc.n_head,
                                  wc.n_kv_head, wc.head_dim, wc.cap, wc.scale, n_threads=16)
-        assert_close(got, ref, "7b ctx=%d" % ctx)
+        for variant in (0,) + tuple(VARIANTS):
+            got = run_decode(pkg, dev, wc.n_head, wc.n_kv_head, wc.head_dim, wc.cap, wc.scale,
+                             variant=variant).cpu().numpy()
+            assert_close(got, ref, "7b ctx=%d variant %d" % (ctx, variant))
 
 
 def test_full_long_grouped_all_blocks(pkg):
@@ -217,9 +239,11 @@ def test_full_long_grouped_all_blocks(pkg):
     ref = oracle.attn_decode(lay["q"], lay["k"], lay["v"], lay["positions"], w.n_head,
                              w.n_kv_head, w.head_dim, w.cap, w.scale, n_threads=16)
     for blk in syn.BLOCK_SWEEP_LONG:
-        got = run_decode(pkg, dev, w.n_head, w.n_kv_head, w.head_dim, w.cap, w.scale,
-                         n_splits=-(-w.cap // blk), split_len=blk).cpu().numpy()
-        assert_close(got, ref, "long blk=%d" % blk)
+        for variant in (0,) + tuple(VARIANTS):
+            got = run_decode(pkg, dev, w.n_head, w.n_kv_head, w.head_dim, w.cap, w.scale,
+                             n_splits=-(-w.cap // blk), split_len=blk,
+                             variant=variant).cpu().numpy()
+            assert_close(got, ref, "long blk=%d variant %d" % (blk, variant))
 
 
 def test_full_stress(pkg):
