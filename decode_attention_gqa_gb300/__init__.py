@@ -19,6 +19,7 @@ __all__ = [
     "ATTN_ERR_CUDA", "ATTN_DEVERR_POSITION_CLAMPED", "ATTN_DEVERR_PIPELINE_TIMEOUT",
     "ATTN_VARIANT_AUTO", "ATTN_VARIANT_SIMT", "ATTN_VARIANT_TC", "library_path", "load",
     "attn_decode", "attn_decode_ex", "attn_decode_partial", "attn_decode_combine",
+    "attn_decode_static",
     "attn_split_heuristic", "attn_workspace_size",
     "attn_read_device_error", "attn_status_string", "attn_last_cuda_error", "attn_version",
 ]
@@ -69,6 +70,9 @@ def load():
                                             i32, vp, sz, vp]
         lib.attn_decode_combine.restype = i32
         lib.attn_decode_combine.argtypes = [vp, sz, vp, i32, i32, i32, i32, vp]
+        lib.attn_decode_static.restype = i32
+        lib.attn_decode_static.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i64, i32,
+                                           i32, i32, vp]
         lib.attn_split_heuristic.restype = i32
         lib.attn_split_heuristic.argtypes = [i32, i32, i32, i32, i64, i32]
         lib.attn_workspace_size.restype = sz
@@ -153,6 +157,16 @@ def attn_decode_combine(workspace, workspace_bytes, out, n_seq, n_head, head_dim
     _check(load().attn_decode_combine(_ptr(workspace), workspace_bytes, _ptr(out), n_seq, n_head,
                                       head_dim, n_splits, _stream(stream)),
            "attn_decode_combine")
+
+
+def attn_decode_static(q, k_cache, v_cache, positions, out, n_seq, n_head, n_kv_head, head_dim,
+                       scale, cap, n_splits=0, split_len=0, variant=ATTN_VARIANT_AUTO, stream=None):
+    """attn_decode_ex with the library's fixed scratch array instead of a
+    workspace: allocates nothing (see include/attn_decode.h)."""
+    _check(load().attn_decode_static(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(positions),
+                                     _ptr(out), n_seq, n_head, n_kv_head, head_dim, scale, cap,
+                                     n_splits, split_len, variant, _stream(stream)),
+           "attn_decode_static")
 
 
 def attn_split_heuristic(n_seq, n_head, n_kv_head, head_dim, cap, sm_count) -> int:

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn_decode.so")
 
-SOURCES = ["attn_api.cu", "attn_kernels_hd8.cu", "attn_kernels_hd64.cu",
+SOURCES = ["attn_api.cu", "attn_noalloc.cu", "attn_kernels_hd8.cu", "attn_kernels_hd64.cu",
            "attn_kernels_hd128.cu", "attn_kernels_hd256.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -142,6 +142,37 @@ attn_status attn_decode_combine(const void *workspace, size_t workspace_bytes, f
                                 attn_stream_t stream);
 
 /*
+ * attn_decode_static -- attn_decode_ex for callers that cannot allocate device
+ * memory when they call it: an engine step running under CUDA stream capture
+ * (no cudaMalloc while capturing), a plugin whose host framework owns all
+ * device memory, a process with a fixed device-memory budget. The pages this
+ * library follows have no counterpart to this entry point.
+ *
+ * Same arguments and results as attn_decode_ex without the workspace: the
+ * partial triples go to a fixed device array of ATTN_STATIC_SCRATCH_BYTES
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits. The call allocates nothing (no cudaMalloc/cudaFree, no
+ * allocating library routine). The first call on a device, with that device
+ * current, looks up the array's device address (cudaGetSymbolAddress); make
+ * that first call before any stream capture.
+ *   - n_splits == 0 takes attn_split_heuristic(); a shape whose
+ *     attn_workspace_size(n_seq, n_head, head_dim, P) exceeds
+ *     ATTN_STATIC_SCRATCH_BYTES returns ATTN_ERR_WORKSPACE and launches nothing.
+ *   - All calls share the one array and it keeps the last call's contents.
+ *     Nothing in it has to start at zero: every split writes its (mx, S) before
+ *     the combine reads it, and oc is only read for splits that wrote it in
+ *     the same call. Two calls whose kernels can overlap on the GPU (different
+ *     streams without ordering, or different host threads) race on the array
+ *     and give wrong results; serialise them on one stream.
+ */
+#define ATTN_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+attn_status attn_decode_static(const float *q, const void *k_cache, const void *v_cache,
+                               const int32_t *positions, float *out, int n_seq, int n_head,
+                               int n_kv_head, int head_dim, float scale, int64_t cap,
+                               int n_splits, int split_len, int variant, attn_stream_t stream);
+
+/*
  * attn_split_heuristic -- host-only, static split count P for a launch.
  * Chooses P from the shape and the static capacity (never from nkv, which lives
  * on the device) so that (P x n_kv_head x n_seq) blocks fill about two waves of
