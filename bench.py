@@ -246,9 +246,12 @@ def run_ours(args, rank, world, local):
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
-    def layer_calls(stream, partial_only=False):
+    def layer_calls(stream, partial_only=False, combine_only=False):
         for l in range(L):
-            if partial_only:
+            if combine_only:
+                pkg.attn_decode_combine(ws, ws_bytes, out[l], 1, w.n_head, w.head_dim, P,
+                                        stream=stream)
+            elif partial_only:
                 pkg.attn_decode_partial(q[l], kc[l], vc[l], pos, 1, w.n_head, w.n_kv_head,
                                         w.head_dim, w.scale, w.cap, P, 0, args.variant, ws,
                                         ws_bytes, stream=stream)
@@ -257,15 +260,15 @@ def run_ours(args, rank, world, local):
                                    w.head_dim, w.scale, w.cap, n_splits=P, variant=args.variant,
                                    workspace=ws, workspace_bytes=ws_bytes, stream=stream)
 
-    def capture(advance: bool, partial_only=False):
+    def capture(advance: bool, partial_only=False, combine_only=False):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(s):
-            layer_calls(s, partial_only)            # warm the launch path outside capture
+            layer_calls(s, partial_only, combine_only)   # warm the launch path outside capture
         torch.cuda.synchronize()
         with torch.cuda.graph(g, stream=s):
             if advance:
                 pos.add_(1)
-            layer_calls(torch.cuda.current_stream(), partial_only)
+            layer_calls(torch.cuda.current_stream(), partial_only, combine_only)
         return g
 
     def timed_replays(g, n, clocks=None):
@@ -313,21 +316,31 @@ def run_ours(args, rank, world, local):
     got = out[0].cpu().numpy().astype(np.float64)
     parity_ok = bool(np.all(np.abs(got - ref) <= 1e-4 + 1e-3 * np.abs(ref)))
 
-    # ---- the partial kernel alone: graph of L partial launches at nkv = ctx_end
-    pos.fill_(ctx_end - 1)
+    # ---- each stage alone: graphs of L partial-only and L combine-only launches
     gp = capture(advance=False, partial_only=True)
-    with torch.cuda.stream(s):
-        for _ in range(W):
-            gp.replay()
-    ms_p, _ = timed_replays(gp, K)
-    partial_us = ms_p * 1e3 / (K * L)
+    gc = capture(advance=False, combine_only=True)
+
+    def stage_times(c):
+        """(partial µs, combine µs) per launch at nkv = c."""
+        pos.fill_(c - 1)
+        with torch.cuda.stream(s):
+            for _ in range(W):
+                gp.replay()
+        ms_p, _ = timed_replays(gp, K)
+        with torch.cuda.stream(s):
+            for _ in range(W):
+                gc.replay()
+        ms_c, _ = timed_replays(gc, K)
+        return ms_p * 1e3 / (K * L), ms_c * 1e3 / (K * L)
+
+    partial_us, combine_us = stage_times(ctx_end)
     achieved = kv_bytes(ctx_end) / (partial_us * 1e-6) / 1e9
     peak, peak_kind = measured_peak()
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                 "traffic": profiled_traffic("7b_ctx%d" % ctx_end),
                 "kernel": "attn_split_partial", "bytes_per_launch": kv_bytes(ctx_end),
-                "us_per_launch": round(partial_us, 3)}
+                "us_per_launch": round(partial_us, 3), "combine_us_per_launch": round(combine_us, 3)}
 
     # ---- context sweep (same caches, positions set per point)
     sweep = {}
@@ -342,8 +355,11 @@ def run_ours(args, rank, world, local):
             ms_c, _ = timed_replays(g, K)
             ms_c = dist_max(ms_c, world)
             b = sum(kv_bytes(c - K + i + 1) * L for i in range(K))
+            p_us, c_us = stage_times(c)
             sweep[str(c)] = {"us_per_layer": round(ms_c * 1e3 / (K * L), 3),
-                             "gbs": round(b * world / (ms_c * 1e-3) / 1e9, 1)}
+                             "gbs": round(b * world / (ms_c * 1e-3) / 1e9, 1),
+                             "partial_us": round(p_us, 3), "combine_us": round(c_us, 3)}
+    pos.fill_(ctx_end - 1)
 
     # ---- end to end through the C ABI from pinned host buffers
     e2e = None

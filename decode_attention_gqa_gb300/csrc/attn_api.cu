@@ -265,6 +265,11 @@ cudaError_t ensure_smem_attr(const void *func, int bytes)
     std::lock_guard<std::mutex> lock(g_mu);
     if (g_smem_done.count({func, dev})) return cudaSuccess;
     e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    // all of the unified L1/shared array as shared memory, so that as many
+    // blocks as the shared-memory budget allows are resident per SM
+    e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess) g_smem_done.insert({func, dev});
     return e;
 }

@@ -4,14 +4,16 @@
 // splits of mx; each split is reweighted by w = exp(mx - gmx); S = sum w*S_sp,
 // acc = sum w*oc_sp; o = acc / S, and 0 when S is 0 (every split empty).
 //
-// Here the same merge is evaluated in one streaming pass so that every load of
-// a block is issued up front: each warp folds its share of the splits into a
-// running (m, S, acc) with the §2.1 update rule (a new maximum rescales what
-// came before), then the warps' states are folded together the same way. The
-// result equals the two-pass form up to rounding. A split whose mx is -inf
-// (no rows) is skipped, so an all-empty row gives o = 0 without evaluating
-// -inf - (-inf). mx is in log2 units (the partial kernel folds log2 e into q),
-// so the weights use the base-2 exponential.
+// The same merge is evaluated as a fold so that every load of a block is in
+// flight at once: a block covers one (sequence, head) and one 32-wide chunk
+// of head_dim (more blocks than heads, so the partials stream through many
+// SMs); each group of lanes folds its share of the splits into a running
+// (m, S, acc) with the §2.1 update rule (a larger maximum rescales what came
+// before), the groups of a warp are folded with shuffles and the warps
+// through shared memory. The result equals the two-pass form up to rounding.
+// A split whose mx is -inf (no rows) is skipped, so an all-empty row gives
+// o = 0 without evaluating -inf - (-inf). mx is in log2 units (the partial
+// kernel folds log2 e into q), so the weights use the base-2 exponential.
 #pragma once
 
 #include "attn_device.cuh"
@@ -20,12 +22,14 @@ namespace attn {
 
 template <int HD>
 struct CombineCfg {
-    static constexpr int WARPS = 8;                   // split groups per head
+    static constexpr int WARPS = 8;
     static constexpr int THREADS = WARPS * 32;
-    static constexpr int VEC = HD >= 128 ? HD / 32 : 4;   // floats per lane per split row
-    static constexpr int TPS = HD / VEC;              // lanes per split row
-    static constexpr int LG = 32 / TPS;               // split rows per warp step
-    static constexpr int BATCH = 8;                   // split rows in flight per lane
+    static constexpr int DC = HD < 32 ? HD : 32;      // head_dim chunk per block
+    static constexpr int NCHUNK = HD / DC;
+    static constexpr int LPS = DC / 4;                // lanes per split row (float4 each)
+    static constexpr int SPW = 32 / LPS;              // split groups per warp
+    static constexpr int NG = WARPS * SPW;            // split groups per block
+    static constexpr int BATCH = 4;                   // split rows in flight per lane
 };
 
 // Fold (m2, S2, a2) into (m, S, a): the §2.1 rescale-and-add rule.
@@ -47,59 +51,65 @@ __global__ void __launch_bounds__(CombineCfg<HD>::THREADS)
 attn_combine(const CombineArgs a)
 {
     using C = CombineCfg<HD>;
-    constexpr int V = C::VEC;
-    __shared__ float sm_m[C::WARPS * C::LG], sm_s[C::WARPS * C::LG];
-    __shared__ float sm_acc[C::WARPS * C::LG][HD];
+    __shared__ float sm_m[C::WARPS], sm_s[C::WARPS];
+    __shared__ float sm_acc[C::WARPS][C::DC];
 
     pdl_wait();                                      // partials come from the previous grid
     pdl_launch_dependents();
 
-    const int h = blockIdx.x, s = blockIdx.y;
+    const int h = blockIdx.x, s = blockIdx.y, chunk = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int grp = lane / C::TPS, dt = lane % C::TPS;
+    const int sg = lane / C::LPS, dl = lane % C::LPS;
     const int P = a.n_splits;
     const size_t row = (size_t)s * a.n_head + h;
     const float2 *ml = a.ws_ml + row * P;
-    const float *oc = a.ws_o + row * (size_t)P * HD + dt * V;
+    const float *oc = a.ws_o + row * (size_t)P * HD + chunk * C::DC + dl * 4;
 
-    // stream this lane group's splits: sp = stride * i + first
-    const int first = warp * C::LG + grp, stride = C::WARPS * C::LG;
-    float m = -INFINITY, S = 0.f, acc[V];
-#pragma unroll
-    for (int i = 0; i < V; ++i) acc[i] = 0.f;
-    for (int base = first; base < P; base += stride * C::BATCH) {
+    // this lane group's splits: sp = group + NG * i
+    const int group = warp * C::SPW + sg;
+    float m = -INFINITY, S = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int base = group; base < P; base += C::NG * C::BATCH) {
         float2 mlv[C::BATCH];
-        float ov[C::BATCH][V];
+        float ov[C::BATCH][4];
 #pragma unroll
         for (int b = 0; b < C::BATCH; ++b) {
-            const int sp = base + b * stride;
+            const int sp = base + b * C::NG;
             mlv[b] = sp < P ? ml[sp] : make_float2(-INFINITY, 0.f);
-            const float *src = oc + (size_t)(sp < P ? sp : 0) * HD;
-#pragma unroll
-            for (int i = 0; i < V; i += 4) {
-                const float4 t = *reinterpret_cast<const float4 *>(src + i);
-                ov[b][i] = t.x; ov[b][i + 1] = t.y; ov[b][i + 2] = t.z; ov[b][i + 3] = t.w;
-            }
+            const float4 t = *reinterpret_cast<const float4 *>(oc + (size_t)(sp < P ? sp : 0) * HD);
+            ov[b][0] = t.x; ov[b][1] = t.y; ov[b][2] = t.z; ov[b][3] = t.w;
         }
 #pragma unroll
-        for (int b = 0; b < C::BATCH; ++b) fold<V>(m, S, acc, mlv[b].x, mlv[b].y, ov[b]);
+        for (int b = 0; b < C::BATCH; ++b) fold<4>(m, S, acc, mlv[b].x, mlv[b].y, ov[b]);
     }
-    // fold the lane groups and warps: publish, then thread d folds dim d
-    const int slot = warp * C::LG + grp;
-    if (dt == 0) {
-        sm_m[slot] = m;
-        sm_s[slot] = S;
-    }
+    // fold the warp's split groups (lanes LPS apart hold the same dims)
 #pragma unroll
-    for (int i = 0; i < V; ++i) sm_acc[slot][dt * V + i] = acc[i];
+    for (int off = C::LPS; off < 32; off <<= 1) {
+        float a2[4];
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+        const float S2 = __shfl_xor_sync(0xffffffffu, S, off);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a2[i] = __shfl_xor_sync(0xffffffffu, acc[i], off);
+        fold<4>(m, S, acc, m2, S2, a2);
+    }
+    if (sg == 0) {
+        if (dl == 0) {
+            sm_m[warp] = m;
+            sm_s[warp] = S;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sm_acc[warp][dl * 4 + i] = acc[i];
+    }
     __syncthreads();
-    for (int d = threadIdx.x; d < HD; d += C::THREADS) {
+    // fold the warps: thread d of the chunk
+    if (threadIdx.x < C::DC) {
+        const int d = threadIdx.x;
         float M = -INFINITY, St = 0.f, A[1] = {0.f};
-        for (int k = 0; k < C::WARPS * C::LG; ++k) {
-            const float a2[1] = {sm_acc[k][d]};
-            fold<1>(M, St, A, sm_m[k], sm_s[k], a2);
+#pragma unroll
+        for (int w = 0; w < C::WARPS; ++w) {
+            const float a2[1] = {sm_acc[w][d]};
+            fold<1>(M, St, A, sm_m[w], sm_s[w], a2);
         }
-        a.out[row * HD + d] = St > 0.f ? A[0] / St : 0.f;
+        a.out[row * HD + chunk * C::DC + d] = St > 0.f ? A[0] / St : 0.f;
     }
 }
 

@@ -12,19 +12,22 @@ namespace attn {
 // Pipeline shape per (policy, head_dim): compute warps and stages, sized so
 // the stage ring fits the 227 KB shared-memory budget with enough bytes in
 // flight per SM (about two stages ahead of the compute warps).
+// MINB is the number of resident blocks per SM the register budget is sized
+// for (the shared memory must allow as many).
 template <int HD> struct SimtShape;
-template <> struct SimtShape<8>   { static constexpr int NWC = 4, S = 4; };
-template <> struct SimtShape<64>  { static constexpr int NWC = 4, S = 3; };
-template <> struct SimtShape<128> { static constexpr int NWC = 4, S = 3; };
-template <> struct SimtShape<256> { static constexpr int NWC = 2, S = 3; };
+template <> struct SimtShape<8>   { static constexpr int NWC = 4, S = 4, MINB = 1; };
+template <> struct SimtShape<64>  { static constexpr int NWC = 4, S = 3, MINB = 1; };
+template <> struct SimtShape<128> { static constexpr int NWC = 4, S = 3, MINB = 1; };
+template <> struct SimtShape<256> { static constexpr int NWC = 2, S = 3, MINB = 1; };
 
-template <int HD> struct TcShape { static constexpr int NWC = 4, S = 3; };
-template <> struct TcShape<64>    { static constexpr int NWC = 4, S = 4; };
+template <int HD> struct TcShape  { static constexpr int NWC = 4, S = 3, MINB = 2; };
+template <> struct TcShape<64>    { static constexpr int NWC = 4, S = 4, MINB = 2; };
+template <> struct TcShape<256>   { static constexpr int NWC = 4, S = 3, MINB = 1; };
 
 template <int HD, int G>
-using SimtCfg = PartialCfg<HD, G, SimtWarp, SimtShape<HD>::NWC, SimtShape<HD>::S>;
+using SimtCfg = PartialCfg<HD, G, SimtWarp, SimtShape<HD>::NWC, SimtShape<HD>::S, SimtShape<HD>::MINB>;
 template <int HD, int G>
-using TcCfg = PartialCfg<HD, G, TcWarp, TcShape<HD>::NWC, TcShape<HD>::S>;
+using TcCfg = PartialCfg<HD, G, TcWarp, TcShape<HD>::NWC, TcShape<HD>::S, TcShape<HD>::MINB>;
 
 // Resident blocks per SM for a configuration: 228 KB of shared memory per SM
 // with 1 KB reserved per block, 64 K registers, at most 32 blocks.
@@ -64,7 +67,8 @@ cudaError_t launch_combine(const LaunchRequest &r)
     ca.n_splits = r.pa.n_splits;
     const void *fn = reinterpret_cast<const void *>(&attn_combine<HD>);
     void *args[] = {&ca};
-    return launch_pdl(fn, dim3(ca.n_head, r.n_seq), dim3(CombineCfg<HD>::THREADS), 0, r.stream, args);
+    return launch_pdl(fn, dim3(ca.n_head, r.n_seq, CombineCfg<HD>::NCHUNK),
+                      dim3(CombineCfg<HD>::THREADS), 0, r.stream, args);
 }
 
 template <int HD, int G>

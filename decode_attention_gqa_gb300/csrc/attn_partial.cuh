@@ -30,10 +30,11 @@
 
 namespace attn {
 
-template <int HD, int G, template <int, int, int> class W, int NWC_, int S_>
+template <int HD, int G, template <int, int, int> class W, int NWC_, int S_, int MINB_>
 struct PartialCfg {
     static constexpr int NWC = NWC_;                 // compute warps
     static constexpr int S = S_;                     // pipeline stages
+    static constexpr int MIN_BLOCKS = MINB_;         // resident blocks per SM the registers must allow
     using Warp = W<HD, G, NWC>;
     static constexpr int WR = Warp::WR;
     static constexpr int TILE = NWC * WR;            // rows per stage
@@ -52,10 +53,13 @@ struct PartialCfg {
     static_assert(MERGE_BYTES <= S * STAGE_BYTES, "merge area must fit in the stage buffers");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(HD < 64 || (TILE_BYTES / NCH) % 1024 == 0, "swizzled chunks must stay 1024-aligned");
+    // the shared memory must allow MIN_BLOCKS resident blocks (228 KB per SM,
+    // 1 KB reserved per block)
+    static_assert(MIN_BLOCKS * (SMEM_BYTES + 1024u) <= 233472u, "MIN_BLOCKS exceeds shared memory");
 };
 
 template <class Cfg, int HD, int G>
-__global__ void __launch_bounds__(Cfg::THREADS, 1)
+__global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS)
 attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                    const PartialArgs a)
 {
@@ -78,11 +82,9 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     pdl_wait();
     pdl_launch_dependents();
 
-    // a1 and a2 overlap: the positions load and the group's q loads are in
-    // flight together (an empty split prepares q for nothing; it is cheap).
+    // a1: rows attended and this split's range; an empty split leaves at once
     const int64_t nkv = rows_attended(a, s, sp == 0 && hk == 0 && tid == 0);
     const size_t head0 = (size_t)s * a.n_head + (size_t)hk * G;          // first query head of the group
-    Warp::prepare(extra, a.q + head0 * HD, a.qscale, tid, Cfg::THREADS);
     int64_t lo, hi;
     split_range(nkv, sp, P, a.split_len, WR, lo, hi);
     if (lo >= hi) {                                                      // empty split: mx=-inf, S=0
@@ -125,6 +127,8 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         }
         flags[1] = early;
     }
+    // a2, while the first tiles are in flight
+    Warp::template prepare<Cfg::THREADS>(extra, a.q + head0 * HD, a.qscale, tid);
     __syncthreads();
     early = flags[1];
 
@@ -146,21 +150,28 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
             if (nrows == TILE || tail_by_tma) {
                 if (lane == 0) tma_tile(t, st);
             } else {
-                // hi < TILE: rows [first, hi) to tile rows [TILE - nrows, TILE), zeros before
+                // hi < TILE: rows [first, hi) to tile rows [vs0, TILE), vs0 = TILE - nrows.
+                // V rows of the slice holding vs0 that lie before it are zeroed
+                // (their p is 0 and must not meet stale non-finite data); slices
+                // wholly before vs0 are skipped by the compute warps.
                 constexpr int NU = HD / 8;
                 uint8_t *kst = smem + st * Cfg::STAGE_BYTES;
                 uint8_t *vst = kst + Cfg::TILE_BYTES;
                 const int vs0 = TILE - nrows;
+                const int zs = vs0 / WR * WR;
                 const size_t rstride = (size_t)a.n_kv_head * HD;               // elements per row
                 const __half *kg = a.k + (size_t)(seq_row0 + first) * rstride + (size_t)hk * HD;
                 const __half *vg = a.v + (size_t)(seq_row0 + first) * rstride + (size_t)hk * HD;
-                for (int i = lane; i < TILE * NU; i += 32) {
-                    const int r = i / NU, U = i % NU;
-                    const bool in = r >= vs0;
-                    const size_t off = in ? (size_t)(r - vs0) * rstride + (size_t)U * 8 : 0;
+                for (int i = lane; i < (TILE - zs) * NU; i += 32) {
+                    const int r = zs + i / NU, U = i % NU;
                     const uint32_t so = tile_unit_offset<HD, TILE>(r, U);
-                    cp_async16(kst + so, kg + off, in ? 16u : 0u);
-                    cp_async16(vst + so, vg + off, in ? 16u : 0u);
+                    if (r >= vs0) {
+                        const size_t off = (size_t)(r - vs0) * rstride + (size_t)U * 8;
+                        cp_async16(kst + so, kg + off, 16u);
+                        cp_async16(vst + so, vg + off, 16u);
+                    } else {
+                        *reinterpret_cast<uint4 *>(vst + so) = make_uint4(0u, 0u, 0u, 0u);
+                    }
                 }
                 cp_async_mbar_arrive(full + st);
                 __syncwarp();

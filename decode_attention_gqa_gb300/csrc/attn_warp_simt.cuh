@@ -29,15 +29,28 @@ struct SimtWarp {
 
     // a2: the group's G query rows (f32), pre-multiplied by scale*log2(e),
     // into shared memory. All threads of the block take part.
+    template <int NTHREADS>
     static __device__ __forceinline__ void prepare(uint8_t *extra, const float *qg, float qscale,
-                                                   int tid, int nthreads)
+                                                   int tid)
     {
+        constexpr int N4 = G * HD / 4;                    // float4s of the group's q
+        constexpr int ITER = (N4 + NTHREADS - 1) / NTHREADS;
         const float4 *src = reinterpret_cast<const float4 *>(qg);
         float4 *dst = reinterpret_cast<float4 *>(extra);
-        for (int i = tid; i < G * HD / 4; i += nthreads) {
-            float4 t = __ldg(src + i);
-            t.x *= qscale; t.y *= qscale; t.z *= qscale; t.w *= qscale;
-            dst[i] = t;
+        float4 t[ITER];
+#pragma unroll
+        for (int it = 0; it < ITER; ++it) {
+            const int i = tid + it * NTHREADS;
+            if (i < N4) t[it] = __ldg(src + i);
+        }
+#pragma unroll
+        for (int it = 0; it < ITER; ++it) {
+            const int i = tid + it * NTHREADS;
+            if (i < N4) {
+                float4 u = t[it];
+                u.x *= qscale; u.y *= qscale; u.z *= qscale; u.w *= qscale;
+                dst[i] = u;
+            }
         }
     }
 

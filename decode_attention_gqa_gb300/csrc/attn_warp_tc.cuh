@@ -34,7 +34,7 @@ struct TcWarp {
     static constexpr int WR = 16;                     // rows per warp slice
     static constexpr int KSTEPS = HD / 16;            // k-steps of q·Kᵀ
     static constexpr int NTD = HD / 8;                // n-tiles of p·V
-    static constexpr bool Q_REGS = HD <= 128;         // keep q fragments in registers
+    static constexpr bool Q_REGS = HD <= 64;          // keep q fragments in registers (else smem)
     static constexpr float TAU = 8.f;                 // lazy-rescale threshold
     static constexpr float OFF = 7.f;                 // p headroom: max p in [2^OFF, 2^(OFF+TAU)]
     static constexpr uint32_t QT_BYTES = 16u * HD * 2;  // Q tile, f16, swizzled like K
@@ -45,35 +45,47 @@ struct TcWarp {
     float m_ref, l, inv_sc;
 
     // a2: Q tile rows g (hi) and 8 + g (lo) for g < G, zero rows for g >= G,
-    // and the per-head power-of-two scale. One warp per head.
+    // and the per-head power-of-two scale. Warp w takes heads w, w + NW, ...;
+    // all of a warp's loads are issued before any of its reductions.
+    template <int NTHREADS>
     static __device__ __forceinline__ void prepare(uint8_t *extra, const float *qg, float qscale,
-                                                   int tid, int nthreads)
+                                                   int tid)
     {
+        constexpr int NW = NTHREADS / 32;
+        constexpr int ITER = (8 + NW - 1) / NW;           // heads per warp
+        constexpr int PER = (HD + 31) / 32;               // elements per lane per head
         float *inv = reinterpret_cast<float *>(extra + QT_BYTES);
-        const int warp = tid >> 5, lane = tid & 31, nwarps = nthreads >> 5;
-        for (int g = warp; g < 8; g += nwarps) {
-            constexpr int PER = (HD + 31) / 32;
-            float x[PER];
-            float amax = 0.f;
+        const int warp = tid >> 5, lane = tid & 31;
+        float x[ITER][PER];
+#pragma unroll
+        for (int it = 0; it < ITER; ++it) {
+            const int g = warp + it * NW;
 #pragma unroll
             for (int i = 0; i < PER; ++i) {
                 const int d = lane + 32 * i;
-                x[i] = (g < G && d < HD) ? __ldg(qg + g * HD + d) * qscale : 0.f;
-                amax = fmaxf(amax, fabsf(x[i]));
+                x[it][i] = (g < G && d < HD) ? __ldg(qg + g * HD + d) * qscale : 0.f;
             }
+        }
+#pragma unroll
+        for (int it = 0; it < ITER; ++it) {
+            const int g = warp + it * NW;
+            if (g >= 8) break;                            // warp-uniform
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < PER; ++i) amax = fmaxf(amax, fabsf(x[it][i]));
             amax = warp_max(amax);
             int e = 0;
             float sc = 1.f;
             if (amax > 0.f) {
-                (void)frexpf(amax, &e);               // amax in [2^(e-1), 2^e)
-                sc = ldexpf(1.f, 15 - e);             // scaled max in [2^14, 2^15)
+                (void)frexpf(amax, &e);                   // amax in [2^(e-1), 2^e)
+                sc = ldexpf(1.f, 15 - e);                 // scaled max in [2^14, 2^15)
             }
             if (lane == 0) inv[g] = amax > 0.f ? ldexpf(1.f, e - 15) : 1.f;
 #pragma unroll
             for (int i = 0; i < PER; ++i) {
                 const int d = lane + 32 * i;
                 if (d < HD) {
-                    const float v = x[i] * sc;
+                    const float v = x[it][i] * sc;
                     const __half hi = __float2half_rn(v);
                     const __half lo = __float2half_rn(v - __half2float(hi));
                     const uint32_t off = tile_unit_offset<HD, 16>(g, d >> 3) + (d & 7) * 2;
