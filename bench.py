@@ -36,8 +36,8 @@ sys.path.insert(0, ROOT)
 METRIC = "decode-attn µs/layer and achieved HBM GB/s (K+V bytes/time) vs GB300 peak"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["attn_device.cuh", "attn_partial.cuh", "attn_combine.cuh",
-                  "attn_kernels_impl.cuh"]
+KERNEL_SOURCES = ["attn_device.cuh", "attn_partial.cuh", "attn_warp_tc.cuh", "attn_warp_simt.cuh",
+                  "attn_combine.cuh", "attn_kernels_impl.cuh"]
 
 
 def parse_args():
@@ -46,8 +46,10 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="7b", choices=["7b"])
-    ap.add_argument("--ctx", type=int, default=8192)
+    ap.add_argument("--workload", default="7b", choices=["7b", "long", "stress", "ragged", "tiny"],
+                    help="7b (the default bench line) or another workload, for the record")
+    ap.add_argument("--ctx", type=int, default=0, help="context override (0 = the workload's)")
+    ap.add_argument("--split-len", type=int, default=0, help="0 = split by count")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
     ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 simt, 2 tensor core")
     ap.add_argument("--splits", type=int, default=0, help="0 = library heuristic")
@@ -109,18 +111,19 @@ def kernel_source_hash() -> str:
 
 
 def profiled_traffic(workload_key: str):
-    """DRAM bytes per partial launch from the committed ncu summary, if it was
-    taken on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", "attn_split_partial_7b_ctx8192.md")
-    try:
+    """DRAM read+write bytes per partial launch for a workload from the committed
+    ncu summaries (profiles/*.md lines `traffic_per_launch_bytes[<key>]: N`),
+    only if the summary's `source_hash` matches the current kernel sources."""
+    import glob
+    want = kernel_source_hash()
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
         text = open(path).read()
-    except OSError:
-        return None
-    m_hash = re.search(r"^source_hash:\s*(\w+)", text, re.M)
-    m_key = re.search(r"^traffic_per_launch_bytes\[%s\]:\s*(\d+)" % re.escape(workload_key), text, re.M)
-    if not m_hash or not m_key or m_hash.group(1) != kernel_source_hash():
-        return None
-    return int(m_key.group(1))
+        m_hash = re.search(r"^source_hash:\s*(\w+)", text, re.M)
+        m_key = re.search(r"^traffic_per_launch_bytes\[%s\]:\s*(\d+)" % re.escape(workload_key),
+                          text, re.M)
+        if m_hash and m_key and m_hash.group(1) == want:
+            return int(m_key.group(1))
+    return None
 
 
 class ClockSampler:
@@ -181,35 +184,63 @@ class ClockSampler:
 
 # ------------------------------------------------------------ CPU oracle leg
 
-def oracle_rate(layers_host, w, ctx, budget_s: float, max_layers=None):
-    """Run the oracle (all host cores) over layers until budget_s; return
-    (GB/s of K+V, layers done, seconds, threads)."""
+def oracle_sample(layers_host, w, budget_s: float, max_units=None):
+    """Run the oracle on all host cores over (layer, KV head group) units of the
+    workload -- every query head of one KV head against that head's rows -- until
+    budget_s (or max_units); return (GB/s of K+V, units, seconds, threads, what)."""
+    import numpy as np
     import oracle
     threads = len(os.sched_getaffinity(0))
-    bytes_per_layer = ctx * w.n_kv_head * w.head_dim * 4
-    done, t0 = 0, time.perf_counter()
-    n = len(layers_host) if max_layers is None else max_layers
+    G = w.n_head // w.n_kv_head
+    units = [(l, hk) for l in range(len(layers_host)) for hk in range(w.n_kv_head)]
+    done, nbytes, t0 = 0, 0, time.perf_counter()
     while True:
-        lay = layers_host[done % len(layers_host)]
-        oracle.attn_decode(lay["q"], lay["k"], lay["v"], lay["positions"], w.n_head, w.n_kv_head,
-                           w.head_dim, w.cap, w.scale, n_threads=threads)
+        l, hk = units[done % len(units)]
+        lay = layers_host[l]
+        qg = np.ascontiguousarray(lay["q"][:, hk * G:(hk + 1) * G])
+        kg = np.ascontiguousarray(lay["k"][:, :, hk:hk + 1])
+        vg = np.ascontiguousarray(lay["v"][:, :, hk:hk + 1])
+        oracle.attn_decode(qg, kg, vg, lay["positions"], G, 1, w.head_dim, w.cap, w.scale,
+                           n_threads=threads)
+        nbytes += sum(min(max(int(p) + 1, 0), w.cap) for p in lay["positions"]) * w.head_dim * 4
         done += 1
         el = time.perf_counter() - t0
-        if el >= budget_s or done >= n:
+        if max_units is not None:
+            if done >= max_units:
+                break
+        elif el >= budget_s or done >= 100 * len(units):
             break
-    return done * bytes_per_layer / el / 1e9, done, el, threads
+    what = "%d (layer, KV-head group) units" % done
+    return nbytes / el / 1e9, done, el, threads, what
 
 
 # ------------------------------------------------------------------ our arm
 
-def make_host_layers(w, ctx, layers):
+def make_host_layers(w, layers):
     from decode_attention_gqa_gb300 import synthetic as syn
-    wc = w.with_ctx(ctx)
-    out = []
-    for l in range(layers):
-        lay = syn.make_layer(wc, layer=l)
-        out.append(lay)
-    return wc, out
+    return [syn.make_layer(w, layer=l) for l in range(layers)]
+
+
+def workload_for(args):
+    from decode_attention_gqa_gb300 import synthetic as syn
+    w = syn.WORKLOADS[args.workload]
+    if args.ctx:
+        w = w.with_ctx(args.ctx)
+    return w
+
+
+def describe(w, L):
+    return {
+        "7b": "7b-like decode: 1 sequence, 28 q / 4 KV heads, head_dim 128, f16 KV cache, "
+              "%d layers, graph replay with positions += 1 per step" % L,
+        "long": "long-context grouped decode: 1 sequence, 16 q / 2 KV heads, head_dim 256, "
+                "context 8400, %d layers, graph replay with positions += 1 per step" % L,
+        "stress": "stress decode: 1 sequence, context 131072, 64 q / 8 KV heads, head_dim 128, "
+                  "K x8, graph replay with positions += 1 per step",
+        "ragged": "batched ragged decode: 32 sequences, context ~ U[1, 32768], 32 q / 8 KV heads, "
+                  "head_dim 128, contiguous per-sequence f16 KV, static grid",
+        "tiny": "tiny decode: 1 sequence, 8 q / 2 KV heads, head_dim 128, context 512",
+    }.get(w.name, w.name)
 
 
 def run_ours(args, rank, world, local):
@@ -227,49 +258,63 @@ def run_ours(args, rank, world, local):
     dist_barrier(world)
     pkg.load()
 
-    w = syn.WORKLOADS[args.workload]
+    w = workload_for(args)
     L = args.layers or w.layers
-    ctx_end = args.ctx
     W, K = args.warmup, args.steps
-    wc, host = make_host_layers(w, ctx_end, L)
+    n_seq = w.n_seq
+    advance = n_seq == 1                 # single sequence: nkv grows by one per step
+    host = make_host_layers(w, L)
     dev = torch.device("cuda", local)
     s = torch.cuda.Stream(device=dev)
 
-    # device copies: every layer its own q, K, V, out; one positions array
     q = [torch.from_numpy(h["q"]).to(dev) for h in host]
     kc = [torch.from_numpy(h["k"]).to(dev) for h in host]
     vc = [torch.from_numpy(h["v"]).to(dev) for h in host]
     out = [torch.empty_like(x) for x in q]
-    pos = torch.zeros(1, dtype=torch.int32, device=dev)
-    P = args.splits or pkg.attn_split_heuristic(1, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0)
-    ws_bytes = pkg.attn_workspace_size(1, w.n_head, w.head_dim, P)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    pos = torch.from_numpy(host[0]["positions"].copy()).to(dev)
     torch.cuda.synchronize()
 
-    def layer_calls(stream, partial_only=False, combine_only=False):
-        for l in range(L):
-            if combine_only:
-                pkg.attn_decode_combine(ws, ws_bytes, out[l], 1, w.n_head, w.head_dim, P,
-                                        stream=stream)
-            elif partial_only:
-                pkg.attn_decode_partial(q[l], kc[l], vc[l], pos, 1, w.n_head, w.n_kv_head,
-                                        w.head_dim, w.scale, w.cap, P, 0, args.variant, ws,
-                                        ws_bytes, stream=stream)
-            else:
-                pkg.attn_decode_ex(q[l], kc[l], vc[l], pos, out[l], 1, w.n_head, w.n_kv_head,
-                                   w.head_dim, w.scale, w.cap, n_splits=P, variant=args.variant,
-                                   workspace=ws, workspace_bytes=ws_bytes, stream=stream)
+    def kv_bytes_for(nkvs):
+        return sum(min(max(int(n), 0), w.cap) for n in nkvs) * w.n_kv_head * w.head_dim * 4
 
-    def capture(advance: bool, partial_only=False, combine_only=False):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(s):
-            layer_calls(s, partial_only, combine_only)   # warm the launch path outside capture
-        torch.cuda.synchronize()
-        with torch.cuda.graph(g, stream=s):
-            if advance:
-                pos.add_(1)
-            layer_calls(torch.cuda.current_stream(), partial_only, combine_only)
-        return g
+    class Plan:
+        """Graphs of the L layer calls for one (P, split_len): the whole call, the
+        partial stage alone and the combine stage alone."""
+
+        def __init__(self, P, blk):
+            self.P, self.blk = P, blk
+            self.ws_bytes = pkg.attn_workspace_size(n_seq, w.n_head, w.head_dim, P)
+            self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+            self.g_full = self._capture(advance, "full")
+            self.g_partial = self._capture(False, "partial")
+            self.g_combine = self._capture(False, "combine")
+
+        def _calls(self, stream, stage):
+            for l in range(L):
+                if stage == "combine":
+                    pkg.attn_decode_combine(self.ws, self.ws_bytes, out[l], n_seq, w.n_head,
+                                            w.head_dim, self.P, stream=stream)
+                elif stage == "partial":
+                    pkg.attn_decode_partial(q[l], kc[l], vc[l], pos, n_seq, w.n_head, w.n_kv_head,
+                                            w.head_dim, w.scale, w.cap, self.P, self.blk,
+                                            args.variant, self.ws, self.ws_bytes, stream=stream)
+                else:
+                    pkg.attn_decode_ex(q[l], kc[l], vc[l], pos, out[l], n_seq, w.n_head,
+                                       w.n_kv_head, w.head_dim, w.scale, w.cap, n_splits=self.P,
+                                       split_len=self.blk, variant=args.variant,
+                                       workspace=self.ws, workspace_bytes=self.ws_bytes,
+                                       stream=stream)
+
+        def _capture(self, adv, stage):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(s):
+                self._calls(s, stage)              # warm the launch path outside capture
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=s):
+                if adv:
+                    pos.add_(1)
+                self._calls(torch.cuda.current_stream(), stage)
+            return g
 
     def timed_replays(g, n, clocks=None):
         e0 = torch.cuda.Event(enable_timing=True)
@@ -288,78 +333,104 @@ def run_ours(args, rank, world, local):
         dist_barrier(world)
         return e0.elapsed_time(e1), clk
 
-    def kv_bytes(nkv):
-        return nkv * w.n_kv_head * w.head_dim * 2 * 2
+    def warm(g):
+        with torch.cuda.stream(s):
+            for _ in range(W):
+                g.replay()
 
-    # ---- main timed region: W warm-up + K timed replays of the 28-layer step
-    g = capture(advance=True)
-    start_pos = ctx_end - 1 - (W + K)
-    assert start_pos >= 0, "context too short for the step count"
-    pos.fill_(start_pos)
-    with torch.cuda.stream(s):
-        for _ in range(W):
-            g.replay()
+    def measure(plan, ctx_end, clocks=None):
+        """Whole-step time and bytes (positions advancing for one sequence), then
+        each stage alone at the final nkv. Returns a dict."""
+        if advance:
+            start = ctx_end - 1 - (W + K)
+            assert start >= 0, "context too short for the step count"
+            pos.fill_(start)
+            nkv_steps = [[start + W + i + 2] for i in range(K)]
+        else:
+            nkv_steps = [[c for c in w.ctx] for _ in range(K)]
+        warm(plan.g_full)
+        ms, clk = timed_replays(plan.g_full, K, clocks)
+        ms = dist_max(ms, world)
+        step_bytes = [kv_bytes_for(n) * L for n in nkv_steps]
+        final = nkv_steps[-1]
+        if advance:
+            pos.fill_(final[0] - 1)
+        warm(plan.g_partial)
+        ms_p, _ = timed_replays(plan.g_partial, K)
+        warm(plan.g_combine)
+        ms_c, _ = timed_replays(plan.g_combine, K)
+        return {"ms": ms, "clk": clk, "bytes": sum(step_bytes) * world,
+                "partial_us": ms_p * 1e3 / (K * L), "combine_us": ms_c * 1e3 / (K * L),
+                "launch_bytes": kv_bytes_for(final)}
+
+    # ---- main timed region: the library's default split choice
+    blk0 = args.split_len
+    if args.splits:
+        P0 = args.splits
+    elif blk0:
+        P0 = -(-w.cap // blk0)
+    else:
+        P0 = pkg.attn_split_heuristic(n_seq, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0)
+    plan = Plan(P0, blk0)
+    ctx_end = max(w.ctx)
     clocks = ClockSampler(local, enabled=not args.no_clocks)
-    ms, clk = timed_replays(g, K, clocks)
-    nkvs = [start_pos + W + i + 2 for i in range(K)]        # nkv seen by timed step i
-    step_bytes = [kv_bytes(n) * L for n in nkvs]
-    ms_max = dist_max(ms, world)
-    total_bytes = sum(step_bytes) * world
-    value = total_bytes / (ms_max * 1e-3) / 1e9
-    us_per_layer = ms_max * 1e3 / (K * L)
+    m0 = measure(plan, ctx_end, clocks)
+    value = m0["bytes"] / (m0["ms"] * 1e-3) / 1e9
+    us_per_layer = m0["ms"] * 1e3 / (K * L)
 
-    # correctness spot check of the last step (oracle, one layer)
+    # correctness spot check of layer 0 at the final nkv (oracle)
     import oracle
-    lay0 = dict(host[0], positions=np.array([nkvs[-1] - 1], np.int32))
-    ref = oracle.attn_decode(lay0["q"], lay0["k"], lay0["v"], lay0["positions"], w.n_head,
-                             w.n_kv_head, w.head_dim, w.cap, w.scale, n_threads=8)
-    got = out[0].cpu().numpy().astype(np.float64)
+    torch.cuda.synchronize()
+    pos_now = pos.cpu().numpy()
+    with torch.cuda.stream(s):
+        plan._calls(s, "full")
+    torch.cuda.synchronize()
+    lay0 = dict(host[0], positions=pos_now)
+    if n_seq == 1:
+        ref = oracle.attn_decode(lay0["q"], lay0["k"], lay0["v"], lay0["positions"], w.n_head,
+                                 w.n_kv_head, w.head_dim, w.cap, w.scale, n_threads=8)
+        got = out[0].cpu().numpy().astype(np.float64)
+    else:
+        sidx = [0, n_seq // 2, n_seq - 1]
+        ref = np.stack([oracle.attn_decode_one(lay0["q"], lay0["k"], lay0["v"], lay0["positions"],
+                                               w.n_head, w.n_kv_head, w.head_dim, w.cap, w.scale,
+                                               si, 0) for si in sidx])
+        got = out[0].cpu().numpy().astype(np.float64)[sidx, 0]
     parity_ok = bool(np.all(np.abs(got - ref) <= 1e-4 + 1e-3 * np.abs(ref)))
 
-    # ---- each stage alone: graphs of L partial-only and L combine-only launches
-    gp = capture(advance=False, partial_only=True)
-    gc = capture(advance=False, combine_only=True)
-
-    def stage_times(c):
-        """(partial µs, combine µs) per launch at nkv = c."""
-        pos.fill_(c - 1)
-        with torch.cuda.stream(s):
-            for _ in range(W):
-                gp.replay()
-        ms_p, _ = timed_replays(gp, K)
-        with torch.cuda.stream(s):
-            for _ in range(W):
-                gc.replay()
-        ms_c, _ = timed_replays(gc, K)
-        return ms_p * 1e3 / (K * L), ms_c * 1e3 / (K * L)
-
-    partial_us, combine_us = stage_times(ctx_end)
-    achieved = kv_bytes(ctx_end) / (partial_us * 1e-6) / 1e9
+    achieved = m0["launch_bytes"] / (m0["partial_us"] * 1e-6) / 1e9
     peak, peak_kind = measured_peak()
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                "traffic": profiled_traffic("7b_ctx%d" % ctx_end),
-                "kernel": "attn_split_partial", "bytes_per_launch": kv_bytes(ctx_end),
-                "us_per_launch": round(partial_us, 3), "combine_us_per_launch": round(combine_us, 3)}
+                "traffic": profiled_traffic("%s_ctx%d" % (w.name, ctx_end)),
+                "kernel": "attn_split_partial", "bytes_per_launch": m0["launch_bytes"],
+                "us_per_launch": round(m0["partial_us"], 3),
+                "combine_us_per_launch": round(m0["combine_us"], 3)}
 
-    # ---- context sweep (same caches, positions set per point)
+    # ---- sweeps: context (7b) or split block length (long)
     sweep = {}
     if not args.no_sweep:
-        for c in syn.CTX_SWEEP_7B:
-            if c == ctx_end or c - 1 - (W + K) < 0:
-                continue
-            pos.fill_(c - 1 - (W + K))
-            with torch.cuda.stream(s):
-                for _ in range(W):
-                    g.replay()
-            ms_c, _ = timed_replays(g, K)
-            ms_c = dist_max(ms_c, world)
-            b = sum(kv_bytes(c - K + i + 1) * L for i in range(K))
-            p_us, c_us = stage_times(c)
-            sweep[str(c)] = {"us_per_layer": round(ms_c * 1e3 / (K * L), 3),
-                             "gbs": round(b * world / (ms_c * 1e-3) / 1e9, 1),
-                             "partial_us": round(p_us, 3), "combine_us": round(c_us, 3)}
-    pos.fill_(ctx_end - 1)
+        if w.name == "7b":
+            for c in syn.CTX_SWEEP_7B:
+                if c == ctx_end or c - 1 - (W + K) < 0:
+                    continue
+                m = measure(plan, c)
+                sweep["ctx%d" % c] = {"us_per_layer": round(m["ms"] * 1e3 / (K * L), 3),
+                                      "gbs": round(m["bytes"] / (m["ms"] * 1e-3) / 1e9, 1),
+                                      "partial_us": round(m["partial_us"], 3),
+                                      "combine_us": round(m["combine_us"], 3)}
+        elif w.name == "long":
+            for blk in syn.BLOCK_SWEEP_LONG:
+                pb = Plan(-(-w.cap // blk), blk)
+                m = measure(pb, ctx_end)
+                sweep["blk%d" % blk] = {"n_splits": pb.P,
+                                        "us_per_layer": round(m["ms"] * 1e3 / (K * L), 3),
+                                        "gbs": round(m["bytes"] / (m["ms"] * 1e-3) / 1e9, 1),
+                                        "partial_us": round(m["partial_us"], 3),
+                                        "combine_us": round(m["combine_us"], 3)}
+                del pb
+        if advance:
+            pos.fill_(ctx_end - 1)
 
     # ---- end to end through the C ABI from pinned host buffers
     e2e = None
@@ -367,9 +438,12 @@ def run_ours(args, rank, world, local):
         hq = [torch.from_numpy(h["q"]).pin_memory() for h in host]
         hk = [torch.from_numpy(h["k"]).pin_memory() for h in host]
         hv = [torch.from_numpy(h["v"]).pin_memory() for h in host]
-        hpos = torch.tensor([ctx_end - 2], dtype=torch.int32).pin_memory()   # +1 in the graph
+        hpos_np = host[0]["positions"].copy()
+        if advance:
+            hpos_np[:] = ctx_end - 2                    # the graph adds 1
+        hpos = torch.from_numpy(hpos_np).pin_memory()
         hout = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in out]
-        h2d = sum(t.numel() * t.element_size() for t in hq + hk + hv) + 4
+        h2d = sum(t.numel() * t.element_size() for t in hq + hk + hv) + hpos.numel() * 4
         d2h = sum(t.numel() * t.element_size() for t in hout)
 
         def e2e_step():
@@ -379,7 +453,7 @@ def run_ours(args, rank, world, local):
                     q[l].copy_(hq[l], non_blocking=True)
                     kc[l].copy_(hk[l], non_blocking=True)
                     vc[l].copy_(hv[l], non_blocking=True)
-                g.replay()
+                plan.g_full.replay()
                 for l in range(L):
                     hout[l].copy_(out[l], non_blocking=True)
 
@@ -392,37 +466,35 @@ def run_ours(args, rank, world, local):
             e2e_step()
         torch.cuda.synchronize()
         el = dist_max(time.perf_counter() - t0, world)
-        e2e = {"value": round(kv_bytes(ctx_end) * L * K * world / el / 1e9, 1), "unit": UNIT,
+        nkv_e2e = [ctx_end] if advance else list(w.ctx)
+        e2e = {"value": round(kv_bytes_for(nkv_e2e) * L * K * world / el / 1e9, 1), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(el * 1e3 / K, 3)}
 
     # ---- CPU oracle baseline (rank 0 only, N == 1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        rate, done, el, threads = oracle_rate(host, wc, ctx_end, budget_s=10.0, max_layers=10 * L)
+        rate, done, el, threads, what = oracle_sample(host, w, budget_s=10.0)
         cpu = {"value": round(rate, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": "%d layer calls of the %s workload at context %d (%.1f s)"
-                         % (done, args.workload, ctx_end, el)}
+               "sample": "%s of the %s workload (%.1f s)" % (what, w.name, el)}
 
     spills = cuda_build.spill_report()
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
-            "steps": K, "warmup": W, "ms_per_step": round(ms_max / K, 4),
+            "steps": K, "warmup": W, "ms_per_step": round(m0["ms"] / K, 4),
             "us_per_layer": round(us_per_layer, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": "7b-like decode: 1 sequence, 28 q / 4 KV heads, head_dim 128, "
-                                   "f16 KV cache, %d layers, graph replay with positions += 1 "
-                                   "per step" % L,
-                       "ctx": ctx_end, "cap": w.cap, "n_head": w.n_head, "n_kv_head": w.n_kv_head,
-                       "head_dim": w.head_dim, "layers": L, "n_splits": P,
+            "config": {"workload": describe(w, L), "name": w.name, "ctx": ctx_end, "cap": w.cap,
+                       "n_seq": n_seq, "n_head": w.n_head, "n_kv_head": w.n_kv_head,
+                       "head_dim": w.head_dim, "layers": L, "n_splits": P0, "split_len": blk0,
                        "variant": args.variant, "kv_dtype": "f16",
                        "l2": "inputs larger than L2 (%d MB of K+V per step)"
-                             % (kv_bytes(ctx_end) * L // 2 ** 20),
+                             % (kv_bytes_for([ctx_end] if advance else w.ctx) * L // 2 ** 20),
                        "parallelism": "replicas" if world > 1 else "single"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": 2 * L * K, "clocks": clk, "sweep": sweep,
-            "parity_last_step": parity_ok,
+            "gpu_launches": 2 * L * K, "clocks": m0["clk"], "sweep": sweep,
+            "parity_spot_check": parity_ok,
             "ptxas_spill_bytes": sum(v["spill_stores"] + v["spill_loads"] for v in spills.values()),
         }
         print(json.dumps(line), flush=True)
@@ -435,40 +507,35 @@ def run_ours(args, rank, world, local):
 
 def run_reference(args, rank, world, local):
     """The oracle timed on the host cores, on this arm's metric and workload;
-    each step is a bounded sample (a few layer calls) of the step."""
+    each step is a bounded sample -- a few (layer, KV-head group) units -- of
+    the step, sized so that warm-up plus steps stay within about two minutes."""
     if rank != 0:
         return
-    from decode_attention_gqa_gb300 import synthetic as syn
-    w = syn.WORKLOADS[args.workload]
+    w = workload_for(args)
     L = args.layers or w.layers
-    ctx = args.ctx
-    wc, host = make_host_layers(w, ctx, min(L, 4))
-    bytes_per_layer = ctx * w.n_kv_head * w.head_dim * 4
-    threads = len(os.sched_getaffinity(0))
-    # size a step so that warmup + steps stay within about two minutes
-    _, _, el1, _ = oracle_rate(host, wc, ctx, budget_s=0.0, max_layers=1)
-    per_step_layers = max(1, min(L, int(4.0 / max(el1, 1e-6))))
-    per_step_layers = min(per_step_layers, max(1, int(100.0 / max(el1 * (args.steps + args.warmup), 1e-6))))
+    host = make_host_layers(w, min(L, 2))
+    rate1, _, el1, threads, _ = oracle_sample(host, w, budget_s=0.0, max_units=1)
+    per_step = max(1, min(L * w.n_kv_head,
+                          int(100.0 / max(el1 * (args.steps + args.warmup), 1e-6))))
     for _ in range(args.warmup):
-        oracle_rate(host, wc, ctx, budget_s=0.0, max_layers=per_step_layers)
-    t0 = time.perf_counter()
+        oracle_sample(host, w, budget_s=0.0, max_units=per_step)
+    total_bytes, total_s = 0.0, 0.0
     for _ in range(args.steps):
-        oracle_rate(host, wc, ctx, budget_s=0.0, max_layers=per_step_layers)
-    el = time.perf_counter() - t0
-    value = per_step_layers * args.steps * bytes_per_layer / el / 1e9
-    sample = ("%d of %d layer calls per step of the %s workload at context %d"
-              % (per_step_layers, L, args.workload, ctx))
+        rate, done, el, threads, what = oracle_sample(host, w, budget_s=0.0, max_units=per_step)
+        total_bytes += rate * el * 1e9
+        total_s += el
+    value = total_bytes / total_s / 1e9
+    sample = ("%d of the %d (layer, KV-head group) units of a step of the %s workload, per step"
+              % (per_step, L * w.n_kv_head, w.name))
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(el * 1e3 / args.steps, 3),
-        "us_per_layer": round(el * 1e6 / (args.steps * per_step_layers), 1),
+        "ms_per_step": round(total_s * 1e3 / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "7b-like decode: 1 sequence, 28 q / 4 KV heads, head_dim 128, "
-                               "f16 KV cache, %d layers" % L, "ctx": ctx, "layers": L},
-        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": sample},
+        "config": {"workload": describe(w, L), "name": w.name, "ctx": max(w.ctx), "layers": L},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": threads,
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

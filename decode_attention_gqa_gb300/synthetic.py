@@ -72,7 +72,7 @@ WORKLOADS = {
     # 7B-like decode: 28/4 heads (group 7), hd 128, context swept, 28 layers, cap 8192
     "7b": Workload("7b", 1, 28, 4, 128, 8192, (8192,), layers=28, seed=1),
     # long-context grouped: 16/2 heads (group 8), hd 256, context 8400, 12 layers
-    "long": Workload("long", 1, 16, 2, 256, 8400, (8400,), layers=12, seed=2, split_len=128),
+    "long": Workload("long", 1, 16, 2, 256, 8400, (8400,), layers=12, seed=2),
     # batched ragged: 32 sequences, context ~ U[1, 32768], 32/8 heads, hd 128
     "ragged": Workload("ragged", 32, 32, 8, 128, 32768, _ragged_ctx(3, 32, 1, 32768), seed=3),
     # stress: context 131072, 64/8 heads, hd 128, K x8
