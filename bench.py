@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
     ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 simt, 2 tensor core")
     ap.add_argument("--splits", type=int, default=0, help="0 = library heuristic")
+    ap.add_argument("--append", action="store_true",
+                    help="time attn_decode_append (write the new K/V row, then attend)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
@@ -272,6 +274,8 @@ def run_ours(args, rank, world, local):
     vc = [torch.from_numpy(h["v"]).to(dev) for h in host]
     out = [torch.empty_like(x) for x in q]
     pos = torch.from_numpy(host[0]["positions"].copy()).to(dev)
+    kn = [torch.randn(n_seq, w.n_kv_head, w.head_dim, device=dev).half() for _ in range(L)]
+    vn = [torch.randn(n_seq, w.n_kv_head, w.head_dim, device=dev).half() for _ in range(L)]
     torch.cuda.synchronize()
 
     def kv_bytes_for(nkvs):
@@ -298,6 +302,12 @@ def run_ours(args, rank, world, local):
                     pkg.attn_decode_partial(q[l], kc[l], vc[l], pos, n_seq, w.n_head, w.n_kv_head,
                                             w.head_dim, w.scale, w.cap, self.P, self.blk,
                                             args.variant, self.ws, self.ws_bytes, stream=stream)
+                elif args.append:
+                    pkg.attn_decode_append(q[l], kn[l], vn[l], kc[l], vc[l], pos, out[l], n_seq,
+                                           w.n_head, w.n_kv_head, w.head_dim, w.scale, w.cap,
+                                           n_splits=self.P, split_len=self.blk,
+                                           variant=args.variant, workspace=self.ws,
+                                           workspace_bytes=self.ws_bytes, stream=stream)
                 else:
                     pkg.attn_decode_ex(q[l], kc[l], vc[l], pos, out[l], n_seq, w.n_head,
                                        w.n_kv_head, w.head_dim, w.scale, w.cap, n_splits=self.P,
@@ -386,6 +396,9 @@ def run_ours(args, rank, world, local):
         plan._calls(s, "full")
     torch.cuda.synchronize()
     lay0 = dict(host[0], positions=pos_now)
+    if args.append:                      # the cache now holds appended rows: compare with it
+        lay0["k"] = kc[0].cpu().numpy()
+        lay0["v"] = vc[0].cpu().numpy()
     if n_seq == 1:
         ref = oracle.attn_decode(lay0["q"], lay0["k"], lay0["v"], lay0["positions"], w.n_head,
                                  w.n_kv_head, w.head_dim, w.cap, w.scale, n_threads=8)
@@ -488,7 +501,7 @@ def run_ours(args, rank, world, local):
             "config": {"workload": describe(w, L), "name": w.name, "ctx": ctx_end, "cap": w.cap,
                        "n_seq": n_seq, "n_head": w.n_head, "n_kv_head": w.n_kv_head,
                        "head_dim": w.head_dim, "layers": L, "n_splits": P0, "split_len": blk0,
-                       "variant": args.variant, "kv_dtype": "f16",
+                       "variant": args.variant, "kv_dtype": "f16", "append": args.append,
                        "l2": "inputs larger than L2 (%d MB of K+V per step)"
                              % (kv_bytes_for([ctx_end] if advance else w.ctx) * L // 2 ** 20),
                        "parallelism": "replicas" if world > 1 else "single"},

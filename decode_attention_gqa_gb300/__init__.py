@@ -18,7 +18,8 @@ __all__ = [
     "AttnError", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_WORKSPACE",
     "ATTN_ERR_CUDA", "ATTN_DEVERR_POSITION_CLAMPED", "ATTN_DEVERR_PIPELINE_TIMEOUT",
     "ATTN_VARIANT_AUTO", "ATTN_VARIANT_SIMT", "ATTN_VARIANT_TC", "library_path", "load",
-    "attn_decode", "attn_decode_ex", "attn_decode_partial", "attn_decode_combine",
+    "attn_decode", "attn_decode_ex", "attn_decode_append", "attn_decode_partial",
+    "attn_decode_combine",
     "attn_decode_static",
     "attn_split_heuristic", "attn_workspace_size",
     "attn_read_device_error", "attn_status_string", "attn_last_cuda_error", "attn_version",
@@ -65,6 +66,9 @@ def load():
         lib.attn_decode_ex.restype = i32
         lib.attn_decode_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i64, i32, i32,
                                        i32, vp, sz, vp]
+        lib.attn_decode_append.restype = i32
+        lib.attn_decode_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i64,
+                                           i32, i32, i32, vp, sz, vp]
         lib.attn_decode_partial.restype = i32
         lib.attn_decode_partial.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, i64, i32, i32,
                                             i32, vp, sz, vp]
@@ -134,6 +138,19 @@ def attn_decode_ex(q, k_cache, v_cache, positions, out, n_seq, n_head, n_kv_head
                                  split_len, variant, _ptr(workspace), workspace_bytes,
                                  _stream(stream)),
            "attn_decode_ex")
+
+
+def attn_decode_append(q, k_new, v_new, k_cache, v_cache, positions, out, n_seq, n_head, n_kv_head,
+                       head_dim, scale, cap, n_splits=0, split_len=0, variant=ATTN_VARIANT_AUTO,
+                       workspace=None, workspace_bytes=0, stream=None):
+    """Write the new token's K/V row at positions[s] and attend, fused."""
+    if workspace is not None and not workspace_bytes and hasattr(workspace, "nbytes"):
+        workspace_bytes = workspace.nbytes
+    _check(load().attn_decode_append(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                     _ptr(v_cache), _ptr(positions), _ptr(out), n_seq, n_head,
+                                     n_kv_head, head_dim, scale, cap, n_splits, split_len, variant,
+                                     _ptr(workspace), workspace_bytes, _stream(stream)),
+           "attn_decode_append")
 
 
 def attn_decode_partial(q, k_cache, v_cache, positions, n_seq, n_head, n_kv_head, head_dim,

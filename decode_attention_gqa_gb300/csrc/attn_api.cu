@@ -124,7 +124,8 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
                         const int32_t *positions, float *out, int n_seq, int n_head,
                         int n_kv_head, int head_dim, float scale, int64_t cap, bool cap_known,
                         int n_splits, int split_len, int variant, void *workspace,
-                        size_t workspace_bytes, int stages, cudaStream_t stream)
+                        size_t workspace_bytes, int stages, cudaStream_t stream,
+                        const void *k_new = nullptr, const void *v_new = nullptr)
 {
     // ---- synchronous argument checks, nothing launched yet ----
     if (n_seq < 0 || n_head <= 0 || n_kv_head <= 0 || head_dim <= 0) return ATTN_ERR_INVALID_ARG;
@@ -138,8 +139,9 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     if (n_seq > 0 && (stages & attn::kStageCombine) && !out) return ATTN_ERR_INVALID_ARG;
     if (n_seq > 65535 || n_kv_head > 65535) return ATTN_ERR_INVALID_ARG;   // grid y / z limits
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(positions) ||
-        !aligned16(out))
+        !aligned16(out) || !aligned16(k_new) || !aligned16(v_new))
         return ATTN_ERR_INVALID_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr)) return ATTN_ERR_INVALID_ARG;
     if ((int64_t)n_seq * cap > kMaxFlatRows - 1024) return ATTN_ERR_INVALID_ARG;
     const int group = n_head / n_kv_head;
     if (!head_dim_supported(head_dim) || group > 8) return ATTN_ERR_UNSUPPORTED;
@@ -202,6 +204,12 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     r.pa.split_len = split_len;
     r.pa.cap = cap;
     r.pa.qscale = (float)((double)scale * 1.4426950408889634);
+    if (k_new) {
+        r.pa.k_new = static_cast<const __half *>(k_new);
+        r.pa.v_new = static_cast<const __half *>(v_new);
+        r.pa.k_w = static_cast<__half *>(const_cast<void *>(k_cache));
+        r.pa.v_w = static_cast<__half *>(const_cast<void *>(v_cache));
+    }
     r.k_cache = k_cache;
     r.v_cache = v_cache;
     r.out = out;
@@ -318,6 +326,19 @@ attn_status attn_decode_ex(const float *q, const void *k_cache, const void *v_ca
                        scale, cap, true, n_splits, split_len, variant, workspace, workspace_bytes,
                        attn::kStagePartial | attn::kStageCombine,
                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_decode_append(const float *q, const void *k_new, const void *v_new,
+                               void *k_cache, void *v_cache, const int32_t *positions, float *out,
+                               int n_seq, int n_head, int n_kv_head, int head_dim, float scale,
+                               int64_t cap, int n_splits, int split_len, int variant,
+                               void *workspace, size_t workspace_bytes, attn_stream_t stream)
+{
+    if (n_seq > 0 && (!k_new || !v_new)) return ATTN_ERR_INVALID_ARG;
+    return decode_impl(q, k_cache, v_cache, positions, out, n_seq, n_head, n_kv_head, head_dim,
+                       scale, cap, true, n_splits, split_len, variant, workspace, workspace_bytes,
+                       attn::kStagePartial | attn::kStageCombine,
+                       reinterpret_cast<cudaStream_t>(stream), k_new, v_new);
 }
 
 attn_status attn_decode_partial(const float *q, const void *k_cache, const void *v_cache,

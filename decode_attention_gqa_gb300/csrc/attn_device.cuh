@@ -37,6 +37,12 @@ struct PartialArgs {
     int split_len;            // 0 = by count
     int64_t cap;              // cache rows per sequence
     float qscale;             // scale * log2(e): scores come out in log2 units
+    // Fused append (optional): the new token's rows [n_seq][n_kv_head][HD] f16,
+    // written into cache row positions[s] and attended in the same launch.
+    const __half *k_new;      // null: no append
+    const __half *v_new;
+    __half *k_w;              // the caches again, writable, when appending
+    __half *v_w;
 };
 
 struct CombineArgs {
@@ -52,13 +58,16 @@ struct CombineArgs {
 // to [0, cap] ("10 · R4" §2.2). By count: chunk = ceil(nkv / P) rounded up to
 // kSplitGranule rows; by block (Red Lite dev35 "Change"): chunk = split_len.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ int64_t rows_attended(const PartialArgs &a, int s, bool report)
+__device__ __forceinline__ int64_t rows_attended(const PartialArgs &a, int s, bool report,
+                                                 bool *in_range = nullptr)
 {
     int64_t n = (int64_t)__ldg(a.positions + s) + 1;
-    if (n < 0 || n > a.cap) {
+    const bool ok = n >= 0 && n <= a.cap;
+    if (!ok) {
         if (report) atomicOr(a.err, kErrPositionClamped);
         n = n < 0 ? 0 : a.cap;
     }
+    if (in_range) *in_range = ok;
     return n;
 }
 
@@ -156,6 +165,11 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z),
            "r"(smem_u32(bar))
         : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)

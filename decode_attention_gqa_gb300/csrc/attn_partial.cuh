@@ -83,7 +83,8 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     pdl_launch_dependents();
 
     // a1: rows attended and this split's range; an empty split leaves at once
-    const int64_t nkv = rows_attended(a, s, sp == 0 && hk == 0 && tid == 0);
+    bool pos_ok;
+    const int64_t nkv = rows_attended(a, s, sp == 0 && hk == 0 && tid == 0, &pos_ok);
     const size_t head0 = (size_t)s * a.n_head + (size_t)hk * G;          // first query head of the group
     int64_t lo, hi;
     split_range(nkv, sp, P, a.split_len, WR, lo, hi);
@@ -183,6 +184,25 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         // ---------------- compute warps ----------------
         Warp wst;
         wst.init(extra, warp, lane);
+        // Fused append: the split ending at nkv holds the new row nkv - 1, and in
+        // its last tile that row is always shared-memory row TILE - 1, owned by
+        // the last compute warp. That warp puts the new K/V row into the tile
+        // (over whatever the cache held there) and into the cache itself; no
+        // other block reads this row.
+        constexpr int NU = HD / 8;
+        constexpr int NJ = (2 * NU + 31) / 32;
+        const bool appending = a.k_new != nullptr && pos_ok && hi == nkv && warp == NWC - 1;
+        uint4 newrow[NJ];
+        if (appending) {
+            const size_t src = ((size_t)s * a.n_kv_head + hk) * HD;
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+                const int i = lane + 32 * j;
+                if (i < 2 * NU)
+                    newrow[j] = __ldg(reinterpret_cast<const uint4 *>((i < NU ? a.k_new : a.v_new) + src) +
+                                      (i < NU ? i : i - NU));
+            }
+        }
         for (int t = 0; t < ntiles; ++t) {
             const int st = t % S;
             const bool landed = mbar_wait_bounded(full + st, (t / S) & 1);
@@ -196,6 +216,21 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
             const int64_t first = lo + (int64_t)t * TILE;
             const int nrows = (int)(hi - first < TILE ? hi - first : TILE);
             const int ra = TILE - nrows - warp * WR;      // first in-range row of the slice
+            if (appending && t == ntiles - 1) {
+                const size_t dst = ((size_t)(seq_row0 + nkv - 1) * a.n_kv_head + hk) * HD;
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) {
+                    const int i = lane + 32 * j;
+                    if (i < 2 * NU) {
+                        const int U = i < NU ? i : i - NU;
+                        uint8_t *tile = const_cast<uint8_t *>(i < NU ? kst : vst);
+                        *reinterpret_cast<uint4 *>(tile + tile_unit_offset<HD, TILE>(TILE - 1, U)) = newrow[j];
+                        reinterpret_cast<uint4 *>((i < NU ? a.k_w : a.v_w) + dst)[U] = newrow[j];
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
             if (ra < WR) wst.template process<TILE>(kst, vst, warp * WR, ra > 0 ? ra : 0, extra, warp, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(empty + st);

@@ -113,6 +113,25 @@ attn_status attn_decode_ex(const float *q, const void *k_cache, const void *v_ca
                            size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * attn_decode_append -- append the new token's K/V row to the cache and attend,
+ * in the same launches (dotLLM #199 §1: each decode step first writes the new
+ * K/V row into the f16 cache, then attends over [0, nkv)).
+ *   k_new, v_new    f16 [n_seq][n_kv_head][head_dim], 16-byte aligned: the row
+ *                   of the token at position positions[s].
+ *   k_cache, v_cache  as in attn_decode_ex, but written: row positions[s] of
+ *                   sequence s receives k_new[s] / v_new[s] for every KV head.
+ * The result is that of attn_decode_ex on the cache after the write (the new
+ * row is attended from the new values, never from the cache's old contents).
+ * A positions[s] outside [0, cap - 1] writes nothing for that sequence and is
+ * clamped and flagged as in attn_decode_ex. Other arguments as attn_decode_ex.
+ */
+attn_status attn_decode_append(const float *q, const void *k_new, const void *v_new,
+                               void *k_cache, void *v_cache, const int32_t *positions, float *out,
+                               int n_seq, int n_head, int n_kv_head, int head_dim, float scale,
+                               int64_t cap, int n_splits, int split_len, int variant,
+                               void *workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/*
  * attn_decode_partial / attn_decode_combine -- the two stages of attn_decode_ex
  * as separate calls (same arguments, same validation), for callers that time
  * the stages apart or merge partials produced elsewhere before combining.
