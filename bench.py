@@ -53,6 +53,7 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
     ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 simt, 2 tensor core")
     ap.add_argument("--splits", type=int, default=0, help="0 = library heuristic")
+    ap.add_argument("--kv-dtype", choices=["f16", "bf16"], default="f16")
     ap.add_argument("--append", action="store_true",
                     help="time attn_decode_append (write the new K/V row, then attend)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -186,7 +187,7 @@ class ClockSampler:
 
 # ------------------------------------------------------------ CPU oracle leg
 
-def oracle_sample(layers_host, w, budget_s: float, max_units=None):
+def oracle_sample(layers_host, w, budget_s: float, max_units=None, kv_dtype="f16"):
     """Run the oracle on all host cores over (layer, KV head group) units of the
     workload -- every query head of one KV head against that head's rows -- until
     budget_s (or max_units); return (GB/s of K+V, units, seconds, threads, what)."""
@@ -203,7 +204,7 @@ def oracle_sample(layers_host, w, budget_s: float, max_units=None):
         kg = np.ascontiguousarray(lay["k"][:, :, hk:hk + 1])
         vg = np.ascontiguousarray(lay["v"][:, :, hk:hk + 1])
         oracle.attn_decode(qg, kg, vg, lay["positions"], G, 1, w.head_dim, w.cap, w.scale,
-                           n_threads=threads)
+                           n_threads=threads, kv_dtype=kv_dtype)
         nbytes += sum(min(max(int(p) + 1, 0), w.cap) for p in lay["positions"]) * w.head_dim * 4
         done += 1
         el = time.perf_counter() - t0
@@ -218,9 +219,16 @@ def oracle_sample(layers_host, w, budget_s: float, max_units=None):
 
 # ------------------------------------------------------------------ our arm
 
-def make_host_layers(w, layers):
+def make_host_layers(w, layers, kv_dtype="f16"):
     from decode_attention_gqa_gb300 import synthetic as syn
-    return [syn.make_layer(w, layer=l) for l in range(layers)]
+    return [syn.make_layer(w, layer=l, kv_dtype=kv_dtype) for l in range(layers)]
+
+
+def _t(a):
+    """numpy -> torch CPU tensor; bfloat16 bit patterns (uint16) travel as int16."""
+    import numpy as np
+    import torch
+    return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
 
 
 def workload_for(args):
@@ -265,17 +273,19 @@ def run_ours(args, rank, world, local):
     W, K = args.warmup, args.steps
     n_seq = w.n_seq
     advance = n_seq == 1                 # single sequence: nkv grows by one per step
-    host = make_host_layers(w, L)
+    host = make_host_layers(w, L, args.kv_dtype)
     dev = torch.device("cuda", local)
     s = torch.cuda.Stream(device=dev)
+    variant = args.variant | (pkg.ATTN_KV_BF16 if args.kv_dtype == "bf16" else 0)
 
     q = [torch.from_numpy(h["q"]).to(dev) for h in host]
-    kc = [torch.from_numpy(h["k"]).to(dev) for h in host]
-    vc = [torch.from_numpy(h["v"]).to(dev) for h in host]
+    kc = [_t(h["k"]).to(dev) for h in host]
+    vc = [_t(h["v"]).to(dev) for h in host]
     out = [torch.empty_like(x) for x in q]
     pos = torch.from_numpy(host[0]["positions"].copy()).to(dev)
-    kn = [torch.randn(n_seq, w.n_kv_head, w.head_dim, device=dev).half() for _ in range(L)]
-    vn = [torch.randn(n_seq, w.n_kv_head, w.head_dim, device=dev).half() for _ in range(L)]
+    kvt = torch.bfloat16 if args.kv_dtype == "bf16" else torch.float16
+    kn = [torch.randn(n_seq, w.n_kv_head, w.head_dim, device=dev).to(kvt) for _ in range(L)]
+    vn = [torch.randn(n_seq, w.n_kv_head, w.head_dim, device=dev).to(kvt) for _ in range(L)]
     torch.cuda.synchronize()
 
     def kv_bytes_for(nkvs):
@@ -301,17 +311,17 @@ def run_ours(args, rank, world, local):
                 elif stage == "partial":
                     pkg.attn_decode_partial(q[l], kc[l], vc[l], pos, n_seq, w.n_head, w.n_kv_head,
                                             w.head_dim, w.scale, w.cap, self.P, self.blk,
-                                            args.variant, self.ws, self.ws_bytes, stream=stream)
+                                            variant, self.ws, self.ws_bytes, stream=stream)
                 elif args.append:
                     pkg.attn_decode_append(q[l], kn[l], vn[l], kc[l], vc[l], pos, out[l], n_seq,
                                            w.n_head, w.n_kv_head, w.head_dim, w.scale, w.cap,
                                            n_splits=self.P, split_len=self.blk,
-                                           variant=args.variant, workspace=self.ws,
+                                           variant=variant, workspace=self.ws,
                                            workspace_bytes=self.ws_bytes, stream=stream)
                 else:
                     pkg.attn_decode_ex(q[l], kc[l], vc[l], pos, out[l], n_seq, w.n_head,
                                        w.n_kv_head, w.head_dim, w.scale, w.cap, n_splits=self.P,
-                                       split_len=self.blk, variant=args.variant,
+                                       split_len=self.blk, variant=variant,
                                        workspace=self.ws, workspace_bytes=self.ws_bytes,
                                        stream=stream)
 
@@ -397,17 +407,18 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     lay0 = dict(host[0], positions=pos_now)
     if args.append:                      # the cache now holds appended rows: compare with it
-        lay0["k"] = kc[0].cpu().numpy()
-        lay0["v"] = vc[0].cpu().numpy()
+        lay0["k"] = kc[0].cpu().view(torch.int16).numpy().view(np.uint16)
+        lay0["v"] = vc[0].cpu().view(torch.int16).numpy().view(np.uint16)
     if n_seq == 1:
         ref = oracle.attn_decode(lay0["q"], lay0["k"], lay0["v"], lay0["positions"], w.n_head,
-                                 w.n_kv_head, w.head_dim, w.cap, w.scale, n_threads=8)
+                                 w.n_kv_head, w.head_dim, w.cap, w.scale, n_threads=8,
+                                 kv_dtype=args.kv_dtype)
         got = out[0].cpu().numpy().astype(np.float64)
     else:
         sidx = [0, n_seq // 2, n_seq - 1]
         ref = np.stack([oracle.attn_decode_one(lay0["q"], lay0["k"], lay0["v"], lay0["positions"],
                                                w.n_head, w.n_kv_head, w.head_dim, w.cap, w.scale,
-                                               si, 0) for si in sidx])
+                                               si, 0, kv_dtype=args.kv_dtype) for si in sidx])
         got = out[0].cpu().numpy().astype(np.float64)[sidx, 0]
     parity_ok = bool(np.all(np.abs(got - ref) <= 1e-4 + 1e-3 * np.abs(ref)))
 
@@ -449,8 +460,8 @@ def run_ours(args, rank, world, local):
     e2e = None
     if not args.no_e2e:
         hq = [torch.from_numpy(h["q"]).pin_memory() for h in host]
-        hk = [torch.from_numpy(h["k"]).pin_memory() for h in host]
-        hv = [torch.from_numpy(h["v"]).pin_memory() for h in host]
+        hk = [_t(h["k"]).pin_memory() for h in host]
+        hv = [_t(h["v"]).pin_memory() for h in host]
         hpos_np = host[0]["positions"].copy()
         if advance:
             hpos_np[:] = ctx_end - 2                    # the graph adds 1
@@ -487,7 +498,8 @@ def run_ours(args, rank, world, local):
     # ---- CPU oracle baseline (rank 0 only, N == 1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        rate, done, el, threads, what = oracle_sample(host, w, budget_s=10.0)
+        rate, done, el, threads, what = oracle_sample(host, w, budget_s=10.0,
+                                                      kv_dtype=args.kv_dtype)
         cpu = {"value": round(rate, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": "%s of the %s workload (%.1f s)" % (what, w.name, el)}
 
@@ -501,7 +513,7 @@ def run_ours(args, rank, world, local):
             "config": {"workload": describe(w, L), "name": w.name, "ctx": ctx_end, "cap": w.cap,
                        "n_seq": n_seq, "n_head": w.n_head, "n_kv_head": w.n_kv_head,
                        "head_dim": w.head_dim, "layers": L, "n_splits": P0, "split_len": blk0,
-                       "variant": args.variant, "kv_dtype": "f16", "append": args.append,
+                       "variant": args.variant, "kv_dtype": args.kv_dtype, "append": args.append,
                        "l2": "inputs larger than L2 (%d MB of K+V per step)"
                              % (kv_bytes_for([ctx_end] if advance else w.ctx) * L // 2 ** 20),
                        "parallelism": "replicas" if world > 1 else "single"},

@@ -18,8 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn_decode.so")
 
-SOURCES = ["attn_api.cu", "attn_noalloc.cu", "attn_kernels_hd8.cu", "attn_kernels_hd64.cu",
-           "attn_kernels_hd128.cu", "attn_kernels_hd256.cu"]
+SOURCES = ["attn_api.cu", "attn_noalloc.cu"] + [
+    "attn_kernels_hd%d_%s.cu" % (hd, t) for hd in (8, 64, 128, 256) for t in ("f16", "bf16")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -59,7 +59,7 @@ def build(force: bool = False) -> str:
     if not force and not _stale():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+    with cf.ThreadPoolExecutor(max_workers=min(len(SOURCES), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(_compile, SOURCES))
     tmp = LIB + ".tmp%d" % os.getpid()
     cmd = [_nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs]

@@ -128,6 +128,8 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
                         const void *k_new = nullptr, const void *v_new = nullptr)
 {
     // ---- synchronous argument checks, nothing launched yet ----
+    const int kv_dtype = (variant & ATTN_KV_BF16) ? attn::kKvBf16 : attn::kKvF16;
+    variant &= ~ATTN_KV_BF16;
     if (n_seq < 0 || n_head <= 0 || n_kv_head <= 0 || head_dim <= 0) return ATTN_ERR_INVALID_ARG;
     if (n_head % n_kv_head != 0) return ATTN_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
@@ -191,8 +193,8 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
 
     attn::LaunchRequest r{};
     r.pa.q = q;
-    r.pa.k = static_cast<const __half *>(k_cache);
-    r.pa.v = static_cast<const __half *>(v_cache);
+    r.pa.k = static_cast<const uint16_t *>(k_cache);
+    r.pa.v = static_cast<const uint16_t *>(v_cache);
     r.pa.positions = positions;
     const size_t o_bytes = align256((size_t)n_seq * n_head * P * head_dim * sizeof(float));
     r.pa.ws_o = static_cast<float *>(workspace);
@@ -205,10 +207,10 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     r.pa.cap = cap;
     r.pa.qscale = (float)((double)scale * 1.4426950408889634);
     if (k_new) {
-        r.pa.k_new = static_cast<const __half *>(k_new);
-        r.pa.v_new = static_cast<const __half *>(v_new);
-        r.pa.k_w = static_cast<__half *>(const_cast<void *>(k_cache));
-        r.pa.v_w = static_cast<__half *>(const_cast<void *>(v_cache));
+        r.pa.k_new = static_cast<const uint16_t *>(k_new);
+        r.pa.v_new = static_cast<const uint16_t *>(v_new);
+        r.pa.k_w = static_cast<uint16_t *>(const_cast<void *>(k_cache));
+        r.pa.v_w = static_cast<uint16_t *>(const_cast<void *>(v_cache));
     }
     r.k_cache = k_cache;
     r.v_cache = v_cache;
@@ -218,15 +220,10 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     r.group = group;
     r.variant = v;
     r.stages = stages;
+    r.kv_dtype = kv_dtype;
     r.stream = stream;
 
-    switch (head_dim) {
-    case 8: e = attn::launch_hd8(r); break;
-    case 64: e = attn::launch_hd64(r); break;
-    case 128: e = attn::launch_hd128(r); break;
-    case 256: e = attn::launch_hd256(r); break;
-    default: return ATTN_ERR_UNSUPPORTED;
-    }
+    e = attn::launch_any(r);
     if (e != cudaSuccess) return cuda_fail(e);
     return ATTN_OK;
 }
@@ -239,7 +236,7 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
 namespace attn {
 
 cudaError_t encode_kv_map(CUtensorMap *map, const void *base, int64_t rows, int n_kv_head,
-                          int head_dim, int box_x, int box_rows)
+                          int head_dim, int box_x, int box_rows, int kv_dtype)
 {
     {
         std::lock_guard<std::mutex> lock(g_mu);
@@ -258,7 +255,9 @@ cudaError_t encode_kv_map(CUtensorMap *map, const void *base, int64_t rows, int 
     const cuuint32_t box[3] = {(cuuint32_t)box_x, 1u, (cuuint32_t)box_rows};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     const CUtensorMapSwizzle sw = (box_x * 2 == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
-    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims,
+    const CUtensorMapDataType dt = kv_dtype == kKvBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUresult r = g_encode(map, dt, 3, const_cast<void *>(base), dims,
                                 strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -378,14 +377,7 @@ attn_status attn_decode_combine(const void *workspace, size_t workspace_bytes, f
     r.variant = attn::kVariantSimt;
     r.stages = attn::kStageCombine;
     r.stream = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    switch (head_dim) {
-    case 8: e = attn::launch_hd8(r); break;
-    case 64: e = attn::launch_hd64(r); break;
-    case 128: e = attn::launch_hd128(r); break;
-    case 256: e = attn::launch_hd256(r); break;
-    default: return ATTN_ERR_UNSUPPORTED;
-    }
+    const cudaError_t e = attn::launch_any(r);
     if (e != cudaSuccess) return cuda_fail(e);
     return ATTN_OK;
 }

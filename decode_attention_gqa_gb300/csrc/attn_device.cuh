@@ -6,8 +6,11 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 namespace attn {
 
@@ -25,8 +28,8 @@ constexpr int kSplitGranule = 16;
 
 struct PartialArgs {
     const float *q;           // [n_seq][n_head][HD] f32
-    const __half *k;          // [n_seq][cap][n_kv_head][HD] f16 (tail tiles are read directly)
-    const __half *v;
+    const uint16_t *k;        // [n_seq][cap][n_kv_head][HD] 16-bit elements (tail tiles read directly)
+    const uint16_t *v;
     const int32_t *positions; // [n_seq]
     float *ws_o;              // [n_seq][n_head][P][HD]   unnormalised partial accumulators
     float2 *ws_ml;            // [n_seq][n_head][P]       (mx, S), mx in log2 units
@@ -37,12 +40,12 @@ struct PartialArgs {
     int split_len;            // 0 = by count
     int64_t cap;              // cache rows per sequence
     float qscale;             // scale * log2(e): scores come out in log2 units
-    // Fused append (optional): the new token's rows [n_seq][n_kv_head][HD] f16,
+    // Fused append (optional): the new token's rows [n_seq][n_kv_head][HD],
     // written into cache row positions[s] and attended in the same launch.
-    const __half *k_new;      // null: no append
-    const __half *v_new;
-    __half *k_w;              // the caches again, writable, when appending
-    __half *v_w;
+    const uint16_t *k_new;    // null: no append
+    const uint16_t *v_new;
+    uint16_t *k_w;            // the caches again, writable, when appending
+    uint16_t *v_w;
 };
 
 struct CombineArgs {
@@ -209,13 +212,46 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void *p)
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_u32(p)));
 }
 
+// D = A x B + D, 16x8x16, A and B of the cache element type KV (both operands
+// always the same type), f32 accumulation.
+template <typename KV>
 __device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
                                           uint32_t b1)
 {
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-                 "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    if constexpr (std::is_same<KV, __half>::value) {
+        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+                     "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                     : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                     : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    } else {
+        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                     "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                     : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                     : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+}
+
+// Two cache elements (one 32-bit word) to f32, and two f32 to a packed pair of
+// cache elements (round to nearest even), for KV = __half or __nv_bfloat16.
+template <typename KV>
+__device__ __forceinline__ float2 kv2_to_float2(uint32_t w)
+{
+    if constexpr (std::is_same<KV, __half>::value)
+        return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+    else
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
+}
+
+template <typename KV>
+__device__ __forceinline__ uint32_t float2_to_kv2(float lo, float hi)
+{
+    if constexpr (std::is_same<KV, __half>::value) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    } else {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -242,13 +278,14 @@ __device__ __forceinline__ float warp_sum(float x)
     return x;
 }
 
-// Eight f16 (one 16-byte unit) to f32.
+// Eight cache elements (one 16-byte unit) to f32.
+template <typename KV>
 __device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8])
 {
-    const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float2 t = __half22float2(h[i]);
+        const float2 t = kv2_to_float2<KV>(w[i]);
         f[2 * i] = t.x;
         f[2 * i + 1] = t.y;
     }

@@ -1,0 +1,7 @@
+// Kernels for head_dim 128 over a f16 KV cache (partial variants for group sizes 1..8, combine).
+#include "attn_kernels_impl.cuh"
+
+namespace attn {
+cudaError_t launch_hd128_f16(const LaunchRequest &r) { return launch_for_hd<128, __half>(r); }
+KernelInfo kernel_info_hd128(int group, int variant) { return kernel_info_for_hd<128>(group, variant); }
+} // namespace attn

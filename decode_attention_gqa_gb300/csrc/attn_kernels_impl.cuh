@@ -1,6 +1,6 @@
-// attn_kernels_impl.cuh -- per-head_dim kernel instantiation and launch.
-// Each attn_kernels_hd<N>.cu includes this once with its own head_dim, so the
-// instantiations compile in parallel.
+// attn_kernels_impl.cuh -- kernel instantiation and launch per (head_dim,
+// cache element type). Each attn_kernels_hd<N>_<type>.cu includes this once
+// with its own pair, so the instantiations compile in parallel.
 #pragma once
 
 #include "attn_combine.cuh"
@@ -24,10 +24,12 @@ template <int HD> struct TcShape  { static constexpr int NWC = 4, S = 3, MINB = 
 template <> struct TcShape<64>    { static constexpr int NWC = 4, S = 4, MINB = 2; };
 template <> struct TcShape<256>   { static constexpr int NWC = 4, S = 3, MINB = 1; };
 
-template <int HD, int G>
-using SimtCfg = PartialCfg<HD, G, SimtWarp, SimtShape<HD>::NWC, SimtShape<HD>::S, SimtShape<HD>::MINB>;
-template <int HD, int G>
-using TcCfg = PartialCfg<HD, G, TcWarp, TcShape<HD>::NWC, TcShape<HD>::S, TcShape<HD>::MINB>;
+template <int HD, int G, typename KV>
+using SimtCfg = PartialCfg<HD, G, SimtWarp, SimtShape<HD>::NWC, SimtShape<HD>::S, SimtShape<HD>::MINB, KV>;
+template <int HD, int G, typename KV>
+using TcCfg = PartialCfg<HD, G, TcWarp, TcShape<HD>::NWC, TcShape<HD>::S, TcShape<HD>::MINB, KV>;
+
+template <typename KV> constexpr int kv_dtype_code() { return std::is_same<KV, __half>::value ? kKvF16 : kKvBf16; }
 
 // Resident blocks per SM for a configuration: 228 KB of shared memory per SM
 // with 1 KB reserved per block, 64 K registers, at most 32 blocks.
@@ -38,14 +40,15 @@ constexpr int blocks_per_sm()
     return by_smem < 1 ? 1 : (by_smem > 32 ? 32 : by_smem);
 }
 
-template <class Cfg, int HD, int G>
+template <class Cfg, int HD, int G, typename KV>
 cudaError_t launch_partial(const LaunchRequest &r)
 {
     alignas(64) CUtensorMap kmap, vmap;
     const int64_t rows = (int64_t)r.n_seq * r.pa.cap;
-    cudaError_t e = encode_kv_map(&kmap, r.k_cache, rows, r.pa.n_kv_head, HD, Cfg::BOX_X, Cfg::TILE);
+    const int dt = kv_dtype_code<KV>();
+    cudaError_t e = encode_kv_map(&kmap, r.k_cache, rows, r.pa.n_kv_head, HD, Cfg::BOX_X, Cfg::TILE, dt);
     if (e != cudaSuccess) return e;
-    e = encode_kv_map(&vmap, r.v_cache, rows, r.pa.n_kv_head, HD, Cfg::BOX_X, Cfg::TILE);
+    e = encode_kv_map(&vmap, r.v_cache, rows, r.pa.n_kv_head, HD, Cfg::BOX_X, Cfg::TILE, dt);
     if (e != cudaSuccess) return e;
     const void *fn = reinterpret_cast<const void *>(&attn_split_partial<Cfg, HD, G>);
     e = ensure_smem_attr(fn, (int)Cfg::SMEM_BYTES);
@@ -71,17 +74,17 @@ cudaError_t launch_combine(const LaunchRequest &r)
                       dim3(CombineCfg<HD>::THREADS), 0, r.stream, args);
 }
 
-template <int HD, int G>
+template <int HD, int G, typename KV>
 cudaError_t launch_group(const LaunchRequest &r)
 {
     cudaError_t e = cudaSuccess;
     if (r.stages & kStagePartial) {
         if constexpr (HD % 16 == 0) {
-            if (r.variant == kVariantTc) e = launch_partial<TcCfg<HD, G>, HD, G>(r);
-            else e = launch_partial<SimtCfg<HD, G>, HD, G>(r);
+            if (r.variant == kVariantTc) e = launch_partial<TcCfg<HD, G, KV>, HD, G, KV>(r);
+            else e = launch_partial<SimtCfg<HD, G, KV>, HD, G, KV>(r);
         } else {
             if (r.variant != kVariantSimt) return cudaErrorInvalidValue;
-            e = launch_partial<SimtCfg<HD, G>, HD, G>(r);
+            e = launch_partial<SimtCfg<HD, G, KV>, HD, G, KV>(r);
         }
         if (e != cudaSuccess) return e;
     }
@@ -89,18 +92,18 @@ cudaError_t launch_group(const LaunchRequest &r)
     return e;
 }
 
-template <int HD>
+template <int HD, typename KV>
 cudaError_t launch_for_hd(const LaunchRequest &r)
 {
     switch (r.group) {
-    case 1: return launch_group<HD, 1>(r);
-    case 2: return launch_group<HD, 2>(r);
-    case 3: return launch_group<HD, 3>(r);
-    case 4: return launch_group<HD, 4>(r);
-    case 5: return launch_group<HD, 5>(r);
-    case 6: return launch_group<HD, 6>(r);
-    case 7: return launch_group<HD, 7>(r);
-    case 8: return launch_group<HD, 8>(r);
+    case 1: return launch_group<HD, 1, KV>(r);
+    case 2: return launch_group<HD, 2, KV>(r);
+    case 3: return launch_group<HD, 3, KV>(r);
+    case 4: return launch_group<HD, 4, KV>(r);
+    case 5: return launch_group<HD, 5, KV>(r);
+    case 6: return launch_group<HD, 6, KV>(r);
+    case 7: return launch_group<HD, 7, KV>(r);
+    case 8: return launch_group<HD, 8, KV>(r);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -111,14 +114,14 @@ KernelInfo kernel_info_for_hd(int group, int variant)
     KernelInfo k{0, 0, 0, false};
     if (group < 1 || group > 8) return k;
     if (variant == kVariantSimt) {
-        using C = SimtCfg<HD, 8>;     // the largest group sets the shared-memory need
+        using C = SimtCfg<HD, 8, __half>;   // the largest group sets the shared-memory need
         k.tile_rows = C::TILE;
         k.granule = C::WR;
         k.blocks_per_sm = blocks_per_sm<C>();
         k.available = true;
     } else if (variant == kVariantTc) {
         if constexpr (HD % 16 == 0) {
-            using C = TcCfg<HD, 8>;
+            using C = TcCfg<HD, 8, __half>;
             k.tile_rows = C::TILE;
             k.granule = C::WR;
             k.blocks_per_sm = blocks_per_sm<C>();

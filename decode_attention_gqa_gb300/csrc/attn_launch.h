@@ -13,6 +13,8 @@ namespace attn {
 
 constexpr int kVariantSimt = 1;
 constexpr int kVariantTc = 2;
+constexpr int kKvF16 = 0;
+constexpr int kKvBf16 = 1;
 constexpr int kStagePartial = 1;
 constexpr int kStageCombine = 2;
 
@@ -26,6 +28,7 @@ struct LaunchRequest {
     int group;               // G = n_head / n_kv_head
     int variant;             // kVariantSimt / kVariantTc (resolved, never auto)
     int stages;              // kStagePartial | kStageCombine
+    int kv_dtype;            // kKvF16 / kKvBf16
     cudaStream_t stream;
 };
 
@@ -38,24 +41,43 @@ struct KernelInfo {
 };
 
 // Implemented in attn_api.cu.
-// Build a 3-D tensor map over a [rows][n_kv_head][head_dim] f16 cache with a
-// box of (box_x, 1, box_rows); 128-byte swizzle when box_x * 2 == 128.
+// Build a 3-D tensor map over a [rows][n_kv_head][head_dim] 16-bit cache
+// (kv_dtype kKvF16 / kKvBf16) with a box of (box_x, 1, box_rows); 128-byte
+// swizzle when box_x * 2 == 128.
 cudaError_t encode_kv_map(CUtensorMap *map, const void *base, int64_t rows, int n_kv_head,
-                          int head_dim, int box_x, int box_rows);
+                          int head_dim, int box_x, int box_rows, int kv_dtype);
 // Opt a kernel into more than 48 KB of dynamic shared memory (once per device).
 cudaError_t ensure_smem_attr(const void *func, int bytes);
 // Launch with the programmatic-stream-serialisation attribute set.
 cudaError_t launch_pdl(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                        void **args);
 
-// Implemented in attn_kernels_hd{8,64,128,256}.cu.
+// Implemented in attn_kernels_hd{8,64,128,256}_{f16,bf16}.cu (kernel_info in
+// the f16 units: the shapes do not depend on the element type).
 KernelInfo kernel_info_hd8(int group, int variant);
 KernelInfo kernel_info_hd64(int group, int variant);
 KernelInfo kernel_info_hd128(int group, int variant);
 KernelInfo kernel_info_hd256(int group, int variant);
-cudaError_t launch_hd8(const LaunchRequest &r);
-cudaError_t launch_hd64(const LaunchRequest &r);
-cudaError_t launch_hd128(const LaunchRequest &r);
-cudaError_t launch_hd256(const LaunchRequest &r);
+cudaError_t launch_hd8_f16(const LaunchRequest &r);
+cudaError_t launch_hd64_f16(const LaunchRequest &r);
+cudaError_t launch_hd128_f16(const LaunchRequest &r);
+cudaError_t launch_hd256_f16(const LaunchRequest &r);
+cudaError_t launch_hd8_bf16(const LaunchRequest &r);
+cudaError_t launch_hd64_bf16(const LaunchRequest &r);
+cudaError_t launch_hd128_bf16(const LaunchRequest &r);
+cudaError_t launch_hd256_bf16(const LaunchRequest &r);
+
+// Dispatch on (head_dim, kv_dtype).
+inline cudaError_t launch_any(const LaunchRequest &r)
+{
+    const bool bf = r.kv_dtype == kKvBf16;
+    switch (r.head_dim) {
+    case 8: return bf ? launch_hd8_bf16(r) : launch_hd8_f16(r);
+    case 64: return bf ? launch_hd64_bf16(r) : launch_hd64_f16(r);
+    case 128: return bf ? launch_hd128_bf16(r) : launch_hd128_f16(r);
+    case 256: return bf ? launch_hd256_bf16(r) : launch_hd256_f16(r);
+    default: return cudaErrorInvalidValue;
+    }
+}
 
 } // namespace attn

@@ -30,12 +30,13 @@
 
 namespace attn {
 
-template <int HD, int G, template <int, int, int> class W, int NWC_, int S_, int MINB_>
+template <int HD, int G, template <int, int, int, typename> class W, int NWC_, int S_, int MINB_,
+          typename KV>
 struct PartialCfg {
     static constexpr int NWC = NWC_;                 // compute warps
     static constexpr int S = S_;                     // pipeline stages
     static constexpr int MIN_BLOCKS = MINB_;         // resident blocks per SM the registers must allow
-    using Warp = W<HD, G, NWC>;
+    using Warp = W<HD, G, NWC, KV>;
     static constexpr int WR = Warp::WR;
     static constexpr int TILE = NWC * WR;            // rows per stage
     static constexpr int THREADS = (NWC + 1) * 32;
@@ -161,8 +162,8 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
                 const int vs0 = TILE - nrows;
                 const int zs = vs0 / WR * WR;
                 const size_t rstride = (size_t)a.n_kv_head * HD;               // elements per row
-                const __half *kg = a.k + (size_t)(seq_row0 + first) * rstride + (size_t)hk * HD;
-                const __half *vg = a.v + (size_t)(seq_row0 + first) * rstride + (size_t)hk * HD;
+                const uint16_t *kg = a.k + (size_t)(seq_row0 + first) * rstride + (size_t)hk * HD;
+                const uint16_t *vg = a.v + (size_t)(seq_row0 + first) * rstride + (size_t)hk * HD;
                 for (int i = lane; i < (TILE - zs) * NU; i += 32) {
                     const int r = zs + i / NU, U = i % NU;
                     const uint32_t so = tile_unit_offset<HD, TILE>(r, U);

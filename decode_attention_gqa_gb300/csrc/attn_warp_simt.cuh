@@ -13,7 +13,7 @@
 
 namespace attn {
 
-template <int HD, int G, int NWC>
+template <int HD, int G, int NWC, typename KV>
 struct SimtWarp {
     static constexpr int WR = 32;                          // rows per warp slice
     static constexpr int NU = HD / 8;                      // 16-byte units per row
@@ -81,7 +81,7 @@ struct SimtWarp {
         for (int U = 0; U < NU; ++U) {
             const uint4 raw = *reinterpret_cast<const uint4 *>(ks + tile_unit_offset<HD, TILE>(r, U));
             float kf[8];
-            unpack8(raw, kf);
+            unpack8<KV>(raw, kf);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 const float4 qa = *reinterpret_cast<const float4 *>(qs + g * HD + U * 8);
@@ -123,14 +123,14 @@ struct SimtWarp {
             const uint8_t *vp = vs + tile_unit_offset<HD, TILE>(r0 + j, d0 >> 3) + vbyte;
             float v[DPL];
             if constexpr (DPL == 8) {
-                unpack8(*reinterpret_cast<const uint4 *>(vp), v);
+                unpack8<KV>(*reinterpret_cast<const uint4 *>(vp), v);
             } else if constexpr (DPL == 4) {
                 const uint2 raw = *reinterpret_cast<const uint2 *>(vp);
-                const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
-                const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
+                const float2 a = kv2_to_float2<KV>(raw.x);
+                const float2 b = kv2_to_float2<KV>(raw.y);
                 v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
             } else {
-                const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(vp));
+                const float2 a = kv2_to_float2<KV>(*reinterpret_cast<const uint32_t *>(vp));
                 v[0] = a.x; v[1] = a.y;
             }
             float p[GP];

@@ -4,10 +4,11 @@
 //
 // The dotLLM #199 design (§2) pads the single query row to a 16-row MMA tile
 // and wastes 15 rows. Here the 16 rows carry the whole query-head group twice:
-// rows 0..7 hold hi = f16(x) and rows 8..15 hold lo = f16(x - hi) for the G <= 8
-// heads, so q·k = hi·k + lo·k keeps about 22 significant bits of q (f16
-// products are exact in the f32 accumulator) instead of the 11 bits of a plain
-// f16 cast (the precision risk of "Option B", #199 §0). The softmax weights p
+// rows 0..7 hold hi = T(x) and rows 8..15 hold lo = T(x - hi) for the G <= 8
+// heads, T the cache's element type, so q·k = hi·k + lo·k keeps about 22
+// significant bits of q for f16 (16 for bf16; the products are exact in the
+// f32 accumulator) instead of the 11 (8) bits of a plain cast (the precision
+// risk of "Option B", #199 §0). The softmax weights p
 // get the same hi/lo treatment for p·V, and the C fragment of q·Kᵀ is exactly
 // the A fragment layout of p·V, so no data moves between lanes.
 //
@@ -28,7 +29,7 @@
 
 namespace attn {
 
-template <int HD, int G, int NWC>
+template <int HD, int G, int NWC, typename KV>
 struct TcWarp {
     static_assert(HD % 16 == 0, "tensor-core path needs head_dim % 16 == 0");
     static constexpr int WR = 16;                     // rows per warp slice
@@ -86,12 +87,13 @@ struct TcWarp {
                 const int d = lane + 32 * i;
                 if (d < HD) {
                     const float v = x[it][i] * sc;
-                    const __half hi = __float2half_rn(v);
-                    const __half lo = __float2half_rn(v - __half2float(hi));
+                    const uint32_t hw = float2_to_kv2<KV>(v, 0.f);          // hi in the low half
+                    const float hf = kv2_to_float2<KV>(hw).x;
+                    const uint32_t lw = float2_to_kv2<KV>(v - hf, 0.f);
                     const uint32_t off = tile_unit_offset<HD, 16>(g, d >> 3) + (d & 7) * 2;
                     const uint32_t offl = tile_unit_offset<HD, 16>(8 + g, d >> 3) + (d & 7) * 2;
-                    *reinterpret_cast<__half *>(extra + off) = hi;
-                    *reinterpret_cast<__half *>(extra + offl) = lo;
+                    *reinterpret_cast<uint16_t *>(extra + off) = (uint16_t)(hw & 0xffffu);
+                    *reinterpret_cast<uint16_t *>(extra + offl) = (uint16_t)(lw & 0xffffu);
                 }
             }
         }
@@ -147,8 +149,8 @@ struct TcWarp {
             }
             uint32_t b[4];        // (rows 0-7, d lo8), (rows 0-7, d hi8), (rows 8-15, lo8), (8-15, hi8)
             ldsm_x4(b, ks + tile_unit_offset<HD, TILE>(krow, 2 * kk + (i8 & 1)));
-            mma_16816(c[0], a, b[0], b[1]);
-            mma_16816(c[1], a, b[2], b[3]);
+            mma_16816<KV>(c[0], a, b[0], b[1]);
+            mma_16816<KV>(c[1], a, b[2], b[3]);
         }
         const int t = lane & 3;
         float s[4];
@@ -183,15 +185,11 @@ struct TcWarp {
         // p as the A fragment of p·V: hi parts in rows 0-7, lo parts in rows 8-15
         uint32_t pa[4];
         {
-            const __half2 h01 = __floats2half2_rn(p[0], p[1]);
-            const __half2 h23 = __floats2half2_rn(p[2], p[3]);
-            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-            const __half2 l01 = __floats2half2_rn(p[0] - f01.x, p[1] - f01.y);
-            const __half2 l23 = __floats2half2_rn(p[2] - f23.x, p[3] - f23.y);
-            pa[0] = *reinterpret_cast<const uint32_t *>(&h01);
-            pa[1] = *reinterpret_cast<const uint32_t *>(&l01);
-            pa[2] = *reinterpret_cast<const uint32_t *>(&h23);
-            pa[3] = *reinterpret_cast<const uint32_t *>(&l23);
+            pa[0] = float2_to_kv2<KV>(p[0], p[1]);
+            pa[2] = float2_to_kv2<KV>(p[2], p[3]);
+            const float2 f01 = kv2_to_float2<KV>(pa[0]), f23 = kv2_to_float2<KV>(pa[2]);
+            pa[1] = float2_to_kv2<KV>(p[0] - f01.x, p[1] - f01.y);
+            pa[3] = float2_to_kv2<KV>(p[2] - f23.x, p[3] - f23.y);
         }
         // a5: O += P · V over the slice's 16 rows
         const int vrow = r0 + (i8 & 1) * 8 + (lane & 7);
@@ -199,8 +197,8 @@ struct TcWarp {
         for (int n = 0; n < NTD; n += 2) {
             uint32_t b[4];        // (rows 0-7, dims n), (rows 8-15, dims n), (0-7, n+1), (8-15, n+1)
             ldsm_x4_trans(b, vs + tile_unit_offset<HD, TILE>(vrow, n + (i8 >> 1)));
-            mma_16816(o[n], pa, b[0], b[1]);
-            mma_16816(o[n + 1], pa, b[2], b[3]);
+            mma_16816<KV>(o[n], pa, b[0], b[1]);
+            mma_16816<KV>(o[n + 1], pa, b[2], b[3]);
         }
     }
 

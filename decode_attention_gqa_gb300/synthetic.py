@@ -6,7 +6,8 @@ library (after a copy to the device) and the CPU oracle.
 
 Recipe (every workload): q ~ N(0, 1) drawn in float32; K and V ~ N(0, 1)
 drawn in float32, multiplied by ``k_scale`` (K only) and rounded to IEEE
-binary16 with round-to-nearest-even (numpy's float32 -> float16 cast).
+binary16 with round-to-nearest-even (numpy's float32 -> float16 cast), or to
+bfloat16 (round-to-nearest-even on the bit pattern) for a bfloat16 cache.
 Each (workload, layer, sequence) pair draws from its own PCG64 stream seeded
 with ``[seed, layer, sequence]``, so any slice can be regenerated alone.
 Cache rows at or past a sequence's context length are never read by the
@@ -98,29 +99,48 @@ def make_q(w: Workload, layer: int = 0) -> np.ndarray:
     return out
 
 
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bfloat16 bit patterns (uint16), round to nearest even."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    rounded = u + (np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1)))
+    out = (rounded >> np.uint32(16)).astype(np.uint16)
+    nan = np.isnan(x)
+    if nan.any():
+        out[nan] = np.uint16(0x7FC0)
+    return out
+
+
+def _cast(x: np.ndarray, kv_dtype: str) -> np.ndarray:
+    return x.astype(np.float16) if kv_dtype == "f16" else to_bf16_bits(x)
+
+
 def fill_kv_seq(w: Workload, layer: int, s: int, k_out: np.ndarray, v_out: np.ndarray,
-                fill: float = 0.0) -> None:
-    """Fill one sequence's cache rows, k_out/v_out: float16 [cap, n_kv_head, head_dim]."""
+                fill: float = 0.0, kv_dtype: str = "f16") -> None:
+    """Fill one sequence's cache rows, k_out/v_out [cap, n_kv_head, head_dim]:
+    float16, or bfloat16 bit patterns (uint16) for kv_dtype "bf16"."""
     n = min(max(w.ctx[s], 0), w.cap)
     shape = (n, w.n_kv_head, w.head_dim)
     k = _rng(w.seed, layer, s, 1).standard_normal(shape, dtype=np.float32)
     if w.k_scale != 1.0:
         k *= np.float32(w.k_scale)
-    k_out[:n] = k.astype(np.float16)
+    k_out[:n] = _cast(k, kv_dtype)
     del k
-    v_out[:n] = _rng(w.seed, layer, s, 2).standard_normal(shape, dtype=np.float32).astype(np.float16)
+    v_out[:n] = _cast(_rng(w.seed, layer, s, 2).standard_normal(shape, dtype=np.float32), kv_dtype)
     if n < w.cap:
-        k_out[n:] = fill
-        v_out[n:] = fill
+        f = _cast(np.full(1, fill, np.float32), kv_dtype)[0]
+        k_out[n:] = f
+        v_out[n:] = f
 
 
-def make_kv(w: Workload, layer: int = 0, fill: float = 0.0):
-    """K, V: float16 [n_seq, cap, n_kv_head, head_dim]."""
+def make_kv(w: Workload, layer: int = 0, fill: float = 0.0, kv_dtype: str = "f16"):
+    """K, V [n_seq, cap, n_kv_head, head_dim]: float16, or bfloat16 bit
+    patterns (uint16) for kv_dtype "bf16"."""
     shape = (w.n_seq, w.cap, w.n_kv_head, w.head_dim)
-    k = np.empty(shape, dtype=np.float16)
-    v = np.empty(shape, dtype=np.float16)
+    dt = np.float16 if kv_dtype == "f16" else np.uint16
+    k = np.empty(shape, dtype=dt)
+    v = np.empty(shape, dtype=dt)
     for s in range(w.n_seq):
-        fill_kv_seq(w, layer, s, k[s], v[s], fill)
+        fill_kv_seq(w, layer, s, k[s], v[s], fill, kv_dtype)
     return k, v
 
 
@@ -129,6 +149,6 @@ def make_positions(w: Workload) -> np.ndarray:
     return np.asarray([c - 1 for c in w.ctx], dtype=np.int32)
 
 
-def make_layer(w: Workload, layer: int = 0, fill: float = 0.0) -> dict:
-    k, v = make_kv(w, layer, fill)
+def make_layer(w: Workload, layer: int = 0, fill: float = 0.0, kv_dtype: str = "f16") -> dict:
+    k, v = make_kv(w, layer, fill, kv_dtype)
     return {"q": make_q(w, layer), "k": k, "v": v, "positions": make_positions(w)}

@@ -26,8 +26,8 @@
  *    in attn_read_device_error().
  *  - Layouts are dense row-major:
  *        q, out      float  [n_seq][n_head][head_dim]
- *        k_cache,    f16    [n_seq][cap][n_kv_head][head_dim]   (IEEE binary16)
- *        v_cache     f16    [n_seq][cap][n_kv_head][head_dim]
+ *        k_cache,    f16    [n_seq][cap][n_kv_head][head_dim]   (IEEE binary16, or
+ *        v_cache     f16    [n_seq][cap][n_kv_head][head_dim]    bfloat16: ATTN_KV_BF16)
  *        positions   int32  [n_seq]      (device memory; nkv_s = positions[s] + 1)
  *    so row j of sequence s, KV head hk starts at element
  *    ((s * cap + j) * n_kv_head + hk) * head_dim.
@@ -70,9 +70,15 @@ typedef enum {
 /* Kernel variants for attn_decode_ex. */
 #define ATTN_VARIANT_AUTO 0   /* tensor cores where compiled (head_dim % 16 == 0), else CUDA cores */
 #define ATTN_VARIANT_SIMT 1   /* CUDA-core f32 partial kernel (every head_dim) */
-#define ATTN_VARIANT_TC   2   /* tensor-core partial kernel: 16x8x16 f16 MMA, f32 accumulate, q and
-                                 p each carried as an f16 hi + lo pair (about 22 significant bits);
-                                 head_dim 64, 128, 256 only (ATTN_ERR_UNSUPPORTED otherwise) */
+#define ATTN_VARIANT_TC   2   /* tensor-core partial kernel: 16x8x16 MMA, f32 accumulate, q and
+                                 p each carried as a hi + lo pair of the cache's element type (about
+                                 22 significant bits for f16, 16 for bf16); head_dim 64, 128, 256
+                                 only (ATTN_ERR_UNSUPPORTED otherwise) */
+
+/* Cache element type, OR'd into the variant argument: without it K and V are
+   IEEE binary16 (f16); with it they are bfloat16 (1 sign, 8 exponent, 7
+   fraction bits). k_new / v_new of attn_decode_append use the same type. */
+#define ATTN_KV_BF16 0x10
 
 /*
  * attn_decode -- one layer call, single sequence, library-owned workspace.

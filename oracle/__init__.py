@@ -48,11 +48,17 @@ def _bind(lib):
     lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
     lib.oracle_f16_to_double_array.restype = None
     lib.oracle_f16_to_double_array.argtypes = [p, p, i64]
+    lib.oracle_bf16_to_double_array.restype = None
+    lib.oracle_bf16_to_double_array.argtypes = [p, p, i64]
     common = [p, p, p, p, p, i32, i32, i32, i32, i64, dbl]
     lib.oracle_attn_decode.restype = i32
     lib.oracle_attn_decode.argtypes = common + [i32]
     lib.oracle_attn_decode_one.restype = i32
     lib.oracle_attn_decode_one.argtypes = common + [i32, i32]
+    lib.oracle_attn_decode_kv.restype = i32
+    lib.oracle_attn_decode_kv.argtypes = common + [i32, i32]
+    lib.oracle_attn_decode_one_kv.restype = i32
+    lib.oracle_attn_decode_one_kv.argtypes = common + [i32, i32, i32]
     lib.oracle_attn_decode_split.restype = i32
     lib.oracle_attn_decode_split.argtypes = common + [i32, i64]
     return lib
@@ -84,6 +90,18 @@ def _prep(q, k, v, positions):
     return q, k, v, positions
 
 
+KV_DTYPES = {"f16": 0, "bf16": 1}
+
+
+def bf16_to_double(bits, lib=None) -> np.ndarray:
+    """Decode an array of bfloat16 bit patterns (uint16) to float64."""
+    lib = lib or load_library()
+    b = np.ascontiguousarray(bits).view(np.uint16)
+    out = np.empty(b.shape, dtype=np.float64)
+    lib.oracle_bf16_to_double_array(_ptr(b), _ptr(out), b.size)
+    return out
+
+
 def f16_to_double(bits, lib=None) -> np.ndarray:
     """Decode an array of binary16 bit patterns (uint16 or float16) to float64."""
     lib = lib or load_library()
@@ -94,34 +112,39 @@ def f16_to_double(bits, lib=None) -> np.ndarray:
 
 
 def attn_decode(q, k, v, positions, n_head, n_kv_head, head_dim, cap, scale,
-                n_threads=1, lib=None) -> np.ndarray:
+                n_threads=1, lib=None, kv_dtype="f16") -> np.ndarray:
     """Single-pass oracle over every (sequence, head).
 
-    q: f32 [n_seq, n_head, head_dim]; k, v: f16 (or uint16 bits)
-    [n_seq, cap, n_kv_head, head_dim]; positions: int32 [n_seq].
-    Returns float64 [n_seq, n_head, head_dim].
+    q: f32 [n_seq, n_head, head_dim]; k, v: f16, or 16-bit patterns of
+    `kv_dtype` ("f16" or "bf16"), [n_seq, cap, n_kv_head, head_dim];
+    positions: int32 [n_seq]. Returns float64 [n_seq, n_head, head_dim].
     """
     lib = lib or load_library()
     q, k, v, positions = _prep(q, k, v, positions)
     n_seq = positions.shape[0]
     out = np.zeros((n_seq, n_head, head_dim), dtype=np.float64)
-    rc = lib.oracle_attn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(positions), _ptr(out),
-                                n_seq, n_head, n_kv_head, head_dim, cap, float(scale),
-                                int(n_threads))
+    if kv_dtype == "f16":
+        rc = lib.oracle_attn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(positions), _ptr(out),
+                                    n_seq, n_head, n_kv_head, head_dim, cap, float(scale),
+                                    int(n_threads))
+    else:
+        rc = lib.oracle_attn_decode_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(positions), _ptr(out),
+                                       n_seq, n_head, n_kv_head, head_dim, cap, float(scale),
+                                       int(n_threads), KV_DTYPES[kv_dtype])
     if rc != 0:
         raise ValueError("oracle_attn_decode failed with status %d" % rc)
     return out
 
 
 def attn_decode_one(q, k, v, positions, n_head, n_kv_head, head_dim, cap, scale, s, h,
-                    lib=None) -> np.ndarray:
+                    lib=None, kv_dtype="f16") -> np.ndarray:
     """One output row o[s, h, :] (float64), for sampled checks on big workloads."""
     lib = lib or load_library()
     q, k, v, positions = _prep(q, k, v, positions)
     out = np.zeros(head_dim, dtype=np.float64)
-    rc = lib.oracle_attn_decode_one(_ptr(q), _ptr(k), _ptr(v), _ptr(positions), _ptr(out),
-                                    positions.shape[0], n_head, n_kv_head, head_dim, cap,
-                                    float(scale), int(s), int(h))
+    rc = lib.oracle_attn_decode_one_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(positions), _ptr(out),
+                                       positions.shape[0], n_head, n_kv_head, head_dim, cap,
+                                       float(scale), int(s), int(h), KV_DTYPES[kv_dtype])
     if rc != 0:
         raise ValueError("oracle_attn_decode_one failed with status %d" % rc)
     return out

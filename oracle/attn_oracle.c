@@ -22,8 +22,9 @@
  *     o[d] = (sum_j w_j * V[s][j][hk][d]) / (sum_j w_j)
  *     o    = 0 when n == 0  (the combine's "S > 0 ? acc/S : 0" rule, §3.2)
  *
- * Everything is evaluated in double: q (f32) and the f16 cache entries convert
- * exactly, each product q*k is exact, exp is libm's double exp.
+ * Everything is evaluated in double: q (f32) and the cache entries (binary16,
+ * or bfloat16 through the _kv entry points) convert exactly, each product q*k
+ * is exact, exp is libm's double exp.
  *
  * A second entry point restates the two-stage method of §2.1/§2.2 literally
  * (per-split online softmax, then the max-reweighted combine) so that tests
@@ -31,7 +32,7 @@
  *
  * Layouts (row-major, no padding):
  *   q, out      [n_seq][n_head][head_dim]              (f32 in, f64 out)
- *   k, v        [n_seq][cap][n_kv_head][head_dim]      (IEEE binary16 bits)
+ *   k, v        [n_seq][cap][n_kv_head][head_dim]      (binary16 or bfloat16 bits)
  *   positions   [n_seq]                                (int32)
  */
 #include <math.h>
@@ -59,10 +60,44 @@ double oracle_f16_to_double(uint16_t bits)
     return sign ? -mag : mag;
 }
 
+/* ---------------------------------------------------------------------------
+ * bfloat16 -> double, from the format's definition: 1 sign bit, 8 exponent
+ * bits (bias 127), 7 fraction bits. Exponent 0 holds zero and the subnormals
+ * (fraction * 2^-133); exponent 255 holds inf / NaN.
+ * ------------------------------------------------------------------------- */
+double oracle_bf16_to_double(uint16_t bits)
+{
+    const int sign = (bits >> 15) & 1;
+    const int expo = (bits >> 7) & 0xff;
+    const int frac = bits & 0x7f;
+    double mag;
+    if (expo == 0)
+        mag = ldexp((double)frac, -133);
+    else if (expo == 255)
+        mag = frac ? NAN : INFINITY;
+    else
+        mag = ldexp((double)(128 + frac), expo - 134);
+    return sign ? -mag : mag;
+}
+
+typedef double (*decode_fn)(uint16_t);
+
+/* kv_dtype: 0 = binary16, 1 = bfloat16. */
+static decode_fn decoder_for(int kv_dtype)
+{
+    return kv_dtype == 1 ? oracle_bf16_to_double : oracle_f16_to_double;
+}
+
 void oracle_f16_to_double_array(const uint16_t *bits, double *out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i)
         out[i] = oracle_f16_to_double(bits[i]);
+}
+
+void oracle_bf16_to_double_array(const uint16_t *bits, double *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_bf16_to_double(bits[i]);
 }
 
 /* Rows attended by sequence s: positions[s] + 1, clamped to [0, cap]. */
@@ -88,7 +123,7 @@ static int check_args(const float *q, const uint16_t *k, const uint16_t *v,
 static int one_head(const float *q, const uint16_t *k, const uint16_t *v,
                     const int32_t *positions, double *o, int n_head,
                     int n_kv_head, int head_dim, int64_t cap, double scale,
-                    int s, int h)
+                    int s, int h, decode_fn dec)
 {
     const int G = n_head / n_kv_head;
     const int hk = h / G;
@@ -109,7 +144,7 @@ static int one_head(const float *q, const uint16_t *k, const uint16_t *v,
     for (int64_t j = 0; j < n; ++j) {
         double dot = 0.0;
         for (int d = 0; d < head_dim; ++d)
-            dot += (double)qh[d] * oracle_f16_to_double(ks[j * row + d]);
+            dot += (double)qh[d] * dec(ks[j * row + d]);
         x[j] = scale * dot;
         if (x[j] > m) m = x[j];
     }
@@ -119,7 +154,7 @@ static int one_head(const float *q, const uint16_t *k, const uint16_t *v,
         const double w = exp(x[j] - m);
         Z += w;
         for (int d = 0; d < head_dim; ++d)
-            o[d] += w * oracle_f16_to_double(vs[j * row + d]);
+            o[d] += w * dec(vs[j * row + d]);
     }
     for (int d = 0; d < head_dim; ++d) o[d] /= Z;
     free(x);
@@ -131,11 +166,12 @@ static int one_head(const float *q, const uint16_t *k, const uint16_t *v,
  * (sequence, head) pairs over OpenMP threads; the arithmetic per pair is
  * unchanged. Returns 0, -1 (bad arguments) or -2 (out of host memory).
  */
-int oracle_attn_decode(const float *q, const uint16_t *k, const uint16_t *v,
-                       const int32_t *positions, double *out, int n_seq,
-                       int n_head, int n_kv_head, int head_dim, int64_t cap,
-                       double scale, int n_threads)
+int oracle_attn_decode_kv(const float *q, const uint16_t *k, const uint16_t *v,
+                          const int32_t *positions, double *out, int n_seq,
+                          int n_head, int n_kv_head, int head_dim, int64_t cap,
+                          double scale, int n_threads, int kv_dtype)
 {
+    const decode_fn dec = decoder_for(kv_dtype);
     if (check_args(q, k, v, positions, out, n_seq, n_head, n_kv_head, head_dim, cap))
         return -1;
     const int64_t pairs = (int64_t)n_seq * n_head;
@@ -145,23 +181,41 @@ int oracle_attn_decode(const float *q, const uint16_t *k, const uint16_t *v,
     for (int64_t p = 0; p < pairs; ++p) {
         const int s = (int)(p / n_head), h = (int)(p % n_head);
         const int rc = one_head(q, k, v, positions, out + p * head_dim, n_head,
-                                n_kv_head, head_dim, cap, scale, s, h);
+                                n_kv_head, head_dim, cap, scale, s, h, dec);
         if (rc < status) status = rc;
     }
     return status;
 }
 
+int oracle_attn_decode(const float *q, const uint16_t *k, const uint16_t *v,
+                       const int32_t *positions, double *out, int n_seq,
+                       int n_head, int n_kv_head, int head_dim, int64_t cap,
+                       double scale, int n_threads)
+{
+    return oracle_attn_decode_kv(q, k, v, positions, out, n_seq, n_head, n_kv_head, head_dim,
+                                 cap, scale, n_threads, 0);
+}
+
 /* One output row o[s][h][:], for sampled checks on large workloads. */
-int oracle_attn_decode_one(const float *q, const uint16_t *k, const uint16_t *v,
-                           const int32_t *positions, double *out_row, int n_seq,
-                           int n_head, int n_kv_head, int head_dim, int64_t cap,
-                           double scale, int s, int h)
+int oracle_attn_decode_one_kv(const float *q, const uint16_t *k, const uint16_t *v,
+                              const int32_t *positions, double *out_row, int n_seq,
+                              int n_head, int n_kv_head, int head_dim, int64_t cap,
+                              double scale, int s, int h, int kv_dtype)
 {
     if (check_args(q, k, v, positions, out_row, n_seq, n_head, n_kv_head, head_dim, cap))
         return -1;
     if (s < 0 || s >= n_seq || h < 0 || h >= n_head) return -1;
     return one_head(q, k, v, positions, out_row, n_head, n_kv_head, head_dim, cap,
-                    scale, s, h);
+                    scale, s, h, decoder_for(kv_dtype));
+}
+
+int oracle_attn_decode_one(const float *q, const uint16_t *k, const uint16_t *v,
+                           const int32_t *positions, double *out_row, int n_seq,
+                           int n_head, int n_kv_head, int head_dim, int64_t cap,
+                           double scale, int s, int h)
+{
+    return oracle_attn_decode_one_kv(q, k, v, positions, out_row, n_seq, n_head, n_kv_head,
+                                     head_dim, cap, scale, s, h, 0);
 }
 
 /*

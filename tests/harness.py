@@ -27,9 +27,15 @@ def assert_close(got, ref, what="", abs_tol=ABS_TOL, rel_tol=REL_TOL):
 
 
 def to_device(layer, device="cuda"):
+    """numpy arrays -> device tensors; uint16 (bfloat16 bit patterns) travel as int16."""
     import torch
-    return {name: torch.from_numpy(np.ascontiguousarray(arr)).to(device)
-            for name, arr in layer.items()}
+    out = {}
+    for name, arr in layer.items():
+        arr = np.ascontiguousarray(arr)
+        if arr.dtype == np.uint16:
+            arr = arr.view(np.int16)
+        out[name] = torch.from_numpy(arr).to(device)
+    return out
 
 
 def run_decode(pkg, dev, n_head, n_kv_head, head_dim, cap, scale, n_splits=0, split_len=0,
@@ -44,17 +50,23 @@ def run_decode(pkg, dev, n_head, n_kv_head, head_dim, cap, scale, n_splits=0, sp
     return out
 
 
-def make_case(seed, n_seq, n_head, n_kv_head, head_dim, cap, ctx, k_scale=1.0, fill=0.0):
-    """Seeded inputs (q ~ N(0,1) f32; K, V ~ N(0,1) rounded to f16), rows >= ctx set to `fill`."""
+def make_case(seed, n_seq, n_head, n_kv_head, head_dim, cap, ctx, k_scale=1.0, fill=0.0,
+              kv_dtype="f16"):
+    """Seeded inputs (q ~ N(0,1) f32; K, V ~ N(0,1) rounded to f16, or to bfloat16
+    bit patterns for kv_dtype "bf16"), rows >= ctx set to `fill`."""
+    from decode_attention_gqa_gb300.synthetic import to_bf16_bits
     rng = np.random.Generator(np.random.PCG64(seed))
     q = rng.standard_normal((n_seq, n_head, head_dim), dtype=np.float32)
-    k = (rng.standard_normal((n_seq, cap, n_kv_head, head_dim), dtype=np.float32)
-         * np.float32(k_scale)).astype(np.float16)
-    v = rng.standard_normal((n_seq, cap, n_kv_head, head_dim), dtype=np.float32).astype(np.float16)
+    k = rng.standard_normal((n_seq, cap, n_kv_head, head_dim), dtype=np.float32) * np.float32(k_scale)
+    v = rng.standard_normal((n_seq, cap, n_kv_head, head_dim), dtype=np.float32)
     ctx = [int(c) for c in ctx]
     for s, c in enumerate(ctx):
         c = max(0, min(c, cap))
         k[s, c:] = fill
         v[s, c:] = fill
+    if kv_dtype == "f16":
+        k, v = k.astype(np.float16), v.astype(np.float16)
+    else:
+        k, v = to_bf16_bits(k), to_bf16_bits(v)
     positions = np.asarray(ctx, dtype=np.int32) - 1
     return {"q": q, "k": k, "v": v, "positions": positions}

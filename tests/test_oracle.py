@@ -47,6 +47,33 @@ def test_f16_decoder_all_patterns():
     check_f16_decoder()
 
 
+def check_bf16_decoder(lib=None):
+    torch = pytest.importorskip("torch")
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.bf16_to_double(bits, lib=lib)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(ours[~nan]), np.signbit(ref[~nan]))
+
+
+def test_bf16_decoder_all_patterns():
+    check_bf16_decoder()
+
+
+def to_bf16_bits(x):
+    """float32 array -> bfloat16 bit patterns (round to nearest even, via torch)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_bits_to_f64(b):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
 # ------------------------------------------------------- 50-digit brute force
 
 def decimal_attention(q, k, v, pos, n_head, n_kv, hd, cap, scale):
@@ -93,6 +120,30 @@ def check_bruteforce(lib=None):
 
 def test_bruteforce_decimal():
     check_bruteforce()
+
+
+def check_bruteforce_bf16(lib=None):
+    """The bfloat16 entry points against the same 50-digit brute force."""
+    pytest.importorskip("torch")
+    rng = np.random.Generator(np.random.PCG64(21))
+    for (n_seq, n_head, n_kv, hd, cap, ctx) in [(1, 4, 2, 8, 12, (12,)), (2, 6, 3, 8, 9, (4, 9))]:
+        q = rng.standard_normal((n_seq, n_head, hd), dtype=np.float32)
+        kb = to_bf16_bits(rng.standard_normal((n_seq, cap, n_kv, hd), dtype=np.float32) * 3)
+        vb = to_bf16_bits(rng.standard_normal((n_seq, cap, n_kv, hd), dtype=np.float32))
+        pos = np.asarray(ctx, np.int32) - 1
+        scale = 1.0 / math.sqrt(hd)
+        got = oracle.attn_decode(q, kb, vb, pos, n_head, n_kv, hd, cap, scale, lib=lib,
+                                 kv_dtype="bf16")
+        ref = decimal_attention(q, bf16_bits_to_f64(kb), bf16_bits_to_f64(vb), pos, n_head, n_kv,
+                                hd, cap, scale)
+        assert np.max(np.abs(got - ref)) <= 1e-13
+        one = oracle.attn_decode_one(q, kb, vb, pos, n_head, n_kv, hd, cap, scale, n_seq - 1,
+                                     n_head - 1, lib=lib, kv_dtype="bf16")
+        assert np.array_equal(one, got[n_seq - 1, n_head - 1])
+
+
+def test_bruteforce_decimal_bf16():
+    check_bruteforce_bf16()
 
 
 # ------------------------------------------------------------- closed forms

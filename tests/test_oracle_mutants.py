@@ -22,13 +22,18 @@ MUTANTS = {
     "nkv_off_by_one": ("int64_t n = (int64_t)positions[s] + 1;",
                        "int64_t n = (int64_t)positions[s];"),
     "clamp_missing": ("if (n > cap) n = cap;", "if (n > cap + 0x7fffffff) n = cap;"),
-    "k_is_v": ("dot += (double)qh[d] * oracle_f16_to_double(ks[j * row + d]);\n        x[j]",
-               "dot += (double)qh[d] * oracle_f16_to_double(vs[j * row + d]);\n        x[j]"),
+    "k_is_v": ("dot += (double)qh[d] * dec(ks[j * row + d]);\n        x[j]",
+               "dot += (double)qh[d] * dec(vs[j * row + d]);\n        x[j]"),
     "exp_sign": ("const double w = exp(x[j] - m);", "const double w = exp(m - x[j]);"),
     "f16_bias": ("ldexp((double)(1024 + frac), expo - 25)",
                  "ldexp((double)(1024 + frac), expo - 24)"),
     "f16_subnormal": ("mag = ldexp((double)frac, -24);", "mag = ldexp((double)frac, -25);"),
-    "f16_sign": ("return sign ? -mag : mag;", "return mag;"),
+    "f16_sign": ("        mag = ldexp((double)(1024 + frac), expo - 25);\n    return sign ? -mag : mag;",
+                 "        mag = ldexp((double)(1024 + frac), expo - 25);\n    return mag;"),
+    "bf16_bias": ("ldexp((double)(128 + frac), expo - 134)", "ldexp((double)(128 + frac), expo - 133)"),
+    "bf16_fields": ("const int expo = (bits >> 7) & 0xff;", "const int expo = (bits >> 8) & 0xff;"),
+    "bf16_as_f16": ("return kv_dtype == 1 ? oracle_bf16_to_double : oracle_f16_to_double;",
+                    "return oracle_f16_to_double;"),
     "split_no_corr": ("const double corr = exp(m_ - nmx);", "const double corr = 1.0;"),
     "combine_no_weight": ("exp(mx[sp] - gmx);", "1.0;"),
     "split_chunk_floor": ("(nkv + n_splits - 1) / n_splits", "nkv / n_splits"),
@@ -36,7 +41,8 @@ MUTANTS = {
                     "const float *qh = q + ((int64_t)s * n_head + hk) * head_dim;\n\n"),
 }
 
-PIN_SUITE = [pins.check_f16_decoder, pins.check_bruteforce, pins.check_closed_forms,
+PIN_SUITE = [pins.check_f16_decoder, pins.check_bf16_decoder, pins.check_bruteforce,
+             pins.check_bruteforce_bf16, pins.check_closed_forms,
              pins.check_invariants, pins.check_gqa_mapping, pins.check_positions,
              pins.check_split_equivalence, pins.check_stability]
 
