@@ -19,7 +19,8 @@ __all__ = [
     "ATTN_ERR_CUDA", "ATTN_DEVERR_POSITION_CLAMPED", "ATTN_DEVERR_PIPELINE_TIMEOUT",
     "ATTN_VARIANT_AUTO", "ATTN_VARIANT_SIMT", "ATTN_VARIANT_TC", "ATTN_KV_BF16", "library_path",
     "load",
-    "attn_decode", "attn_decode_ex", "attn_decode_append", "attn_decode_partial",
+    "attn_decode", "attn_decode_ex", "attn_decode_append", "attn_decode_multi",
+    "attn_decode_partial",
     "attn_decode_combine",
     "attn_decode_static",
     "attn_split_heuristic", "attn_workspace_size",
@@ -71,6 +72,9 @@ def load():
         lib.attn_decode_append.restype = i32
         lib.attn_decode_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i64,
                                            i32, i32, i32, vp, sz, vp]
+        lib.attn_decode_multi.restype = i32
+        lib.attn_decode_multi.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i64, i32,
+                                          i32, i32, vp, sz, vp]
         lib.attn_decode_partial.restype = i32
         lib.attn_decode_partial.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, i64, i32, i32,
                                             i32, vp, sz, vp]
@@ -153,6 +157,19 @@ def attn_decode_append(q, k_new, v_new, k_cache, v_cache, positions, out, n_seq,
                                      n_kv_head, head_dim, scale, cap, n_splits, split_len, variant,
                                      _ptr(workspace), workspace_bytes, _stream(stream)),
            "attn_decode_append")
+
+
+def attn_decode_multi(q, k_cache, v_cache, positions, out, n_seq, n_q, n_head, n_kv_head, head_dim,
+                      scale, cap, n_splits=0, split_len=0, variant=ATTN_VARIANT_AUTO,
+                      workspace=None, workspace_bytes=0, stream=None):
+    """n_q causal query rows per sequence (see include/attn_decode.h)."""
+    if workspace is not None and not workspace_bytes and hasattr(workspace, "nbytes"):
+        workspace_bytes = workspace.nbytes
+    _check(load().attn_decode_multi(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(positions),
+                                    _ptr(out), n_seq, n_q, n_head, n_kv_head, head_dim, scale, cap,
+                                    n_splits, split_len, variant, _ptr(workspace), workspace_bytes,
+                                    _stream(stream)),
+           "attn_decode_multi")
 
 
 def attn_decode_partial(q, k_cache, v_cache, positions, n_seq, n_head, n_kv_head, head_dim,

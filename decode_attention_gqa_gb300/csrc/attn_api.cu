@@ -125,7 +125,7 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
                         int n_kv_head, int head_dim, float scale, int64_t cap, bool cap_known,
                         int n_splits, int split_len, int variant, void *workspace,
                         size_t workspace_bytes, int stages, cudaStream_t stream,
-                        const void *k_new = nullptr, const void *v_new = nullptr)
+                        const void *k_new = nullptr, const void *v_new = nullptr, int n_q = 1)
 {
     // ---- synchronous argument checks, nothing launched yet ----
     const int kv_dtype = (variant & ATTN_KV_BF16) ? attn::kKvBf16 : attn::kKvF16;
@@ -146,8 +146,13 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     if ((k_new == nullptr) != (v_new == nullptr)) return ATTN_ERR_INVALID_ARG;
     if ((int64_t)n_seq * cap > kMaxFlatRows - 1024) return ATTN_ERR_INVALID_ARG;
     const int group = n_head / n_kv_head;
+    if (n_q < 1 || n_q > 1024) return ATTN_ERR_INVALID_ARG;
+    if (n_q > 1 && k_new) return ATTN_ERR_INVALID_ARG;
     if (!head_dim_supported(head_dim) || group > 8) return ATTN_ERR_UNSUPPORTED;
+    if (n_q > 1 && (head_dim % 16 != 0 || variant == ATTN_VARIANT_SIMT)) return ATTN_ERR_UNSUPPORTED;
     const int v = resolve_variant(variant, head_dim, group);
+    const int qgroups = (n_q * group + attn::kMqHeadsPerBlock - 1) / attn::kMqHeadsPerBlock;
+    if (n_q > 1 && (int64_t)n_kv_head * qgroups > 65535) return ATTN_ERR_INVALID_ARG;
     const attn::KernelInfo ki = kernel_info(head_dim, group, v);
     if (!ki.available) return ATTN_ERR_UNSUPPORTED;
     if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return ATTN_ERR_INVALID_ARG;
@@ -165,7 +170,7 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     const int P = n_splits > 0 ? n_splits
                                : heuristic(n_seq, n_kv_head, cap_known ? cap : 0, ds->sm_count, ki);
     if (split_len > 0 && (int64_t)P * split_len < cap) return ATTN_ERR_INVALID_ARG;
-    const size_t need = attn_workspace_size(n_seq, n_head, head_dim, P);
+    const size_t need = attn_workspace_size(n_seq, n_q * n_head, head_dim, P);
 
     if (!workspace) {
         if (stages != (attn::kStagePartial | attn::kStageCombine)) return ATTN_ERR_INVALID_ARG;
@@ -196,7 +201,7 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     r.pa.k = static_cast<const uint16_t *>(k_cache);
     r.pa.v = static_cast<const uint16_t *>(v_cache);
     r.pa.positions = positions;
-    const size_t o_bytes = align256((size_t)n_seq * n_head * P * head_dim * sizeof(float));
+    const size_t o_bytes = align256((size_t)n_seq * n_q * n_head * P * head_dim * sizeof(float));
     r.pa.ws_o = static_cast<float *>(workspace);
     r.pa.ws_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) + o_bytes);
     r.pa.err = err_word;
@@ -206,6 +211,8 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     r.pa.split_len = split_len;
     r.pa.cap = cap;
     r.pa.qscale = (float)((double)scale * 1.4426950408889634);
+    r.pa.n_q = n_q;
+    r.pa.qgroups = n_q > 1 ? qgroups : 1;
     if (k_new) {
         r.pa.k_new = static_cast<const uint16_t *>(k_new);
         r.pa.v_new = static_cast<const uint16_t *>(v_new);
@@ -338,6 +345,18 @@ attn_status attn_decode_append(const float *q, const void *k_new, const void *v_
                        scale, cap, true, n_splits, split_len, variant, workspace, workspace_bytes,
                        attn::kStagePartial | attn::kStageCombine,
                        reinterpret_cast<cudaStream_t>(stream), k_new, v_new);
+}
+
+attn_status attn_decode_multi(const float *q, const void *k_cache, const void *v_cache,
+                              const int32_t *positions, float *out, int n_seq, int n_q, int n_head,
+                              int n_kv_head, int head_dim, float scale, int64_t cap, int n_splits,
+                              int split_len, int variant, void *workspace, size_t workspace_bytes,
+                              attn_stream_t stream)
+{
+    return decode_impl(q, k_cache, v_cache, positions, out, n_seq, n_head, n_kv_head, head_dim,
+                       scale, cap, true, n_splits, split_len, variant, workspace, workspace_bytes,
+                       attn::kStagePartial | attn::kStageCombine,
+                       reinterpret_cast<cudaStream_t>(stream), nullptr, nullptr, n_q);
 }
 
 attn_status attn_decode_partial(const float *q, const void *k_cache, const void *v_cache,

@@ -40,6 +40,8 @@ struct PartialArgs {
     int split_len;            // 0 = by count
     int64_t cap;              // cache rows per sequence
     float qscale;             // scale * log2(e): scores come out in log2 units
+    int n_q;                  // query rows per sequence (1: decode; > 1: causal multi-query)
+    int qgroups;              // blocks per (split, KV head) along the query heads
     // Fused append (optional): the new token's rows [n_seq][n_kv_head][HD],
     // written into cache row positions[s] and attended in the same launch.
     const uint16_t *k_new;    // null: no append

@@ -24,10 +24,19 @@ template <int HD> struct TcShape  { static constexpr int NWC = 4, S = 3, MINB = 
 template <> struct TcShape<64>    { static constexpr int NWC = 4, S = 4, MINB = 2; };
 template <> struct TcShape<256>   { static constexpr int NWC = 4, S = 3, MINB = 1; };
 
+// Multi-query tensor-core blocks: 16 query heads each.
+template <int HD> struct TcMqShape { static constexpr int NWC = 4, S = 3, MINB = 2; };
+template <> struct TcMqShape<256>  { static constexpr int NWC = 4, S = 3, MINB = 1; };
+constexpr int kMqHeads = 16;
+
 template <int HD, int G, typename KV>
 using SimtCfg = PartialCfg<HD, G, SimtWarp, SimtShape<HD>::NWC, SimtShape<HD>::S, SimtShape<HD>::MINB, KV>;
 template <int HD, int G, typename KV>
 using TcCfg = PartialCfg<HD, G, TcWarp, TcShape<HD>::NWC, TcShape<HD>::S, TcShape<HD>::MINB, KV>;
+
+template <int HD, typename KV>
+using TcMqCfg = PartialCfg<HD, kMqHeads, TcWarpMQ, TcMqShape<HD>::NWC, TcMqShape<HD>::S,
+                           TcMqShape<HD>::MINB, KV>;
 
 template <typename KV> constexpr int kv_dtype_code() { return std::is_same<KV, __half>::value ? kKvF16 : kKvBf16; }
 
@@ -55,7 +64,7 @@ cudaError_t launch_partial(const LaunchRequest &r)
     if (e != cudaSuccess) return e;
     PartialArgs pa = r.pa;
     void *args[] = {&kmap, &vmap, &pa};
-    return launch_pdl(fn, dim3(pa.n_splits, pa.n_kv_head, r.n_seq), dim3(Cfg::THREADS),
+    return launch_pdl(fn, dim3(pa.n_splits, pa.n_kv_head * pa.qgroups, r.n_seq), dim3(Cfg::THREADS),
                       Cfg::SMEM_BYTES, r.stream, args);
 }
 
@@ -66,7 +75,7 @@ cudaError_t launch_combine(const LaunchRequest &r)
     ca.ws_o = r.pa.ws_o;
     ca.ws_ml = r.pa.ws_ml;
     ca.out = r.out;
-    ca.n_head = r.pa.n_head;
+    ca.n_head = r.pa.n_head * (r.pa.n_q > 0 ? r.pa.n_q : 1);   // partial heads per sequence
     ca.n_splits = r.pa.n_splits;
     const void *fn = reinterpret_cast<const void *>(&attn_combine<HD>);
     void *args[] = {&ca};
@@ -95,6 +104,19 @@ cudaError_t launch_group(const LaunchRequest &r)
 template <int HD, typename KV>
 cudaError_t launch_for_hd(const LaunchRequest &r)
 {
+    if (r.pa.n_q > 1) {                     // several causal query rows: tensor cores only
+        if constexpr (HD % 16 == 0) {
+            cudaError_t e = cudaSuccess;
+            if (r.stages & kStagePartial) {
+                e = launch_partial<TcMqCfg<HD, KV>, HD, kMqHeads, KV>(r);
+                if (e != cudaSuccess) return e;
+            }
+            if (r.stages & kStageCombine) e = launch_combine<HD>(r);
+            return e;
+        } else {
+            return cudaErrorInvalidValue;
+        }
+    }
     switch (r.group) {
     case 1: return launch_group<HD, 1, KV>(r);
     case 2: return launch_group<HD, 2, KV>(r);

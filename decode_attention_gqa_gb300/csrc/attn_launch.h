@@ -13,6 +13,7 @@ namespace attn {
 
 constexpr int kVariantSimt = 1;
 constexpr int kVariantTc = 2;
+constexpr int kMqHeadsPerBlock = 16;        // query heads per multi-query block
 constexpr int kKvF16 = 0;
 constexpr int kKvBf16 = 1;
 constexpr int kStagePartial = 1;

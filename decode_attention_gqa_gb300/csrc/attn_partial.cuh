@@ -21,12 +21,14 @@
 // memory and the block writes one partial triple per query head (§3.2).
 //
 // The per-warp arithmetic is a policy class: SimtWarp (attn_warp_simt.cuh,
-// CUDA cores, f32) or TcWarp (attn_warp_tc.cuh, tensor cores).
+// CUDA cores, f32), TcWarp (attn_warp_tc.cuh, tensor cores, one query row)
+// or TcWarpMQ (attn_warp_tcmq.cuh, tensor cores, several causal query rows).
 #pragma once
 
 #include "attn_device.cuh"
 #include "attn_warp_simt.cuh"
 #include "attn_warp_tc.cuh"
+#include "attn_warp_tcmq.cuh"
 
 namespace attn {
 
@@ -50,7 +52,8 @@ struct PartialCfg {
     static constexpr uint32_t BAR_BYTES = 2 * S * 8 + 16;
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;   // + base alignment slack
     // merge area (reuses the stage buffers after the main loop)
-    static constexpr uint32_t MERGE_BYTES = (uint32_t)NWC * G * (HD + 2) * 4;
+    static constexpr int NQH = Warp::NQH;            // query heads per block
+    static constexpr uint32_t MERGE_BYTES = (uint32_t)NWC * NQH * (HD + 2) * 4;
     static_assert(MERGE_BYTES <= S * STAGE_BYTES, "merge area must fit in the stage buffers");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(HD < 64 || (TILE_BYTES / NCH) % 1024 == 0, "swizzled chunks must stay 1024-aligned");
@@ -74,7 +77,10 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     uint64_t *empty = full + S;
     volatile int *flags = reinterpret_cast<volatile int *>(empty + S);   // [0] abort, [1] tiles issued
 
-    const int sp = blockIdx.x, hk = blockIdx.y, s = blockIdx.z;
+    const int sp = blockIdx.x, s = blockIdx.z;
+    const int hk = blockIdx.y / a.qgroups, qg = blockIdx.y % a.qgroups;
+    constexpr int NQH = Cfg::NQH;
+    const size_t heads = (size_t)a.n_q * a.n_head;          // partial heads per sequence
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = a.n_splits;
 
@@ -85,12 +91,14 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
 
     // a1: rows attended and this split's range; an empty split leaves at once
     bool pos_ok;
-    const int64_t nkv = rows_attended(a, s, sp == 0 && hk == 0 && tid == 0, &pos_ok);
-    const size_t head0 = (size_t)s * a.n_head + (size_t)hk * G;          // first query head of the group
+    const int64_t nkv = rows_attended(a, s, sp == 0 && blockIdx.y == 0 && tid == 0, &pos_ok);
     int64_t lo, hi;
     split_range(nkv, sp, P, a.split_len, WR, lo, hi);
     if (lo >= hi) {                                                      // empty split: mx=-inf, S=0
-        if (tid < G) a.ws_ml[(head0 + tid) * P + sp] = make_float2(-INFINITY, 0.f);
+        if (tid < NQH) {
+            const int hp = Warp::slot_head(a, hk, qg, tid);
+            if (hp >= 0) a.ws_ml[((size_t)s * heads + hp) * P + sp] = make_float2(-INFINITY, 0.f);
+        }
         return;
     }
     const int ntiles = (int)((hi - lo + TILE - 1) / TILE);
@@ -130,7 +138,7 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         flags[1] = early;
     }
     // a2, while the first tiles are in flight
-    Warp::template prepare<Cfg::THREADS>(extra, a.q + head0 * HD, a.qscale, tid);
+    Warp::template prepare<Cfg::THREADS>(extra, a, s, hk, qg, tid);
     __syncthreads();
     early = flags[1];
 
@@ -232,7 +240,10 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
                 fence_proxy_async_smem();
                 __syncwarp();
             }
-            if (ra < WR) wst.template process<TILE>(kst, vst, warp * WR, ra > 0 ? ra : 0, extra, warp, lane);
+            const int64_t row0 = nrows == TILE ? first : hi - TILE;   // sequence row of tile row 0
+            if (ra < WR)
+                wst.template process<TILE>(kst, vst, warp * WR, ra > 0 ? ra : 0, row0, nkv, a, extra,
+                                           warp, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(empty + st);
         }
@@ -240,8 +251,8 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         // done with the ring before any of them publishes its state
         asm volatile("bar.sync 1, %0;" :: "r"(NWC * 32) : "memory");
         if (!__shfl_sync(0xffffffffu, flags[0], 0))
-            wst.publish(reinterpret_cast<float2 *>(smem) + warp * G,
-                        reinterpret_cast<float *>(smem) + 2 * NWC * G + warp * G * HD, lane);
+            wst.publish(reinterpret_cast<float2 *>(smem) + warp * NQH,
+                        reinterpret_cast<float *>(smem) + 2 * NWC * NQH + warp * NQH * HD, lane);
     }
     __syncthreads();
 
@@ -254,22 +265,26 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     if (flags[0]) return;        // partial left unwritten; the error word says why
 
     // a6: merge the NWC warp states and write the partial triple of each head
+    // (a query head no warp saw a row for -- possible with causal limits --
+    // keeps mx = -inf and S = 0)
     const float2 *mm = reinterpret_cast<const float2 *>(smem);
-    const float *mo = reinterpret_cast<const float *>(smem) + 2 * NWC * G;
-    for (int i = tid; i < G * HD; i += Cfg::THREADS) {
+    const float *mo = reinterpret_cast<const float *>(smem) + 2 * NWC * NQH;
+    for (int i = tid; i < NQH * HD; i += Cfg::THREADS) {
         const int g = i / HD, d = i % HD;
+        const int hp = Warp::slot_head(a, hk, qg, g);
+        if (hp < 0) continue;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NWC; ++w) M = fmaxf(M, mm[w * G + g].x);
+        for (int w = 0; w < NWC; ++w) M = fmaxf(M, mm[w * NQH + g].x);
         float O = 0.f, L = 0.f;
 #pragma unroll
         for (int w = 0; w < NWC; ++w) {
-            const float2 ml = mm[w * G + g];
-            const float wt = ex2(ml.x - M);                 // 0 for a warp that saw no rows
-            O = fmaf(wt, mo[(w * G + g) * HD + d], O);
+            const float2 ml = mm[w * NQH + g];
+            const float wt = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
+            O = fmaf(wt, mo[(w * NQH + g) * HD + d], O);
             L = fmaf(wt, ml.y, L);
         }
-        const size_t slot = (head0 + g) * P + sp;
+        const size_t slot = ((size_t)s * heads + hp) * P + sp;
         a.ws_o[slot * HD + d] = O;
         if (d == 0) a.ws_ml[slot] = make_float2(M, L);
     }

@@ -16,6 +16,15 @@ namespace attn {
 template <int HD, int G, int NWC, typename KV>
 struct SimtWarp {
     static constexpr int WR = 32;                          // rows per warp slice
+    static constexpr int NQH = G;                     // query heads per block (one query row)
+
+    // Partial-head index of block-local query head i (single query row: the
+    // group's heads hk*G .. hk*G+G-1).
+    static __device__ __forceinline__ int slot_head(const PartialArgs &a, int hk, int, int i)
+    {
+        (void)a;
+        return hk * G + i;
+    }
     static constexpr int NU = HD / 8;                      // 16-byte units per row
     static constexpr int DPL = HD >= 64 ? HD / 32 : 2;     // dims per lane, value phase
     static constexpr int LPRV = HD / DPL;                  // lanes per row, value phase
@@ -30,9 +39,11 @@ struct SimtWarp {
     // a2: the group's G query rows (f32), pre-multiplied by scale*log2(e),
     // into shared memory. All threads of the block take part.
     template <int NTHREADS>
-    static __device__ __forceinline__ void prepare(uint8_t *extra, const float *qg, float qscale,
-                                                   int tid)
+    static __device__ __forceinline__ void prepare(uint8_t *extra, const PartialArgs &a, int s,
+                                                   int hk, int, int tid)
     {
+        const float *qg = a.q + ((size_t)s * a.n_head + (size_t)hk * G) * HD;
+        const float qscale = a.qscale;
         constexpr int N4 = G * HD / 4;                    // float4s of the group's q
         constexpr int ITER = (N4 + NTHREADS - 1) / NTHREADS;
         const float4 *src = reinterpret_cast<const float4 *>(qg);
@@ -68,6 +79,7 @@ struct SimtWarp {
     // Rows [r0 + ra, r0 + WR) of a TILE-row stage are in range (0 <= ra < WR).
     template <int TILE>
     __device__ __forceinline__ void process(const uint8_t *ks, const uint8_t *vs, int r0, int ra,
+                                            int64_t, int64_t, const PartialArgs &,
                                             uint8_t *extra, int warp, int lane)
     {
         const float *qs = reinterpret_cast<const float *>(extra);
@@ -77,7 +89,8 @@ struct SimtWarp {
 #pragma unroll
         for (int g = 0; g < G; ++g) acc[g] = 0.f;
         const int r = r0 + lane;
-#pragma unroll 2
+        constexpr int UNROLL = (HD >= 256 && G >= 7) ? 1 : 2;   // register budget of the largest shapes
+#pragma unroll UNROLL
         for (int U = 0; U < NU; ++U) {
             const uint4 raw = *reinterpret_cast<const uint4 *>(ks + tile_unit_offset<HD, TILE>(r, U));
             float kf[8];

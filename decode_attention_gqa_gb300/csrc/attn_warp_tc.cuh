@@ -33,6 +33,15 @@ template <int HD, int G, int NWC, typename KV>
 struct TcWarp {
     static_assert(HD % 16 == 0, "tensor-core path needs head_dim % 16 == 0");
     static constexpr int WR = 16;                     // rows per warp slice
+    static constexpr int NQH = G;                     // query heads per block (one query row)
+
+    // Partial-head index of block-local query head i (single query row: the
+    // group's heads hk*G .. hk*G+G-1).
+    static __device__ __forceinline__ int slot_head(const PartialArgs &a, int hk, int, int i)
+    {
+        (void)a;
+        return hk * G + i;
+    }
     static constexpr int KSTEPS = HD / 16;            // k-steps of q·Kᵀ
     static constexpr int NTD = HD / 8;                // n-tiles of p·V
     static constexpr bool Q_REGS = HD <= 64;          // keep q fragments in registers (else smem)
@@ -49,9 +58,11 @@ struct TcWarp {
     // and the per-head power-of-two scale. Warp w takes heads w, w + NW, ...;
     // all of a warp's loads are issued before any of its reductions.
     template <int NTHREADS>
-    static __device__ __forceinline__ void prepare(uint8_t *extra, const float *qg, float qscale,
-                                                   int tid)
+    static __device__ __forceinline__ void prepare(uint8_t *extra, const PartialArgs &a, int s,
+                                                   int hk, int, int tid)
     {
+        const float *qg = a.q + ((size_t)s * a.n_head + (size_t)hk * G) * HD;
+        const float qscale = a.qscale;
         constexpr int NW = NTHREADS / 32;
         constexpr int ITER = (8 + NW - 1) / NW;           // heads per warp
         constexpr int PER = (HD + 31) / 32;               // elements per lane per head
@@ -128,6 +139,7 @@ struct TcWarp {
     // rows before ra hold finite data (zeros or rows already attended).
     template <int TILE>
     __device__ __forceinline__ void process(const uint8_t *ks, const uint8_t *vs, int r0, int ra,
+                                            int64_t, int64_t, const PartialArgs &,
                                             uint8_t *extra, int, int lane)
     {
         // a3: scores of the slice's 16 rows for all heads

@@ -138,6 +138,29 @@ attn_status attn_decode_append(const float *q, const void *k_new, const void *v_
                                void *workspace, size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * attn_decode_multi -- several causal query rows per sequence (speculative
+ * drafts, short chunks): the variant dotLLM #199 §2 gates out (more than one
+ * query row needs a causal mask offset by the query's position).
+ *   n_q             query rows per sequence (1 <= n_q <= 1024); n_q == 1 is
+ *                   attn_decode_ex.
+ *   q, out          float [n_seq][n_q][n_head][head_dim].
+ *   positions[s]    position of the sequence's LAST query row; with
+ *                   nkv = clamp(positions[s] + 1, 0, cap), query row t sits at
+ *                   position nkv - n_q + t and attends cache rows
+ *                   [0, nkv - n_q + t] (none when that is negative: o = 0).
+ *   workspace       attn_workspace_size(n_seq, n_q * n_head, head_dim, n_splits)
+ *                   bytes (the partials of every query row).
+ * Needs head_dim % 16 == 0 (tensor-core kernel; ATTN_VARIANT_SIMT and
+ * head_dim 8 return ATTN_ERR_UNSUPPORTED). K/V are read once per block of 16
+ * (query row, head) pairs of a KV head. Other arguments as attn_decode_ex.
+ */
+attn_status attn_decode_multi(const float *q, const void *k_cache, const void *v_cache,
+                              const int32_t *positions, float *out, int n_seq, int n_q, int n_head,
+                              int n_kv_head, int head_dim, float scale, int64_t cap, int n_splits,
+                              int split_len, int variant, void *workspace, size_t workspace_bytes,
+                              attn_stream_t stream);
+
+/*
  * attn_decode_partial / attn_decode_combine -- the two stages of attn_decode_ex
  * as separate calls (same arguments, same validation), for callers that time
  * the stages apart or merge partials produced elsewhere before combining.

@@ -59,6 +59,9 @@ def _bind(lib):
     lib.oracle_attn_decode_kv.argtypes = common + [i32, i32]
     lib.oracle_attn_decode_one_kv.restype = i32
     lib.oracle_attn_decode_one_kv.argtypes = common + [i32, i32, i32]
+    lib.oracle_attn_decode_multi.restype = i32
+    lib.oracle_attn_decode_multi.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, i64, dbl, i32,
+                                             i32]
     lib.oracle_attn_decode_split.restype = i32
     lib.oracle_attn_decode_split.argtypes = common + [i32, i64]
     return lib
@@ -162,4 +165,21 @@ def attn_decode_split(q, k, v, positions, n_head, n_kv_head, head_dim, cap, scal
                                       int(n_splits), int(split_len))
     if rc != 0:
         raise ValueError("oracle_attn_decode_split failed with status %d" % rc)
+    return out
+
+
+def attn_decode_multi(q, k, v, positions, n_q, n_head, n_kv_head, head_dim, cap, scale,
+                      n_threads=1, lib=None, kv_dtype="f16") -> np.ndarray:
+    """Causal multi-query oracle: q f32 [n_seq, n_q, n_head, head_dim]; query row t
+    attends the first clamp(positions[s]+1, 0, cap) - n_q + t + 1 rows.
+    Returns float64 [n_seq, n_q, n_head, head_dim]."""
+    lib = lib or load_library()
+    q, k, v, positions = _prep(q, k, v, positions)
+    n_seq = positions.shape[0]
+    out = np.zeros((n_seq, n_q, n_head, head_dim), dtype=np.float64)
+    rc = lib.oracle_attn_decode_multi(_ptr(q), _ptr(k), _ptr(v), _ptr(positions), _ptr(out),
+                                      n_seq, n_q, n_head, n_kv_head, head_dim, cap, float(scale),
+                                      int(n_threads), KV_DTYPES[kv_dtype])
+    if rc != 0:
+        raise ValueError("oracle_attn_decode_multi failed with status %d" % rc)
     return out

@@ -119,22 +119,13 @@ static int check_args(const float *q, const uint16_t *k, const uint16_t *v,
     return 0;
 }
 
-/* One (sequence, query head): single softmax over all n rows. */
-static int one_head(const float *q, const uint16_t *k, const uint16_t *v,
-                    const int32_t *positions, double *o, int n_head,
-                    int n_kv_head, int head_dim, int64_t cap, double scale,
-                    int s, int h, decode_fn dec)
+/* One query vector against the first n rows of one KV head's cache: a single
+ * softmax over all n rows (o = 0 when n <= 0). */
+static int one_query(const float *qh, const uint16_t *ks, const uint16_t *vs, int64_t row,
+                     int head_dim, int64_t n, double scale, decode_fn dec, double *o)
 {
-    const int G = n_head / n_kv_head;
-    const int hk = h / G;
-    const int64_t n = rows_for(positions, s, cap);
-    const int64_t row = (int64_t)n_kv_head * head_dim;          /* elements per cache row */
-    const uint16_t *ks = k + (int64_t)s * cap * row + (int64_t)hk * head_dim;
-    const uint16_t *vs = v + (int64_t)s * cap * row + (int64_t)hk * head_dim;
-    const float *qh = q + ((int64_t)s * n_head + h) * head_dim;
-
     for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
-    if (n == 0) return 0;
+    if (n <= 0) return 0;
 
     double *x = (double *)malloc((size_t)n * sizeof(double));
     if (!x) return -2;
@@ -159,6 +150,22 @@ static int one_head(const float *q, const uint16_t *k, const uint16_t *v,
     for (int d = 0; d < head_dim; ++d) o[d] /= Z;
     free(x);
     return 0;
+}
+
+/* One (sequence, query head) of a single-query decode. */
+static int one_head(const float *q, const uint16_t *k, const uint16_t *v,
+                    const int32_t *positions, double *o, int n_head,
+                    int n_kv_head, int head_dim, int64_t cap, double scale,
+                    int s, int h, decode_fn dec)
+{
+    const int G = n_head / n_kv_head;
+    const int hk = h / G;
+    const int64_t n = rows_for(positions, s, cap);
+    const int64_t row = (int64_t)n_kv_head * head_dim;          /* elements per cache row */
+    const uint16_t *ks = k + (int64_t)s * cap * row + (int64_t)hk * head_dim;
+    const uint16_t *vs = v + (int64_t)s * cap * row + (int64_t)hk * head_dim;
+    const float *qh = q + ((int64_t)s * n_head + h) * head_dim;
+    return one_query(qh, ks, vs, row, head_dim, n, scale, dec, o);
 }
 
 /*
@@ -216,6 +223,43 @@ int oracle_attn_decode_one(const float *q, const uint16_t *k, const uint16_t *v,
 {
     return oracle_attn_decode_one_kv(q, k, v, positions, out_row, n_seq, n_head, n_kv_head,
                                      head_dim, cap, scale, s, h, 0);
+}
+
+/*
+ * Several causal query rows per sequence (the variant dotLLM #199 §2 gates
+ * out: a query at position p attends cache rows [0, p]). With
+ * nkv = clamp(positions[s] + 1, 0, cap), query row t of sequence s sits at
+ * position nkv - n_q + t and attends its first nkv - n_q + t + 1 rows
+ * (o = 0 when that count is not positive).
+ * q, out: [n_seq][n_q][n_head][head_dim].
+ */
+int oracle_attn_decode_multi(const float *q, const uint16_t *k, const uint16_t *v,
+                             const int32_t *positions, double *out, int n_seq, int n_q,
+                             int n_head, int n_kv_head, int head_dim, int64_t cap,
+                             double scale, int n_threads, int kv_dtype)
+{
+    if (check_args(q, k, v, positions, out, n_seq, n_head, n_kv_head, head_dim, cap) || n_q < 1)
+        return -1;
+    const decode_fn dec = decoder_for(kv_dtype);
+    const int G = n_head / n_kv_head;
+    const int64_t row = (int64_t)n_kv_head * head_dim;
+    const int64_t items = (int64_t)n_seq * n_q * n_head;
+    int status = 0;
+    if (n_threads < 1) n_threads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(n_threads) reduction(min : status)
+    for (int64_t it = 0; it < items; ++it) {
+        const int h = (int)(it % n_head);
+        const int t = (int)((it / n_head) % n_q);
+        const int s = (int)(it / ((int64_t)n_head * n_q));
+        const int hk = h / G;
+        const int64_t n = rows_for(positions, s, cap) - n_q + t + 1;
+        const uint16_t *ks = k + (int64_t)s * cap * row + (int64_t)hk * head_dim;
+        const uint16_t *vs = v + (int64_t)s * cap * row + (int64_t)hk * head_dim;
+        const int rc = one_query(q + it * head_dim, ks, vs, row, head_dim, n, scale, dec,
+                                 out + it * head_dim);
+        if (rc < status) status = rc;
+    }
+    return status;
 }
 
 /*

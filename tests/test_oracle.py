@@ -372,3 +372,43 @@ def test_golden_regression_fixture():
                            sh["n_kv_head"], sh["head_dim"], sh["cap"], doc["scale"])
     want = np.array([float(x) for x in doc["o_f64"]]).reshape(o.shape)
     assert np.max(np.abs(o - want)) <= 1e-15
+
+
+# ------------------------------------------------------ causal multi-query
+
+def decimal_attention_multi(q, k, v, pos, n_q, n_head, n_kv, hd, cap, scale):
+    """50-digit brute force with a per-query causal limit (row t sees the first
+    nkv - n_q + t + 1 rows)."""
+    n_seq = q.shape[0]
+    out = np.zeros((n_seq, n_q, n_head, hd))
+    for s in range(n_seq):
+        nkv = max(0, min(int(pos[s]) + 1, cap))
+        for t in range(n_q):
+            lim = nkv - n_q + t + 1
+            if lim <= 0:
+                continue
+            sub = decimal_attention(q[s:s + 1, t], k[s:s + 1], v[s:s + 1],
+                                    np.array([lim - 1], np.int32), n_head, n_kv, hd, cap, scale)
+            out[s, t] = sub[0]
+    return out
+
+
+def check_multi_query(lib=None):
+    rng = np.random.Generator(np.random.PCG64(18))
+    n_q, n_head, n_kv, hd, cap = 3, 4, 2, 8, 10
+    q = rng.standard_normal((2, n_q, n_head, hd), dtype=np.float32)
+    k = rng.standard_normal((2, cap, n_kv, hd), dtype=np.float32).astype(np.float16)
+    v = rng.standard_normal((2, cap, n_kv, hd), dtype=np.float32).astype(np.float16)
+    pos = np.array([9, 1], np.int32)          # the second sequence: row 0 sees nothing
+    got = oracle.attn_decode_multi(q, k, v, pos, n_q, n_head, n_kv, hd, cap, 0.4, lib=lib)
+    ref = decimal_attention_multi(q, k, v, pos, n_q, n_head, n_kv, hd, cap, 0.4)
+    assert np.max(np.abs(got - ref)) <= 1e-13
+    assert np.all(got[1, 0] == 0)
+    # one query row is the single-query oracle exactly
+    one = oracle.attn_decode_multi(q[:, :1], k, v, pos, 1, n_head, n_kv, hd, cap, 0.4, lib=lib)
+    single = oracle.attn_decode(q[:, 0], k, v, pos, n_head, n_kv, hd, cap, 0.4, lib=lib)
+    assert np.array_equal(one[:, 0], single)
+
+
+def test_multi_query_causal():
+    check_multi_query()

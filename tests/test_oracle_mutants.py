@@ -37,14 +37,16 @@ MUTANTS = {
     "split_no_corr": ("const double corr = exp(m_ - nmx);", "const double corr = 1.0;"),
     "combine_no_weight": ("exp(mx[sp] - gmx);", "1.0;"),
     "split_chunk_floor": ("(nkv + n_splits - 1) / n_splits", "nkv / n_splits"),
-    "head_stride": ("const float *qh = q + ((int64_t)s * n_head + h) * head_dim;\n\n",
-                    "const float *qh = q + ((int64_t)s * n_head + hk) * head_dim;\n\n"),
+    "causal_off_by_one": ("rows_for(positions, s, cap) - n_q + t + 1;",
+                          "rows_for(positions, s, cap) - n_q + t;"),
+    "head_stride": ("const float *qh = q + ((int64_t)s * n_head + h) * head_dim;\n    return one_query",
+                    "const float *qh = q + ((int64_t)s * n_head + hk) * head_dim;\n    return one_query"),
 }
 
 PIN_SUITE = [pins.check_f16_decoder, pins.check_bf16_decoder, pins.check_bruteforce,
              pins.check_bruteforce_bf16, pins.check_closed_forms,
              pins.check_invariants, pins.check_gqa_mapping, pins.check_positions,
-             pins.check_split_equivalence, pins.check_stability]
+             pins.check_split_equivalence, pins.check_stability, pins.check_multi_query]
 
 
 def _pins_fail(lib) -> bool:
