@@ -37,6 +37,7 @@ METRIC = "decode-attn µs/layer and achieved HBM GB/s (K+V bytes/time) vs GB300 
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["attn_device.cuh", "attn_partial.cuh", "attn_warp_tc.cuh", "attn_warp_simt.cuh",
+                  "attn_warp_tcmq.cuh",
                   "attn_combine.cuh", "attn_kernels_impl.cuh"]
 
 
@@ -56,6 +57,9 @@ def parse_args():
     ap.add_argument("--kv-dtype", choices=["f16", "bf16"], default="f16")
     ap.add_argument("--append", action="store_true",
                     help="time attn_decode_append (write the new K/V row, then attend)")
+    ap.add_argument("--kv-stable", choices=["on", "off"], default="on",
+                    help="flag layers after the first with ATTN_KV_STABLE (their cache and "
+                         "positions are not written inside the step)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
@@ -305,23 +309,24 @@ def run_ours(args, rank, world, local):
 
         def _calls(self, stream, stage):
             for l in range(L):
+                var = variant | (pkg.ATTN_KV_STABLE if args.kv_stable == "on" and l > 0 else 0)
                 if stage == "combine":
                     pkg.attn_decode_combine(self.ws, self.ws_bytes, out[l], n_seq, w.n_head,
                                             w.head_dim, self.P, stream=stream)
                 elif stage == "partial":
                     pkg.attn_decode_partial(q[l], kc[l], vc[l], pos, n_seq, w.n_head, w.n_kv_head,
                                             w.head_dim, w.scale, w.cap, self.P, self.blk,
-                                            variant, self.ws, self.ws_bytes, stream=stream)
+                                            var, self.ws, self.ws_bytes, stream=stream)
                 elif args.append:
                     pkg.attn_decode_append(q[l], kn[l], vn[l], kc[l], vc[l], pos, out[l], n_seq,
                                            w.n_head, w.n_kv_head, w.head_dim, w.scale, w.cap,
                                            n_splits=self.P, split_len=self.blk,
-                                           variant=variant, workspace=self.ws,
+                                           variant=var, workspace=self.ws,
                                            workspace_bytes=self.ws_bytes, stream=stream)
                 else:
                     pkg.attn_decode_ex(q[l], kc[l], vc[l], pos, out[l], n_seq, w.n_head,
                                        w.n_kv_head, w.head_dim, w.scale, w.cap, n_splits=self.P,
-                                       split_len=self.blk, variant=variant,
+                                       split_len=self.blk, variant=var,
                                        workspace=self.ws, workspace_bytes=self.ws_bytes,
                                        stream=stream)
 
@@ -390,7 +395,9 @@ def run_ours(args, rank, world, local):
     elif blk0:
         P0 = -(-w.cap // blk0)
     else:
-        P0 = pkg.attn_split_heuristic(n_seq, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0)
+        P0 = pkg.attn_split_heuristic_ex(n_seq, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0,
+                                         variant | (pkg.ATTN_KV_STABLE
+                                                    if args.kv_stable == "on" and L > 1 else 0))
     plan = Plan(P0, blk0)
     ctx_end = max(w.ctx)
     clocks = ClockSampler(local, enabled=not args.no_clocks)
@@ -514,6 +521,7 @@ def run_ours(args, rank, world, local):
                        "n_seq": n_seq, "n_head": w.n_head, "n_kv_head": w.n_kv_head,
                        "head_dim": w.head_dim, "layers": L, "n_splits": P0, "split_len": blk0,
                        "variant": args.variant, "kv_dtype": args.kv_dtype, "append": args.append,
+                       "kv_stable": args.kv_stable,
                        "l2": "inputs larger than L2 (%d MB of K+V per step)"
                              % (kv_bytes_for([ctx_end] if advance else w.ctx) * L // 2 ** 20),
                        "parallelism": "replicas" if world > 1 else "single"},

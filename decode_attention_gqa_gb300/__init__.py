@@ -17,13 +17,14 @@ import threading
 __all__ = [
     "AttnError", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_WORKSPACE",
     "ATTN_ERR_CUDA", "ATTN_DEVERR_POSITION_CLAMPED", "ATTN_DEVERR_PIPELINE_TIMEOUT",
-    "ATTN_VARIANT_AUTO", "ATTN_VARIANT_SIMT", "ATTN_VARIANT_TC", "ATTN_KV_BF16", "library_path",
+    "ATTN_VARIANT_AUTO", "ATTN_VARIANT_SIMT", "ATTN_VARIANT_TC", "ATTN_KV_BF16", "ATTN_KV_STABLE",
+    "library_path",
     "load",
     "attn_decode", "attn_decode_ex", "attn_decode_append", "attn_decode_multi",
     "attn_decode_partial",
     "attn_decode_combine",
     "attn_decode_static",
-    "attn_split_heuristic", "attn_workspace_size",
+    "attn_split_heuristic", "attn_split_heuristic_ex", "attn_workspace_size",
     "attn_read_device_error", "attn_status_string", "attn_last_cuda_error", "attn_version",
 ]
 
@@ -32,6 +33,7 @@ ATTN_DEVERR_POSITION_CLAMPED = 0x1
 ATTN_DEVERR_PIPELINE_TIMEOUT = 0x2
 ATTN_VARIANT_AUTO, ATTN_VARIANT_SIMT, ATTN_VARIANT_TC = 0, 1, 2
 ATTN_KV_BF16 = 0x10
+ATTN_KV_STABLE = 0x20
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -85,6 +87,8 @@ def load():
                                            i32, i32, vp]
         lib.attn_split_heuristic.restype = i32
         lib.attn_split_heuristic.argtypes = [i32, i32, i32, i32, i64, i32]
+        lib.attn_split_heuristic_ex.restype = i32
+        lib.attn_split_heuristic_ex.argtypes = [i32, i32, i32, i32, i64, i32, i32]
         lib.attn_workspace_size.restype = sz
         lib.attn_workspace_size.argtypes = [i32, i32, i32, i32]
         lib.attn_read_device_error.restype = i32
@@ -207,6 +211,11 @@ def attn_decode_static(q, k_cache, v_cache, positions, out, n_seq, n_head, n_kv_
 
 def attn_split_heuristic(n_seq, n_head, n_kv_head, head_dim, cap, sm_count) -> int:
     return load().attn_split_heuristic(n_seq, n_head, n_kv_head, head_dim, cap, sm_count)
+
+
+def attn_split_heuristic_ex(n_seq, n_head, n_kv_head, head_dim, cap, sm_count, variant) -> int:
+    return load().attn_split_heuristic_ex(n_seq, n_head, n_kv_head, head_dim, cap, sm_count,
+                                          variant)
 
 
 def attn_workspace_size(n_seq, n_head, head_dim, n_splits) -> int:

@@ -20,6 +20,7 @@ constexpr int kMaxDevices = 64;
 constexpr int kMaxSplits = 4096;                  // combine keeps P weights in shared memory
 constexpr int64_t kMaxFlatRows = (int64_t)1 << 31; // TMA row coordinates are int32
 constexpr int64_t kUnknownCap = kMaxFlatRows - 1024;
+constexpr int kStableTiles = 4;                    // "short call": <= 4 tiles per block at one per SM
 
 thread_local int t_last_cuda_error = 0;
 
@@ -100,11 +101,19 @@ int resolve_variant(int variant, int head_dim, int group)
 // `waves` waves of resident blocks -- one wave for a single sequence, eight for
 // a batch whose lengths may be ragged, so blocks of unequal work still balance
 // -- round it up to the kernel's row granule and take P = ceil(cap / chunk).
-// Without it: one wave.
-int heuristic(int n_seq, int n_kv_head, int64_t cap, int sm_count, const attn::KernelInfo &ki)
+// Without it: one wave. With kv_stable, one sequence and a short call (at one
+// block per SM each block's rows fit in a few tiles, so the launch is bound by
+// latency rather than bandwidth) the wave is one block per SM, leaving room
+// for the next flagged call's blocks.
+int heuristic(int n_seq, int n_kv_head, int64_t cap, int sm_count, const attn::KernelInfo &ki,
+              bool kv_stable)
 {
     const int64_t units = (int64_t)n_seq * n_kv_head;
-    const int64_t slots = (int64_t)sm_count * (ki.blocks_per_sm > 0 ? ki.blocks_per_sm : 1);
+    int per_sm = ki.blocks_per_sm > 0 ? ki.blocks_per_sm : 1;
+    if (kv_stable && n_seq == 1 && cap > 0 && sm_count > 0 &&
+        (cap * units + sm_count - 1) / sm_count <= (int64_t)kStableTiles * ki.tile_rows)
+        per_sm = 1;
+    const int64_t slots = (int64_t)sm_count * per_sm;
     const int64_t gran = ki.granule > 0 ? ki.granule : attn::kSplitGranule;
     int64_t P;
     if (cap > 0) {
@@ -129,7 +138,8 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
 {
     // ---- synchronous argument checks, nothing launched yet ----
     const int kv_dtype = (variant & ATTN_KV_BF16) ? attn::kKvBf16 : attn::kKvF16;
-    variant &= ~ATTN_KV_BF16;
+    const int kv_stable = (variant & ATTN_KV_STABLE) ? 1 : 0;
+    variant &= ~(ATTN_KV_BF16 | ATTN_KV_STABLE);
     if (n_seq < 0 || n_head <= 0 || n_kv_head <= 0 || head_dim <= 0) return ATTN_ERR_INVALID_ARG;
     if (n_head % n_kv_head != 0) return ATTN_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
@@ -168,7 +178,8 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     if (e != cudaSuccess) return cuda_fail(e);
 
     const int P = n_splits > 0 ? n_splits
-                               : heuristic(n_seq, n_kv_head, cap_known ? cap : 0, ds->sm_count, ki);
+                               : heuristic(n_seq, n_kv_head, cap_known ? cap : 0, ds->sm_count, ki,
+                                           kv_stable != 0);
     if (split_len > 0 && (int64_t)P * split_len < cap) return ATTN_ERR_INVALID_ARG;
     const size_t need = attn_workspace_size(n_seq, n_q * n_head, head_dim, P);
 
@@ -213,6 +224,7 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     r.pa.qscale = (float)((double)scale * 1.4426950408889634);
     r.pa.n_q = n_q;
     r.pa.qgroups = n_q > 1 ? qgroups : 1;
+    r.pa.kv_stable = kv_stable;
     if (k_new) {
         r.pa.k_new = static_cast<const uint16_t *>(k_new);
         r.pa.v_new = static_cast<const uint16_t *>(v_new);
@@ -272,16 +284,19 @@ cudaError_t encode_kv_map(CUtensorMap *map, const void *base, int64_t rows, int 
 
 cudaError_t ensure_smem_attr(const void *func, int bytes)
 {
-    if (bytes <= 48 * 1024) return cudaSuccess;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(g_mu);
     if (g_smem_done.count({func, dev})) return cudaSuccess;
-    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) return e;
-    // all of the unified L1/shared array as shared memory, so that as many
-    // blocks as the shared-memory budget allows are resident per SM
+    if (bytes > 48 * 1024) {
+        e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+    }
+    // All of the unified L1/shared array as shared memory, for every kernel of
+    // the library (the combine too, although it needs 1 KB): an SM holds one
+    // carve-out at a time, so a kernel that preferred a small one would keep
+    // the next layer's partial blocks off the SMs it occupies.
     e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess) g_smem_done.insert({func, dev});
@@ -401,9 +416,13 @@ attn_status attn_decode_combine(const void *workspace, size_t workspace_bytes, f
     return ATTN_OK;
 }
 
-int attn_split_heuristic(int n_seq, int n_head, int n_kv_head, int head_dim, int64_t cap,
-                         int sm_count)
+int attn_split_heuristic_ex(int n_seq, int n_head, int n_kv_head, int head_dim, int64_t cap,
+                            int sm_count, int variant)
 {
+    const bool stable = (variant & ATTN_KV_STABLE) != 0;
+    variant &= ~(ATTN_KV_BF16 | ATTN_KV_STABLE);
+    if (variant != ATTN_VARIANT_AUTO && variant != ATTN_VARIANT_SIMT && variant != ATTN_VARIANT_TC)
+        return 0;
     if (n_seq <= 0 || n_head <= 0 || n_kv_head <= 0 || n_head % n_kv_head != 0) return 0;
     const int group = n_head / n_kv_head;
     if (!head_dim_supported(head_dim) || group > 8) return 0;
@@ -413,8 +432,16 @@ int attn_split_heuristic(int n_seq, int n_head, int n_kv_head, int head_dim, int
         if (cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return 0;
     }
-    const int v = resolve_variant(ATTN_VARIANT_AUTO, head_dim, group);
-    return heuristic(n_seq, n_kv_head, cap, sm_count, kernel_info(head_dim, group, v));
+    const attn::KernelInfo ki = kernel_info(head_dim, group, resolve_variant(variant, head_dim, group));
+    if (!ki.available) return 0;
+    return heuristic(n_seq, n_kv_head, cap, sm_count, ki, stable);
+}
+
+int attn_split_heuristic(int n_seq, int n_head, int n_kv_head, int head_dim, int64_t cap,
+                         int sm_count)
+{
+    return attn_split_heuristic_ex(n_seq, n_head, n_kv_head, head_dim, cap, sm_count,
+                                   ATTN_VARIANT_AUTO);
 }
 
 size_t attn_workspace_size(int n_seq, int n_head, int head_dim, int n_splits)

@@ -54,8 +54,11 @@ attn_combine(const CombineArgs a)
     __shared__ float sm_m[C::WARPS], sm_s[C::WARPS];
     __shared__ float sm_acc[C::WARPS][C::DC];
 
-    pdl_wait();                                      // partials come from the previous grid
+    // Let the next kernel's blocks get resident now (they wait for this grid
+    // before touching anything it writes); the partials come from the grid
+    // before this one.
     pdl_launch_dependents();
+    pdl_wait();
 
     const int h = blockIdx.x, s = blockIdx.y, chunk = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -74,42 +77,54 @@ attn_combine(const CombineArgs a)
 #pragma unroll
         for (int b = 0; b < C::BATCH; ++b) {
             const int sp = base + b * C::NG;
-            mlv[b] = sp < P ? ml[sp] : make_float2(-INFINITY, 0.f);
-            const float4 t = *reinterpret_cast<const float4 *>(oc + (size_t)(sp < P ? sp : 0) * HD);
+            mlv[b] = sp < P ? ld_dep(ml + sp) : make_float2(-INFINITY, 0.f);
+            const float4 t = ld_dep(reinterpret_cast<const float4 *>(oc + (size_t)(sp < P ? sp : 0) * HD));
             ov[b][0] = t.x; ov[b][1] = t.y; ov[b][2] = t.z; ov[b][3] = t.w;
         }
 #pragma unroll
         for (int b = 0; b < C::BATCH; ++b) fold<4>(m, S, acc, mlv[b].x, mlv[b].y, ov[b]);
     }
-    // fold the warp's split groups (lanes LPS apart hold the same dims)
+    // Fold the warp's split groups (lanes LPS apart hold the same dims) and
+    // then the warps, each as maximum first, then one rescale and a sum, so
+    // that the exponentials do not form a serial chain.
+    float mw = m;
+#pragma unroll
+    for (int off = C::LPS; off < 32; off <<= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, off));
+    {
+        const float c = m == -INFINITY ? 0.f : ex2(m - mw);   // a group that saw no split adds 0
+        S *= c;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] *= c;
+    }
 #pragma unroll
     for (int off = C::LPS; off < 32; off <<= 1) {
-        float a2[4];
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-        const float S2 = __shfl_xor_sync(0xffffffffu, S, off);
+        S += __shfl_xor_sync(0xffffffffu, S, off);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) a2[i] = __shfl_xor_sync(0xffffffffu, acc[i], off);
-        fold<4>(m, S, acc, m2, S2, a2);
+        for (int i = 0; i < 4; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], off);
     }
     if (sg == 0) {
         if (dl == 0) {
-            sm_m[warp] = m;
+            sm_m[warp] = mw;
             sm_s[warp] = S;
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) sm_acc[warp][dl * 4 + i] = acc[i];
     }
     __syncthreads();
-    // fold the warps: thread d of the chunk
+    // the warps: thread d of the chunk
     if (threadIdx.x < C::DC) {
         const int d = threadIdx.x;
-        float M = -INFINITY, St = 0.f, A[1] = {0.f};
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < C::WARPS; ++w) M = fmaxf(M, sm_m[w]);
+        float St = 0.f, A = 0.f;
 #pragma unroll
         for (int w = 0; w < C::WARPS; ++w) {
-            const float a2[1] = {sm_acc[w][d]};
-            fold<1>(M, St, A, sm_m[w], sm_s[w], a2);
+            const float wt = sm_m[w] == -INFINITY ? 0.f : ex2(sm_m[w] - M);
+            St = fmaf(wt, sm_s[w], St);
+            A = fmaf(wt, sm_acc[w][d], A);
         }
-        a.out[row * HD + chunk * C::DC + d] = St > 0.f ? A[0] / St : 0.f;
+        a.out[row * HD + chunk * C::DC + d] = St > 0.f ? A / St : 0.f;
     }
 }
 

@@ -26,6 +26,47 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 // The host heuristic never makes a split shorter than this at full capacity.
 constexpr int kSplitGranule = 16;
 
+// ---------------------------------------------------------------------------
+// Loads of inputs that the previous kernel in the stream may have written (q,
+// positions, the appended rows, the partials). They go through L2 (.cg), the
+// point of coherence, and are volatile with a memory clobber, so the compiler
+// keeps them after griddepcontrol.wait. The read-only path (__ldg) is not
+// used for these: its loads may be hoisted above the wait and may return
+// lines cached before the other grid wrote them.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float ld_dep(const float *p)
+{
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ int ld_dep(const int *p)
+{
+    int v;
+    asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ float2 ld_dep(const float2 *p)
+{
+    float2 v;
+    asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 ld_dep(const float4 *p)
+{
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint4 ld_dep(const uint4 *p)
+{
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+    return v;
+}
+
 struct PartialArgs {
     const float *q;           // [n_seq][n_head][HD] f32
     const uint16_t *k;        // [n_seq][cap][n_kv_head][HD] 16-bit elements (tail tiles read directly)
@@ -48,6 +89,7 @@ struct PartialArgs {
     const uint16_t *v_new;
     uint16_t *k_w;            // the caches again, writable, when appending
     uint16_t *v_w;
+    int kv_stable;            // 1: positions and cache rows may be read before the grid dependency
 };
 
 struct CombineArgs {
@@ -66,7 +108,7 @@ struct CombineArgs {
 __device__ __forceinline__ int64_t rows_attended(const PartialArgs &a, int s, bool report,
                                                  bool *in_range = nullptr)
 {
-    int64_t n = (int64_t)__ldg(a.positions + s) + 1;
+    int64_t n = (int64_t)ld_dep(a.positions + s) + 1;
     const bool ok = n >= 0 && n <= a.cap;
     if (!ok) {
         if (report) atomicOr(a.err, kErrPositionClamped);
@@ -90,6 +132,20 @@ __device__ __forceinline__ void split_range(int64_t nkv, int sp, int n_splits, i
     }
     lo = (int64_t)sp * chunk;
     hi = lo + chunk < nkv ? lo + chunk : nkv;
+}
+
+// Row stride (floats) of a warp's published accumulators in the merge area:
+// 8 floats of padding put the rows of consecutive heads 8 banks apart, so
+// that the tensor-core fragments (lanes 4 apart hold the same dims of
+// different heads) store without bank conflicts.
+template <int HD> __host__ __device__ constexpr int merge_stride() { return HD + 8; }
+
+// Warm L2 with [p, p + bytes) (p and bytes multiples of 16). A hint with no
+// effect on what any load returns: L2 is coherent, so it may be issued before
+// the data's producer has finished.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
 }
 
 // ---------------------------------------------------------------------------

@@ -78,6 +78,8 @@ cudaError_t launch_combine(const LaunchRequest &r)
     ca.n_head = r.pa.n_head * (r.pa.n_q > 0 ? r.pa.n_q : 1);   // partial heads per sequence
     ca.n_splits = r.pa.n_splits;
     const void *fn = reinterpret_cast<const void *>(&attn_combine<HD>);
+    const cudaError_t e = ensure_smem_attr(fn, 0);
+    if (e != cudaSuccess) return e;
     void *args[] = {&ca};
     return launch_pdl(fn, dim3(ca.n_head, r.n_seq, CombineCfg<HD>::NCHUNK),
                       dim3(CombineCfg<HD>::THREADS), 0, r.stream, args);

@@ -47,7 +47,8 @@ struct KernelInfo {
 // swizzle when box_x * 2 == 128.
 cudaError_t encode_kv_map(CUtensorMap *map, const void *base, int64_t rows, int n_kv_head,
                           int head_dim, int box_x, int box_rows, int kv_dtype);
-// Opt a kernel into more than 48 KB of dynamic shared memory (once per device).
+// Opt a kernel into `bytes` of dynamic shared memory (when above 48 KB) and the
+// largest shared-memory carve-out (once per device).
 cudaError_t ensure_smem_attr(const void *func, int bytes);
 // Launch with the programmatic-stream-serialisation attribute set.
 cudaError_t launch_pdl(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,

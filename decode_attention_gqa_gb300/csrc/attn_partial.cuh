@@ -53,7 +53,9 @@ struct PartialCfg {
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;   // + base alignment slack
     // merge area (reuses the stage buffers after the main loop)
     static constexpr int NQH = Warp::NQH;            // query heads per block
-    static constexpr uint32_t MERGE_BYTES = (uint32_t)NWC * NQH * (HD + 2) * 4;
+    static constexpr int MS = merge_stride<HD>();    // floats per published accumulator row
+    static constexpr uint32_t OFF_WTS = (uint32_t)NWC * NQH * (MS + 2);   // floats: merge weights
+    static constexpr uint32_t MERGE_BYTES = (OFF_WTS + (uint32_t)NWC * NQH) * 4;
     static_assert(MERGE_BYTES <= S * STAGE_BYTES, "merge area must fit in the stage buffers");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(HD < 64 || (TILE_BYTES / NCH) % 1024 == 0, "swizzled chunks must stay 1024-aligned");
@@ -85,8 +87,21 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     const int P = a.n_splits;
 
     // Inputs may be produced by the previous kernel in the stream: wait for it
-    // before the first read, then let the combine kernel get scheduled.
-    pdl_wait();
+    // before the first read of them. The next kernel (the combine) may get
+    // resident at once; it waits for this grid in turn. With kv_stable the
+    // caller has promised that positions and the attended cache rows are not
+    // written by anything still running, so the wait moves to just before q
+    // is read, after the first K/V copies are in flight.
+    const bool stable = a.kv_stable != 0;
+    if (tid == NWC * 32) {
+        // q of this block's query heads into L2 while the previous grid runs
+        // (query rows t0..t1 hold the block's (row, group head) pairs)
+        const uint32_t gbytes = (uint32_t)(G * HD * sizeof(float));
+        const int t0 = qg * NQH / G, t1 = min(a.n_q - 1, (qg * NQH + NQH - 1) / G);
+        for (int t = t0; t <= t1; ++t)
+            prefetch_l2(a.q + (((size_t)s * a.n_q + t) * a.n_head + (size_t)hk * G) * HD, gbytes);
+    }
+    if (!stable) pdl_wait();
     pdl_launch_dependents();
 
     // a1: rows attended and this split's range; an empty split leaves at once
@@ -95,6 +110,7 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     int64_t lo, hi;
     split_range(nkv, sp, P, a.split_len, WR, lo, hi);
     if (lo >= hi) {                                                      // empty split: mx=-inf, S=0
+        if (stable) pdl_wait();               // the workspace may still be read by the previous grid
         if (tid < NQH) {
             const int hp = Warp::slot_head(a, hk, qg, tid);
             if (hp >= 0) a.ws_ml[((size_t)s * heads + hp) * P + sp] = make_float2(-INFINITY, 0.f);
@@ -138,6 +154,7 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         flags[1] = early;
     }
     // a2, while the first tiles are in flight
+    if (stable) pdl_wait();
     Warp::template prepare<Cfg::THREADS>(extra, a, s, hk, qg, tid);
     __syncthreads();
     early = flags[1];
@@ -208,7 +225,7 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
             for (int j = 0; j < NJ; ++j) {
                 const int i = lane + 32 * j;
                 if (i < 2 * NU)
-                    newrow[j] = __ldg(reinterpret_cast<const uint4 *>((i < NU ? a.k_new : a.v_new) + src) +
+                    newrow[j] = ld_dep(reinterpret_cast<const uint4 *>((i < NU ? a.k_new : a.v_new) + src) +
                                       (i < NU ? i : i - NU));
             }
         }
@@ -252,12 +269,13 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         asm volatile("bar.sync 1, %0;" :: "r"(NWC * 32) : "memory");
         if (!__shfl_sync(0xffffffffu, flags[0], 0))
             wst.publish(reinterpret_cast<float2 *>(smem) + warp * NQH,
-                        reinterpret_cast<float *>(smem) + 2 * NWC * NQH + warp * NQH * HD, lane);
+                        reinterpret_cast<float *>(smem) + 2 * NWC * NQH + warp * NQH * Cfg::MS, lane);
     }
     __syncthreads();
 
     // Drain: no copy may still be writing shared memory when the block exits.
-    if (tid == NWC * 32) {
+    // Without an abort the compute warps have waited for every issued tile.
+    if (tid == NWC * 32 && flags[0]) {
         const int issued = flags[1];
         for (int t = issued - S > 0 ? issued - S : 0; t < issued; ++t)
             (void)mbar_wait_bounded(full + (t % S), (t / S) & 1);
@@ -266,27 +284,46 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
 
     // a6: merge the NWC warp states and write the partial triple of each head
     // (a query head no warp saw a row for -- possible with causal limits --
-    // keeps mx = -inf and S = 0)
+    // keeps mx = -inf and S = 0). First one thread per head takes the maximum
+    // and the NWC weights, then all threads scale and add the accumulators in
+    // float4 units.
     const float2 *mm = reinterpret_cast<const float2 *>(smem);
     const float *mo = reinterpret_cast<const float *>(smem) + 2 * NWC * NQH;
-    for (int i = tid; i < NQH * HD; i += Cfg::THREADS) {
-        const int g = i / HD, d = i % HD;
-        const int hp = Warp::slot_head(a, hk, qg, g);
-        if (hp < 0) continue;
+    float *wts = reinterpret_cast<float *>(smem) + Cfg::OFF_WTS;
+    if (tid < NQH) {
+        const int g = tid;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < NWC; ++w) M = fmaxf(M, mm[w * NQH + g].x);
-        float O = 0.f, L = 0.f;
+        float L = 0.f;
 #pragma unroll
         for (int w = 0; w < NWC; ++w) {
             const float2 ml = mm[w * NQH + g];
             const float wt = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
-            O = fmaf(wt, mo[(w * NQH + g) * HD + d], O);
+            wts[w * NQH + g] = wt;
             L = fmaf(wt, ml.y, L);
         }
+        const int hp = Warp::slot_head(a, hk, qg, g);
+        if (hp >= 0) a.ws_ml[((size_t)s * heads + hp) * P + sp] = make_float2(M, L);
+    }
+    __syncthreads();
+    constexpr int D4 = HD / 4;
+    for (int i = tid; i < NQH * D4; i += Cfg::THREADS) {
+        const int g = i / D4, d = (i % D4) * 4;
+        const int hp = Warp::slot_head(a, hk, qg, g);
+        if (hp < 0) continue;
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < NWC; ++w) {
+            const float wt = wts[w * NQH + g];
+            const float4 v = *reinterpret_cast<const float4 *>(mo + (w * NQH + g) * Cfg::MS + d);
+            O.x = fmaf(wt, v.x, O.x);
+            O.y = fmaf(wt, v.y, O.y);
+            O.z = fmaf(wt, v.z, O.z);
+            O.w = fmaf(wt, v.w, O.w);
+        }
         const size_t slot = ((size_t)s * heads + hp) * P + sp;
-        a.ws_o[slot * HD + d] = O;
-        if (d == 0) a.ws_ml[slot] = make_float2(M, L);
+        *reinterpret_cast<float4 *>(a.ws_o + slot * HD + d) = O;
     }
 }
 

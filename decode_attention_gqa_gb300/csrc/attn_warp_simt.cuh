@@ -52,7 +52,7 @@ struct SimtWarp {
 #pragma unroll
         for (int it = 0; it < ITER; ++it) {
             const int i = tid + it * NTHREADS;
-            if (i < N4) t[it] = __ldg(src + i);
+            if (i < N4) t[it] = ld_dep(src + i);
         }
 #pragma unroll
         for (int it = 0; it < ITER; ++it) {
@@ -183,7 +183,7 @@ struct SimtWarp {
 #pragma unroll
             for (int g = 0; g < G; ++g)
 #pragma unroll
-                for (int d = 0; d < DPL; ++d) mo[g * HD + lane * DPL + d] = o[g][d];
+                for (int d = 0; d < DPL; ++d) mo[g * merge_stride<HD>() + lane * DPL + d] = o[g][d];
         }
     }
 };

@@ -75,7 +75,7 @@ struct TcWarp {
 #pragma unroll
             for (int i = 0; i < PER; ++i) {
                 const int d = lane + 32 * i;
-                x[it][i] = (g < G && d < HD) ? __ldg(qg + g * HD + d) * qscale : 0.f;
+                x[it][i] = (g < G && d < HD) ? ld_dep(qg + g * HD + d) * qscale : 0.f;
             }
         }
 #pragma unroll
@@ -215,9 +215,10 @@ struct TcWarp {
     }
 
     // mm[g] = (mx, S) in the partial's convention (mx is the reference the p's
-    // were taken against), mo[g * HD + d] = oc.
+    // were taken against), mo[g * merge_stride + d] = oc.
     __device__ __forceinline__ void publish(float2 *mm, float *mo, int lane)
     {
+        constexpr int MS = merge_stride<HD>();
         float lt = l;
         lt += __shfl_xor_sync(0xffffffffu, lt, 1);
         lt += __shfl_xor_sync(0xffffffffu, lt, 2);
@@ -225,10 +226,9 @@ struct TcWarp {
         if (g < G) {
             if (t == 0) mm[g] = make_float2(m_ref - OFF, lt);
 #pragma unroll
-            for (int n = 0; n < NTD; ++n) {
-                mo[g * HD + n * 8 + 2 * t] = o[n][0] + o[n][2];
-                mo[g * HD + n * 8 + 2 * t + 1] = o[n][1] + o[n][3];
-            }
+            for (int n = 0; n < NTD; ++n)
+                *reinterpret_cast<float2 *>(mo + g * MS + n * 8 + 2 * t) =
+                    make_float2(o[n][0] + o[n][2], o[n][1] + o[n][3]);
         }
     }
 };

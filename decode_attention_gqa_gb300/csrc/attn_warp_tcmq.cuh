@@ -70,7 +70,7 @@ struct TcWarpMQ {
 #pragma unroll
             for (int k = 0; k < PER; ++k) {
                 const int d = lane + 32 * k;
-                x[it][k] = (qrow_p && d < HD) ? __ldg(qrow_p + d) * a.qscale : 0.f;
+                x[it][k] = (qrow_p && d < HD) ? ld_dep(qrow_p + d) * a.qscale : 0.f;
             }
         }
 #pragma unroll
@@ -248,10 +248,9 @@ struct TcWarpMQ {
             if (h < QH) {
                 if (u == 0) mm[h] = make_float2(m_ref[k] - OFF, lt);
 #pragma unroll
-                for (int n = 0; n < NTD; ++n) {
-                    mo[h * HD + n * 8 + 2 * u] = o[n][2 * k];
-                    mo[h * HD + n * 8 + 2 * u + 1] = o[n][2 * k + 1];
-                }
+                for (int n = 0; n < NTD; ++n)
+                    *reinterpret_cast<float2 *>(mo + h * merge_stride<HD>() + n * 8 + 2 * u) =
+                        make_float2(o[n][2 * k], o[n][2 * k + 1]);
             }
         }
     }

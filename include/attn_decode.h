@@ -80,6 +80,21 @@ typedef enum {
    fraction bits). k_new / v_new of attn_decode_append use the same type. */
 #define ATTN_KV_BF16 0x10
 
+/* Early start, OR'd into the variant argument. Every launch of this library
+   is a programmatic dependent launch: its blocks may become resident while the
+   kernel before it on the stream still runs, and wait for that kernel to end
+   before the first read of anything it could have written. With this flag the
+   caller promises that `positions` and the cache rows the call attends (rows
+   below positions[s], and row positions[s] itself unless attn_decode_append
+   supplies it) are written by nothing that can still be running when the call
+   is launched -- in a decode step, true for every attention layer after the
+   first once positions has been advanced. The partial kernel then reads
+   positions and starts its K/V copies before that wait, so the cache stream
+   of this layer overlaps the tail of the previous kernel. q, k_new, v_new
+   and the workspace are still touched only after the wait. Breaking the
+   promise gives stale rows, not a fault: all reads stay inside the cache. */
+#define ATTN_KV_STABLE 0x20
+
 /*
  * attn_decode -- one layer call, single sequence, library-owned workspace.
  *
@@ -101,7 +116,8 @@ attn_status attn_decode(const float *q, const void *k_cache, const void *v_cache
 /*
  * attn_decode_ex -- full control.
  *   cap             cache rows per sequence (>= 1); nkv_s is clamped to cap.
- *   n_splits        splits P per (sequence, KV head); 0 = attn_split_heuristic().
+ *   n_splits        splits P per (sequence, KV head); 0 = attn_split_heuristic_ex()
+ *                   for this call's variant.
  *   split_len       0: split by count, chunk = ceil(nkv / P) rounded up to the
  *                   kernel's row granule, 16 rows (tensor cores) or 32 rows
  *                   (CUDA cores) (minfer R4 §2.2); > 0: fixed block of split_len
@@ -223,13 +239,26 @@ attn_status attn_decode_static(const float *q, const void *k_cache, const void *
 /*
  * attn_split_heuristic -- host-only, static split count P for a launch.
  * Chooses P from the shape and the static capacity (never from nkv, which lives
- * on the device) so that (P x n_kv_head x n_seq) blocks fill about two waves of
- * sm_count SMs while each split keeps at least one kernel tile of rows at full
- * capacity. cap <= 0 means "unknown". sm_count <= 0 queries the current device
- * (and returns 0 with no device).
+ * on the device). With the capacity known, the chunk is sized so that at full
+ * capacity the (sequence, KV head) units fill one wave of resident blocks for a
+ * single sequence, eight waves for a batch (whose ragged lengths then balance),
+ * rounded up to the kernel's row granule; P = ceil(cap / chunk). cap <= 0
+ * means "unknown": one wave. sm_count <= 0 queries the current device (and
+ * returns 0 with no device). The same rule serves attn_decode_ex's n_splits = 0.
  */
 int attn_split_heuristic(int n_seq, int n_head, int n_kv_head, int head_dim, int64_t cap,
                          int sm_count);
+
+/*
+ * attn_split_heuristic_ex -- the same, for the call's variant argument
+ * (ATTN_VARIANT_*, ATTN_KV_BF16, ATTN_KV_STABLE). With ATTN_KV_STABLE, a
+ * single sequence and a short call (at most 4 kernel tiles of rows per block
+ * at one block per SM) the wave is one block per SM rather than as many as
+ * fit, so that the next flagged call's blocks find room beside this call's
+ * and start their copies while it finishes. Returns 0 for an invalid variant.
+ */
+int attn_split_heuristic_ex(int n_seq, int n_head, int n_kv_head, int head_dim, int64_t cap,
+                            int sm_count, int variant);
 
 /* attn_workspace_size -- bytes of workspace attn_decode_ex needs (host-only). */
 size_t attn_workspace_size(int n_seq, int n_head, int head_dim, int n_splits);

@@ -38,6 +38,23 @@ def test_header_declares_the_boundary():
         assert want in names
 
 
+def test_binding_constants_match_the_header():
+    """Every ATTN_* macro and enumerator of the header has the same value in the binding."""
+    text = open(os.path.join(ROOT, "include", "attn_decode.h")).read()
+    found = 0
+    for m in re.finditer(r"^#define (ATTN_\w+)\s+(0x[0-9a-fA-F]+|\d+)u?\b", text, flags=re.M):
+        name, val = m.group(1), int(m.group(2), 0)
+        if name in ("ATTN_STATIC_SCRATCH_BYTES",) or not hasattr(pkg, name):
+            continue
+        assert getattr(pkg, name) == val, name
+        found += 1
+    for m in re.finditer(r"^\s*(ATTN_(?:OK|ERR_\w+))\s*=\s*(\d+)", text, flags=re.M):
+        assert getattr(pkg, m.group(1)) == int(m.group(2)), m.group(1)
+        found += 1
+    assert found >= 12
+    assert pkg.ATTN_KV_STABLE & pkg.ATTN_KV_BF16 == 0
+
+
 def test_every_declared_symbol_is_exported(lib):
     raw = ctypes.CDLL(pkg.library_path())
     for name in declared_functions():
@@ -76,6 +93,25 @@ def test_split_heuristic_host_only(lib):
     assert pkg.attn_split_heuristic(1, 28, 5, 128, 8192, 152) == 0
     assert pkg.attn_split_heuristic(1, 18, 2, 128, 8192, 152) == 0      # group 9
     assert pkg.attn_split_heuristic(1, 8, 2, 96, 8192, 152) == 0        # head_dim 96
+
+
+def test_split_heuristic_for_flagged_calls(lib):
+    h = pkg.attn_split_heuristic_ex
+    # the plain call and variant 0 agree; the element type does not change P
+    assert h(1, 28, 4, 128, 8192, 152, 0) == pkg.attn_split_heuristic(1, 28, 4, 128, 8192, 152)
+    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_BF16) == 74
+    # early start, one sequence: one block per SM -> 4 x 37 blocks of 224 rows
+    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_STABLE) == 37
+    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_STABLE | pkg.ATTN_KV_BF16) == 37
+    # a long call keeps every resident block: 131072 rows x 8 KV heads
+    assert h(1, 64, 8, 128, 131072, 152, pkg.ATTN_KV_STABLE) == h(1, 64, 8, 128, 131072, 152, 0) == 38
+    # a batch keeps its eight waves
+    assert h(32, 32, 8, 128, 32768, 152, pkg.ATTN_KV_STABLE) == 10
+    # head_dim 256 already runs one block per SM
+    assert h(1, 16, 2, 256, 8400, 152, pkg.ATTN_KV_STABLE) == h(1, 16, 2, 256, 8400, 152, 0) == 75
+    # the CUDA-core kernel has its own granule and residency
+    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_VARIANT_SIMT) >= 1
+    assert h(1, 28, 4, 128, 8192, 152, 7) == 0                           # no such variant
 
 
 def _ex(lib, **kw):

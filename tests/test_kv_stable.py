@@ -1,0 +1,168 @@
+"""GPU: ATTN_KV_STABLE (early start). Layers after the first read positions and
+start their K/V copies before the previous kernel on the stream has ended;
+q, k_new and the workspace must still wait for it. The chains below make any
+early read of those visible: layer l + 1 takes the previous layer's output as
+its q (written by the combine kernel just before it, NaN until then), and all
+layers share one workspace (the flagged partial kernel overwrites what the
+previous combine reads). The expected values are the oracle's own chain, with
+its f32-rounded output as the next layer's q."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from harness import assert_close, make_case, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import decode_attention_gqa_gb300 as p
+    from decode_attention_gqa_gb300 import build
+    build.build()
+    p.load()
+    return p
+
+
+def _oracle_chain(q0, layers, positions, n_head, n_kv, hd, cap, scale, kv_dtype="f16"):
+    outs, q = [], q0
+    for lay in layers:
+        o = oracle.attn_decode(q, lay["k"], lay["v"], positions, n_head, n_kv, hd, cap, scale,
+                               n_threads=8, kv_dtype=kv_dtype)
+        outs.append(o)
+        q = o.astype(np.float32)
+    return outs
+
+
+def _chain(pkg, L, n_head, n_kv, hd, cap, ctx, P, blk, variant, graph, replays, seed, stable=True):
+    import torch
+    n_seq = len(ctx)
+    layers = [make_case(seed + l, n_seq, n_head, n_kv, hd, cap, ctx) for l in range(L)]
+    dev = [to_device(c) for c in layers]
+    q0 = torch.from_numpy(layers[0]["q"]).cuda()
+    pos = torch.from_numpy(layers[0]["positions"] - 1).cuda()      # the step adds 1
+    outs = [torch.empty_like(q0) for _ in range(L)]
+    scale = 1 / math.sqrt(hd)
+    P = P or pkg.attn_split_heuristic(n_seq, n_head, n_kv, hd, cap, 0)
+    ws_bytes = pkg.attn_workspace_size(n_seq, n_head, hd, P)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    pkg.attn_read_device_error()                     # clear what earlier tests left
+
+    def step():
+        pos.add_(1)
+        for l in range(L):
+            var = variant | (pkg.ATTN_KV_STABLE if stable and l > 0 else 0)
+            pkg.attn_decode_ex(q0 if l == 0 else outs[l - 1], dev[l]["k"], dev[l]["v"], pos,
+                               outs[l], n_seq, n_head, n_kv, hd, scale, cap, n_splits=P,
+                               split_len=blk, variant=var, workspace=ws, workspace_bytes=ws_bytes,
+                               stream=s)
+
+    g = None
+    if graph:
+        with torch.cuda.stream(s):
+            step()                                   # uncaptured warm-up of the launch path
+        torch.cuda.synchronize()
+        pos.sub_(1)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            step()
+        torch.cuda.synchronize()
+    for r in range(replays):
+        for o in outs:
+            o.fill_(float("nan"))
+        torch.cuda.synchronize()
+        if graph:
+            with torch.cuda.stream(s):
+                g.replay()
+        else:
+            with torch.cuda.stream(s):
+                step()
+        torch.cuda.synchronize()
+        positions = pos.cpu().numpy()
+        ref = _oracle_chain(layers[0]["q"], layers, positions, n_head, n_kv, hd, cap, scale)
+        for l in range(L):
+            assert_close(outs[l].cpu().numpy(), ref[l], "layer %d replay %d" % (l, r))
+    flags = pkg.attn_read_device_error()
+    assert flags == 0
+
+
+@pytest.mark.parametrize("graph, stable", [(False, True), (True, True), (True, False)])
+def test_stable_chain_7b_shape(pkg, graph, stable):
+    # stable=False: the same chain without the flag (every read after the wait)
+    _chain(pkg, L=5, n_head=28, n_kv=4, hd=128, cap=2048, ctx=(1900,), P=0, blk=0, variant=0,
+           graph=graph, replays=3, seed=900, stable=stable)
+
+
+@pytest.mark.parametrize("P, blk", [(1, 0), (19, 0), (40, 64)])
+def test_stable_chain_split_choices(pkg, P, blk):
+    # P = 40 with 64-row blocks at nkv ~ 1000: the later splits are empty
+    _chain(pkg, L=4, n_head=16, n_kv=2, hd=256, cap=2560, ctx=(1000,), P=P, blk=blk, variant=0,
+           graph=True, replays=2, seed=910)
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+def test_stable_chain_ragged_batch(pkg, variant):
+    _chain(pkg, L=3, n_head=32, n_kv=8, hd=128, cap=700, ctx=(1, 699, 17, 450, 0, 333),
+           P=0, blk=0, variant=variant, graph=True, replays=2, seed=920)
+
+
+def test_stable_append_chain(pkg):
+    """Flagged appends: the new row still comes from k_new / v_new, which the
+    kernel reads only after the wait."""
+    import torch
+    L, n_head, n_kv, hd, cap, nkv = 3, 28, 4, 128, 1024, 777
+    layers = [make_case(930 + l, 1, n_head, n_kv, hd, cap, (nkv,)) for l in range(L)]
+    dev = [to_device(c) for c in layers]
+    rng = np.random.Generator(np.random.PCG64(931))
+    kn = [rng.standard_normal((1, n_kv, hd), dtype=np.float32).astype(np.float16) for _ in range(L)]
+    vn = [rng.standard_normal((1, n_kv, hd), dtype=np.float32).astype(np.float16) for _ in range(L)]
+    kn_d = [torch.from_numpy(x).cuda() for x in kn]
+    vn_d = [torch.from_numpy(x).cuda() for x in vn]
+    q0 = torch.from_numpy(layers[0]["q"]).cuda()
+    pos = torch.from_numpy(layers[0]["positions"]).cuda()
+    outs = [torch.full_like(q0, float("nan")) for _ in range(L)]
+    P = 24
+    ws_bytes = pkg.attn_workspace_size(1, n_head, hd, P)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for l in range(L):
+            pkg.attn_decode_append(q0 if l == 0 else outs[l - 1], kn_d[l], vn_d[l], dev[l]["k"],
+                                   dev[l]["v"], pos, outs[l], 1, n_head, n_kv, hd, 1 / math.sqrt(hd),
+                                   cap, n_splits=P, variant=pkg.ATTN_KV_STABLE if l else 0,
+                                   workspace=ws, workspace_bytes=ws_bytes, stream=s)
+    torch.cuda.synchronize()
+    for l in range(L):
+        layers[l]["k"][0, nkv - 1] = kn[l][0]
+        layers[l]["v"][0, nkv - 1] = vn[l][0]
+    ref = _oracle_chain(layers[0]["q"], layers, layers[0]["positions"], n_head, n_kv, hd, cap,
+                        1 / math.sqrt(hd))
+    for l in range(L):
+        assert_close(outs[l].cpu().numpy(), ref[l], "append layer %d" % l)
+        np.testing.assert_array_equal(dev[l]["k"].cpu().numpy(), layers[l]["k"])
+
+
+def test_stable_flag_accepted_with_every_entry_point(pkg):
+    import torch
+    n_head, n_kv, hd, cap = 8, 2, 128, 300
+    case = make_case(940, 1, n_head, n_kv, hd, cap, (250,))
+    d = to_device(case)
+    ref = oracle.attn_decode(case["q"], case["k"], case["v"], case["positions"], n_head, n_kv, hd,
+                             cap, 0.1)
+    out = torch.full_like(d["q"], float("nan"))
+    pkg.attn_decode_static(d["q"], d["k"], d["v"], d["positions"], out, 1, n_head, n_kv, hd, 0.1,
+                           cap, variant=pkg.ATTN_KV_STABLE)
+    torch.cuda.synchronize()
+    assert_close(out.cpu().numpy(), ref, "static + stable")
+    qm = torch.from_numpy(np.repeat(case["q"][:, None], 2, axis=1)).cuda()
+    outm = torch.full_like(qm, float("nan"))
+    pkg.attn_decode_multi(qm, d["k"], d["v"], d["positions"], outm, 1, 2, n_head, n_kv, hd, 0.1,
+                          cap, variant=pkg.ATTN_KV_STABLE)
+    torch.cuda.synchronize()
+    assert_close(outm.cpu().numpy()[:, 1], ref, "multi + stable, last query row")
