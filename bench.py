@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--kv-dtype", choices=["f16", "bf16"], default="f16")
     ap.add_argument("--append", action="store_true",
                     help="time attn_decode_append (write the new K/V row, then attend)")
+    ap.add_argument("--n-q", type=int, default=1,
+                    help="causal query rows per sequence (> 1: attn_decode_multi)")
     ap.add_argument("--kv-stable", choices=["on", "off"], default="on",
                     help="flag layers after the first with ATTN_KV_STABLE (their cache and "
                          "positions are not written inside the step)")
@@ -191,10 +193,11 @@ class ClockSampler:
 
 # ------------------------------------------------------------ CPU oracle leg
 
-def oracle_sample(layers_host, w, budget_s: float, max_units=None, kv_dtype="f16"):
+def oracle_sample(layers_host, w, budget_s: float, max_units=None, kv_dtype="f16", n_q=1):
     """Run the oracle on all host cores over (layer, KV head group) units of the
     workload -- every query head of one KV head against that head's rows -- until
-    budget_s (or max_units); return (GB/s of K+V, units, seconds, threads, what)."""
+    budget_s (or max_units); return (GB/s of K+V, units, seconds, threads, what).
+    With n_q > 1 the unit holds all n_q causal query rows of the group."""
     import numpy as np
     import oracle
     threads = len(os.sched_getaffinity(0))
@@ -204,11 +207,16 @@ def oracle_sample(layers_host, w, budget_s: float, max_units=None, kv_dtype="f16
     while True:
         l, hk = units[done % len(units)]
         lay = layers_host[l]
-        qg = np.ascontiguousarray(lay["q"][:, hk * G:(hk + 1) * G])
         kg = np.ascontiguousarray(lay["k"][:, :, hk:hk + 1])
         vg = np.ascontiguousarray(lay["v"][:, :, hk:hk + 1])
-        oracle.attn_decode(qg, kg, vg, lay["positions"], G, 1, w.head_dim, w.cap, w.scale,
-                           n_threads=threads, kv_dtype=kv_dtype)
+        if n_q > 1:
+            qg = np.ascontiguousarray(lay["q"][:, :, hk * G:(hk + 1) * G])
+            oracle.attn_decode_multi(qg, kg, vg, lay["positions"], n_q, G, 1, w.head_dim, w.cap,
+                                     w.scale, n_threads=threads, kv_dtype=kv_dtype)
+        else:
+            qg = np.ascontiguousarray(lay["q"][:, hk * G:(hk + 1) * G])
+            oracle.attn_decode(qg, kg, vg, lay["positions"], G, 1, w.head_dim, w.cap, w.scale,
+                               n_threads=threads, kv_dtype=kv_dtype)
         nbytes += sum(min(max(int(p) + 1, 0), w.cap) for p in lay["positions"]) * w.head_dim * 4
         done += 1
         el = time.perf_counter() - t0
@@ -282,14 +290,20 @@ def run_ours(args, rank, world, local):
     s = torch.cuda.Stream(device=dev)
     variant = args.variant | (pkg.ATTN_KV_BF16 if args.kv_dtype == "bf16" else 0)
 
+    n_q = args.n_q
+    if n_q > 1:
+        if args.append:
+            raise SystemExit("--n-q > 1 and --append do not combine (attn_decode_multi has no append)")
+        for l, h in enumerate(host):
+            h["q"] = syn.make_q_multi(w, n_q, layer=l)
     q = [torch.from_numpy(h["q"]).to(dev) for h in host]
     kc = [_t(h["k"]).to(dev) for h in host]
     vc = [_t(h["v"]).to(dev) for h in host]
     out = [torch.empty_like(x) for x in q]
     pos = torch.from_numpy(host[0]["positions"].copy()).to(dev)
-    kvt = torch.bfloat16 if args.kv_dtype == "bf16" else torch.float16
-    kn = [torch.randn(n_seq, w.n_kv_head, w.head_dim, device=dev).to(kvt) for _ in range(L)]
-    vn = [torch.randn(n_seq, w.n_kv_head, w.head_dim, device=dev).to(kvt) for _ in range(L)]
+    new_rows = [syn.make_new_rows(w, l, args.kv_dtype) for l in range(L)] if args.append else []
+    kn = [_t(r[0]).to(dev) for r in new_rows]
+    vn = [_t(r[1]).to(dev) for r in new_rows]
     torch.cuda.synchronize()
 
     def kv_bytes_for(nkvs):
@@ -301,11 +315,13 @@ def run_ours(args, rank, world, local):
 
         def __init__(self, P, blk):
             self.P, self.blk = P, blk
-            self.ws_bytes = pkg.attn_workspace_size(n_seq, w.n_head, w.head_dim, P)
+            self.ws_bytes = pkg.attn_workspace_size(n_seq, n_q * w.n_head, w.head_dim, P)
             self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
             self.g_full = self._capture(advance, "full")
-            self.g_partial = self._capture(False, "partial")
-            self.g_combine = self._capture(False, "combine")
+            # the stage entry points serve one query row; with n_q > 1 the
+            # whole call stands for the kernel pair
+            self.g_partial = self._capture(False, "partial") if n_q == 1 else None
+            self.g_combine = self._capture(False, "combine") if n_q == 1 else None
 
         def _calls(self, stream, stage):
             for l in range(L):
@@ -317,6 +333,12 @@ def run_ours(args, rank, world, local):
                     pkg.attn_decode_partial(q[l], kc[l], vc[l], pos, n_seq, w.n_head, w.n_kv_head,
                                             w.head_dim, w.scale, w.cap, self.P, self.blk,
                                             var, self.ws, self.ws_bytes, stream=stream)
+                elif n_q > 1:
+                    pkg.attn_decode_multi(q[l], kc[l], vc[l], pos, out[l], n_seq, n_q, w.n_head,
+                                          w.n_kv_head, w.head_dim, w.scale, w.cap,
+                                          n_splits=self.P, split_len=self.blk, variant=var,
+                                          workspace=self.ws, workspace_bytes=self.ws_bytes,
+                                          stream=stream)
                 elif args.append:
                     pkg.attn_decode_append(q[l], kn[l], vn[l], kc[l], vc[l], pos, out[l], n_seq,
                                            w.n_head, w.n_kv_head, w.head_dim, w.scale, w.cap,
@@ -380,10 +402,15 @@ def run_ours(args, rank, world, local):
         final = nkv_steps[-1]
         if advance:
             pos.fill_(final[0] - 1)
-        warm(plan.g_partial)
-        ms_p, _ = timed_replays(plan.g_partial, K)
-        warm(plan.g_combine)
-        ms_c, _ = timed_replays(plan.g_combine, K)
+        if plan.g_partial is not None:
+            warm(plan.g_partial)
+            ms_p, _ = timed_replays(plan.g_partial, K)
+            warm(plan.g_combine)
+            ms_c, _ = timed_replays(plan.g_combine, K)
+        else:
+            warm(plan.g_full)
+            ms_p, _ = timed_replays(plan.g_full, K)
+            ms_c = 0.0
         return {"ms": ms, "clk": clk, "bytes": sum(step_bytes) * world,
                 "partial_us": ms_p * 1e3 / (K * L), "combine_us": ms_c * 1e3 / (K * L),
                 "launch_bytes": kv_bytes_for(final)}
@@ -395,7 +422,7 @@ def run_ours(args, rank, world, local):
     elif blk0:
         P0 = -(-w.cap // blk0)
     else:
-        P0 = pkg.attn_split_heuristic_ex(n_seq, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0,
+        P0 = pkg.attn_split_heuristic_ex(n_seq, n_q, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0,
                                          variant | (pkg.ATTN_KV_STABLE
                                                     if args.kv_stable == "on" and L > 1 else 0))
     plan = Plan(P0, blk0)
@@ -405,18 +432,36 @@ def run_ours(args, rank, world, local):
     value = m0["bytes"] / (m0["ms"] * 1e-3) / 1e9
     us_per_layer = m0["ms"] * 1e3 / (K * L)
 
-    # correctness spot check of layer 0 at the final nkv (oracle)
+    # correctness spot check of layer 0 at the final nkv (oracle). Its inputs
+    # are the host copies: for the fused append, layer 0's cache is restored
+    # from the host first and the expected cache is built on the host from the
+    # original rows and k_new / v_new.
     import oracle
     torch.cuda.synchronize()
     pos_now = pos.cpu().numpy()
+    lay0 = dict(host[0], positions=pos_now)
+    if args.append:
+        kc[0].copy_(_t(host[0]["k"]).to(dev))
+        vc[0].copy_(_t(host[0]["v"]).to(dev))
+        torch.cuda.synchronize()
+        lay0["k"], lay0["v"] = host[0]["k"].copy(), host[0]["v"].copy()
+        kn0, vn0 = new_rows[0]
+        for si in range(n_seq):
+            r = int(pos_now[si])
+            if 0 <= r < w.cap:
+                lay0["k"][si, r] = kn0[si]
+                lay0["v"][si, r] = vn0[si]
     with torch.cuda.stream(s):
         plan._calls(s, "full")
     torch.cuda.synchronize()
-    lay0 = dict(host[0], positions=pos_now)
-    if args.append:                      # the cache now holds appended rows: compare with it
-        lay0["k"] = kc[0].cpu().view(torch.int16).numpy().view(np.uint16)
-        lay0["v"] = vc[0].cpu().view(torch.int16).numpy().view(np.uint16)
-    if n_seq == 1:
+    if n_q > 1:
+        ref = oracle.attn_decode_multi(lay0["q"], lay0["k"], lay0["v"], lay0["positions"], n_q,
+                                       w.n_head, w.n_kv_head, w.head_dim, w.cap, w.scale,
+                                       n_threads=8, kv_dtype=args.kv_dtype)
+        got = out[0].cpu().numpy().astype(np.float64)
+        if n_seq > 1:
+            ref, got = ref[:3], got[:3]
+    elif n_seq == 1:
         ref = oracle.attn_decode(lay0["q"], lay0["k"], lay0["v"], lay0["positions"], w.n_head,
                                  w.n_kv_head, w.head_dim, w.cap, w.scale, n_threads=8,
                                  kv_dtype=args.kv_dtype)
@@ -433,8 +478,10 @@ def run_ours(args, rank, world, local):
     peak, peak_kind = measured_peak()
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
-                "traffic": profiled_traffic("%s_ctx%d" % (w.name, ctx_end)),
-                "kernel": "attn_split_partial", "bytes_per_launch": m0["launch_bytes"],
+                "traffic": profiled_traffic("%s_ctx%d%s" % (w.name, ctx_end,
+                                                            "_nq%d" % n_q if n_q > 1 else "")),
+                "kernel": "attn_split_partial" if n_q == 1 else "attn_split_partial + attn_combine",
+                "bytes_per_launch": m0["launch_bytes"],
                 "us_per_launch": round(m0["partial_us"], 3),
                 "combine_us_per_launch": round(m0["combine_us"], 3)}
 
@@ -506,7 +553,7 @@ def run_ours(args, rank, world, local):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         rate, done, el, threads, what = oracle_sample(host, w, budget_s=10.0,
-                                                      kv_dtype=args.kv_dtype)
+                                                      kv_dtype=args.kv_dtype, n_q=n_q)
         cpu = {"value": round(rate, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": "%s of the %s workload (%.1f s)" % (what, w.name, el)}
 
@@ -517,11 +564,13 @@ def run_ours(args, rank, world, local):
             "steps": K, "warmup": W, "ms_per_step": round(m0["ms"] / K, 4),
             "us_per_layer": round(us_per_layer, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": describe(w, L), "name": w.name, "ctx": ctx_end, "cap": w.cap,
+            "config": {"workload": describe(w, L) + (", %d causal query rows per sequence" % n_q
+                                                      if n_q > 1 else ""),
+                       "name": w.name, "ctx": ctx_end, "cap": w.cap,
                        "n_seq": n_seq, "n_head": w.n_head, "n_kv_head": w.n_kv_head,
                        "head_dim": w.head_dim, "layers": L, "n_splits": P0, "split_len": blk0,
                        "variant": args.variant, "kv_dtype": args.kv_dtype, "append": args.append,
-                       "kv_stable": args.kv_stable,
+                       "kv_stable": args.kv_stable, "n_q": n_q,
                        "l2": "inputs larger than L2 (%d MB of K+V per step)"
                              % (kv_bytes_for([ctx_end] if advance else w.ctx) * L // 2 ** 20),
                        "parallelism": "replicas" if world > 1 else "single"},

@@ -88,7 +88,7 @@ def load():
         lib.attn_split_heuristic.restype = i32
         lib.attn_split_heuristic.argtypes = [i32, i32, i32, i32, i64, i32]
         lib.attn_split_heuristic_ex.restype = i32
-        lib.attn_split_heuristic_ex.argtypes = [i32, i32, i32, i32, i64, i32, i32]
+        lib.attn_split_heuristic_ex.argtypes = [i32, i32, i32, i32, i32, i64, i32, i32]
         lib.attn_workspace_size.restype = sz
         lib.attn_workspace_size.argtypes = [i32, i32, i32, i32]
         lib.attn_read_device_error.restype = i32
@@ -213,8 +213,8 @@ def attn_split_heuristic(n_seq, n_head, n_kv_head, head_dim, cap, sm_count) -> i
     return load().attn_split_heuristic(n_seq, n_head, n_kv_head, head_dim, cap, sm_count)
 
 
-def attn_split_heuristic_ex(n_seq, n_head, n_kv_head, head_dim, cap, sm_count, variant) -> int:
-    return load().attn_split_heuristic_ex(n_seq, n_head, n_kv_head, head_dim, cap, sm_count,
+def attn_split_heuristic_ex(n_seq, n_q, n_head, n_kv_head, head_dim, cap, sm_count, variant) -> int:
+    return load().attn_split_heuristic_ex(n_seq, n_q, n_head, n_kv_head, head_dim, cap, sm_count,
                                           variant)
 
 

@@ -72,14 +72,14 @@ cudaError_t device_state(int dev, DeviceState **out)
     return cudaSuccess;
 }
 
-attn::KernelInfo kernel_info(int head_dim, int group, int variant)
+attn::KernelInfo kernel_info(int head_dim, int group, int variant, bool multi = false)
 {
     switch (head_dim) {
-    case 8: return attn::kernel_info_hd8(group, variant);
-    case 64: return attn::kernel_info_hd64(group, variant);
-    case 128: return attn::kernel_info_hd128(group, variant);
-    case 256: return attn::kernel_info_hd256(group, variant);
-    default: return attn::KernelInfo{0, 0, false};
+    case 8: return attn::kernel_info_hd8(group, variant, multi);
+    case 64: return attn::kernel_info_hd64(group, variant, multi);
+    case 128: return attn::kernel_info_hd128(group, variant, multi);
+    case 256: return attn::kernel_info_hd256(group, variant, multi);
+    default: return attn::KernelInfo{0, 0, 0, false};
     }
 }
 
@@ -101,14 +101,15 @@ int resolve_variant(int variant, int head_dim, int group)
 // `waves` waves of resident blocks -- one wave for a single sequence, eight for
 // a batch whose lengths may be ragged, so blocks of unequal work still balance
 // -- round it up to the kernel's row granule and take P = ceil(cap / chunk).
-// Without it: one wave. With kv_stable, one sequence and a short call (at one
-// block per SM each block's rows fit in a few tiles, so the launch is bound by
-// latency rather than bandwidth) the wave is one block per SM, leaving room
-// for the next flagged call's blocks.
-int heuristic(int n_seq, int n_kv_head, int64_t cap, int sm_count, const attn::KernelInfo &ki,
-              bool kv_stable)
+// Without it: one wave. A unit is one (sequence, KV head, query group) block
+// column. With kv_stable, one sequence and a short call (at one block per SM
+// each block's rows fit in a few tiles, so the launch is bound by latency
+// rather than bandwidth) the wave is one block per SM, leaving room for the
+// next flagged call's blocks.
+int heuristic(int n_seq, int n_kv_head, int qgroups, int64_t cap, int sm_count,
+              const attn::KernelInfo &ki, bool kv_stable)
 {
-    const int64_t units = (int64_t)n_seq * n_kv_head;
+    const int64_t units = (int64_t)n_seq * n_kv_head * (qgroups > 0 ? qgroups : 1);
     int per_sm = ki.blocks_per_sm > 0 ? ki.blocks_per_sm : 1;
     if (kv_stable && n_seq == 1 && cap > 0 && sm_count > 0 &&
         (cap * units + sm_count - 1) / sm_count <= (int64_t)kStableTiles * ki.tile_rows)
@@ -163,7 +164,7 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     const int v = resolve_variant(variant, head_dim, group);
     const int qgroups = (n_q * group + attn::kMqHeadsPerBlock - 1) / attn::kMqHeadsPerBlock;
     if (n_q > 1 && (int64_t)n_kv_head * qgroups > 65535) return ATTN_ERR_INVALID_ARG;
-    const attn::KernelInfo ki = kernel_info(head_dim, group, v);
+    const attn::KernelInfo ki = kernel_info(head_dim, group, v, n_q > 1);
     if (!ki.available) return ATTN_ERR_UNSUPPORTED;
     if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return ATTN_ERR_INVALID_ARG;
     if (n_seq == 0) return ATTN_OK;
@@ -178,8 +179,8 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     if (e != cudaSuccess) return cuda_fail(e);
 
     const int P = n_splits > 0 ? n_splits
-                               : heuristic(n_seq, n_kv_head, cap_known ? cap : 0, ds->sm_count, ki,
-                                           kv_stable != 0);
+                               : heuristic(n_seq, n_kv_head, n_q > 1 ? qgroups : 1,
+                                           cap_known ? cap : 0, ds->sm_count, ki, kv_stable != 0);
     if (split_len > 0 && (int64_t)P * split_len < cap) return ATTN_ERR_INVALID_ARG;
     const size_t need = attn_workspace_size(n_seq, n_q * n_head, head_dim, P);
 
@@ -416,14 +417,16 @@ attn_status attn_decode_combine(const void *workspace, size_t workspace_bytes, f
     return ATTN_OK;
 }
 
-int attn_split_heuristic_ex(int n_seq, int n_head, int n_kv_head, int head_dim, int64_t cap,
-                            int sm_count, int variant)
+int attn_split_heuristic_ex(int n_seq, int n_q, int n_head, int n_kv_head, int head_dim,
+                            int64_t cap, int sm_count, int variant)
 {
     const bool stable = (variant & ATTN_KV_STABLE) != 0;
     variant &= ~(ATTN_KV_BF16 | ATTN_KV_STABLE);
     if (variant != ATTN_VARIANT_AUTO && variant != ATTN_VARIANT_SIMT && variant != ATTN_VARIANT_TC)
         return 0;
-    if (n_seq <= 0 || n_head <= 0 || n_kv_head <= 0 || n_head % n_kv_head != 0) return 0;
+    if (n_seq <= 0 || n_q < 1 || n_q > 1024 || n_head <= 0 || n_kv_head <= 0 ||
+        n_head % n_kv_head != 0)
+        return 0;
     const int group = n_head / n_kv_head;
     if (!head_dim_supported(head_dim) || group > 8) return 0;
     if (sm_count <= 0) {
@@ -432,15 +435,17 @@ int attn_split_heuristic_ex(int n_seq, int n_head, int n_kv_head, int head_dim, 
         if (cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return 0;
     }
-    const attn::KernelInfo ki = kernel_info(head_dim, group, resolve_variant(variant, head_dim, group));
+    const attn::KernelInfo ki =
+        kernel_info(head_dim, group, resolve_variant(variant, head_dim, group), n_q > 1);
     if (!ki.available) return 0;
-    return heuristic(n_seq, n_kv_head, cap, sm_count, ki, stable);
+    const int qgroups = n_q > 1 ? (n_q * group + attn::kMqHeadsPerBlock - 1) / attn::kMqHeadsPerBlock : 1;
+    return heuristic(n_seq, n_kv_head, qgroups, cap, sm_count, ki, stable);
 }
 
 int attn_split_heuristic(int n_seq, int n_head, int n_kv_head, int head_dim, int64_t cap,
                          int sm_count)
 {
-    return attn_split_heuristic_ex(n_seq, n_head, n_kv_head, head_dim, cap, sm_count,
+    return attn_split_heuristic_ex(n_seq, 1, n_head, n_kv_head, head_dim, cap, sm_count,
                                    ATTN_VARIANT_AUTO);
 }
 

@@ -3,5 +3,5 @@
 
 namespace attn {
 cudaError_t launch_hd64_f16(const LaunchRequest &r) { return launch_for_hd<64, __half>(r); }
-KernelInfo kernel_info_hd64(int group, int variant) { return kernel_info_for_hd<64>(group, variant); }
+KernelInfo kernel_info_hd64(int group, int variant, bool multi) { return kernel_info_for_hd<64>(group, variant, multi); }
 } // namespace attn

@@ -3,5 +3,5 @@
 
 namespace attn {
 cudaError_t launch_hd8_f16(const LaunchRequest &r) { return launch_for_hd<8, __half>(r); }
-KernelInfo kernel_info_hd8(int group, int variant) { return kernel_info_for_hd<8>(group, variant); }
+KernelInfo kernel_info_hd8(int group, int variant, bool multi) { return kernel_info_for_hd<8>(group, variant, multi); }
 } // namespace attn

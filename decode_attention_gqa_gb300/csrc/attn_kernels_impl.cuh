@@ -133,11 +133,12 @@ cudaError_t launch_for_hd(const LaunchRequest &r)
 }
 
 template <int HD>
-KernelInfo kernel_info_for_hd(int group, int variant)
+KernelInfo kernel_info_for_hd(int group, int variant, bool multi)
 {
     KernelInfo k{0, 0, 0, false};
     if (group < 1 || group > 8) return k;
     if (variant == kVariantSimt) {
+        if (multi) return k;
         using C = SimtCfg<HD, 8, __half>;   // the largest group sets the shared-memory need
         k.tile_rows = C::TILE;
         k.granule = C::WR;
@@ -145,10 +146,17 @@ KernelInfo kernel_info_for_hd(int group, int variant)
         k.available = true;
     } else if (variant == kVariantTc) {
         if constexpr (HD % 16 == 0) {
-            using C = TcCfg<HD, 8, __half>;
-            k.tile_rows = C::TILE;
-            k.granule = C::WR;
-            k.blocks_per_sm = blocks_per_sm<C>();
+            if (multi) {
+                using C = TcMqCfg<HD, __half>;
+                k.tile_rows = C::TILE;
+                k.granule = C::WR;
+                k.blocks_per_sm = blocks_per_sm<C>();
+            } else {
+                using C = TcCfg<HD, 8, __half>;
+                k.tile_rows = C::TILE;
+                k.granule = C::WR;
+                k.blocks_per_sm = blocks_per_sm<C>();
+            }
             k.available = true;
         }
     }

@@ -56,10 +56,10 @@ cudaError_t launch_pdl(const void *func, dim3 grid, dim3 block, size_t smem, cud
 
 // Implemented in attn_kernels_hd{8,64,128,256}_{f16,bf16}.cu (kernel_info in
 // the f16 units: the shapes do not depend on the element type).
-KernelInfo kernel_info_hd8(int group, int variant);
-KernelInfo kernel_info_hd64(int group, int variant);
-KernelInfo kernel_info_hd128(int group, int variant);
-KernelInfo kernel_info_hd256(int group, int variant);
+KernelInfo kernel_info_hd8(int group, int variant, bool multi);
+KernelInfo kernel_info_hd64(int group, int variant, bool multi);
+KernelInfo kernel_info_hd128(int group, int variant, bool multi);
+KernelInfo kernel_info_hd256(int group, int variant, bool multi);
 cudaError_t launch_hd8_f16(const LaunchRequest &r);
 cudaError_t launch_hd64_f16(const LaunchRequest &r);
 cudaError_t launch_hd128_f16(const LaunchRequest &r);

@@ -135,6 +135,16 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         }
     };
     const bool tail_by_tma = hi >= TILE;
+    // The same rows into L2 only, for a tile that has no free stage yet.
+    auto tma_prefetch_tile = [&](int t) {
+        const int64_t first = lo + (int64_t)t * TILE;
+        const int z = (int)(seq_row0 + (hi - first >= TILE ? first : hi - TILE));
+#pragma unroll
+        for (int c = 0; c < Cfg::NCH; ++c) {
+            tma_prefetch_3d(&kmap, c * Cfg::BOX_X, hk, z);
+            tma_prefetch_3d(&vmap, c * Cfg::BOX_X, hk, z);
+        }
+    };
 
     int early = 0;                          // tiles the producer issues before the block syncs
     if (tid == NWC * 32) {
@@ -152,6 +162,11 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
             tma_tile(early, early);
         }
         flags[1] = early;
+        // the next S tiles into L2, so that a stage freed later refills from L2
+        for (int t = early; t < ntiles && t < early + S; ++t) {
+            if (hi - (lo + (int64_t)t * TILE) < TILE && !tail_by_tma) break;
+            tma_prefetch_tile(t);
+        }
     }
     // a2, while the first tiles are in flight
     if (stable) pdl_wait();

@@ -44,7 +44,7 @@ struct TcWarp {
     }
     static constexpr int KSTEPS = HD / 16;            // k-steps of q·Kᵀ
     static constexpr int NTD = HD / 8;                // n-tiles of p·V
-    static constexpr bool Q_REGS = HD <= 64;          // keep q fragments in registers (else smem)
+    static constexpr bool Q_REGS = HD <= 128;         // keep q fragments in registers (else smem)
     static constexpr float TAU = 8.f;                 // lazy-rescale threshold
     static constexpr float OFF = 7.f;                 // p headroom: max p in [2^OFF, 2^(OFF+TAU)]
     static constexpr uint32_t QT_BYTES = 16u * HD * 2;  // Q tile, f16, swizzled like K
@@ -142,12 +142,16 @@ struct TcWarp {
                                             int64_t, int64_t, const PartialArgs &,
                                             uint8_t *extra, int, int lane)
     {
-        // a3: scores of the slice's 16 rows for all heads
-        float c[2][4];
+        // a3: scores of the slice's 16 rows for all heads; even and odd
+        // k-steps accumulate into separate fragments (two independent MMA
+        // chains of half the depth), added at the end
+        float c[2][2][4];
 #pragma unroll
-        for (int n = 0; n < 2; ++n)
+        for (int e = 0; e < 2; ++e)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) c[n][i] = 0.f;
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) c[e][n][i] = 0.f;
         const int i8 = lane >> 3;
         const int krow = r0 + (i8 >> 1) * 8 + (lane & 7);
 #pragma unroll
@@ -161,15 +165,15 @@ struct TcWarp {
             }
             uint32_t b[4];        // (rows 0-7, d lo8), (rows 0-7, d hi8), (rows 8-15, lo8), (8-15, hi8)
             ldsm_x4(b, ks + tile_unit_offset<HD, TILE>(krow, 2 * kk + (i8 & 1)));
-            mma_16816<KV>(c[0], a, b[0], b[1]);
-            mma_16816<KV>(c[1], a, b[2], b[3]);
+            mma_16816<KV>(c[kk & 1][0], a, b[0], b[1]);
+            mma_16816<KV>(c[kk & 1][1], a, b[2], b[3]);
         }
         const int t = lane & 3;
         float s[4];
-        s[0] = (c[0][0] + c[0][2]) * inv_sc;      // row 2t
-        s[1] = (c[0][1] + c[0][3]) * inv_sc;      // row 2t + 1
-        s[2] = (c[1][0] + c[1][2]) * inv_sc;      // row 8 + 2t
-        s[3] = (c[1][1] + c[1][3]) * inv_sc;      // row 9 + 2t
+        s[0] = ((c[0][0][0] + c[1][0][0]) + (c[0][0][2] + c[1][0][2])) * inv_sc;   // row 2t
+        s[1] = ((c[0][0][1] + c[1][0][1]) + (c[0][0][3] + c[1][0][3])) * inv_sc;   // row 2t + 1
+        s[2] = ((c[0][1][0] + c[1][1][0]) + (c[0][1][2] + c[1][1][2])) * inv_sc;   // row 8 + 2t
+        s[3] = ((c[0][1][1] + c[1][1][1]) + (c[0][1][3] + c[1][1][3])) * inv_sc;   // row 9 + 2t
         if (2 * t < ra) s[0] = -INFINITY;
         if (2 * t + 1 < ra) s[1] = -INFINITY;
         if (8 + 2 * t < ra) s[2] = -INFINITY;

@@ -141,12 +141,14 @@ struct TcWarpMQ {
                                             int64_t row0, int64_t nkv, const PartialArgs &a,
                                             uint8_t *extra, int, int lane)
     {
-        // a3: scores, C rows = query heads, C columns = the slice's rows
-        float c[2][4];
+        // a3: scores, C rows = query heads, C columns = the slice's rows; the
+        // hi and lo parts of q accumulate separately (two independent MMA
+        // chains) and are added at the end
+        float ch[2][4], cl[2][4];
 #pragma unroll
         for (int n = 0; n < 2; ++n)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) c[n][i] = 0.f;
+            for (int i = 0; i < 4; ++i) ch[n][i] = cl[n][i] = 0.f;
         const int i8 = lane >> 3;
         const int krow = r0 + (i8 >> 1) * 8 + (lane & 7);
 #pragma unroll
@@ -155,11 +157,16 @@ struct TcWarpMQ {
             load_q(ah, extra, kk, lane);
             load_q(al, extra + QT_BYTES, kk, lane);
             ldsm_x4(b, ks + tile_unit_offset<HD, TILE>(krow, 2 * kk + (i8 & 1)));
-            mma_16816<KV>(c[0], ah, b[0], b[1]);
-            mma_16816<KV>(c[0], al, b[0], b[1]);
-            mma_16816<KV>(c[1], ah, b[2], b[3]);
-            mma_16816<KV>(c[1], al, b[2], b[3]);
+            mma_16816<KV>(ch[0], ah, b[0], b[1]);
+            mma_16816<KV>(cl[0], al, b[0], b[1]);
+            mma_16816<KV>(ch[1], ah, b[2], b[3]);
+            mma_16816<KV>(cl[1], al, b[2], b[3]);
         }
+        float c[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c[n][i] = ch[n][i] + cl[n][i];
         const int u = lane & 3;
         const int cols[4] = {2 * u, 2 * u + 1, 8 + 2 * u, 9 + 2 * u};
         float sc[2][4];

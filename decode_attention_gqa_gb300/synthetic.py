@@ -99,6 +99,15 @@ def make_q(w: Workload, layer: int = 0) -> np.ndarray:
     return out
 
 
+def make_q_multi(w: Workload, n_q: int, layer: int = 0) -> np.ndarray:
+    """q for n_q causal query rows: float32 [n_seq, n_q, n_head, head_dim]."""
+    out = np.empty((w.n_seq, n_q, w.n_head, w.head_dim), dtype=np.float32)
+    for s in range(w.n_seq):
+        out[s] = _rng(w.seed, layer, s, 3).standard_normal(
+            (n_q, w.n_head, w.head_dim), dtype=np.float32)
+    return out
+
+
 def to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """float32 -> bfloat16 bit patterns (uint16), round to nearest even."""
     u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
@@ -147,6 +156,18 @@ def make_kv(w: Workload, layer: int = 0, fill: float = 0.0, kv_dtype: str = "f16
 def make_positions(w: Workload) -> np.ndarray:
     """positions[s] = ctx[s] - 1 (index of the current token), int32."""
     return np.asarray([c - 1 for c in w.ctx], dtype=np.int32)
+
+
+def make_new_rows(w: Workload, layer: int = 0, kv_dtype: str = "f16"):
+    """The new token's K and V rows for a fused append, [n_seq, n_kv_head,
+    head_dim] each, in the cache's element type."""
+    shape = (w.n_seq, w.n_kv_head, w.head_dim)
+    kn = np.empty(shape, dtype=np.float16 if kv_dtype == "f16" else np.uint16)
+    vn = np.empty_like(kn)
+    for s in range(w.n_seq):
+        kn[s] = _cast(_rng(w.seed, layer, s, 4).standard_normal(shape[1:], dtype=np.float32), kv_dtype)
+        vn[s] = _cast(_rng(w.seed, layer, s, 5).standard_normal(shape[1:], dtype=np.float32), kv_dtype)
+    return kn, vn
 
 
 def make_layer(w: Workload, layer: int = 0, fill: float = 0.0, kv_dtype: str = "f16") -> dict:

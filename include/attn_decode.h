@@ -250,15 +250,18 @@ int attn_split_heuristic(int n_seq, int n_head, int n_kv_head, int head_dim, int
                          int sm_count);
 
 /*
- * attn_split_heuristic_ex -- the same, for the call's variant argument
- * (ATTN_VARIANT_*, ATTN_KV_BF16, ATTN_KV_STABLE). With ATTN_KV_STABLE, a
- * single sequence and a short call (at most 4 kernel tiles of rows per block
- * at one block per SM) the wave is one block per SM rather than as many as
- * fit, so that the next flagged call's blocks find room beside this call's
- * and start their copies while it finishes. Returns 0 for an invalid variant.
+ * attn_split_heuristic_ex -- the same for a call with n_q query rows per
+ * sequence (1 for attn_decode_ex / attn_decode_append, n_q for
+ * attn_decode_multi, whose blocks each serve 16 (query row, head) pairs) and
+ * the call's variant argument (ATTN_VARIANT_*, ATTN_KV_BF16, ATTN_KV_STABLE).
+ * With ATTN_KV_STABLE, a single sequence and a short call (at most 4 kernel
+ * tiles of rows per block at one block per SM) the wave is one block per SM
+ * rather than as many as fit, so that the next flagged call's blocks find room
+ * beside this call's and start their copies while it finishes. Returns 0 for
+ * an invalid shape or variant.
  */
-int attn_split_heuristic_ex(int n_seq, int n_head, int n_kv_head, int head_dim, int64_t cap,
-                            int sm_count, int variant);
+int attn_split_heuristic_ex(int n_seq, int n_q, int n_head, int n_kv_head, int head_dim,
+                            int64_t cap, int sm_count, int variant);
 
 /* attn_workspace_size -- bytes of workspace attn_decode_ex needs (host-only). */
 size_t attn_workspace_size(int n_seq, int n_head, int head_dim, int n_splits);

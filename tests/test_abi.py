@@ -96,7 +96,8 @@ def test_split_heuristic_host_only(lib):
 
 
 def test_split_heuristic_for_flagged_calls(lib):
-    h = pkg.attn_split_heuristic_ex
+    def h(n_seq, n_head, n_kv, hd, cap, sms, variant, n_q=1):
+        return pkg.attn_split_heuristic_ex(n_seq, n_q, n_head, n_kv, hd, cap, sms, variant)
     # the plain call and variant 0 agree; the element type does not change P
     assert h(1, 28, 4, 128, 8192, 152, 0) == pkg.attn_split_heuristic(1, 28, 4, 128, 8192, 152)
     assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_BF16) == 74
@@ -109,9 +110,17 @@ def test_split_heuristic_for_flagged_calls(lib):
     assert h(32, 32, 8, 128, 32768, 152, pkg.ATTN_KV_STABLE) == 10
     # head_dim 256 already runs one block per SM
     assert h(1, 16, 2, 256, 8400, 152, pkg.ATTN_KV_STABLE) == h(1, 16, 2, 256, 8400, 152, 0) == 75
+    # several query rows: 4 rows x 7 heads = 28 pairs -> 2 query groups of 16 per KV
+    # head; at one block per SM a block would hold 431 rows (not a short call), so
+    # two blocks per SM: 8 x 37 blocks of 224 rows
+    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_STABLE, n_q=4) == 37
+    assert h(1, 28, 4, 128, 2048, 152, pkg.ATTN_KV_STABLE, n_q=4) == 19    # short: one per SM
+    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_STABLE, n_q=2) == 37     # 14 pairs: one group
+    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_VARIANT_SIMT, n_q=2) == 0  # tensor cores only
     # the CUDA-core kernel has its own granule and residency
     assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_VARIANT_SIMT) >= 1
     assert h(1, 28, 4, 128, 8192, 152, 7) == 0                           # no such variant
+    assert h(1, 28, 4, 128, 8192, 152, 0, n_q=0) == 0
 
 
 def _ex(lib, **kw):
