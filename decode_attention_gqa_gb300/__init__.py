@@ -25,7 +25,8 @@ __all__ = [
     "attn_decode_combine",
     "attn_decode_static",
     "attn_split_heuristic", "attn_split_heuristic_ex", "attn_workspace_size",
-    "attn_read_device_error", "attn_status_string", "attn_last_cuda_error", "attn_version",
+    "attn_read_device_error", "attn_selftest_bounded_wait", "attn_status_string",
+    "attn_last_cuda_error", "attn_version",
 ]
 
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE, ATTN_ERR_CUDA = range(5)
@@ -93,6 +94,8 @@ def load():
         lib.attn_workspace_size.argtypes = [i32, i32, i32, i32]
         lib.attn_read_device_error.restype = i32
         lib.attn_read_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint)]
+        lib.attn_selftest_bounded_wait.restype = i32
+        lib.attn_selftest_bounded_wait.argtypes = [ctypes.c_ulonglong, vp]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_status_string.argtypes = [i32]
         lib.attn_last_cuda_error.restype = i32
@@ -220,6 +223,12 @@ def attn_split_heuristic_ex(n_seq, n_q, n_head, n_kv_head, head_dim, cap, sm_cou
 
 def attn_workspace_size(n_seq, n_head, head_dim, n_splits) -> int:
     return load().attn_workspace_size(n_seq, n_head, head_dim, n_splits)
+
+
+def attn_selftest_bounded_wait(limit_ns, stream=None) -> None:
+    """Launch the bounded-wait self-test (see include/attn_decode.h)."""
+    _check(load().attn_selftest_bounded_wait(limit_ns, _stream(stream)),
+           "attn_selftest_bounded_wait")
 
 
 def attn_read_device_error(stream=None) -> int:

@@ -42,6 +42,21 @@ DeviceState g_dev[kMaxDevices];
 // One sticky error word per device, set by the kernels with atomicOr.
 __device__ unsigned g_attn_error_word;
 
+// Self-test of the bounded wait: one warp waits on an mbarrier that nothing
+// arrives on, through the same helper the kernels use, and reports the
+// timeout in the error word as they do.
+__global__ void attn_selftest_wait_kernel(unsigned *err, unsigned long long limit_ns)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        attn::mbar_init(&bar, 1);
+        attn::fence_barrier_init();
+    }
+    __syncthreads();
+    const bool landed = attn::mbar_wait_bounded(&bar, 0, limit_ns);   // phase 0 never completes
+    if (!__all_sync(0xffffffffu, landed) && threadIdx.x == 0) atomicOr(err, attn::kErrPipelineTimeout);
+}
+
 namespace {
 
 attn_status cuda_fail(cudaError_t e)
@@ -481,6 +496,25 @@ const char *attn_status_string(attn_status status)
     case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
     default: return "ATTN_ERR_UNKNOWN";
     }
+}
+
+attn_status attn_selftest_bounded_wait(unsigned long long limit_ns, attn_stream_t stream)
+{
+    if (limit_ns == 0 || limit_ns > attn::kWaitLimitNs) return ATTN_ERR_INVALID_ARG;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    DeviceState *ds = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        e = device_state(dev, &ds);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    attn_selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(ds->err_word,
+                                                                                    limit_ns);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return ATTN_OK;
 }
 
 int attn_last_cuda_error(void) { return t_last_cuda_error; }

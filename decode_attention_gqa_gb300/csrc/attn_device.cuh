@@ -203,13 +203,14 @@ __device__ __forceinline__ unsigned long long globaltimer_ns()
 
 // Wait for the phase with the given parity to complete. Gives up after
 // kWaitLimitNs and returns false; never spins forever.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, unsigned parity)
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, unsigned parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 

@@ -263,6 +263,19 @@ int attn_split_heuristic(int n_seq, int n_head, int n_kv_head, int head_dim, int
 int attn_split_heuristic_ex(int n_seq, int n_q, int n_head, int n_kv_head, int head_dim,
                             int64_t cap, int sm_count, int variant);
 
+/*
+ * attn_selftest_bounded_wait -- diagnostic: launch one warp that waits on a
+ * shared-memory mbarrier nothing ever arrives on, through the same bounded
+ * wait the kernels use, with a limit of limit_ns nanoseconds (1 ..
+ * 1,000,000,000; the kernels use 1 s). When the limit passes, the warp sets
+ * ATTN_DEVERR_PIPELINE_TIMEOUT in the device error word and returns, leaving
+ * the context usable; read it with attn_read_device_error. Asynchronous on
+ * `stream`; returns the launch status. The pages have no counterpart: it
+ * exists to check, without hanging a GPU, that no wait of the library spins
+ * forever.
+ */
+attn_status attn_selftest_bounded_wait(unsigned long long limit_ns, attn_stream_t stream);
+
 /* attn_workspace_size -- bytes of workspace attn_decode_ex needs (host-only). */
 size_t attn_workspace_size(int n_seq, int n_head, int head_dim, int n_splits);
 

@@ -169,3 +169,9 @@ def test_ptxas_reports_no_spills(lib):
     assert rep, "no ptxas report found"
     for fn, r in rep.items():
         assert r["spill_stores"] == 0 and r["spill_loads"] == 0 and r["stack"] == 0, fn
+
+
+def test_selftest_limit_is_checked_before_any_launch(lib):
+    # the bounded-wait self-test takes 1 ns .. 1 s, like the kernels' own waits
+    assert lib.attn_selftest_bounded_wait(0, None) == pkg.ATTN_ERR_INVALID_ARG
+    assert lib.attn_selftest_bounded_wait(2_000_000_000, None) == pkg.ATTN_ERR_INVALID_ARG

@@ -117,3 +117,28 @@ def test_workspace_errors(pkg):
                                     hd, scale, cap, 4000, 0, 0, None, 0,
                                     torch.cuda.current_stream().cuda_stream)
     assert status == pkg.ATTN_ERR_WORKSPACE
+
+
+def test_bounded_wait_runs_out_and_reports(pkg):
+    """A wait on an mbarrier nothing arrives on gives up after its limit, sets
+    ATTN_DEVERR_PIPELINE_TIMEOUT and returns; the context keeps working."""
+    import torch
+    pkg.attn_read_device_error()                                  # clear
+    s = torch.cuda.Stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        pkg.attn_selftest_bounded_wait(20_000_000, stream=s)      # 20 ms
+        e1.record(s)
+    torch.cuda.synchronize()
+    assert e0.elapsed_time(e1) >= 19.0                            # it did wait for the limit
+    assert pkg.attn_read_device_error(s) == pkg.ATTN_DEVERR_PIPELINE_TIMEOUT
+    assert pkg.attn_read_device_error(s) == 0                     # read clears
+    # the context still serves a normal call
+    n_head, n_kv, hd, cap = 8, 2, 128, 300
+    case = make_case(77, 1, n_head, n_kv, hd, cap, (260,))
+    got = run_decode(pkg, to_device(case), n_head, n_kv, hd, cap, 0.1).cpu().numpy()
+    ref = oracle.attn_decode(case["q"], case["k"], case["v"], case["positions"], n_head, n_kv, hd,
+                             cap, 0.1)
+    assert_close(got, ref, "after the self-test")
+    assert pkg.attn_read_device_error() == 0
