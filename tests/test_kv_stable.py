@@ -166,3 +166,80 @@ def test_stable_flag_accepted_with_every_entry_point(pkg):
                           cap, variant=pkg.ATTN_KV_STABLE)
     torch.cuda.synchronize()
     assert_close(outm.cpu().numpy()[:, 1], ref, "multi + stable, last query row")
+
+
+# ------------------------------------- full size, in the launch configuration bench.py times
+
+def _bench_configuration(pkg, name, L, n_q=1):
+    """L independent layers of a workload at full size in one captured graph:
+    positions += 1, then layer 0 without and layers 1.. with ATTN_KV_STABLE,
+    split count from attn_split_heuristic_ex for that flag -- the step bench.py
+    times. Every layer is compared with the oracle after one replay."""
+    import torch
+    from decode_attention_gqa_gb300 import synthetic as syn
+    w = syn.WORKLOADS[name]
+    layers = [syn.make_layer(w, layer=l) for l in range(L)]
+    if n_q > 1:
+        for l, lay in enumerate(layers):
+            lay["q"] = syn.make_q_multi(w, n_q, layer=l)
+    dev = [to_device(c) for c in layers]
+    pos = torch.from_numpy(layers[0]["positions"] - 1).cuda()
+    outs = [torch.full_like(d["q"], float("nan")) for d in dev]
+    P = pkg.attn_split_heuristic_ex(w.n_seq, n_q, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0,
+                                    pkg.ATTN_KV_STABLE)
+    ws_bytes = pkg.attn_workspace_size(w.n_seq, n_q * w.n_head, w.head_dim, P)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+
+    def step():
+        pos.add_(1)
+        for l in range(L):
+            var = pkg.ATTN_KV_STABLE if l > 0 else 0
+            if n_q > 1:
+                pkg.attn_decode_multi(dev[l]["q"], dev[l]["k"], dev[l]["v"], pos, outs[l], w.n_seq,
+                                      n_q, w.n_head, w.n_kv_head, w.head_dim, w.scale, w.cap,
+                                      n_splits=P, variant=var, workspace=ws,
+                                      workspace_bytes=ws_bytes, stream=s)
+            else:
+                pkg.attn_decode_ex(dev[l]["q"], dev[l]["k"], dev[l]["v"], pos, outs[l], w.n_seq,
+                                   w.n_head, w.n_kv_head, w.head_dim, w.scale, w.cap, n_splits=P,
+                                   variant=var, workspace=ws, workspace_bytes=ws_bytes, stream=s)
+
+    with torch.cuda.stream(s):
+        step()                                        # warm the launch path
+    torch.cuda.synchronize()
+    pos.sub_(1)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    for o in outs:
+        o.fill_(float("nan"))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        g.replay()
+    torch.cuda.synchronize()
+    positions = pos.cpu().numpy()
+    assert np.array_equal(positions, layers[0]["positions"])
+    for l in range(L):
+        lay = layers[l]
+        if n_q > 1:
+            ref = oracle.attn_decode_multi(lay["q"], lay["k"], lay["v"], positions, n_q, w.n_head,
+                                           w.n_kv_head, w.head_dim, w.cap, w.scale, n_threads=16)
+        else:
+            ref = oracle.attn_decode(lay["q"], lay["k"], lay["v"], positions, w.n_head,
+                                     w.n_kv_head, w.head_dim, w.cap, w.scale, n_threads=16)
+        assert_close(outs[l].cpu().numpy(), ref, "%s n_q=%d layer %d (P=%d)" % (name, n_q, l, P))
+    assert pkg.attn_read_device_error() == 0
+    return P
+
+
+def test_full_7b_bench_configuration(pkg):
+    assert _bench_configuration(pkg, "7b", L=4) == 37
+
+
+def test_full_long_bench_configuration(pkg):
+    assert _bench_configuration(pkg, "long", L=3) == 75
+
+
+def test_full_7b_four_query_rows_bench_configuration(pkg):
+    _bench_configuration(pkg, "7b", L=3, n_q=4)
