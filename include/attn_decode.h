@@ -193,7 +193,10 @@ attn_status attn_decode_multi(const float *q, const void *k_cache, const void *v
  * where oc is the unnormalised weighted V sum of the split, S its softmax
  * denominator and mx its running maximum, all relative to exp2(scores *
  * log2 e) (mx is in log2 units). An empty split has mx = -inf, S = 0 and its
- * oc is never read.
+ * oc is never read. Splits combine in any order: partials of disjoint row
+ * ranges computed elsewhere (another device's shard of the rows, say) can be
+ * laid side by side along the split axis and combined with n_splits = the
+ * total split count.
  */
 attn_status attn_decode_partial(const float *q, const void *k_cache, const void *v_cache,
                                 const int32_t *positions, int n_seq, int n_head, int n_kv_head,
