@@ -66,16 +66,31 @@ struct TcWarp {
         constexpr int NW = NTHREADS / 32;
         constexpr int ITER = (8 + NW - 1) / NW;           // heads per warp
         constexpr int PER = (HD + 31) / 32;               // elements per lane per head
+        static_assert(PER % 2 == 0 && PER <= 8, "lane owns PER consecutive elements");
         float *inv = reinterpret_cast<float *>(extra + QT_BYTES);
         const int warp = tid >> 5, lane = tid & 31;
+        // lane owns elements [lane * PER, lane * PER + PER) of a head: one or
+        // two 16-byte loads (8 bytes at head_dim 64) per head row, so the many
+        // blocks reading the same q lines send few requests
         float x[ITER][PER];
 #pragma unroll
         for (int it = 0; it < ITER; ++it) {
             const int g = warp + it * NW;
+            const float *row = qg + g * HD + lane * PER;
+            if constexpr (PER == 2) {
+                const float2 u = g < G ? ld_dep(reinterpret_cast<const float2 *>(row)) : make_float2(0.f, 0.f);
+                x[it][0] = u.x * qscale;
+                x[it][1] = u.y * qscale;
+            } else {
 #pragma unroll
-            for (int i = 0; i < PER; ++i) {
-                const int d = lane + 32 * i;
-                x[it][i] = (g < G && d < HD) ? ld_dep(qg + g * HD + d) * qscale : 0.f;
+                for (int j = 0; j < PER; j += 4) {
+                    const float4 u = g < G ? ld_dep(reinterpret_cast<const float4 *>(row + j))
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                    x[it][j] = u.x * qscale;
+                    x[it][j + 1] = u.y * qscale;
+                    x[it][j + 2] = u.z * qscale;
+                    x[it][j + 3] = u.w * qscale;
+                }
             }
         }
 #pragma unroll
@@ -93,19 +108,28 @@ struct TcWarp {
                 sc = ldexpf(1.f, 15 - e);                 // scaled max in [2^14, 2^15)
             }
             if (lane == 0) inv[g] = amax > 0.f ? ldexpf(1.f, e - 15) : 1.f;
+            // hi = T(v), lo = T(v - hi) element by element, packed in pairs; the
+            // lane's PER elements share one 16-byte unit of the swizzled tile
+            uint32_t hw[PER / 2], lw[PER / 2];
 #pragma unroll
-            for (int i = 0; i < PER; ++i) {
-                const int d = lane + 32 * i;
-                if (d < HD) {
-                    const float v = x[it][i] * sc;
-                    const uint32_t hw = float2_to_kv2<KV>(v, 0.f);          // hi in the low half
-                    const float hf = kv2_to_float2<KV>(hw).x;
-                    const uint32_t lw = float2_to_kv2<KV>(v - hf, 0.f);
-                    const uint32_t off = tile_unit_offset<HD, 16>(g, d >> 3) + (d & 7) * 2;
-                    const uint32_t offl = tile_unit_offset<HD, 16>(8 + g, d >> 3) + (d & 7) * 2;
-                    *reinterpret_cast<uint16_t *>(extra + off) = (uint16_t)(hw & 0xffffu);
-                    *reinterpret_cast<uint16_t *>(extra + offl) = (uint16_t)(lw & 0xffffu);
-                }
+            for (int j = 0; j < PER / 2; ++j) {
+                const float v0 = x[it][2 * j] * sc, v1 = x[it][2 * j + 1] * sc;
+                hw[j] = float2_to_kv2<KV>(v0, v1);
+                const float2 f = kv2_to_float2<KV>(hw[j]);
+                lw[j] = float2_to_kv2<KV>(v0 - f.x, v1 - f.y);
+            }
+            const int d0 = lane * PER;
+            const uint32_t off = tile_unit_offset<HD, 16>(g, d0 >> 3) + (d0 & 7) * 2;
+            const uint32_t offl = tile_unit_offset<HD, 16>(8 + g, d0 >> 3) + (d0 & 7) * 2;
+            if constexpr (PER == 2) {
+                *reinterpret_cast<uint32_t *>(extra + off) = hw[0];
+                *reinterpret_cast<uint32_t *>(extra + offl) = lw[0];
+            } else if constexpr (PER == 4) {
+                *reinterpret_cast<uint2 *>(extra + off) = make_uint2(hw[0], hw[1]);
+                *reinterpret_cast<uint2 *>(extra + offl) = make_uint2(lw[0], lw[1]);
+            } else {
+                *reinterpret_cast<uint4 *>(extra + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4 *>(extra + offl) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
         }
     }
