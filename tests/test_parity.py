@@ -255,3 +255,34 @@ def test_full_ragged_sampled(pkg):
     rng = np.random.Generator(np.random.PCG64(77))
     pairs = [(s, int(rng.integers(0, w.n_head))) for s in range(w.n_seq)]
     _full_workload(pkg, "ragged", sample_pairs=pairs)
+
+
+# ------------------------------------------------------------ grid extremes
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_grid_z_at_its_limit(pkg, variant):
+    """65535 sequences (the largest grid z) of 0 to 2 rows each, every one
+    checked against the oracle."""
+    n_seq, n_head, n_kv, hd, cap = 65535, 8, 2, 64, 2
+    rng = np.random.Generator(np.random.PCG64(1400))
+    ctx = tuple(int(c) for c in rng.integers(0, cap + 1, n_seq))
+    case = make_case(1401, n_seq, n_head, n_kv, hd, cap, ctx)
+    ref = oracle.attn_decode(case["q"], case["k"], case["v"], case["positions"], n_head, n_kv, hd,
+                             cap, 0.125, n_threads=16)
+    got = run_decode(pkg, to_device(case), n_head, n_kv, hd, cap, 0.125, variant=variant)
+    assert_close(got.cpu().numpy(), ref, "65535 sequences variant %d" % variant)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_largest_split_count(pkg, variant):
+    """P = 4096 (the most the library takes): by count most splits are empty;
+    by 1-row blocks every row is a split of its own."""
+    n_head, n_kv, hd, cap = 8, 2, 128, 4096
+    case = make_case(1402, 2, n_head, n_kv, hd, cap, (4096, 1999))
+    ref = oracle.attn_decode(case["q"], case["k"], case["v"], case["positions"], n_head, n_kv, hd,
+                             cap, 0.09, n_threads=16)
+    dev = to_device(case)
+    for blk in (0, 1):
+        got = run_decode(pkg, dev, n_head, n_kv, hd, cap, 0.09, n_splits=4096, split_len=blk,
+                         variant=variant)
+        assert_close(got.cpu().numpy(), ref, "P=4096 blk=%d variant %d" % (blk, variant))
