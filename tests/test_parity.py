@@ -125,7 +125,7 @@ def test_split_count_invariance(pkg, variant):
     ref = _oracle(case, n_head, n_kv, hd, cap, scale)
     dev = to_device(case)
     outs = []
-    for P in (1, 2, 3, 7, 32, 64, 188, 400):
+    for P in (1, 2, 3, 7, 32, 33, 63, 64, 65, 188, 400):
         out = run_decode(pkg, dev, n_head, n_kv, hd, cap, scale, n_splits=P, variant=variant)
         outs.append(out.cpu().numpy())
         assert_close(outs[-1], ref, "P=%d" % P)

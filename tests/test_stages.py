@@ -49,7 +49,7 @@ def test_partial_then_combine(pkg, hd, variant):
     scale = 1 / math.sqrt(hd)
     ref = oracle.attn_decode(case["q"], case["k"], case["v"], case["positions"], n_head, n_kv, hd,
                              cap, scale, n_threads=8)
-    for P, blk in ((7, 0), (12, 64)):
+    for P, blk in ((7, 0), (12, 64), (64, 0), (70, 16)):
         got, _ = _stages(pkg, to_device(case), len(ctx), n_head, n_kv, hd, cap, scale, P, blk,
                          variant)
         assert_close(got, ref, "stages hd%d variant %d P=%d blk=%d" % (hd, variant, P, blk))
