@@ -111,11 +111,19 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def strip_comments(src: str) -> str:
+    """C++ source without comments and with whitespace collapsed: what the
+    compiler sees, so that a comment edit does not count as a kernel change."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "decode_attention_gqa_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "decode_attention_gqa_gb300", "csrc", name)) as f:
+            h.update(strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

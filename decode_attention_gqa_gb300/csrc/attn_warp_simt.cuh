@@ -161,7 +161,7 @@ struct SimtWarp {
     }
 
     // Reduce the per-lane pieces and publish (mx, S) and oc of every head:
-    // mm[g] = (mx, S), mo[g * HD + d] = oc.
+    // mm[g] = (mx, S), mo[g * merge_stride + d] = oc.
     __device__ __forceinline__ void publish(float2 *mm, float *mo, int lane)
     {
 #pragma unroll

@@ -243,6 +243,8 @@ struct TcWarpMQ {
         }
     }
 
+    // mm[h] = (mx, S) and mo[h * merge_stride + d] = oc for the block-local
+    // heads h = g and g + 8 of lane group g.
     __device__ __forceinline__ void publish(float2 *mm, float *mo, int lane)
     {
         const int g = lane >> 2, u = lane & 3;
