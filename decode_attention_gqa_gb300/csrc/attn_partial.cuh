@@ -54,8 +54,12 @@ struct PartialCfg {
     // merge area (reuses the stage buffers after the main loop)
     static constexpr int NQH = Warp::NQH;            // query heads per block
     static constexpr int MS = merge_stride<HD>();    // floats per published accumulator row
-    static constexpr uint32_t OFF_WTS = (uint32_t)NWC * NQH * (MS + 2);   // floats: merge weights
+    // merge area (floats): (mx, S) pairs, then the accumulator rows from a
+    // 16-byte boundary (the merge reads them as float4), then the weights
+    static constexpr uint32_t OFF_MO = ((uint32_t)2 * NWC * NQH + 3) / 4 * 4;
+    static constexpr uint32_t OFF_WTS = OFF_MO + (uint32_t)NWC * NQH * MS;
     static constexpr uint32_t MERGE_BYTES = (OFF_WTS + (uint32_t)NWC * NQH) * 4;
+    static_assert(OFF_MO % 4 == 0 && MS % 4 == 0, "float4 rows in the merge area");
     static_assert(MERGE_BYTES <= S * STAGE_BYTES, "merge area must fit in the stage buffers");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(HD < 64 || (TILE_BYTES / NCH) % 1024 == 0, "swizzled chunks must stay 1024-aligned");
@@ -284,7 +288,7 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
         asm volatile("bar.sync 1, %0;" :: "r"(NWC * 32) : "memory");
         if (!__shfl_sync(0xffffffffu, flags[0], 0))
             wst.publish(reinterpret_cast<float2 *>(smem) + warp * NQH,
-                        reinterpret_cast<float *>(smem) + 2 * NWC * NQH + warp * NQH * Cfg::MS, lane);
+                        reinterpret_cast<float *>(smem) + Cfg::OFF_MO + warp * NQH * Cfg::MS, lane);
     }
     __syncthreads();
 
@@ -303,7 +307,7 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     // and the NWC weights, then all threads scale and add the accumulators in
     // float4 units.
     const float2 *mm = reinterpret_cast<const float2 *>(smem);
-    const float *mo = reinterpret_cast<const float *>(smem) + 2 * NWC * NQH;
+    const float *mo = reinterpret_cast<const float *>(smem) + Cfg::OFF_MO;
     float *wts = reinterpret_cast<float *>(smem) + Cfg::OFF_WTS;
     if (tid < NQH) {
         const int g = tid;
