@@ -172,6 +172,7 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     if ((k_new == nullptr) != (v_new == nullptr)) return ATTN_ERR_INVALID_ARG;
     if ((int64_t)n_seq * cap > kMaxFlatRows - 1024) return ATTN_ERR_INVALID_ARG;
     const int group = n_head / n_kv_head;
+    // n_q * G <= 8192 also keeps the kernels' multiply-shift division by G exact
     if (n_q < 1 || n_q > 1024) return ATTN_ERR_INVALID_ARG;
     if (n_q > 1 && k_new) return ATTN_ERR_INVALID_ARG;
     if (!head_dim_supported(head_dim) || group > 8) return ATTN_ERR_UNSUPPORTED;
@@ -241,6 +242,8 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     r.pa.n_q = n_q;
     r.pa.qgroups = n_q > 1 ? qgroups : 1;
     r.pa.kv_stable = kv_stable;
+    r.pa.group = group;
+    r.pa.group_magic = (65536u + (unsigned)group - 1u) / (unsigned)group;
     if (k_new) {
         r.pa.k_new = static_cast<const uint16_t *>(k_new);
         r.pa.v_new = static_cast<const uint16_t *>(v_new);

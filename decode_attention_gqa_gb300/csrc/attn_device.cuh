@@ -90,7 +90,16 @@ struct PartialArgs {
     uint16_t *k_w;            // the caches again, writable, when appending
     uint16_t *v_w;
     int kv_stable;            // 1: positions and cache rows may be read before the grid dependency
+    int group;                // G = n_head / n_kv_head
+    unsigned group_magic;     // ceil(2^16 / G): x / G == (x * group_magic) >> 16 for 0 <= x < 8192
 };
+
+// x / G for a (query row, group head) index x < 8192 without an integer
+// division (exact for every G in 1..8 over that range).
+__device__ __forceinline__ int div_group(const PartialArgs &a, int x)
+{
+    return (int)(((unsigned)x * a.group_magic) >> 16);
+}
 
 struct CombineArgs {
     const float *ws_o;

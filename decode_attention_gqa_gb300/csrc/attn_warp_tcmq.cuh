@@ -37,10 +37,10 @@ struct TcWarpMQ {
     // Block-local query head i -> (t, g) -> partial-head index t * n_head + hk * G + g.
     static __device__ __forceinline__ int slot_head(const PartialArgs &a, int hk, int qg, int i)
     {
-        const int G = a.n_head / a.n_kv_head;
+        const int G = a.group;
         const int qh = qg * QH + i;
         if (i >= QH || qh >= a.n_q * G) return -1;
-        const int t = qh / G, g = qh % G;
+        const int t = div_group(a, qh), g = qh - t * G;
         return t * a.n_head + hk * G + g;
     }
 
@@ -53,10 +53,14 @@ struct TcWarpMQ {
         constexpr int NW = NTHREADS / 32;
         constexpr int ITER = (16 + NW - 1) / NW;
         constexpr int PER = (HD + 31) / 32;
+        static_assert(PER % 2 == 0 && PER <= 8, "lane owns PER consecutive elements");
         float *inv = reinterpret_cast<float *>(extra + 2 * QT_BYTES);
         int *qr = reinterpret_cast<int *>(inv + 16);
         const int warp = tid >> 5, lane = tid & 31;
-        const int G = a.n_head / a.n_kv_head;
+        const int G = a.group;
+        // lane owns elements [lane * PER, lane * PER + PER) of a head row: one
+        // or two 16-byte loads (8 bytes at head_dim 64) per row, few requests
+        // for the q lines that every split's block reads
         float x[ITER][PER];
 #pragma unroll
         for (int it = 0; it < ITER; ++it) {
@@ -64,13 +68,25 @@ struct TcWarpMQ {
             const int hp = i < 16 ? slot_head(a, hk, qg, i) : -1;
             const float *qrow_p = nullptr;
             if (hp >= 0) {
-                const int qh = qg * QH + i, t = qh / G, g = qh % G;
-                qrow_p = a.q + (((size_t)s * a.n_q + t) * a.n_head + (size_t)hk * G + g) * HD;
+                const int qh = qg * QH + i, t = div_group(a, qh), g = qh - t * G;
+                qrow_p = a.q + (((size_t)s * a.n_q + t) * a.n_head + (size_t)hk * G + g) * HD +
+                         lane * PER;
             }
+            if constexpr (PER == 2) {
+                const float2 u = qrow_p ? ld_dep(reinterpret_cast<const float2 *>(qrow_p))
+                                        : make_float2(0.f, 0.f);
+                x[it][0] = u.x * a.qscale;
+                x[it][1] = u.y * a.qscale;
+            } else {
 #pragma unroll
-            for (int k = 0; k < PER; ++k) {
-                const int d = lane + 32 * k;
-                x[it][k] = (qrow_p && d < HD) ? ld_dep(qrow_p + d) * a.qscale : 0.f;
+                for (int j = 0; j < PER; j += 4) {
+                    const float4 u = qrow_p ? ld_dep(reinterpret_cast<const float4 *>(qrow_p + j))
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                    x[it][j] = u.x * a.qscale;
+                    x[it][j + 1] = u.y * a.qscale;
+                    x[it][j + 2] = u.z * a.qscale;
+                    x[it][j + 3] = u.w * a.qscale;
+                }
             }
         }
 #pragma unroll
@@ -90,20 +106,29 @@ struct TcWarpMQ {
             if (lane == 0) {
                 inv[i] = amax > 0.f ? ldexpf(1.f, e - 15) : 1.f;
                 const int hp = slot_head(a, hk, qg, i);
-                qr[i] = hp >= 0 ? (qg * QH + i) / G : -1;
+                qr[i] = hp >= 0 ? div_group(a, qg * QH + i) : -1;
             }
+            // hi = T(v), lo = T(v - hi) element by element, packed in pairs; the
+            // lane's PER elements share one 16-byte unit of the swizzled tile
+            uint32_t hw[PER / 2], lw[PER / 2];
 #pragma unroll
-            for (int k = 0; k < PER; ++k) {
-                const int d = lane + 32 * k;
-                if (d < HD) {
-                    const float v = x[it][k] * sc;
-                    const uint32_t hw = float2_to_kv2<KV>(v, 0.f);
-                    const float hf = kv2_to_float2<KV>(hw).x;
-                    const uint32_t lw = float2_to_kv2<KV>(v - hf, 0.f);
-                    const uint32_t off = tile_unit_offset<HD, 16>(i, d >> 3) + (d & 7) * 2;
-                    *reinterpret_cast<uint16_t *>(extra + off) = (uint16_t)(hw & 0xffffu);
-                    *reinterpret_cast<uint16_t *>(extra + QT_BYTES + off) = (uint16_t)(lw & 0xffffu);
-                }
+            for (int j = 0; j < PER / 2; ++j) {
+                const float v0 = x[it][2 * j] * sc, v1 = x[it][2 * j + 1] * sc;
+                hw[j] = float2_to_kv2<KV>(v0, v1);
+                const float2 f = kv2_to_float2<KV>(hw[j]);
+                lw[j] = float2_to_kv2<KV>(v0 - f.x, v1 - f.y);
+            }
+            const int d0 = lane * PER;
+            const uint32_t off = tile_unit_offset<HD, 16>(i, d0 >> 3) + (d0 & 7) * 2;
+            if constexpr (PER == 2) {
+                *reinterpret_cast<uint32_t *>(extra + off) = hw[0];
+                *reinterpret_cast<uint32_t *>(extra + QT_BYTES + off) = lw[0];
+            } else if constexpr (PER == 4) {
+                *reinterpret_cast<uint2 *>(extra + off) = make_uint2(hw[0], hw[1]);
+                *reinterpret_cast<uint2 *>(extra + QT_BYTES + off) = make_uint2(lw[0], lw[1]);
+            } else {
+                *reinterpret_cast<uint4 *>(extra + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4 *>(extra + QT_BYTES + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
         }
     }
