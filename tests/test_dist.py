@@ -67,3 +67,28 @@ def test_reference_arm_prints_only_on_rank_zero(capsys):
     ns = argparse.Namespace(workload="tiny", ctx=0, layers=0, steps=1, warmup=0, split_len=0)
     bench.run_reference(ns, rank=1, world=2, local=1)
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_json_line_contract():
+    """`bench.py --impl reference` (the oracle on the host cores) prints one
+    JSON line with the keys the benchmark contract names."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    res = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny",
+                          "--steps", "1", "--warmup", "1"], cwd=root, capture_output=True,
+                         text=True, timeout=600)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [l for l in res.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["n_gpus"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"]
