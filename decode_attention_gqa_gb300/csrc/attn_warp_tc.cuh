@@ -72,27 +72,32 @@ struct TcWarp {
         // lane owns elements [lane * PER, lane * PER + PER) of a head: one or
         // two 16-byte loads (8 bytes at head_dim 64) per head row, so the many
         // blocks reading the same q lines send few requests
+        // every row's load is issued unconditionally (a head past G reads
+        // head 0 and is zeroed afterwards), so the loads leave back to back
         float x[ITER][PER];
 #pragma unroll
         for (int it = 0; it < ITER; ++it) {
             const int g = warp + it * NW;
-            const float *row = qg + g * HD + lane * PER;
+            const float *row = qg + (g < G ? g : 0) * HD + lane * PER;
             if constexpr (PER == 2) {
-                const float2 u = g < G ? ld_dep(reinterpret_cast<const float2 *>(row)) : make_float2(0.f, 0.f);
-                x[it][0] = u.x * qscale;
-                x[it][1] = u.y * qscale;
+                const float2 u = ld_dep(reinterpret_cast<const float2 *>(row));
+                x[it][0] = u.x;
+                x[it][1] = u.y;
             } else {
 #pragma unroll
                 for (int j = 0; j < PER; j += 4) {
-                    const float4 u = g < G ? ld_dep(reinterpret_cast<const float4 *>(row + j))
-                                           : make_float4(0.f, 0.f, 0.f, 0.f);
-                    x[it][j] = u.x * qscale;
-                    x[it][j + 1] = u.y * qscale;
-                    x[it][j + 2] = u.z * qscale;
-                    x[it][j + 3] = u.w * qscale;
+                    const float4 u = ld_dep(reinterpret_cast<const float4 *>(row + j));
+                    x[it][j] = u.x;
+                    x[it][j + 1] = u.y;
+                    x[it][j + 2] = u.z;
+                    x[it][j + 3] = u.w;
                 }
             }
         }
+#pragma unroll
+        for (int it = 0; it < ITER; ++it)
+#pragma unroll
+            for (int j = 0; j < PER; ++j) x[it][j] = warp + it * NW < G ? x[it][j] * qscale : 0.f;
 #pragma unroll
         for (int it = 0; it < ITER; ++it) {
             const int g = warp + it * NW;

@@ -61,34 +61,40 @@ struct TcWarpMQ {
         // lane owns elements [lane * PER, lane * PER + PER) of a head row: one
         // or two 16-byte loads (8 bytes at head_dim 64) per row, few requests
         // for the q lines that every split's block reads
+        // Every row's load is issued unconditionally -- a head the block does
+        // not have reads the block's first (row, head) pair instead, which
+        // always exists, and is zeroed afterwards -- so that all of a lane's
+        // loads leave back to back.
         float x[ITER][PER];
+        bool have[ITER];
 #pragma unroll
         for (int it = 0; it < ITER; ++it) {
             const int i = warp + it * NW;
             const int hp = i < 16 ? slot_head(a, hk, qg, i) : -1;
-            const float *qrow_p = nullptr;
-            if (hp >= 0) {
-                const int qh = qg * QH + i, t = div_group(a, qh), g = qh - t * G;
-                qrow_p = a.q + (((size_t)s * a.n_q + t) * a.n_head + (size_t)hk * G + g) * HD +
-                         lane * PER;
-            }
+            have[it] = hp >= 0;
+            const int qh = qg * QH + (have[it] ? i : 0);
+            const int t = div_group(a, qh);
+            const int g = hk * G + qh - t * G;
+            const float *qrow_p = a.q + (((size_t)s * a.n_q + t) * a.n_head + g) * HD + lane * PER;
             if constexpr (PER == 2) {
-                const float2 u = qrow_p ? ld_dep(reinterpret_cast<const float2 *>(qrow_p))
-                                        : make_float2(0.f, 0.f);
-                x[it][0] = u.x * a.qscale;
-                x[it][1] = u.y * a.qscale;
+                const float2 u = ld_dep(reinterpret_cast<const float2 *>(qrow_p));
+                x[it][0] = u.x;
+                x[it][1] = u.y;
             } else {
 #pragma unroll
                 for (int j = 0; j < PER; j += 4) {
-                    const float4 u = qrow_p ? ld_dep(reinterpret_cast<const float4 *>(qrow_p + j))
-                                            : make_float4(0.f, 0.f, 0.f, 0.f);
-                    x[it][j] = u.x * a.qscale;
-                    x[it][j + 1] = u.y * a.qscale;
-                    x[it][j + 2] = u.z * a.qscale;
-                    x[it][j + 3] = u.w * a.qscale;
+                    const float4 u = ld_dep(reinterpret_cast<const float4 *>(qrow_p + j));
+                    x[it][j] = u.x;
+                    x[it][j + 1] = u.y;
+                    x[it][j + 2] = u.z;
+                    x[it][j + 3] = u.w;
                 }
             }
         }
+#pragma unroll
+        for (int it = 0; it < ITER; ++it)
+#pragma unroll
+            for (int j = 0; j < PER; ++j) x[it][j] = have[it] ? x[it][j] * a.qscale : 0.f;
 #pragma unroll
         for (int it = 0; it < ITER; ++it) {
             const int i = warp + it * NW;
