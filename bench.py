@@ -283,7 +283,7 @@ def run_ours(args, rank, world, local):
 
     torch.cuda.set_device(local)
     dist_init(world, "nccl")
-    if rank == 0 or not os.path.exists(pkg.library_path()):
+    if rank == 0:                        # one build; the other ranks wait for it
         cuda_build.build()
     dist_barrier(world)
     pkg.load()
