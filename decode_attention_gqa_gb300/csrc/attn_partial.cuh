@@ -55,10 +55,9 @@ struct PartialCfg {
     static constexpr int NQH = Warp::NQH;            // query heads per block
     static constexpr int MS = merge_stride<HD>();    // floats per published accumulator row
     // merge area (floats): (mx, S) pairs, then the accumulator rows from a
-    // 16-byte boundary (the merge reads them as float4), then the weights
+    // 16-byte boundary (the merge reads them as float4)
     static constexpr uint32_t OFF_MO = ((uint32_t)2 * NWC * NQH + 3) / 4 * 4;
-    static constexpr uint32_t OFF_WTS = OFF_MO + (uint32_t)NWC * NQH * MS;
-    static constexpr uint32_t MERGE_BYTES = (OFF_WTS + (uint32_t)NWC * NQH) * 4;
+    static constexpr uint32_t MERGE_BYTES = (OFF_MO + (uint32_t)NWC * NQH * MS) * 4;
     static_assert(OFF_MO % 4 == 0 && MS % 4 == 0, "float4 rows in the merge area");
     static_assert(MERGE_BYTES <= S * STAGE_BYTES, "merge area must fit in the stage buffers");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -303,46 +302,39 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
 
     // a6: merge the NWC warp states and write the partial triple of each head
     // (a query head no warp saw a row for -- possible with causal limits --
-    // keeps mx = -inf and S = 0). First one thread per head takes the maximum
-    // and the NWC weights, then all threads scale and add the accumulators in
-    // float4 units.
+    // keeps mx = -inf and S = 0). Each thread takes the maximum and the NWC
+    // weights of its own head from the published (mx, S) pairs, then scales
+    // and adds the accumulators in float4 units; the thread holding a head's
+    // first unit also writes its (mx, S).
     const float2 *mm = reinterpret_cast<const float2 *>(smem);
     const float *mo = reinterpret_cast<const float *>(smem) + Cfg::OFF_MO;
-    float *wts = reinterpret_cast<float *>(smem) + Cfg::OFF_WTS;
-    if (tid < NQH) {
-        const int g = tid;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NWC; ++w) M = fmaxf(M, mm[w * NQH + g].x);
-        float L = 0.f;
-#pragma unroll
-        for (int w = 0; w < NWC; ++w) {
-            const float2 ml = mm[w * NQH + g];
-            const float wt = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
-            wts[w * NQH + g] = wt;
-            L = fmaf(wt, ml.y, L);
-        }
-        const int hp = Warp::slot_head(a, hk, qg, g);
-        if (hp >= 0) a.ws_ml[((size_t)s * heads + hp) * P + sp] = make_float2(M, L);
-    }
-    __syncthreads();
     constexpr int D4 = HD / 4;
     for (int i = tid; i < NQH * D4; i += Cfg::THREADS) {
         const int g = i / D4, d = (i % D4) * 4;
         const int hp = Warp::slot_head(a, hk, qg, g);
         if (hp < 0) continue;
-        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        float2 ml[NWC];
+        float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < NWC; ++w) {
-            const float wt = wts[w * NQH + g];
+            ml[w] = mm[w * NQH + g];
+            M = fmaxf(M, ml[w].x);
+        }
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        float L = 0.f;
+#pragma unroll
+        for (int w = 0; w < NWC; ++w) {
+            const float wt = ml[w].x == -INFINITY ? 0.f : ex2(ml[w].x - M);
             const float4 v = *reinterpret_cast<const float4 *>(mo + (w * NQH + g) * Cfg::MS + d);
             O.x = fmaf(wt, v.x, O.x);
             O.y = fmaf(wt, v.y, O.y);
             O.z = fmaf(wt, v.z, O.z);
             O.w = fmaf(wt, v.w, O.w);
+            L = fmaf(wt, ml[w].y, L);
         }
         const size_t slot = ((size_t)s * heads + hp) * P + sp;
         *reinterpret_cast<float4 *>(a.ws_o + slot * HD + d) = O;
+        if (d == 0) a.ws_ml[slot] = make_float2(M, L);
     }
 }
 
