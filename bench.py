@@ -36,6 +36,7 @@ sys.path.insert(0, ROOT)
 METRIC = "decode-attn µs/layer and achieved HBM GB/s (K+V bytes/time) vs GB300 peak"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0          # GB300 HBM3e data-sheet bandwidth, for context only
 KERNEL_SOURCES = ["attn_device.cuh", "attn_partial.cuh", "attn_warp_tc.cuh", "attn_warp_simt.cuh",
                   "attn_warp_tcmq.cuh",
                   "attn_combine.cuh", "attn_kernels_impl.cuh"]
@@ -486,6 +487,7 @@ def run_ours(args, rank, world, local):
     peak, peak_kind = measured_peak()
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                 "traffic": profiled_traffic("%s_ctx%d%s" % (w.name, ctx_end,
                                                             "_nq%d" % n_q if n_q > 1 else "")),
                 "kernel": "attn_split_partial" if n_q == 1 else "attn_split_partial + attn_combine",
