@@ -175,3 +175,36 @@ def test_selftest_limit_is_checked_before_any_launch(lib):
     # the bounded-wait self-test takes 1 ns .. 1 s, like the kernels' own waits
     assert lib.attn_selftest_bounded_wait(0, None) == pkg.ATTN_ERR_INVALID_ARG
     assert lib.attn_selftest_bounded_wait(2_000_000_000, None) == pkg.ATTN_ERR_INVALID_ARG
+
+
+def test_plain_c99_program_links_and_calls_the_host_entry_points(lib, tmp_path):
+    """The boundary is a C ABI: a C99 program includes the header, links the
+    library and calls the host-only entry points (no GPU needed)."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no gcc")
+    src = tmp_path / "use_abi.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "attn_decode.h"
+int main(void) {
+    if (attn_version() <= 0) return 1;
+    if (strcmp(attn_status_string(ATTN_ERR_WORKSPACE), "ATTN_ERR_WORKSPACE") != 0) return 2;
+    if (attn_workspace_size(1, 28, 128, 37) == 0) return 3;
+    if (attn_split_heuristic(1, 28, 4, 128, 8192, 152) != 74) return 4;
+    if (attn_split_heuristic_ex(1, 1, 28, 4, 128, 8192, 152, ATTN_KV_STABLE) != 37) return 5;
+    if (attn_decode(0, 0, 0, 0, 0, 1, 28, 5, 128, 0.1f, 0) != ATTN_ERR_INVALID_ARG) return 6;
+    if (attn_selftest_bounded_wait(0, 0) != ATTN_ERR_INVALID_ARG) return 7;
+    printf("ok\n");
+    return 0;
+}
+''')
+    libdir = os.path.dirname(pkg.library_path())
+    exe = tmp_path / "use_abi"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-L", libdir, "-lattn_decode", "-Wl,-rpath," + libdir, "-o", str(exe)],
+                   check=True)
+    res = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert res.returncode == 0 and res.stdout.strip() == "ok", (res.returncode, res.stderr)
