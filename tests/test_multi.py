@@ -113,3 +113,18 @@ def test_multi_query_rejections(pkg):
     st = lib.attn_decode_multi(q2.data_ptr(), kv2.data_ptr(), kv2.data_ptr(), pos.data_ptr(),
                                q2.data_ptr(), 1, 0, 4, 2, 128, 1.0, 16, 0, 0, 0, None, 0, None)
     assert st == pkg.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("n_q, G, nkv", [(64, 4, 300), (50, 8, 20), (33, 1, 700), (128, 7, 1000)])
+def test_many_query_rows(pkg, n_q, G, nkv):
+    """Prefill-sized chunks: many query groups per KV head (up to 56 blocks
+    along y), and with n_q > nkv the first n_q - nkv rows see no cache row."""
+    n_kv, hd, cap = 2, 128, 1024
+    n_head = G * n_kv
+    case = _case(800 + n_q + G, 1, n_q, n_head, n_kv, hd, cap, (nkv,))
+    got = _run(pkg, case, n_q, n_head, n_kv, hd, cap, 1 / math.sqrt(hd))
+    ref = oracle.attn_decode_multi(case["q"], case["k"], case["v"], case["positions"], n_q, n_head,
+                                   n_kv, hd, cap, 1 / math.sqrt(hd), n_threads=8)
+    assert_close(got, ref, "n_q=%d G=%d nkv=%d" % (n_q, G, nkv))
+    if n_q > nkv:
+        assert np.all(got[0, :n_q - nkv] == 0)
