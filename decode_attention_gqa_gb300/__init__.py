@@ -20,7 +20,7 @@ __all__ = [
     "ATTN_VARIANT_AUTO", "ATTN_VARIANT_SIMT", "ATTN_VARIANT_TC", "ATTN_KV_BF16", "ATTN_KV_STABLE",
     "library_path",
     "load",
-    "attn_decode", "attn_decode_ex", "attn_decode_append", "attn_decode_multi",
+    "attn_decode", "attn_decode_ex", "attn_decode_append", "attn_decode_multi", "decode_attention",
     "attn_decode_partial",
     "attn_decode_combine",
     "attn_decode_static",
@@ -151,6 +151,50 @@ def attn_decode_ex(q, k_cache, v_cache, positions, out, n_seq, n_head, n_kv_head
                                  split_len, variant, _ptr(workspace), workspace_bytes,
                                  _stream(stream)),
            "attn_decode_ex")
+
+
+def decode_attention(q, k_cache, v_cache, positions, scale=None, out=None, n_splits=0,
+                     kv_stable=False, stream=None):
+    """Convenience form of attn_decode_ex for torch tensors: the sizes come
+    from the shapes -- q f32 [n_seq, n_head, head_dim] (or [n_seq, n_q,
+    n_head, head_dim] for several causal query rows, attn_decode_multi),
+    k_cache / v_cache float16 or bfloat16 [n_seq, cap, n_kv_head, head_dim],
+    positions int32 [n_seq] -- scale defaults to 1/sqrt(head_dim), the cache
+    dtype picks ATTN_KV_BF16, and `out` is allocated when not given. The
+    library-owned workspace is used. Returns out."""
+    import math
+    import torch
+    if q.dtype != torch.float32 or positions.dtype != torch.int32:
+        raise TypeError("q must be float32 and positions int32")
+    if k_cache.dtype != v_cache.dtype or k_cache.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("k_cache and v_cache must both be float16 or both bfloat16")
+    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache / v_cache must be [n_seq, cap, n_kv_head, head_dim]")
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("positions", positions)):
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+    n_seq, cap, n_kv_head, head_dim = k_cache.shape
+    if q.dim() == 3:
+        n_q, (qs, n_head, qd) = 1, q.shape
+    elif q.dim() == 4:
+        qs, n_q, n_head, qd = q.shape
+    else:
+        raise ValueError("q must be [n_seq, n_head, head_dim] or [n_seq, n_q, n_head, head_dim]")
+    if qs != n_seq or qd != head_dim or positions.numel() != n_seq:
+        raise ValueError("q, the caches and positions disagree on n_seq or head_dim")
+    if scale is None:
+        scale = 1.0 / math.sqrt(head_dim)
+    if out is None:
+        out = torch.empty_like(q)
+    variant = (ATTN_KV_BF16 if k_cache.dtype == torch.bfloat16 else 0) | \
+        (ATTN_KV_STABLE if kv_stable else 0)
+    if n_q > 1:
+        attn_decode_multi(q, k_cache, v_cache, positions, out, n_seq, n_q, n_head, n_kv_head,
+                          head_dim, scale, cap, n_splits=n_splits, variant=variant, stream=stream)
+    else:
+        attn_decode_ex(q, k_cache, v_cache, positions, out, n_seq, n_head, n_kv_head, head_dim,
+                       scale, cap, n_splits=n_splits, variant=variant, stream=stream)
+    return out
 
 
 def attn_decode_append(q, k_new, v_new, k_cache, v_cache, positions, out, n_seq, n_head, n_kv_head,

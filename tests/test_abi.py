@@ -208,3 +208,20 @@ int main(void) {
                    check=True)
     res = subprocess.run([str(exe)], capture_output=True, text=True)
     assert res.returncode == 0 and res.stdout.strip() == "ok", (res.returncode, res.stderr)
+
+
+def test_decode_attention_checks_its_tensors_before_any_call():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 8, 128)
+    k = torch.zeros(1, 64, 2, 128, dtype=torch.float16)
+    pos = torch.zeros(1, dtype=torch.int32)
+    with pytest.raises(TypeError):
+        pkg.decode_attention(q.double(), k, k, pos)                    # q must be f32
+    with pytest.raises(TypeError):
+        pkg.decode_attention(q, k.float(), k.float(), pos)             # cache must be 16-bit
+    with pytest.raises(TypeError):
+        pkg.decode_attention(q, k, k.bfloat16(), pos)                  # K and V of one type
+    with pytest.raises(ValueError):
+        pkg.decode_attention(q[:, :, :64], k, k, pos)                  # head_dim mismatch
+    with pytest.raises(ValueError):
+        pkg.decode_attention(q, k.transpose(1, 2), k.transpose(1, 2), pos)   # not contiguous

@@ -286,3 +286,27 @@ def test_largest_split_count(pkg, variant):
         got = run_decode(pkg, dev, n_head, n_kv, hd, cap, 0.09, n_splits=4096, split_len=blk,
                          variant=variant)
         assert_close(got.cpu().numpy(), ref, "P=4096 blk=%d variant %d" % (blk, variant))
+
+
+@pytest.mark.parametrize("kv", ["f16", "bf16"])
+def test_decode_attention_convenience_call(pkg, kv):
+    """decode_attention infers the sizes from the tensors and picks the cache
+    type; one and several query rows."""
+    import torch
+    n_head, n_kv, hd, cap = 28, 4, 128, 900
+    case = make_case(1500, 2, n_head, n_kv, hd, cap, (900, 321), kv_dtype=kv)
+    dev = to_device(case)
+    if kv == "bf16":
+        dev["k"], dev["v"] = dev["k"].view(torch.bfloat16), dev["v"].view(torch.bfloat16)
+    out = pkg.decode_attention(dev["q"], dev["k"], dev["v"], dev["positions"])
+    torch.cuda.synchronize()
+    ref = oracle.attn_decode(case["q"], case["k"], case["v"], case["positions"], n_head, n_kv, hd,
+                             cap, 1 / math.sqrt(hd), n_threads=8, kv_dtype=kv)
+    assert_close(out.cpu().numpy(), ref, "decode_attention %s" % kv)
+    rng = np.random.Generator(np.random.PCG64(1501))
+    qm = rng.standard_normal((2, 3, n_head, hd), dtype=np.float32)
+    outm = pkg.decode_attention(torch.from_numpy(qm).cuda(), dev["k"], dev["v"], dev["positions"])
+    torch.cuda.synchronize()
+    refm = oracle.attn_decode_multi(qm, case["k"], case["v"], case["positions"], 3, n_head, n_kv,
+                                    hd, cap, 1 / math.sqrt(hd), n_threads=8, kv_dtype=kv)
+    assert_close(outm.cpu().numpy(), refm, "decode_attention %s, 3 rows" % kv)
