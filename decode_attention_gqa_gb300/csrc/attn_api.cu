@@ -94,7 +94,7 @@ attn::KernelInfo kernel_info(int head_dim, int group, int variant, bool multi = 
     case 64: return attn::kernel_info_hd64(group, variant, multi);
     case 128: return attn::kernel_info_hd128(group, variant, multi);
     case 256: return attn::kernel_info_hd256(group, variant, multi);
-    default: return attn::KernelInfo{0, 0, 0, false};
+    default: return attn::KernelInfo{0, 0, 0, false, 0};
     }
 }
 
@@ -126,9 +126,9 @@ int heuristic(int n_seq, int n_kv_head, int qgroups, int64_t cap, int sm_count,
 {
     const int64_t units = (int64_t)n_seq * n_kv_head * (qgroups > 0 ? qgroups : 1);
     int per_sm = ki.blocks_per_sm > 0 ? ki.blocks_per_sm : 1;
-    if (kv_stable && n_seq == 1 && cap > 0 && sm_count > 0 &&
-        (cap * units + sm_count - 1) / sm_count <= (int64_t)kStableTiles * ki.tile_rows)
-        per_sm = 1;
+    const bool short_stable = kv_stable && n_seq == 1 && cap > 0 && sm_count > 0 &&
+        (cap * units + sm_count - 1) / sm_count <= (int64_t)kStableTiles * ki.tile_rows;
+    if (short_stable) per_sm = 1;
     const int64_t slots = (int64_t)sm_count * per_sm;
     const int64_t gran = ki.granule > 0 ? ki.granule : attn::kSplitGranule;
     int64_t P;
@@ -136,6 +136,10 @@ int heuristic(int n_seq, int n_kv_head, int qgroups, int64_t cap, int sm_count,
         const int64_t waves = n_seq > 1 ? 8 : 1;
         int64_t chunk = (cap * units + waves * slots - 1) / (waves * slots);
         chunk = (chunk + gran - 1) / gran * gran;
+        // a short early-start block takes no more rows than its stage ring
+        // holds, so that all of its copies start before the grid dependency
+        const int64_t ring = (int64_t)ki.stages * ki.tile_rows;
+        if (short_stable && ring >= gran && chunk > ring) chunk = ring / gran * gran;
         P = (cap + chunk - 1) / chunk;
     } else {
         P = slots / (units > 0 ? units : 1);

@@ -135,13 +135,14 @@ cudaError_t launch_for_hd(const LaunchRequest &r)
 template <int HD>
 KernelInfo kernel_info_for_hd(int group, int variant, bool multi)
 {
-    KernelInfo k{0, 0, 0, false};
+    KernelInfo k{0, 0, 0, false, 0};
     if (group < 1 || group > 8) return k;
     if (variant == kVariantSimt) {
         if (multi) return k;
         using C = SimtCfg<HD, 8, __half>;   // the largest group sets the shared-memory need
         k.tile_rows = C::TILE;
-        k.granule = C::WR;
+        k.granule = C::GRANULE;
+        k.stages = C::S;
         k.blocks_per_sm = blocks_per_sm<C>();
         k.available = true;
     } else if (variant == kVariantTc) {
@@ -149,12 +150,14 @@ KernelInfo kernel_info_for_hd(int group, int variant, bool multi)
             if (multi) {
                 using C = TcMqCfg<HD, __half>;
                 k.tile_rows = C::TILE;
-                k.granule = C::WR;
+                k.granule = C::GRANULE;
+        k.stages = C::S;
                 k.blocks_per_sm = blocks_per_sm<C>();
             } else {
                 using C = TcCfg<HD, 8, __half>;
                 k.tile_rows = C::TILE;
-                k.granule = C::WR;
+                k.granule = C::GRANULE;
+        k.stages = C::S;
                 k.blocks_per_sm = blocks_per_sm<C>();
             }
             k.available = true;

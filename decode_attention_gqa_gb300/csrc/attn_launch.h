@@ -39,6 +39,7 @@ struct KernelInfo {
     int granule;             // split chunks (by count) are rounded up to this many rows
     int blocks_per_sm;       // resident blocks per SM (from its shared-memory need)
     bool available;          // compiled for this (head_dim, group)
+    int stages;              // pipeline stages (tiles in flight per block)
 };
 
 // Implemented in attn_api.cu.

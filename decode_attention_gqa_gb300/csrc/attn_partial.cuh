@@ -41,6 +41,7 @@ struct PartialCfg {
     using Warp = W<HD, G, NWC, KV>;
     static constexpr int WR = Warp::WR;
     static constexpr int TILE = NWC * WR;            // rows per stage
+    static constexpr int GRANULE = Warp::WHOLE_TILE_SPLITS ? TILE : WR;   // count-mode chunk unit
     static constexpr int THREADS = (NWC + 1) * 32;
     static constexpr int NCH = HD >= 64 ? HD / 64 : 1;
     static constexpr int BOX_X = HD >= 64 ? 64 : HD; // TMA box inner extent (elements)
@@ -111,7 +112,7 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     bool pos_ok;
     const int64_t nkv = rows_attended(a, s, sp == 0 && blockIdx.y == 0 && tid == 0, &pos_ok);
     int64_t lo, hi;
-    split_range(nkv, sp, P, a.split_len, WR, lo, hi);
+    split_range(nkv, sp, P, a.split_len, Cfg::GRANULE, lo, hi);
     if (lo >= hi) {                                                      // empty split: mx=-inf, S=0
         if (stable) pdl_wait();               // the workspace may still be read by the previous grid
         if (tid < NQH) {

@@ -16,6 +16,7 @@ namespace attn {
 template <int HD, int G, int NWC, typename KV>
 struct SimtWarp {
     static constexpr int WR = 32;                          // rows per warp slice
+    static constexpr bool WHOLE_TILE_SPLITS = false;      // count-mode splits in warp slices
     static constexpr int NQH = G;                     // query heads per block (one query row)
 
     // Partial-head index of block-local query head i (single query row: the

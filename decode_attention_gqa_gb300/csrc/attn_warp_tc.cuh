@@ -33,6 +33,9 @@ template <int HD, int G, int NWC, typename KV>
 struct TcWarp {
     static_assert(HD % 16 == 0, "tensor-core path needs head_dim % 16 == 0");
     static constexpr int WR = 16;                     // rows per warp slice
+    // count-mode splits are whole tiles (head_dim <= 128): a block's rows then
+    // fill its stage ring exactly and no split re-reads a neighbour's rows
+    static constexpr bool WHOLE_TILE_SPLITS = HD <= 128;
     static constexpr int NQH = G;                     // query heads per block (one query row)
 
     // Partial-head index of block-local query head i (single query row: the

@@ -22,6 +22,7 @@ template <int HD, int QH, int NWC, typename KV>
 struct TcWarpMQ {
     static_assert(HD % 16 == 0 && QH <= 16, "tensor-core multi-query needs head_dim % 16 == 0");
     static constexpr int WR = 16;
+    static constexpr bool WHOLE_TILE_SPLITS = false;      // count-mode splits in warp slices
     static constexpr int NQH = QH;
     static constexpr int KSTEPS = HD / 16;
     static constexpr int NTD = HD / 8;

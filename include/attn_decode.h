@@ -119,8 +119,9 @@ attn_status attn_decode(const float *q, const void *k_cache, const void *v_cache
  *   n_splits        splits P per (sequence, KV head); 0 = attn_split_heuristic_ex()
  *                   for this call's variant.
  *   split_len       0: split by count, chunk = ceil(nkv / P) rounded up to the
- *                   kernel's row granule, 16 rows (tensor cores) or 32 rows
- *                   (CUDA cores) (minfer R4 §2.2); > 0: fixed block of split_len
+ *                   kernel's row granule: 64 rows (tensor cores, head_dim <= 128,
+ *                   one query row: whole tiles), 16 rows (tensor cores otherwise)
+ *                   or 32 rows (CUDA cores) (minfer R4 §2.2); > 0: fixed block of split_len
  *                   rows per split (Red Lite dev35 "Change"), which needs
  *                   P * split_len >= cap, else ATTN_ERR_INVALID_ARG.
  *   variant         ATTN_VARIANT_*.
@@ -260,8 +261,10 @@ int attn_split_heuristic(int n_seq, int n_head, int n_kv_head, int head_dim, int
  * With ATTN_KV_STABLE, a single sequence and a short call (at most 4 kernel
  * tiles of rows per block at one block per SM) the wave is one block per SM
  * rather than as many as fit, so that the next flagged call's blocks find room
- * beside this call's and start their copies while it finishes. Returns 0 for
- * an invalid shape or variant.
+ * beside this call's and start their copies while it finishes, and a block
+ * takes no more rows than its pipeline holds at once (3 tiles of 64 rows at
+ * head_dim 128), so that all of its copies start before the previous kernel
+ * ends. Returns 0 for an invalid shape or variant.
  */
 int attn_split_heuristic_ex(int n_seq, int n_q, int n_head, int n_kv_head, int head_dim,
                             int64_t cap, int sm_count, int variant);

@@ -81,10 +81,12 @@ def test_split_heuristic_host_only(lib):
     assert 1 <= P <= 8192 // 16
     # more independent (sequence, KV head) units -> fewer splits each
     assert pkg.attn_split_heuristic(32, 32, 8, 128, 32768, 152) <= P
-    # no split is shorter than the kernel's 16-row granule: 40 rows -> 3 splits
-    assert pkg.attn_split_heuristic(1, 8, 2, 128, 40, 152) == 3
-    # one sequence fills one wave: 28/4 heads at 8192 rows -> 4 x 74 blocks of 112 rows
-    assert pkg.attn_split_heuristic(1, 28, 4, 128, 8192, 152) == 74
+    # splits of the head_dim-128 tensor-core kernel are whole 64-row tiles: 40 rows -> 1 split
+    assert pkg.attn_split_heuristic(1, 8, 2, 128, 40, 152) == 1
+    # ... and the CUDA-core kernel's are 32-row warp slices: 40 rows -> 2 splits
+    assert pkg.attn_split_heuristic_ex(1, 1, 8, 2, 128, 40, 152, pkg.ATTN_VARIANT_SIMT) == 2
+    # one sequence fills one wave: 28/4 heads at 8192 rows -> 4 x 64 blocks of 128 rows
+    assert pkg.attn_split_heuristic(1, 28, 4, 128, 8192, 152) == 64
     # a batch aims at eight waves so ragged lengths still balance
     assert pkg.attn_split_heuristic(32, 32, 8, 128, 32768, 152) == 10
     # unknown capacity: one wave of blocks over the (sequence, KV head) units
@@ -100,10 +102,13 @@ def test_split_heuristic_for_flagged_calls(lib):
         return pkg.attn_split_heuristic_ex(n_seq, n_q, n_head, n_kv, hd, cap, sms, variant)
     # the plain call and variant 0 agree; the element type does not change P
     assert h(1, 28, 4, 128, 8192, 152, 0) == pkg.attn_split_heuristic(1, 28, 4, 128, 8192, 152)
-    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_BF16) == 74
-    # early start, one sequence: one block per SM -> 4 x 37 blocks of 224 rows
-    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_STABLE) == 37
-    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_STABLE | pkg.ATTN_KV_BF16) == 37
+    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_BF16) == 64
+    # early start, one sequence: one block per SM would give each block 256 rows,
+    # more than its 3 x 64-row stage ring, so blocks of 192 rows: 4 x 43
+    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_STABLE) == 43
+    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_STABLE | pkg.ATTN_KV_BF16) == 43
+    # a shorter cache fits the ring at one block per SM: 2048 x 4 / 152 -> 64 rows
+    assert h(1, 28, 4, 128, 2048, 152, pkg.ATTN_KV_STABLE) == 32
     # a long call keeps every resident block: 131072 rows x 8 KV heads
     assert h(1, 64, 8, 128, 131072, 152, pkg.ATTN_KV_STABLE) == h(1, 64, 8, 128, 131072, 152, 0) == 38
     # a batch keeps its eight waves
@@ -115,7 +120,7 @@ def test_split_heuristic_for_flagged_calls(lib):
     # two blocks per SM: 8 x 37 blocks of 224 rows
     assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_STABLE, n_q=4) == 37
     assert h(1, 28, 4, 128, 2048, 152, pkg.ATTN_KV_STABLE, n_q=4) == 19    # short: one per SM
-    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_STABLE, n_q=2) == 37     # 14 pairs: one group
+    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_STABLE, n_q=2) == 43     # 14 pairs: one group
     assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_VARIANT_SIMT, n_q=2) == 0  # tensor cores only
     # the CUDA-core kernel has its own granule and residency
     assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_VARIANT_SIMT) >= 1
@@ -193,8 +198,8 @@ int main(void) {
     if (attn_version() <= 0) return 1;
     if (strcmp(attn_status_string(ATTN_ERR_WORKSPACE), "ATTN_ERR_WORKSPACE") != 0) return 2;
     if (attn_workspace_size(1, 28, 128, 37) == 0) return 3;
-    if (attn_split_heuristic(1, 28, 4, 128, 8192, 152) != 74) return 4;
-    if (attn_split_heuristic_ex(1, 1, 28, 4, 128, 8192, 152, ATTN_KV_STABLE) != 37) return 5;
+    if (attn_split_heuristic(1, 28, 4, 128, 8192, 152) != 64) return 4;
+    if (attn_split_heuristic_ex(1, 1, 28, 4, 128, 8192, 152, ATTN_KV_STABLE) != 43) return 5;
     if (attn_decode(0, 0, 0, 0, 0, 1, 28, 5, 128, 0.1f, 0) != ATTN_ERR_INVALID_ARG) return 6;
     if (attn_selftest_bounded_wait(0, 0) != ATTN_ERR_INVALID_ARG) return 7;
     printf("ok\n");

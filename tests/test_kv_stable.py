@@ -234,7 +234,7 @@ def _bench_configuration(pkg, name, L, n_q=1):
 
 
 def test_full_7b_bench_configuration(pkg):
-    assert _bench_configuration(pkg, "7b", L=4) == 37
+    assert _bench_configuration(pkg, "7b", L=4) == 43
 
 
 def test_full_long_bench_configuration(pkg):
