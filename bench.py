@@ -53,7 +53,8 @@ def parse_args():
     ap.add_argument("--ctx", type=int, default=0, help="context override (0 = the workload's)")
     ap.add_argument("--split-len", type=int, default=0, help="0 = split by count")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
-    ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 simt, 2 tensor core")
+    ap.add_argument("--variant", type=int, default=0,
+                    help="0 auto, 1 simt, 2 tensor core (mma.sync), 3 tensor core (tcgen05)")
     ap.add_argument("--splits", type=int, default=0, help="0 = library heuristic")
     ap.add_argument("--kv-dtype", choices=["f16", "bf16"], default="f16")
     ap.add_argument("--append", action="store_true",
@@ -490,7 +491,8 @@ def run_ours(args, rank, world, local):
                 "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                 "traffic": profiled_traffic("%s_ctx%d%s" % (w.name, ctx_end,
                                                             "_nq%d" % n_q if n_q > 1 else "")),
-                "kernel": "attn_split_partial" if n_q == 1 else "attn_split_partial + attn_combine",
+                "kernel": ("attn_split_partial_umma" if args.variant == 3 else "attn_split_partial")
+                          if n_q == 1 else "attn_split_partial + attn_combine",
                 "bytes_per_launch": m0["launch_bytes"],
                 "us_per_launch": round(m0["partial_us"], 3),
                 "combine_us_per_launch": round(m0["combine_us"], 3)}

@@ -17,7 +17,8 @@ import threading
 __all__ = [
     "AttnError", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_WORKSPACE",
     "ATTN_ERR_CUDA", "ATTN_DEVERR_POSITION_CLAMPED", "ATTN_DEVERR_PIPELINE_TIMEOUT",
-    "ATTN_VARIANT_AUTO", "ATTN_VARIANT_SIMT", "ATTN_VARIANT_TC", "ATTN_KV_BF16", "ATTN_KV_STABLE",
+    "ATTN_VARIANT_AUTO", "ATTN_VARIANT_SIMT", "ATTN_VARIANT_TC", "ATTN_VARIANT_TCGEN05", "ATTN_KV_BF16",
+    "ATTN_KV_STABLE",
     "library_path",
     "load",
     "attn_decode", "attn_decode_ex", "attn_decode_append", "attn_decode_multi", "decode_attention",
@@ -32,7 +33,7 @@ __all__ = [
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE, ATTN_ERR_CUDA = range(5)
 ATTN_DEVERR_POSITION_CLAMPED = 0x1
 ATTN_DEVERR_PIPELINE_TIMEOUT = 0x2
-ATTN_VARIANT_AUTO, ATTN_VARIANT_SIMT, ATTN_VARIANT_TC = 0, 1, 2
+ATTN_VARIANT_AUTO, ATTN_VARIANT_SIMT, ATTN_VARIANT_TC, ATTN_VARIANT_TCGEN05 = 0, 1, 2, 3
 ATTN_KV_BF16 = 0x10
 ATTN_KV_STABLE = 0x20
 

@@ -94,7 +94,7 @@ attn::KernelInfo kernel_info(int head_dim, int group, int variant, bool multi = 
     case 64: return attn::kernel_info_hd64(group, variant, multi);
     case 128: return attn::kernel_info_hd128(group, variant, multi);
     case 256: return attn::kernel_info_hd256(group, variant, multi);
-    default: return attn::KernelInfo{0, 0, 0, false, 0};
+    default: return attn::KernelInfo{0, 0, 0, false, 0, 0};
     }
 }
 
@@ -144,6 +144,12 @@ int heuristic(int n_seq, int n_kv_head, int qgroups, int64_t cap, int sm_count,
     } else {
         P = slots / (units > 0 ? units : 1);
     }
+    // a kernel whose block takes at most max_chunk rows needs enough splits
+    // to cover the capacity
+    if (ki.max_chunk > 0 && cap > 0) {
+        const int64_t need = (cap + ki.max_chunk - 1) / ki.max_chunk;
+        if (P < need) P = need;
+    }
     if (P < 1) P = 1;
     if (P > kMaxSplits) P = kMaxSplits;
     return (int)P;
@@ -165,7 +171,8 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
     if (cap < 1) return ATTN_ERR_INVALID_ARG;
     if (n_splits < 0 || n_splits > kMaxSplits || split_len < 0) return ATTN_ERR_INVALID_ARG;
-    if (variant != ATTN_VARIANT_AUTO && variant != ATTN_VARIANT_SIMT && variant != ATTN_VARIANT_TC)
+    if (variant != ATTN_VARIANT_AUTO && variant != ATTN_VARIANT_SIMT && variant != ATTN_VARIANT_TC &&
+        variant != ATTN_VARIANT_TCGEN05)
         return ATTN_ERR_INVALID_ARG;
     if (n_seq > 0 && (!q || !k_cache || !v_cache || !positions)) return ATTN_ERR_INVALID_ARG;
     if (n_seq > 0 && (stages & attn::kStageCombine) && !out) return ATTN_ERR_INVALID_ARG;
@@ -202,6 +209,10 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
                                : heuristic(n_seq, n_kv_head, n_q > 1 ? qgroups : 1,
                                            cap_known ? cap : 0, ds->sm_count, ki, kv_stable != 0);
     if (split_len > 0 && (int64_t)P * split_len < cap) return ATTN_ERR_INVALID_ARG;
+    // one tile per block: every split must fit in max_chunk rows at any nkv <= cap
+    if (ki.max_chunk > 0 && (split_len > 0 ? split_len > ki.max_chunk
+                                           : (!cap_known || (int64_t)P * ki.max_chunk < cap)))
+        return ATTN_ERR_INVALID_ARG;
     const size_t need = attn_workspace_size(n_seq, n_q * n_head, head_dim, P);
 
     if (!workspace) {
@@ -277,21 +288,27 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
 // ---------------------------------------------------------------------------
 namespace attn {
 
+// The driver's tensor-map encoder, looked up once.
+static cudaError_t load_encoder()
+{
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                         cudaEnableDefault, &qr);
+        if (e != cudaSuccess) return e;
+        if (qr != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    return cudaSuccess;
+}
+
 cudaError_t encode_kv_map(CUtensorMap *map, const void *base, int64_t rows, int n_kv_head,
                           int head_dim, int box_x, int box_rows, int kv_dtype)
 {
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (!g_encode) {
-            void *fn = nullptr;
-            cudaDriverEntryPointQueryResult qr;
-            cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                             cudaEnableDefault, &qr);
-            if (e != cudaSuccess) return e;
-            if (qr != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-        }
-    }
+    const cudaError_t le = load_encoder();
+    if (le != cudaSuccess) return le;
     const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)n_kv_head, (cuuint64_t)rows};
     const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)n_kv_head * head_dim * 2};
     const cuuint32_t box[3] = {(cuuint32_t)box_x, 1u, (cuuint32_t)box_rows};
@@ -302,6 +319,26 @@ cudaError_t encode_kv_map(CUtensorMap *map, const void *base, int64_t rows, int 
     const CUresult r = g_encode(map, dt, 3, const_cast<void *>(base), dims,
                                 strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t encode_kv_map4(CUtensorMap *map, const void *base, int n_seq, int64_t cap, int n_kv_head,
+                           int head_dim, int box_x, int box_rows, int kv_dtype)
+{
+    const cudaError_t le = load_encoder();
+    if (le != cudaSuccess) return le;
+    const cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)n_kv_head, (cuuint64_t)cap,
+                                (cuuint64_t)n_seq};
+    const cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2, (cuuint64_t)n_kv_head * head_dim * 2,
+                                   (cuuint64_t)cap * n_kv_head * head_dim * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)box_x, 1u, (cuuint32_t)box_rows, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUtensorMapSwizzle sw = (box_x * 2 == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+    const CUtensorMapDataType dt = kv_dtype == kKvBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUresult r = g_encode(map, dt, 4, const_cast<void *>(base), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -444,7 +481,8 @@ int attn_split_heuristic_ex(int n_seq, int n_q, int n_head, int n_kv_head, int h
 {
     const bool stable = (variant & ATTN_KV_STABLE) != 0;
     variant &= ~(ATTN_KV_BF16 | ATTN_KV_STABLE);
-    if (variant != ATTN_VARIANT_AUTO && variant != ATTN_VARIANT_SIMT && variant != ATTN_VARIANT_TC)
+    if (variant != ATTN_VARIANT_AUTO && variant != ATTN_VARIANT_SIMT && variant != ATTN_VARIANT_TC &&
+        variant != ATTN_VARIANT_TCGEN05)
         return 0;
     if (n_seq <= 0 || n_q < 1 || n_q > 1024 || n_head <= 0 || n_kv_head <= 0 ||
         n_head % n_kv_head != 0)

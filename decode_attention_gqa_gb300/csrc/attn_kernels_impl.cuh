@@ -6,6 +6,7 @@
 #include "attn_combine.cuh"
 #include "attn_launch.h"
 #include "attn_partial.cuh"
+#include "attn_partial_umma.cuh"
 
 namespace attn {
 
@@ -68,6 +69,26 @@ cudaError_t launch_partial(const LaunchRequest &r)
                       Cfg::SMEM_BYTES, r.stream, args);
 }
 
+// The tcgen05 kernel: one block per (split, KV head, sequence), one 128-row tile each.
+template <int HD, int G, typename KV>
+cudaError_t launch_partial_umma(const LaunchRequest &r)
+{
+    using C = UmmaCfg<HD, G, KV>;
+    alignas(64) CUtensorMap kmap, vmap;
+    const int dt = kv_dtype_code<KV>();
+    cudaError_t e = encode_kv_map4(&kmap, r.k_cache, r.n_seq, r.pa.cap, r.pa.n_kv_head, HD, 64, C::TILE, dt);
+    if (e != cudaSuccess) return e;
+    e = encode_kv_map4(&vmap, r.v_cache, r.n_seq, r.pa.cap, r.pa.n_kv_head, HD, 64, C::TILE, dt);
+    if (e != cudaSuccess) return e;
+    const void *fn = reinterpret_cast<const void *>(&attn_split_partial_umma<C, HD, G, KV>);
+    e = ensure_smem_attr(fn, (int)C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    PartialArgs pa = r.pa;
+    void *args[] = {&kmap, &vmap, &pa};
+    return launch_pdl(fn, dim3(pa.n_splits, pa.n_kv_head, r.n_seq), dim3(C::THREADS), C::SMEM_BYTES,
+                      r.stream, args);
+}
+
 template <int HD>
 cudaError_t launch_combine(const LaunchRequest &r)
 {
@@ -91,8 +112,14 @@ cudaError_t launch_group(const LaunchRequest &r)
     cudaError_t e = cudaSuccess;
     if (r.stages & kStagePartial) {
         if constexpr (HD % 16 == 0) {
-            if (r.variant == kVariantTc) e = launch_partial<TcCfg<HD, G, KV>, HD, G, KV>(r);
-            else e = launch_partial<SimtCfg<HD, G, KV>, HD, G, KV>(r);
+            if (r.variant == kVariantUmma) {
+                if constexpr (HD == 128) e = launch_partial_umma<HD, G, KV>(r);
+                else return cudaErrorInvalidValue;
+            } else if (r.variant == kVariantTc) {
+                e = launch_partial<TcCfg<HD, G, KV>, HD, G, KV>(r);
+            } else {
+                e = launch_partial<SimtCfg<HD, G, KV>, HD, G, KV>(r);
+            }
         } else {
             if (r.variant != kVariantSimt) return cudaErrorInvalidValue;
             e = launch_partial<SimtCfg<HD, G, KV>, HD, G, KV>(r);
@@ -135,8 +162,21 @@ cudaError_t launch_for_hd(const LaunchRequest &r)
 template <int HD>
 KernelInfo kernel_info_for_hd(int group, int variant, bool multi)
 {
-    KernelInfo k{0, 0, 0, false, 0};
+    KernelInfo k{0, 0, 0, false, 0, 0};
     if (group < 1 || group > 8) return k;
+    if (variant == kVariantUmma) {
+        if constexpr (HD == 128) {
+            if (multi) return k;
+            using C = UmmaCfg<HD, 8, __half>;
+            k.tile_rows = C::TILE;
+            k.granule = C::GRANULE;
+            k.stages = 1;
+            k.blocks_per_sm = (int)(233472u / (C::SMEM_BYTES + 1024u));
+            k.max_chunk = C::TILE;
+            k.available = true;
+        }
+        return k;
+    }
     if (variant == kVariantSimt) {
         if (multi) return k;
         using C = SimtCfg<HD, 8, __half>;   // the largest group sets the shared-memory need
@@ -151,13 +191,13 @@ KernelInfo kernel_info_for_hd(int group, int variant, bool multi)
                 using C = TcMqCfg<HD, __half>;
                 k.tile_rows = C::TILE;
                 k.granule = C::GRANULE;
-        k.stages = C::S;
+                k.stages = C::S;
                 k.blocks_per_sm = blocks_per_sm<C>();
             } else {
                 using C = TcCfg<HD, 8, __half>;
                 k.tile_rows = C::TILE;
                 k.granule = C::GRANULE;
-        k.stages = C::S;
+                k.stages = C::S;
                 k.blocks_per_sm = blocks_per_sm<C>();
             }
             k.available = true;

@@ -13,6 +13,7 @@ namespace attn {
 
 constexpr int kVariantSimt = 1;
 constexpr int kVariantTc = 2;
+constexpr int kVariantUmma = 3;             // tcgen05 kernel (attn_partial_umma.cuh)
 constexpr int kMqHeadsPerBlock = 16;        // query heads per multi-query block
 constexpr int kKvF16 = 0;
 constexpr int kKvBf16 = 1;
@@ -27,7 +28,7 @@ struct LaunchRequest {
     int n_seq;
     int head_dim;
     int group;               // G = n_head / n_kv_head
-    int variant;             // kVariantSimt / kVariantTc (resolved, never auto)
+    int variant;             // kVariantSimt / kVariantTc / kVariantUmma (resolved, never auto)
     int stages;              // kStagePartial | kStageCombine
     int kv_dtype;            // kKvF16 / kKvBf16
     cudaStream_t stream;
@@ -40,6 +41,7 @@ struct KernelInfo {
     int blocks_per_sm;       // resident blocks per SM (from its shared-memory need)
     bool available;          // compiled for this (head_dim, group)
     int stages;              // pipeline stages (tiles in flight per block)
+    int max_chunk;           // rows one block can take (0: any; the tcgen05 kernel: one tile)
 };
 
 // Implemented in attn_api.cu.
@@ -48,6 +50,11 @@ struct KernelInfo {
 // swizzle when box_x * 2 == 128.
 cudaError_t encode_kv_map(CUtensorMap *map, const void *base, int64_t rows, int n_kv_head,
                           int head_dim, int box_x, int box_rows, int kv_dtype);
+// The same cache as a 4-D tensor [n_seq][cap][n_kv_head][head_dim] with a box
+// of (box_x, 1, box_rows, 1): a box that starts before a sequence's first row
+// reads zeros there instead of the previous sequence's rows.
+cudaError_t encode_kv_map4(CUtensorMap *map, const void *base, int n_seq, int64_t cap, int n_kv_head,
+                           int head_dim, int box_x, int box_rows, int kv_dtype);
 // Opt a kernel into `bytes` of dynamic shared memory (when above 48 KB) and the
 // largest shared-memory carve-out (once per device).
 cudaError_t ensure_smem_attr(const void *func, int bytes);

@@ -74,6 +74,12 @@ typedef enum {
                                  p each carried as a hi + lo pair of the cache's element type (about
                                  22 significant bits for f16, 16 for bf16); head_dim 64, 128, 256
                                  only (ATTN_ERR_UNSUPPORTED otherwise) */
+#define ATTN_VARIANT_TCGEN05 3 /* tensor-core partial kernel on tcgen05 (accumulators in tensor
+                                 memory): one 128-row tile per block, q and p as the same hi + lo
+                                 pairs, a block-wide softmax in one pass; head_dim 128 and one
+                                 query row only (ATTN_ERR_UNSUPPORTED otherwise). Every split must
+                                 fit one tile: split_len <= 128, or by count n_splits * 128 >= cap
+                                 (ATTN_ERR_INVALID_ARG otherwise; the heuristic picks such a count) */
 
 /* Cache element type, OR'd into the variant argument: without it K and V are
    IEEE binary16 (f16); with it they are bfloat16 (1 sign, 8 exponent, 7
