@@ -176,7 +176,7 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
         return ATTN_ERR_INVALID_ARG;
     if (n_seq > 0 && (!q || !k_cache || !v_cache || !positions)) return ATTN_ERR_INVALID_ARG;
     if (n_seq > 0 && (stages & attn::kStageCombine) && !out) return ATTN_ERR_INVALID_ARG;
-    if (n_seq > 65535 || n_kv_head > 65535) return ATTN_ERR_INVALID_ARG;   // grid y / z limits
+    if (n_seq > 65535 || n_kv_head > 65535) return ATTN_ERR_INVALID_ARG;   // grid z limit; heads kept as before
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(positions) ||
         !aligned16(out) || !aligned16(k_new) || !aligned16(v_new))
         return ATTN_ERR_INVALID_ARG;

@@ -65,7 +65,7 @@ cudaError_t launch_partial(const LaunchRequest &r)
     if (e != cudaSuccess) return e;
     PartialArgs pa = r.pa;
     void *args[] = {&kmap, &vmap, &pa};
-    return launch_pdl(fn, dim3(pa.n_splits, pa.n_kv_head * pa.qgroups, r.n_seq), dim3(Cfg::THREADS),
+    return launch_pdl(fn, dim3(pa.n_kv_head * pa.qgroups, pa.n_splits, r.n_seq), dim3(Cfg::THREADS),
                       Cfg::SMEM_BYTES, r.stream, args);
 }
 
@@ -85,7 +85,7 @@ cudaError_t launch_partial_umma(const LaunchRequest &r)
     if (e != cudaSuccess) return e;
     PartialArgs pa = r.pa;
     void *args[] = {&kmap, &vmap, &pa};
-    return launch_pdl(fn, dim3(pa.n_splits, pa.n_kv_head, r.n_seq), dim3(C::THREADS), C::SMEM_BYTES,
+    return launch_pdl(fn, dim3(pa.n_kv_head, pa.n_splits, r.n_seq), dim3(C::THREADS), C::SMEM_BYTES,
                       r.stream, args);
 }
 

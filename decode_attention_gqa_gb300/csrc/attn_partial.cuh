@@ -83,8 +83,11 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
     uint64_t *empty = full + S;
     volatile int *flags = reinterpret_cast<volatile int *>(empty + S);   // [0] abort, [1] tiles issued
 
-    const int sp = blockIdx.x, s = blockIdx.z;
-    const int hk = blockIdx.y / a.qgroups, qg = blockIdx.y % a.qgroups;
+    // grid (KV head x query group, split, sequence): the KV heads vary
+    // fastest, so the low splits of every head -- the ones a short context
+    // fills -- are dispatched first
+    const int sp = blockIdx.y, s = blockIdx.z;
+    const int hk = blockIdx.x / a.qgroups, qg = blockIdx.x % a.qgroups;
     constexpr int NQH = Cfg::NQH;
     const size_t heads = (size_t)a.n_q * a.n_head;          // partial heads per sequence
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -110,7 +113,7 @@ attn_split_partial(const __grid_constant__ CUtensorMap kmap, const __grid_consta
 
     // a1: rows attended and this split's range; an empty split leaves at once
     bool pos_ok;
-    const int64_t nkv = rows_attended(a, s, sp == 0 && blockIdx.y == 0 && tid == 0, &pos_ok);
+    const int64_t nkv = rows_attended(a, s, sp == 0 && blockIdx.x == 0 && tid == 0, &pos_ok);
     int64_t lo, hi;
     split_range(nkv, sp, P, a.split_len, Cfg::GRANULE, lo, hi);
     if (lo >= hi) {                                                      // empty split: mx=-inf, S=0

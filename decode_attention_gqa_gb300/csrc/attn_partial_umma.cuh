@@ -165,7 +165,7 @@ attn_split_partial_umma(const __grid_constant__ CUtensorMap kmap, const __grid_c
     volatile int *flags = reinterpret_cast<volatile int *>(tslot + 1);   // [0] abort
     float *red = reinterpret_cast<float *>(smem + Cfg::OFF_RED);
 
-    const int sp = blockIdx.x, hk = blockIdx.y, s = blockIdx.z;
+    const int hk = blockIdx.x, sp = blockIdx.y, s = blockIdx.z;   // KV heads vary fastest
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = a.n_splits;
     const size_t heads = (size_t)a.n_head;
