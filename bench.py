@@ -435,6 +435,12 @@ def run_ours(args, rank, world, local):
         P0 = pkg.attn_split_heuristic_ex(n_seq, n_q, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0,
                                          variant | (pkg.ATTN_KV_STABLE
                                                     if args.kv_stable == "on" and L > 1 else 0))
+    # the partial kernel this plan runs (variant 0 resolves by the call's shape;
+    # explicit splits longer than one 128-row tile keep the mma.sync kernel)
+    resolved = pkg.attn_resolve_variant(n_seq, n_q, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0,
+                                        variant)
+    if resolved == 3 and not (blk0 <= 128 if blk0 else P0 * 128 >= w.cap):
+        resolved = 2
     plan = Plan(P0, blk0)
     ctx_end = max(w.ctx)
     clocks = ClockSampler(local, enabled=not args.no_clocks)
@@ -491,8 +497,9 @@ def run_ours(args, rank, world, local):
                 "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                 "traffic": profiled_traffic("%s_ctx%d%s" % (w.name, ctx_end,
                                                             "_nq%d" % n_q if n_q > 1 else "")),
-                "kernel": ("attn_split_partial_umma" if args.variant == 3 else "attn_split_partial")
+                "kernel": ("attn_split_partial_umma" if resolved == 3 else "attn_split_partial")
                           if n_q == 1 else "attn_split_partial + attn_combine",
+                "partial_variant": {1: "simt", 2: "mma.sync", 3: "tcgen05"}.get(resolved, resolved),
                 "bytes_per_launch": m0["launch_bytes"],
                 "us_per_launch": round(m0["partial_us"], 3),
                 "combine_us_per_launch": round(m0["combine_us"], 3)}

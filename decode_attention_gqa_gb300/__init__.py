@@ -25,7 +25,7 @@ __all__ = [
     "attn_decode_partial",
     "attn_decode_combine",
     "attn_decode_static",
-    "attn_split_heuristic", "attn_split_heuristic_ex", "attn_workspace_size",
+    "attn_split_heuristic", "attn_split_heuristic_ex", "attn_resolve_variant", "attn_workspace_size",
     "attn_read_device_error", "attn_selftest_bounded_wait", "attn_status_string",
     "attn_last_cuda_error", "attn_version",
 ]
@@ -91,6 +91,8 @@ def load():
         lib.attn_split_heuristic.argtypes = [i32, i32, i32, i32, i64, i32]
         lib.attn_split_heuristic_ex.restype = i32
         lib.attn_split_heuristic_ex.argtypes = [i32, i32, i32, i32, i32, i64, i32, i32]
+        lib.attn_resolve_variant.restype = i32
+        lib.attn_resolve_variant.argtypes = [i32, i32, i32, i32, i32, i64, i32, i32]
         lib.attn_workspace_size.restype = sz
         lib.attn_workspace_size.argtypes = [i32, i32, i32, i32]
         lib.attn_read_device_error.restype = i32
@@ -264,6 +266,13 @@ def attn_split_heuristic(n_seq, n_head, n_kv_head, head_dim, cap, sm_count) -> i
 def attn_split_heuristic_ex(n_seq, n_q, n_head, n_kv_head, head_dim, cap, sm_count, variant) -> int:
     return load().attn_split_heuristic_ex(n_seq, n_q, n_head, n_kv_head, head_dim, cap, sm_count,
                                           variant)
+
+
+def attn_resolve_variant(n_seq, n_q, n_head, n_kv_head, head_dim, cap, sm_count, variant) -> int:
+    """The partial kernel (ATTN_VARIANT_SIMT / _TC / _TCGEN05) such a call runs with
+    the heuristic's split count; 0 for an unsupported shape."""
+    return load().attn_resolve_variant(n_seq, n_q, n_head, n_kv_head, head_dim, cap, sm_count,
+                                       variant)
 
 
 def attn_workspace_size(n_seq, n_head, head_dim, n_splits) -> int:

@@ -100,15 +100,27 @@ attn::KernelInfo kernel_info(int head_dim, int group, int variant, bool multi = 
 
 bool head_dim_supported(int hd) { return hd == 8 || hd == 64 || hd == 128 || hd == 256; }
 
-// ATTN_VARIANT_AUTO: the tensor-core kernel wherever it is compiled
-// (head_dim % 16 == 0); it was measured faster than the CUDA-core kernel for
-// every group size. head_dim 8 runs on CUDA cores.
+// ATTN_VARIANT_AUTO, first choice: the mma.sync tensor-core kernel wherever it
+// is compiled (head_dim % 16 == 0); it was measured faster than the CUDA-core
+// kernel for every group size. head_dim 8 runs on CUDA cores.
 int resolve_variant(int variant, int head_dim, int group)
 {
     (void)group;
     if (variant == ATTN_VARIANT_AUTO)
         return head_dim % 16 == 0 ? attn::kVariantTc : attn::kVariantSimt;
     return variant;
+}
+
+// ATTN_VARIANT_AUTO prefers the tcgen05 kernel for calls bound by latency
+// rather than bandwidth: head_dim 128, one query row, a known capacity, and at
+// full capacity at most kStableTiles 128-row tiles per SM over the whole call.
+// There it was measured as fast or faster at every context of the 7b-like
+// layer (one block per tile, no warp merge); on long caches and batches the
+// mma.sync kernel streams faster.
+bool auto_prefers_umma(int head_dim, int n_q, int n_seq, int n_kv_head, int64_t cap, int sm_count)
+{
+    return head_dim == 128 && n_q == 1 && cap > 0 && sm_count > 0 &&
+           cap * n_seq * n_kv_head <= (int64_t)sm_count * kStableTiles * 128;
 }
 
 // Static split count P (the host never sees nkv). With the capacity known,
@@ -188,10 +200,10 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     if (n_q > 1 && k_new) return ATTN_ERR_INVALID_ARG;
     if (!head_dim_supported(head_dim) || group > 8) return ATTN_ERR_UNSUPPORTED;
     if (n_q > 1 && (head_dim % 16 != 0 || variant == ATTN_VARIANT_SIMT)) return ATTN_ERR_UNSUPPORTED;
-    const int v = resolve_variant(variant, head_dim, group);
+    int v = resolve_variant(variant, head_dim, group);
     const int qgroups = (n_q * group + attn::kMqHeadsPerBlock - 1) / attn::kMqHeadsPerBlock;
     if (n_q > 1 && (int64_t)n_kv_head * qgroups > 65535) return ATTN_ERR_INVALID_ARG;
-    const attn::KernelInfo ki = kernel_info(head_dim, group, v, n_q > 1);
+    attn::KernelInfo ki = kernel_info(head_dim, group, v, n_q > 1);
     if (!ki.available) return ATTN_ERR_UNSUPPORTED;
     if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return ATTN_ERR_INVALID_ARG;
     if (n_seq == 0) return ATTN_OK;
@@ -205,6 +217,17 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     e = device_state(dev, &ds);
     if (e != cudaSuccess) return cuda_fail(e);
 
+    if (variant == ATTN_VARIANT_AUTO &&
+        auto_prefers_umma(head_dim, n_q, n_seq, n_kv_head, cap_known ? cap : 0, ds->sm_count)) {
+        const attn::KernelInfo ku = kernel_info(head_dim, group, attn::kVariantUmma, false);
+        // explicit splits that leave a split larger than one tile keep the mma.sync kernel
+        const bool fits = split_len > 0 ? split_len <= ku.max_chunk
+                                        : n_splits == 0 || (int64_t)n_splits * ku.max_chunk >= cap;
+        if (ku.available && fits) {
+            v = attn::kVariantUmma;
+            ki = ku;
+        }
+    }
     const int P = n_splits > 0 ? n_splits
                                : heuristic(n_seq, n_kv_head, n_q > 1 ? qgroups : 1,
                                            cap_known ? cap : 0, ds->sm_count, ki, kv_stable != 0);
@@ -476,10 +499,16 @@ attn_status attn_decode_combine(const void *workspace, size_t workspace_bytes, f
     return ATTN_OK;
 }
 
-int attn_split_heuristic_ex(int n_seq, int n_q, int n_head, int n_kv_head, int head_dim,
-                            int64_t cap, int sm_count, int variant)
+} // extern "C"
+
+namespace {
+
+// The kernel a call with the heuristic's split count runs (and that kernel's
+// properties), or 0 when the shape is not supported. sm_count <= 0: the
+// current device's.
+int plan_variant(int n_seq, int n_q, int n_head, int n_kv_head, int head_dim, int64_t cap,
+                 int &sm_count, int variant, attn::KernelInfo &ki)
 {
-    const bool stable = (variant & ATTN_KV_STABLE) != 0;
     variant &= ~(ATTN_KV_BF16 | ATTN_KV_STABLE);
     if (variant != ATTN_VARIANT_AUTO && variant != ATTN_VARIANT_SIMT && variant != ATTN_VARIANT_TC &&
         variant != ATTN_VARIANT_TCGEN05)
@@ -495,11 +524,33 @@ int attn_split_heuristic_ex(int n_seq, int n_q, int n_head, int n_kv_head, int h
         if (cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return 0;
     }
-    const attn::KernelInfo ki =
-        kernel_info(head_dim, group, resolve_variant(variant, head_dim, group), n_q > 1);
-    if (!ki.available) return 0;
+    int v = resolve_variant(variant, head_dim, group);
+    if (variant == ATTN_VARIANT_AUTO && auto_prefers_umma(head_dim, n_q, n_seq, n_kv_head, cap, sm_count) &&
+        kernel_info(head_dim, group, attn::kVariantUmma, false).available)
+        v = attn::kVariantUmma;
+    ki = kernel_info(head_dim, group, v, n_q > 1);
+    return ki.available ? v : 0;
+}
+
+} // namespace
+
+extern "C" {
+
+int attn_split_heuristic_ex(int n_seq, int n_q, int n_head, int n_kv_head, int head_dim,
+                            int64_t cap, int sm_count, int variant)
+{
+    attn::KernelInfo ki{};
+    if (!plan_variant(n_seq, n_q, n_head, n_kv_head, head_dim, cap, sm_count, variant, ki)) return 0;
+    const int group = n_head / n_kv_head;
     const int qgroups = n_q > 1 ? (n_q * group + attn::kMqHeadsPerBlock - 1) / attn::kMqHeadsPerBlock : 1;
-    return heuristic(n_seq, n_kv_head, qgroups, cap, sm_count, ki, stable);
+    return heuristic(n_seq, n_kv_head, qgroups, cap, sm_count, ki, (variant & ATTN_KV_STABLE) != 0);
+}
+
+int attn_resolve_variant(int n_seq, int n_q, int n_head, int n_kv_head, int head_dim, int64_t cap,
+                         int sm_count, int variant)
+{
+    attn::KernelInfo ki{};
+    return plan_variant(n_seq, n_q, n_head, n_kv_head, head_dim, cap, sm_count, variant, ki);
 }
 
 int attn_split_heuristic(int n_seq, int n_head, int n_kv_head, int head_dim, int64_t cap,

@@ -135,7 +135,7 @@ struct UmmaCfg {
     static constexpr int TILE = 128;                  // rows per block (one MMA M extent)
     static constexpr int THREADS = 192;               // TMA/MMA warp, TMEM warp, 4 softmax warps
     static constexpr int NCH = HD / 64;               // 128-byte column chunks per row
-    static constexpr int GRANULE = 16;                // count-mode chunk unit (one MMA K step)
+    static constexpr int GRANULE = TILE;              // count-mode chunks are whole tiles
     using QStage = TcWarp<HD, G, 4, KV>;              // q staging: the same Q tile and scales
     static constexpr uint32_t TILE_BYTES = (uint32_t)TILE * HD * 2;
     static constexpr uint32_t OFF_K = 0;

@@ -68,7 +68,8 @@ typedef enum {
 #define ATTN_DEVERR_PIPELINE_TIMEOUT 0x2u  /* a bounded in-kernel wait gave up (block skipped) */
 
 /* Kernel variants for attn_decode_ex. */
-#define ATTN_VARIANT_AUTO 0   /* tensor cores where compiled (head_dim % 16 == 0), else CUDA cores */
+#define ATTN_VARIANT_AUTO 0   /* tensor cores where compiled (head_dim % 16 == 0), else CUDA cores;
+                                 the tcgen05 kernel for short calls (attn_resolve_variant) */
 #define ATTN_VARIANT_SIMT 1   /* CUDA-core f32 partial kernel (every head_dim) */
 #define ATTN_VARIANT_TC   2   /* tensor-core partial kernel: 16x8x16 MMA, f32 accumulate, q and
                                  p each carried as a hi + lo pair of the cache's element type (about
@@ -274,6 +275,20 @@ int attn_split_heuristic(int n_seq, int n_head, int n_kv_head, int head_dim, int
  */
 int attn_split_heuristic_ex(int n_seq, int n_q, int n_head, int n_kv_head, int head_dim,
                             int64_t cap, int sm_count, int variant);
+
+/*
+ * attn_resolve_variant -- which partial kernel a call with these arguments and
+ * n_splits = 0 runs: ATTN_VARIANT_SIMT, ATTN_VARIANT_TC or ATTN_VARIANT_TCGEN05
+ * (0 for an invalid shape or variant). An explicit variant is returned as is;
+ * ATTN_VARIANT_AUTO picks the tcgen05 kernel for a short call -- head_dim 128,
+ * one query row, cap > 0 and cap * n_seq * n_kv_head at most 4 tiles of 128
+ * rows per SM -- and otherwise the mma.sync tensor-core kernel (head_dim % 16
+ * == 0) or the CUDA-core kernel. With explicit splits that leave a split
+ * longer than 128 rows, attn_decode_ex keeps the mma.sync kernel instead.
+ * Host only; sm_count <= 0 queries the current device.
+ */
+int attn_resolve_variant(int n_seq, int n_q, int n_head, int n_kv_head, int head_dim, int64_t cap,
+                         int sm_count, int variant);
 
 /*
  * attn_selftest_bounded_wait -- diagnostic: launch one warp that waits on a

@@ -81,12 +81,16 @@ def test_split_heuristic_host_only(lib):
     assert 1 <= P <= 8192 // 16
     # more independent (sequence, KV head) units -> fewer splits each
     assert pkg.attn_split_heuristic(32, 32, 8, 128, 32768, 152) <= P
-    # splits of the head_dim-128 tensor-core kernel are whole 64-row tiles: 40 rows -> 1 split
+    # a short head_dim-128 call runs the tcgen05 kernel, one 128-row tile per split:
+    # 40 rows -> 1 split; the mma.sync kernel's splits are whole 64-row tiles: also 1
     assert pkg.attn_split_heuristic(1, 8, 2, 128, 40, 152) == 1
+    assert pkg.attn_split_heuristic_ex(1, 1, 8, 2, 128, 40, 152, pkg.ATTN_VARIANT_TC) == 1
     # ... and the CUDA-core kernel's are 32-row warp slices: 40 rows -> 2 splits
     assert pkg.attn_split_heuristic_ex(1, 1, 8, 2, 128, 40, 152, pkg.ATTN_VARIANT_SIMT) == 2
-    # one sequence fills one wave: 28/4 heads at 8192 rows -> 4 x 64 blocks of 128 rows
+    # one sequence, 28/4 heads at 8192 rows: the tcgen05 kernel needs 8192 / 128 = 64
+    # splits; the mma.sync kernel fills one wave, 4 x 64 blocks of 128 rows
     assert pkg.attn_split_heuristic(1, 28, 4, 128, 8192, 152) == 64
+    assert pkg.attn_split_heuristic_ex(1, 1, 28, 4, 128, 8192, 152, pkg.ATTN_VARIANT_TC) == 64
     # a batch aims at eight waves so ragged lengths still balance
     assert pkg.attn_split_heuristic(32, 32, 8, 128, 32768, 152) == 10
     # unknown capacity: one wave of blocks over the (sequence, KV head) units
@@ -103,12 +107,17 @@ def test_split_heuristic_for_flagged_calls(lib):
     # the plain call and variant 0 agree; the element type does not change P
     assert h(1, 28, 4, 128, 8192, 152, 0) == pkg.attn_split_heuristic(1, 28, 4, 128, 8192, 152)
     assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_BF16) == 64
-    # early start, one sequence: one block per SM would give each block 256 rows,
-    # more than its 3 x 64-row stage ring, so blocks of 192 rows: 4 x 43
-    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_STABLE) == 43
-    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_STABLE | pkg.ATTN_KV_BF16) == 43
+    # variant 0 on this short call is the tcgen05 kernel: one 128-row tile per split
+    S, TC, T5 = pkg.ATTN_KV_STABLE, pkg.ATTN_VARIANT_TC, pkg.ATTN_VARIANT_TCGEN05
+    assert h(1, 28, 4, 128, 8192, 152, S) == h(1, 28, 4, 128, 8192, 152, T5 | S) == 64
+    assert h(1, 28, 4, 128, 8192, 152, S | pkg.ATTN_KV_BF16) == 64
+    assert h(1, 28, 4, 128, 2048, 152, S) == 16
+    # mma.sync kernel, early start, one sequence: one block per SM would give each
+    # block 256 rows, more than its 3 x 64-row stage ring, so blocks of 192 rows: 4 x 43
+    assert h(1, 28, 4, 128, 8192, 152, TC | S) == 43
+    assert h(1, 28, 4, 128, 8192, 152, TC | S | pkg.ATTN_KV_BF16) == 43
     # a shorter cache fits the ring at one block per SM: 2048 x 4 / 152 -> 64 rows
-    assert h(1, 28, 4, 128, 2048, 152, pkg.ATTN_KV_STABLE) == 32
+    assert h(1, 28, 4, 128, 2048, 152, TC | S) == 32
     # a long call keeps every resident block: 131072 rows x 8 KV heads
     assert h(1, 64, 8, 128, 131072, 152, pkg.ATTN_KV_STABLE) == h(1, 64, 8, 128, 131072, 152, 0) == 38
     # a batch keeps its eight waves
@@ -126,6 +135,34 @@ def test_split_heuristic_for_flagged_calls(lib):
     assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_VARIANT_SIMT) >= 1
     assert h(1, 28, 4, 128, 8192, 152, 7) == 0                           # no such variant
     assert h(1, 28, 4, 128, 8192, 152, 0, n_q=0) == 0
+
+
+def test_resolved_variant(lib):
+    r = pkg.attn_resolve_variant
+    S, B = pkg.ATTN_KV_STABLE, pkg.ATTN_KV_BF16
+    T5, TC, SI = pkg.ATTN_VARIANT_TCGEN05, pkg.ATTN_VARIANT_TC, pkg.ATTN_VARIANT_SIMT
+    # variant 0: the tcgen05 kernel for a short head_dim-128 call of one query row
+    assert r(1, 1, 28, 4, 128, 8192, 152, 0) == T5
+    assert r(1, 1, 28, 4, 128, 8192, 152, S | B) == T5
+    assert r(1, 1, 8, 2, 128, 40, 152, 0) == T5
+    # ... the mma.sync kernel for long caches, batches, several query rows, other
+    # head dims and an unknown capacity; CUDA cores for head_dim 8
+    assert r(1, 1, 64, 8, 128, 131072, 152, 0) == TC
+    assert r(32, 1, 32, 8, 128, 32768, 152, 0) == TC
+    assert r(1, 4, 28, 4, 128, 8192, 152, 0) == TC
+    assert r(1, 1, 16, 2, 256, 8400, 152, 0) == TC
+    assert r(1, 1, 28, 4, 128, 0, 152, 0) == TC
+    assert r(1, 1, 4, 2, 8, 64, 152, 0) == SI
+    # the boundary: cap * n_seq * n_kv_head <= 4 tiles of 128 rows per SM
+    assert r(1, 1, 28, 4, 128, 152 * 128, 152, 0) == T5
+    assert r(1, 1, 28, 4, 128, 152 * 128 + 1, 152, 0) == TC
+    # explicit variants are kept; tcgen05 is built for head_dim 128 and one query row
+    assert r(1, 1, 28, 4, 128, 8192, 152, SI) == SI
+    assert r(1, 1, 28, 4, 128, 8192, 152, TC) == TC
+    assert r(1, 1, 64, 8, 128, 131072, 152, T5) == T5
+    assert r(1, 1, 8, 2, 64, 1024, 152, T5) == 0
+    assert r(1, 2, 8, 2, 128, 1024, 152, T5) == 0
+    assert r(1, 1, 28, 5, 128, 8192, 152, 0) == 0
 
 
 def _ex(lib, **kw):
@@ -199,7 +236,9 @@ int main(void) {
     if (strcmp(attn_status_string(ATTN_ERR_WORKSPACE), "ATTN_ERR_WORKSPACE") != 0) return 2;
     if (attn_workspace_size(1, 28, 128, 37) == 0) return 3;
     if (attn_split_heuristic(1, 28, 4, 128, 8192, 152) != 64) return 4;
-    if (attn_split_heuristic_ex(1, 1, 28, 4, 128, 8192, 152, ATTN_KV_STABLE) != 43) return 5;
+    if (attn_split_heuristic_ex(1, 1, 28, 4, 128, 8192, 152, ATTN_KV_STABLE | ATTN_VARIANT_TC) != 43)
+        return 5;
+    if (attn_split_heuristic_ex(1, 1, 28, 4, 128, 8192, 152, ATTN_VARIANT_TCGEN05) != 64) return 10;
     if (attn_decode(0, 0, 0, 0, 0, 1, 28, 5, 128, 0.1f, 0) != ATTN_ERR_INVALID_ARG) return 6;
     if (attn_selftest_bounded_wait(0, 0) != ATTN_ERR_INVALID_ARG) return 7;
     printf("ok\n");

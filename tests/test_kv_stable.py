@@ -170,7 +170,7 @@ def test_stable_flag_accepted_with_every_entry_point(pkg):
 
 # ------------------------------------- full size, in the launch configuration bench.py times
 
-def _bench_configuration(pkg, name, L, n_q=1):
+def _bench_configuration(pkg, name, L, n_q=1, variant=0):
     """L independent layers of a workload at full size in one captured graph:
     positions += 1, then layer 0 without and layers 1.. with ATTN_KV_STABLE,
     split count from attn_split_heuristic_ex for that flag -- the step bench.py
@@ -186,7 +186,7 @@ def _bench_configuration(pkg, name, L, n_q=1):
     pos = torch.from_numpy(layers[0]["positions"] - 1).cuda()
     outs = [torch.full_like(d["q"], float("nan")) for d in dev]
     P = pkg.attn_split_heuristic_ex(w.n_seq, n_q, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0,
-                                    pkg.ATTN_KV_STABLE)
+                                    variant | pkg.ATTN_KV_STABLE)
     ws_bytes = pkg.attn_workspace_size(w.n_seq, n_q * w.n_head, w.head_dim, P)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     s = torch.cuda.Stream()
@@ -194,7 +194,7 @@ def _bench_configuration(pkg, name, L, n_q=1):
     def step():
         pos.add_(1)
         for l in range(L):
-            var = pkg.ATTN_KV_STABLE if l > 0 else 0
+            var = variant | (pkg.ATTN_KV_STABLE if l > 0 else 0)
             if n_q > 1:
                 pkg.attn_decode_multi(dev[l]["q"], dev[l]["k"], dev[l]["v"], pos, outs[l], w.n_seq,
                                       n_q, w.n_head, w.n_kv_head, w.head_dim, w.scale, w.cap,
@@ -234,7 +234,10 @@ def _bench_configuration(pkg, name, L, n_q=1):
 
 
 def test_full_7b_bench_configuration(pkg):
-    assert _bench_configuration(pkg, "7b", L=4) == 43
+    # variant 0 runs this short call on the tcgen05 kernel: 8192 / 128 = 64 splits
+    assert _bench_configuration(pkg, "7b", L=4) == 64
+    # the mma.sync kernel at its own split count (blocks of its three-tile ring)
+    assert _bench_configuration(pkg, "7b", L=3, variant=pkg.ATTN_VARIANT_TC) == 43
 
 
 def test_full_long_bench_configuration(pkg):
