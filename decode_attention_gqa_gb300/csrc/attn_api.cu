@@ -112,14 +112,14 @@ int resolve_variant(int variant, int head_dim, int group)
 }
 
 // ATTN_VARIANT_AUTO prefers the tcgen05 kernel for calls bound by latency
-// rather than bandwidth: head_dim 128, one query row, a known capacity, and at
-// full capacity at most kStableTiles 128-row tiles per SM over the whole call.
-// There it was measured as fast or faster at every context of the 7b-like
-// layer (one block per tile, no warp merge); on long caches and batches the
-// mma.sync kernel streams faster.
+// rather than bandwidth: head_dim 128 or 256, one query row, a known capacity,
+// and at full capacity at most kStableTiles 128-row tiles per SM over the whole
+// call. There it was measured as fast or faster at every context of the
+// 7b-like layer and on the head_dim-256 layer (one block per tile, no warp
+// merge); on long caches and batches the mma.sync kernel streams faster.
 bool auto_prefers_umma(int head_dim, int n_q, int n_seq, int n_kv_head, int64_t cap, int sm_count)
 {
-    return head_dim == 128 && n_q == 1 && cap > 0 && sm_count > 0 &&
+    return (head_dim == 128 || head_dim == 256) && n_q == 1 && cap > 0 && sm_count > 0 &&
            cap * n_seq * n_kv_head <= (int64_t)sm_count * kStableTiles * 128;
 }
 
@@ -220,10 +220,15 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     if (variant == ATTN_VARIANT_AUTO &&
         auto_prefers_umma(head_dim, n_q, n_seq, n_kv_head, cap_known ? cap : 0, ds->sm_count)) {
         const attn::KernelInfo ku = kernel_info(head_dim, group, attn::kVariantUmma, false);
-        // explicit splits that leave a split larger than one tile keep the mma.sync kernel
+        // explicit splits that leave a split larger than one tile keep the mma.sync kernel,
+        // and so do splits that need more than one wave of its blocks (short split
+        // lengths: one tile per block leaves the blocks too little work each)
         const bool fits = split_len > 0 ? split_len <= ku.max_chunk
                                         : n_splits == 0 || (int64_t)n_splits * ku.max_chunk >= cap;
-        if (ku.available && fits) {
+        const int64_t pu = n_splits > 0 ? n_splits
+                                        : heuristic(n_seq, n_kv_head, 1, cap, ds->sm_count, ku, kv_stable != 0);
+        const bool one_wave = pu * n_kv_head * n_seq <= (int64_t)ds->sm_count * ku.blocks_per_sm;
+        if (ku.available && fits && one_wave) {
             v = attn::kVariantUmma;
             ki = ku;
         }

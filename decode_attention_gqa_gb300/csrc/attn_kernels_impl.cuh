@@ -113,7 +113,7 @@ cudaError_t launch_group(const LaunchRequest &r)
     if (r.stages & kStagePartial) {
         if constexpr (HD % 16 == 0) {
             if (r.variant == kVariantUmma) {
-                if constexpr (HD == 128) e = launch_partial_umma<HD, G, KV>(r);
+                if constexpr (HD == 128 || HD == 256) e = launch_partial_umma<HD, G, KV>(r);
                 else return cudaErrorInvalidValue;
             } else if (r.variant == kVariantTc) {
                 e = launch_partial<TcCfg<HD, G, KV>, HD, G, KV>(r);
@@ -165,7 +165,7 @@ KernelInfo kernel_info_for_hd(int group, int variant, bool multi)
     KernelInfo k{0, 0, 0, false, 0, 0};
     if (group < 1 || group > 8) return k;
     if (variant == kVariantUmma) {
-        if constexpr (HD == 128) {
+        if constexpr (HD == 128 || HD == 256) {
             if (multi) return k;
             using C = UmmaCfg<HD, 8, __half>;
             k.tile_rows = C::TILE;

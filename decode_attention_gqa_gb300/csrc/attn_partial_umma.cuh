@@ -1,6 +1,6 @@
 // attn_partial_umma.cuh -- the split partial kernel on the fifth-generation
 // tensor cores (tcgen05, accumulators in tensor memory): steps a1-a6 for a
-// split of at most 128 rows, one query row, head_dim 128.
+// split of at most 128 rows, one query row, head_dim 128 or 256.
 //
 // One block per (split sp, KV head hk, sequence s), the static grid of minfer
 // "10 · R4" §2.2 with the KV head in place of the query head (Red Lite dev35
@@ -19,8 +19,9 @@
 //      thread), take each head's maximum over the block, p = 2^(s - m + OFF)
 //      (0 outside the split), and store p as a hi/lo pair of 16-bit values:
 //      P[row][g] = hi, P[row][8 + g] = lo.
-//   4. The same thread issues Oᵀ = Vᵀ · P: M = head_dim, N = 16, K = 128 rows,
-//      into a second tensor-memory accumulator.
+//   4. The same thread issues Oᵀ = Vᵀ · P: M = 128 dimensions per MMA (two
+//      halves at head_dim 256), N = 16, K = 128 rows, into tensor-memory
+//      accumulators of their own.
 //   5. The four warps read Oᵀ back, one dimension per thread, and write the
 //      partial triple (mx, S, oc) of every head (§3.2); column g plus column
 //      8 + g is head g's accumulator.
@@ -131,10 +132,11 @@ __device__ __forceinline__ uint32_t p_offset(int row, int n)
 
 template <int HD, int G, typename KV>
 struct UmmaCfg {
-    static_assert(HD == 128, "the tcgen05 partial kernel is built for head_dim 128");
+    static_assert(HD == 128 || HD == 256, "the tcgen05 partial kernel is built for head_dim 128 and 256");
     static constexpr int TILE = 128;                  // rows per block (one MMA M extent)
     static constexpr int THREADS = 192;               // TMA/MMA warp, TMEM warp, 4 softmax warps
     static constexpr int NCH = HD / 64;               // 128-byte column chunks per row
+    static constexpr int NMO = HD / 128;              // 128-dimension halves of Oᵀ (one MMA M each)
     static constexpr int GRANULE = TILE;              // count-mode chunks are whole tiles
     using QStage = TcWarp<HD, G, 4, KV>;              // q staging: the same Q tile and scales
     static constexpr uint32_t TILE_BYTES = (uint32_t)TILE * HD * 2;
@@ -146,7 +148,8 @@ struct UmmaCfg {
     static constexpr uint32_t OFF_RED = OFF_P + P_BYTES;          // [2][4][8] floats: maxima, sums
     static constexpr uint32_t OFF_BAR = OFF_RED + 2 * 4 * 8 * 4;  // 4 mbarriers, TMEM slot, flags
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 4 * 8 + 16 + 1024;   // + base alignment slack
-    static constexpr uint32_t TMEM_COLS = 32;         // S in columns 0-15, Oᵀ in 16-31
+    // S in columns 0-15, Oᵀ half h in 16 + 16h .. 31 + 16h (a power of two >= 32)
+    static constexpr uint32_t TMEM_COLS = NMO == 1 ? 32 : 64;
     static constexpr float OFF = 7.f;                 // p headroom: p <= 2^OFF
     static_assert(OFF_Q % 1024 == 0 && OFF_V % 1024 == 0, "swizzled operands start 1024-aligned");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -215,13 +218,18 @@ attn_split_partial_umma(const __grid_constant__ CUtensorMap kmap, const __grid_c
     // Fused append: the split ending at nkv holds the new row nkv - 1 as the
     // tile's last row. Warp 0 fetches it now (one 16-byte unit per lane) and
     // writes it into the tile and the cache once the copy has landed.
-    constexpr int NU = HD / 8;
-    static_assert(2 * NU == 32, "one unit of the new K/V row per lane");
+    constexpr int NU = HD / 8;                    // 16-byte units per row
+    constexpr int NJ = 2 * NU / 32;               // units of the new K and V rows per lane
+    static_assert(2 * NU % 32 == 0, "whole units per lane");
     const bool appending = a.k_new != nullptr && pos_ok && hi == nkv && warp == 0;
-    uint4 newrow = make_uint4(0u, 0u, 0u, 0u);
+    uint4 newrow[NJ];
     if (appending) {
         const size_t src = ((size_t)s * a.n_kv_head + hk) * HD;
-        newrow = ld_dep(reinterpret_cast<const uint4 *>((lane < NU ? a.k_new : a.v_new) + src) + (lane % NU));
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            const int i = lane + 32 * j;
+            newrow[j] = ld_dep(reinterpret_cast<const uint4 *>((i < NU ? a.k_new : a.v_new) + src) + (i % NU));
+        }
     }
     fence_proxy_async_smem();                 // the Q tile is read by the tensor cores
     tc_fence_before();
@@ -238,9 +246,13 @@ attn_split_partial_umma(const __grid_constant__ CUtensorMap kmap, const __grid_c
         } else {
             if (appending) {
                 const size_t dst = ((size_t)((int64_t)s * a.cap + nkv - 1) * a.n_kv_head + hk) * HD;
-                uint8_t *tile = smem + (lane < NU ? Cfg::OFF_K : Cfg::OFF_V);
-                *reinterpret_cast<uint4 *>(tile + tile_unit_offset<HD, TILE>(TILE - 1, lane % NU)) = newrow;
-                reinterpret_cast<uint4 *>((lane < NU ? a.k_w : a.v_w) + dst)[lane % NU] = newrow;
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) {
+                    const int i = lane + 32 * j;
+                    uint8_t *tile = smem + (i < NU ? Cfg::OFF_K : Cfg::OFF_V);
+                    *reinterpret_cast<uint4 *>(tile + tile_unit_offset<HD, TILE>(TILE - 1, i % NU)) = newrow[j];
+                    reinterpret_cast<uint4 *>((i < NU ? a.k_w : a.v_w) + dst)[i % NU] = newrow[j];
+                }
                 fence_proxy_async_smem();
                 __syncwarp();
             }
@@ -265,13 +277,16 @@ attn_split_partial_umma(const __grid_constant__ CUtensorMap kmap, const __grid_c
             } else if (lane == 0) {
                 tc_fence_after();
                 const uint32_t sv = smem_u32(smem + Cfg::OFF_V), spp = smem_u32(smem + Cfg::OFF_P);
-                constexpr uint32_t id_o = umma_idesc<KV>(HD, 16, 1, 1);
+                constexpr uint32_t id_o = umma_idesc<KV>(128, 16, 1, 1);
+                // half h covers dimensions [128h, 128h + 128): column chunks 2h and 2h + 1;
                 // k-step kk covers tile rows [16kk, 16kk + 16): two 8-row groups of V
                 // (2048 bytes) and of P (512 bytes)
 #pragma unroll
-                for (int kk = 0; kk < TILE / 16; ++kk)
-                    umma_f16(tm_o, umma_desc(sv + kk * 2048, TILE * 128, 1024, 2),
-                             umma_desc(spp + kk * 512, 256, 128, 0), id_o, kk > 0);
+                for (int h = 0; h < Cfg::NMO; ++h)
+#pragma unroll
+                    for (int kk = 0; kk < TILE / 16; ++kk)
+                        umma_f16(tm_o + 16 * h, umma_desc(sv + h * 2 * (TILE * 128) + kk * 2048, TILE * 128, 1024, 2),
+                                 umma_desc(spp + kk * 512, 256, 128, 0), id_o, kk > 0);
                 umma_commit(bar + 3);
             }
         }
@@ -341,11 +356,14 @@ attn_split_partial_umma(const __grid_constant__ CUtensorMap kmap, const __grid_c
         }
         if (ok) {
             tc_fence_after();
-            float c[16];
-            tmem_ld16(tm_o + lane_base, c);
             const size_t slot0 = ((size_t)s * heads + (size_t)hk * G) * P + sp;
 #pragma unroll
-            for (int g = 0; g < G; ++g) a.ws_o[(slot0 + (size_t)g * P) * HD + r] = c[g] + c[8 + g];
+            for (int h = 0; h < Cfg::NMO; ++h) {
+                float c[16];
+                tmem_ld16(tm_o + 16 * h + lane_base, c);
+#pragma unroll
+                for (int g = 0; g < G; ++g) a.ws_o[(slot0 + (size_t)g * P) * HD + 128 * h + r] = c[g] + c[8 + g];
+            }
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (warp == 4 && lane < G && !flags[0]) {

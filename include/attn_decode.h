@@ -77,8 +77,8 @@ typedef enum {
                                  only (ATTN_ERR_UNSUPPORTED otherwise) */
 #define ATTN_VARIANT_TCGEN05 3 /* tensor-core partial kernel on tcgen05 (accumulators in tensor
                                  memory): one 128-row tile per block, q and p as the same hi + lo
-                                 pairs, a block-wide softmax in one pass; head_dim 128 and one
-                                 query row only (ATTN_ERR_UNSUPPORTED otherwise). Every split must
+                                 pairs, a block-wide softmax in one pass; head_dim 128 or 256 and
+                                 one query row only (ATTN_ERR_UNSUPPORTED otherwise). Every split must
                                  fit one tile: split_len <= 128, or by count n_splits * 128 >= cap
                                  (ATTN_ERR_INVALID_ARG otherwise; the heuristic picks such a count) */
 
@@ -280,8 +280,8 @@ int attn_split_heuristic_ex(int n_seq, int n_q, int n_head, int n_kv_head, int h
  * attn_resolve_variant -- which partial kernel a call with these arguments and
  * n_splits = 0 runs: ATTN_VARIANT_SIMT, ATTN_VARIANT_TC or ATTN_VARIANT_TCGEN05
  * (0 for an invalid shape or variant). An explicit variant is returned as is;
- * ATTN_VARIANT_AUTO picks the tcgen05 kernel for a short call -- head_dim 128,
- * one query row, cap > 0 and cap * n_seq * n_kv_head at most 4 tiles of 128
+ * ATTN_VARIANT_AUTO picks the tcgen05 kernel for a short call -- head_dim 128
+ * or 256, one query row, cap > 0 and cap * n_seq * n_kv_head at most 4 tiles of 128
  * rows per SM -- and otherwise the mma.sync tensor-core kernel (head_dim % 16
  * == 0) or the CUDA-core kernel. With explicit splits that leave a split
  * longer than 128 rows, attn_decode_ex keeps the mma.sync kernel instead.

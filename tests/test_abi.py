@@ -122,8 +122,10 @@ def test_split_heuristic_for_flagged_calls(lib):
     assert h(1, 64, 8, 128, 131072, 152, pkg.ATTN_KV_STABLE) == h(1, 64, 8, 128, 131072, 152, 0) == 38
     # a batch keeps its eight waves
     assert h(32, 32, 8, 128, 32768, 152, pkg.ATTN_KV_STABLE) == 10
-    # head_dim 256 already runs one block per SM
-    assert h(1, 16, 2, 256, 8400, 152, pkg.ATTN_KV_STABLE) == h(1, 16, 2, 256, 8400, 152, 0) == 75
+    # head_dim 256: variant 0 runs the tcgen05 kernel, ceil(8400 / 128) = 66 splits; the
+    # mma.sync kernel already runs one block per SM
+    assert h(1, 16, 2, 256, 8400, 152, S) == h(1, 16, 2, 256, 8400, 152, 0) == 66
+    assert h(1, 16, 2, 256, 8400, 152, TC | S) == h(1, 16, 2, 256, 8400, 152, TC) == 75
     # several query rows: 4 rows x 7 heads = 28 pairs -> 2 query groups of 16 per KV
     # head; at one block per SM a block would hold 431 rows (not a short call), so
     # two blocks per SM: 8 x 37 blocks of 224 rows
@@ -145,12 +147,13 @@ def test_resolved_variant(lib):
     assert r(1, 1, 28, 4, 128, 8192, 152, 0) == T5
     assert r(1, 1, 28, 4, 128, 8192, 152, S | B) == T5
     assert r(1, 1, 8, 2, 128, 40, 152, 0) == T5
-    # ... the mma.sync kernel for long caches, batches, several query rows, other
-    # head dims and an unknown capacity; CUDA cores for head_dim 8
+    assert r(1, 1, 16, 2, 256, 8400, 152, 0) == T5
+    # ... the mma.sync kernel for long caches, batches, several query rows, head_dim
+    # 64 and an unknown capacity; CUDA cores for head_dim 8
     assert r(1, 1, 64, 8, 128, 131072, 152, 0) == TC
     assert r(32, 1, 32, 8, 128, 32768, 152, 0) == TC
     assert r(1, 4, 28, 4, 128, 8192, 152, 0) == TC
-    assert r(1, 1, 16, 2, 256, 8400, 152, 0) == TC
+    assert r(1, 1, 8, 2, 64, 1024, 152, 0) == TC
     assert r(1, 1, 28, 4, 128, 0, 152, 0) == TC
     assert r(1, 1, 4, 2, 8, 64, 152, 0) == SI
     # the boundary: cap * n_seq * n_kv_head <= 4 tiles of 128 rows per SM

@@ -241,7 +241,9 @@ def test_full_7b_bench_configuration(pkg):
 
 
 def test_full_long_bench_configuration(pkg):
-    assert _bench_configuration(pkg, "long", L=3) == 75
+    # variant 0 runs the tcgen05 kernel at head_dim 256 too: ceil(8400 / 128) = 66 splits
+    assert _bench_configuration(pkg, "long", L=3) == 66
+    assert _bench_configuration(pkg, "long", L=2, variant=pkg.ATTN_VARIANT_TC) == 75
 
 
 def test_full_7b_four_query_rows_bench_configuration(pkg):

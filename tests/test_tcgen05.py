@@ -1,6 +1,6 @@
 """GPU parity of the tcgen05 partial kernel (ATTN_VARIANT_TCGEN05: one 128-row
-tile per block, accumulators in tensor memory) against the double-precision
-oracle, element by element, through the C ABI.
+tile per block, accumulators in tensor memory; head_dim 128 and 256) against
+the double-precision oracle, element by element, through the C ABI.
 
 Covers every group size, both split rules at the chunk boundaries (splits of
 1..128 rows, empty splits), tiles that start before the sequence's first row
@@ -41,53 +41,55 @@ def _oracle(case, n_head, n_kv, hd, cap, scale, kv_dtype="f16"):
                               hd, cap, scale, n_threads=8, kv_dtype=kv_dtype)
 
 
-def _check(pkg, case, n_head, n_kv, cap, what, variant=V5, kv_dtype="f16", **kw):
-    hd = 128
+def _check(pkg, case, n_head, n_kv, cap, what, variant=V5, kv_dtype="f16", hd=128, **kw):
     scale = 1 / math.sqrt(hd)
     out = run_decode(pkg, to_device(case), n_head, n_kv, hd, cap, scale, variant=variant, **kw)
     return assert_close(out.cpu().numpy(), _oracle(case, n_head, n_kv, hd, cap, scale, kv_dtype),
                         what)
 
 
-def test_every_group_size(pkg):
+@pytest.mark.parametrize("hd", [128, 256])
+def test_every_group_size(pkg, hd):
     for G in range(1, 9):
         n_kv = 2
-        case = make_case(3100 + G, 1, G * n_kv, n_kv, 128, 700, (613,))
+        case = make_case(3100 + G + hd, 1, G * n_kv, n_kv, hd, 700, (613,))
         for P in (0, 6, 11):
-            _check(pkg, case, G * n_kv, n_kv, 700, "G%d P=%d" % (G, P), n_splits=P)
+            _check(pkg, case, G * n_kv, n_kv, 700, "hd%d G%d P=%d" % (hd, G, P), hd=hd, n_splits=P)
 
 
-def test_count_split_boundaries(pkg):
+@pytest.mark.parametrize("hd", [128, 256])
+def test_count_split_boundaries(pkg, hd):
     n_head, n_kv, cap, P = 28, 4, 1024, 8             # chunks up to exactly one tile
-    base = make_case(3200, 1, n_head, n_kv, 128, cap, (cap,))
-    scale = 1 / math.sqrt(128)
+    base = make_case(3200 + hd, 1, n_head, n_kv, hd, cap, (cap,))
+    scale = 1 / math.sqrt(hd)
     dev = to_device(base)
     import torch
     for nkv in sorted({0, 1, 2, 15, 16, 17, 7, 8, 9, 127, 128, 129, 255, 256, 257, 500, 1000,
                        cap - 1, cap}):
         dev["positions"].fill_(nkv - 1)
-        out = run_decode(pkg, dev, n_head, n_kv, 128, cap, scale, n_splits=P, variant=V5)
-        ref = _oracle(dict(base, positions=np.array([nkv - 1], np.int32)), n_head, n_kv, 128, cap,
+        out = run_decode(pkg, dev, n_head, n_kv, hd, cap, scale, n_splits=P, variant=V5)
+        ref = _oracle(dict(base, positions=np.array([nkv - 1], np.int32)), n_head, n_kv, hd, cap,
                       scale)
-        assert_close(out.cpu().numpy(), ref, "count split nkv=%d" % nkv)
+        assert_close(out.cpu().numpy(), ref, "hd%d count split nkv=%d" % (hd, nkv))
         if nkv == 0:
             assert torch.count_nonzero(out).item() == 0
 
 
-def test_block_split_boundaries(pkg):
+@pytest.mark.parametrize("hd", [128, 256])
+def test_block_split_boundaries(pkg, hd):
     n_head, n_kv, cap = 16, 2, 1100
-    base = make_case(3300, 1, n_head, n_kv, 128, cap, (cap,))
-    scale = 1 / math.sqrt(128)
+    base = make_case(3300 + hd, 1, n_head, n_kv, hd, cap, (cap,))
+    scale = 1 / math.sqrt(hd)
     dev = to_device(base)
     for blk in (16, 32, 100, 128):
         P = -(-cap // blk)
         for nkv in (1, blk - 1, blk, blk + 1, 3 * blk + 7, cap - 1, cap):
             dev["positions"].fill_(nkv - 1)
-            out = run_decode(pkg, dev, n_head, n_kv, 128, cap, scale, n_splits=P, split_len=blk,
+            out = run_decode(pkg, dev, n_head, n_kv, hd, cap, scale, n_splits=P, split_len=blk,
                              variant=V5)
-            ref = _oracle(dict(base, positions=np.array([nkv - 1], np.int32)), n_head, n_kv, 128,
+            ref = _oracle(dict(base, positions=np.array([nkv - 1], np.int32)), n_head, n_kv, hd,
                           cap, scale)
-            assert_close(out.cpu().numpy(), ref, "block %d nkv=%d" % (blk, nkv))
+            assert_close(out.cpu().numpy(), ref, "hd%d block %d nkv=%d" % (hd, blk, nkv))
 
 
 def test_split_count_invariance_and_agreement_with_the_mma_sync_kernel(pkg):
@@ -101,14 +103,15 @@ def test_split_count_invariance_and_agreement_with_the_mma_sync_kernel(pkg):
     assert_close(got, ref, "tensor-core kernel, same inputs")
 
 
-def test_ragged_batch_with_nan_beyond_every_sequence(pkg):
+@pytest.mark.parametrize("hd", [128, 256])
+def test_ragged_batch_with_nan_beyond_every_sequence(pkg, hd):
     # sequences after the first start their first tile inside the previous
     # sequence's rows in a flat view; those rows are NaN here
     n_head, n_kv, cap = 32, 8, 900
     ctx = (1, 900, 0, 17, 450, 899, 64, 333, 128, 129)
-    case = make_case(3500, len(ctx), n_head, n_kv, 128, cap, ctx, fill=np.nan)
+    case = make_case(3500 + hd, len(ctx), n_head, n_kv, hd, cap, ctx, fill=np.nan)
     for P in (0, 8, 57):
-        _check(pkg, case, n_head, n_kv, cap, "ragged P=%d" % P, n_splits=P)
+        _check(pkg, case, n_head, n_kv, cap, "hd%d ragged P=%d" % (hd, P), hd=hd, n_splits=P)
 
 
 def test_large_score_spread_and_single_row(pkg):
@@ -124,28 +127,31 @@ def test_large_score_spread_and_single_row(pkg):
                                rtol=1e-6, atol=1e-6)
 
 
-def test_bfloat16_cache(pkg):
+@pytest.mark.parametrize("hd", [128, 256])
+def test_bfloat16_cache(pkg, hd):
     n_head, n_kv, cap = 28, 4, 1500
-    case = make_case(3700, 2, n_head, n_kv, 128, cap, (1500, 700), kv_dtype="bf16")
-    _check(pkg, case, n_head, n_kv, cap, "bf16", variant=V5 | pkg.ATTN_KV_BF16, kv_dtype="bf16")
+    case = make_case(3700 + hd, 2, n_head, n_kv, hd, cap, (1500, 700), kv_dtype="bf16")
+    _check(pkg, case, n_head, n_kv, cap, "hd%d bf16" % hd, variant=V5 | pkg.ATTN_KV_BF16,
+           kv_dtype="bf16", hd=hd)
 
 
-def test_fused_append(pkg):
+@pytest.mark.parametrize("hd", [128, 256])
+def test_fused_append(pkg, hd):
     import torch
     n_kv, G, cap = 2, 7, 300
     n_head = G * n_kv
-    scale = 1 / math.sqrt(128)
+    scale = 1 / math.sqrt(hd)
     for nkv in (1, 16, 17, 127, 128, 129, 200, cap):
-        case = make_case(3800 + nkv, 1, n_head, n_kv, 128, cap, (nkv,))
+        case = make_case(3800 + nkv + hd, 1, n_head, n_kv, hd, cap, (nkv,))
         case["k"][0, nkv - 1] = np.nan
         case["v"][0, nkv - 1] = np.nan
-        k_new, v_new = _new_rows(nkv, 1, n_kv, 128)
+        k_new, v_new = _new_rows(nkv, 1, n_kv, hd)
         dev = to_device(case)
         kn, vn = torch.from_numpy(k_new).cuda(), torch.from_numpy(v_new).cuda()
         for P in (0, 3):
-            got = _run_append(pkg, dev, kn, vn, n_head, n_kv, 128, cap, scale, V5, P)
+            got = _run_append(pkg, dev, kn, vn, n_head, n_kv, hd, cap, scale, V5, P)
             kh, vh = _host_after_append(case, k_new, v_new, cap)
-            ref = oracle.attn_decode(case["q"], kh, vh, case["positions"], n_head, n_kv, 128, cap,
+            ref = oracle.attn_decode(case["q"], kh, vh, case["positions"], n_head, n_kv, hd, cap,
                                      scale)
             assert_close(got, ref, "append nkv=%d P=%d" % (nkv, P))
             np.testing.assert_array_equal(dev["k"].cpu().numpy().view(np.uint16), kh.view(np.uint16))
@@ -158,6 +164,21 @@ def test_early_start_chain(pkg, graph, stable):
     assert P * 128 >= 2048
     _chain(pkg, L=5, n_head=28, n_kv=4, hd=128, cap=2048, ctx=(1900,), P=P, blk=0, variant=V5,
            graph=graph, replays=3, seed=3900, stable=stable)
+
+
+def test_full_long_workload(pkg):
+    w = syn.WORKLOADS["long"]
+    lay = syn.make_layer(w)
+    P = pkg.attn_split_heuristic_ex(1, 1, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0,
+                                    V5 | pkg.ATTN_KV_STABLE)
+    assert P * 128 >= w.cap
+    _check(pkg, lay, w.n_head, w.n_kv_head, w.cap, "long", hd=w.head_dim, n_splits=P)
+
+
+def test_stable_chain_head_dim_256(pkg):
+    P = pkg.attn_split_heuristic_ex(1, 1, 16, 2, 256, 2560, 0, V5 | pkg.ATTN_KV_STABLE)
+    _chain(pkg, L=4, n_head=16, n_kv=2, hd=256, cap=2560, ctx=(1000,), P=P, blk=0, variant=V5,
+           graph=True, replays=2, seed=3950)
 
 
 def test_full_7b_workload(pkg):
@@ -181,7 +202,7 @@ def test_arguments_that_leave_a_split_larger_than_a_tile(pkg):
         with pytest.raises(pkg.AttnError) as ei:
             run_decode(pkg, case, 8, 2, 128, 1024, 0.1, variant=V5, **kw)
         assert ei.value.status == pkg.ATTN_ERR_INVALID_ARG, kw
-    # head_dim other than 128, and several query rows, are not built for this kernel
+    # head_dim 64 and several query rows are not built for this kernel
     c64 = to_device(make_case(4001, 1, 8, 2, 64, 256, (200,)))
     with pytest.raises(pkg.AttnError) as ei:
         run_decode(pkg, c64, 8, 2, 64, 256, 0.1, variant=V5)
