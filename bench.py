@@ -39,7 +39,8 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0          # GB300 HBM3e data-sheet bandwidth, for context only
 KERNEL_SOURCES = ["attn_device.cuh", "attn_partial.cuh", "attn_warp_tc.cuh", "attn_warp_simt.cuh",
                   "attn_warp_tcmq.cuh",
-                  "attn_partial_umma.cuh", "attn_combine.cuh", "attn_kernels_impl.cuh"]
+                  "attn_partial_umma.cuh", "attn_fused_umma.cuh", "attn_combine.cuh",
+                  "attn_kernels_impl.cuh"]
 
 
 def parse_args():
@@ -51,10 +52,14 @@ def parse_args():
     ap.add_argument("--workload", default="7b", choices=["7b", "long", "stress", "ragged", "tiny"],
                     help="7b (the default bench line) or another workload, for the record")
     ap.add_argument("--ctx", type=int, default=0, help="context override (0 = the workload's)")
+    ap.add_argument("--cap", type=int, default=0,
+                    help="cache capacity override in rows per sequence (0 = the workload's); "
+                         "contexts are clipped to it")
     ap.add_argument("--split-len", type=int, default=0, help="0 = split by count")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
     ap.add_argument("--variant", type=int, default=0,
-                    help="0 auto, 1 simt, 2 tensor core (mma.sync), 3 tensor core (tcgen05)")
+                    help="0 auto, 1 simt, 2 tensor core (mma.sync), 3 tensor core (tcgen05), "
+                         "4 tcgen05 with the combine in a thread-block cluster")
     ap.add_argument("--splits", type=int, default=0, help="0 = library heuristic")
     ap.add_argument("--kv-dtype", choices=["f16", "bf16"], default="f16")
     ap.add_argument("--append", action="store_true",
@@ -258,6 +263,9 @@ def workload_for(args):
     w = syn.WORKLOADS[args.workload]
     if args.ctx:
         w = w.with_ctx(args.ctx)
+    if args.cap:
+        from dataclasses import replace
+        w = replace(w, cap=args.cap, ctx=tuple(min(int(c), args.cap) for c in w.ctx))
     return w
 
 
@@ -328,10 +336,12 @@ def run_ours(args, rank, world, local):
             self.ws_bytes = pkg.attn_workspace_size(n_seq, n_q * w.n_head, w.head_dim, P)
             self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
             self.g_full = self._capture(advance, "full")
-            # the stage entry points serve one query row; with n_q > 1 the
-            # whole call stands for the kernel pair
-            self.g_partial = self._capture(False, "partial") if n_q == 1 else None
-            self.g_combine = self._capture(False, "combine") if n_q == 1 else None
+            # the stage entry points serve one query row and keep their partials
+            # in the workspace; with n_q > 1, or the cluster-fused kernel (partial
+            # and combine in one launch), the whole call stands for the kernel pair
+            staged = n_q == 1 and resolved != 4
+            self.g_partial = self._capture(False, "partial") if staged else None
+            self.g_combine = self._capture(False, "combine") if staged else None
 
         def _calls(self, stream, stage):
             for l in range(L):
@@ -441,6 +451,8 @@ def run_ours(args, rank, world, local):
                                         variant)
     if resolved == 3 and not (blk0 <= 128 if blk0 else P0 * 128 >= w.cap):
         resolved = 2
+    if resolved == 4 and (blk0 or P0 != 16):
+        resolved = 3 if (blk0 <= 128 if blk0 else P0 * 128 >= w.cap) else 2
     plan = Plan(P0, blk0)
     ctx_end = max(w.ctx)
     clocks = ClockSampler(local, enabled=not args.no_clocks)
@@ -497,9 +509,11 @@ def run_ours(args, rank, world, local):
                 "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                 "traffic": profiled_traffic("%s_ctx%d%s" % (w.name, ctx_end,
                                                             "_nq%d" % n_q if n_q > 1 else "")),
-                "kernel": ("attn_split_partial_umma" if resolved == 3 else "attn_split_partial")
+                "kernel": ("attn_fused_umma (partial and combine in one kernel)" if resolved == 4 else
+                           "attn_split_partial_umma" if resolved == 3 else "attn_split_partial")
                           if n_q == 1 else "attn_split_partial + attn_combine",
-                "partial_variant": {1: "simt", 2: "mma.sync", 3: "tcgen05"}.get(resolved, resolved),
+                "partial_variant": {1: "simt", 2: "mma.sync", 3: "tcgen05",
+                                    4: "tcgen05, cluster-fused"}.get(resolved, resolved),
                 "bytes_per_launch": m0["launch_bytes"],
                 "us_per_launch": round(m0["partial_us"], 3),
                 "combine_us_per_launch": round(m0["combine_us"], 3)}
@@ -509,7 +523,7 @@ def run_ours(args, rank, world, local):
     if not args.no_sweep:
         if w.name == "7b":
             for c in syn.CTX_SWEEP_7B:
-                if c == ctx_end or c - 1 - (W + K) < 0:
+                if c == ctx_end or c > w.cap or c - 1 - (W + K) < 0:
                     continue
                 m = measure(plan, c)
                 sweep["ctx%d" % c] = {"us_per_layer": round(m["ms"] * 1e3 / (K * L), 3),

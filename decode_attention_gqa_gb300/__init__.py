@@ -17,7 +17,8 @@ import threading
 __all__ = [
     "AttnError", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_WORKSPACE",
     "ATTN_ERR_CUDA", "ATTN_DEVERR_POSITION_CLAMPED", "ATTN_DEVERR_PIPELINE_TIMEOUT",
-    "ATTN_VARIANT_AUTO", "ATTN_VARIANT_SIMT", "ATTN_VARIANT_TC", "ATTN_VARIANT_TCGEN05", "ATTN_KV_BF16",
+    "ATTN_VARIANT_AUTO", "ATTN_VARIANT_SIMT", "ATTN_VARIANT_TC", "ATTN_VARIANT_TCGEN05",
+    "ATTN_VARIANT_TCGEN05_CLUSTER", "ATTN_KV_BF16",
     "ATTN_KV_STABLE",
     "library_path",
     "load",
@@ -34,6 +35,7 @@ ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE, ATTN_ER
 ATTN_DEVERR_POSITION_CLAMPED = 0x1
 ATTN_DEVERR_PIPELINE_TIMEOUT = 0x2
 ATTN_VARIANT_AUTO, ATTN_VARIANT_SIMT, ATTN_VARIANT_TC, ATTN_VARIANT_TCGEN05 = 0, 1, 2, 3
+ATTN_VARIANT_TCGEN05_CLUSTER = 4
 ATTN_KV_BF16 = 0x10
 ATTN_KV_STABLE = 0x20
 

@@ -20,6 +20,7 @@ constexpr int kMaxDevices = 64;
 constexpr int kMaxSplits = 4096;                  // combine keeps P weights in shared memory
 constexpr int64_t kMaxFlatRows = (int64_t)1 << 31; // TMA row coordinates are int32
 constexpr int64_t kUnknownCap = kMaxFlatRows - 1024;
+constexpr int kFusedSplits = 16;                   // blocks per cluster of the fused tcgen05 kernel
 constexpr int kStableTiles = 4;                    // "short call": <= 4 tiles per block at one per SM
 
 thread_local int t_last_cuda_error = 0;
@@ -34,6 +35,7 @@ struct DeviceState {
     unsigned *err_word = nullptr;                 // device address of g_attn_error_word
     void *ws = nullptr;                           // library-owned workspace
     size_t ws_bytes = 0;
+    int fused_ok = -1;                            // the device holds a fused kernel's cluster (-1: not asked yet)
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -81,6 +83,7 @@ cudaError_t device_state(int dev, DeviceState **out)
         e = cudaGetSymbolAddress(&p, g_attn_error_word);
         if (e != cudaSuccess) return e;
         d.err_word = static_cast<unsigned *>(p);
+        d.fused_ok = attn::fused_fits_hd128() ? 1 : 0;
         d.ready = true;
     }
     *out = &d;
@@ -184,7 +187,7 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     if (cap < 1) return ATTN_ERR_INVALID_ARG;
     if (n_splits < 0 || n_splits > kMaxSplits || split_len < 0) return ATTN_ERR_INVALID_ARG;
     if (variant != ATTN_VARIANT_AUTO && variant != ATTN_VARIANT_SIMT && variant != ATTN_VARIANT_TC &&
-        variant != ATTN_VARIANT_TCGEN05)
+        variant != ATTN_VARIANT_TCGEN05 && variant != ATTN_VARIANT_TCGEN05_CLUSTER)
         return ATTN_ERR_INVALID_ARG;
     if (n_seq > 0 && (!q || !k_cache || !v_cache || !positions)) return ATTN_ERR_INVALID_ARG;
     if (n_seq > 0 && (stages & attn::kStageCombine) && !out) return ATTN_ERR_INVALID_ARG;
@@ -233,7 +236,24 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
             ki = ku;
         }
     }
-    const int P = n_splits > 0 ? n_splits
+    // The cluster-fused form of the tcgen05 kernel (partial and combine in one launch,
+    // 16 splits per (sequence, KV head) merged through distributed shared memory),
+    // on request only: a whole call, one query row, head_dim 128, splits by count with
+    // P = 16 (n_splits 0 or 16), a capacity of at most 16 blocks of 4 tiles, and a
+    // device that holds the 16-block cluster. Variant 0 does not take it: on one box it
+    // was 1 % faster than the plain tcgen05 kernel at context 2048 and 7-13 % slower at
+    // 512 and 128 (capacity 2048), and 20 % slower at the 7b capacity of 8192.
+    if (v == attn::kVariantFused) {
+        const attn::KernelInfo kf = kernel_info(head_dim, group, attn::kVariantFused, n_q > 1);
+        bool ok = kf.available && n_q == 1 && stages == (attn::kStagePartial | attn::kStageCombine) &&
+                  split_len == 0 && (n_splits == 0 || n_splits == kFusedSplits) && cap_known &&
+                  cap <= (int64_t)kFusedSplits * kf.max_chunk;
+        if (!ok) return ATTN_ERR_INVALID_ARG;
+        if (ds->fused_ok != 1) return ATTN_ERR_UNSUPPORTED;
+        ki = kf;
+    }
+    const int P = v == attn::kVariantFused ? kFusedSplits
+                : n_splits > 0 ? n_splits
                                : heuristic(n_seq, n_kv_head, n_q > 1 ? qgroups : 1,
                                            cap_known ? cap : 0, ds->sm_count, ki, kv_stable != 0);
     if (split_len > 0 && (int64_t)P * split_len < cap) return ATTN_ERR_INVALID_ARG;
@@ -241,9 +261,10 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     if (ki.max_chunk > 0 && (split_len > 0 ? split_len > ki.max_chunk
                                            : (!cap_known || (int64_t)P * ki.max_chunk < cap)))
         return ATTN_ERR_INVALID_ARG;
-    const size_t need = attn_workspace_size(n_seq, n_q * n_head, head_dim, P);
+    // the fused form keeps its partial states on chip: no workspace
+    const size_t need = v == attn::kVariantFused ? 0 : attn_workspace_size(n_seq, n_q * n_head, head_dim, P);
 
-    if (!workspace) {
+    if (!workspace && need > 0) {
         if (stages != (attn::kStagePartial | attn::kStageCombine)) return ATTN_ERR_INVALID_ARG;
         if (ds->ws_bytes < need) {
             cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -273,8 +294,8 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     r.pa.v = static_cast<const uint16_t *>(v_cache);
     r.pa.positions = positions;
     const size_t o_bytes = align256((size_t)n_seq * n_q * n_head * P * head_dim * sizeof(float));
-    r.pa.ws_o = static_cast<float *>(workspace);
-    r.pa.ws_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) + o_bytes);
+    r.pa.ws_o = need > 0 ? static_cast<float *>(workspace) : nullptr;
+    r.pa.ws_ml = need > 0 ? reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) + o_bytes) : nullptr;
     r.pa.err = err_word;
     r.pa.n_head = n_head;
     r.pa.n_kv_head = n_kv_head;
@@ -407,6 +428,47 @@ cudaError_t launch_pdl(const void *func, dim3 grid, dim3 block, size_t smem, cud
     return cudaLaunchKernelExC(&cfg, func, args);
 }
 
+cudaError_t launch_pdl_cluster(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                               void **args, unsigned cluster_x)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelExC(&cfg, func, args);
+}
+
+int cluster_slots(const void *func, dim3 block, size_t smem, unsigned cluster_x)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cluster_x, 1, 1);
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster_x;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, func, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
 } // namespace attn
 
 // ---------------------------------------------------------------------------
@@ -516,7 +578,7 @@ int plan_variant(int n_seq, int n_q, int n_head, int n_kv_head, int head_dim, in
 {
     variant &= ~(ATTN_KV_BF16 | ATTN_KV_STABLE);
     if (variant != ATTN_VARIANT_AUTO && variant != ATTN_VARIANT_SIMT && variant != ATTN_VARIANT_TC &&
-        variant != ATTN_VARIANT_TCGEN05)
+        variant != ATTN_VARIANT_TCGEN05 && variant != ATTN_VARIANT_TCGEN05_CLUSTER)
         return 0;
     if (n_seq <= 0 || n_q < 1 || n_q > 1024 || n_head <= 0 || n_kv_head <= 0 ||
         n_head % n_kv_head != 0)
@@ -545,7 +607,9 @@ int attn_split_heuristic_ex(int n_seq, int n_q, int n_head, int n_kv_head, int h
                             int64_t cap, int sm_count, int variant)
 {
     attn::KernelInfo ki{};
-    if (!plan_variant(n_seq, n_q, n_head, n_kv_head, head_dim, cap, sm_count, variant, ki)) return 0;
+    const int v = plan_variant(n_seq, n_q, n_head, n_kv_head, head_dim, cap, sm_count, variant, ki);
+    if (!v) return 0;
+    if (v == attn::kVariantFused) return kFusedSplits;
     const int group = n_head / n_kv_head;
     const int qgroups = n_q > 1 ? (n_q * group + attn::kMqHeadsPerBlock - 1) / attn::kMqHeadsPerBlock : 1;
     return heuristic(n_seq, n_kv_head, qgroups, cap, sm_count, ki, (variant & ATTN_KV_STABLE) != 0);

@@ -4,4 +4,5 @@
 namespace attn {
 cudaError_t launch_hd128_f16(const LaunchRequest &r) { return launch_for_hd<128, __half>(r); }
 KernelInfo kernel_info_hd128(int group, int variant, bool multi) { return kernel_info_for_hd<128>(group, variant, multi); }
+bool fused_fits_hd128() { return fused_cluster_fits<128>(); }
 } // namespace attn

@@ -7,6 +7,7 @@
 #include "attn_launch.h"
 #include "attn_partial.cuh"
 #include "attn_partial_umma.cuh"
+#include "attn_fused_umma.cuh"
 
 namespace attn {
 
@@ -89,6 +90,48 @@ cudaError_t launch_partial_umma(const LaunchRequest &r)
                       r.stream, args);
 }
 
+// The cluster-fused tcgen05 kernel: partial and combine in one launch, o written directly.
+template <int HD, int G, typename KV>
+cudaError_t launch_fused_umma(const LaunchRequest &r)
+{
+    using C = FusedCfg<HD, G, KV>;
+    alignas(64) CUtensorMap kmap, vmap;
+    const int dt = kv_dtype_code<KV>();
+    cudaError_t e = encode_kv_map4(&kmap, r.k_cache, r.n_seq, r.pa.cap, r.pa.n_kv_head, HD, 64, C::TILE, dt);
+    if (e != cudaSuccess) return e;
+    e = encode_kv_map4(&vmap, r.v_cache, r.n_seq, r.pa.cap, r.pa.n_kv_head, HD, 64, C::TILE, dt);
+    if (e != cudaSuccess) return e;
+    const void *fn = reinterpret_cast<const void *>(&attn_fused_umma<C, HD, G, KV>);
+    e = ensure_smem_attr(fn, (int)C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    PartialArgs pa = r.pa;
+    float *o = r.out;
+    void *args[] = {&kmap, &vmap, &pa, &o};
+    return launch_pdl_cluster(fn, dim3(C::CLUSTER, pa.n_kv_head, r.n_seq), dim3(C::THREADS), C::SMEM_BYTES,
+                              r.stream, args, C::CLUSTER);
+}
+
+// Whether the current device can hold a cluster of the fused kernel (16 blocks
+// of one SM each). Host only; takes no library lock.
+template <int HD>
+bool fused_cluster_fits()
+{
+    if constexpr (HD == 128) {
+        using C = FusedCfg<HD, 8, __half>;
+        const void *fn = reinterpret_cast<const void *>(&attn_fused_umma<C, HD, 8, __half>);
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return false;
+        }
+        return cluster_slots(fn, dim3(C::THREADS), C::SMEM_BYTES, C::CLUSTER) > 0;
+    } else {
+        return false;
+    }
+}
+
 template <int HD>
 cudaError_t launch_combine(const LaunchRequest &r)
 {
@@ -112,7 +155,11 @@ cudaError_t launch_group(const LaunchRequest &r)
     cudaError_t e = cudaSuccess;
     if (r.stages & kStagePartial) {
         if constexpr (HD % 16 == 0) {
-            if (r.variant == kVariantUmma) {
+            if (r.variant == kVariantFused) {
+                // partial and combine in one launch
+                if constexpr (HD == 128) return launch_fused_umma<HD, G, KV>(r);
+                else return cudaErrorInvalidValue;
+            } else if (r.variant == kVariantUmma) {
                 if constexpr (HD == 128 || HD == 256) e = launch_partial_umma<HD, G, KV>(r);
                 else return cudaErrorInvalidValue;
             } else if (r.variant == kVariantTc) {
@@ -164,6 +211,19 @@ KernelInfo kernel_info_for_hd(int group, int variant, bool multi)
 {
     KernelInfo k{0, 0, 0, false, 0, 0};
     if (group < 1 || group > 8) return k;
+    if (variant == kVariantFused) {
+        if constexpr (HD == 128) {
+            if (multi) return k;
+            using C = FusedCfg<HD, 8, __half>;
+            k.tile_rows = C::TILE;
+            k.granule = C::TILE;
+            k.stages = C::STAGES;
+            k.blocks_per_sm = 1;
+            k.max_chunk = C::TILE * C::NT_MAX;
+            k.available = true;
+        }
+        return k;
+    }
     if (variant == kVariantUmma) {
         if constexpr (HD == 128 || HD == 256) {
             if (multi) return k;

@@ -14,6 +14,7 @@ namespace attn {
 constexpr int kVariantSimt = 1;
 constexpr int kVariantTc = 2;
 constexpr int kVariantUmma = 3;             // tcgen05 kernel (attn_partial_umma.cuh)
+constexpr int kVariantFused = 4;            // tcgen05 + cluster combine (attn_fused_umma.cuh)
 constexpr int kMqHeadsPerBlock = 16;        // query heads per multi-query block
 constexpr int kKvF16 = 0;
 constexpr int kKvBf16 = 1;
@@ -62,12 +63,21 @@ cudaError_t ensure_smem_attr(const void *func, int bytes);
 cudaError_t launch_pdl(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                        void **args);
 
+// The same with a thread-block cluster of cluster_x blocks along x.
+cudaError_t launch_pdl_cluster(const void *func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                               void **args, unsigned cluster_x);
+// How many clusters of cluster_x blocks of `func` the device can hold at once
+// (0: none, or the query failed).
+int cluster_slots(const void *func, dim3 block, size_t smem, unsigned cluster_x);
+
 // Implemented in attn_kernels_hd{8,64,128,256}_{f16,bf16}.cu (kernel_info in
 // the f16 units: the shapes do not depend on the element type).
 KernelInfo kernel_info_hd8(int group, int variant, bool multi);
 KernelInfo kernel_info_hd64(int group, int variant, bool multi);
 KernelInfo kernel_info_hd128(int group, int variant, bool multi);
 KernelInfo kernel_info_hd256(int group, int variant, bool multi);
+// Whether the current device holds a cluster of the fused head_dim-128 kernel.
+bool fused_fits_hd128();
 cudaError_t launch_hd8_f16(const LaunchRequest &r);
 cudaError_t launch_hd64_f16(const LaunchRequest &r);
 cudaError_t launch_hd128_f16(const LaunchRequest &r);

@@ -81,6 +81,17 @@ typedef enum {
                                  one query row only (ATTN_ERR_UNSUPPORTED otherwise). Every split must
                                  fit one tile: split_len <= 128, or by count n_splits * 128 >= cap
                                  (ATTN_ERR_INVALID_ARG otherwise; the heuristic picks such a count) */
+#define ATTN_VARIANT_TCGEN05_CLUSTER 4 /* the tcgen05 kernel with the combine inside it: the 16
+                                 splits of a (sequence, KV head) run as one 16-block thread-block
+                                 cluster that merges its blocks' states in distributed shared
+                                 memory and writes out directly (no workspace is used, no combine
+                                 kernel is launched); each block takes up to 4 tiles of 128 rows.
+                                 head_dim 128, one query row, a whole call (not the stage entry
+                                 points), splits by count with n_splits 0 or 16, cap <= 8192;
+                                 ATTN_ERR_INVALID_ARG otherwise, ATTN_ERR_UNSUPPORTED where the
+                                 device cannot hold the cluster. On request only: variant 0
+                                 does not take it (measured no faster than the tcgen05 kernel
+                                 with its separate combine). */
 
 /* Cache element type, OR'd into the variant argument: without it K and V are
    IEEE binary16 (f16); with it they are bfloat16 (1 sign, 8 exponent, 7
@@ -279,7 +290,8 @@ int attn_split_heuristic_ex(int n_seq, int n_q, int n_head, int n_kv_head, int h
 /*
  * attn_resolve_variant -- which partial kernel a call with these arguments and
  * n_splits = 0 runs: ATTN_VARIANT_SIMT, ATTN_VARIANT_TC or ATTN_VARIANT_TCGEN05
- * (0 for an invalid shape or variant). An explicit variant is returned as is;
+ * or ATTN_VARIANT_TCGEN05_CLUSTER (0 for an invalid shape or variant). An
+ * explicit variant is returned as is;
  * ATTN_VARIANT_AUTO picks the tcgen05 kernel for a short call -- head_dim 128
  * or 256, one query row, cap > 0 and cap * n_seq * n_kv_head at most 4 tiles of 128
  * rows per SM -- and otherwise the mma.sync tensor-core kernel (head_dim % 16

@@ -82,9 +82,12 @@ def test_split_heuristic_host_only(lib):
     # more independent (sequence, KV head) units -> fewer splits each
     assert pkg.attn_split_heuristic(32, 32, 8, 128, 32768, 152) <= P
     # a short head_dim-128 call runs the tcgen05 kernel, one 128-row tile per split:
-    # 40 rows -> 1 split; the mma.sync kernel's splits are whole 64-row tiles: also 1
+    # 40 rows -> 1 split; the mma.sync kernel's splits are whole 64-row tiles: also 1;
+    # the cluster-fused form always takes 16 splits
     assert pkg.attn_split_heuristic(1, 8, 2, 128, 40, 152) == 1
     assert pkg.attn_split_heuristic_ex(1, 1, 8, 2, 128, 40, 152, pkg.ATTN_VARIANT_TC) == 1
+    assert pkg.attn_split_heuristic_ex(1, 1, 8, 2, 128, 8192, 152,
+                                       pkg.ATTN_VARIANT_TCGEN05_CLUSTER) == 16
     # ... and the CUDA-core kernel's are 32-row warp slices: 40 rows -> 2 splits
     assert pkg.attn_split_heuristic_ex(1, 1, 8, 2, 128, 40, 152, pkg.ATTN_VARIANT_SIMT) == 2
     # one sequence, 28/4 heads at 8192 rows: the tcgen05 kernel needs 8192 / 128 = 64
@@ -147,6 +150,10 @@ def test_resolved_variant(lib):
     assert r(1, 1, 28, 4, 128, 8192, 152, 0) == T5
     assert r(1, 1, 28, 4, 128, 8192, 152, S | B) == T5
     assert r(1, 1, 8, 2, 128, 40, 152, 0) == T5
+    # the cluster-fused form only on request
+    assert r(1, 1, 28, 4, 128, 2048, 152, pkg.ATTN_VARIANT_TCGEN05_CLUSTER) == \
+        pkg.ATTN_VARIANT_TCGEN05_CLUSTER
+    assert r(1, 1, 16, 2, 256, 2048, 152, pkg.ATTN_VARIANT_TCGEN05_CLUSTER) == 0
     assert r(1, 1, 16, 2, 256, 8400, 152, 0) == T5
     # ... the mma.sync kernel for long caches, batches, several query rows, head_dim
     # 64 and an unknown capacity; CUDA cores for head_dim 8
