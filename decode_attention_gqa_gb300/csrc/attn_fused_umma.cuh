@@ -310,8 +310,8 @@ attn_fused_umma(const __grid_constant__ CUtensorMap kmap, const __grid_constant_
                     lw[j] = float2_to_kv2<KV>(p[2 * j] - f.x, p[2 * j + 1] - f.y);
                 }
                 uint8_t *pt = smem + Cfg::OFF_P + t * Cfg::P_BYTES;
-                *reinterpret_cast<uint4 *>(pt + p_offset(r, 0)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4 *>(pt + p_offset(r, 8)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                *reinterpret_cast<uint4 *>(pt + p_offset<16>(r, 0)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4 *>(pt + p_offset<16>(r, 8)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 fence_proxy_async_smem();
             }
             mbar_arrive(p_ready + t);

@@ -70,11 +70,12 @@ cudaError_t launch_partial(const LaunchRequest &r)
                       Cfg::SMEM_BYTES, r.stream, args);
 }
 
-// The tcgen05 kernel: one block per (split, KV head, sequence), one 128-row tile each.
-template <int HD, int G, typename KV>
+// The tcgen05 kernel: one block per (KV head x query group, split, sequence),
+// one 128-row tile each; MQ: several causal query rows, 16 slots per block.
+template <int HD, int G, typename KV, bool MQ = false>
 cudaError_t launch_partial_umma(const LaunchRequest &r)
 {
-    using C = UmmaCfg<HD, G, KV>;
+    using C = UmmaCfg<HD, G, KV, MQ>;
     alignas(64) CUtensorMap kmap, vmap;
     const int dt = kv_dtype_code<KV>();
     cudaError_t e = encode_kv_map4(&kmap, r.k_cache, r.n_seq, r.pa.cap, r.pa.n_kv_head, HD, 64, C::TILE, dt);
@@ -86,8 +87,8 @@ cudaError_t launch_partial_umma(const LaunchRequest &r)
     if (e != cudaSuccess) return e;
     PartialArgs pa = r.pa;
     void *args[] = {&kmap, &vmap, &pa};
-    return launch_pdl(fn, dim3(pa.n_kv_head, pa.n_splits, r.n_seq), dim3(C::THREADS), C::SMEM_BYTES,
-                      r.stream, args);
+    return launch_pdl(fn, dim3(pa.n_kv_head * pa.qgroups, pa.n_splits, r.n_seq), dim3(C::THREADS),
+                      C::SMEM_BYTES, r.stream, args);
 }
 
 // The cluster-fused tcgen05 kernel: partial and combine in one launch, o written directly.
@@ -184,7 +185,12 @@ cudaError_t launch_for_hd(const LaunchRequest &r)
         if constexpr (HD % 16 == 0) {
             cudaError_t e = cudaSuccess;
             if (r.stages & kStagePartial) {
-                e = launch_partial<TcMqCfg<HD, KV>, HD, kMqHeads, KV>(r);
+                if (r.variant == kVariantUmma) {
+                    if constexpr (HD == 128 || HD == 256) e = launch_partial_umma<HD, kMqHeads, KV, true>(r);
+                    else return cudaErrorInvalidValue;
+                } else {
+                    e = launch_partial<TcMqCfg<HD, KV>, HD, kMqHeads, KV>(r);
+                }
                 if (e != cudaSuccess) return e;
             }
             if (r.stages & kStageCombine) e = launch_combine<HD>(r);
@@ -226,8 +232,18 @@ KernelInfo kernel_info_for_hd(int group, int variant, bool multi)
     }
     if (variant == kVariantUmma) {
         if constexpr (HD == 128 || HD == 256) {
-            if (multi) return k;
-            using C = UmmaCfg<HD, 8, __half>;
+            using C1 = UmmaCfg<HD, 8, __half>;
+            using CM = UmmaCfg<HD, kMqHeads, __half, true>;
+            using C = C1;
+            if (multi) {
+                k.tile_rows = CM::TILE;
+                k.granule = CM::GRANULE;
+                k.stages = 1;
+                k.blocks_per_sm = (int)(233472u / (CM::SMEM_BYTES + 1024u));
+                k.max_chunk = CM::TILE;
+                k.available = true;
+                return k;
+            }
             k.tile_rows = C::TILE;
             k.granule = C::GRANULE;
             k.stages = 1;

@@ -34,6 +34,7 @@
 
 #include "attn_device.cuh"
 #include "attn_warp_tc.cuh"
+#include "attn_warp_tcmq.cuh"
 
 namespace attn {
 
@@ -122,15 +123,22 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
-// Byte offset of P[row][n] (n < 16) in the MN-major, unswizzled B operand:
-// 8 x 8 core matrices of 128 bytes; the two 8-column groups 128 bytes apart,
-// 8-row groups 256 bytes apart.
+// Byte offset of P[row][n] (n < NCOL) in the MN-major, unswizzled B operand:
+// 8 x 8 core matrices of 128 bytes; 8-column groups 128 bytes apart, 8-row
+// groups NCOL * 16 bytes apart.
+template <int NCOL>
 __device__ __forceinline__ uint32_t p_offset(int row, int n)
 {
-    return (uint32_t)((row >> 3) * 256 + (n >> 3) * 128 + (row & 7) * 16 + (n & 7) * 2);
+    return (uint32_t)((row >> 3) * (NCOL * 16) + (n >> 3) * 128 + (row & 7) * 16 + (n & 7) * 2);
 }
 
-template <int HD, int G, typename KV>
+// MQ = false: one query row, the G heads of the group in slots 0..G-1 (q as in
+// attn_warp_tc.cuh: one 16-row Q tile, hi parts in rows 0-7, lo in 8-15).
+// MQ = true: several causal query rows, 16 (query row, head) slots per block
+// (q as in attn_warp_tcmq.cuh: a 16-row hi tile and a 16-row lo tile).
+// Either way slot i's score is column i plus column NQH + i of S, and P and Oᵀ
+// use the same columns.
+template <int HD, int G, typename KV, bool MQ = false>
 struct UmmaCfg {
     static_assert(HD == 128 || HD == 256, "the tcgen05 partial kernel is built for head_dim 128 and 256");
     static constexpr int TILE = 128;                  // rows per block (one MMA M extent)
@@ -138,20 +146,29 @@ struct UmmaCfg {
     static constexpr int NCH = HD / 64;               // 128-byte column chunks per row
     static constexpr int NMO = HD / 128;              // 128-dimension halves of Oᵀ (one MMA M each)
     static constexpr int GRANULE = TILE;              // count-mode chunks are whole tiles
-    using QStage = TcWarp<HD, G, 4, KV>;              // q staging: the same Q tile and scales
+    static constexpr int NQH = MQ ? 16 : 8;           // query-head slots (columns per hi or lo half)
+    static constexpr int NSLOT = MQ ? 16 : G;         // slots a block may fill
+    static constexpr int NCOL = 2 * NQH;              // MMA N of S, P and Oᵀ
+    static constexpr int NQT = MQ ? 2 : 1;            // 16-row Q tiles (B operands of S)
+    using QStage = typename std::conditional<MQ, TcWarpMQ<HD, 16, 4, KV>, TcWarp<HD, G, 4, KV>>::type;
+    static constexpr uint32_t QT_BYTES = 16u * HD * 2;
+    static constexpr uint32_t OFF_INV = NQT * QT_BYTES;           // per-slot scales in the q area
     static constexpr uint32_t TILE_BYTES = (uint32_t)TILE * HD * 2;
     static constexpr uint32_t OFF_K = 0;
     static constexpr uint32_t OFF_V = TILE_BYTES;
     static constexpr uint32_t OFF_Q = 2 * TILE_BYTES;
     static constexpr uint32_t OFF_P = (OFF_Q + QStage::EXTRA_BYTES + 127) / 128 * 128;
-    static constexpr uint32_t P_BYTES = (uint32_t)TILE * 16 * 2;
-    static constexpr uint32_t OFF_RED = OFF_P + P_BYTES;          // [2][4][8] floats: maxima, sums
-    static constexpr uint32_t OFF_BAR = OFF_RED + 2 * 4 * 8 * 4;  // 4 mbarriers, TMEM slot, flags
+    static constexpr uint32_t P_BYTES = (uint32_t)TILE * NCOL * 2;
+    static constexpr uint32_t OFF_RED = OFF_P + P_BYTES;          // [2][4][NQH] floats: maxima, sums
+    static constexpr uint32_t OFF_BAR = OFF_RED + 2 * 4 * NQH * 4; // 4 mbarriers, TMEM slot, flags
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 4 * 8 + 16 + 1024;   // + base alignment slack
-    // S in columns 0-15, Oᵀ half h in 16 + 16h .. 31 + 16h (a power of two >= 32)
-    static constexpr uint32_t TMEM_COLS = NMO == 1 ? 32 : 64;
+    // S in columns 0 .. NCOL-1, Oᵀ half h in NCOL (1 + h) .. ; a power of two >= 32
+    static constexpr uint32_t TMEM_NEED = (uint32_t)NCOL * (1 + NMO);
+    static constexpr uint32_t TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : 128;
     static constexpr float OFF = 7.f;                 // p headroom: p <= 2^OFF
-    static_assert(OFF_Q % 1024 == 0 && OFF_V % 1024 == 0, "swizzled operands start 1024-aligned");
+    static_assert(QStage::QT_BYTES == QT_BYTES, "Q tile layout of the staging policy");
+    static_assert(OFF_Q % 1024 == 0 && OFF_V % 1024 == 0 && QT_BYTES % 1024 == 0,
+                  "swizzled operands start 1024-aligned");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -160,7 +177,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 attn_split_partial_umma(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const PartialArgs a)
 {
-    constexpr int TILE = Cfg::TILE;
+    constexpr int TILE = Cfg::TILE, NQH = Cfg::NQH, NSLOT = Cfg::NSLOT, NCOL = Cfg::NCOL;
+    constexpr bool MQ = Cfg::NQT == 2;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + Cfg::OFF_BAR);   // full, s_done, p_ready, o_done
@@ -168,27 +186,38 @@ attn_split_partial_umma(const __grid_constant__ CUtensorMap kmap, const __grid_c
     volatile int *flags = reinterpret_cast<volatile int *>(tslot + 1);   // [0] abort
     float *red = reinterpret_cast<float *>(smem + Cfg::OFF_RED);
 
-    const int hk = blockIdx.x, sp = blockIdx.y, s = blockIdx.z;   // KV heads vary fastest
+    // grid (KV head x query group, split, sequence): KV heads vary fastest
+    const int hk = blockIdx.x / a.qgroups, qg = blockIdx.x % a.qgroups, sp = blockIdx.y, s = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = a.n_splits;
-    const size_t heads = (size_t)a.n_head;
+    const size_t heads = (size_t)a.n_q * a.n_head;       // partial heads per sequence
 
     // Dependencies as in attn_partial.cuh: with kv_stable the positions read
     // and the tile copy go ahead of the grid dependency, q waits for it.
     const bool stable = a.kv_stable != 0;
-    if (tid == 0)
-        prefetch_l2(a.q + ((size_t)s * a.n_head + (size_t)hk * G) * HD, (uint32_t)(G * HD * sizeof(float)));
+    if (tid == 0) {
+        // q of this block's slots into L2 (query rows t0..t1 of the group's heads)
+        const int gq = MQ ? a.group : G;
+        const int t0 = MQ ? qg * NQH / gq : 0;
+        const int t1 = MQ ? min(a.n_q - 1, (qg * NQH + NQH - 1) / gq) : 0;
+        for (int t = t0; t <= t1; ++t)
+            prefetch_l2(a.q + (((size_t)s * a.n_q + t) * a.n_head + (size_t)hk * gq) * HD,
+                        (uint32_t)(gq * HD * sizeof(float)));
+    }
     if (!stable) pdl_wait();
     pdl_launch_dependents();
 
     // a1: rows attended and this split's rows; an empty split leaves at once
     bool pos_ok;
-    const int64_t nkv = rows_attended(a, s, sp == 0 && hk == 0 && tid == 0, &pos_ok);
+    const int64_t nkv = rows_attended(a, s, sp == 0 && blockIdx.x == 0 && tid == 0, &pos_ok);
     int64_t lo, hi;
     split_range(nkv, sp, P, a.split_len, Cfg::GRANULE, lo, hi);
     if (lo >= hi) {
         if (stable) pdl_wait();               // the workspace may still be read by the previous grid
-        if (tid < G) a.ws_ml[((size_t)s * heads + (size_t)hk * G + tid) * P + sp] = make_float2(-INFINITY, 0.f);
+        if (tid < NSLOT) {
+            const int hp = Cfg::QStage::slot_head(a, hk, qg, tid);
+            if (hp >= 0) a.ws_ml[((size_t)s * heads + hp) * P + sp] = make_float2(-INFINITY, 0.f);
+        }
         return;
     }
     const int n = (int)(hi - lo);             // 1..TILE rows: the tile's last n rows
@@ -214,7 +243,7 @@ attn_split_partial_umma(const __grid_constant__ CUtensorMap kmap, const __grid_c
 
     // a2, while the tile is in flight: the Q tile and per-head scales
     if (stable) pdl_wait();
-    Cfg::QStage::template prepare<Cfg::THREADS>(smem + Cfg::OFF_Q, a, s, hk, 0, tid);
+    Cfg::QStage::template prepare<Cfg::THREADS>(smem + Cfg::OFF_Q, a, s, hk, qg, tid);
     // Fused append: the split ending at nkv holds the new row nkv - 1 as the
     // tile's last row. Warp 0 fetches it now (one 16-byte unit per lane) and
     // writes it into the tile and the cache once the copy has landed.
@@ -236,7 +265,7 @@ attn_split_partial_umma(const __grid_constant__ CUtensorMap kmap, const __grid_c
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = *tslot;
-    const uint32_t tm_s = tm, tm_o = tm + 16;
+    const uint32_t tm_s = tm, tm_o = tm + NCOL;
 
     if (warp == 0) {
         // ---------------- TMA / MMA warp ----------------
@@ -260,14 +289,17 @@ attn_split_partial_umma(const __grid_constant__ CUtensorMap kmap, const __grid_c
                 tc_fence_after();
                 const uint32_t sk = smem_u32(smem + Cfg::OFF_K), sq = smem_u32(smem + Cfg::OFF_Q);
                 constexpr uint32_t id_s = umma_idesc<KV>(TILE, 16, 0, 0);
-                // k-step kk covers dims [16kk, 16kk + 16): chunk kk / 4, 32 bytes per step within it
+                // Q tile qt (one, or hi and lo) into columns 16qt .. 16qt + 15; k-step kk
+                // covers dims [16kk, 16kk + 16): chunk kk / 4, 32 bytes per step within it
 #pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk) {
-                    const uint32_t ok = (kk >> 2) * (TILE * 128) + (kk & 3) * 32;
-                    const uint32_t oq = (kk >> 2) * (16 * 128) + (kk & 3) * 32;
-                    umma_f16(tm_s, umma_desc(sk + ok, 16, 1024, 2), umma_desc(sq + oq, 16, 1024, 2), id_s,
-                             kk > 0);
-                }
+                for (int qt = 0; qt < Cfg::NQT; ++qt)
+#pragma unroll
+                    for (int kk = 0; kk < HD / 16; ++kk) {
+                        const uint32_t ok = (kk >> 2) * (TILE * 128) + (kk & 3) * 32;
+                        const uint32_t oq = qt * Cfg::QT_BYTES + (kk >> 2) * (16 * 128) + (kk & 3) * 32;
+                        umma_f16(tm_s + 16 * qt, umma_desc(sk + ok, 16, 1024, 2), umma_desc(sq + oq, 16, 1024, 2),
+                                 id_s, kk > 0);
+                    }
                 umma_commit(bar + 1);
             }
             __syncwarp();
@@ -277,16 +309,16 @@ attn_split_partial_umma(const __grid_constant__ CUtensorMap kmap, const __grid_c
             } else if (lane == 0) {
                 tc_fence_after();
                 const uint32_t sv = smem_u32(smem + Cfg::OFF_V), spp = smem_u32(smem + Cfg::OFF_P);
-                constexpr uint32_t id_o = umma_idesc<KV>(128, 16, 1, 1);
+                constexpr uint32_t id_o = umma_idesc<KV>(128, NCOL, 1, 1);
                 // half h covers dimensions [128h, 128h + 128): column chunks 2h and 2h + 1;
                 // k-step kk covers tile rows [16kk, 16kk + 16): two 8-row groups of V
-                // (2048 bytes) and of P (512 bytes)
+                // (2048 bytes) and of P (2 * NCOL * 16 bytes)
 #pragma unroll
                 for (int h = 0; h < Cfg::NMO; ++h)
 #pragma unroll
                     for (int kk = 0; kk < TILE / 16; ++kk)
-                        umma_f16(tm_o + 16 * h, umma_desc(sv + h * 2 * (TILE * 128) + kk * 2048, TILE * 128, 1024, 2),
-                                 umma_desc(spp + kk * 512, 256, 128, 0), id_o, kk > 0);
+                        umma_f16(tm_o + NCOL * h, umma_desc(sv + h * 2 * (TILE * 128) + kk * 2048, TILE * 128, 1024, 2),
+                                 umma_desc(spp + kk * (2 * NCOL * 16), NCOL * 16, 128, 0), id_o, kk > 0);
                 umma_commit(bar + 3);
             }
         }
@@ -295,60 +327,79 @@ attn_split_partial_umma(const __grid_constant__ CUtensorMap kmap, const __grid_c
         const int q4 = warp & 3;                       // tensor-memory lane quadrant
         const int r = q4 * 32 + lane;                  // tile row (S) and dimension (Oᵀ)
         const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-        const float *inv = reinterpret_cast<const float *>(smem + Cfg::OFF_Q + Cfg::QStage::QT_BYTES);
+        const float *inv = reinterpret_cast<const float *>(smem + Cfg::OFF_Q + Cfg::OFF_INV);
+        const int *qrow = reinterpret_cast<const int *>(inv + 16);   // several rows: slot -> query row
         // Both named barriers below are passed by all four warps whatever
         // happened before them; a warp whose wait gave up sets the abort flag
         // and the block writes no partial.
         const bool sd = mbar_wait_bounded(bar + 1, 0);
         bool ok = __all_sync(0xffffffffu, sd);
         if (!ok && lane == 0) { flags[0] = 1; atomicOr(a.err, kErrPipelineTimeout); }
-        float sc[G];
+        float sc[NSLOT];
         if (ok) {
             tc_fence_after();
-            float c[16];
-            tmem_ld16(tm_s + lane_base, c);
-            const bool valid = r >= TILE - n;
+            float c[NCOL];
 #pragma unroll
-            for (int g = 0; g < G; ++g) sc[g] = valid ? (c[g] + c[8 + g]) * inv[g] : -INFINITY;
-            // a4: each head's maximum over the block
+            for (int j = 0; j < NCOL / 16; ++j) {
+                float cj[16];
+                tmem_ld16(tm_s + 16 * j + lane_base, cj);
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float m = warp_max(sc[g]);
-                if (lane == 0) red[q4 * 8 + g] = m;
+                for (int i = 0; i < 16; ++i) c[16 * j + i] = cj[i];
+            }
+            const bool in_split = r >= TILE - n;
+            // several query rows: slot i (query row t) sees cache rows [0, nkv - n_q + t]
+            const int64_t row = hi - TILE + r;
+#pragma unroll
+            for (int i = 0; i < NSLOT; ++i) {
+                bool valid = in_split;
+                if constexpr (MQ) valid = valid && qrow[i] >= 0 && row <= nkv - a.n_q + qrow[i];
+                sc[i] = valid ? (c[i] + c[NQH + i]) * inv[i] : -INFINITY;
+            }
+            // a4: each slot's maximum over the block
+#pragma unroll
+            for (int i = 0; i < NSLOT; ++i) {
+                const float m = warp_max(sc[i]);
+                if (lane == 0) red[q4 * NQH + i] = m;
             }
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");
         ok = ok && !flags[0];
-        float p[8];
+        float p[NQH];
         if (ok) {
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
-                if (g < G) {
-                    const float M = fmaxf(fmaxf(red[g], red[8 + g]), fmaxf(red[16 + g], red[24 + g]));
-                    p[g] = ex2(sc[g] - (M - Cfg::OFF));   // 0 outside the split
+            for (int i = 0; i < NQH; ++i) {
+                if (i < NSLOT) {
+                    const float M = fmaxf(fmaxf(red[i], red[NQH + i]), fmaxf(red[2 * NQH + i], red[3 * NQH + i]));
+                    // 0 outside the split; a slot that sees no row here (several query rows) has M = -inf
+                    p[i] = M == -INFINITY ? 0.f : ex2(sc[i] - (M - Cfg::OFF));
                 } else {
-                    p[g] = 0.f;
+                    p[i] = 0.f;
                 }
             }
-            // P row r: hi parts in columns 0-7, lo parts in 8-15
-            uint32_t hw[4], lw[4];
+            // P row r: hi parts in columns 0 .. NQH-1, lo parts in NQH .. NCOL-1
+            uint32_t hw[NQH / 2], lw[NQH / 2];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < NQH / 2; ++j) {
                 hw[j] = float2_to_kv2<KV>(p[2 * j], p[2 * j + 1]);
                 const float2 f = kv2_to_float2<KV>(hw[j]);
                 lw[j] = float2_to_kv2<KV>(p[2 * j] - f.x, p[2 * j + 1] - f.y);
             }
-            *reinterpret_cast<uint4 *>(smem + Cfg::OFF_P + p_offset(r, 0)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4 *>(smem + Cfg::OFF_P + p_offset(r, 8)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+#pragma unroll
+            for (int u = 0; u < NQH / 8; ++u) {
+                *reinterpret_cast<uint4 *>(smem + Cfg::OFF_P + p_offset<NCOL>(r, 8 * u)) =
+                    make_uint4(hw[4 * u], hw[4 * u + 1], hw[4 * u + 2], hw[4 * u + 3]);
+                *reinterpret_cast<uint4 *>(smem + Cfg::OFF_P + p_offset<NCOL>(r, NQH + 8 * u)) =
+                    make_uint4(lw[4 * u], lw[4 * u + 1], lw[4 * u + 2], lw[4 * u + 3]);
+            }
             fence_proxy_async_smem();
         }
         mbar_arrive(bar + 2);
         if (ok) {
-            // S of each head over the block, while the p·V MMAs run
+            // S of each slot over the block, while the p·V MMAs run
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float l = warp_sum(p[g]);
-                if (lane == 0) red[32 + q4 * 8 + g] = l;
+            for (int i = 0; i < NSLOT; ++i) {
+                const float l = warp_sum(p[i]);
+                if (lane == 0) red[4 * NQH + q4 * NQH + i] = l;
             }
             const bool od = mbar_wait_bounded(bar + 3, 0);
             ok = __all_sync(0xffffffffu, od);
@@ -356,21 +407,32 @@ attn_split_partial_umma(const __grid_constant__ CUtensorMap kmap, const __grid_c
         }
         if (ok) {
             tc_fence_after();
-            const size_t slot0 = ((size_t)s * heads + (size_t)hk * G) * P + sp;
 #pragma unroll
             for (int h = 0; h < Cfg::NMO; ++h) {
-                float c[16];
-                tmem_ld16(tm_o + 16 * h + lane_base, c);
+                float c[NCOL];
 #pragma unroll
-                for (int g = 0; g < G; ++g) a.ws_o[(slot0 + (size_t)g * P) * HD + 128 * h + r] = c[g] + c[8 + g];
+                for (int j = 0; j < NCOL / 16; ++j) {
+                    float cj[16];
+                    tmem_ld16(tm_o + NCOL * h + 16 * j + lane_base, cj);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) c[16 * j + i] = cj[i];
+                }
+#pragma unroll
+                for (int i = 0; i < NSLOT; ++i) {
+                    const int hp = Cfg::QStage::slot_head(a, hk, qg, i);
+                    if (hp >= 0)
+                        a.ws_o[(((size_t)s * heads + hp) * P + sp) * HD + 128 * h + r] = c[i] + c[NQH + i];
+                }
             }
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (warp == 4 && lane < G && !flags[0]) {
-            const int g = lane;
-            const float M = fmaxf(fmaxf(red[g], red[8 + g]), fmaxf(red[16 + g], red[24 + g]));
-            const float L = (red[32 + g] + red[40 + g]) + (red[48 + g] + red[56 + g]);
-            a.ws_ml[((size_t)s * heads + (size_t)hk * G + g) * P + sp] = make_float2(M - Cfg::OFF, L);
+        if (warp == 4 && lane < NSLOT && !flags[0]) {
+            const int i = lane;
+            const int hp = Cfg::QStage::slot_head(a, hk, qg, i);
+            const float M = fmaxf(fmaxf(red[i], red[NQH + i]), fmaxf(red[2 * NQH + i], red[3 * NQH + i]));
+            const float L = (red[4 * NQH + i] + red[5 * NQH + i]) + (red[6 * NQH + i] + red[7 * NQH + i]);
+            if (hp >= 0)
+                a.ws_ml[((size_t)s * heads + hp) * P + sp] = make_float2(M == -INFINITY ? M : M - Cfg::OFF, L);
         }
     }
 

@@ -77,8 +77,9 @@ typedef enum {
                                  only (ATTN_ERR_UNSUPPORTED otherwise) */
 #define ATTN_VARIANT_TCGEN05 3 /* tensor-core partial kernel on tcgen05 (accumulators in tensor
                                  memory): one 128-row tile per block, q and p as the same hi + lo
-                                 pairs, a block-wide softmax in one pass; head_dim 128 or 256 and
-                                 one query row only (ATTN_ERR_UNSUPPORTED otherwise). Every split must
+                                 pairs, a block-wide softmax in one pass; head_dim 128 or 256
+                                 (ATTN_ERR_UNSUPPORTED otherwise); with attn_decode_multi 16
+                                 (query row, head) pairs per block. Every split must
                                  fit one tile: split_len <= 128, or by count n_splits * 128 >= cap
                                  (ATTN_ERR_INVALID_ARG otherwise; the heuristic picks such a count) */
 #define ATTN_VARIANT_TCGEN05_CLUSTER 4 /* the tcgen05 kernel with the combine inside it: the 16

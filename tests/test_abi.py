@@ -171,7 +171,7 @@ def test_resolved_variant(lib):
     assert r(1, 1, 28, 4, 128, 8192, 152, TC) == TC
     assert r(1, 1, 64, 8, 128, 131072, 152, T5) == T5
     assert r(1, 1, 8, 2, 64, 1024, 152, T5) == 0
-    assert r(1, 2, 8, 2, 128, 1024, 152, T5) == 0
+    assert r(1, 2, 8, 2, 128, 1024, 152, T5) == T5                         # several query rows too
     assert r(1, 1, 28, 5, 128, 8192, 152, 0) == 0
 
 

@@ -25,8 +25,9 @@ def pkg():
     return p
 
 
-def _case(seed, n_seq, n_q, n_head, n_kv, hd, cap, ctx, kv_dtype="f16", k_scale=1.0):
-    c = make_case(seed, n_seq, n_head, n_kv, hd, cap, ctx, kv_dtype=kv_dtype, k_scale=k_scale)
+def _case(seed, n_seq, n_q, n_head, n_kv, hd, cap, ctx, kv_dtype="f16", k_scale=1.0, fill=0.0):
+    c = make_case(seed, n_seq, n_head, n_kv, hd, cap, ctx, kv_dtype=kv_dtype, k_scale=k_scale,
+                  fill=fill)
     rng = np.random.Generator(np.random.PCG64([seed, 9]))
     c["q"] = rng.standard_normal((n_seq, n_q, n_head, hd), dtype=np.float32)
     return c
@@ -43,10 +44,14 @@ def _run(pkg, case, n_q, n_head, n_kv, hd, cap, scale, P=0, blk=0, variant=0):
     return out.cpu().numpy()
 
 
+# variant 0 runs the mma.sync multi-query kernel; 3 the tcgen05 kernel (16 slots per block)
+@pytest.mark.parametrize("variant", [0, 3])
 @pytest.mark.parametrize("hd", [64, 128, 256])
 @pytest.mark.parametrize("kv", ["f16", "bf16"])
-def test_multi_query_shapes(pkg, hd, kv):
-    flag = pkg.ATTN_KV_BF16 if kv == "bf16" else 0
+def test_multi_query_shapes(pkg, hd, kv, variant):
+    if variant == 3 and hd == 64:
+        pytest.skip("the tcgen05 kernel is built for head_dim 128 and 256")
+    flag = (pkg.ATTN_KV_BF16 if kv == "bf16" else 0) | variant
     for (G, n_q) in ((1, 2), (4, 3), (7, 2), (8, 2), (7, 4), (2, 9)):
         n_kv, cap = 2, 500
         n_head = G * n_kv
@@ -55,16 +60,18 @@ def test_multi_query_shapes(pkg, hd, kv):
         got = _run(pkg, case, n_q, n_head, n_kv, hd, cap, scale, variant=flag)
         ref = oracle.attn_decode_multi(case["q"], case["k"], case["v"], case["positions"], n_q,
                                        n_head, n_kv, hd, cap, scale, n_threads=8, kv_dtype=kv)
-        assert_close(got, ref, "multi hd%d G%d n_q%d %s" % (hd, G, n_q, kv))
+        assert_close(got, ref, "multi hd%d G%d n_q%d %s variant %d" % (hd, G, n_q, kv, variant))
 
 
-def test_multi_query_short_contexts_and_boundaries(pkg):
+@pytest.mark.parametrize("variant", [0, 3])
+def test_multi_query_short_contexts_and_boundaries(pkg, variant):
     n_q, n_head, n_kv, hd, cap = 4, 28, 4, 128, 1024
     scale = 1 / math.sqrt(hd)
-    for nkv in (1, 2, 3, 4, 5, 16, 17, 63, 64, 65, 112, 113, 1000, 1024):
+    splits = ((0, 0), (7, 0), (17, 64)) if variant == 0 else ((0, 0), (8, 0), (17, 64), (9, 128))
+    for nkv in (1, 2, 3, 4, 5, 16, 17, 63, 64, 65, 112, 113, 127, 128, 129, 1000, 1024):
         case = _case(500 + nkv, 1, n_q, n_head, n_kv, hd, cap, (nkv,))
-        for P, blk in ((0, 0), (7, 0), (17, 64)):
-            got = _run(pkg, case, n_q, n_head, n_kv, hd, cap, scale, P, blk)
+        for P, blk in splits:
+            got = _run(pkg, case, n_q, n_head, n_kv, hd, cap, scale, P, blk, variant)
             ref = oracle.attn_decode_multi(case["q"], case["k"], case["v"], case["positions"], n_q,
                                            n_head, n_kv, hd, cap, scale, n_threads=8)
             assert_close(got, ref, "multi nkv=%d P=%d blk=%d" % (nkv, P, blk))
@@ -72,12 +79,13 @@ def test_multi_query_short_contexts_and_boundaries(pkg):
                 assert np.all(got[0, :n_q - nkv] == 0)
 
 
-def test_multi_query_ragged_batch_and_large_spread(pkg):
+@pytest.mark.parametrize("variant", [0, 3])
+def test_multi_query_ragged_batch_and_large_spread(pkg, variant):
     n_q, n_head, n_kv, hd, cap = 3, 32, 8, 128, 900
     ctx = (2, 900, 0, 17, 450, 899, 64, 333)
-    case = _case(600, len(ctx), n_q, n_head, n_kv, hd, cap, ctx, k_scale=6.0)
+    case = _case(600, len(ctx), n_q, n_head, n_kv, hd, cap, ctx, k_scale=6.0, fill=np.nan)
     scale = 1 / math.sqrt(hd)
-    got = _run(pkg, case, n_q, n_head, n_kv, hd, cap, scale)
+    got = _run(pkg, case, n_q, n_head, n_kv, hd, cap, scale, variant=variant)
     ref = oracle.attn_decode_multi(case["q"], case["k"], case["v"], case["positions"], n_q,
                                    n_head, n_kv, hd, cap, scale, n_threads=8)
     assert_close(got, ref, "multi ragged")
@@ -115,16 +123,17 @@ def test_multi_query_rejections(pkg):
     assert st == pkg.ATTN_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("variant", [0, 3])
 @pytest.mark.parametrize("n_q, G, nkv", [(64, 4, 300), (50, 8, 20), (33, 1, 700), (128, 7, 1000)])
-def test_many_query_rows(pkg, n_q, G, nkv):
+def test_many_query_rows(pkg, n_q, G, nkv, variant):
     """Prefill-sized chunks: many query groups per KV head (up to 56 blocks
     along y), and with n_q > nkv the first n_q - nkv rows see no cache row."""
     n_kv, hd, cap = 2, 128, 1024
     n_head = G * n_kv
     case = _case(800 + n_q + G, 1, n_q, n_head, n_kv, hd, cap, (nkv,))
-    got = _run(pkg, case, n_q, n_head, n_kv, hd, cap, 1 / math.sqrt(hd))
+    got = _run(pkg, case, n_q, n_head, n_kv, hd, cap, 1 / math.sqrt(hd), variant=variant)
     ref = oracle.attn_decode_multi(case["q"], case["k"], case["v"], case["positions"], n_q, n_head,
                                    n_kv, hd, cap, 1 / math.sqrt(hd), n_threads=8)
-    assert_close(got, ref, "n_q=%d G=%d nkv=%d" % (n_q, G, nkv))
+    assert_close(got, ref, "n_q=%d G=%d nkv=%d variant %d" % (n_q, G, nkv, variant))
     if n_q > nkv:
         assert np.all(got[0, :n_q - nkv] == 0)

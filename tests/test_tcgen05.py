@@ -202,14 +202,15 @@ def test_arguments_that_leave_a_split_larger_than_a_tile(pkg):
         with pytest.raises(pkg.AttnError) as ei:
             run_decode(pkg, case, 8, 2, 128, 1024, 0.1, variant=V5, **kw)
         assert ei.value.status == pkg.ATTN_ERR_INVALID_ARG, kw
-    # head_dim 64 and several query rows are not built for this kernel
+    # head_dim 64 is not built for this kernel
     c64 = to_device(make_case(4001, 1, 8, 2, 64, 256, (200,)))
     with pytest.raises(pkg.AttnError) as ei:
         run_decode(pkg, c64, 8, 2, 64, 256, 0.1, variant=V5)
     assert ei.value.status == pkg.ATTN_ERR_UNSUPPORTED
+    # several query rows keep the one-tile rule
     q2 = torch.zeros((1, 2, 8, 128), device="cuda")
     out = torch.empty_like(q2)
     with pytest.raises(pkg.AttnError) as ei:
         pkg.attn_decode_multi(q2, case["k"], case["v"], case["positions"], out, 1, 2, 8, 2, 128,
-                              0.1, 1024, variant=V5)
-    assert ei.value.status == pkg.ATTN_ERR_UNSUPPORTED
+                              0.1, 1024, n_splits=7, variant=V5)
+    assert ei.value.status == pkg.ATTN_ERR_INVALID_ARG
