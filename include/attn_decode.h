@@ -138,15 +138,18 @@ attn_status attn_decode(const float *q, const void *k_cache, const void *v_cache
  *   n_splits        splits P per (sequence, KV head); 0 = attn_split_heuristic_ex()
  *                   for this call's variant.
  *   split_len       0: split by count, chunk = ceil(nkv / P) rounded up to the
- *                   kernel's row granule: 64 rows (tensor cores, head_dim <= 128,
- *                   one query row: whole tiles), 16 rows (tensor cores otherwise)
- *                   or 32 rows (CUDA cores) (minfer R4 §2.2); > 0: fixed block of split_len
+ *                   kernel's row granule: 128 rows (tcgen05: whole tiles), 64 rows
+ *                   (mma.sync, head_dim <= 128, one query row: whole tiles), 16 rows
+ *                   (mma.sync otherwise) or 32 rows (CUDA cores) (minfer R4 §2.2);
+ *                   the kernel variant 0 runs is reported by attn_resolve_variant;
+ *                   > 0: fixed block of split_len
  *                   rows per split (Red Lite dev35 "Change"), which needs
  *                   P * split_len >= cap, else ATTN_ERR_INVALID_ARG.
  *   variant         ATTN_VARIANT_*.
  *   workspace       device buffer of at least attn_workspace_size(...) bytes,
  *                   256-byte aligned; NULL selects the library-owned buffer as in
- *                   attn_decode. Its contents on entry do not matter.
+ *                   attn_decode. Its contents on entry do not matter. The
+ *                   cluster-fused variant uses none (it may be NULL).
  */
 attn_status attn_decode_ex(const float *q, const void *k_cache, const void *v_cache,
                            const int32_t *positions, float *out, int n_seq, int n_head,
