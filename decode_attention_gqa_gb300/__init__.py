@@ -159,14 +159,15 @@ def attn_decode_ex(q, k_cache, v_cache, positions, out, n_seq, n_head, n_kv_head
 
 
 def decode_attention(q, k_cache, v_cache, positions, scale=None, out=None, n_splits=0,
-                     kv_stable=False, stream=None):
+                     kv_stable=False, stream=None, kernel=ATTN_VARIANT_AUTO):
     """Convenience form of attn_decode_ex for torch tensors: the sizes come
     from the shapes -- q f32 [n_seq, n_head, head_dim] (or [n_seq, n_q,
     n_head, head_dim] for several causal query rows, attn_decode_multi),
     k_cache / v_cache float16 or bfloat16 [n_seq, cap, n_kv_head, head_dim],
     positions int32 [n_seq] -- scale defaults to 1/sqrt(head_dim), the cache
-    dtype picks ATTN_KV_BF16, and `out` is allocated when not given. The
-    library-owned workspace is used. Returns out."""
+    dtype picks ATTN_KV_BF16, and `out` is allocated when not given. `kernel`
+    is one of the ATTN_VARIANT_* values (variant 0, the library's choice, by
+    default). The library-owned workspace is used. Returns out."""
     import math
     import torch
     if q.dtype != torch.float32 or positions.dtype != torch.int32:
@@ -191,7 +192,10 @@ def decode_attention(q, k_cache, v_cache, positions, scale=None, out=None, n_spl
         scale = 1.0 / math.sqrt(head_dim)
     if out is None:
         out = torch.empty_like(q)
-    variant = (ATTN_KV_BF16 if k_cache.dtype == torch.bfloat16 else 0) | \
+    if kernel not in (ATTN_VARIANT_AUTO, ATTN_VARIANT_SIMT, ATTN_VARIANT_TC, ATTN_VARIANT_TCGEN05,
+                      ATTN_VARIANT_TCGEN05_CLUSTER):
+        raise ValueError("kernel must be one of the ATTN_VARIANT_* values")
+    variant = kernel | (ATTN_KV_BF16 if k_cache.dtype == torch.bfloat16 else 0) | \
         (ATTN_KV_STABLE if kv_stable else 0)
     if n_q > 1:
         attn_decode_multi(q, k_cache, v_cache, positions, out, n_seq, n_q, n_head, n_kv_head,

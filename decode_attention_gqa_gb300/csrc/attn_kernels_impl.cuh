@@ -232,22 +232,14 @@ KernelInfo kernel_info_for_hd(int group, int variant, bool multi)
     }
     if (variant == kVariantUmma) {
         if constexpr (HD == 128 || HD == 256) {
-            using C1 = UmmaCfg<HD, 8, __half>;
-            using CM = UmmaCfg<HD, kMqHeads, __half, true>;
-            using C = C1;
-            if (multi) {
-                k.tile_rows = CM::TILE;
-                k.granule = CM::GRANULE;
-                k.stages = 1;
-                k.blocks_per_sm = (int)(233472u / (CM::SMEM_BYTES + 1024u));
-                k.max_chunk = CM::TILE;
-                k.available = true;
-                return k;
-            }
+            // one query row (the largest group sets the shared-memory need) or 16 slots
+            const uint32_t smem = multi ? UmmaCfg<HD, kMqHeads, __half, true>::SMEM_BYTES
+                                        : UmmaCfg<HD, 8, __half>::SMEM_BYTES;
+            using C = UmmaCfg<HD, 8, __half>;     // tile and granule are the same for both
             k.tile_rows = C::TILE;
             k.granule = C::GRANULE;
             k.stages = 1;
-            k.blocks_per_sm = (int)(233472u / (C::SMEM_BYTES + 1024u));
+            k.blocks_per_sm = (int)(233472u / (smem + 1024u));
             k.max_chunk = C::TILE;
             k.available = true;
         }

@@ -279,3 +279,5 @@ def test_decode_attention_checks_its_tensors_before_any_call():
         pkg.decode_attention(q[:, :, :64], k, k, pos)                  # head_dim mismatch
     with pytest.raises(ValueError):
         pkg.decode_attention(q, k.transpose(1, 2), k.transpose(1, 2), pos)   # not contiguous
+    with pytest.raises(ValueError):
+        pkg.decode_attention(q, k, k, pos, kernel=9)                   # no such kernel

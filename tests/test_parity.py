@@ -310,3 +310,9 @@ def test_decode_attention_convenience_call(pkg, kv):
     refm = oracle.attn_decode_multi(qm, case["k"], case["v"], case["positions"], 3, n_head, n_kv,
                                     hd, cap, 1 / math.sqrt(hd), n_threads=8, kv_dtype=kv)
     assert_close(outm.cpu().numpy(), refm, "decode_attention %s, 3 rows" % kv)
+    # each kernel by name
+    for kernel in (pkg.ATTN_VARIANT_SIMT, pkg.ATTN_VARIANT_TC, pkg.ATTN_VARIANT_TCGEN05,
+                   pkg.ATTN_VARIANT_TCGEN05_CLUSTER):
+        outk = pkg.decode_attention(dev["q"], dev["k"], dev["v"], dev["positions"], kernel=kernel)
+        torch.cuda.synchronize()
+        assert_close(outk.cpu().numpy(), ref, "decode_attention %s kernel %d" % (kv, kernel))
