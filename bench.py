@@ -449,10 +449,11 @@ def run_ours(args, rank, world, local):
     # explicit splits longer than one 128-row tile keep the mma.sync kernel)
     resolved = pkg.attn_resolve_variant(n_seq, n_q, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0,
                                         variant)
-    if resolved == 3 and not (blk0 <= 128 if blk0 else P0 * 128 >= w.cap):
+    tile5 = 96 if w.head_dim == 256 else 128           # rows per tcgen05 block
+    if resolved == 3 and not (blk0 <= tile5 if blk0 else P0 * tile5 >= w.cap):
         resolved = 2
     if resolved == 4 and (blk0 or P0 != 16):
-        resolved = 3 if (blk0 <= 128 if blk0 else P0 * 128 >= w.cap) else 2
+        resolved = 3 if (blk0 <= tile5 if blk0 else P0 * tile5 >= w.cap) else 2
     plan = Plan(P0, blk0)
     ctx_end = max(w.ctx)
     clocks = ClockSampler(local, enabled=not args.no_clocks)

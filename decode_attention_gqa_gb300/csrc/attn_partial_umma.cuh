@@ -1,11 +1,12 @@
 // attn_partial_umma.cuh -- the split partial kernel on the fifth-generation
 // tensor cores (tcgen05, accumulators in tensor memory): steps a1-a6 for a
-// split of at most 128 rows, one query row, head_dim 128 or 256.
+// split of at most one tile (128 rows; 96 at head_dim 256), one query row or
+// several causal ones, head_dim 128 or 256.
 //
 // One block per (split sp, KV head hk, sequence s), the static grid of minfer
 // "10 · R4" §2.2 with the KV head in place of the query head (Red Lite dev35
 // "Change": the whole query-head group from one K/V read). The split is a
-// single 128-row tile, so the block sees each of its rows once and its softmax
+// single tile of rows, so the block sees each of its rows once and its softmax
 // is one pass over the tile with a block-wide maximum (§2.1 with one step):
 //   1. TMA brings the 128 cache rows that end at hi, K and V (128-byte
 //      swizzled, as in attn_partial.cuh). The rows of the split are the tile's
@@ -141,7 +142,11 @@ __device__ __forceinline__ uint32_t p_offset(int row, int n)
 template <int HD, int G, typename KV, bool MQ = false>
 struct UmmaCfg {
     static_assert(HD == 128 || HD == 256, "the tcgen05 partial kernel is built for head_dim 128 and 256");
-    static constexpr int TILE = 128;                  // rows per block (one MMA M extent)
+    // rows per block: 128 (one MMA M extent); 96 at head_dim 256, so that two
+    // blocks fit an SM -- S is still an M = 128 MMA, whose last 32 rows read
+    // past the K tile (finite data) and are masked
+    static constexpr int TILE = HD == 256 ? 96 : 128;
+    static constexpr int MMA_M = 128;
     static constexpr int THREADS = 192;               // TMA/MMA warp, TMEM warp, 4 softmax warps
     static constexpr int NCH = HD / 64;               // 128-byte column chunks per row
     static constexpr int NMO = HD / 128;              // 128-dimension halves of Oᵀ (one MMA M each)
@@ -158,7 +163,7 @@ struct UmmaCfg {
     static constexpr uint32_t OFF_V = TILE_BYTES;
     static constexpr uint32_t OFF_Q = 2 * TILE_BYTES;
     static constexpr uint32_t OFF_P = (OFF_Q + QStage::EXTRA_BYTES + 127) / 128 * 128;
-    static constexpr uint32_t P_BYTES = (uint32_t)TILE * NCOL * 2;
+    static constexpr uint32_t P_BYTES = (uint32_t)MMA_M * NCOL * 2;
     static constexpr uint32_t OFF_RED = OFF_P + P_BYTES;          // [2][4][NQH] floats: maxima, sums
     static constexpr uint32_t OFF_BAR = OFF_RED + 2 * 4 * NQH * 4; // 4 mbarriers, TMEM slot, flags
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 4 * 8 + 16 + 1024;   // + base alignment slack
@@ -170,6 +175,7 @@ struct UmmaCfg {
     static_assert(OFF_Q % 1024 == 0 && OFF_V % 1024 == 0 && QT_BYTES % 1024 == 0,
                   "swizzled operands start 1024-aligned");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(TILE % 16 == 0 && TILE <= MMA_M && (TILE * 128) % 1024 == 0, "tile rows");
 };
 
 template <class Cfg, int HD, int G, typename KV>
@@ -288,7 +294,7 @@ attn_split_partial_umma(const __grid_constant__ CUtensorMap kmap, const __grid_c
             if (lane == 0) {
                 tc_fence_after();
                 const uint32_t sk = smem_u32(smem + Cfg::OFF_K), sq = smem_u32(smem + Cfg::OFF_Q);
-                constexpr uint32_t id_s = umma_idesc<KV>(TILE, 16, 0, 0);
+                constexpr uint32_t id_s = umma_idesc<KV>(Cfg::MMA_M, 16, 0, 0);
                 // Q tile qt (one, or hi and lo) into columns 16qt .. 16qt + 15; k-step kk
                 // covers dims [16kk, 16kk + 16): chunk kk / 4, 32 bytes per step within it
 #pragma unroll
@@ -346,7 +352,7 @@ attn_split_partial_umma(const __grid_constant__ CUtensorMap kmap, const __grid_c
 #pragma unroll
                 for (int i = 0; i < 16; ++i) c[16 * j + i] = cj[i];
             }
-            const bool in_split = r >= TILE - n;
+            const bool in_split = r >= TILE - n && r < TILE;
             // several query rows: slot i (query row t) sees cache rows [0, nkv - n_q + t]
             const int64_t row = hi - TILE + r;
 #pragma unroll

@@ -76,12 +76,13 @@ typedef enum {
                                  22 significant bits for f16, 16 for bf16); head_dim 64, 128, 256
                                  only (ATTN_ERR_UNSUPPORTED otherwise) */
 #define ATTN_VARIANT_TCGEN05 3 /* tensor-core partial kernel on tcgen05 (accumulators in tensor
-                                 memory): one 128-row tile per block, q and p as the same hi + lo
-                                 pairs, a block-wide softmax in one pass; head_dim 128 or 256
-                                 (ATTN_ERR_UNSUPPORTED otherwise); with attn_decode_multi 16
-                                 (query row, head) pairs per block. Every split must
-                                 fit one tile: split_len <= 128, or by count n_splits * 128 >= cap
-                                 (ATTN_ERR_INVALID_ARG otherwise; the heuristic picks such a count) */
+                                 memory): one tile of T rows per block (T = 128; 96 at head_dim
+                                 256), q and p as the same hi + lo pairs, a block-wide softmax in
+                                 one pass; head_dim 128 or 256 (ATTN_ERR_UNSUPPORTED otherwise);
+                                 with attn_decode_multi 16 (query row, head) pairs per block.
+                                 Every split must fit one tile: split_len <= T, or by count
+                                 n_splits * T >= cap (ATTN_ERR_INVALID_ARG otherwise; the
+                                 heuristic picks such a count) */
 #define ATTN_VARIANT_TCGEN05_CLUSTER 4 /* the tcgen05 kernel with the combine inside it: the 16
                                  splits of a (sequence, KV head) run as one 16-block thread-block
                                  cluster that merges its blocks' states in distributed shared
@@ -138,7 +139,8 @@ attn_status attn_decode(const float *q, const void *k_cache, const void *v_cache
  *   n_splits        splits P per (sequence, KV head); 0 = attn_split_heuristic_ex()
  *                   for this call's variant.
  *   split_len       0: split by count, chunk = ceil(nkv / P) rounded up to the
- *                   kernel's row granule: 128 rows (tcgen05: whole tiles), 64 rows
+ *                   kernel's row granule: 128 rows (tcgen05: whole tiles; 96 at
+ *                   head_dim 256), 64 rows
  *                   (mma.sync, head_dim <= 128, one query row: whole tiles), 16 rows
  *                   (mma.sync otherwise) or 32 rows (CUDA cores) (minfer R4 §2.2);
  *                   the kernel variant 0 runs is reported by attn_resolve_variant;

@@ -125,9 +125,9 @@ def test_split_heuristic_for_flagged_calls(lib):
     assert h(1, 64, 8, 128, 131072, 152, pkg.ATTN_KV_STABLE) == h(1, 64, 8, 128, 131072, 152, 0) == 38
     # a batch keeps its eight waves
     assert h(32, 32, 8, 128, 32768, 152, pkg.ATTN_KV_STABLE) == 10
-    # head_dim 256: variant 0 runs the tcgen05 kernel, ceil(8400 / 128) = 66 splits; the
-    # mma.sync kernel already runs one block per SM
-    assert h(1, 16, 2, 256, 8400, 152, S) == h(1, 16, 2, 256, 8400, 152, 0) == 66
+    # head_dim 256: variant 0 runs the tcgen05 kernel, 96-row tiles, ceil(8400 / 96) = 88
+    # splits; the mma.sync kernel already runs one block per SM
+    assert h(1, 16, 2, 256, 8400, 152, S) == h(1, 16, 2, 256, 8400, 152, 0) == 88
     assert h(1, 16, 2, 256, 8400, 152, TC | S) == h(1, 16, 2, 256, 8400, 152, TC) == 75
     # several query rows: 4 rows x 7 heads = 28 pairs -> 2 query groups of 16 per KV
     # head; at one block per SM a block would hold 431 rows (not a short call), so

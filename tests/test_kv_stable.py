@@ -241,8 +241,8 @@ def test_full_7b_bench_configuration(pkg):
 
 
 def test_full_long_bench_configuration(pkg):
-    # variant 0 runs the tcgen05 kernel at head_dim 256 too: ceil(8400 / 128) = 66 splits
-    assert _bench_configuration(pkg, "long", L=3) == 66
+    # variant 0 runs the tcgen05 kernel at head_dim 256 too: 96-row tiles, ceil(8400 / 96) = 88
+    assert _bench_configuration(pkg, "long", L=3) == 88
     assert _bench_configuration(pkg, "long", L=2, variant=pkg.ATTN_VARIANT_TC) == 75
 
 

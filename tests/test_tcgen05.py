@@ -53,13 +53,15 @@ def test_every_group_size(pkg, hd):
     for G in range(1, 9):
         n_kv = 2
         case = make_case(3100 + G + hd, 1, G * n_kv, n_kv, hd, 700, (613,))
-        for P in (0, 6, 11):
+        # a tile is 128 rows (96 at head_dim 256): P * tile >= 700
+        for P in ((0, 6, 11) if hd == 128 else (0, 8, 11)):
             _check(pkg, case, G * n_kv, n_kv, 700, "hd%d G%d P=%d" % (hd, G, P), hd=hd, n_splits=P)
 
 
 @pytest.mark.parametrize("hd", [128, 256])
 def test_count_split_boundaries(pkg, hd):
-    n_head, n_kv, cap, P = 28, 4, 1024, 8             # chunks up to exactly one tile
+    n_head, n_kv, cap = 28, 4, 1024
+    P = 8 if hd == 128 else 11                        # chunks up to exactly one tile (128 / 96 rows)
     base = make_case(3200 + hd, 1, n_head, n_kv, hd, cap, (cap,))
     scale = 1 / math.sqrt(hd)
     dev = to_device(base)
@@ -81,7 +83,7 @@ def test_block_split_boundaries(pkg, hd):
     base = make_case(3300 + hd, 1, n_head, n_kv, hd, cap, (cap,))
     scale = 1 / math.sqrt(hd)
     dev = to_device(base)
-    for blk in (16, 32, 100, 128):
+    for blk in ((16, 32, 100, 128) if hd == 128 else (16, 32, 80, 96)):
         P = -(-cap // blk)
         for nkv in (1, blk - 1, blk, blk + 1, 3 * blk + 7, cap - 1, cap):
             dev["positions"].fill_(nkv - 1)
@@ -110,7 +112,7 @@ def test_ragged_batch_with_nan_beyond_every_sequence(pkg, hd):
     n_head, n_kv, cap = 32, 8, 900
     ctx = (1, 900, 0, 17, 450, 899, 64, 333, 128, 129)
     case = make_case(3500 + hd, len(ctx), n_head, n_kv, hd, cap, ctx, fill=np.nan)
-    for P in (0, 8, 57):
+    for P in ((0, 8, 57) if hd == 128 else (0, 10, 57)):      # P * tile >= 900
         _check(pkg, case, n_head, n_kv, cap, "hd%d ragged P=%d" % (hd, P), hd=hd, n_splits=P)
 
 
@@ -148,7 +150,7 @@ def test_fused_append(pkg, hd):
         k_new, v_new = _new_rows(nkv, 1, n_kv, hd)
         dev = to_device(case)
         kn, vn = torch.from_numpy(k_new).cuda(), torch.from_numpy(v_new).cuda()
-        for P in (0, 3):
+        for P in (0, 3 if hd == 128 else 4):
             got = _run_append(pkg, dev, kn, vn, n_head, n_kv, hd, cap, scale, V5, P)
             kh, vh = _host_after_append(case, k_new, v_new, cap)
             ref = oracle.attn_decode(case["q"], kh, vh, case["positions"], n_head, n_kv, hd, cap,
@@ -171,7 +173,7 @@ def test_full_long_workload(pkg):
     lay = syn.make_layer(w)
     P = pkg.attn_split_heuristic_ex(1, 1, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0,
                                     V5 | pkg.ATTN_KV_STABLE)
-    assert P * 128 >= w.cap
+    assert P * 96 >= w.cap
     _check(pkg, lay, w.n_head, w.n_kv_head, w.cap, "long", hd=w.head_dim, n_splits=P)
 
 
