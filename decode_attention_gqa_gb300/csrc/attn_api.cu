@@ -83,7 +83,6 @@ cudaError_t device_state(int dev, DeviceState **out)
         e = cudaGetSymbolAddress(&p, g_attn_error_word);
         if (e != cudaSuccess) return e;
         d.err_word = static_cast<unsigned *>(p);
-        d.fused_ok = attn::fused_fits_hd128() ? 1 : 0;
         d.ready = true;
     }
     *out = &d;
@@ -249,6 +248,7 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
                   split_len == 0 && (n_splits == 0 || n_splits == kFusedSplits) && cap_known &&
                   cap <= (int64_t)kFusedSplits * kf.max_chunk;
         if (!ok) return ATTN_ERR_INVALID_ARG;
+        if (ds->fused_ok < 0) ds->fused_ok = attn::fused_fits_hd128() ? 1 : 0;   // asked once per device
         if (ds->fused_ok != 1) return ATTN_ERR_UNSUPPORTED;
         ki = kf;
     }
