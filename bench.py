@@ -383,22 +383,26 @@ def run_ours(args, rank, world, local):
                 self._calls(torch.cuda.current_stream(), stage)
             return g
 
-    def timed_replays(g, n, clocks=None):
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
+    def timed_replays(g, n, clocks=None, per_step=None):
+        """Total ms of n replays (events on the launching stream); with
+        per_step a list, also each replay's ms, from one event between replays."""
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
         torch.cuda.synchronize()
         dist_barrier(world)
         if clocks:
             clocks.start()
         with torch.cuda.stream(s):
-            e0.record(s)
-            for _ in range(n):
+            ev[0].record(s)
+            for i in range(n):
                 g.replay()
-            e1.record(s)
+                if per_step is not None or i == n - 1:
+                    ev[i + 1].record(s)
         torch.cuda.synchronize()
         clk = clocks.stop() if clocks else None
         dist_barrier(world)
-        return e0.elapsed_time(e1), clk
+        if per_step is not None:
+            per_step.extend(ev[i].elapsed_time(ev[i + 1]) for i in range(n))
+        return ev[0].elapsed_time(ev[n]), clk
 
     def warm(g):
         with torch.cuda.stream(s):
@@ -417,6 +421,12 @@ def run_ours(args, rank, world, local):
             nkv_steps = [[c for c in w.ctx] for _ in range(K)]
         warm(plan.g_full)
         ms, clk = timed_replays(plan.g_full, K, clocks)
+        # the spread from a second pass with an event between replays, so that
+        # the events cannot touch the timed total
+        steps = []
+        if advance:
+            pos.fill_(start)
+        timed_replays(plan.g_full, K, per_step=steps)
         ms = dist_max(ms, world)
         step_bytes = [kv_bytes_for(n) * L for n in nkv_steps]
         final = nkv_steps[-1]
@@ -431,7 +441,7 @@ def run_ours(args, rank, world, local):
             warm(plan.g_full)
             ms_p, _ = timed_replays(plan.g_full, K)
             ms_c = 0.0
-        return {"ms": ms, "clk": clk, "bytes": sum(step_bytes) * world,
+        return {"ms": ms, "clk": clk, "steps_ms": steps, "bytes": sum(step_bytes) * world,
                 "partial_us": ms_p * 1e3 / (K * L), "combine_us": ms_c * 1e3 / (K * L),
                 "launch_bytes": kv_bytes_for(final)}
 
@@ -460,6 +470,10 @@ def run_ours(args, rank, world, local):
     m0 = measure(plan, ctx_end, clocks)
     value = m0["bytes"] / (m0["ms"] * 1e-3) / 1e9
     us_per_layer = m0["ms"] * 1e3 / (K * L)
+    # spread of the timed steps: p10 / median / p90 of each replay's µs per layer
+    st = sorted(x * 1e3 / L for x in m0["steps_ms"])
+    us_spread = [round(st[int(0.1 * (len(st) - 1))], 3), round(statistics.median(st), 3),
+                 round(st[int(0.9 * (len(st) - 1))], 3)] if st else None
 
     # correctness spot check of layer 0 at the final nkv (oracle). Its inputs
     # are the host copies: for the fused append, layer 0's cache is restored
@@ -596,7 +610,9 @@ def run_ours(args, rank, world, local):
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": K, "warmup": W, "ms_per_step": round(m0["ms"] / K, 4),
-            "us_per_layer": round(us_per_layer, 3), "higher_is_better": True, "scaling": "weak",
+            "us_per_layer": round(us_per_layer, 3),
+            "us_per_layer_p10_p50_p90": us_spread,
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": describe(w, L) + (", %d causal query rows per sequence" % n_q
                                                       if n_q > 1 else ""),
