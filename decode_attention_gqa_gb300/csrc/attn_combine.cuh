@@ -8,9 +8,11 @@
 // flight at once: a block covers one (sequence, head) and one 32-wide chunk
 // of head_dim (more blocks than heads, so the partials stream through many
 // SMs); each group of lanes folds its share of the splits into a running
-// (m, S, acc) with the §2.1 update rule (a larger maximum rescales what came
-// before), the groups of a warp are folded with shuffles and the warps
-// through shared memory. The result equals the two-pass form up to rounding.
+// (m, S, acc) with the §2.1 update rule, a batch of splits at a time (the
+// batch's maximum first, so that its weights are independent exponentials; a
+// larger maximum rescales what came before), the groups of a warp are folded
+// with shuffles and the warps through shared memory. The result equals the
+// two-pass form up to rounding.
 // A split whose mx is -inf (no rows) is skipped, so an all-empty row gives
 // o = 0 without evaluating -inf - (-inf). mx is in log2 units (the partial
 // kernel folds log2 e into q), so the weights use the base-2 exponential.
@@ -31,20 +33,6 @@ struct CombineCfg {
     static constexpr int NG = WARPS * SPW;            // split groups per block
     static constexpr int BATCH = 4;                   // split rows in flight per lane
 };
-
-// Fold (m2, S2, a2) into (m, S, a): the §2.1 rescale-and-add rule.
-template <int V>
-__device__ __forceinline__ void fold(float &m, float &S, float (&acc)[V], float m2, float S2,
-                                     const float (&a2)[V])
-{
-    if (m2 == -INFINITY) return;
-    const float mn = fmaxf(m, m2);
-    const float c1 = ex2(m - mn), c2 = ex2(m2 - mn);      // c1 = 0 while m = -inf
-    S = S * c1 + S2 * c2;
-#pragma unroll
-    for (int i = 0; i < V; ++i) acc[i] = acc[i] * c1 + a2[i] * c2;
-    m = mn;
-}
 
 template <int HD>
 __global__ void __launch_bounds__(CombineCfg<HD>::THREADS)
@@ -81,8 +69,25 @@ attn_combine(const CombineArgs a)
             const float4 t = ld_dep(reinterpret_cast<const float4 *>(oc + (size_t)(sp < P ? sp : 0) * HD));
             ov[b][0] = t.x; ov[b][1] = t.y; ov[b][2] = t.z; ov[b][3] = t.w;
         }
+        // the batch's maximum first, then independent weights (no serial exp chain)
+        float mb = m;
 #pragma unroll
-        for (int b = 0; b < C::BATCH; ++b) fold<4>(m, S, acc, mlv[b].x, mlv[b].y, ov[b]);
+        for (int b = 0; b < C::BATCH; ++b) mb = fmaxf(mb, mlv[b].x);
+        if (mb == -INFINITY) continue;                       // every split so far empty
+        const float c0 = m == -INFINITY ? 0.f : ex2(m - mb);
+        S *= c0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] *= c0;
+#pragma unroll
+        for (int b = 0; b < C::BATCH; ++b) {
+            // an empty split's o row was never written: skip it, never scale it by 0
+            if (mlv[b].x == -INFINITY) continue;
+            const float w = ex2(mlv[b].x - mb);
+            S = fmaf(w, mlv[b].y, S);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[i] = fmaf(w, ov[b][i], acc[i]);
+        }
+        m = mb;
     }
     // Fold the warp's split groups (lanes LPS apart hold the same dims) and
     // then the warps, each as maximum first, then one rescale and a sum, so
