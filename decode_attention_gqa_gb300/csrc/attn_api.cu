@@ -113,18 +113,6 @@ int resolve_variant(int variant, int head_dim, int group)
     return variant;
 }
 
-// ATTN_VARIANT_AUTO prefers the tcgen05 kernel for calls bound by latency
-// rather than bandwidth: head_dim 128 or 256, one query row, a known capacity,
-// and at full capacity at most kStableTiles 128-row tiles per SM over the whole
-// call. There it was measured as fast or faster at every context of the
-// 7b-like layer and on the head_dim-256 layer (one block per tile, no warp
-// merge); on long caches and batches the mma.sync kernel streams faster.
-bool auto_prefers_umma(int head_dim, int n_q, int n_seq, int n_kv_head, int64_t cap, int sm_count)
-{
-    return (head_dim == 128 || head_dim == 256) && n_q == 1 && cap > 0 && sm_count > 0 &&
-           cap * n_seq * n_kv_head <= (int64_t)sm_count * kStableTiles * 128;
-}
-
 // Static split count P (the host never sees nkv). With the capacity known,
 // size the chunk so that at full capacity the (sequence, KV head) units fill
 // `waves` waves of resident blocks -- one wave for a single sequence, eight for
@@ -167,6 +155,31 @@ int heuristic(int n_seq, int n_kv_head, int qgroups, int64_t cap, int sm_count,
     if (P < 1) P = 1;
     if (P > kMaxSplits) P = kMaxSplits;
     return (int)P;
+}
+
+// ATTN_VARIANT_AUTO takes the tcgen05 kernel for calls bound by latency rather
+// than bandwidth: head_dim 128 or 256; one query row, or several whose
+// (row, head) slots of a KV head fit one 16-slot block; a known capacity;
+// splits of at most one tile each; and one wave of its one-tile blocks (at
+// most 3 x 128 or 2 x 96 rows per SM at full capacity, so a short call). There
+// it was measured as fast or faster at every context of the 7b-like layer, on
+// the head_dim-256 layer and at two query rows; on long caches and batches the
+// mma.sync kernel streams faster, and several query groups per KV head or a
+// second wave of one-tile blocks make the tcgen05 kernel slower. On success
+// `ku` holds its kernel info. The call path and the planning entry points
+// share this rule, so that they report the kernel and split count a call uses.
+bool auto_takes_umma(int head_dim, int group, int n_q, int n_seq, int n_kv_head, int64_t cap,
+                     int sm_count, int n_splits, int split_len, bool kv_stable, attn::KernelInfo &ku)
+{
+    const int qgroups = (n_q * group + attn::kMqHeadsPerBlock - 1) / attn::kMqHeadsPerBlock;
+    if ((head_dim != 128 && head_dim != 256) || (n_q > 1 && qgroups != 1) || cap <= 0 || sm_count <= 0)
+        return false;
+    ku = kernel_info(head_dim, group, attn::kVariantUmma, n_q > 1);
+    if (!ku.available) return false;
+    const bool fits = split_len > 0 ? split_len <= ku.max_chunk
+                                    : n_splits == 0 || (int64_t)n_splits * ku.max_chunk >= cap;
+    const int64_t pu = n_splits > 0 ? n_splits : heuristic(n_seq, n_kv_head, 1, cap, sm_count, ku, kv_stable);
+    return fits && pu * n_kv_head * n_seq <= (int64_t)sm_count * ku.blocks_per_sm;
 }
 
 attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache,
@@ -219,18 +232,10 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     e = device_state(dev, &ds);
     if (e != cudaSuccess) return cuda_fail(e);
 
-    if (variant == ATTN_VARIANT_AUTO &&
-        auto_prefers_umma(head_dim, n_q, n_seq, n_kv_head, cap_known ? cap : 0, ds->sm_count)) {
-        const attn::KernelInfo ku = kernel_info(head_dim, group, attn::kVariantUmma, false);
-        // explicit splits that leave a split larger than one tile keep the mma.sync kernel,
-        // and so do splits that need more than one wave of its blocks (short split
-        // lengths: one tile per block leaves the blocks too little work each)
-        const bool fits = split_len > 0 ? split_len <= ku.max_chunk
-                                        : n_splits == 0 || (int64_t)n_splits * ku.max_chunk >= cap;
-        const int64_t pu = n_splits > 0 ? n_splits
-                                        : heuristic(n_seq, n_kv_head, 1, cap, ds->sm_count, ku, kv_stable != 0);
-        const bool one_wave = pu * n_kv_head * n_seq <= (int64_t)ds->sm_count * ku.blocks_per_sm;
-        if (ku.available && fits && one_wave) {
+    if (variant == ATTN_VARIANT_AUTO) {
+        attn::KernelInfo ku{};
+        if (auto_takes_umma(head_dim, group, n_q, n_seq, n_kv_head, cap_known ? cap : 0, ds->sm_count,
+                            n_splits, split_len, kv_stable != 0, ku)) {
             v = attn::kVariantUmma;
             ki = ku;
         }
@@ -576,6 +581,7 @@ namespace {
 int plan_variant(int n_seq, int n_q, int n_head, int n_kv_head, int head_dim, int64_t cap,
                  int &sm_count, int variant, attn::KernelInfo &ki)
 {
+    const bool kv_stable = (variant & ATTN_KV_STABLE) != 0;
     variant &= ~(ATTN_KV_BF16 | ATTN_KV_STABLE);
     if (variant != ATTN_VARIANT_AUTO && variant != ATTN_VARIANT_SIMT && variant != ATTN_VARIANT_TC &&
         variant != ATTN_VARIANT_TCGEN05 && variant != ATTN_VARIANT_TCGEN05_CLUSTER)
@@ -592,8 +598,9 @@ int plan_variant(int n_seq, int n_q, int n_head, int n_kv_head, int head_dim, in
             return 0;
     }
     int v = resolve_variant(variant, head_dim, group);
-    if (variant == ATTN_VARIANT_AUTO && auto_prefers_umma(head_dim, n_q, n_seq, n_kv_head, cap, sm_count) &&
-        kernel_info(head_dim, group, attn::kVariantUmma, false).available)
+    attn::KernelInfo ku{};
+    if (variant == ATTN_VARIANT_AUTO &&
+        auto_takes_umma(head_dim, group, n_q, n_seq, n_kv_head, cap, sm_count, 0, 0, kv_stable, ku))
         v = attn::kVariantUmma;
     ki = kernel_info(head_dim, group, v, n_q > 1);
     return ki.available ? v : 0;

@@ -299,11 +299,15 @@ int attn_split_heuristic_ex(int n_seq, int n_q, int n_head, int n_kv_head, int h
  * or ATTN_VARIANT_TCGEN05_CLUSTER (0 for an invalid shape or variant). An
  * explicit variant is returned as is;
  * ATTN_VARIANT_AUTO picks the tcgen05 kernel for a short call -- head_dim 128
- * or 256, one query row, cap > 0 and cap * n_seq * n_kv_head at most 4 tiles of 128
- * rows per SM -- and otherwise the mma.sync tensor-core kernel (head_dim % 16
- * == 0) or the CUDA-core kernel. With explicit splits that leave a split
- * longer than 128 rows, attn_decode_ex keeps the mma.sync kernel instead.
- * Host only; sm_count <= 0 queries the current device.
+ * or 256; one query row, or n_q * group <= 16 (a KV head's (row, head) pairs
+ * in one block); cap > 0; and the heuristic's splits, one tile each, in one
+ * wave of its blocks (3 per SM at head_dim 128, 2 at 256 for one query row,
+ * fewer for several) -- and otherwise the mma.sync tensor-core kernel
+ * (head_dim % 16 == 0) or the CUDA-core kernel. With ATTN_KV_STABLE in
+ * variant the split count follows the flagged heuristic. With explicit splits
+ * that leave a split longer than one tile, or too many blocks for one wave,
+ * attn_decode_ex keeps the mma.sync kernel instead. Host only; sm_count <= 0
+ * queries the current device.
  */
 int attn_resolve_variant(int n_seq, int n_q, int n_head, int n_kv_head, int head_dim, int64_t cap,
                          int sm_count, int variant);

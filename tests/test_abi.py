@@ -134,7 +134,10 @@ def test_split_heuristic_for_flagged_calls(lib):
     # two blocks per SM: 8 x 37 blocks of 224 rows
     assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_STABLE, n_q=4) == 37
     assert h(1, 28, 4, 128, 2048, 152, pkg.ATTN_KV_STABLE, n_q=4) == 19    # short: one per SM
-    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_STABLE, n_q=2) == 43     # 14 pairs: one group
+    # 2 rows x 7 heads = 14 pairs: one group, so variant 0 runs the tcgen05 kernel with one
+    # 128-row tile per split; the mma.sync kernel keeps its ring-sized blocks
+    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_STABLE, n_q=2) == 64
+    assert h(1, 28, 4, 128, 8192, 152, TC | S, n_q=2) == 43
     assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_VARIANT_SIMT, n_q=2) == 0  # tensor cores only
     # the CUDA-core kernel has its own granule and residency
     assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_VARIANT_SIMT) >= 1
@@ -159,13 +162,25 @@ def test_resolved_variant(lib):
     # 64 and an unknown capacity; CUDA cores for head_dim 8
     assert r(1, 1, 64, 8, 128, 131072, 152, 0) == TC
     assert r(32, 1, 32, 8, 128, 32768, 152, 0) == TC
-    assert r(1, 4, 28, 4, 128, 8192, 152, 0) == TC
+    assert r(1, 4, 28, 4, 128, 8192, 152, 0) == TC                 # 2 query groups per KV head
+    assert r(1, 2, 28, 4, 128, 8192, 152, 0) == T5                 # 14 slots: one group
+    assert r(1, 2, 28, 4, 128, 8192, 152, S) == T5
+    assert r(1, 3, 28, 4, 128, 8192, 152, 0) == TC                 # 21 slots
+    # 16 slots at head_dim 256: one block per SM, so 2 x 88 blocks are a second wave
+    assert r(1, 2, 16, 2, 256, 8400, 152, 0) == TC
+    assert r(1, 2, 16, 2, 256, 76 * 96, 152, 0) == T5
     assert r(1, 1, 8, 2, 64, 1024, 152, 0) == TC
     assert r(1, 1, 28, 4, 128, 0, 152, 0) == TC
     assert r(1, 1, 4, 2, 8, 64, 152, 0) == SI
-    # the boundary: cap * n_seq * n_kv_head <= 4 tiles of 128 rows per SM
-    assert r(1, 1, 28, 4, 128, 152 * 128, 152, 0) == T5
-    assert r(1, 1, 28, 4, 128, 152 * 128 + 1, 152, 0) == TC
+    # the boundary: one wave of one-tile blocks, 3 per SM at head_dim 128 (4 x 114 = 456
+    # blocks of 128 rows), 2 at head_dim 256 (2 x 152 = 304 blocks of 96 rows)
+    assert r(1, 1, 28, 4, 128, 114 * 128, 152, 0) == T5
+    assert r(1, 1, 28, 4, 128, 114 * 128 + 1, 152, 0) == TC
+    assert r(1, 1, 28, 4, 128, 114 * 128 + 1, 152, S) == TC
+    assert r(1, 1, 16, 2, 256, 152 * 96, 152, 0) == T5
+    assert r(1, 1, 16, 2, 256, 152 * 96 + 1, 152, 0) == TC
+    assert r(2, 1, 28, 4, 128, 57 * 128, 152, 0) == T5            # 2 sequences x 4 x 57
+    assert r(2, 1, 28, 4, 128, 57 * 128 + 1, 152, 0) == TC
     # explicit variants are kept; tcgen05 is built for head_dim 128 and one query row
     assert r(1, 1, 28, 4, 128, 8192, 152, SI) == SI
     assert r(1, 1, 28, 4, 128, 8192, 152, TC) == TC
