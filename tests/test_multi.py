@@ -44,8 +44,9 @@ def _run(pkg, case, n_q, n_head, n_kv, hd, cap, scale, P=0, blk=0, variant=0):
     return out.cpu().numpy()
 
 
-# variant 0 runs the mma.sync multi-query kernel; 3 the tcgen05 kernel (16 slots per block)
-@pytest.mark.parametrize("variant", [0, 3])
+# 2 forces the mma.sync multi-query kernel, 3 the tcgen05 kernel (16 slots per block);
+# variant 0 takes the tcgen05 kernel where a KV head's n_q x G slots fit one block
+@pytest.mark.parametrize("variant", [0, 2, 3])
 @pytest.mark.parametrize("hd", [64, 128, 256])
 @pytest.mark.parametrize("kv", ["f16", "bf16"])
 def test_multi_query_shapes(pkg, hd, kv, variant):
