@@ -24,14 +24,14 @@ namespace attn {
 
 template <int HD>
 struct CombineCfg {
-    static constexpr int WARPS = 8;
+    static constexpr int WARPS = 4;
     static constexpr int THREADS = WARPS * 32;
     static constexpr int DC = HD < 32 ? HD : 32;      // head_dim chunk per block
     static constexpr int NCHUNK = HD / DC;
     static constexpr int LPS = DC / 4;                // lanes per split row (float4 each)
     static constexpr int SPW = 32 / LPS;              // split groups per warp
     static constexpr int NG = WARPS * SPW;            // split groups per block
-    static constexpr int BATCH = 4;                   // split rows in flight per lane
+    static constexpr int BATCH = 8;                   // split rows in flight per lane
 };
 
 template <int HD>
@@ -65,8 +65,12 @@ attn_combine(const CombineArgs a)
 #pragma unroll
         for (int b = 0; b < C::BATCH; ++b) {
             const int sp = base + b * C::NG;
-            mlv[b] = sp < P ? ld_dep(ml + sp) : make_float2(-INFINITY, 0.f);
-            const float4 t = ld_dep(reinterpret_cast<const float4 *>(oc + (size_t)(sp < P ? sp : 0) * HD));
+            float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+            mlv[b] = make_float2(-INFINITY, 0.f);
+            if (sp < P) {                                     // past the last split: no load
+                mlv[b] = ld_dep(ml + sp);
+                t = ld_dep(reinterpret_cast<const float4 *>(oc + (size_t)sp * HD));
+            }
             ov[b][0] = t.x; ov[b][1] = t.y; ov[b][2] = t.z; ov[b][3] = t.w;
         }
         // the batch's maximum first, then independent weights (no serial exp chain)
