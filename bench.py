@@ -345,32 +345,36 @@ def run_ours(args, rank, world, local):
 
         def _calls(self, stream, stage):
             for l in range(L):
-                var = variant | (pkg.ATTN_KV_STABLE if args.kv_stable == "on" and l > 0 else 0)
-                if stage == "combine":
-                    pkg.attn_decode_combine(self.ws, self.ws_bytes, out[l], n_seq, w.n_head,
-                                            w.head_dim, self.P, stream=stream)
-                elif stage == "partial":
-                    pkg.attn_decode_partial(q[l], kc[l], vc[l], pos, n_seq, w.n_head, w.n_kv_head,
-                                            w.head_dim, w.scale, w.cap, self.P, self.blk,
-                                            var, self.ws, self.ws_bytes, stream=stream)
-                elif n_q > 1:
-                    pkg.attn_decode_multi(q[l], kc[l], vc[l], pos, out[l], n_seq, n_q, w.n_head,
-                                          w.n_kv_head, w.head_dim, w.scale, w.cap,
-                                          n_splits=self.P, split_len=self.blk, variant=var,
-                                          workspace=self.ws, workspace_bytes=self.ws_bytes,
-                                          stream=stream)
-                elif args.append:
-                    pkg.attn_decode_append(q[l], kn[l], vn[l], kc[l], vc[l], pos, out[l], n_seq,
-                                           w.n_head, w.n_kv_head, w.head_dim, w.scale, w.cap,
-                                           n_splits=self.P, split_len=self.blk,
-                                           variant=var, workspace=self.ws,
-                                           workspace_bytes=self.ws_bytes, stream=stream)
-                else:
-                    pkg.attn_decode_ex(q[l], kc[l], vc[l], pos, out[l], n_seq, w.n_head,
-                                       w.n_kv_head, w.head_dim, w.scale, w.cap, n_splits=self.P,
-                                       split_len=self.blk, variant=var,
-                                       workspace=self.ws, workspace_bytes=self.ws_bytes,
-                                       stream=stream)
+                self.call(l, stream, stage)
+
+        def call(self, l, stream, stage="full"):
+            """Layer l's library call on `stream` (the whole call, or one stage)."""
+            var = variant | (pkg.ATTN_KV_STABLE if args.kv_stable == "on" and l > 0 else 0)
+            if stage == "combine":
+                pkg.attn_decode_combine(self.ws, self.ws_bytes, out[l], n_seq, w.n_head,
+                                        w.head_dim, self.P, stream=stream)
+            elif stage == "partial":
+                pkg.attn_decode_partial(q[l], kc[l], vc[l], pos, n_seq, w.n_head, w.n_kv_head,
+                                        w.head_dim, w.scale, w.cap, self.P, self.blk,
+                                        var, self.ws, self.ws_bytes, stream=stream)
+            elif n_q > 1:
+                pkg.attn_decode_multi(q[l], kc[l], vc[l], pos, out[l], n_seq, n_q, w.n_head,
+                                      w.n_kv_head, w.head_dim, w.scale, w.cap,
+                                      n_splits=self.P, split_len=self.blk, variant=var,
+                                      workspace=self.ws, workspace_bytes=self.ws_bytes,
+                                      stream=stream)
+            elif args.append:
+                pkg.attn_decode_append(q[l], kn[l], vn[l], kc[l], vc[l], pos, out[l], n_seq,
+                                       w.n_head, w.n_kv_head, w.head_dim, w.scale, w.cap,
+                                       n_splits=self.P, split_len=self.blk,
+                                       variant=var, workspace=self.ws,
+                                       workspace_bytes=self.ws_bytes, stream=stream)
+            else:
+                pkg.attn_decode_ex(q[l], kc[l], vc[l], pos, out[l], n_seq, w.n_head,
+                                   w.n_kv_head, w.head_dim, w.scale, w.cap, n_splits=self.P,
+                                   split_len=self.blk, variant=var,
+                                   workspace=self.ws, workspace_bytes=self.ws_bytes,
+                                   stream=stream)
 
         def _capture(self, adv, stage):
             g = torch.cuda.CUDAGraph()
@@ -572,16 +576,34 @@ def run_ours(args, rank, world, local):
         h2d = sum(t.numel() * t.element_size() for t in hq + hk + hv) + hpos.numel() * 4
         d2h = sum(t.numel() * t.element_size() for t in hout)
 
-        def e2e_step():
-            with torch.cuda.stream(s):
+        # One graph per step: a copy stream brings the inputs layer by layer and
+        # layer l's call waits only for its own copies, so the calls (and the
+        # read-back of each layer's output) overlap the remaining copies.
+        cs = torch.cuda.Stream(device=dev)
+        landed = [torch.cuda.Event() for _ in range(L)]
+        g_e2e = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g_e2e, stream=s):
+            cur = torch.cuda.current_stream()
+            cs.wait_stream(cur)
+            with torch.cuda.stream(cs):
                 pos.copy_(hpos, non_blocking=True)
                 for l in range(L):
                     q[l].copy_(hq[l], non_blocking=True)
                     kc[l].copy_(hk[l], non_blocking=True)
                     vc[l].copy_(hv[l], non_blocking=True)
-                plan.g_full.replay()
-                for l in range(L):
-                    hout[l].copy_(out[l], non_blocking=True)
+                    landed[l].record(cs)
+            for l in range(L):
+                cur.wait_event(landed[l])
+                if l == 0 and advance:
+                    pos.add_(1)
+                plan.call(l, cur)
+                hout[l].copy_(out[l], non_blocking=True)
+            cur.wait_stream(cs)
+
+        def e2e_step():
+            with torch.cuda.stream(s):
+                g_e2e.replay()
 
         for _ in range(W):
             e2e_step()
