@@ -446,11 +446,13 @@ attn_split_partial_umma(const __grid_constant__ CUtensorMap kmap, const __grid_c
     // exits: after an abort, wait (bounded) for the copy and the MMAs.
     tc_fence_before();
     __syncthreads();
-    if (flags[0] && tid == 0) {
-        (void)mbar_wait_bounded(bar + 0, 0);
-        (void)mbar_wait_bounded(bar + 3, 0, 1000000ull);
+    if (flags[0]) {                           // read after the barrier: the same for every thread
+        if (tid == 0) {
+            (void)mbar_wait_bounded(bar + 0, 0);
+            (void)mbar_wait_bounded(bar + 3, 0, 1000000ull);
+        }
+        __syncthreads();
     }
-    __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tm, Cfg::TMEM_COLS);
 }

@@ -75,13 +75,17 @@ struct TcWarp {
         // lane owns elements [lane * PER, lane * PER + PER) of a head: one or
         // two 16-byte loads (8 bytes at head_dim 64) per head row, so the many
         // blocks reading the same q lines send few requests
-        // every row's load is issued unconditionally (a head past G reads
-        // head 0 and is zeroed afterwards), so the loads leave back to back
+        // a slot past G loads nothing (warp-uniform): re-reading head 0 for
+        // it would pile more requests onto the lines every block of the KV
+        // head already reads
         float x[ITER][PER];
 #pragma unroll
         for (int it = 0; it < ITER; ++it) {
             const int g = warp + it * NW;
-            const float *row = qg + (g < G ? g : 0) * HD + lane * PER;
+#pragma unroll
+            for (int j = 0; j < PER; ++j) x[it][j] = 0.f;
+            if (g >= G) continue;
+            const float *row = qg + g * HD + lane * PER;
             if constexpr (PER == 2) {
                 const float2 u = ld_dep(reinterpret_cast<const float2 *>(row));
                 x[it][0] = u.x;
