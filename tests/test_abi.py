@@ -7,6 +7,7 @@ import glob
 import os
 import re
 
+import numpy as np
 import pytest
 
 import decode_attention_gqa_gb300 as pkg
@@ -296,3 +297,34 @@ def test_decode_attention_checks_its_tensors_before_any_call():
         pkg.decode_attention(q, k.transpose(1, 2), k.transpose(1, 2), pos)   # not contiguous
     with pytest.raises(ValueError):
         pkg.decode_attention(q, k, k, pos, kernel=9)                   # no such kernel
+
+
+def test_tcgen05_choice_keeps_its_limits(lib):
+    """Wherever variant 0 names the tcgen05 kernel, the planned splits cover the
+    capacity one tile each and fit one wave of its blocks; several query rows
+    only when a KV head's pairs fit one 16-slot block. Seeded random shapes."""
+    rng = np.random.default_rng(12)
+    T5 = pkg.ATTN_VARIANT_TCGEN05
+    tile = {128: 128, 256: 96}
+    per_sm = {(128, False): 3, (256, False): 2, (128, True): 2, (256, True): 1}
+    seen = set()
+    for _ in range(4000):
+        hd = int(rng.choice([64, 128, 256]))
+        n_kv = int(rng.integers(1, 9))
+        G = int(rng.integers(1, 9))
+        n_q = int(rng.choice([1, 1, 2, 3, 4]))
+        n_seq = int(rng.integers(1, 5))
+        cap = int(rng.integers(1, 40000))
+        sms = int(rng.choice([132, 148, 152]))
+        flags = int(rng.choice([0, pkg.ATTN_KV_STABLE]))
+        v = pkg.attn_resolve_variant(n_seq, n_q, G * n_kv, n_kv, hd, cap, sms, flags)
+        P = pkg.attn_split_heuristic_ex(n_seq, n_q, G * n_kv, n_kv, hd, cap, sms, flags)
+        assert v in (pkg.ATTN_VARIANT_TC, T5) and P > 0
+        if v != T5:
+            continue
+        seen.add((hd, n_q > 1))
+        assert hd in (128, 256)
+        assert n_q == 1 or n_q * G <= 16
+        assert P * tile[hd] >= cap
+        assert P * n_kv * n_seq <= sms * per_sm[(hd, n_q > 1)]
+    assert seen == {(128, False), (256, False), (128, True), (256, True)}
