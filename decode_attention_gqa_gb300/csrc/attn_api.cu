@@ -178,7 +178,9 @@ bool auto_takes_umma(int head_dim, int group, int n_q, int n_seq, int n_kv_head,
     if (!ku.available) return false;
     const bool fits = split_len > 0 ? split_len <= ku.max_chunk
                                     : n_splits == 0 || (int64_t)n_splits * ku.max_chunk >= cap;
-    const int64_t pu = n_splits > 0 ? n_splits : heuristic(n_seq, n_kv_head, 1, cap, sm_count, ku, kv_stable);
+    const int64_t pu = n_splits > 0 ? n_splits
+                       : split_len > 0 ? (cap + split_len - 1) / split_len
+                                       : heuristic(n_seq, n_kv_head, 1, cap, sm_count, ku, kv_stable);
     return fits && pu * n_kv_head * n_seq <= (int64_t)sm_count * ku.blocks_per_sm;
 }
 
@@ -257,8 +259,13 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
         if (ds->fused_ok != 1) return ATTN_ERR_UNSUPPORTED;
         ki = kf;
     }
+    // by block length with no split count: one split per block of rows of the
+    // capacity (Red Lite dev35 "Change": P = ceil(positions / block))
+    const int64_t P_blk = split_len > 0 && n_splits == 0 ? (cap + split_len - 1) / split_len : 0;
+    if (P_blk > kMaxSplits) return ATTN_ERR_INVALID_ARG;
     const int P = v == attn::kVariantFused ? kFusedSplits
                 : n_splits > 0 ? n_splits
+                : P_blk > 0    ? (int)P_blk
                                : heuristic(n_seq, n_kv_head, n_q > 1 ? qgroups : 1,
                                            cap_known ? cap : 0, ds->sm_count, ki, kv_stable != 0);
     if (split_len > 0 && (int64_t)P * split_len < cap) return ATTN_ERR_INVALID_ARG;

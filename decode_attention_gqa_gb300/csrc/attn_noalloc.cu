@@ -45,17 +45,6 @@ extern "C" attn_status attn_decode_static(const float *q, const void *k_cache, c
         return attn_decode_ex(q, k_cache, v_cache, positions, out, n_seq, n_head, n_kv_head,
                               head_dim, scale, cap, n_splits, split_len, variant, nullptr, 0, stream);
 
-    int P = n_splits;
-    if (P == 0) {
-        P = attn_split_heuristic(n_seq, n_head, n_kv_head, head_dim, cap, 0);
-        if (P == 0)     // unsupported shape or no device: the regular path reports which
-            return attn_decode_ex(q, k_cache, v_cache, positions, out, n_seq, n_head, n_kv_head,
-                                  head_dim, scale, cap, n_splits, split_len, variant, nullptr, 0,
-                                  stream);
-    }
-    if (attn_workspace_size(n_seq, n_head, head_dim, P) > (size_t)ATTN_STATIC_SCRATCH_BYTES)
-        return ATTN_ERR_WORKSPACE;
-
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
@@ -70,7 +59,11 @@ extern "C" attn_status attn_decode_static(const float *q, const void *k_cache, c
         }
         scratch = g_static_ptr[dev];
     }
+    // attn_decode_ex plans the call exactly as it would with its own workspace
+    // (n_splits == 0: the split count for this variant, the early-start flag
+    // and the cache type included) and answers ATTN_ERR_WORKSPACE, before
+    // launching anything, when that plan needs more than the fixed array.
     return attn_decode_ex(q, k_cache, v_cache, positions, out, n_seq, n_head, n_kv_head, head_dim,
-                          scale, cap, P, split_len, variant, scratch, ATTN_STATIC_SCRATCH_BYTES,
-                          stream);
+                          scale, cap, n_splits, split_len, variant, scratch,
+                          ATTN_STATIC_SCRATCH_BYTES, stream);
 }

@@ -146,7 +146,9 @@ attn_status attn_decode(const float *q, const void *k_cache, const void *v_cache
  *                   the kernel variant 0 runs is reported by attn_resolve_variant;
  *                   > 0: fixed block of split_len
  *                   rows per split (Red Lite dev35 "Change"), which needs
- *                   P * split_len >= cap, else ATTN_ERR_INVALID_ARG.
+ *                   P * split_len >= cap, else ATTN_ERR_INVALID_ARG; with
+ *                   n_splits = 0 the call takes P = ceil(cap / split_len)
+ *                   (ATTN_ERR_INVALID_ARG past 4096 splits).
  *   variant         ATTN_VARIANT_*.
  *   workspace       device buffer of at least attn_workspace_size(...) bytes,
  *                   256-byte aligned; NULL selects the library-owned buffer as in
@@ -247,9 +249,12 @@ attn_status attn_decode_combine(const void *workspace, size_t workspace_bytes, f
  * allocating library routine). The first call on a device, with that device
  * current, looks up the array's device address (cudaGetSymbolAddress); make
  * that first call before any stream capture.
- *   - n_splits == 0 takes attn_split_heuristic(); a shape whose
- *     attn_workspace_size(n_seq, n_head, head_dim, P) exceeds
- *     ATTN_STATIC_SCRATCH_BYTES returns ATTN_ERR_WORKSPACE and launches nothing.
+ *   - n_splits == 0 takes the split count attn_decode_ex takes for the same
+ *     variant argument (attn_split_heuristic_ex: the kernel variant, the
+ *     early-start flag and the cache type all count). A call whose partials
+ *     need more than ATTN_STATIC_SCRATCH_BYTES (attn_workspace_size(n_seq,
+ *     n_head, head_dim, P)) returns ATTN_ERR_WORKSPACE and launches nothing;
+ *     ATTN_VARIANT_TCGEN05_CLUSTER keeps its partials on chip and uses none.
  *   - All calls share the one array and it keeps the last call's contents.
  *     Nothing in it has to start at zero: every split writes its (mx, S) before
  *     the combine reads it, and oc is only read for splits that wrote it in
@@ -288,7 +293,9 @@ int attn_split_heuristic(int n_seq, int n_head, int n_kv_head, int head_dim, int
  * beside this call's and start their copies while it finishes, and a block
  * takes no more rows than its pipeline holds at once (3 tiles of 64 rows at
  * head_dim 128), so that all of its copies start before the previous kernel
- * ends. Returns 0 for an invalid shape or variant.
+ * ends. Returns 0 for an invalid shape or variant. This is the count-mode
+ * plan; a call by block length (split_len > 0) with n_splits = 0 takes
+ * P = ceil(cap / split_len) instead.
  */
 int attn_split_heuristic_ex(int n_seq, int n_q, int n_head, int n_kv_head, int head_dim,
                             int64_t cap, int sm_count, int variant);

@@ -90,3 +90,31 @@ def test_call_runs_the_planned_kernel_and_split_count(pkg, shape, stable):
         ref = oracle.attn_decode_multi(case["q"], case["k"], case["v"], case["positions"], n_q,
                                        n_head, n_kv, hd, cap, scale, n_threads=8)
     assert_close(outs[0], ref, "plan %s stable=%s: variant %d, P=%d" % (shape, stable, v, P))
+
+
+@pytest.mark.parametrize("blk", [32, 64, 96, 128, 256])
+def test_block_length_without_split_count_takes_one_split_per_block(pkg, blk):
+    """By block length with n_splits = 0 the call takes P = ceil(cap / split_len)
+    (Red Lite dev35 "Change": one split per block of positions): bit for bit the
+    call with that P given, in a workspace of exactly that size; both match the
+    oracle."""
+    import torch
+    n_head, n_kv, hd, cap = 16, 2, 256, 8400
+    case = make_case(7300 + blk, 1, n_head, n_kv, hd, cap, (cap - 5,))
+    dev = to_device(case)
+    scale = 1 / math.sqrt(hd)
+    P = -(-cap // blk)
+    ws_bytes = pkg.attn_workspace_size(1, n_head, hd, P)
+    outs = []
+    for n_splits in (0, P):
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        out = torch.full_like(dev["q"], float("nan"))
+        pkg.attn_decode_ex(dev["q"], dev["k"], dev["v"], dev["positions"], out, 1, n_head, n_kv,
+                           hd, scale, cap, n_splits=n_splits, split_len=blk, workspace=ws,
+                           workspace_bytes=ws_bytes)
+        torch.cuda.synchronize()
+        outs.append(out.cpu().numpy())
+    np.testing.assert_array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+    ref = oracle.attn_decode(case["q"], case["k"], case["v"], case["positions"], n_head, n_kv, hd,
+                             cap, scale, n_threads=8)
+    assert_close(outs[0], ref, "block %d, n_splits 0 -> P %d" % (blk, P))
