@@ -73,6 +73,8 @@ def parse_args():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other configurations the default run records under `workloads`")
     return ap.parse_args()
 
 
@@ -208,14 +210,17 @@ class ClockSampler:
 
 # ------------------------------------------------------------ CPU oracle leg
 
-def oracle_sample(layers_host, w, budget_s: float, max_units=None, kv_dtype="f16", n_q=1):
-    """Run the oracle on all host cores over (layer, KV head group) units of the
-    workload -- every query head of one KV head against that head's rows -- until
-    budget_s (or max_units); return (GB/s of K+V, units, seconds, threads, what).
-    With n_q > 1 the unit holds all n_q causal query rows of the group."""
+def oracle_sample(layers_host, w, budget_s: float, max_units=None, kv_dtype="f16", n_q=1,
+                  threads=None):
+    """Run the oracle over (layer, KV head group) units of the workload -- every
+    query head of one KV head against that head's rows -- until budget_s (or
+    max_units), on `threads` host threads (default: every core the process may
+    use); return (GB/s of K+V, units, seconds, threads, what). With n_q > 1 the
+    unit holds all n_q causal query rows of the group."""
     import numpy as np
     import oracle
-    threads = len(os.sched_getaffinity(0))
+    if threads is None:
+        threads = len(os.sched_getaffinity(0))
     G = w.n_head // w.n_kv_head
     units = [(l, hk) for l in range(len(layers_host)) for hk in range(w.n_kv_head)]
     done, nbytes, t0 = 0, 0, time.perf_counter()
@@ -248,7 +253,26 @@ def oracle_sample(layers_host, w, budget_s: float, max_units=None, kv_dtype="f16
 
 def make_host_layers(w, layers, kv_dtype="f16"):
     from decode_attention_gqa_gb300 import synthetic as syn
-    return [syn.make_layer(w, layer=l, kv_dtype=kv_dtype) for l in range(layers)]
+    threads = len(os.sched_getaffinity(0))
+    return [syn.make_layer(w, layer=l, kv_dtype=kv_dtype, threads=threads) for l in range(layers)]
+
+
+def config_of(args, w, L, world):
+    """The workload as both arms print it: shapes, sizes and mode, nothing
+    that depends on the implementation (split count, kernel, flags)."""
+    advance = w.n_seq == 1
+    ctx_end = max(w.ctx)
+    rows = sum(min(max(int(c), 0), w.cap) for c in ([ctx_end] if advance else w.ctx))
+    n_q = args.n_q
+    return {"workload": describe(w, L) + (", %d causal query rows per sequence" % n_q
+                                          if n_q > 1 else ""),
+            "name": w.name, "ctx": ctx_end, "cap": w.cap,
+            "n_seq": w.n_seq, "n_head": w.n_head, "n_kv_head": w.n_kv_head,
+            "head_dim": w.head_dim, "layers": L, "split_len": args.split_len,
+            "kv_dtype": args.kv_dtype, "append": args.append, "n_q": n_q,
+            "l2": "inputs larger than L2 (%d MB of K+V per step)"
+                  % (rows * w.n_kv_head * w.head_dim * 4 * L // 2 ** 20),
+            "parallelism": "replicas" if world > 1 else "single"}
 
 
 def _t(a):
@@ -283,13 +307,53 @@ def describe(w, L):
     }.get(w.name, w.name)
 
 
+# The other configurations a default run records under `workloads`: the long
+# grouped layer by count and at each block length of its sweep, the stress and
+# ragged calls, several causal query rows, the fused append and the bfloat16
+# cache on the 7b layer. Each entry is timed like the headline (graph replay,
+# events on the launching stream, its own parity spot check against the oracle).
+EXTRA_WORKLOADS = [
+    ("long", {"workload": "long"}),
+    ("long_blk32", {"workload": "long", "split_len": 32}),
+    ("long_blk64", {"workload": "long", "split_len": 64}),
+    ("long_blk128", {"workload": "long", "split_len": 128}),
+    ("long_blk256", {"workload": "long", "split_len": 256}),
+    ("stress", {"workload": "stress"}),
+    ("ragged", {"workload": "ragged"}),
+    ("7b_nq2", {"n_q": 2}),
+    ("7b_nq4", {"n_q": 4}),
+    ("7b_nq8", {"n_q": 8}),
+    ("7b_append", {"append": True}),
+    ("7b_bf16", {"kv_dtype": "bf16"}),
+]
+
+
+def is_default_run(args) -> bool:
+    return (args.workload == "7b" and not args.ctx and not args.cap and not args.split_len
+            and not args.layers and not args.variant and not args.splits and args.kv_dtype == "f16"
+            and not args.append and args.n_q == 1 and args.kv_stable == "on")
+
+
+def summarize(r):
+    """One `workloads` entry from a measured line."""
+    rf = r["roofline"]
+    return {"config": r["config"]["workload"], "kernel": rf["kernel"],
+            "partial_variant": rf["partial_variant"], "n_splits": r["plan"]["n_splits"],
+            "split_len": r["config"]["split_len"], "us_per_call": r["us_per_layer"],
+            "gbs": r["value"], "frac": round(r["value"] / rf["peak"], 4),
+            "partial_us": rf["us_per_launch"], "partial_gbs": rf["achieved"],
+            "partial_frac": rf["frac"], "combine_us": rf["combine_us_per_launch"],
+            "traffic": rf["traffic"], "parity_spot_check": r["parity_spot_check"],
+            "steps": r["steps"], "warmup": r["warmup"]}
+
+
 def run_ours(args, rank, world, local):
-    import numpy as np
+    import copy
+
     import torch
 
     import decode_attention_gqa_gb300 as pkg
     from decode_attention_gqa_gb300 import build as cuda_build
-    from decode_attention_gqa_gb300 import synthetic as syn
 
     torch.cuda.set_device(local)
     dist_init(world, "nccl")
@@ -297,6 +361,34 @@ def run_ours(args, rank, world, local):
         cuda_build.build()
     dist_barrier(world)
     pkg.load()
+
+    line = measure_one(args, rank, world, local)
+    if not args.no_workloads and is_default_run(args):
+        extra = {}
+        for name, over in EXTRA_WORKLOADS:
+            a2 = copy.copy(args)
+            for k, v in over.items():
+                setattr(a2, k, v)
+            a2.no_e2e = a2.no_cpu = a2.no_clocks = a2.no_sweep = True
+            extra[name] = summarize(measure_one(a2, rank, world, local))
+            torch.cuda.empty_cache()
+        line["workloads"] = extra
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def measure_one(args, rank, world, local):
+    """Time one configuration (the headline, or one `workloads` entry) and
+    return its JSON line as a dict."""
+    import numpy as np
+    import torch
+
+    import decode_attention_gqa_gb300 as pkg
+    from decode_attention_gqa_gb300 import build as cuda_build
+    from decode_attention_gqa_gb300 import synthetic as syn
 
     w = workload_for(args)
     L = args.layers or w.layers
@@ -449,26 +541,17 @@ def run_ours(args, rank, world, local):
                 "partial_us": ms_p * 1e3 / (K * L), "combine_us": ms_c * 1e3 / (K * L),
                 "launch_bytes": kv_bytes_for(final)}
 
-    # ---- main timed region: the library's default split choice
+    # ---- main timed region: the library's own plan (the split count of the
+    # flagged layers 2..L; layer 1 runs the same count without the flag)
     blk0 = args.split_len
-    if args.splits:
-        P0 = args.splits
-    elif blk0:
-        P0 = -(-w.cap // blk0)
-    else:
-        P0 = pkg.attn_split_heuristic_ex(n_seq, n_q, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0,
-                                         variant | (pkg.ATTN_KV_STABLE
-                                                    if args.kv_stable == "on" and L > 1 else 0))
-    # the partial kernel this plan runs (variant 0 resolves by the call's shape;
-    # explicit splits longer than one 128-row tile keep the mma.sync kernel)
-    resolved = pkg.attn_resolve_variant(n_seq, n_q, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0,
-                                        variant)
-    tile5 = 96 if w.head_dim == 256 else 128           # rows per tcgen05 block
-    if resolved == 3 and not (blk0 <= tile5 if blk0 else P0 * tile5 >= w.cap):
-        resolved = 2
-    if resolved == 4 and (blk0 or P0 != 16):
-        resolved = 3 if (blk0 <= tile5 if blk0 else P0 * tile5 >= w.cap) else 2
+    stable_flag = pkg.ATTN_KV_STABLE if args.kv_stable == "on" and L > 1 else 0
+    _, P0, _ = pkg.attn_plan_call(n_seq, n_q, w.n_head, w.n_kv_head, w.head_dim, w.cap,
+                                  args.splits, blk0, variant | stable_flag)
+    # the partial kernel every layer's call runs with that count
+    resolved, _, _ = pkg.attn_plan_call(n_seq, n_q, w.n_head, w.n_kv_head, w.head_dim, w.cap, P0,
+                                        blk0, variant)
     plan = Plan(P0, blk0)
+    launches_per_call = 1 if resolved == 4 else 2       # the cluster-fused kernel has no combine
     ctx_end = max(w.ctx)
     clocks = ClockSampler(local, enabled=not args.no_clocks)
     m0 = measure(plan, ctx_end, clocks)
@@ -619,42 +702,40 @@ def run_ours(args, rank, world, local):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(el * 1e3 / K, 3)}
 
-    # ---- CPU oracle baseline (rank 0 only, N == 1)
+    # ---- CPU oracle baseline (rank 0 only, N == 1): on every core the process
+    # may use, and on one thread
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         rate, done, el, threads, what = oracle_sample(host, w, budget_s=10.0,
                                                       kv_dtype=args.kv_dtype, n_q=n_q)
+        rate1, done1, el1, _, what1 = oracle_sample(host, w, budget_s=8.0, kv_dtype=args.kv_dtype,
+                                                    n_q=n_q, threads=1)
         cpu = {"value": round(rate, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": "%s of the %s workload (%.1f s)" % (what, w.name, el)}
+               "sample": "%s of the %s workload (%.1f s)" % (what, w.name, el),
+               "single_thread": {"value": round(rate1, 4), "unit": UNIT, "cores": 1,
+                                 "sample": "%s of the %s workload (%.1f s)" % (what1, w.name, el1)},
+               "ms_per_layer_call": round(kv_bytes_for([ctx_end] if advance else w.ctx)
+                                          / (rate * 1e9) * 1e3, 3),
+               "ms_per_layer_call_single_thread": round(kv_bytes_for([ctx_end] if advance else w.ctx)
+                                                        / (rate1 * 1e9) * 1e3, 3)}
 
     spills = cuda_build.spill_report()
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
-            "steps": K, "warmup": W, "ms_per_step": round(m0["ms"] / K, 4),
-            "us_per_layer": round(us_per_layer, 3),
-            "us_per_layer_p10_p50_p90": us_spread,
-            "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": describe(w, L) + (", %d causal query rows per sequence" % n_q
-                                                      if n_q > 1 else ""),
-                       "name": w.name, "ctx": ctx_end, "cap": w.cap,
-                       "n_seq": n_seq, "n_head": w.n_head, "n_kv_head": w.n_kv_head,
-                       "head_dim": w.head_dim, "layers": L, "n_splits": P0, "split_len": blk0,
-                       "variant": args.variant, "kv_dtype": args.kv_dtype, "append": args.append,
-                       "kv_stable": args.kv_stable, "n_q": n_q,
-                       "l2": "inputs larger than L2 (%d MB of K+V per step)"
-                             % (kv_bytes_for([ctx_end] if advance else w.ctx) * L // 2 ** 20),
-                       "parallelism": "replicas" if world > 1 else "single"},
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": 2 * L * K, "clocks": m0["clk"], "sweep": sweep,
-            "parity_spot_check": parity_ok,
-            "ptxas_spill_bytes": sum(v["spill_stores"] + v["spill_loads"] for v in spills.values()),
-        }
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    return {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(m0["ms"] / K, 4),
+        "us_per_layer": round(us_per_layer, 3),
+        "us_per_layer_p10_p50_p90": us_spread,
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_of(args, w, L, world),
+        "plan": {"n_splits": P0, "split_len": blk0, "variant": args.variant,
+                 "kv_stable": args.kv_stable, "partial_kernel": roofline["kernel"],
+                 "kernels_per_call": launches_per_call},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches_per_call * L * K, "clocks": m0["clk"], "sweep": sweep,
+        "parity_spot_check": parity_ok,
+        "ptxas_spill_bytes": sum(v["spill_stores"] + v["spill_loads"] for v in spills.values()),
+    }
 
 
 # ------------------------------------------------------- reference arm (oracle)
@@ -665,17 +746,23 @@ def run_reference(args, rank, world, local):
     the step, sized so that warm-up plus steps stay within about two minutes."""
     if rank != 0:
         return
+    from decode_attention_gqa_gb300 import synthetic as syn
     w = workload_for(args)
     L = args.layers or w.layers
-    host = make_host_layers(w, min(L, 2))
-    rate1, _, el1, threads, _ = oracle_sample(host, w, budget_s=0.0, max_units=1)
+    host = make_host_layers(w, min(L, 2), args.kv_dtype)
+    if args.n_q > 1:
+        for l, h in enumerate(host):
+            h["q"] = syn.make_q_multi(w, args.n_q, layer=l)
+    kw = dict(kv_dtype=args.kv_dtype, n_q=args.n_q)
+    rate1, _, el1, threads, _ = oracle_sample(host, w, budget_s=0.0, max_units=1, **kw)
     per_step = max(1, min(L * w.n_kv_head,
                           int(100.0 / max(el1 * (args.steps + args.warmup), 1e-6))))
     for _ in range(args.warmup):
-        oracle_sample(host, w, budget_s=0.0, max_units=per_step)
+        oracle_sample(host, w, budget_s=0.0, max_units=per_step, **kw)
     total_bytes, total_s = 0.0, 0.0
     for _ in range(args.steps):
-        rate, done, el, threads, what = oracle_sample(host, w, budget_s=0.0, max_units=per_step)
+        rate, done, el, threads, what = oracle_sample(host, w, budget_s=0.0, max_units=per_step,
+                                                      **kw)
         total_bytes += rate * el * 1e9
         total_s += el
     value = total_bytes / total_s / 1e9
@@ -687,7 +774,7 @@ def run_reference(args, rank, world, local):
         "ms_per_step": round(total_s * 1e3 / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": describe(w, L), "name": w.name, "ctx": max(w.ctx), "layers": L},
+        "config": config_of(args, w, L, world),
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,

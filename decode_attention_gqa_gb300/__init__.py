@@ -26,7 +26,8 @@ __all__ = [
     "attn_decode_partial",
     "attn_decode_combine",
     "attn_decode_static",
-    "attn_split_heuristic", "attn_split_heuristic_ex", "attn_resolve_variant", "attn_workspace_size",
+    "attn_split_heuristic", "attn_split_heuristic_ex", "attn_resolve_variant", "attn_plan_call",
+    "attn_workspace_size",
     "attn_read_device_error", "attn_selftest_bounded_wait", "attn_status_string",
     "attn_last_cuda_error", "attn_version",
 ]
@@ -95,6 +96,9 @@ def load():
         lib.attn_split_heuristic_ex.argtypes = [i32, i32, i32, i32, i32, i64, i32, i32]
         lib.attn_resolve_variant.restype = i32
         lib.attn_resolve_variant.argtypes = [i32, i32, i32, i32, i32, i64, i32, i32]
+        lib.attn_plan_call.restype = i32
+        lib.attn_plan_call.argtypes = [i32, i32, i32, i32, i32, i64, i32, i32, i32,
+                                       ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(sz)]
         lib.attn_workspace_size.restype = sz
         lib.attn_workspace_size.argtypes = [i32, i32, i32, i32]
         lib.attn_read_device_error.restype = i32
@@ -279,6 +283,19 @@ def attn_resolve_variant(n_seq, n_q, n_head, n_kv_head, head_dim, cap, sm_count,
     the heuristic's split count; 0 for an unsupported shape."""
     return load().attn_resolve_variant(n_seq, n_q, n_head, n_kv_head, head_dim, cap, sm_count,
                                        variant)
+
+
+def attn_plan_call(n_seq, n_q, n_head, n_kv_head, head_dim, cap, n_splits=0, split_len=0,
+                   variant=0):
+    """(kernel variant, split count, workspace bytes) of the call with these
+    arguments; raises AttnError with the status the call would return."""
+    v = ctypes.c_int(0)
+    p = ctypes.c_int(0)
+    ws = ctypes.c_size_t(0)
+    _check(load().attn_plan_call(n_seq, n_q, n_head, n_kv_head, head_dim, cap, n_splits, split_len,
+                                 variant, ctypes.byref(v), ctypes.byref(p), ctypes.byref(ws)),
+           "attn_plan_call")
+    return v.value, p.value, ws.value
 
 
 def attn_workspace_size(n_seq, n_head, head_dim, n_splits) -> int:

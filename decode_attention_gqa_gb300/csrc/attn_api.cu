@@ -184,6 +184,104 @@ bool auto_takes_umma(int head_dim, int group, int n_q, int n_seq, int n_kv_head,
     return fits && pu * n_kv_head * n_seq <= (int64_t)sm_count * ku.blocks_per_sm;
 }
 
+// The plan of a call: which partial kernel runs, how many splits, how many
+// workspace bytes, and the facts the launch needs besides.
+struct CallPlan {
+    int variant = 0;                  // resolved kernel (attn::kVariant*), never auto
+    attn::KernelInfo ki{};
+    int n_splits = 0;
+    size_t workspace = 0;             // bytes of partials (0: the fused form keeps them on chip)
+    int group = 0;
+    int qgroups = 1;
+    int kv_dtype = attn::kKvF16;
+    int kv_stable = 0;
+};
+
+// Checks of everything but the pointers, done before the device is touched.
+attn_status check_shape(int n_seq, int n_head, int n_kv_head, int head_dim, int64_t cap,
+                        int n_splits, int split_len, int variant, int n_q, bool appending,
+                        CallPlan &pl)
+{
+    pl.kv_dtype = (variant & ATTN_KV_BF16) ? attn::kKvBf16 : attn::kKvF16;
+    pl.kv_stable = (variant & ATTN_KV_STABLE) ? 1 : 0;
+    variant &= ~(ATTN_KV_BF16 | ATTN_KV_STABLE);
+    if (n_seq < 0 || n_head <= 0 || n_kv_head <= 0 || head_dim <= 0) return ATTN_ERR_INVALID_ARG;
+    if (n_head % n_kv_head != 0) return ATTN_ERR_INVALID_ARG;
+    if (cap < 1) return ATTN_ERR_INVALID_ARG;
+    if (n_splits < 0 || n_splits > kMaxSplits || split_len < 0) return ATTN_ERR_INVALID_ARG;
+    if (variant != ATTN_VARIANT_AUTO && variant != ATTN_VARIANT_SIMT && variant != ATTN_VARIANT_TC &&
+        variant != ATTN_VARIANT_TCGEN05 && variant != ATTN_VARIANT_TCGEN05_CLUSTER)
+        return ATTN_ERR_INVALID_ARG;
+    if (n_seq > 65535 || n_kv_head > 65535) return ATTN_ERR_INVALID_ARG;   // grid z limit; heads kept as before
+    if ((int64_t)n_seq * cap > kMaxFlatRows - 1024) return ATTN_ERR_INVALID_ARG;
+    pl.group = n_head / n_kv_head;
+    // n_q * G <= 8192 also keeps the kernels' multiply-shift division by G exact
+    if (n_q < 1 || n_q > 1024) return ATTN_ERR_INVALID_ARG;
+    if (n_q > 1 && appending) return ATTN_ERR_INVALID_ARG;
+    if (!head_dim_supported(head_dim) || pl.group > 8) return ATTN_ERR_UNSUPPORTED;
+    if (n_q > 1 && (head_dim % 16 != 0 || variant == ATTN_VARIANT_SIMT)) return ATTN_ERR_UNSUPPORTED;
+    pl.variant = resolve_variant(variant, head_dim, pl.group);
+    const int qg = (n_q * pl.group + attn::kMqHeadsPerBlock - 1) / attn::kMqHeadsPerBlock;
+    if (n_q > 1 && (int64_t)n_kv_head * qg > 65535) return ATTN_ERR_INVALID_ARG;
+    pl.qgroups = n_q > 1 ? qg : 1;
+    pl.ki = kernel_info(head_dim, pl.group, pl.variant, n_q > 1);
+    if (!pl.ki.available) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+// The rest of the plan, which needs the device (its SM count; for the fused
+// form whether it holds the cluster). Called with g_mu held, after
+// check_shape, for n_seq > 0.
+attn_status finish_plan(DeviceState *ds, int n_seq, int n_head, int n_kv_head, int head_dim,
+                        int64_t cap, bool cap_known, int n_splits, int split_len, int variant,
+                        int stages, int n_q, CallPlan &pl)
+{
+    variant &= ~(ATTN_KV_BF16 | ATTN_KV_STABLE);
+    if (variant == ATTN_VARIANT_AUTO) {
+        attn::KernelInfo ku{};
+        if (auto_takes_umma(head_dim, pl.group, n_q, n_seq, n_kv_head, cap_known ? cap : 0, ds->sm_count,
+                            n_splits, split_len, pl.kv_stable != 0, ku)) {
+            pl.variant = attn::kVariantUmma;
+            pl.ki = ku;
+        }
+    }
+    // The cluster-fused form of the tcgen05 kernel (partial and combine in one launch,
+    // 16 splits per (sequence, KV head) merged through distributed shared memory),
+    // on request only: a whole call, one query row, head_dim 128, splits by count with
+    // P = 16 (n_splits 0 or 16), a capacity of at most 16 blocks of 4 tiles, and a
+    // device that holds the 16-block cluster. Variant 0 does not take it: on one box it
+    // was 1 % faster than the plain tcgen05 kernel at context 2048 and 7-13 % slower at
+    // 512 and 128 (capacity 2048), and 20 % slower at the 7b capacity of 8192.
+    if (pl.variant == attn::kVariantFused) {
+        const attn::KernelInfo kf = kernel_info(head_dim, pl.group, attn::kVariantFused, n_q > 1);
+        bool ok = kf.available && n_q == 1 && stages == (attn::kStagePartial | attn::kStageCombine) &&
+                  split_len == 0 && (n_splits == 0 || n_splits == kFusedSplits) && cap_known &&
+                  cap <= (int64_t)kFusedSplits * kf.max_chunk;
+        if (!ok) return ATTN_ERR_INVALID_ARG;
+        if (ds->fused_ok < 0) ds->fused_ok = attn::fused_fits_hd128() ? 1 : 0;   // asked once per device
+        if (ds->fused_ok != 1) return ATTN_ERR_UNSUPPORTED;
+        pl.ki = kf;
+    }
+    // by block length with no split count: one split per block of rows of the
+    // capacity (Red Lite dev35 "Change": P = ceil(positions / block))
+    const int64_t P_blk = split_len > 0 && n_splits == 0 ? (cap + split_len - 1) / split_len : 0;
+    if (P_blk > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+    const int P = pl.variant == attn::kVariantFused ? kFusedSplits
+                : n_splits > 0 ? n_splits
+                : P_blk > 0    ? (int)P_blk
+                               : heuristic(n_seq, n_kv_head, pl.qgroups, cap_known ? cap : 0,
+                                           ds->sm_count, pl.ki, pl.kv_stable != 0);
+    if (split_len > 0 && (int64_t)P * split_len < cap) return ATTN_ERR_INVALID_ARG;
+    // one tile per block: every split must fit in max_chunk rows at any nkv <= cap
+    if (pl.ki.max_chunk > 0 && (split_len > 0 ? split_len > pl.ki.max_chunk
+                                              : (!cap_known || (int64_t)P * pl.ki.max_chunk < cap)))
+        return ATTN_ERR_INVALID_ARG;
+    pl.n_splits = P;
+    // the fused form keeps its partial states on chip: no workspace
+    pl.workspace = pl.variant == attn::kVariantFused ? 0 : attn_workspace_size(n_seq, n_q * n_head, head_dim, P);
+    return ATTN_OK;
+}
+
 attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache,
                         const int32_t *positions, float *out, int n_seq, int n_head,
                         int n_kv_head, int head_dim, float scale, int64_t cap, bool cap_known,
@@ -192,36 +290,19 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
                         const void *k_new = nullptr, const void *v_new = nullptr, int n_q = 1)
 {
     // ---- synchronous argument checks, nothing launched yet ----
-    const int kv_dtype = (variant & ATTN_KV_BF16) ? attn::kKvBf16 : attn::kKvF16;
-    const int kv_stable = (variant & ATTN_KV_STABLE) ? 1 : 0;
-    variant &= ~(ATTN_KV_BF16 | ATTN_KV_STABLE);
-    if (n_seq < 0 || n_head <= 0 || n_kv_head <= 0 || head_dim <= 0) return ATTN_ERR_INVALID_ARG;
-    if (n_head % n_kv_head != 0) return ATTN_ERR_INVALID_ARG;
+    // (every check that answers ATTN_ERR_INVALID_ARG for the pointers and the
+    // scale comes before the shape checks that can answer ATTN_ERR_UNSUPPORTED)
     if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-    if (cap < 1) return ATTN_ERR_INVALID_ARG;
-    if (n_splits < 0 || n_splits > kMaxSplits || split_len < 0) return ATTN_ERR_INVALID_ARG;
-    if (variant != ATTN_VARIANT_AUTO && variant != ATTN_VARIANT_SIMT && variant != ATTN_VARIANT_TC &&
-        variant != ATTN_VARIANT_TCGEN05 && variant != ATTN_VARIANT_TCGEN05_CLUSTER)
-        return ATTN_ERR_INVALID_ARG;
     if (n_seq > 0 && (!q || !k_cache || !v_cache || !positions)) return ATTN_ERR_INVALID_ARG;
     if (n_seq > 0 && (stages & attn::kStageCombine) && !out) return ATTN_ERR_INVALID_ARG;
-    if (n_seq > 65535 || n_kv_head > 65535) return ATTN_ERR_INVALID_ARG;   // grid z limit; heads kept as before
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(positions) ||
         !aligned16(out) || !aligned16(k_new) || !aligned16(v_new))
         return ATTN_ERR_INVALID_ARG;
     if ((k_new == nullptr) != (v_new == nullptr)) return ATTN_ERR_INVALID_ARG;
-    if ((int64_t)n_seq * cap > kMaxFlatRows - 1024) return ATTN_ERR_INVALID_ARG;
-    const int group = n_head / n_kv_head;
-    // n_q * G <= 8192 also keeps the kernels' multiply-shift division by G exact
-    if (n_q < 1 || n_q > 1024) return ATTN_ERR_INVALID_ARG;
-    if (n_q > 1 && k_new) return ATTN_ERR_INVALID_ARG;
-    if (!head_dim_supported(head_dim) || group > 8) return ATTN_ERR_UNSUPPORTED;
-    if (n_q > 1 && (head_dim % 16 != 0 || variant == ATTN_VARIANT_SIMT)) return ATTN_ERR_UNSUPPORTED;
-    int v = resolve_variant(variant, head_dim, group);
-    const int qgroups = (n_q * group + attn::kMqHeadsPerBlock - 1) / attn::kMqHeadsPerBlock;
-    if (n_q > 1 && (int64_t)n_kv_head * qgroups > 65535) return ATTN_ERR_INVALID_ARG;
-    attn::KernelInfo ki = kernel_info(head_dim, group, v, n_q > 1);
-    if (!ki.available) return ATTN_ERR_UNSUPPORTED;
+    CallPlan pl;
+    attn_status st = check_shape(n_seq, n_head, n_kv_head, head_dim, cap, n_splits, split_len, variant,
+                                 n_q, k_new != nullptr, pl);
+    if (st != ATTN_OK) return st;
     if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return ATTN_ERR_INVALID_ARG;
     if (n_seq == 0) return ATTN_OK;
 
@@ -233,48 +314,12 @@ attn_status decode_impl(const float *q, const void *k_cache, const void *v_cache
     DeviceState *ds = nullptr;
     e = device_state(dev, &ds);
     if (e != cudaSuccess) return cuda_fail(e);
-
-    if (variant == ATTN_VARIANT_AUTO) {
-        attn::KernelInfo ku{};
-        if (auto_takes_umma(head_dim, group, n_q, n_seq, n_kv_head, cap_known ? cap : 0, ds->sm_count,
-                            n_splits, split_len, kv_stable != 0, ku)) {
-            v = attn::kVariantUmma;
-            ki = ku;
-        }
-    }
-    // The cluster-fused form of the tcgen05 kernel (partial and combine in one launch,
-    // 16 splits per (sequence, KV head) merged through distributed shared memory),
-    // on request only: a whole call, one query row, head_dim 128, splits by count with
-    // P = 16 (n_splits 0 or 16), a capacity of at most 16 blocks of 4 tiles, and a
-    // device that holds the 16-block cluster. Variant 0 does not take it: on one box it
-    // was 1 % faster than the plain tcgen05 kernel at context 2048 and 7-13 % slower at
-    // 512 and 128 (capacity 2048), and 20 % slower at the 7b capacity of 8192.
-    if (v == attn::kVariantFused) {
-        const attn::KernelInfo kf = kernel_info(head_dim, group, attn::kVariantFused, n_q > 1);
-        bool ok = kf.available && n_q == 1 && stages == (attn::kStagePartial | attn::kStageCombine) &&
-                  split_len == 0 && (n_splits == 0 || n_splits == kFusedSplits) && cap_known &&
-                  cap <= (int64_t)kFusedSplits * kf.max_chunk;
-        if (!ok) return ATTN_ERR_INVALID_ARG;
-        if (ds->fused_ok < 0) ds->fused_ok = attn::fused_fits_hd128() ? 1 : 0;   // asked once per device
-        if (ds->fused_ok != 1) return ATTN_ERR_UNSUPPORTED;
-        ki = kf;
-    }
-    // by block length with no split count: one split per block of rows of the
-    // capacity (Red Lite dev35 "Change": P = ceil(positions / block))
-    const int64_t P_blk = split_len > 0 && n_splits == 0 ? (cap + split_len - 1) / split_len : 0;
-    if (P_blk > kMaxSplits) return ATTN_ERR_INVALID_ARG;
-    const int P = v == attn::kVariantFused ? kFusedSplits
-                : n_splits > 0 ? n_splits
-                : P_blk > 0    ? (int)P_blk
-                               : heuristic(n_seq, n_kv_head, n_q > 1 ? qgroups : 1,
-                                           cap_known ? cap : 0, ds->sm_count, ki, kv_stable != 0);
-    if (split_len > 0 && (int64_t)P * split_len < cap) return ATTN_ERR_INVALID_ARG;
-    // one tile per block: every split must fit in max_chunk rows at any nkv <= cap
-    if (ki.max_chunk > 0 && (split_len > 0 ? split_len > ki.max_chunk
-                                           : (!cap_known || (int64_t)P * ki.max_chunk < cap)))
-        return ATTN_ERR_INVALID_ARG;
-    // the fused form keeps its partial states on chip: no workspace
-    const size_t need = v == attn::kVariantFused ? 0 : attn_workspace_size(n_seq, n_q * n_head, head_dim, P);
+    st = finish_plan(ds, n_seq, n_head, n_kv_head, head_dim, cap, cap_known, n_splits, split_len, variant,
+                     stages, n_q, pl);
+    if (st != ATTN_OK) return st;
+    const int v = pl.variant, P = pl.n_splits, group = pl.group, qgroups = pl.qgroups;
+    const int kv_dtype = pl.kv_dtype, kv_stable = pl.kv_stable;
+    const size_t need = pl.workspace;
 
     if (!workspace && need > 0) {
         if (stages != (attn::kStagePartial | attn::kStageCombine)) return ATTN_ERR_INVALID_ARG;
@@ -634,6 +679,33 @@ int attn_resolve_variant(int n_seq, int n_q, int n_head, int n_kv_head, int head
 {
     attn::KernelInfo ki{};
     return plan_variant(n_seq, n_q, n_head, n_kv_head, head_dim, cap, sm_count, variant, ki);
+}
+
+attn_status attn_plan_call(int n_seq, int n_q, int n_head, int n_kv_head, int head_dim, int64_t cap,
+                           int n_splits, int split_len, int variant, int *variant_out,
+                           int *n_splits_out, size_t *workspace_bytes_out)
+{
+    CallPlan pl;
+    attn_status st = check_shape(n_seq, n_head, n_kv_head, head_dim, cap, n_splits, split_len, variant,
+                                 n_q, false, pl);
+    if (st != ATTN_OK) return st;
+    if (n_seq == 0) return ATTN_ERR_INVALID_ARG;          // nothing to plan
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        DeviceState *ds = nullptr;
+        e = device_state(dev, &ds);
+        if (e != cudaSuccess) return cuda_fail(e);
+        st = finish_plan(ds, n_seq, n_head, n_kv_head, head_dim, cap, true, n_splits, split_len, variant,
+                         attn::kStagePartial | attn::kStageCombine, n_q, pl);
+    }
+    if (st != ATTN_OK) return st;
+    if (variant_out) *variant_out = pl.variant;
+    if (n_splits_out) *n_splits_out = pl.n_splits;
+    if (workspace_bytes_out) *workspace_bytes_out = pl.workspace;
+    return ATTN_OK;
 }
 
 int attn_split_heuristic(int n_seq, int n_head, int n_kv_head, int head_dim, int64_t cap,

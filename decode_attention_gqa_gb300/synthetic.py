@@ -141,15 +141,24 @@ def fill_kv_seq(w: Workload, layer: int, s: int, k_out: np.ndarray, v_out: np.nd
         v_out[n:] = f
 
 
-def make_kv(w: Workload, layer: int = 0, fill: float = 0.0, kv_dtype: str = "f16"):
+def make_kv(w: Workload, layer: int = 0, fill: float = 0.0, kv_dtype: str = "f16",
+            threads: int = 1):
     """K, V [n_seq, cap, n_kv_head, head_dim]: float16, or bfloat16 bit
-    patterns (uint16) for kv_dtype "bf16"."""
+    patterns (uint16) for kv_dtype "bf16". With threads > 1 the sequences are
+    drawn in parallel; every sequence has its own stream, so the bytes do not
+    depend on the thread count."""
     shape = (w.n_seq, w.cap, w.n_kv_head, w.head_dim)
     dt = np.float16 if kv_dtype == "f16" else np.uint16
     k = np.empty(shape, dtype=dt)
     v = np.empty(shape, dtype=dt)
-    for s in range(w.n_seq):
-        fill_kv_seq(w, layer, s, k[s], v[s], fill, kv_dtype)
+    if threads > 1 and w.n_seq > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max_workers=min(threads, w.n_seq)) as ex:
+            list(ex.map(lambda s: fill_kv_seq(w, layer, s, k[s], v[s], fill, kv_dtype),
+                        range(w.n_seq)))
+    else:
+        for s in range(w.n_seq):
+            fill_kv_seq(w, layer, s, k[s], v[s], fill, kv_dtype)
     return k, v
 
 
@@ -170,6 +179,7 @@ def make_new_rows(w: Workload, layer: int = 0, kv_dtype: str = "f16"):
     return kn, vn
 
 
-def make_layer(w: Workload, layer: int = 0, fill: float = 0.0, kv_dtype: str = "f16") -> dict:
-    k, v = make_kv(w, layer, fill, kv_dtype)
+def make_layer(w: Workload, layer: int = 0, fill: float = 0.0, kv_dtype: str = "f16",
+               threads: int = 1) -> dict:
+    k, v = make_kv(w, layer, fill, kv_dtype, threads)
     return {"q": make_q(w, layer), "k": k, "v": v, "positions": make_positions(w)}

@@ -320,6 +320,26 @@ int attn_resolve_variant(int n_seq, int n_q, int n_head, int n_kv_head, int head
                          int sm_count, int variant);
 
 /*
+ * attn_plan_call -- the whole plan of one call, host-only: for the arguments
+ * of attn_decode_ex (n_q = 1) or attn_decode_multi (n_q rows), including an
+ * explicit n_splits or split_len, returns the partial kernel the call runs
+ * (*variant_out: ATTN_VARIANT_SIMT, _TC, _TCGEN05 or _TCGEN05_CLUSTER), its
+ * split count P (*n_splits_out) and the workspace bytes it needs
+ * (*workspace_bytes_out; 0 for the cluster-fused kernel). A call with these
+ * arguments and a workspace of that size runs exactly this plan. Any output
+ * pointer may be NULL. Uses the current device (its SM count; for
+ * ATTN_VARIANT_TCGEN05_CLUSTER, whether it holds the cluster). Returns the
+ * status the call itself would return for these arguments (ATTN_ERR_INVALID_ARG
+ * also for n_seq == 0, where there is nothing to plan); launches nothing.
+ * The planning rules are the ones the ATTN_VARIANT_* descriptions, n_splits
+ * and split_len above state (splits by count: minfer "10 · R4" §2.2; by block
+ * length: Red Lite dev35 "Change").
+ */
+attn_status attn_plan_call(int n_seq, int n_q, int n_head, int n_kv_head, int head_dim, int64_t cap,
+                           int n_splits, int split_len, int variant, int *variant_out,
+                           int *n_splits_out, size_t *workspace_bytes_out);
+
+/*
  * attn_selftest_bounded_wait -- diagnostic: launch one warp that waits on a
  * shared-memory mbarrier nothing ever arrives on, through the same bounded
  * wait the kernels use, with a limit of limit_ns nanoseconds (1 ..

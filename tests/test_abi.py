@@ -226,6 +226,27 @@ def test_argument_validation_is_synchronous(lib):
     assert lib.attn_decode(16, 16, 16, 16, 16, 2, 8, 2, 128, 0.1, None) == pkg.ATTN_ERR_INVALID_ARG
 
 
+def test_plan_call_checks_its_arguments_before_the_device(lib):
+    """attn_plan_call answers every shape error the call would answer, before it
+    asks for the device (so here, without one, they still come back as such)."""
+    import ctypes
+    v, p, ws = ctypes.c_int(-1), ctypes.c_int(-1), ctypes.c_size_t(7)
+
+    def plan(n_seq=1, n_q=1, n_head=8, n_kv=2, hd=128, cap=64, P=0, blk=0, variant=0):
+        return lib.attn_plan_call(n_seq, n_q, n_head, n_kv, hd, cap, P, blk, variant,
+                                  ctypes.byref(v), ctypes.byref(p), ctypes.byref(ws))
+    assert plan(n_head=8, n_kv=3) == pkg.ATTN_ERR_INVALID_ARG
+    assert plan(cap=0) == pkg.ATTN_ERR_INVALID_ARG
+    assert plan(P=5000) == pkg.ATTN_ERR_INVALID_ARG
+    assert plan(variant=7) == pkg.ATTN_ERR_INVALID_ARG
+    assert plan(n_q=0) == pkg.ATTN_ERR_INVALID_ARG
+    assert plan(n_seq=0) == pkg.ATTN_ERR_INVALID_ARG        # nothing to plan
+    assert plan(hd=96) == pkg.ATTN_ERR_UNSUPPORTED
+    assert plan(n_head=18, n_kv=2) == pkg.ATTN_ERR_UNSUPPORTED
+    assert plan(n_q=2, hd=8) == pkg.ATTN_ERR_UNSUPPORTED
+    assert (v.value, p.value, ws.value) == (-1, -1, 7)       # outputs untouched on error
+
+
 def test_binding_raises_attn_error(lib):
     with pytest.raises(pkg.AttnError) as ei:
         pkg.attn_decode_ex(16, 16, 16, 16, 16, 1, 8, 3, 128, 0.1, 64, stream=0)

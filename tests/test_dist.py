@@ -92,3 +92,13 @@ def test_reference_arm_json_line_contract():
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["config"]["workload"]
+    # the same config dict the GPU arm prints for these arguments
+    import bench
+    old_argv = sys.argv
+    try:
+        sys.argv = ["bench.py", "--workload", "tiny", "--steps", "1", "--warmup", "1"]
+        args = bench.parse_args()
+    finally:
+        sys.argv = old_argv
+    w = bench.workload_for(args)
+    assert d["config"] == bench.config_of(args, w, args.layers or w.layers, 1)
