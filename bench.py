@@ -59,7 +59,8 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
     ap.add_argument("--variant", type=int, default=0,
                     help="0 auto, 1 simt, 2 tensor core (mma.sync), 3 tensor core (tcgen05), "
-                         "4 tcgen05 with the combine in a thread-block cluster")
+                         "4 tcgen05 with the combine in a thread-block cluster, "
+                         "5 one-tile mma.sync")
     ap.add_argument("--splits", type=int, default=0, help="0 = library heuristic")
     ap.add_argument("--kv-dtype", choices=["f16", "bf16"], default="f16")
     ap.add_argument("--append", action="store_true",
@@ -611,11 +612,13 @@ def measure_one(args, rank, world, local):
                 "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                 "traffic": profiled_traffic("%s_ctx%d%s" % (w.name, ctx_end,
                                                             "_nq%d" % n_q if n_q > 1 else "")),
-                "kernel": ("attn_fused_umma (partial and combine in one kernel)" if resolved == 4 else
-                           "attn_split_partial_umma" if resolved == 3 else "attn_split_partial")
+                "kernel": ({4: "attn_fused_umma (partial and combine in one kernel)",
+                            3: "attn_split_partial_umma", 5: "attn_split_partial_tile"}
+                           .get(resolved, "attn_split_partial"))
                           if n_q == 1 else "attn_split_partial + attn_combine",
                 "partial_variant": {1: "simt", 2: "mma.sync", 3: "tcgen05",
-                                    4: "tcgen05, cluster-fused"}.get(resolved, resolved),
+                                    4: "tcgen05, cluster-fused",
+                                    5: "mma.sync, one tile"}.get(resolved, resolved),
                 "bytes_per_launch": m0["launch_bytes"],
                 "us_per_launch": round(m0["partial_us"], 3),
                 "combine_us_per_launch": round(m0["combine_us"], 3)}

@@ -18,7 +18,7 @@ __all__ = [
     "AttnError", "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_WORKSPACE",
     "ATTN_ERR_CUDA", "ATTN_DEVERR_POSITION_CLAMPED", "ATTN_DEVERR_PIPELINE_TIMEOUT",
     "ATTN_VARIANT_AUTO", "ATTN_VARIANT_SIMT", "ATTN_VARIANT_TC", "ATTN_VARIANT_TCGEN05",
-    "ATTN_VARIANT_TCGEN05_CLUSTER", "ATTN_KV_BF16",
+    "ATTN_VARIANT_TCGEN05_CLUSTER", "ATTN_VARIANT_TC_TILE", "ATTN_KV_BF16",
     "ATTN_KV_STABLE",
     "library_path",
     "load",
@@ -37,6 +37,7 @@ ATTN_DEVERR_POSITION_CLAMPED = 0x1
 ATTN_DEVERR_PIPELINE_TIMEOUT = 0x2
 ATTN_VARIANT_AUTO, ATTN_VARIANT_SIMT, ATTN_VARIANT_TC, ATTN_VARIANT_TCGEN05 = 0, 1, 2, 3
 ATTN_VARIANT_TCGEN05_CLUSTER = 4
+ATTN_VARIANT_TC_TILE = 5
 ATTN_KV_BF16 = 0x10
 ATTN_KV_STABLE = 0x20
 
@@ -197,7 +198,7 @@ def decode_attention(q, k_cache, v_cache, positions, scale=None, out=None, n_spl
     if out is None:
         out = torch.empty_like(q)
     if kernel not in (ATTN_VARIANT_AUTO, ATTN_VARIANT_SIMT, ATTN_VARIANT_TC, ATTN_VARIANT_TCGEN05,
-                      ATTN_VARIANT_TCGEN05_CLUSTER):
+                      ATTN_VARIANT_TCGEN05_CLUSTER, ATTN_VARIANT_TC_TILE):
         raise ValueError("kernel must be one of the ATTN_VARIANT_* values")
     variant = kernel | (ATTN_KV_BF16 if k_cache.dtype == torch.bfloat16 else 0) | \
         (ATTN_KV_STABLE if kv_stable else 0)

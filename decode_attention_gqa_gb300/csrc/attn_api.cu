@@ -157,24 +157,19 @@ int heuristic(int n_seq, int n_kv_head, int qgroups, int64_t cap, int sm_count,
     return (int)P;
 }
 
-// ATTN_VARIANT_AUTO takes the tcgen05 kernel for calls bound by latency rather
-// than bandwidth: head_dim 128 or 256; one query row, or several whose
-// (row, head) slots of a KV head fit one 16-slot block; a known capacity;
-// splits of at most one tile each; and one wave of its one-tile blocks (at
-// most 3 x 128 or 2 x 96 rows per SM at full capacity, so a short call). There
-// it was measured as fast or faster at every context of the 7b-like layer, on
-// the head_dim-256 layer and at two query rows; on long caches and batches the
-// mma.sync kernel streams faster, and several query groups per KV head or a
-// second wave of one-tile blocks make the tcgen05 kernel slower. On success
-// `ku` holds its kernel info. The call path and the planning entry points
-// share this rule, so that they report the kernel and split count a call uses.
-bool auto_takes_umma(int head_dim, int group, int n_q, int n_seq, int n_kv_head, int64_t cap,
-                     int sm_count, int n_splits, int split_len, bool kv_stable, attn::KernelInfo &ku)
+// Whether a one-tile kernel (max_chunk rows per block) can take the call:
+// head_dim 128 or 256; one query row, or several whose (row, head) slots of a
+// KV head fit one 16-slot block; a known capacity; splits of at most one tile
+// each; and one wave of its blocks (at full capacity at most blocks_per_sm
+// tiles per SM, so a short call, bound by its chain of dependent steps rather
+// than by bandwidth). On success `ku` holds the kernel's info.
+bool one_tile_fits(int variant, int head_dim, int group, int n_q, int n_seq, int n_kv_head, int64_t cap,
+                   int sm_count, int n_splits, int split_len, bool kv_stable, attn::KernelInfo &ku)
 {
     const int qgroups = (n_q * group + attn::kMqHeadsPerBlock - 1) / attn::kMqHeadsPerBlock;
     if ((head_dim != 128 && head_dim != 256) || (n_q > 1 && qgroups != 1) || cap <= 0 || sm_count <= 0)
         return false;
-    ku = kernel_info(head_dim, group, attn::kVariantUmma, n_q > 1);
+    ku = kernel_info(head_dim, group, variant, n_q > 1);
     if (!ku.available) return false;
     const bool fits = split_len > 0 ? split_len <= ku.max_chunk
                                     : n_splits == 0 || (int64_t)n_splits * ku.max_chunk >= cap;
@@ -182,6 +177,28 @@ bool auto_takes_umma(int head_dim, int group, int n_q, int n_seq, int n_kv_head,
                        : split_len > 0 ? (cap + split_len - 1) / split_len
                                        : heuristic(n_seq, n_kv_head, 1, cap, sm_count, ku, kv_stable);
     return fits && pu * n_kv_head * n_seq <= (int64_t)sm_count * ku.blocks_per_sm;
+}
+
+// ATTN_VARIANT_AUTO for short calls (one_tile_fits): one query row runs the
+// one-tile mma.sync kernel (operands in registers, no tensor-memory round
+// trips; measured faster than the tcgen05 kernel at every context of the
+// 7b-like layer -- 3.7 against 4.5 us per call at context 128, 5.8 against
+// 6.0 at 8192 -- and on the head_dim-256 layer, 6.3 against 7.2 us); several
+// query rows run the tcgen05 kernel (faster there at two rows). Long caches
+// and batches keep the mma.sync streaming kernel (0: no short-call kernel).
+// The call path and the planning entry points share this rule, so that they
+// report the kernel and split count a call uses.
+int auto_short_kernel(int head_dim, int group, int n_q, int n_seq, int n_kv_head, int64_t cap,
+                      int sm_count, int n_splits, int split_len, bool kv_stable, attn::KernelInfo &ku)
+{
+    if (n_q == 1 &&
+        one_tile_fits(attn::kVariantTile, head_dim, group, n_q, n_seq, n_kv_head, cap, sm_count, n_splits,
+                      split_len, kv_stable, ku))
+        return attn::kVariantTile;
+    if (one_tile_fits(attn::kVariantUmma, head_dim, group, n_q, n_seq, n_kv_head, cap, sm_count, n_splits,
+                      split_len, kv_stable, ku))
+        return attn::kVariantUmma;
+    return 0;
 }
 
 // The plan of a call: which partial kernel runs, how many splits, how many
@@ -210,7 +227,8 @@ attn_status check_shape(int n_seq, int n_head, int n_kv_head, int head_dim, int6
     if (cap < 1) return ATTN_ERR_INVALID_ARG;
     if (n_splits < 0 || n_splits > kMaxSplits || split_len < 0) return ATTN_ERR_INVALID_ARG;
     if (variant != ATTN_VARIANT_AUTO && variant != ATTN_VARIANT_SIMT && variant != ATTN_VARIANT_TC &&
-        variant != ATTN_VARIANT_TCGEN05 && variant != ATTN_VARIANT_TCGEN05_CLUSTER)
+        variant != ATTN_VARIANT_TCGEN05 && variant != ATTN_VARIANT_TCGEN05_CLUSTER &&
+        variant != ATTN_VARIANT_TC_TILE)
         return ATTN_ERR_INVALID_ARG;
     if (n_seq > 65535 || n_kv_head > 65535) return ATTN_ERR_INVALID_ARG;   // grid z limit; heads kept as before
     if ((int64_t)n_seq * cap > kMaxFlatRows - 1024) return ATTN_ERR_INVALID_ARG;
@@ -239,9 +257,10 @@ attn_status finish_plan(DeviceState *ds, int n_seq, int n_head, int n_kv_head, i
     variant &= ~(ATTN_KV_BF16 | ATTN_KV_STABLE);
     if (variant == ATTN_VARIANT_AUTO) {
         attn::KernelInfo ku{};
-        if (auto_takes_umma(head_dim, pl.group, n_q, n_seq, n_kv_head, cap_known ? cap : 0, ds->sm_count,
-                            n_splits, split_len, pl.kv_stable != 0, ku)) {
-            pl.variant = attn::kVariantUmma;
+        const int vs = auto_short_kernel(head_dim, pl.group, n_q, n_seq, n_kv_head, cap_known ? cap : 0,
+                                         ds->sm_count, n_splits, split_len, pl.kv_stable != 0, ku);
+        if (vs) {
+            pl.variant = vs;
             pl.ki = ku;
         }
     }
@@ -636,7 +655,8 @@ int plan_variant(int n_seq, int n_q, int n_head, int n_kv_head, int head_dim, in
     const bool kv_stable = (variant & ATTN_KV_STABLE) != 0;
     variant &= ~(ATTN_KV_BF16 | ATTN_KV_STABLE);
     if (variant != ATTN_VARIANT_AUTO && variant != ATTN_VARIANT_SIMT && variant != ATTN_VARIANT_TC &&
-        variant != ATTN_VARIANT_TCGEN05 && variant != ATTN_VARIANT_TCGEN05_CLUSTER)
+        variant != ATTN_VARIANT_TCGEN05 && variant != ATTN_VARIANT_TCGEN05_CLUSTER &&
+        variant != ATTN_VARIANT_TC_TILE)
         return 0;
     if (n_seq <= 0 || n_q < 1 || n_q > 1024 || n_head <= 0 || n_kv_head <= 0 ||
         n_head % n_kv_head != 0)
@@ -651,9 +671,11 @@ int plan_variant(int n_seq, int n_q, int n_head, int n_kv_head, int head_dim, in
     }
     int v = resolve_variant(variant, head_dim, group);
     attn::KernelInfo ku{};
-    if (variant == ATTN_VARIANT_AUTO &&
-        auto_takes_umma(head_dim, group, n_q, n_seq, n_kv_head, cap, sm_count, 0, 0, kv_stable, ku))
-        v = attn::kVariantUmma;
+    if (variant == ATTN_VARIANT_AUTO) {
+        const int vs = auto_short_kernel(head_dim, group, n_q, n_seq, n_kv_head, cap, sm_count, 0, 0,
+                                         kv_stable, ku);
+        if (vs) v = vs;
+    }
     ki = kernel_info(head_dim, group, v, n_q > 1);
     return ki.available ? v : 0;
 }

@@ -282,6 +282,12 @@ __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p)
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(smem_u32(p)));
 }
 
+__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], const void *p)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1]) : "r"(smem_u32(p)));
+}
+
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void *p)
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -338,6 +344,20 @@ __device__ __forceinline__ float ex2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Power-of-two scale for a row of q whose largest magnitude is amax >= 0:
+// sc = 2^s brings amax into [2^14, 2^15) (amax in [2^(e-1), 2^e) gives
+// s = 15 - e, read off the exponent field, no library call), and inv = 2^-s
+// undoes it; both are exact. s is capped at 126 so that both stay normal
+// floats (rows below 2^-113 then scale to less than 2^14, still far from the
+// 16-bit types' limits); a zero row gets sc = inv = 1.
+__device__ __forceinline__ void pow2_scale(float amax, float &sc, float &inv)
+{
+    const int E = (int)((__float_as_uint(amax) >> 23) & 0xFFu);   // biased exponent
+    const int s = min(141 - E, 126);                              // 15 - e with e = E - 126
+    sc = amax > 0.f ? __uint_as_float((unsigned)(127 + s) << 23) : 1.f;
+    inv = amax > 0.f ? __uint_as_float((unsigned)(127 - s) << 23) : 1.f;
 }
 
 __device__ __forceinline__ float warp_max(float x)

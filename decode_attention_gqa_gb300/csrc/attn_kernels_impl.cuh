@@ -8,6 +8,7 @@
 #include "attn_partial.cuh"
 #include "attn_partial_umma.cuh"
 #include "attn_fused_umma.cuh"
+#include "attn_partial_tile.cuh"
 
 namespace attn {
 
@@ -91,6 +92,27 @@ cudaError_t launch_partial_umma(const LaunchRequest &r)
                       C::SMEM_BYTES, r.stream, args);
 }
 
+// The one-tile mma.sync kernel: one block per (KV head, split, sequence), one
+// tile of TileCfg::TILE rows each, one query row.
+template <int HD, int G, typename KV>
+cudaError_t launch_partial_tile(const LaunchRequest &r)
+{
+    using C = TileCfg<HD, G, KV>;
+    alignas(64) CUtensorMap kmap, vmap;
+    const int dt = kv_dtype_code<KV>();
+    cudaError_t e = encode_kv_map4(&kmap, r.k_cache, r.n_seq, r.pa.cap, r.pa.n_kv_head, HD, 64, C::TILE, dt);
+    if (e != cudaSuccess) return e;
+    e = encode_kv_map4(&vmap, r.v_cache, r.n_seq, r.pa.cap, r.pa.n_kv_head, HD, 64, C::TILE, dt);
+    if (e != cudaSuccess) return e;
+    const void *fn = reinterpret_cast<const void *>(&attn_split_partial_tile<C, HD, G, KV>);
+    e = ensure_smem_attr(fn, (int)C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    PartialArgs pa = r.pa;
+    void *args[] = {&kmap, &vmap, &pa};
+    return launch_pdl(fn, dim3(pa.n_kv_head, pa.n_splits, r.n_seq), dim3(C::THREADS), C::SMEM_BYTES,
+                      r.stream, args);
+}
+
 // The cluster-fused tcgen05 kernel: partial and combine in one launch, o written directly.
 template <int HD, int G, typename KV>
 cudaError_t launch_fused_umma(const LaunchRequest &r)
@@ -162,6 +184,9 @@ cudaError_t launch_group(const LaunchRequest &r)
                 else return cudaErrorInvalidValue;
             } else if (r.variant == kVariantUmma) {
                 if constexpr (HD == 128 || HD == 256) e = launch_partial_umma<HD, G, KV>(r);
+                else return cudaErrorInvalidValue;
+            } else if (r.variant == kVariantTile) {
+                if constexpr (HD == 128 || HD == 256) e = launch_partial_tile<HD, G, KV>(r);
                 else return cudaErrorInvalidValue;
             } else if (r.variant == kVariantTc) {
                 e = launch_partial<TcCfg<HD, G, KV>, HD, G, KV>(r);
@@ -240,6 +265,19 @@ KernelInfo kernel_info_for_hd(int group, int variant, bool multi)
             k.granule = C::GRANULE;
             k.stages = 1;
             k.blocks_per_sm = (int)(233472u / (smem + 1024u));
+            k.max_chunk = C::TILE;
+            k.available = true;
+        }
+        return k;
+    }
+    if (variant == kVariantTile) {
+        if constexpr (HD == 128 || HD == 256) {
+            if (multi) return k;
+            using C = TileCfg<HD, 8, __half>;   // the shapes do not depend on the group
+            k.tile_rows = C::TILE;
+            k.granule = C::GRANULE;
+            k.stages = 1;
+            k.blocks_per_sm = (int)(233472u / (C::SMEM_BYTES + 1024u));
             k.max_chunk = C::TILE;
             k.available = true;
         }

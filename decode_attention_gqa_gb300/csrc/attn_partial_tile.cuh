@@ -1,0 +1,318 @@
+// attn_partial_tile.cuh -- the split partial kernel (steps a1-a6) for a split
+// of at most one tile, arranged for the shortest chain of dependent steps:
+// 16x8x16 MMAs with their operands in registers, no tensor memory, no merge
+// of warp states.
+//
+// One block per (split sp, KV head hk, sequence s): the static grid of minfer
+// "10 · R4" §2.2 with the KV head in place of the query head, so the whole
+// group is served from one K/V read (Red Lite dev35 "Change"). The split is
+// one tile of TILE rows (128 at head_dim 128, 96 at 256), so the block sees
+// each row once and its softmax is one pass with a block-wide maximum (§2.1
+// with a single step). Four warps:
+//   1. TMA brings the TILE cache rows that end at hi, K and V on separate
+//      mbarriers (128-byte swizzled; rows in front of the sequence arrive as
+//      zeros, other rows outside the split are earlier rows of the same
+//      sequence: finite data that gets weight 0).
+//   2. q of the group becomes a 16-row Q tile: hi parts of the scaled q in
+//      rows 0-7, lo parts in rows 8-15 (attn_warp_tc.cuh), so q·k keeps about
+//      22 bits of q through 16-bit MMA operands.
+//   3. S: warp w takes tile rows [w·TILE/4, (w+1)·TILE/4): Q (16 x head_dim)
+//      times those K rows, f32 accumulation in registers; slot g's score is C
+//      row g plus C row 8 + g.
+//   4. a4: each head's maximum over the block (warp maxima through shared
+//      memory, one barrier); p = 2^(s - m + OFF), 0 outside the split, stored
+//      as a hi/lo pair into a P tile [16 slots][TILE rows] laid over the Q tile.
+//   5. a5: O = P · V split by head dimension: warp w takes dimensions
+//      [w·head_dim/4, (w+1)·head_dim/4) over all TILE rows, so every warp ends
+//      with the block's final accumulator for its dimensions.
+//   6. a6: each warp writes its dimensions of oc for every head; one thread
+//      per head writes (mx, S), S from the warps' partial sums.
+#pragma once
+
+#include "attn_device.cuh"
+#include "attn_warp_tc.cuh"
+
+namespace attn {
+
+// A fragment (16 x 16) of a 16-row operand stored like the Q tile (rows of
+// COLS 16-bit elements, 128-byte swizzled chunks): k-step kk covers columns
+// [16kk, 16kk + 16); matrices (rows 0-7, low 8 columns), (rows 8-15, low 8),
+// (rows 0-7, high 8), (rows 8-15, high 8).
+template <int COLS>
+__device__ __forceinline__ void ldsm_a16(uint32_t (&a)[4], const uint8_t *base, int kk, int lane)
+{
+    const int i = lane >> 3;
+    const int row = (i & 1) * 8 + (lane & 7);
+    ldsm_x4(a, base + tile_unit_offset<COLS, 16>(row, 2 * kk + (i >> 1)));
+}
+
+template <int HD, int G, typename KV>
+struct TileCfg {
+    static_assert(HD == 128 || HD == 256, "the one-tile kernel is built for head_dim 128 and 256");
+    static constexpr int TILE = HD == 256 ? 96 : 128;   // rows per block
+    static constexpr int MINB = HD == 256 ? 2 : 3;      // resident blocks per SM
+    static constexpr int NW = 4;
+    static constexpr int THREADS = NW * 32;
+    static constexpr int WR = TILE / NW;                // S rows per warp (32 or 24)
+    static constexpr int DW = HD / NW;                  // O dimensions per warp (32 or 64)
+    static constexpr int NS = WR / 8;                   // S n-tiles (8 rows each) per warp (4 or 3)
+    static constexpr int KS = HD / 16;                  // S k-steps
+    static constexpr int NO = DW / 8;                   // O n-tiles (8 dimensions each) per warp
+    static constexpr int KO = TILE / 16;                // O k-steps
+    static constexpr int NCH = HD / 64;                 // 128-byte column chunks per row
+    static constexpr int GRANULE = TILE;                // count-mode chunks are whole tiles
+    static constexpr bool Q_REGS = KS <= 8;             // Q fragments held in registers
+    using QStage = TcWarp<HD, G, NW, KV>;
+    static constexpr uint32_t TILE_BYTES = (uint32_t)TILE * HD * 2;
+    static constexpr uint32_t OFF_K = 0;
+    static constexpr uint32_t OFF_V = TILE_BYTES;
+    static constexpr uint32_t OFF_Q = 2 * TILE_BYTES;   // Q tile, then per-head scales
+    static constexpr uint32_t OFF_P = OFF_Q;            // P tile over the Q tile once S is done
+    // P tile: 16 rows of TILE elements in 128-byte swizzled chunks of 64
+    static constexpr uint32_t P_BYTES = 16u * ((TILE + 63) / 64 * 64) * 2;
+    static constexpr uint32_t OFF_RED = OFF_Q + (QStage::EXTRA_BYTES + 15) / 16 * 16;   // [2][NW][8] floats
+    static constexpr uint32_t OFF_BAR = OFF_RED + 2 * NW * 8 * 4;                       // 2 mbarriers, flags
+    static constexpr uint32_t SMEM_BYTES = OFF_BAR + 2 * 8 + 16 + 1024;                 // + alignment slack
+    static constexpr float OFF = 7.f;                   // p headroom: p <= 2^OFF
+    static_assert(P_BYTES <= QStage::QT_BYTES, "the P tile must not reach the per-head scales");
+    static_assert(TILE % 32 == 0 && WR % 8 == 0 && DW % 16 == 0, "fragment shapes");
+    static_assert((TILE * 128) % 1024 == 0, "swizzled chunks stay 1024-aligned");
+    static_assert(MINB * (SMEM_BYTES + 1024) <= 233472u, "resident blocks per SM");
+};
+
+template <class Cfg, int HD, int G, typename KV>
+__global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
+attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                        const PartialArgs a)
+{
+    constexpr int TILE = Cfg::TILE, NS = Cfg::NS, KS = Cfg::KS, NO = Cfg::NO, KO = Cfg::KO;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + Cfg::OFF_BAR);    // [0] K landed, [1] V landed
+    volatile int *flags = reinterpret_cast<volatile int *>(bar + 2);     // [0] abort
+    float *red_m = reinterpret_cast<float *>(smem + Cfg::OFF_RED);      // [NW][8] warp maxima
+    float *red_l = red_m + Cfg::NW * 8;                                 // [NW][8] warp sums
+
+    const int hk = blockIdx.x, sp = blockIdx.y, s = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int P = a.n_splits;
+    const size_t heads = (size_t)a.n_head;
+
+    // Dependencies as in attn_partial.cuh: with kv_stable the positions read
+    // and the tile copies go ahead of the grid dependency, q waits for it.
+    const bool stable = a.kv_stable != 0;
+    if (tid == 32)
+        prefetch_l2(a.q + ((size_t)s * a.n_head + (size_t)hk * G) * HD, (uint32_t)(G * HD * sizeof(float)));
+    if (!stable) pdl_wait();
+    pdl_launch_dependents();
+
+    // a1: rows attended and this split's rows; an empty split leaves at once
+    bool pos_ok;
+    const int64_t nkv = rows_attended(a, s, sp == 0 && hk == 0 && tid == 0, &pos_ok);
+    int64_t lo, hi;
+    split_range(nkv, sp, P, a.split_len, Cfg::GRANULE, lo, hi);
+    if (lo >= hi) {
+        if (stable) pdl_wait();               // the workspace may still be read by the previous grid
+        if (tid < G) a.ws_ml[((size_t)s * heads + (size_t)hk * G + tid) * P + sp] = make_float2(-INFINITY, 0.f);
+        return;
+    }
+    const int n = (int)(hi - lo);             // 1..TILE rows: the tile's last n rows
+    const int row_first = (int)(hi - TILE);   // negative near the sequence start: zero rows
+
+    if (tid == 0) {
+        mbar_init(bar + 0, 1);
+        mbar_init(bar + 1, 1);
+        flags[0] = 0;
+        fence_barrier_init();
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+        mbar_arrive_expect_tx(bar + 0, Cfg::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < Cfg::NCH; ++c)
+            tma_load_4d(smem + Cfg::OFF_K + c * (Cfg::TILE_BYTES / Cfg::NCH), &kmap, bar + 0, c * 64, hk, row_first, s);
+        mbar_arrive_expect_tx(bar + 1, Cfg::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < Cfg::NCH; ++c)
+            tma_load_4d(smem + Cfg::OFF_V + c * (Cfg::TILE_BYTES / Cfg::NCH), &vmap, bar + 1, c * 64, hk, row_first, s);
+    }
+
+    // a2, while the tile is in flight: the Q tile and the per-head scales
+    if (stable) pdl_wait();
+    Cfg::QStage::template prepare<Cfg::THREADS>(smem + Cfg::OFF_Q, a, s, hk, 0, tid);
+    // Fused append: the split ending at nkv holds the new row nkv - 1 as the
+    // tile's last row, which is in warp 3's S rows; warp 3 fetches it now (one
+    // 16-byte unit per lane) and writes it into both tiles and the cache once
+    // they have landed, before the barrier that precedes any read of V.
+    constexpr int NU = HD / 8;                    // 16-byte units per row
+    constexpr int NJ = 2 * NU / 32;               // units of the new K and V rows per lane
+    static_assert(2 * NU % 32 == 0, "whole units per lane");
+    const bool appending = a.k_new != nullptr && pos_ok && hi == nkv && warp == Cfg::NW - 1;
+    uint4 newrow[NJ];
+    if (appending) {
+        const size_t src = ((size_t)s * a.n_kv_head + hk) * HD;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            const int i = lane + 32 * j;
+            newrow[j] = ld_dep(reinterpret_cast<const uint4 *>((i < NU ? a.k_new : a.v_new) + src) + (i % NU));
+        }
+    }
+    __syncthreads();
+
+    const uint8_t *qt = smem + Cfg::OFF_Q;
+    const float inv = reinterpret_cast<const float *>(qt + Cfg::QStage::QT_BYTES)[lane >> 2];
+    const int i8 = lane >> 3, g = lane >> 2, t = lane & 3;
+    bool ok = mbar_wait_bounded(bar + 0, 0);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok && appending) {
+        const bool vl = __all_sync(0xffffffffu, mbar_wait_bounded(bar + 1, 0));
+        if (vl) {
+            const size_t dst = ((size_t)((int64_t)s * a.cap + nkv - 1) * a.n_kv_head + hk) * HD;
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+                const int i = lane + 32 * j;
+                uint8_t *tile = smem + (i < NU ? Cfg::OFF_K : Cfg::OFF_V);
+                *reinterpret_cast<uint4 *>(tile + tile_unit_offset<HD, TILE>(TILE - 1, i % NU)) = newrow[j];
+                reinterpret_cast<uint4 *>((i < NU ? a.k_w : a.v_w) + dst)[i % NU] = newrow[j];
+            }
+            __syncwarp();
+        }
+        ok = vl;
+    }
+    if (!ok && lane == 0) { flags[0] = 1; atomicOr(a.err, kErrPipelineTimeout); }
+
+    // ---- a3: S for this warp's rows r0 .. r0 + WR - 1 ----
+    const int r0 = warp * Cfg::WR;
+    float sc[NS][2];                          // head g, rows r0 + 8j + 2t + {0, 1}
+    {
+        float c[2][NS][4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int j = 0; j < NS; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) c[e][j][i] = 0.f;
+        if (ok) {
+            uint32_t qa[Cfg::Q_REGS ? KS : 1][4];
+            if constexpr (Cfg::Q_REGS) {
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk) ldsm_a16<HD>(qa[kk], qt, kk, lane);
+            }
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                uint32_t aq[4];
+                if constexpr (Cfg::Q_REGS) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) aq[i] = qa[kk][i];
+                } else {
+                    ldsm_a16<HD>(aq, qt, kk, lane);
+                }
+#pragma unroll
+                for (int j = 0; j + 1 < NS; j += 2) {
+                    // (rows 8j..8j+7, dims lo 8), (.., hi 8), (rows 8j+8.., lo 8), (.., hi 8)
+                    uint32_t b[4];
+                    const int krow = r0 + 8 * j + (i8 >> 1) * 8 + (lane & 7);
+                    ldsm_x4(b, smem + Cfg::OFF_K + tile_unit_offset<HD, TILE>(krow, 2 * kk + (i8 & 1)));
+                    mma_16816<KV>(c[kk & 1][j], aq, b[0], b[1]);
+                    mma_16816<KV>(c[kk & 1][j + 1], aq, b[2], b[3]);
+                }
+                if constexpr (NS % 2 == 1) {
+                    // the last 8 rows alone: (dims lo 8), (dims hi 8); lanes 16-31 repeat the addresses
+                    uint32_t b[2];
+                    const int krow = r0 + 8 * (NS - 1) + (lane & 7);
+                    ldsm_x2(b, smem + Cfg::OFF_K + tile_unit_offset<HD, TILE>(krow, 2 * kk + (i8 & 1)));
+                    mma_16816<KV>(c[kk & 1][NS - 1], aq, b[0], b[1]);
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < NS; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int r = r0 + 8 * j + 2 * t + e;   // tile row
+                const float v = ((c[0][j][e] + c[1][j][e]) + (c[0][j][2 + e] + c[1][j][2 + e])) * inv;
+                sc[j][e] = r >= TILE - n ? v : -INFINITY;
+            }
+    }
+    // ---- a4: each head's maximum over the block ----
+    {
+        float m = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < NS; ++j) m = fmaxf(m, fmaxf(sc[j][0], sc[j][1]));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        if (t == 0) red_m[warp * 8 + g] = m;
+    }
+    __syncthreads();                          // the maxima are in; S is done, so Q is dead
+    const float M = fmaxf(fmaxf(red_m[g], red_m[8 + g]), fmaxf(red_m[16 + g], red_m[24 + g]));
+    const float base = M - Cfg::OFF;          // M is finite: the split has rows in every block
+    {
+        float lsum = 0.f;
+        uint8_t *pt = smem + Cfg::OFF_P;
+#pragma unroll
+        for (int j = 0; j < NS; ++j) {
+            const float p0 = ex2(sc[j][0] - base), p1 = ex2(sc[j][1] - base);   // 0 at -inf
+            lsum += p0 + p1;
+            const uint32_t hw = float2_to_kv2<KV>(p0, p1);
+            const float2 f = kv2_to_float2<KV>(hw);
+            const uint32_t lw = float2_to_kv2<KV>(p0 - f.x, p1 - f.y);
+            // P[slot][row]: row pair (r, r + 1) of unit r / 8, 4 bytes apart per t
+            const int r = r0 + 8 * j;
+            *reinterpret_cast<uint32_t *>(pt + tile_unit_offset<TILE, 16>(g, r >> 3) + 4 * t) = hw;
+            *reinterpret_cast<uint32_t *>(pt + tile_unit_offset<TILE, 16>(8 + g, r >> 3) + 4 * t) = lw;
+        }
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+        if (t == 0) red_l[warp * 8 + g] = lsum;
+    }
+    bool vok = ok;
+    if (vok && !appending) vok = __all_sync(0xffffffffu, mbar_wait_bounded(bar + 1, 0));
+    if (ok && !vok && lane == 0) { flags[0] = 1; atomicOr(a.err, kErrPipelineTimeout); }
+    __syncthreads();                          // P and the sums are in; every V wait is done
+    // ---- a5: O = P · V for this warp's dimensions d0 .. d0 + DW - 1 ----
+    const int d0 = warp * Cfg::DW;
+    const bool abort = flags[0] != 0;         // the same for every thread past the barrier
+    if (!abort) {
+        float o[2][NO][4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int j = 0; j < NO; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) o[e][j][i] = 0.f;
+        const uint8_t *pt = smem + Cfg::OFF_P;
+#pragma unroll
+        for (int kk = 0; kk < KO; ++kk) {
+            uint32_t ap[4];                   // P rows (slots) x tile rows 16kk .. 16kk + 15
+            ldsm_a16<TILE>(ap, pt, kk, lane);
+            const int vrow = 16 * kk + (i8 & 1) * 8 + (lane & 7);
+#pragma unroll
+            for (int j = 0; j < NO; j += 2) {
+                // (rows 0-7, dims j), (rows 8-15, dims j), (0-7, j+1), (8-15, j+1)
+                uint32_t b[4];
+                ldsm_x4_trans(b, smem + Cfg::OFF_V + tile_unit_offset<HD, TILE>(vrow, (d0 >> 3) + j + (i8 >> 1)));
+                mma_16816<KV>(o[kk & 1][j], ap, b[0], b[1]);
+                mma_16816<KV>(o[kk & 1][j + 1], ap, b[2], b[3]);
+            }
+        }
+        // ---- a6: oc of every head for these dimensions; (mx, S) per head ----
+        if (g < G) {
+            float *dst = a.ws_o + (((size_t)s * heads + (size_t)hk * G + g) * P + sp) * HD + d0 + 2 * t;
+#pragma unroll
+            for (int j = 0; j < NO; ++j)
+                *reinterpret_cast<float2 *>(dst + 8 * j) =
+                    make_float2((o[0][j][0] + o[1][j][0]) + (o[0][j][2] + o[1][j][2]),
+                                (o[0][j][1] + o[1][j][1]) + (o[0][j][3] + o[1][j][3]));
+        }
+        if (warp == 0 && t == 0 && g < G) {
+            const float L = (red_l[g] + red_l[8 + g]) + (red_l[16 + g] + red_l[24 + g]);
+            a.ws_ml[((size_t)s * heads + (size_t)hk * G + g) * P + sp] = make_float2(base, L);
+        }
+    } else if (tid == 0) {
+        // nothing may still be writing shared memory when the block exits:
+        // wait (bounded) for both copies before leaving
+        (void)mbar_wait_bounded(bar + 0, 0);
+        (void)mbar_wait_bounded(bar + 1, 0);
+    }
+}
+
+} // namespace attn

@@ -113,13 +113,9 @@ struct TcWarp {
 #pragma unroll
             for (int i = 0; i < PER; ++i) amax = fmaxf(amax, fabsf(x[it][i]));
             amax = warp_max(amax);
-            int e = 0;
-            float sc = 1.f;
-            if (amax > 0.f) {
-                (void)frexpf(amax, &e);                   // amax in [2^(e-1), 2^e)
-                sc = ldexpf(1.f, 15 - e);                 // scaled max in [2^14, 2^15)
-            }
-            if (lane == 0) inv[g] = amax > 0.f ? ldexpf(1.f, e - 15) : 1.f;
+            float sc, ig;                                 // scaled max in [2^14, 2^15)
+            pow2_scale(amax, sc, ig);
+            if (lane == 0) inv[g] = ig;
             // hi = T(v), lo = T(v - hi) element by element, packed in pairs; the
             // lane's PER elements share one 16-byte unit of the swizzled tile
             uint32_t hw[PER / 2], lw[PER / 2];

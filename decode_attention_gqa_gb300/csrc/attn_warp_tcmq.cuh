@@ -104,14 +104,10 @@ struct TcWarpMQ {
 #pragma unroll
             for (int k = 0; k < PER; ++k) amax = fmaxf(amax, fabsf(x[it][k]));
             amax = warp_max(amax);
-            int e = 0;
-            float sc = 1.f;
-            if (amax > 0.f) {
-                (void)frexpf(amax, &e);
-                sc = ldexpf(1.f, 15 - e);
-            }
+            float sc, ig;
+            pow2_scale(amax, sc, ig);
             if (lane == 0) {
-                inv[i] = amax > 0.f ? ldexpf(1.f, e - 15) : 1.f;
+                inv[i] = ig;
                 const int hp = slot_head(a, hk, qg, i);
                 qr[i] = hp >= 0 ? div_group(a, qg * QH + i) : -1;
             }

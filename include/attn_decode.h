@@ -95,6 +95,15 @@ typedef enum {
                                  does not take it (measured no faster than the tcgen05 kernel
                                  with its separate combine). */
 
+#define ATTN_VARIANT_TC_TILE 5 /* tensor-core partial kernel for splits of one tile, built for the
+                                 shortest chain of dependent steps: 16x8x16 MMAs with operands in
+                                 registers (q and p as hi + lo pairs as above), S split by rows
+                                 over four warps, one block-wide maximum, O = P·V split by head
+                                 dimension over the warps (no merge of warp states). One tile of
+                                 T rows per block (T = 128; 64 at head_dim 256); head_dim 128 or
+                                 256, one query row (ATTN_ERR_UNSUPPORTED otherwise). Every split
+                                 must fit one tile, as for ATTN_VARIANT_TCGEN05. */
+
 /* Cache element type, OR'd into the variant argument: without it K and V are
    IEEE binary16 (f16); with it they are bfloat16 (1 sign, 8 exponent, 7
    fraction bits). k_new / v_new of attn_decode_append use the same type. */

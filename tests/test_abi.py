@@ -150,15 +150,17 @@ def test_resolved_variant(lib):
     r = pkg.attn_resolve_variant
     S, B = pkg.ATTN_KV_STABLE, pkg.ATTN_KV_BF16
     T5, TC, SI = pkg.ATTN_VARIANT_TCGEN05, pkg.ATTN_VARIANT_TC, pkg.ATTN_VARIANT_SIMT
-    # variant 0: the tcgen05 kernel for a short head_dim-128 call of one query row
-    assert r(1, 1, 28, 4, 128, 8192, 152, 0) == T5
-    assert r(1, 1, 28, 4, 128, 8192, 152, S | B) == T5
-    assert r(1, 1, 8, 2, 128, 40, 152, 0) == T5
+    VT = pkg.ATTN_VARIANT_TC_TILE
+    # variant 0: the one-tile mma.sync kernel for a short call of one query row;
+    # the tcgen05 kernel for several query rows
+    assert r(1, 1, 28, 4, 128, 8192, 152, 0) == VT
+    assert r(1, 1, 28, 4, 128, 8192, 152, S | B) == VT
+    assert r(1, 1, 8, 2, 128, 40, 152, 0) == VT
     # the cluster-fused form only on request
     assert r(1, 1, 28, 4, 128, 2048, 152, pkg.ATTN_VARIANT_TCGEN05_CLUSTER) == \
         pkg.ATTN_VARIANT_TCGEN05_CLUSTER
     assert r(1, 1, 16, 2, 256, 2048, 152, pkg.ATTN_VARIANT_TCGEN05_CLUSTER) == 0
-    assert r(1, 1, 16, 2, 256, 8400, 152, 0) == T5
+    assert r(1, 1, 16, 2, 256, 8400, 152, 0) == VT
     # ... the mma.sync kernel for long caches, batches, several query rows, head_dim
     # 64 and an unknown capacity; CUDA cores for head_dim 8
     assert r(1, 1, 64, 8, 128, 131072, 152, 0) == TC
@@ -175,12 +177,12 @@ def test_resolved_variant(lib):
     assert r(1, 1, 4, 2, 8, 64, 152, 0) == SI
     # the boundary: one wave of one-tile blocks, 3 per SM at head_dim 128 (4 x 114 = 456
     # blocks of 128 rows), 2 at head_dim 256 (2 x 152 = 304 blocks of 96 rows)
-    assert r(1, 1, 28, 4, 128, 114 * 128, 152, 0) == T5
+    assert r(1, 1, 28, 4, 128, 114 * 128, 152, 0) == VT
     assert r(1, 1, 28, 4, 128, 114 * 128 + 1, 152, 0) == TC
     assert r(1, 1, 28, 4, 128, 114 * 128 + 1, 152, S) == TC
-    assert r(1, 1, 16, 2, 256, 152 * 96, 152, 0) == T5
+    assert r(1, 1, 16, 2, 256, 152 * 96, 152, 0) == VT
     assert r(1, 1, 16, 2, 256, 152 * 96 + 1, 152, 0) == TC
-    assert r(2, 1, 28, 4, 128, 57 * 128, 152, 0) == T5            # 2 sequences x 4 x 57
+    assert r(2, 1, 28, 4, 128, 57 * 128, 152, 0) == VT            # 2 sequences x 4 x 57
     assert r(2, 1, 28, 4, 128, 57 * 128 + 1, 152, 0) == TC
     # explicit variants are kept; tcgen05 is built for head_dim 128 and one query row
     assert r(1, 1, 28, 4, 128, 8192, 152, SI) == SI
@@ -188,6 +190,9 @@ def test_resolved_variant(lib):
     assert r(1, 1, 64, 8, 128, 131072, 152, T5) == T5
     assert r(1, 1, 8, 2, 64, 1024, 152, T5) == 0
     assert r(1, 2, 8, 2, 128, 1024, 152, T5) == T5                         # several query rows too
+    assert r(1, 1, 28, 4, 256, 8192, 152, VT) == VT                        # explicit one-tile kernel
+    assert r(1, 2, 8, 2, 128, 1024, 152, VT) == 0                          # one query row only
+    assert r(1, 1, 8, 2, 64, 1024, 152, VT) == 0
     assert r(1, 1, 28, 5, 128, 8192, 152, 0) == 0
 
 
@@ -321,11 +326,13 @@ def test_decode_attention_checks_its_tensors_before_any_call():
 
 
 def test_tcgen05_choice_keeps_its_limits(lib):
-    """Wherever variant 0 names the tcgen05 kernel, the planned splits cover the
-    capacity one tile each and fit one wave of its blocks; several query rows
-    only when a KV head's pairs fit one 16-slot block. Seeded random shapes."""
+    """Wherever variant 0 names a one-tile kernel (tcgen05, or the one-tile
+    mma.sync kernel), the planned splits cover the capacity one tile each and
+    fit one wave of its blocks; the mma.sync form only for one query row;
+    several query rows only when a KV head's pairs fit one 16-slot block.
+    Seeded random shapes."""
     rng = np.random.default_rng(12)
-    T5 = pkg.ATTN_VARIANT_TCGEN05
+    T5, VT = pkg.ATTN_VARIANT_TCGEN05, pkg.ATTN_VARIANT_TC_TILE
     tile = {128: 128, 256: 96}
     per_sm = {(128, False): 3, (256, False): 2, (128, True): 2, (256, True): 1}
     seen = set()
@@ -340,8 +347,10 @@ def test_tcgen05_choice_keeps_its_limits(lib):
         flags = int(rng.choice([0, pkg.ATTN_KV_STABLE]))
         v = pkg.attn_resolve_variant(n_seq, n_q, G * n_kv, n_kv, hd, cap, sms, flags)
         P = pkg.attn_split_heuristic_ex(n_seq, n_q, G * n_kv, n_kv, hd, cap, sms, flags)
-        assert v in (pkg.ATTN_VARIANT_TC, T5) and P > 0
-        if v != T5:
+        assert v in (pkg.ATTN_VARIANT_TC, T5, VT) and P > 0
+        if v == VT:
+            assert n_q == 1
+        elif v != T5:
             continue
         seen.add((hd, n_q > 1))
         assert hd in (128, 256)

@@ -312,7 +312,7 @@ def test_decode_attention_convenience_call(pkg, kv):
     assert_close(outm.cpu().numpy(), refm, "decode_attention %s, 3 rows" % kv)
     # each kernel by name
     for kernel in (pkg.ATTN_VARIANT_SIMT, pkg.ATTN_VARIANT_TC, pkg.ATTN_VARIANT_TCGEN05,
-                   pkg.ATTN_VARIANT_TCGEN05_CLUSTER):
+                   pkg.ATTN_VARIANT_TCGEN05_CLUSTER, pkg.ATTN_VARIANT_TC_TILE):
         outk = pkg.decode_attention(dev["q"], dev["k"], dev["v"], dev["positions"], kernel=kernel)
         torch.cuda.synchronize()
         assert_close(outk.cpu().numpy(), ref, "decode_attention %s kernel %d" % (kv, kernel))

@@ -59,7 +59,7 @@ def test_call_runs_the_planned_kernel_and_split_count(pkg, shape, stable):
     sms = _sms()
     P = pkg.attn_split_heuristic_ex(n_seq, n_q, n_head, n_kv, hd, cap, sms, flags)
     v = pkg.attn_resolve_variant(n_seq, n_q, n_head, n_kv, hd, cap, sms, flags)
-    assert P > 0 and v in (pkg.ATTN_VARIANT_TC, pkg.ATTN_VARIANT_TCGEN05)
+    assert P > 0 and v in (pkg.ATTN_VARIANT_TC, pkg.ATTN_VARIANT_TCGEN05, pkg.ATTN_VARIANT_TC_TILE)
     ctx = tuple(cap - 3 - 17 * s for s in range(n_seq))
     case = make_case(7100 + cap % 97 + n_q, n_seq, n_head, n_kv, hd, cap, ctx)
     scale = 1 / math.sqrt(hd)
@@ -149,7 +149,7 @@ def test_plan_call_is_the_call(pkg, call):
             pytest.skip("this device cannot hold the fused kernel's cluster")
         raise
     assert v in (pkg.ATTN_VARIANT_SIMT, pkg.ATTN_VARIANT_TC, pkg.ATTN_VARIANT_TCGEN05,
-                 pkg.ATTN_VARIANT_TCGEN05_CLUSTER)
+                 pkg.ATTN_VARIANT_TCGEN05_CLUSTER, pkg.ATTN_VARIANT_TC_TILE)
     want_ws = 0 if v == pkg.ATTN_VARIANT_TCGEN05_CLUSTER else pkg.attn_workspace_size(
         n_seq, n_q * n_head, hd, P)
     assert ws_bytes == want_ws

@@ -1,0 +1,239 @@
+"""GPU parity of the one-tile mma.sync partial kernel (ATTN_VARIANT_TC_TILE:
+one tile per block -- 128 rows at head_dim 128, 96 at 256 -- S split by rows
+over four warps, one block-wide maximum, O = P·V split by head dimension)
+against the double-precision oracle, element by element, through the C ABI.
+
+Covers every group size, both split rules at the chunk boundaries, tiles that
+start before the sequence's first row (zero rows from the 4-D tensor map) in a
+ragged batch whose unread rows are NaN, large score spread and a planted
+dominant row, extreme query magnitudes, bfloat16, the fused append,
+early-start chains under graph replay, the 7b and long workloads at full size,
+and the argument checks that keep every split within one tile."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from decode_attention_gqa_gb300 import synthetic as syn
+from harness import assert_close, make_case, run_decode, to_device
+from test_append import _host_after_append, _new_rows, _run_append
+from test_kv_stable import _chain
+
+pytestmark = pytest.mark.gpu
+
+VT = 5                       # ATTN_VARIANT_TC_TILE
+TILE = {128: 128, 256: 96}   # rows per block
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import decode_attention_gqa_gb300 as p
+    from decode_attention_gqa_gb300 import build
+    build.build()
+    p.load()
+    assert p.ATTN_VARIANT_TC_TILE == VT
+    return p
+
+
+def _oracle(case, n_head, n_kv, hd, cap, scale, kv_dtype="f16"):
+    return oracle.attn_decode(case["q"], case["k"], case["v"], case["positions"], n_head, n_kv,
+                              hd, cap, scale, n_threads=8, kv_dtype=kv_dtype)
+
+
+def _check(pkg, case, n_head, n_kv, cap, what, variant=VT, kv_dtype="f16", hd=128, **kw):
+    scale = 1 / math.sqrt(hd)
+    out = run_decode(pkg, to_device(case), n_head, n_kv, hd, cap, scale, variant=variant, **kw)
+    return assert_close(out.cpu().numpy(), _oracle(case, n_head, n_kv, hd, cap, scale, kv_dtype),
+                        what)
+
+
+@pytest.mark.parametrize("hd", [128, 256])
+def test_every_group_size(pkg, hd):
+    for G in range(1, 9):
+        n_kv = 2
+        case = make_case(5100 + G + hd, 1, G * n_kv, n_kv, hd, 700, (613,))
+        # P * tile >= 700
+        for P in ((0, 6, 11) if hd == 128 else (0, 8, 11)):
+            _check(pkg, case, G * n_kv, n_kv, 700, "hd%d G%d P=%d" % (hd, G, P), hd=hd, n_splits=P)
+
+
+@pytest.mark.parametrize("hd", [128, 256])
+def test_count_split_boundaries(pkg, hd):
+    import torch
+    n_head, n_kv, cap = 28, 4, 1024
+    P = -(-cap // TILE[hd])                           # chunks of (up to) one tile at full capacity
+    base = make_case(5200 + hd, 1, n_head, n_kv, hd, cap, (cap,))
+    scale = 1 / math.sqrt(hd)
+    dev = to_device(base)
+    for nkv in sorted({0, 1, 2, 15, 16, 17, 7, 8, 9, 63, 64, 65, 127, 128, 129, 255, 256, 257,
+                       500, 1000, cap - 1, cap}):
+        dev["positions"].fill_(nkv - 1)
+        out = run_decode(pkg, dev, n_head, n_kv, hd, cap, scale, n_splits=P, variant=VT)
+        ref = _oracle(dict(base, positions=np.array([nkv - 1], np.int32)), n_head, n_kv, hd, cap,
+                      scale)
+        assert_close(out.cpu().numpy(), ref, "hd%d count split nkv=%d" % (hd, nkv))
+        if nkv == 0:
+            assert torch.count_nonzero(out).item() == 0
+
+
+@pytest.mark.parametrize("hd", [128, 256])
+def test_block_split_boundaries(pkg, hd):
+    n_head, n_kv, cap = 16, 2, 1100
+    base = make_case(5300 + hd, 1, n_head, n_kv, hd, cap, (cap,))
+    scale = 1 / math.sqrt(hd)
+    dev = to_device(base)
+    for blk in ((16, 32, 100, 128) if hd == 128 else (16, 32, 64, 96)):
+        P = -(-cap // blk)
+        for nkv in (1, blk - 1, blk, blk + 1, 3 * blk + 7, cap - 1, cap):
+            dev["positions"].fill_(nkv - 1)
+            out = run_decode(pkg, dev, n_head, n_kv, hd, cap, scale, n_splits=P, split_len=blk,
+                             variant=VT)
+            ref = _oracle(dict(base, positions=np.array([nkv - 1], np.int32)), n_head, n_kv, hd,
+                          cap, scale)
+            assert_close(out.cpu().numpy(), ref, "hd%d block %d nkv=%d" % (hd, blk, nkv))
+
+
+def test_split_count_invariance_and_agreement_with_the_other_kernels(pkg):
+    n_head, n_kv, cap = 32, 8, 3000
+    case = make_case(5400, 2, n_head, n_kv, 128, cap, (3000, 1234))
+    ref = _oracle(case, n_head, n_kv, 128, cap, 1 / math.sqrt(128))
+    for P in (24, 25, 32, 64, 188, 400):
+        _check(pkg, case, n_head, n_kv, cap, "P=%d" % P, n_splits=P)
+    for other in (2, 3):
+        got = run_decode(pkg, to_device(case), n_head, n_kv, 128, cap, 1 / math.sqrt(128),
+                         n_splits=0, variant=other).cpu().numpy()
+        assert_close(got, ref, "variant %d, same inputs" % other)
+
+
+@pytest.mark.parametrize("hd", [128, 256])
+def test_ragged_batch_with_nan_beyond_every_sequence(pkg, hd):
+    # sequences after the first start their first tile inside the previous
+    # sequence's rows in a flat view; those rows are NaN here
+    n_head, n_kv, cap = 32, 8, 900
+    ctx = (1, 900, 0, 17, 450, 899, 64, 333, 128, 129)
+    case = make_case(5500 + hd, len(ctx), n_head, n_kv, hd, cap, ctx, fill=np.nan)
+    for P in ((0, 8, 57) if hd == 128 else (0, 15, 57)):      # P * tile >= 900
+        _check(pkg, case, n_head, n_kv, cap, "hd%d ragged P=%d" % (hd, P), hd=hd, n_splits=P)
+
+
+def test_large_score_spread_and_single_row(pkg):
+    n_head, n_kv, cap = 64, 8, 2000
+    case = make_case(5600, 1, n_head, n_kv, 128, cap, (1999,), k_scale=8.0)
+    case["k"][0, 1234] = (case["k"][0, 1234].astype(np.float32) * 4).astype(np.float16)
+    _check(pkg, case, n_head, n_kv, cap, "K x8, planted row")
+    one = make_case(5601, 1, 28, 4, 128, 256, (1,), fill=np.nan)
+    dev = to_device(one)
+    out = run_decode(pkg, dev, 28, 4, 128, 256, 1 / math.sqrt(128), variant=VT).cpu().numpy()
+    want = one["v"][0, 0].astype(np.float32)          # [n_kv, hd]
+    np.testing.assert_allclose(out[0].reshape(4, 7, 128), np.repeat(want[:, None, :], 7, 1),
+                               rtol=1e-6, atol=1e-6)
+
+
+@pytest.mark.parametrize("hd", [128, 256])
+def test_extreme_query_magnitudes(pkg, hd):
+    # per-head power-of-two scaling of q: no f16 overflow at |q| ~ 1e6 and no
+    # loss of the lo part at |q| ~ 1e-6
+    n_head, n_kv, cap = 16, 2, 600
+    case = make_case(5650 + hd, 1, n_head, n_kv, hd, cap, (555,))
+    case["q"][0, :4] *= np.float32(1e6)
+    case["q"][0, 4:8] *= np.float32(1e-6)
+    case["q"][0, 8] = 0.0
+    _check(pkg, case, n_head, n_kv, cap, "hd%d extreme q" % hd, hd=hd)
+
+
+@pytest.mark.parametrize("hd", [128, 256])
+def test_bfloat16_cache(pkg, hd):
+    n_head, n_kv, cap = 28, 4, 1500
+    case = make_case(5700 + hd, 2, n_head, n_kv, hd, cap, (1500, 700), kv_dtype="bf16")
+    _check(pkg, case, n_head, n_kv, cap, "hd%d bf16" % hd, variant=VT | pkg.ATTN_KV_BF16,
+           kv_dtype="bf16", hd=hd)
+
+
+@pytest.mark.parametrize("hd", [128, 256])
+def test_fused_append(pkg, hd):
+    import torch
+    n_kv, G, cap = 2, 7, 300
+    n_head = G * n_kv
+    scale = 1 / math.sqrt(hd)
+    for nkv in (1, 16, 17, 63, 64, 65, 127, 128, 129, 200, cap):
+        case = make_case(5800 + nkv + hd, 1, n_head, n_kv, hd, cap, (nkv,))
+        case["k"][0, nkv - 1] = np.nan
+        case["v"][0, nkv - 1] = np.nan
+        k_new, v_new = _new_rows(nkv, 1, n_kv, hd)
+        dev = to_device(case)
+        kn, vn = torch.from_numpy(k_new).cuda(), torch.from_numpy(v_new).cuda()
+        for P in (0, 3 if hd == 128 else 5):
+            dev = to_device(case)
+            got = _run_append(pkg, dev, kn, vn, n_head, n_kv, hd, cap, scale, VT, P)
+            kh, vh = _host_after_append(case, k_new, v_new, cap)
+            ref = oracle.attn_decode(case["q"], kh, vh, case["positions"], n_head, n_kv, hd, cap,
+                                     scale)
+            assert_close(got, ref, "append nkv=%d P=%d" % (nkv, P))
+            np.testing.assert_array_equal(dev["k"].cpu().numpy().view(np.uint16), kh.view(np.uint16))
+            np.testing.assert_array_equal(dev["v"].cpu().numpy().view(np.uint16), vh.view(np.uint16))
+
+
+@pytest.mark.parametrize("graph, stable", [(False, True), (True, True), (True, False)])
+def test_early_start_chain(pkg, graph, stable):
+    P = pkg.attn_split_heuristic_ex(1, 1, 28, 4, 128, 2048, 0, VT | pkg.ATTN_KV_STABLE)
+    assert P * 128 >= 2048
+    _chain(pkg, L=5, n_head=28, n_kv=4, hd=128, cap=2048, ctx=(1900,), P=P, blk=0, variant=VT,
+           graph=graph, replays=3, seed=5900, stable=stable)
+
+
+def test_stable_chain_head_dim_256(pkg):
+    P = pkg.attn_split_heuristic_ex(1, 1, 16, 2, 256, 2560, 0, VT | pkg.ATTN_KV_STABLE)
+    assert P * TILE[256] >= 2560
+    _chain(pkg, L=4, n_head=16, n_kv=2, hd=256, cap=2560, ctx=(1000,), P=P, blk=0, variant=VT,
+           graph=True, replays=2, seed=5950)
+
+
+def test_full_long_workload(pkg):
+    w = syn.WORKLOADS["long"]
+    lay = syn.make_layer(w)
+    P = pkg.attn_split_heuristic_ex(1, 1, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0,
+                                    VT | pkg.ATTN_KV_STABLE)
+    assert P * TILE[256] >= w.cap
+    _check(pkg, lay, w.n_head, w.n_kv_head, w.cap, "long", hd=w.head_dim, n_splits=P)
+
+
+def test_full_7b_workload(pkg):
+    w = syn.WORKLOADS["7b"]
+    lay = syn.make_layer(w)
+    P = pkg.attn_split_heuristic_ex(1, 1, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0,
+                                    VT | pkg.ATTN_KV_STABLE)
+    assert P * 128 >= w.cap
+    for ctx in syn.CTX_SWEEP_7B:
+        case = dict(lay, positions=np.array([ctx - 1], np.int32))
+        _check(pkg, case, w.n_head, w.n_kv_head, w.cap, "7b ctx %d" % ctx, n_splits=P)
+
+
+def test_arguments_that_leave_a_split_larger_than_a_tile(pkg):
+    import torch
+    case = to_device(make_case(6000, 1, 8, 2, 128, 1024, (1000,)))
+    bad = [dict(n_splits=7),                          # 7 * 128 < 1024
+           dict(n_splits=8, split_len=129),
+           dict(n_splits=4, split_len=256)]
+    for kw in bad:
+        with pytest.raises(pkg.AttnError) as ei:
+            run_decode(pkg, case, 8, 2, 128, 1024, 0.1, variant=VT, **kw)
+        assert ei.value.status == pkg.ATTN_ERR_INVALID_ARG, kw
+    c256 = to_device(make_case(6002, 1, 8, 2, 256, 1024, (1000,)))
+    with pytest.raises(pkg.AttnError) as ei:
+        run_decode(pkg, c256, 8, 2, 256, 1024, 0.1, variant=VT, n_splits=10)   # 10 * 96 < 1024
+    assert ei.value.status == pkg.ATTN_ERR_INVALID_ARG
+    # head_dim 64 is not built for this kernel, nor are several query rows
+    c64 = to_device(make_case(6001, 1, 8, 2, 64, 256, (200,)))
+    with pytest.raises(pkg.AttnError) as ei:
+        run_decode(pkg, c64, 8, 2, 64, 256, 0.1, variant=VT)
+    assert ei.value.status == pkg.ATTN_ERR_UNSUPPORTED
+    q2 = torch.zeros((1, 2, 8, 128), device="cuda")
+    out = torch.empty_like(q2)
+    with pytest.raises(pkg.AttnError) as ei:
+        pkg.attn_decode_multi(q2, case["k"], case["v"], case["positions"], out, 1, 2, 8, 2, 128,
+                              0.1, 1024, n_splits=8, variant=VT)
+    assert ei.value.status == pkg.ATTN_ERR_UNSUPPORTED
