@@ -38,7 +38,7 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0          # GB300 HBM3e data-sheet bandwidth, for context only
 KERNEL_SOURCES = ["attn_device.cuh", "attn_partial.cuh", "attn_warp_tc.cuh", "attn_warp_simt.cuh",
-                  "attn_warp_tcmq.cuh",
+                  "attn_warp_tcmq.cuh", "attn_partial_tile.cuh",
                   "attn_partial_umma.cuh", "attn_fused_umma.cuh", "attn_combine.cuh",
                   "attn_kernels_impl.cuh"]
 

@@ -246,6 +246,27 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, i
                  : "memory");
 }
 
+// TMA: one 4-D tile (x = element, y = KV head, z = row within the sequence,
+// w = sequence). z may be negative: rows outside the tensor arrive as zeros.
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y, int z, int w)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];"
+        :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w),
+           "r"(smem_u32(bar))
+        : "memory");
+}
+
+// The same 4-D box into L2 only (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *map, int x, int y, int z, int w)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
+                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -111,19 +111,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// TMA: one 4-D tile (x = element, y = KV head, z = row within the sequence,
-// w = sequence). z may be negative: rows outside the tensor arrive as zeros.
-__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar,
-                                            int x, int y, int z, int w)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5}], [%6];"
-        :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w),
-           "r"(smem_u32(bar))
-        : "memory");
-}
-
 // Byte offset of P[row][n] (n < NCOL) in the MN-major, unswizzled B operand:
 // 8 x 8 core matrices of 128 bytes; 8-column groups 128 bytes apart, 8-row
 // groups NCOL * 16 bytes apart.
