@@ -176,7 +176,10 @@ bool one_tile_fits(int variant, int head_dim, int group, int n_q, int n_seq, int
     const int64_t pu = n_splits > 0 ? n_splits
                        : split_len > 0 ? (cap + split_len - 1) / split_len
                                        : heuristic(n_seq, n_kv_head, 1, cap, sm_count, ku, kv_stable);
-    return fits && pu * n_kv_head * n_seq <= (int64_t)sm_count * ku.blocks_per_sm;
+    // the one-tile mma.sync kernel serves several block-length splits per block
+    const int64_t spb = variant == attn::kVariantTile && n_q == 1 && attn::tile_serves_splits(ku.tile_rows, split_len)
+                            ? ku.tile_rows / split_len : 1;
+    return fits && (pu + spb - 1) / spb * n_kv_head * n_seq <= (int64_t)sm_count * ku.blocks_per_sm;
 }
 
 // ATTN_VARIANT_AUTO for short calls (one_tile_fits): one query row runs the

@@ -104,13 +104,18 @@ cudaError_t launch_partial_tile(const LaunchRequest &r)
     if (e != cudaSuccess) return e;
     e = encode_kv_map4(&vmap, r.v_cache, r.n_seq, r.pa.cap, r.pa.n_kv_head, HD, 64, C::TILE, dt);
     if (e != cudaSuccess) return e;
-    const void *fn = reinterpret_cast<const void *>(&attn_split_partial_tile<C, HD, G, KV>);
+    // by block length with blk dividing the tile: one block per SPB = TILE / blk splits
+    const int blk = r.pa.split_len;
+    const bool ms = tile_serves_splits(C::TILE, blk);
+    const void *fn = ms ? reinterpret_cast<const void *>(&attn_split_partial_tile_ms<C, HD, G, KV>)
+                        : reinterpret_cast<const void *>(&attn_split_partial_tile<C, HD, G, KV>);
     e = ensure_smem_attr(fn, (int)C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     PartialArgs pa = r.pa;
     void *args[] = {&kmap, &vmap, &pa};
-    return launch_pdl(fn, dim3(pa.n_kv_head, pa.n_splits, r.n_seq), dim3(C::THREADS), C::SMEM_BYTES,
-                      r.stream, args);
+    const int spb = ms ? C::TILE / blk : 1;
+    return launch_pdl(fn, dim3(pa.n_kv_head, (pa.n_splits + spb - 1) / spb, r.n_seq), dim3(C::THREADS),
+                      C::SMEM_BYTES, r.stream, args);
 }
 
 // The cluster-fused tcgen05 kernel: partial and combine in one launch, o written directly.

@@ -46,6 +46,14 @@ struct KernelInfo {
     int max_chunk;           // rows one block can take (0: any; the tcgen05 kernel: one tile)
 };
 
+// Whether the one-tile kernel serves several block-length splits per block:
+// split_len divides the tile (tile_rows rows) into at least two whole 16-row
+// parts (SPB = tile_rows / split_len splits per block).
+inline bool tile_serves_splits(int tile_rows, int split_len)
+{
+    return split_len > 0 && split_len < tile_rows && split_len % 16 == 0 && tile_rows % split_len == 0;
+}
+
 // Implemented in attn_api.cu.
 // Build a 3-D tensor map over a [rows][n_kv_head][head_dim] 16-bit cache
 // (kv_dtype kKvF16 / kKvBf16) with a box of (box_x, 1, box_rows); 128-byte

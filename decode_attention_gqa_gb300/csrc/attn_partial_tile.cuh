@@ -27,6 +27,12 @@
 //      with the block's final accumulator for its dimensions.
 //   6. a6: each warp writes its dimensions of oc for every head; one thread
 //      per head writes (mx, S), S from the warps' partial sums.
+// By block length (Red Lite dev35 "Change": split sp covers [sp·blk, sp·blk +
+// blk)) with blk dividing the tile, a second kernel lets one block serve
+// SPB = TILE / blk consecutive splits from one tile: the maxima and sums are
+// taken per split (over 8-row groups through shared memory), O = P · V is
+// accumulated one split at a time over that split's k-steps, and every warp
+// writes each split's partial for its dimensions.
 #pragma once
 
 #include "attn_device.cuh"
@@ -70,8 +76,10 @@ struct TileCfg {
     static constexpr uint32_t OFF_P = OFF_Q;            // P tile over the Q tile once S is done
     // P tile: 16 rows of TILE elements in 128-byte swizzled chunks of 64
     static constexpr uint32_t P_BYTES = 16u * ((TILE + 63) / 64 * 64) * 2;
-    static constexpr uint32_t OFF_RED = OFF_Q + (QStage::EXTRA_BYTES + 15) / 16 * 16;   // [2][NW][8] floats
-    static constexpr uint32_t OFF_BAR = OFF_RED + 2 * NW * 8 * 4;                       // 2 mbarriers, flags
+    // maxima and sums per 8-row group (the several-split kernel) or per warp
+    static constexpr int NRED = TILE / 8 > NW ? TILE / 8 : NW;
+    static constexpr uint32_t OFF_RED = OFF_Q + (QStage::EXTRA_BYTES + 15) / 16 * 16;   // [2][NRED][8] floats
+    static constexpr uint32_t OFF_BAR = OFF_RED + 2 * NRED * 8 * 4;                     // 2 mbarriers, flags
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 2 * 8 + 16 + 1024;                 // + alignment slack
     static constexpr float OFF = 7.f;                   // p headroom: p <= 2^OFF
     static_assert(P_BYTES <= QStage::QT_BYTES, "the P tile must not reach the per-head scales");
@@ -80,18 +88,106 @@ struct TileCfg {
     static_assert(MINB * (SMEM_BYTES + 1024) <= 233472u, "resident blocks per SM");
 };
 
+
+// a3 for one warp: S = Q · Kᵀ over tile rows r0 .. r0 + WR - 1 (Q fragments in
+// registers, K by ldmatrix), even and odd k-steps in separate accumulators;
+// head g's score for row r0 + 8j + 2t + e is (c[.][j][e] + c[.][j][2 + e]).
+template <class Cfg, int HD, typename KV>
+__device__ __forceinline__ void tile_scores(const uint8_t *smem, int r0, int lane, float (&c)[2][Cfg::NS][4])
+{
+    constexpr int TILE = Cfg::TILE, NS = Cfg::NS, KS = Cfg::KS;
+    const uint8_t *qt = smem + Cfg::OFF_Q;
+    const int i8 = lane >> 3;
+    uint32_t qa[Cfg::Q_REGS ? KS : 1][4];
+    if constexpr (Cfg::Q_REGS) {
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) ldsm_a16<HD>(qa[kk], qt, kk, lane);
+    }
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+        uint32_t aq[4];
+        if constexpr (Cfg::Q_REGS) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) aq[i] = qa[kk][i];
+        } else {
+            ldsm_a16<HD>(aq, qt, kk, lane);
+        }
+#pragma unroll
+        for (int j = 0; j + 1 < NS; j += 2) {
+            // (rows 8j..8j+7, dims lo 8), (.., hi 8), (rows 8j+8.., lo 8), (.., hi 8)
+            uint32_t b[4];
+            const int krow = r0 + 8 * j + (i8 >> 1) * 8 + (lane & 7);
+            ldsm_x4(b, smem + Cfg::OFF_K + tile_unit_offset<HD, TILE>(krow, 2 * kk + (i8 & 1)));
+            mma_16816<KV>(c[kk & 1][j], aq, b[0], b[1]);
+            mma_16816<KV>(c[kk & 1][j + 1], aq, b[2], b[3]);
+        }
+        if constexpr (NS % 2 == 1) {
+            // the last 8 rows alone: (dims lo 8), (dims hi 8); lanes 16-31 repeat the addresses
+            uint32_t b[2];
+            const int krow = r0 + 8 * (NS - 1) + (lane & 7);
+            ldsm_x2(b, smem + Cfg::OFF_K + tile_unit_offset<HD, TILE>(krow, 2 * kk + (i8 & 1)));
+            mma_16816<KV>(c[kk & 1][NS - 1], aq, b[0], b[1]);
+        }
+    }
+}
+
+// p of head g for tile rows (r, r + 1) as a hi/lo pair into the P tile
+// [16 slots][TILE rows]: hi in slot row g, lo in slot row 8 + g.
+template <class Cfg, typename KV>
+__device__ __forceinline__ void store_p_pair(uint8_t *pt, int r, int g, int t, float p0, float p1)
+{
+    const uint32_t hw = float2_to_kv2<KV>(p0, p1);
+    const float2 f = kv2_to_float2<KV>(hw);
+    const uint32_t lw = float2_to_kv2<KV>(p0 - f.x, p1 - f.y);
+    // row pair (r, r + 1) of unit r / 8, 4 bytes apart per t
+    *reinterpret_cast<uint32_t *>(pt + tile_unit_offset<Cfg::TILE, 16>(g, r >> 3) + 4 * t) = hw;
+    *reinterpret_cast<uint32_t *>(pt + tile_unit_offset<Cfg::TILE, 16>(8 + g, r >> 3) + 4 * t) = lw;
+}
+
+// a5 for one warp, one k-step: o += P · V over tile rows 16kk .. 16kk + 15 for
+// dimensions d0 .. d0 + DW - 1.
+template <class Cfg, int HD, typename KV>
+__device__ __forceinline__ void tile_pv_step(const uint8_t *smem, int d0, int lane, int kk, float (&o)[Cfg::NO][4])
+{
+    constexpr int TILE = Cfg::TILE, NO = Cfg::NO;
+    const int i8 = lane >> 3;
+    uint32_t ap[4];                       // P rows (slots) x tile rows 16kk .. 16kk + 15
+    ldsm_a16<TILE>(ap, smem + Cfg::OFF_P, kk, lane);
+    const int vrow = 16 * kk + (i8 & 1) * 8 + (lane & 7);
+#pragma unroll
+    for (int j = 0; j < NO; j += 2) {
+        // (rows 0-7, dims j), (rows 8-15, dims j), (0-7, j+1), (8-15, j+1)
+        uint32_t b[4];
+        ldsm_x4_trans(b, smem + Cfg::OFF_V + tile_unit_offset<HD, TILE>(vrow, (d0 >> 3) + j + (i8 >> 1)));
+        mma_16816<KV>(o[j], ap, b[0], b[1]);
+        mma_16816<KV>(o[j + 1], ap, b[2], b[3]);
+    }
+}
+
+// o += P · V over k-steps [k0, k1), even and odd k-steps into o[0] and o[1]
+// (two independent MMA chains).
+template <class Cfg, int HD, typename KV>
+__device__ __forceinline__ void tile_pv(const uint8_t *smem, int d0, int lane, int k0, int k1,
+                                        float (&o)[2][Cfg::NO][4])
+{
+    for (int kk = k0; kk < k1; kk += 2) {
+        tile_pv_step<Cfg, HD, KV>(smem, d0, lane, kk, o[0]);
+        if (kk + 1 < k1) tile_pv_step<Cfg, HD, KV>(smem, d0, lane, kk + 1, o[1]);
+    }
+}
+
 template <class Cfg, int HD, int G, typename KV>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
 attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const PartialArgs a)
 {
-    constexpr int TILE = Cfg::TILE, NS = Cfg::NS, KS = Cfg::KS, NO = Cfg::NO, KO = Cfg::KO;
+    constexpr int TILE = Cfg::TILE, NS = Cfg::NS, NO = Cfg::NO, KO = Cfg::KO;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + Cfg::OFF_BAR);    // [0] K landed, [1] V landed
     volatile int *flags = reinterpret_cast<volatile int *>(bar + 2);     // [0] abort
     float *red_m = reinterpret_cast<float *>(smem + Cfg::OFF_RED);      // [NW][8] warp maxima
-    float *red_l = red_m + Cfg::NW * 8;                                 // [NW][8] warp sums
+    float *red_l = red_m + Cfg::NRED * 8;                               // [NW][8] warp sums
 
     const int hk = blockIdx.x, sp = blockIdx.y, s = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -158,9 +254,8 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
     }
     __syncthreads();
 
-    const uint8_t *qt = smem + Cfg::OFF_Q;
-    const float inv = reinterpret_cast<const float *>(qt + Cfg::QStage::QT_BYTES)[lane >> 2];
-    const int i8 = lane >> 3, g = lane >> 2, t = lane & 3;
+    const float inv = reinterpret_cast<const float *>(smem + Cfg::OFF_Q + Cfg::QStage::QT_BYTES)[lane >> 2];
+    const int g = lane >> 2, t = lane & 3;
     bool ok = mbar_wait_bounded(bar + 0, 0);
     ok = __all_sync(0xffffffffu, ok);
     if (ok && appending) {
@@ -191,39 +286,7 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
             for (int j = 0; j < NS; ++j)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) c[e][j][i] = 0.f;
-        if (ok) {
-            uint32_t qa[Cfg::Q_REGS ? KS : 1][4];
-            if constexpr (Cfg::Q_REGS) {
-#pragma unroll
-                for (int kk = 0; kk < KS; ++kk) ldsm_a16<HD>(qa[kk], qt, kk, lane);
-            }
-#pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
-                uint32_t aq[4];
-                if constexpr (Cfg::Q_REGS) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) aq[i] = qa[kk][i];
-                } else {
-                    ldsm_a16<HD>(aq, qt, kk, lane);
-                }
-#pragma unroll
-                for (int j = 0; j + 1 < NS; j += 2) {
-                    // (rows 8j..8j+7, dims lo 8), (.., hi 8), (rows 8j+8.., lo 8), (.., hi 8)
-                    uint32_t b[4];
-                    const int krow = r0 + 8 * j + (i8 >> 1) * 8 + (lane & 7);
-                    ldsm_x4(b, smem + Cfg::OFF_K + tile_unit_offset<HD, TILE>(krow, 2 * kk + (i8 & 1)));
-                    mma_16816<KV>(c[kk & 1][j], aq, b[0], b[1]);
-                    mma_16816<KV>(c[kk & 1][j + 1], aq, b[2], b[3]);
-                }
-                if constexpr (NS % 2 == 1) {
-                    // the last 8 rows alone: (dims lo 8), (dims hi 8); lanes 16-31 repeat the addresses
-                    uint32_t b[2];
-                    const int krow = r0 + 8 * (NS - 1) + (lane & 7);
-                    ldsm_x2(b, smem + Cfg::OFF_K + tile_unit_offset<HD, TILE>(krow, 2 * kk + (i8 & 1)));
-                    mma_16816<KV>(c[kk & 1][NS - 1], aq, b[0], b[1]);
-                }
-            }
-        }
+        if (ok) tile_scores<Cfg, HD, KV>(smem, r0, lane, c);
 #pragma unroll
         for (int j = 0; j < NS; ++j)
 #pragma unroll
@@ -252,13 +315,7 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
         for (int j = 0; j < NS; ++j) {
             const float p0 = ex2(sc[j][0] - base), p1 = ex2(sc[j][1] - base);   // 0 at -inf
             lsum += p0 + p1;
-            const uint32_t hw = float2_to_kv2<KV>(p0, p1);
-            const float2 f = kv2_to_float2<KV>(hw);
-            const uint32_t lw = float2_to_kv2<KV>(p0 - f.x, p1 - f.y);
-            // P[slot][row]: row pair (r, r + 1) of unit r / 8, 4 bytes apart per t
-            const int r = r0 + 8 * j;
-            *reinterpret_cast<uint32_t *>(pt + tile_unit_offset<TILE, 16>(g, r >> 3) + 4 * t) = hw;
-            *reinterpret_cast<uint32_t *>(pt + tile_unit_offset<TILE, 16>(8 + g, r >> 3) + 4 * t) = lw;
+            store_p_pair<Cfg, KV>(pt, r0 + 8 * j, g, t, p0, p1);
         }
         lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
         lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
@@ -279,21 +336,7 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
             for (int j = 0; j < NO; ++j)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) o[e][j][i] = 0.f;
-        const uint8_t *pt = smem + Cfg::OFF_P;
-#pragma unroll
-        for (int kk = 0; kk < KO; ++kk) {
-            uint32_t ap[4];                   // P rows (slots) x tile rows 16kk .. 16kk + 15
-            ldsm_a16<TILE>(ap, pt, kk, lane);
-            const int vrow = 16 * kk + (i8 & 1) * 8 + (lane & 7);
-#pragma unroll
-            for (int j = 0; j < NO; j += 2) {
-                // (rows 0-7, dims j), (rows 8-15, dims j), (0-7, j+1), (8-15, j+1)
-                uint32_t b[4];
-                ldsm_x4_trans(b, smem + Cfg::OFF_V + tile_unit_offset<HD, TILE>(vrow, (d0 >> 3) + j + (i8 >> 1)));
-                mma_16816<KV>(o[kk & 1][j], ap, b[0], b[1]);
-                mma_16816<KV>(o[kk & 1][j + 1], ap, b[2], b[3]);
-            }
-        }
+        tile_pv<Cfg, HD, KV>(smem, d0, lane, 0, KO, o);
         // ---- a6: oc of every head for these dimensions; (mx, S) per head ----
         if (g < G) {
             float *dst = a.ws_o + (((size_t)s * heads + (size_t)hk * G + g) * P + sp) * HD + d0 + 2 * t;
@@ -310,6 +353,217 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
     } else if (tid == 0) {
         // nothing may still be writing shared memory when the block exits:
         // wait (bounded) for both copies before leaving
+        (void)mbar_wait_bounded(bar + 0, 0);
+        (void)mbar_wait_bounded(bar + 1, 0);
+    }
+}
+
+// By block length with blk = split_len dividing TILE (and a multiple of 16):
+// block b serves the SPB = TILE / blk splits b·SPB .. b·SPB + SPB - 1, whose
+// rows [b·TILE, b·TILE + TILE) are one tile starting at row b·TILE. Cache
+// rows of that tile at or past nkv (in the last block only; all within cap,
+// and rows past cap arrive as zeros) are read but never used: their scores
+// are masked and their V rows are set to zero in shared memory before P · V,
+// so whatever the cache holds there cannot reach the result.
+template <class Cfg, int HD, int G, typename KV>
+__global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
+attn_split_partial_tile_ms(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                           const PartialArgs a)
+{
+    constexpr int TILE = Cfg::TILE, NS = Cfg::NS, NO = Cfg::NO;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + Cfg::OFF_BAR);    // [0] K landed, [1] V landed
+    volatile int *flags = reinterpret_cast<volatile int *>(bar + 2);     // [0] abort
+    float *red_m = reinterpret_cast<float *>(smem + Cfg::OFF_RED);      // [TILE / 8][8] group maxima
+    float *red_l = red_m + Cfg::NRED * 8;                               // [TILE / 8][8] group sums
+
+    const int hk = blockIdx.x, b = blockIdx.y, s = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int P = a.n_splits, blk = a.split_len, SPB = TILE / blk, GPS = blk / 8;   // 8-row groups per split
+    const size_t heads = (size_t)a.n_head;
+
+    const bool stable = a.kv_stable != 0;
+    if (tid == 32)
+        prefetch_l2(a.q + ((size_t)s * a.n_head + (size_t)hk * G) * HD, (uint32_t)(G * HD * sizeof(float)));
+    if (!stable) pdl_wait();
+    pdl_launch_dependents();
+
+    // a1: rows attended; this block's rows are [row0, row0 + nv)
+    bool pos_ok;
+    const int64_t nkv = rows_attended(a, s, b == 0 && hk == 0 && tid == 0, &pos_ok);
+    const int64_t row0 = (int64_t)b * TILE;
+    const int nv = nkv > row0 ? (int)(nkv - row0 < TILE ? nkv - row0 : TILE) : 0;
+    auto write_empty = [&](int j0) {
+        // (mx, S) = (-inf, 0) for the splits j0 .. SPB - 1 of this block
+        for (int i = tid; i < (SPB - j0) * 8; i += Cfg::THREADS) {
+            const int j = j0 + i / 8, gg = i % 8, sp = b * SPB + j;
+            if (gg < G && sp < P)
+                a.ws_ml[((size_t)s * heads + (size_t)hk * G + gg) * P + sp] = make_float2(-INFINITY, 0.f);
+        }
+    };
+    if (nv == 0) {
+        if (stable) pdl_wait();               // the workspace may still be read by the previous grid
+        write_empty(0);
+        return;
+    }
+    const int nsplit = (nv + blk - 1) / blk;  // splits of this block with rows (the rest are empty)
+
+    if (tid == 0) {
+        mbar_init(bar + 0, 1);
+        mbar_init(bar + 1, 1);
+        flags[0] = 0;
+        fence_barrier_init();
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+        mbar_arrive_expect_tx(bar + 0, Cfg::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < Cfg::NCH; ++c)
+            tma_load_4d(smem + Cfg::OFF_K + c * (Cfg::TILE_BYTES / Cfg::NCH), &kmap, bar + 0, c * 64, hk, (int)row0, s);
+        mbar_arrive_expect_tx(bar + 1, Cfg::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < Cfg::NCH; ++c)
+            tma_load_4d(smem + Cfg::OFF_V + c * (Cfg::TILE_BYTES / Cfg::NCH), &vmap, bar + 1, c * 64, hk, (int)row0, s);
+    }
+
+    if (stable) pdl_wait();
+    Cfg::QStage::template prepare<Cfg::THREADS>(smem + Cfg::OFF_Q, a, s, hk, 0, tid);
+    // Fused append: the new row nkv - 1 is tile row nv - 1 of the block that
+    // holds it; the warp whose S rows contain it writes it into both tiles and
+    // the cache once they have landed, before the barrier that precedes any
+    // read of V.
+    constexpr int NU = HD / 8;
+    constexpr int NJ = 2 * NU / 32;
+    static_assert(2 * NU % 32 == 0, "whole units per lane");
+    const bool appending = a.k_new != nullptr && pos_ok && row0 + nv == nkv && warp == (nv - 1) / Cfg::WR;
+    uint4 newrow[NJ];
+    if (appending) {
+        const size_t src = ((size_t)s * a.n_kv_head + hk) * HD;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            const int i = lane + 32 * j;
+            newrow[j] = ld_dep(reinterpret_cast<const uint4 *>((i < NU ? a.k_new : a.v_new) + src) + (i % NU));
+        }
+    }
+    if (nsplit < SPB) write_empty(nsplit);    // before the barrier: the workspace is ours past the wait
+    __syncthreads();
+
+    const float inv = reinterpret_cast<const float *>(smem + Cfg::OFF_Q + Cfg::QStage::QT_BYTES)[lane >> 2];
+    const int g = lane >> 2, t = lane & 3;
+    bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar + 0, 0));
+    if (ok && appending) {
+        const bool vl = __all_sync(0xffffffffu, mbar_wait_bounded(bar + 1, 0));
+        if (vl) {
+            const size_t dst = ((size_t)((int64_t)s * a.cap + nkv - 1) * a.n_kv_head + hk) * HD;
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) {
+                const int i = lane + 32 * j;
+                uint8_t *tile = smem + (i < NU ? Cfg::OFF_K : Cfg::OFF_V);
+                *reinterpret_cast<uint4 *>(tile + tile_unit_offset<HD, TILE>(nv - 1, i % NU)) = newrow[j];
+                reinterpret_cast<uint4 *>((i < NU ? a.k_w : a.v_w) + dst)[i % NU] = newrow[j];
+            }
+            __syncwarp();
+        }
+        ok = vl;
+    }
+    if (!ok && lane == 0) { flags[0] = 1; atomicOr(a.err, kErrPipelineTimeout); }
+
+    // ---- a3: S for this warp's rows r0 .. r0 + WR - 1 (rows at or past nv masked) ----
+    const int r0 = warp * Cfg::WR;
+    float sc[NS][2];
+    {
+        float c[2][NS][4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int j = 0; j < NS; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) c[e][j][i] = 0.f;
+        if (ok) tile_scores<Cfg, HD, KV>(smem, r0, lane, c);
+#pragma unroll
+        for (int j = 0; j < NS; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int r = r0 + 8 * j + 2 * t + e;
+                const float v = ((c[0][j][e] + c[1][j][e]) + (c[0][j][2 + e] + c[1][j][2 + e])) * inv;
+                sc[j][e] = r < nv ? v : -INFINITY;
+            }
+    }
+    // ---- a4: each head's maximum per 8-row group, then per split ----
+#pragma unroll
+    for (int j = 0; j < NS; ++j) {
+        float m = fmaxf(sc[j][0], sc[j][1]);
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        if (t == 0) red_m[(r0 / 8 + j) * 8 + g] = m;
+    }
+    __syncthreads();                          // the maxima are in; S is done, so Q is dead
+    {
+        uint8_t *pt = smem + Cfg::OFF_P;
+#pragma unroll
+        for (int j = 0; j < NS; ++j) {
+            const int grp = r0 / 8 + j, first = grp / GPS * GPS;   // the split's first 8-row group
+            float M = red_m[first * 8 + g];
+            for (int k = 1; k < GPS; ++k) M = fmaxf(M, red_m[(first + k) * 8 + g]);
+            // a split with no row before nv has M = -inf and p = 0 throughout
+            const float base = M - Cfg::OFF;
+            const float p0 = M == -INFINITY ? 0.f : ex2(sc[j][0] - base);
+            const float p1 = M == -INFINITY ? 0.f : ex2(sc[j][1] - base);
+            store_p_pair<Cfg, KV>(pt, r0 + 8 * j, g, t, p0, p1);
+            float l = p0 + p1;
+            l += __shfl_xor_sync(0xffffffffu, l, 1);
+            l += __shfl_xor_sync(0xffffffffu, l, 2);
+            if (t == 0) red_l[grp * 8 + g] = l;
+        }
+    }
+    bool vok = ok;
+    if (vok && !appending) vok = __all_sync(0xffffffffu, mbar_wait_bounded(bar + 1, 0));
+    if (ok && !vok && lane == 0) { flags[0] = 1; atomicOr(a.err, kErrPipelineTimeout); }
+    if (vok && nv < TILE) {
+        // V rows at or past nkv in this warp's row range: zero, so P = 0 there meets 0
+        const int rlo = r0 > nv ? r0 : nv, rhi = r0 + Cfg::WR;
+        for (int i = lane; i < (rhi - rlo) * NU; i += 32)
+            if (rlo < rhi)
+                *reinterpret_cast<uint4 *>(smem + Cfg::OFF_V + tile_unit_offset<HD, TILE>(rlo + i / NU, i % NU)) =
+                    make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncthreads();                          // P, the sums and the zeroed rows are in
+    // ---- a5, a6: per split, O = P · V over its k-steps, oc and (mx, S) written ----
+    const int d0 = warp * Cfg::DW;
+    const bool abort = flags[0] != 0;
+    if (!abort) {
+        const int KPS = blk / 16;             // k-steps per split
+        for (int j = 0; j < nsplit; ++j) {
+            const int sp = b * SPB + j;
+            float o[2][NO][4];
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+#pragma unroll
+                for (int jj = 0; jj < NO; ++jj)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) o[e][jj][i] = 0.f;
+            tile_pv<Cfg, HD, KV>(smem, d0, lane, j * KPS, (j + 1) * KPS, o);
+            if (g < G && sp < P) {
+                float *dst = a.ws_o + (((size_t)s * heads + (size_t)hk * G + g) * P + sp) * HD + d0 + 2 * t;
+#pragma unroll
+                for (int jj = 0; jj < NO; ++jj)
+                    *reinterpret_cast<float2 *>(dst + 8 * jj) =
+                        make_float2((o[0][jj][0] + o[1][jj][0]) + (o[0][jj][2] + o[1][jj][2]),
+                                    (o[0][jj][1] + o[1][jj][1]) + (o[0][jj][3] + o[1][jj][3]));
+            }
+        }
+        // (mx, S) of every non-empty split: thread (j, head)
+        for (int i = tid; i < nsplit * 8; i += Cfg::THREADS) {
+            const int j = i / 8, gg = i % 8, sp = b * SPB + j;
+            if (gg < G && sp < P) {
+                float M = -INFINITY, L = 0.f;
+                for (int k = 0; k < GPS; ++k) M = fmaxf(M, red_m[(j * GPS + k) * 8 + gg]);
+                for (int k = 0; k < GPS; ++k) L += red_l[(j * GPS + k) * 8 + gg];
+                a.ws_ml[((size_t)s * heads + (size_t)hk * G + gg) * P + sp] =
+                    make_float2(M == -INFINITY ? M : M - Cfg::OFF, L);
+            }
+        }
+    } else if (tid == 0) {
         (void)mbar_wait_bounded(bar + 0, 0);
         (void)mbar_wait_bounded(bar + 1, 0);
     }

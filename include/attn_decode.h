@@ -100,9 +100,13 @@ typedef enum {
                                  registers (q and p as hi + lo pairs as above), S split by rows
                                  over four warps, one block-wide maximum, O = P·V split by head
                                  dimension over the warps (no merge of warp states). One tile of
-                                 T rows per block (T = 128; 64 at head_dim 256); head_dim 128 or
+                                 T rows per block (T = 128; 96 at head_dim 256); head_dim 128 or
                                  256, one query row (ATTN_ERR_UNSUPPORTED otherwise). Every split
-                                 must fit one tile, as for ATTN_VARIANT_TCGEN05. */
+                                 must fit one tile, as for ATTN_VARIANT_TCGEN05. By block length
+                                 with split_len a multiple of 16 that divides T, one block serves
+                                 T / split_len consecutive splits from one tile (cache rows of
+                                 that tile past nkv are then read -- all below cap -- but never
+                                 used). */
 
 /* Cache element type, OR'd into the variant argument: without it K and V are
    IEEE binary16 (f16); with it they are bfloat16 (1 sign, 8 exponent, 7

@@ -237,3 +237,77 @@ def test_arguments_that_leave_a_split_larger_than_a_tile(pkg):
         pkg.attn_decode_multi(q2, case["k"], case["v"], case["positions"], out, 1, 2, 8, 2, 128,
                               0.1, 1024, n_splits=8, variant=VT)
     assert ei.value.status == pkg.ATTN_ERR_UNSUPPORTED
+
+
+# ---- several block-length splits per block (split_len divides the tile) ----
+
+@pytest.mark.parametrize("hd,blk", [(128, 16), (128, 32), (128, 64), (256, 16), (256, 32), (256, 48)])
+def test_several_splits_per_block_with_nan_past_nkv(pkg, hd, blk):
+    """One block serves TILE / blk consecutive splits from one tile that starts
+    at a multiple of the tile; its rows at or past nkv are read but must never
+    reach the result, so they hold NaN here (capacity not a multiple of the tile,
+    so the last tile also reaches past the cache)."""
+    n_head, n_kv, cap = 14, 2, 1100
+    T = TILE[hd]
+    base = make_case(6100 + hd + blk, 1, n_head, n_kv, hd, cap, (cap,))
+    scale = 1 / math.sqrt(hd)
+    P = -(-cap // blk)
+    for nkv in sorted({1, 2, blk - 1, blk, blk + 1, T - 1, T, T + 1, 2 * T - blk, 2 * T + 7, 513,
+                       cap - T - 1, cap - 1, cap}):
+        case = dict(base)
+        case["k"] = base["k"].copy()
+        case["v"] = base["v"].copy()
+        case["k"][0, nkv:] = np.nan
+        case["v"][0, nkv:] = np.nan
+        case["positions"] = np.array([nkv - 1], np.int32)
+        _check(pkg, case, n_head, n_kv, cap, "hd%d blk %d nkv=%d" % (hd, blk, nkv), hd=hd,
+               n_splits=P, split_len=blk)
+
+
+@pytest.mark.parametrize("hd,blk", [(128, 32), (256, 32)])
+def test_several_splits_per_block_ragged_batch(pkg, hd, blk):
+    n_head, n_kv, cap = 32, 8, 900
+    ctx = (1, 900, 0, 17, 450, 899, 64, 333, 128, 129)
+    case = make_case(6200 + hd, len(ctx), n_head, n_kv, hd, cap, ctx, fill=np.nan)
+    P = -(-cap // blk)
+    for variant in (VT, 0):                       # and whatever variant 0 picks
+        _check(pkg, case, n_head, n_kv, cap, "hd%d ragged blk %d variant %d" % (hd, blk, variant),
+               hd=hd, n_splits=P, split_len=blk, variant=variant)
+
+
+@pytest.mark.parametrize("hd", [128, 256])
+def test_several_splits_per_block_fused_append(pkg, hd):
+    import torch
+    n_kv, G, cap, blk = 2, 7, 300, 32
+    n_head = G * n_kv
+    scale = 1 / math.sqrt(hd)
+    P = -(-cap // blk)
+    for nkv in (1, 31, 32, 33, 95, 96, 97, 128, 129, 200, cap):
+        case = make_case(6300 + nkv + hd, 1, n_head, n_kv, hd, cap, (nkv,))
+        case["k"][0, nkv - 1] = np.nan
+        case["v"][0, nkv - 1] = np.nan
+        k_new, v_new = _new_rows(nkv + 7, 1, n_kv, hd)
+        dev = to_device(case)
+        kn, vn = torch.from_numpy(k_new).cuda(), torch.from_numpy(v_new).cuda()
+        out = torch.full_like(dev["q"], float("nan"))
+        pkg.attn_decode_append(dev["q"], kn, vn, dev["k"], dev["v"], dev["positions"], out, 1,
+                               n_head, n_kv, hd, scale, cap, n_splits=P, split_len=blk, variant=VT)
+        torch.cuda.synchronize()
+        kh, vh = _host_after_append(case, k_new, v_new, cap)
+        ref = oracle.attn_decode(case["q"], kh, vh, case["positions"], n_head, n_kv, hd, cap, scale)
+        assert_close(out.cpu().numpy(), ref, "hd%d append blk %d nkv=%d" % (hd, blk, nkv))
+        np.testing.assert_array_equal(dev["k"].cpu().numpy().view(np.uint16), kh.view(np.uint16))
+        np.testing.assert_array_equal(dev["v"].cpu().numpy().view(np.uint16), vh.view(np.uint16))
+
+
+def test_several_splits_per_block_stable_chain(pkg):
+    _chain(pkg, L=4, n_head=16, n_kv=2, hd=256, cap=2560, ctx=(1000,), P=-(-2560 // 32), blk=32,
+           variant=VT, graph=True, replays=2, seed=6400)
+
+
+def test_full_long_workload_block_32(pkg):
+    w = syn.WORKLOADS["long"]
+    lay = syn.make_layer(w)
+    v, P, _ = pkg.attn_plan_call(1, 1, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0, 32, 0)
+    assert v == VT and P == -(-w.cap // 32)
+    _check(pkg, lay, w.n_head, w.n_kv_head, w.cap, "long blk 32", hd=w.head_dim, split_len=32)
