@@ -137,6 +137,23 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def traffic_key(args, w, ctx_end) -> str:
+    """The key of a configuration in the profiles/*.md traffic lines: workload,
+    context, and every option that changes the kernel or its bytes."""
+    key = "%s_ctx%d" % (w.name, ctx_end)
+    if args.split_len:
+        key += "_blk%d" % args.split_len
+    if args.n_q > 1:
+        key += "_nq%d" % args.n_q
+    if args.kv_dtype != "f16":
+        key += "_" + args.kv_dtype
+    if args.append:
+        key += "_append"
+    if args.variant:
+        key += "_v%d" % args.variant
+    return key
+
+
 def profiled_traffic(workload_key: str):
     """DRAM read+write bytes per partial launch for a workload from the committed
     ncu summaries (profiles/*.md lines `traffic_per_launch_bytes[<key>]: N`),
@@ -610,8 +627,7 @@ def measure_one(args, rank, world, local):
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                 "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
-                "traffic": profiled_traffic("%s_ctx%d%s" % (w.name, ctx_end,
-                                                            "_nq%d" % n_q if n_q > 1 else "")),
+                "traffic": profiled_traffic(traffic_key(args, w, ctx_end)),
                 "kernel": ({4: "attn_fused_umma (partial and combine in one kernel)",
                             3: "attn_split_partial_umma", 5: "attn_split_partial_tile"}
                            .get(resolved, "attn_split_partial"))
