@@ -57,6 +57,9 @@ struct TileCfg {
     static_assert(HD == 128 || HD == 256, "the one-tile kernel is built for head_dim 128 and 256");
     static constexpr int TILE = HD == 256 ? 96 : 128;   // rows per block
     static constexpr int MINB = HD == 256 ? 2 : 3;      // resident blocks per SM
+    // warps: S rows and O dimensions split NW ways (8 warps at head_dim 128 were measured
+    // slower: each warp reads all of Q and P from shared memory, and more warps meet at
+    // each barrier)
     static constexpr int NW = 4;
     static constexpr int THREADS = NW * 32;
     static constexpr int WR = TILE / NW;                // S rows per warp (32 or 24)
@@ -306,7 +309,9 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
         if (t == 0) red_m[warp * 8 + g] = m;
     }
     __syncthreads();                          // the maxima are in; S is done, so Q is dead
-    const float M = fmaxf(fmaxf(red_m[g], red_m[8 + g]), fmaxf(red_m[16 + g], red_m[24 + g]));
+    float M = red_m[g];
+#pragma unroll
+    for (int w = 1; w < Cfg::NW; ++w) M = fmaxf(M, red_m[w * 8 + g]);
     const float base = M - Cfg::OFF;          // M is finite: the split has rows in every block
     {
         float lsum = 0.f;
@@ -347,7 +352,9 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
                                 (o[0][j][1] + o[1][j][1]) + (o[0][j][3] + o[1][j][3]));
         }
         if (warp == 0 && t == 0 && g < G) {
-            const float L = (red_l[g] + red_l[8 + g]) + (red_l[16 + g] + red_l[24 + g]);
+            float L = 0.f;
+#pragma unroll
+            for (int w = 0; w < Cfg::NW; ++w) L += red_l[w * 8 + g];
             a.ws_ml[((size_t)s * heads + (size_t)hk * G + g) * P + sp] = make_float2(base, L);
         }
     } else if (tid == 0) {
