@@ -158,8 +158,9 @@ int heuristic(int n_seq, int n_kv_head, int qgroups, int64_t cap, int sm_count,
 }
 
 // Whether a one-tile kernel (max_chunk rows per block) can take the call:
-// head_dim 128 or 256; one query row, or several whose (row, head) slots of a
-// KV head fit one 16-slot block; a known capacity; splits of at most one tile
+// head_dim 128 or 256 (several query rows: the one-tile mma.sync kernel at 128,
+// ceil(n_q * group / 16) blocks per split and KV head; tcgen05 when a KV head's
+// (row, head) slots fit one 16-slot block); a known capacity; splits of at most one tile
 // each; and one wave of its blocks (at full capacity at most blocks_per_sm
 // tiles per SM, so a short call, bound by its chain of dependent steps rather
 // than by bandwidth). On success `ku` holds the kernel's info.
@@ -167,7 +168,10 @@ bool one_tile_fits(int variant, int head_dim, int group, int n_q, int n_seq, int
                    int sm_count, int n_splits, int split_len, bool kv_stable, attn::KernelInfo &ku)
 {
     const int qgroups = (n_q * group + attn::kMqHeadsPerBlock - 1) / attn::kMqHeadsPerBlock;
-    if ((head_dim != 128 && head_dim != 256) || (n_q > 1 && qgroups != 1) || cap <= 0 || sm_count <= 0)
+    // the tcgen05 kernel takes one query group per KV head; the one-tile mma.sync
+    // kernel as many as fit one wave
+    if ((head_dim != 128 && head_dim != 256) || (variant == attn::kVariantUmma && n_q > 1 && qgroups != 1) ||
+        cap <= 0 || sm_count <= 0)
         return false;
     ku = kernel_info(head_dim, group, variant, n_q > 1);
     if (!ku.available) return false;
@@ -175,26 +179,30 @@ bool one_tile_fits(int variant, int head_dim, int group, int n_q, int n_seq, int
                                     : n_splits == 0 || (int64_t)n_splits * ku.max_chunk >= cap;
     const int64_t pu = n_splits > 0 ? n_splits
                        : split_len > 0 ? (cap + split_len - 1) / split_len
-                                       : heuristic(n_seq, n_kv_head, 1, cap, sm_count, ku, kv_stable);
+                                       : heuristic(n_seq, n_kv_head, n_q > 1 ? qgroups : 1, cap, sm_count, ku,
+                                                   kv_stable);
     // the one-tile mma.sync kernel serves several block-length splits per block
     const int64_t spb = variant == attn::kVariantTile && n_q == 1 && attn::tile_serves_splits(ku.tile_rows, split_len)
                             ? ku.tile_rows / split_len : 1;
-    return fits && (pu + spb - 1) / spb * n_kv_head * n_seq <= (int64_t)sm_count * ku.blocks_per_sm;
+    const int64_t qb = n_q > 1 ? qgroups : 1;
+    return fits && (pu + spb - 1) / spb * n_kv_head * n_seq * qb <= (int64_t)sm_count * ku.blocks_per_sm;
 }
 
 // ATTN_VARIANT_AUTO for short calls (one_tile_fits): one query row runs the
 // one-tile mma.sync kernel (operands in registers, no tensor-memory round
 // trips; measured faster than the tcgen05 kernel at every context of the
 // 7b-like layer -- 3.7 against 4.5 us per call at context 128, 5.8 against
-// 6.0 at 8192 -- and on the head_dim-256 layer, 6.3 against 7.2 us); several
-// query rows run the tcgen05 kernel (faster there at two rows). Long caches
-// and batches keep the mma.sync streaming kernel (0: no short-call kernel).
+// 6.0 at 8192 -- and on the head_dim-256 layer, 6.3 against 7.2 us); so do
+// several query rows at head_dim 128 (two rows of the 7b-like layer at context
+// 8192: 7.6 us against 8.7 on tcgen05); several rows at head_dim 256 run the
+// tcgen05 kernel. Long caches and batches keep the mma.sync streaming kernel
+// (0: no short-call kernel).
 // The call path and the planning entry points share this rule, so that they
 // report the kernel and split count a call uses.
 int auto_short_kernel(int head_dim, int group, int n_q, int n_seq, int n_kv_head, int64_t cap,
                       int sm_count, int n_splits, int split_len, bool kv_stable, attn::KernelInfo &ku)
 {
-    if (n_q == 1 &&
+    if ((n_q == 1 || head_dim == 128) &&
         one_tile_fits(attn::kVariantTile, head_dim, group, n_q, n_seq, n_kv_head, cap, sm_count, n_splits,
                       split_len, kv_stable, ku))
         return attn::kVariantTile;

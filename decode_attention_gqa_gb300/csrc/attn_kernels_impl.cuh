@@ -118,6 +118,27 @@ cudaError_t launch_partial_tile(const LaunchRequest &r)
                       C::SMEM_BYTES, r.stream, args);
 }
 
+// The one-tile mma.sync kernel for several causal query rows: 16 (row, head)
+// slots per block, grid (KV head x query group, split, sequence).
+template <int HD, typename KV>
+cudaError_t launch_partial_tile_mq(const LaunchRequest &r)
+{
+    using C = TileCfg<HD, kMqHeads, KV, true>;
+    alignas(64) CUtensorMap kmap, vmap;
+    const int dt = kv_dtype_code<KV>();
+    cudaError_t e = encode_kv_map4(&kmap, r.k_cache, r.n_seq, r.pa.cap, r.pa.n_kv_head, HD, 64, C::TILE, dt);
+    if (e != cudaSuccess) return e;
+    e = encode_kv_map4(&vmap, r.v_cache, r.n_seq, r.pa.cap, r.pa.n_kv_head, HD, 64, C::TILE, dt);
+    if (e != cudaSuccess) return e;
+    const void *fn = reinterpret_cast<const void *>(&attn_split_partial_tile_mq<C, HD, KV>);
+    e = ensure_smem_attr(fn, (int)C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    PartialArgs pa = r.pa;
+    void *args[] = {&kmap, &vmap, &pa};
+    return launch_pdl(fn, dim3(pa.n_kv_head * pa.qgroups, pa.n_splits, r.n_seq), dim3(C::THREADS),
+                      C::SMEM_BYTES, r.stream, args);
+}
+
 // The cluster-fused tcgen05 kernel: partial and combine in one launch, o written directly.
 template <int HD, int G, typename KV>
 cudaError_t launch_fused_umma(const LaunchRequest &r)
@@ -218,6 +239,9 @@ cudaError_t launch_for_hd(const LaunchRequest &r)
                 if (r.variant == kVariantUmma) {
                     if constexpr (HD == 128 || HD == 256) e = launch_partial_umma<HD, kMqHeads, KV, true>(r);
                     else return cudaErrorInvalidValue;
+                } else if (r.variant == kVariantTile) {
+                    if constexpr (HD == 128) e = launch_partial_tile_mq<HD, KV>(r);
+                    else return cudaErrorInvalidValue;
                 } else {
                     e = launch_partial<TcMqCfg<HD, KV>, HD, kMqHeads, KV>(r);
                 }
@@ -277,12 +301,13 @@ KernelInfo kernel_info_for_hd(int group, int variant, bool multi)
     }
     if (variant == kVariantTile) {
         if constexpr (HD == 128 || HD == 256) {
-            if (multi) return k;
+            if (multi && HD != 128) return k;   // several query rows: head_dim 128 only
             using C = TileCfg<HD, 8, __half>;   // the shapes do not depend on the group
             k.tile_rows = C::TILE;
             k.granule = C::GRANULE;
             k.stages = 1;
-            k.blocks_per_sm = (int)(233472u / (C::SMEM_BYTES + 1024u));
+            const uint32_t smem = multi ? TileCfg<128, kMqHeads, __half, true>::SMEM_BYTES : C::SMEM_BYTES;
+            k.blocks_per_sm = (int)(233472u / (smem + 1024u));
             k.max_chunk = C::TILE;
             k.available = true;
         }

@@ -37,6 +37,7 @@
 
 #include "attn_device.cuh"
 #include "attn_warp_tc.cuh"
+#include "attn_warp_tcmq.cuh"
 
 namespace attn {
 
@@ -52,9 +53,14 @@ __device__ __forceinline__ void ldsm_a16(uint32_t (&a)[4], const uint8_t *base, 
     ldsm_x4(a, base + tile_unit_offset<COLS, 16>(row, 2 * kk + (i >> 1)));
 }
 
-template <int HD, int G, typename KV>
+// MQ = false: one query row, the G heads of the group in slots 0..G-1, one
+// 16-row Q tile (hi parts in rows 0-7, lo parts in 8-15). MQ = true: several
+// causal query rows, 16 (query row, head) slots per block, a 16-row hi tile
+// and a 16-row lo tile (attn_warp_tcmq.cuh), and P as a hi and a lo tile.
+template <int HD, int G, typename KV, bool MQ = false>
 struct TileCfg {
     static_assert(HD == 128 || HD == 256, "the one-tile kernel is built for head_dim 128 and 256");
+    static_assert(!MQ || HD == 128, "several query rows: head_dim 128 (two blocks per SM would not fit at 256)");
     static constexpr int TILE = HD == 256 ? 96 : 128;   // rows per block
     static constexpr int MINB = HD == 256 ? 2 : 3;      // resident blocks per SM
     // warps: S rows and O dimensions split NW ways (8 warps at head_dim 128 were measured
@@ -70,22 +76,25 @@ struct TileCfg {
     static constexpr int KO = TILE / 16;                // O k-steps
     static constexpr int NCH = HD / 64;                 // 128-byte column chunks per row
     static constexpr int GRANULE = TILE;                // count-mode chunks are whole tiles
-    static constexpr bool Q_REGS = KS <= 8;             // Q fragments held in registers
-    using QStage = TcWarp<HD, G, NW, KV>;
+    static constexpr bool Q_REGS = KS <= 8 && !MQ;      // Q fragments held in registers
+    using QStage = typename std::conditional<MQ, TcWarpMQ<HD, 16, NW, KV>, TcWarp<HD, G, NW, KV>>::type;
+    static constexpr uint32_t Q_AREA = (MQ ? 2u : 1u) * QStage::QT_BYTES;   // Q tiles, before the scales
     static constexpr uint32_t TILE_BYTES = (uint32_t)TILE * HD * 2;
     static constexpr uint32_t OFF_K = 0;
     static constexpr uint32_t OFF_V = TILE_BYTES;
     static constexpr uint32_t OFF_Q = 2 * TILE_BYTES;   // Q tile, then per-head scales
     static constexpr uint32_t OFF_P = OFF_Q;            // P tile over the Q tile once S is done
-    // P tile: 16 rows of TILE elements in 128-byte swizzled chunks of 64
-    static constexpr uint32_t P_BYTES = 16u * ((TILE + 63) / 64 * 64) * 2;
-    // maxima and sums per 8-row group (the several-split kernel) or per warp
-    static constexpr int NRED = TILE / 8 > NW ? TILE / 8 : NW;
-    static constexpr uint32_t OFF_RED = OFF_Q + (QStage::EXTRA_BYTES + 15) / 16 * 16;   // [2][NRED][8] floats
-    static constexpr uint32_t OFF_BAR = OFF_RED + 2 * NRED * 8 * 4;                     // 2 mbarriers, flags
+    // P tile(s): 16 rows of TILE elements in 128-byte swizzled chunks of 64 (MQ: hi, then lo)
+    static constexpr uint32_t P_TILE = 16u * ((TILE + 63) / 64 * 64) * 2;
+    static constexpr uint32_t P_BYTES = (MQ ? 2u : 1u) * P_TILE;
+    // maxima and sums: per warp, or per 8-row group (the several-split kernel); RSL slots each
+    static constexpr int NRED = MQ ? NW : (TILE / 8 > NW ? TILE / 8 : NW);
+    static constexpr int RSL = MQ ? 16 : 8;
+    static constexpr uint32_t OFF_RED = OFF_Q + (QStage::EXTRA_BYTES + 15) / 16 * 16;   // [2][NRED][RSL] floats
+    static constexpr uint32_t OFF_BAR = OFF_RED + 2 * NRED * RSL * 4;                   // 2 mbarriers, flags
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 2 * 8 + 16 + 1024;                 // + alignment slack
     static constexpr float OFF = 7.f;                   // p headroom: p <= 2^OFF
-    static_assert(P_BYTES <= QStage::QT_BYTES, "the P tile must not reach the per-head scales");
+    static_assert(P_BYTES <= Q_AREA, "the P tile must not reach the per-head scales");
     static_assert(TILE % 32 == 0 && WR % 8 == 0 && DW % 16 == 0, "fragment shapes");
     static_assert((TILE * 128) % 1024 == 0, "swizzled chunks stay 1024-aligned");
     static_assert(MINB * (SMEM_BYTES + 1024) <= 233472u, "resident blocks per SM");
@@ -190,7 +199,7 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + Cfg::OFF_BAR);    // [0] K landed, [1] V landed
     volatile int *flags = reinterpret_cast<volatile int *>(bar + 2);     // [0] abort
     float *red_m = reinterpret_cast<float *>(smem + Cfg::OFF_RED);      // [NW][8] warp maxima
-    float *red_l = red_m + Cfg::NRED * 8;                               // [NW][8] warp sums
+    float *red_l = red_m + Cfg::NRED * Cfg::RSL;                        // [NW][8] warp sums
 
     const int hk = blockIdx.x, sp = blockIdx.y, s = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -383,7 +392,7 @@ attn_split_partial_tile_ms(const __grid_constant__ CUtensorMap kmap, const __gri
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + Cfg::OFF_BAR);    // [0] K landed, [1] V landed
     volatile int *flags = reinterpret_cast<volatile int *>(bar + 2);     // [0] abort
     float *red_m = reinterpret_cast<float *>(smem + Cfg::OFF_RED);      // [TILE / 8][8] group maxima
-    float *red_l = red_m + Cfg::NRED * 8;                               // [TILE / 8][8] group sums
+    float *red_l = red_m + Cfg::NRED * Cfg::RSL;                        // [TILE / 8][8] group sums
 
     const int hk = blockIdx.x, b = blockIdx.y, s = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -568,6 +577,247 @@ attn_split_partial_tile_ms(const __grid_constant__ CUtensorMap kmap, const __gri
                 for (int k = 0; k < GPS; ++k) L += red_l[(j * GPS + k) * 8 + gg];
                 a.ws_ml[((size_t)s * heads + (size_t)hk * G + gg) * P + sp] =
                     make_float2(M == -INFINITY ? M : M - Cfg::OFF, L);
+            }
+        }
+    } else if (tid == 0) {
+        (void)mbar_wait_bounded(bar + 0, 0);
+        (void)mbar_wait_bounded(bar + 1, 0);
+    }
+}
+
+// Several causal query rows (TileCfg<HD, 16, KV, true>): block (KV head, query
+// group qg, split sp) serves 16 (query row, head) slots of one KV head from one
+// tile. The slots' q is a hi and a lo Q tile; S accumulates the hi and the lo
+// MMA of each step into one fragment, so a thread holds slots g and g + 8 of
+// its rows directly. Slot i (query row t) sees cache rows [0, nkv - n_q + t];
+// a slot that sees no row of the split writes (-inf, 0). P is a hi and a lo
+// tile over the Q tiles, and O = P · V accumulates both into one fragment.
+template <class Cfg, int HD, typename KV>
+__global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
+attn_split_partial_tile_mq(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                           const PartialArgs a)
+{
+    constexpr int TILE = Cfg::TILE, NS = Cfg::NS, NO = Cfg::NO, KS = Cfg::KS, KO = Cfg::KO;
+    using QS = typename Cfg::QStage;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + Cfg::OFF_BAR);    // [0] K landed, [1] V landed
+    volatile int *flags = reinterpret_cast<volatile int *>(bar + 2);     // [0] abort
+    float *red_m = reinterpret_cast<float *>(smem + Cfg::OFF_RED);      // [NW][16] warp maxima
+    float *red_l = red_m + Cfg::NRED * Cfg::RSL;                        // [NW][16] warp sums
+
+    const int hk = blockIdx.x / a.qgroups, qg = blockIdx.x % a.qgroups, sp = blockIdx.y, s = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int P = a.n_splits;
+    const size_t heads = (size_t)a.n_q * a.n_head;         // partial heads per sequence
+
+    const bool stable = a.kv_stable != 0;
+    if (tid == 32) {
+        // q of this block's slots into L2 (query rows t0..t1 of the group's heads)
+        const int G = a.group;
+        const int t0 = qg * 16 / G, t1 = min(a.n_q - 1, (qg * 16 + 15) / G);
+        for (int t = t0; t <= t1; ++t)
+            prefetch_l2(a.q + (((size_t)s * a.n_q + t) * a.n_head + (size_t)hk * G) * HD,
+                        (uint32_t)(G * HD * sizeof(float)));
+    }
+    if (!stable) pdl_wait();
+    pdl_launch_dependents();
+
+    bool pos_ok;
+    const int64_t nkv = rows_attended(a, s, sp == 0 && blockIdx.x == 0 && tid == 0, &pos_ok);
+    int64_t lo, hi;
+    split_range(nkv, sp, P, a.split_len, Cfg::GRANULE, lo, hi);
+    if (lo >= hi) {
+        if (stable) pdl_wait();
+        if (tid < 16) {
+            const int hp = QS::slot_head(a, hk, qg, tid);
+            if (hp >= 0) a.ws_ml[((size_t)s * heads + hp) * P + sp] = make_float2(-INFINITY, 0.f);
+        }
+        return;
+    }
+    const int n = (int)(hi - lo);
+    const int row_first = (int)(hi - TILE);
+
+    if (tid == 0) {
+        mbar_init(bar + 0, 1);
+        mbar_init(bar + 1, 1);
+        flags[0] = 0;
+        fence_barrier_init();
+        prefetch_tensormap(&kmap);
+        prefetch_tensormap(&vmap);
+        mbar_arrive_expect_tx(bar + 0, Cfg::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < Cfg::NCH; ++c)
+            tma_load_4d(smem + Cfg::OFF_K + c * (Cfg::TILE_BYTES / Cfg::NCH), &kmap, bar + 0, c * 64, hk, row_first, s);
+        mbar_arrive_expect_tx(bar + 1, Cfg::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < Cfg::NCH; ++c)
+            tma_load_4d(smem + Cfg::OFF_V + c * (Cfg::TILE_BYTES / Cfg::NCH), &vmap, bar + 1, c * 64, hk, row_first, s);
+    }
+
+    if (stable) pdl_wait();
+    QS::template prepare<Cfg::THREADS>(smem + Cfg::OFF_Q, a, s, hk, qg, tid);
+    __syncthreads();
+
+    const uint8_t *qhi = smem + Cfg::OFF_Q, *qlo = qhi + QS::QT_BYTES;
+    const float *inv = reinterpret_cast<const float *>(smem + Cfg::OFF_Q + 2 * QS::QT_BYTES);
+    const int *qrow = reinterpret_cast<const int *>(inv + 16);
+    const int g = lane >> 2, t = lane & 3, i8 = lane >> 3;
+    // this thread's slots g and g + 8: scale, and the last cache row each may see
+    float isc[2];
+    int64_t last[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        isc[k] = inv[g + 8 * k];
+        last[k] = qrow[g + 8 * k] >= 0 ? nkv - a.n_q + qrow[g + 8 * k] : -1;
+    }
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar + 0, 0));
+    if (!ok && lane == 0) { flags[0] = 1; atomicOr(a.err, kErrPipelineTimeout); }
+
+    // ---- a3: S for rows r0 .. r0 + WR - 1, hi and lo q into one accumulator ----
+    const int r0 = warp * Cfg::WR;
+    float sc[NS][2][2];                       // [n-tile][slot g, g + 8][row 2t, 2t + 1]
+    {
+        float c[2][NS][4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int j = 0; j < NS; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) c[e][j][i] = 0.f;
+        if (ok) {
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                uint32_t ah[4], al[4];
+                ldsm_a16<HD>(ah, qhi, kk, lane);
+                ldsm_a16<HD>(al, qlo, kk, lane);
+#pragma unroll
+                for (int j = 0; j < NS; j += 2) {
+                    uint32_t b[4];
+                    const int krow = r0 + 8 * j + (i8 >> 1) * 8 + (lane & 7);
+                    ldsm_x4(b, smem + Cfg::OFF_K + tile_unit_offset<HD, TILE>(krow, 2 * kk + (i8 & 1)));
+                    mma_16816<KV>(c[kk & 1][j], ah, b[0], b[1]);
+                    mma_16816<KV>(c[kk & 1][j], al, b[0], b[1]);
+                    mma_16816<KV>(c[kk & 1][j + 1], ah, b[2], b[3]);
+                    mma_16816<KV>(c[kk & 1][j + 1], al, b[2], b[3]);
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < NS; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int r = r0 + 8 * j + 2 * t + e;
+                const int64_t row = hi - TILE + r;              // the cache row
+                const bool in_split = r >= TILE - n;
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const float v = (c[0][j][2 * k + e] + c[1][j][2 * k + e]) * isc[k];
+                    sc[j][k][e] = in_split && row <= last[k] ? v : -INFINITY;
+                }
+            }
+    }
+    // ---- a4: each slot's maximum over the block ----
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        float m = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < NS; ++j) m = fmaxf(m, fmaxf(sc[j][k][0], sc[j][k][1]));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        if (t == 0) red_m[warp * 16 + g + 8 * k] = m;
+    }
+    __syncthreads();                          // the maxima are in; S is done, so the Q tiles are dead
+    float base[2];
+    bool none[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        float M = red_m[g + 8 * k];
+#pragma unroll
+        for (int w = 1; w < Cfg::NW; ++w) M = fmaxf(M, red_m[w * 16 + g + 8 * k]);
+        none[k] = M == -INFINITY;             // the slot sees no row of this split
+        base[k] = M - Cfg::OFF;
+    }
+    {
+        uint8_t *phi = smem + Cfg::OFF_P, *plo = phi + Cfg::P_TILE;
+        float lsum[2] = {0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < NS; ++j) {
+            const int r = r0 + 8 * j;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const float p0 = none[k] ? 0.f : ex2(sc[j][k][0] - base[k]);
+                const float p1 = none[k] ? 0.f : ex2(sc[j][k][1] - base[k]);
+                lsum[k] += p0 + p1;
+                const uint32_t hw = float2_to_kv2<KV>(p0, p1);
+                const float2 f = kv2_to_float2<KV>(hw);
+                const uint32_t lw = float2_to_kv2<KV>(p0 - f.x, p1 - f.y);
+                const uint32_t off = tile_unit_offset<TILE, 16>(g + 8 * k, r >> 3) + 4 * t;
+                *reinterpret_cast<uint32_t *>(phi + off) = hw;
+                *reinterpret_cast<uint32_t *>(plo + off) = lw;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            float l = lsum[k];
+            l += __shfl_xor_sync(0xffffffffu, l, 1);
+            l += __shfl_xor_sync(0xffffffffu, l, 2);
+            if (t == 0) red_l[warp * 16 + g + 8 * k] = l;
+        }
+    }
+    bool vok = ok;
+    if (vok) vok = __all_sync(0xffffffffu, mbar_wait_bounded(bar + 1, 0));
+    if (ok && !vok && lane == 0) { flags[0] = 1; atomicOr(a.err, kErrPipelineTimeout); }
+    __syncthreads();                          // P and the sums are in; every V wait is done
+    // ---- a5: O = P · V for dimensions d0 .. d0 + DW - 1, hi and lo P into one accumulator ----
+    const int d0 = warp * Cfg::DW;
+    const bool abort = flags[0] != 0;
+    if (!abort) {
+        float o[2][NO][4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int j = 0; j < NO; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) o[e][j][i] = 0.f;
+        const uint8_t *phi = smem + Cfg::OFF_P, *plo = phi + Cfg::P_TILE;
+#pragma unroll
+        for (int kk = 0; kk < KO; ++kk) {
+            uint32_t ah[4], al[4];
+            ldsm_a16<TILE>(ah, phi, kk, lane);
+            ldsm_a16<TILE>(al, plo, kk, lane);
+            const int vrow = 16 * kk + (i8 & 1) * 8 + (lane & 7);
+#pragma unroll
+            for (int j = 0; j < NO; j += 2) {
+                uint32_t b[4];
+                ldsm_x4_trans(b, smem + Cfg::OFF_V + tile_unit_offset<HD, TILE>(vrow, (d0 >> 3) + j + (i8 >> 1)));
+                mma_16816<KV>(o[kk & 1][j], ah, b[0], b[1]);
+                mma_16816<KV>(o[kk & 1][j], al, b[0], b[1]);
+                mma_16816<KV>(o[kk & 1][j + 1], ah, b[2], b[3]);
+                mma_16816<KV>(o[kk & 1][j + 1], al, b[2], b[3]);
+            }
+        }
+        // ---- a6: oc of both slots for these dimensions; (mx, S) per slot ----
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int hp = QS::slot_head(a, hk, qg, g + 8 * k);
+            if (hp < 0) continue;
+            float *dst = a.ws_o + (((size_t)s * heads + hp) * P + sp) * HD + d0 + 2 * t;
+#pragma unroll
+            for (int j = 0; j < NO; ++j)
+                *reinterpret_cast<float2 *>(dst + 8 * j) =
+                    make_float2(o[0][j][2 * k] + o[1][j][2 * k], o[0][j][2 * k + 1] + o[1][j][2 * k + 1]);
+        }
+        if (warp == 0 && t == 0) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int hp = QS::slot_head(a, hk, qg, g + 8 * k);
+                if (hp < 0) continue;
+                float L = 0.f;
+#pragma unroll
+                for (int w = 0; w < Cfg::NW; ++w) L += red_l[w * 16 + g + 8 * k];
+                a.ws_ml[((size_t)s * heads + hp) * P + sp] =
+                    make_float2(none[k] ? -INFINITY : base[k], none[k] ? 0.f : L);
             }
         }
     } else if (tid == 0) {

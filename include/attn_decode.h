@@ -101,8 +101,10 @@ typedef enum {
                                  over four warps, one block-wide maximum, O = P·V split by head
                                  dimension over the warps (no merge of warp states). One tile of
                                  T rows per block (T = 128; 96 at head_dim 256); head_dim 128 or
-                                 256, one query row (ATTN_ERR_UNSUPPORTED otherwise). Every split
-                                 must fit one tile, as for ATTN_VARIANT_TCGEN05. By block length
+                                 256 with one query row, head_dim 128 with several (16 (query
+                                 row, head) pairs per block); ATTN_ERR_UNSUPPORTED otherwise.
+                                 Every split must fit one tile, as for ATTN_VARIANT_TCGEN05. By
+                                 block length, for one query row,
                                  with split_len a multiple of 16 that divides T, one block serves
                                  T / split_len consecutive splits from one tile (cache rows of
                                  that tile past nkv are then read -- all below cap -- but never
@@ -315,15 +317,18 @@ int attn_split_heuristic_ex(int n_seq, int n_q, int n_head, int n_kv_head, int h
 
 /*
  * attn_resolve_variant -- which partial kernel a call with these arguments and
- * n_splits = 0 runs: ATTN_VARIANT_SIMT, ATTN_VARIANT_TC or ATTN_VARIANT_TCGEN05
- * or ATTN_VARIANT_TCGEN05_CLUSTER (0 for an invalid shape or variant). An
- * explicit variant is returned as is;
- * ATTN_VARIANT_AUTO picks the tcgen05 kernel for a short call -- head_dim 128
- * or 256; one query row, or n_q * group <= 16 (a KV head's (row, head) pairs
- * in one block); cap > 0; and the heuristic's splits, one tile each, in one
- * wave of its blocks (3 per SM at head_dim 128, 2 at 256 for one query row,
- * fewer for several) -- and otherwise the mma.sync tensor-core kernel
- * (head_dim % 16 == 0) or the CUDA-core kernel. With ATTN_KV_STABLE in
+ * n_splits = 0 runs: ATTN_VARIANT_SIMT, ATTN_VARIANT_TC, ATTN_VARIANT_TCGEN05,
+ * ATTN_VARIANT_TCGEN05_CLUSTER or ATTN_VARIANT_TC_TILE (0 for an invalid shape
+ * or variant). An explicit variant is returned as is where it supports the
+ * shape. ATTN_VARIANT_AUTO picks a one-tile kernel for a short call -- cap > 0
+ * and the heuristic's splits, one tile each, in one wave of its blocks: the
+ * one-tile mma.sync kernel (ATTN_VARIANT_TC_TILE; 3 blocks per SM at head_dim
+ * 128, 2 at 256) for one query row at head_dim 128 or 256 and for several at
+ * 128 (ceil(n_q * group / 16) blocks per split and KV head); else tcgen05 for
+ * several query rows at head_dim 256 when n_q * group <= 16 (a KV head's (row,
+ * head) pairs in one block, 1 block per SM) -- and otherwise the streaming
+ * mma.sync tensor-core kernel (head_dim % 16 == 0) or the CUDA-core kernel.
+ * With ATTN_KV_STABLE in
  * variant the split count follows the flagged heuristic. With explicit splits
  * that leave a split longer than one tile, or too many blocks for one wave,
  * attn_decode_ex keeps the mma.sync kernel instead. Host only; sm_count <= 0

@@ -134,9 +134,10 @@ def test_split_heuristic_for_flagged_calls(lib):
     # head; at one block per SM a block would hold 431 rows (not a short call), so
     # two blocks per SM: 8 x 37 blocks of 224 rows
     assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_STABLE, n_q=4) == 37
-    assert h(1, 28, 4, 128, 2048, 152, pkg.ATTN_KV_STABLE, n_q=4) == 19    # short: one per SM
-    # 2 rows x 7 heads = 14 pairs: one group, so variant 0 runs the tcgen05 kernel with one
-    # 128-row tile per split; the mma.sync kernel keeps its ring-sized blocks
+    # short: one 128-row tile per split on the one-tile kernel, 16 x 4 x 2 blocks
+    assert h(1, 28, 4, 128, 2048, 152, pkg.ATTN_KV_STABLE, n_q=4) == 16
+    # 2 rows x 7 heads = 14 pairs: one group, so variant 0 runs the one-tile kernel with one
+    # 128-row tile per split; the streaming mma.sync kernel keeps its ring-sized blocks
     assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_STABLE, n_q=2) == 64
     assert h(1, 28, 4, 128, 8192, 152, TC | S, n_q=2) == 43
     assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_VARIANT_SIMT, n_q=2) == 0  # tensor cores only
@@ -151,8 +152,8 @@ def test_resolved_variant(lib):
     S, B = pkg.ATTN_KV_STABLE, pkg.ATTN_KV_BF16
     T5, TC, SI = pkg.ATTN_VARIANT_TCGEN05, pkg.ATTN_VARIANT_TC, pkg.ATTN_VARIANT_SIMT
     VT = pkg.ATTN_VARIANT_TC_TILE
-    # variant 0: the one-tile mma.sync kernel for a short call of one query row;
-    # the tcgen05 kernel for several query rows
+    # variant 0: the one-tile mma.sync kernel for a short call (several query rows at
+    # head_dim 128); the tcgen05 kernel for several query rows at head_dim 256
     assert r(1, 1, 28, 4, 128, 8192, 152, 0) == VT
     assert r(1, 1, 28, 4, 128, 8192, 152, S | B) == VT
     assert r(1, 1, 8, 2, 128, 40, 152, 0) == VT
@@ -165,10 +166,13 @@ def test_resolved_variant(lib):
     # 64 and an unknown capacity; CUDA cores for head_dim 8
     assert r(1, 1, 64, 8, 128, 131072, 152, 0) == TC
     assert r(32, 1, 32, 8, 128, 32768, 152, 0) == TC
-    assert r(1, 4, 28, 4, 128, 8192, 152, 0) == TC                 # 2 query groups per KV head
-    assert r(1, 2, 28, 4, 128, 8192, 152, 0) == T5                 # 14 slots: one group
-    assert r(1, 2, 28, 4, 128, 8192, 152, S) == T5
+    assert r(1, 4, 28, 4, 128, 8192, 152, 0) == TC                 # 2 x 4 x 64 blocks > 3 x 152
+    assert r(1, 2, 28, 4, 128, 8192, 152, 0) == VT                 # 14 slots: one group
+    assert r(1, 2, 28, 4, 128, 8192, 152, S) == VT
     assert r(1, 3, 28, 4, 128, 8192, 152, 0) == TC                 # 21 slots
+    assert r(1, 4, 28, 4, 128, 2048, 152, 0) == VT                 # 2 x 4 x 16 blocks
+    assert r(1, 2, 28, 4, 128, 57 * 128, 152, 0) == VT             # 4 x 114 blocks, 3 per SM
+    assert r(1, 2, 28, 4, 128, 114 * 128 + 1, 152, 0) == TC        # a second wave
     # 16 slots at head_dim 256: one block per SM, so 2 x 88 blocks are a second wave
     assert r(1, 2, 16, 2, 256, 8400, 152, 0) == TC
     assert r(1, 2, 16, 2, 256, 76 * 96, 152, 0) == T5
@@ -191,7 +195,8 @@ def test_resolved_variant(lib):
     assert r(1, 1, 8, 2, 64, 1024, 152, T5) == 0
     assert r(1, 2, 8, 2, 128, 1024, 152, T5) == T5                         # several query rows too
     assert r(1, 1, 28, 4, 256, 8192, 152, VT) == VT                        # explicit one-tile kernel
-    assert r(1, 2, 8, 2, 128, 1024, 152, VT) == 0                          # one query row only
+    assert r(1, 2, 8, 2, 128, 1024, 152, VT) == VT                         # several rows: hd 128
+    assert r(1, 2, 8, 2, 256, 1024, 152, VT) == 0
     assert r(1, 1, 8, 2, 64, 1024, 152, VT) == 0
     assert r(1, 1, 28, 5, 128, 8192, 152, 0) == 0
 
@@ -328,8 +333,8 @@ def test_decode_attention_checks_its_tensors_before_any_call():
 def test_tcgen05_choice_keeps_its_limits(lib):
     """Wherever variant 0 names a one-tile kernel (tcgen05, or the one-tile
     mma.sync kernel), the planned splits cover the capacity one tile each and
-    fit one wave of its blocks; the mma.sync form only for one query row;
-    several query rows only when a KV head's pairs fit one 16-slot block.
+    fit one wave of its blocks; several query rows on the mma.sync form only at
+    head_dim 128, on tcgen05 only when a KV head's pairs fit one 16-slot block.
     Seeded random shapes."""
     rng = np.random.default_rng(12)
     T5, VT = pkg.ATTN_VARIANT_TCGEN05, pkg.ATTN_VARIANT_TC_TILE
@@ -348,13 +353,17 @@ def test_tcgen05_choice_keeps_its_limits(lib):
         v = pkg.attn_resolve_variant(n_seq, n_q, G * n_kv, n_kv, hd, cap, sms, flags)
         P = pkg.attn_split_heuristic_ex(n_seq, n_q, G * n_kv, n_kv, hd, cap, sms, flags)
         assert v in (pkg.ATTN_VARIANT_TC, T5, VT) and P > 0
-        if v == VT:
-            assert n_q == 1
-        elif v != T5:
+        if v not in (T5, VT):
             continue
         seen.add((hd, n_q > 1))
         assert hd in (128, 256)
-        assert n_q == 1 or n_q * G <= 16
         assert P * tile[hd] >= cap
-        assert P * n_kv * n_seq <= sms * per_sm[(hd, n_q > 1)]
+        if v == VT:
+            # 16 (row, head) slots per block; 3 blocks per SM at head_dim 128, 2 at 256
+            assert n_q == 1 or hd == 128
+            qg = 1 if n_q == 1 else -(-n_q * G // 16)
+            assert P * n_kv * n_seq * qg <= sms * (3 if hd == 128 else 2)
+        else:
+            assert n_q == 1 or n_q * G <= 16
+            assert P * n_kv * n_seq <= sms * per_sm[(hd, n_q > 1)]
     assert seen == {(128, False), (256, False), (128, True), (256, True)}

@@ -44,14 +44,18 @@ def _run(pkg, case, n_q, n_head, n_kv, hd, cap, scale, P=0, blk=0, variant=0):
     return out.cpu().numpy()
 
 
-# 2 forces the mma.sync multi-query kernel, 3 the tcgen05 kernel (16 slots per block);
-# variant 0 takes the tcgen05 kernel where a KV head's n_q x G slots fit one block
-@pytest.mark.parametrize("variant", [0, 2, 3])
+# 2 forces the mma.sync streaming multi-query kernel, 3 the tcgen05 kernel and 5 the
+# one-tile mma.sync kernel (16 slots per block each); variant 0 takes the one-tile kernel
+# at head_dim 128 where its blocks fit one wave, else tcgen05 where a KV head's n_q x G
+# slots fit one block, else the streaming kernel
+@pytest.mark.parametrize("variant", [0, 2, 3, 5])
 @pytest.mark.parametrize("hd", [64, 128, 256])
 @pytest.mark.parametrize("kv", ["f16", "bf16"])
 def test_multi_query_shapes(pkg, hd, kv, variant):
     if variant == 3 and hd == 64:
         pytest.skip("the tcgen05 kernel is built for head_dim 128 and 256")
+    if variant == 5 and hd != 128:
+        pytest.skip("the one-tile kernel takes several query rows at head_dim 128")
     flag = (pkg.ATTN_KV_BF16 if kv == "bf16" else 0) | variant
     for (G, n_q) in ((1, 2), (4, 3), (7, 2), (8, 2), (7, 4), (2, 9)):
         n_kv, cap = 2, 500
@@ -64,11 +68,11 @@ def test_multi_query_shapes(pkg, hd, kv, variant):
         assert_close(got, ref, "multi hd%d G%d n_q%d %s variant %d" % (hd, G, n_q, kv, variant))
 
 
-@pytest.mark.parametrize("variant", [0, 3])
+@pytest.mark.parametrize("variant", [0, 3, 5])
 def test_multi_query_short_contexts_and_boundaries(pkg, variant):
     n_q, n_head, n_kv, hd, cap = 4, 28, 4, 128, 1024
     scale = 1 / math.sqrt(hd)
-    splits = ((0, 0), (7, 0), (17, 64)) if variant == 0 else ((0, 0), (8, 0), (17, 64), (9, 128))
+    splits = ((0, 0), (7, 0), (17, 64)) if variant == 0 else ((0, 0), (8, 0), (17, 64), (9, 128))   # tile 128
     for nkv in (1, 2, 3, 4, 5, 16, 17, 63, 64, 65, 112, 113, 127, 128, 129, 1000, 1024):
         case = _case(500 + nkv, 1, n_q, n_head, n_kv, hd, cap, (nkv,))
         for P, blk in splits:
@@ -80,7 +84,7 @@ def test_multi_query_short_contexts_and_boundaries(pkg, variant):
                 assert np.all(got[0, :n_q - nkv] == 0)
 
 
-@pytest.mark.parametrize("variant", [0, 3])
+@pytest.mark.parametrize("variant", [0, 3, 5])
 def test_multi_query_ragged_batch_and_large_spread(pkg, variant):
     n_q, n_head, n_kv, hd, cap = 3, 32, 8, 128, 900
     ctx = (2, 900, 0, 17, 450, 899, 64, 333)
@@ -119,12 +123,18 @@ def test_multi_query_rejections(pkg):
                                q2.data_ptr(), 1, 2, 4, 2, 128, 1.0, 16, 0, 0, pkg.ATTN_VARIANT_SIMT,
                                None, 0, None)
     assert st == pkg.ATTN_ERR_UNSUPPORTED
+    q3 = torch.zeros(1, 2, 4, 256, device="cuda")
+    kv3 = torch.zeros(1, 16, 2, 256, dtype=torch.float16, device="cuda")
+    st = lib.attn_decode_multi(q3.data_ptr(), kv3.data_ptr(), kv3.data_ptr(), pos.data_ptr(),
+                               q3.data_ptr(), 1, 2, 4, 2, 256, 1.0, 16, 0, 0, pkg.ATTN_VARIANT_TC_TILE,
+                               None, 0, None)
+    assert st == pkg.ATTN_ERR_UNSUPPORTED                     # one-tile kernel, several rows: hd 128
     st = lib.attn_decode_multi(q2.data_ptr(), kv2.data_ptr(), kv2.data_ptr(), pos.data_ptr(),
                                q2.data_ptr(), 1, 0, 4, 2, 128, 1.0, 16, 0, 0, 0, None, 0, None)
     assert st == pkg.ATTN_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("variant", [0, 3])
+@pytest.mark.parametrize("variant", [0, 3, 5])
 @pytest.mark.parametrize("n_q, G, nkv", [(64, 4, 300), (50, 8, 20), (33, 1, 700), (128, 7, 1000)])
 def test_many_query_rows(pkg, n_q, G, nkv, variant):
     """Prefill-sized chunks: many query groups per KV head (up to 56 blocks

@@ -226,16 +226,16 @@ def test_arguments_that_leave_a_split_larger_than_a_tile(pkg):
     with pytest.raises(pkg.AttnError) as ei:
         run_decode(pkg, c256, 8, 2, 256, 1024, 0.1, variant=VT, n_splits=10)   # 10 * 96 < 1024
     assert ei.value.status == pkg.ATTN_ERR_INVALID_ARG
-    # head_dim 64 is not built for this kernel, nor are several query rows
+    # head_dim 64 is not built for this kernel, nor are several query rows at head_dim 256
     c64 = to_device(make_case(6001, 1, 8, 2, 64, 256, (200,)))
     with pytest.raises(pkg.AttnError) as ei:
         run_decode(pkg, c64, 8, 2, 64, 256, 0.1, variant=VT)
     assert ei.value.status == pkg.ATTN_ERR_UNSUPPORTED
-    q2 = torch.zeros((1, 2, 8, 128), device="cuda")
+    q2 = torch.zeros((1, 2, 8, 256), device="cuda")
     out = torch.empty_like(q2)
     with pytest.raises(pkg.AttnError) as ei:
-        pkg.attn_decode_multi(q2, case["k"], case["v"], case["positions"], out, 1, 2, 8, 2, 128,
-                              0.1, 1024, n_splits=8, variant=VT)
+        pkg.attn_decode_multi(q2, c256["k"], c256["v"], c256["positions"], out, 1, 2, 8, 2, 256,
+                              0.1, 1024, n_splits=11, variant=VT)
     assert ei.value.status == pkg.ATTN_ERR_UNSUPPORTED
 
 
@@ -311,3 +311,50 @@ def test_full_long_workload_block_32(pkg):
     v, P, _ = pkg.attn_plan_call(1, 1, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0, 32, 0)
     assert v == VT and P == -(-w.cap // 32)
     _check(pkg, lay, w.n_head, w.n_kv_head, w.cap, "long blk 32", hd=w.head_dim, split_len=32)
+
+
+# ---- several causal query rows (head_dim 128, 16 (row, head) slots per block) ----
+
+@pytest.mark.parametrize("n_q", [2, 4])
+def test_several_query_rows_full_7b(pkg, n_q):
+    """The 7b layer at full size with n_q causal rows per sequence: row i sees
+    nkv - n_q + 1 + i cache rows, so the last row of a tile is masked for every
+    row but the last (one tile per split)."""
+    import torch
+    w = syn.WORKLOADS["7b"]
+    lay = syn.make_layer(w)
+    rng = np.random.Generator(np.random.PCG64([7007, n_q]))
+    q = rng.standard_normal((1, n_q, w.n_head, w.head_dim), dtype=np.float32)
+    P = w.cap // TILE[128]
+    scale = 1 / math.sqrt(w.head_dim)
+    for ctx in (w.cap, 3001):
+        pos = np.array([ctx - 1], np.int32)
+        dev = to_device(dict(lay, q=q, positions=pos))
+        out = torch.full_like(dev["q"], float("nan"))
+        pkg.attn_decode_multi(dev["q"], dev["k"], dev["v"], dev["positions"], out, 1, n_q, w.n_head,
+                              w.n_kv_head, w.head_dim, scale, w.cap, n_splits=P, variant=VT)
+        ref = oracle.attn_decode_multi(q, lay["k"], lay["v"], pos, n_q, w.n_head, w.n_kv_head,
+                                       w.head_dim, w.cap, scale, n_threads=8)
+        assert_close(out.cpu().numpy(), ref, "7b n_q=%d ctx %d" % (n_q, ctx))
+
+
+@pytest.mark.parametrize("n_q,G", [(2, 8), (3, 5), (5, 4), (16, 1)])
+def test_several_query_rows_nan_past_each_row(pkg, n_q, G):
+    """Ragged batch whose cache rows past each sequence's end hold NaN: every
+    row's masked positions are read by the tile but must not reach its result."""
+    import torch
+    n_kv, hd, cap = 2, 128, 700
+    n_head = G * n_kv
+    ctx = (1, 5, 130, 257, 700)
+    case = make_case(7100 + n_q, len(ctx), n_head, n_kv, hd, cap, ctx, fill=float("nan"))
+    rng = np.random.Generator(np.random.PCG64([7100, n_q]))
+    case["q"] = rng.standard_normal((len(ctx), n_q, n_head, hd), dtype=np.float32)
+    scale = 1 / math.sqrt(hd)
+    dev = to_device(case)
+    for P in (0, 6, 11):
+        out = torch.full_like(dev["q"], float("nan"))
+        pkg.attn_decode_multi(dev["q"], dev["k"], dev["v"], dev["positions"], out, len(ctx), n_q,
+                              n_head, n_kv, hd, scale, cap, n_splits=P, variant=VT)
+        ref = oracle.attn_decode_multi(case["q"], case["k"], case["v"], case["positions"], n_q,
+                                       n_head, n_kv, hd, cap, scale, n_threads=8)
+        assert_close(out.cpu().numpy(), ref, "n_q=%d G=%d P=%d" % (n_q, G, P))
