@@ -102,6 +102,10 @@ attn::KernelInfo kernel_info(int head_dim, int group, int variant, bool multi = 
 
 bool head_dim_supported(int hd) { return hd == 8 || hd == 64 || hd == 128 || hd == 256; }
 
+// The ATTN_VARIANT_* value that names an internal kernel form: the one-tile
+// kernel's 128-row tiles at head_dim 256 are the one-tile kernel.
+int public_variant(int v) { return v == attn::kVariantTileWide ? ATTN_VARIANT_TC_TILE : v; }
+
 // ATTN_VARIANT_AUTO, first choice: the mma.sync tensor-core kernel wherever it
 // is compiled (head_dim % 16 == 0); it was measured faster than the CUDA-core
 // kernel for every group size. head_dim 8 runs on CUDA cores.
@@ -206,6 +210,11 @@ int auto_short_kernel(int head_dim, int group, int n_q, int n_seq, int n_kv_head
         one_tile_fits(attn::kVariantTile, head_dim, group, n_q, n_seq, n_kv_head, cap, sm_count, n_splits,
                       split_len, kv_stable, ku))
         return attn::kVariantTile;
+    // splits of 97..128 rows at head_dim 256 (block length 128): 128-row tiles, one block per SM
+    if (n_q == 1 && head_dim == 256 &&
+        one_tile_fits(attn::kVariantTileWide, head_dim, group, n_q, n_seq, n_kv_head, cap, sm_count, n_splits,
+                      split_len, kv_stable, ku))
+        return attn::kVariantTileWide;
     if (one_tile_fits(attn::kVariantUmma, head_dim, group, n_q, n_seq, n_kv_head, cap, sm_count, n_splits,
                       split_len, kv_stable, ku))
         return attn::kVariantUmma;
@@ -302,6 +311,16 @@ attn_status finish_plan(DeviceState *ds, int n_seq, int n_head, int n_kv_head, i
                                : heuristic(n_seq, n_kv_head, pl.qgroups, cap_known ? cap : 0,
                                            ds->sm_count, pl.ki, pl.kv_stable != 0);
     if (split_len > 0 && (int64_t)P * split_len < cap) return ATTN_ERR_INVALID_ARG;
+    // the one-tile kernel at head_dim 256 takes splits longer than its 96-row tile
+    // in 128-row tiles
+    if (pl.variant == attn::kVariantTile && head_dim == 256 && n_q == 1 &&
+        (split_len > 0 ? split_len > pl.ki.max_chunk : (cap_known && (int64_t)P * pl.ki.max_chunk < cap))) {
+        const attn::KernelInfo kw = kernel_info(head_dim, pl.group, attn::kVariantTileWide);
+        if (kw.available) {
+            pl.variant = attn::kVariantTileWide;
+            pl.ki = kw;
+        }
+    }
     // one tile per block: every split must fit in max_chunk rows at any nkv <= cap
     if (pl.ki.max_chunk > 0 && (split_len > 0 ? split_len > pl.ki.max_chunk
                                               : (!cap_known || (int64_t)P * pl.ki.max_chunk < cap)))
@@ -711,7 +730,7 @@ int attn_resolve_variant(int n_seq, int n_q, int n_head, int n_kv_head, int head
                          int sm_count, int variant)
 {
     attn::KernelInfo ki{};
-    return plan_variant(n_seq, n_q, n_head, n_kv_head, head_dim, cap, sm_count, variant, ki);
+    return public_variant(plan_variant(n_seq, n_q, n_head, n_kv_head, head_dim, cap, sm_count, variant, ki));
 }
 
 attn_status attn_plan_call(int n_seq, int n_q, int n_head, int n_kv_head, int head_dim, int64_t cap,
@@ -735,7 +754,7 @@ attn_status attn_plan_call(int n_seq, int n_q, int n_head, int n_kv_head, int he
                          attn::kStagePartial | attn::kStageCombine, n_q, pl);
     }
     if (st != ATTN_OK) return st;
-    if (variant_out) *variant_out = pl.variant;
+    if (variant_out) *variant_out = public_variant(pl.variant);
     if (n_splits_out) *n_splits_out = pl.n_splits;
     if (workspace_bytes_out) *workspace_bytes_out = pl.workspace;
     return ATTN_OK;

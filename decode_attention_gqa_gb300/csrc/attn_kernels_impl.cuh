@@ -93,11 +93,12 @@ cudaError_t launch_partial_umma(const LaunchRequest &r)
 }
 
 // The one-tile mma.sync kernel: one block per (KV head, split, sequence), one
-// tile of TileCfg::TILE rows each, one query row.
-template <int HD, int G, typename KV>
+// tile of TileCfg::TILE rows each, one query row (WIDE: 128-row tiles at
+// head_dim 256).
+template <int HD, int G, typename KV, bool WIDE = false>
 cudaError_t launch_partial_tile(const LaunchRequest &r)
 {
-    using C = TileCfg<HD, G, KV>;
+    using C = TileCfg<HD, G, KV, false, WIDE>;
     alignas(64) CUtensorMap kmap, vmap;
     const int dt = kv_dtype_code<KV>();
     cudaError_t e = encode_kv_map4(&kmap, r.k_cache, r.n_seq, r.pa.cap, r.pa.n_kv_head, HD, 64, C::TILE, dt);
@@ -106,9 +107,12 @@ cudaError_t launch_partial_tile(const LaunchRequest &r)
     if (e != cudaSuccess) return e;
     // by block length with blk dividing the tile: one block per SPB = TILE / blk splits
     const int blk = r.pa.split_len;
-    const bool ms = tile_serves_splits(C::TILE, blk);
-    const void *fn = ms ? reinterpret_cast<const void *>(&attn_split_partial_tile_ms<C, HD, G, KV>)
-                        : reinterpret_cast<const void *>(&attn_split_partial_tile<C, HD, G, KV>);
+    const void *fn = reinterpret_cast<const void *>(&attn_split_partial_tile<C, HD, G, KV>);
+    bool ms = false;
+    if constexpr (!WIDE) {              // the wide tile takes splits longer than 96 rows only
+        ms = tile_serves_splits(C::TILE, blk);
+        if (ms) fn = reinterpret_cast<const void *>(&attn_split_partial_tile_ms<C, HD, G, KV>);
+    }
     e = ensure_smem_attr(fn, (int)C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     PartialArgs pa = r.pa;
@@ -214,6 +218,9 @@ cudaError_t launch_group(const LaunchRequest &r)
             } else if (r.variant == kVariantTile) {
                 if constexpr (HD == 128 || HD == 256) e = launch_partial_tile<HD, G, KV>(r);
                 else return cudaErrorInvalidValue;
+            } else if (r.variant == kVariantTileWide) {
+                if constexpr (HD == 256) e = launch_partial_tile<HD, G, KV, true>(r);
+                else return cudaErrorInvalidValue;
             } else if (r.variant == kVariantTc) {
                 e = launch_partial<TcCfg<HD, G, KV>, HD, G, KV>(r);
             } else {
@@ -308,6 +315,19 @@ KernelInfo kernel_info_for_hd(int group, int variant, bool multi)
             k.stages = 1;
             const uint32_t smem = multi ? TileCfg<128, kMqHeads, __half, true>::SMEM_BYTES : C::SMEM_BYTES;
             k.blocks_per_sm = (int)(233472u / (smem + 1024u));
+            k.max_chunk = C::TILE;
+            k.available = true;
+        }
+        return k;
+    }
+    if (variant == kVariantTileWide) {
+        if constexpr (HD == 256) {
+            if (multi) return k;
+            using C = TileCfg<HD, 8, __half, false, true>;
+            k.tile_rows = C::TILE;
+            k.granule = C::GRANULE;
+            k.stages = 1;
+            k.blocks_per_sm = (int)(233472u / (C::SMEM_BYTES + 1024u));
             k.max_chunk = C::TILE;
             k.available = true;
         }

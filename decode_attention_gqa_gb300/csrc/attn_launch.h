@@ -16,6 +16,8 @@ constexpr int kVariantTc = 2;
 constexpr int kVariantUmma = 3;             // tcgen05 kernel (attn_partial_umma.cuh)
 constexpr int kVariantFused = 4;            // tcgen05 + cluster combine (attn_fused_umma.cuh)
 constexpr int kVariantTile = 5;             // one-tile mma.sync kernel (attn_partial_tile.cuh)
+constexpr int kVariantTileWide = 6;         // the same with 128-row tiles at head_dim 256 (internal:
+                                            // reported as the one-tile kernel)
 constexpr int kMqHeadsPerBlock = 16;        // query heads per multi-query block
 constexpr int kKvF16 = 0;
 constexpr int kKvBf16 = 1;
@@ -30,7 +32,7 @@ struct LaunchRequest {
     int n_seq;
     int head_dim;
     int group;               // G = n_head / n_kv_head
-    int variant;             // kVariantSimt / kVariantTc / kVariantUmma / kVariantFused / kVariantTile (resolved, never auto)
+    int variant;             // kVariantSimt / kVariantTc / kVariantUmma / kVariantFused / kVariantTile(Wide) (resolved, never auto)
     int stages;              // kStagePartial | kStageCombine
     int kv_dtype;            // kKvF16 / kKvBf16
     cudaStream_t stream;

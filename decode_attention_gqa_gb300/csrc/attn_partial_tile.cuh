@@ -57,12 +57,15 @@ __device__ __forceinline__ void ldsm_a16(uint32_t (&a)[4], const uint8_t *base, 
 // 16-row Q tile (hi parts in rows 0-7, lo parts in 8-15). MQ = true: several
 // causal query rows, 16 (query row, head) slots per block, a 16-row hi tile
 // and a 16-row lo tile (attn_warp_tcmq.cuh), and P as a hi and a lo tile.
-template <int HD, int G, typename KV, bool MQ = false>
+template <int HD, int G, typename KV, bool MQ = false, bool WIDE = false>
 struct TileCfg {
     static_assert(HD == 128 || HD == 256, "the one-tile kernel is built for head_dim 128 and 256");
     static_assert(!MQ || HD == 128, "several query rows: head_dim 128 (two blocks per SM would not fit at 256)");
-    static constexpr int TILE = HD == 256 ? 96 : 128;   // rows per block
-    static constexpr int MINB = HD == 256 ? 2 : 3;      // resident blocks per SM
+    static_assert(!WIDE || (HD == 256 && !MQ), "the wide tile: head_dim 256, one query row");
+    // rows per block: 96 at head_dim 256 so that two blocks fit an SM, or (WIDE) 128
+    // there for splits of 97..128 rows, one block per SM
+    static constexpr int TILE = HD == 256 && !WIDE ? 96 : 128;
+    static constexpr int MINB = HD == 256 ? (WIDE ? 1 : 2) : 3;   // resident blocks per SM
     // warps: S rows and O dimensions split NW ways (8 warps at head_dim 128 were measured
     // slower: each warp reads all of Q and P from shared memory, and more warps meet at
     // each barrier)

@@ -100,11 +100,14 @@ typedef enum {
                                  registers (q and p as hi + lo pairs as above), S split by rows
                                  over four warps, one block-wide maximum, O = P·V split by head
                                  dimension over the warps (no merge of warp states). One tile of
-                                 T rows per block (T = 128; 96 at head_dim 256); head_dim 128 or
-                                 256 with one query row, head_dim 128 with several (16 (query
-                                 row, head) pairs per block); ATTN_ERR_UNSUPPORTED otherwise.
-                                 Every split must fit one tile, as for ATTN_VARIANT_TCGEN05. By
-                                 block length, for one query row,
+                                 T rows per block (T = 128; 96 at head_dim 256, or 128 there,
+                                 one block per SM, when a split needs 97..128 rows: block
+                                 lengths 97..128, or n_splits * 96 < cap <= n_splits * 128);
+                                 head_dim 128 or 256 with one query row, head_dim 128 with
+                                 several (16 (query row, head) pairs per block);
+                                 ATTN_ERR_UNSUPPORTED otherwise. Every split must fit one tile
+                                 (ATTN_ERR_INVALID_ARG otherwise). By block length, for one
+                                 query row,
                                  with split_len a multiple of 16 that divides T, one block serves
                                  T / split_len consecutive splits from one tile (cache rows of
                                  that tile past nkv are then read -- all below cap -- but never

@@ -223,9 +223,12 @@ def test_arguments_that_leave_a_split_larger_than_a_tile(pkg):
             run_decode(pkg, case, 8, 2, 128, 1024, 0.1, variant=VT, **kw)
         assert ei.value.status == pkg.ATTN_ERR_INVALID_ARG, kw
     c256 = to_device(make_case(6002, 1, 8, 2, 256, 1024, (1000,)))
-    with pytest.raises(pkg.AttnError) as ei:
-        run_decode(pkg, c256, 8, 2, 256, 1024, 0.1, variant=VT, n_splits=10)   # 10 * 96 < 1024
-    assert ei.value.status == pkg.ATTN_ERR_INVALID_ARG
+    # head_dim 256: 96-row tiles, or 128-row tiles for longer splits, never more
+    for kw in (dict(n_splits=7),                                  # 7 * 128 < 1024
+               dict(n_splits=8, split_len=129)):
+        with pytest.raises(pkg.AttnError) as ei:
+            run_decode(pkg, c256, 8, 2, 256, 1024, 0.1, variant=VT, **kw)
+        assert ei.value.status == pkg.ATTN_ERR_INVALID_ARG, kw
     # head_dim 64 is not built for this kernel, nor are several query rows at head_dim 256
     c64 = to_device(make_case(6001, 1, 8, 2, 64, 256, (200,)))
     with pytest.raises(pkg.AttnError) as ei:
@@ -311,6 +314,78 @@ def test_full_long_workload_block_32(pkg):
     v, P, _ = pkg.attn_plan_call(1, 1, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0, 32, 0)
     assert v == VT and P == -(-w.cap // 32)
     _check(pkg, lay, w.n_head, w.n_kv_head, w.cap, "long blk 32", hd=w.head_dim, split_len=32)
+
+
+# ---- splits of 97..128 rows at head_dim 256: 128-row tiles, one block per SM ----
+
+@pytest.mark.parametrize("G", [1, 5, 8])
+def test_wide_tile_block_and_count_boundaries(pkg, G):
+    """Block lengths 97..128 and split counts with 96 P < cap <= 128 P run
+    128-row tiles at head_dim 256; every nkv around the split edges, rows past
+    nkv NaN."""
+    hd, n_kv, cap = 256, 2, 1100
+    n_head = G * n_kv
+    base = make_case(6500 + G, 1, n_head, n_kv, hd, cap, (cap,))
+    scale = 1 / math.sqrt(hd)
+    for P, blk in ((-(-cap // 128), 128), (-(-cap // 112), 112), (-(-cap // 97), 97), (9, 0), (11, 0)):
+        v, Pp, _ = pkg.attn_plan_call(1, 1, n_head, n_kv, hd, cap, P, blk, VT)
+        assert v == VT and Pp == P
+        edge = blk if blk else -(-(-(-cap // P)) // 128) * 128     # whole 128-row tiles
+        for nkv in (1, edge - 1, edge, edge + 1, 3 * edge + 7, cap - 1, cap):
+            case = dict(base, positions=np.array([nkv - 1], np.int32))
+            case["k"] = base["k"].copy()
+            case["v"] = base["v"].copy()
+            case["k"][0, nkv:] = np.nan
+            case["v"][0, nkv:] = np.nan
+            _check(pkg, case, n_head, n_kv, cap, "G%d P%d blk %d nkv=%d" % (G, P, blk, nkv), hd=hd,
+                   n_splits=P, split_len=blk)
+
+
+def test_wide_tile_ragged_batch_and_automatic_choice(pkg):
+    hd, n_head, n_kv, cap, blk = 256, 16, 2, 1000, 128
+    ctx = (1, 1000, 0, 127, 128, 129, 500, 999)
+    case = make_case(6600, len(ctx), n_head, n_kv, hd, cap, ctx, fill=np.nan)
+    v, P, _ = pkg.attn_plan_call(len(ctx), 1, n_head, n_kv, hd, cap, 0, blk, 0)
+    assert v == VT and P == -(-cap // blk)
+    for variant in (VT, 0, VT | pkg.ATTN_KV_STABLE):
+        _check(pkg, case, n_head, n_kv, cap, "wide ragged variant %d" % variant, hd=hd,
+               split_len=blk, variant=variant)
+
+
+def test_wide_tile_fused_append_and_bf16(pkg):
+    import torch
+    hd, n_kv, G, cap, blk = 256, 2, 8, 300, 128
+    n_head = G * n_kv
+    scale = 1 / math.sqrt(hd)
+    for nkv in (1, 127, 128, 129, 257, cap):
+        case = make_case(6700 + nkv, 1, n_head, n_kv, hd, cap, (nkv,))
+        k_new, v_new = _new_rows(nkv + 11, 1, n_kv, hd)
+        dev = to_device(case)
+        kn, vn = torch.from_numpy(k_new).cuda(), torch.from_numpy(v_new).cuda()
+        out = torch.full_like(dev["q"], float("nan"))
+        pkg.attn_decode_append(dev["q"], kn, vn, dev["k"], dev["v"], dev["positions"], out, 1,
+                               n_head, n_kv, hd, scale, cap, split_len=blk, variant=VT)
+        torch.cuda.synchronize()
+        kh, vh = _host_after_append(case, k_new, v_new, cap)
+        ref = oracle.attn_decode(case["q"], kh, vh, case["positions"], n_head, n_kv, hd, cap, scale)
+        assert_close(out.cpu().numpy(), ref, "wide append nkv=%d" % nkv)
+    for nkv in (5, 200, cap):
+        case = make_case(6750 + nkv, 1, n_head, n_kv, hd, cap, (nkv,), kv_dtype="bf16")
+        _check(pkg, case, n_head, n_kv, cap, "wide bf16 nkv=%d" % nkv, hd=hd, split_len=blk,
+               variant=VT | pkg.ATTN_KV_BF16, kv_dtype="bf16")
+
+
+def test_wide_tile_stable_chain(pkg):
+    _chain(pkg, L=4, n_head=16, n_kv=2, hd=256, cap=2560, ctx=(2000,), P=20, blk=128,
+           variant=VT, graph=True, replays=2, seed=6800)
+
+
+def test_full_long_workload_block_128(pkg):
+    w = syn.WORKLOADS["long"]
+    lay = syn.make_layer(w)
+    v, P, _ = pkg.attn_plan_call(1, 1, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0, 128, 0)
+    assert v == VT and P == -(-w.cap // 128)
+    _check(pkg, lay, w.n_head, w.n_kv_head, w.cap, "long blk 128", hd=w.head_dim, split_len=128)
 
 
 # ---- several causal query rows (head_dim 128, 16 (row, head) slots per block) ----
