@@ -282,8 +282,10 @@ def config_of(args, w, L, world):
     ctx_end = max(w.ctx)
     rows = sum(min(max(int(c), 0), w.cap) for c in ([ctx_end] if advance else w.ctx))
     n_q = args.n_q
-    return {"workload": describe(w, L) + (", %d causal query rows per sequence" % n_q
-                                          if n_q > 1 else ""),
+    extra = "".join([", %d causal query rows per sequence" % n_q if n_q > 1 else "",
+                     ", block length %d" % args.split_len if args.split_len else "",
+                     ", new K/V row appended by the call" if args.append else ""])
+    return {"workload": describe(w, L, args.kv_dtype) + extra,
             "name": w.name, "ctx": ctx_end, "cap": w.cap,
             "n_seq": w.n_seq, "n_head": w.n_head, "n_kv_head": w.n_kv_head,
             "head_dim": w.head_dim, "layers": L, "split_len": args.split_len,
@@ -311,17 +313,20 @@ def workload_for(args):
     return w
 
 
-def describe(w, L):
+def describe(w, L, kv_dtype="f16"):
+    kv = {"f16": "f16", "bf16": "bfloat16"}[kv_dtype]
     return {
-        "7b": "7b-like decode: 1 sequence, 28 q / 4 KV heads, head_dim 128, f16 KV cache, "
-              "%d layers, graph replay with positions += 1 per step" % L,
+        "7b": "7b-like decode: 1 sequence, 28 q / 4 KV heads, head_dim 128, %s KV cache, "
+              "%d layers, graph replay with positions += 1 per step" % (kv, L),
         "long": "long-context grouped decode: 1 sequence, 16 q / 2 KV heads, head_dim 256, "
-                "context 8400, %d layers, graph replay with positions += 1 per step" % L,
+                "context 8400, %s KV cache, %d layers, graph replay with positions += 1 per step"
+                % (kv, L),
         "stress": "stress decode: 1 sequence, context 131072, 64 q / 8 KV heads, head_dim 128, "
-                  "K x8, graph replay with positions += 1 per step",
+                  "K x8, %s KV cache, graph replay with positions += 1 per step" % kv,
         "ragged": "batched ragged decode: 32 sequences, context ~ U[1, 32768], 32 q / 8 KV heads, "
-                  "head_dim 128, contiguous per-sequence f16 KV, static grid",
-        "tiny": "tiny decode: 1 sequence, 8 q / 2 KV heads, head_dim 128, context 512",
+                  "head_dim 128, contiguous per-sequence %s KV, static grid" % kv,
+        "tiny": "tiny decode: 1 sequence, 8 q / 2 KV heads, head_dim 128, context 512, %s KV cache"
+                % kv,
     }.get(w.name, w.name)
 
 
