@@ -244,7 +244,8 @@ def test_arguments_that_leave_a_split_larger_than_a_tile(pkg):
 
 # ---- several block-length splits per block (split_len divides the tile) ----
 
-@pytest.mark.parametrize("hd,blk", [(128, 16), (128, 32), (128, 64), (256, 16), (256, 32), (256, 48)])
+@pytest.mark.parametrize("hd,blk", [(128, 16), (128, 32), (128, 64), (256, 16), (256, 32), (256, 48),
+                                    (256, 64)])       # 64 at head_dim 256: one split per 96-row tile
 def test_several_splits_per_block_with_nan_past_nkv(pkg, hd, blk):
     """One block serves TILE / blk consecutive splits from one tile that starts
     at a multiple of the tile; its rows at or past nkv are read but must never
@@ -267,7 +268,7 @@ def test_several_splits_per_block_with_nan_past_nkv(pkg, hd, blk):
                n_splits=P, split_len=blk)
 
 
-@pytest.mark.parametrize("hd,blk", [(128, 32), (256, 32)])
+@pytest.mark.parametrize("hd,blk", [(128, 32), (256, 32), (256, 64)])
 def test_several_splits_per_block_ragged_batch(pkg, hd, blk):
     n_head, n_kv, cap = 32, 8, 900
     ctx = (1, 900, 0, 17, 450, 899, 64, 333, 128, 129)
@@ -380,12 +381,13 @@ def test_wide_tile_stable_chain(pkg):
            variant=VT, graph=True, replays=2, seed=6800)
 
 
-def test_full_long_workload_block_128(pkg):
+@pytest.mark.parametrize("blk", [64, 128])
+def test_full_long_workload_block_64_and_128(pkg, blk):
     w = syn.WORKLOADS["long"]
     lay = syn.make_layer(w)
-    v, P, _ = pkg.attn_plan_call(1, 1, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0, 128, 0)
-    assert v == VT and P == -(-w.cap // 128)
-    _check(pkg, lay, w.n_head, w.n_kv_head, w.cap, "long blk 128", hd=w.head_dim, split_len=128)
+    v, P, _ = pkg.attn_plan_call(1, 1, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0, blk, 0)
+    assert v == VT and P == -(-w.cap // blk)
+    _check(pkg, lay, w.n_head, w.n_kv_head, w.cap, "long blk %d" % blk, hd=w.head_dim, split_len=blk)
 
 
 # ---- several causal query rows (head_dim 128, 16 (row, head) slots per block) ----
