@@ -10,7 +10,9 @@
 // SMs); each group of lanes folds its share of the splits into a running
 // (m, S, acc) with the §2.1 update rule, a batch of splits at a time (the
 // batch's maximum first, so that its weights are independent exponentials; a
-// larger maximum rescales what came before), the groups of a warp are folded
+// larger maximum rescales what came before; the batch is sized from the split
+// count so that every load of a group leaves in one round where it can: each
+// round is a dependent L2 round trip), the groups of a warp are folded
 // with shuffles and the warps through shared memory. The result equals the
 // two-pass form up to rounding.
 // A split whose mx is -inf (no rows) is skipped, so an all-empty row gives
@@ -22,7 +24,7 @@
 
 namespace attn {
 
-template <int HD>
+template <int HD, int BATCH_ = 8>
 struct CombineCfg {
     static constexpr int WARPS = 4;
     static constexpr int THREADS = WARPS * 32;
@@ -31,14 +33,14 @@ struct CombineCfg {
     static constexpr int LPS = DC / 4;                // lanes per split row (float4 each)
     static constexpr int SPW = 32 / LPS;              // split groups per warp
     static constexpr int NG = WARPS * SPW;            // split groups per block
-    static constexpr int BATCH = 8;                   // split rows in flight per lane
+    static constexpr int BATCH = BATCH_;              // split rows in flight per lane
 };
 
-template <int HD>
-__global__ void __launch_bounds__(CombineCfg<HD>::THREADS)
+template <int HD, int BATCH>
+__global__ void __launch_bounds__(CombineCfg<HD, BATCH>::THREADS)
 attn_combine(const CombineArgs a)
 {
-    using C = CombineCfg<HD>;
+    using C = CombineCfg<HD, BATCH>;
     __shared__ float sm_m[C::WARPS], sm_s[C::WARPS];
     __shared__ float sm_acc[C::WARPS][C::DC];
 

@@ -194,7 +194,11 @@ cudaError_t launch_combine(const LaunchRequest &r)
     ca.out = r.out;
     ca.n_head = r.pa.n_head * (r.pa.n_q > 0 ? r.pa.n_q : 1);   // partial heads per sequence
     ca.n_splits = r.pa.n_splits;
-    const void *fn = reinterpret_cast<const void *>(&attn_combine<HD>);
+    // the smallest batch that puts every split of a lane group in one round of loads
+    const int ng = CombineCfg<HD>::NG;
+    const void *fn = ca.n_splits <= ng * 8    ? reinterpret_cast<const void *>(&attn_combine<HD, 8>)
+                     : ca.n_splits <= ng * 16 ? reinterpret_cast<const void *>(&attn_combine<HD, 16>)
+                                              : reinterpret_cast<const void *>(&attn_combine<HD, 24>);
     const cudaError_t e = ensure_smem_attr(fn, 0);
     if (e != cudaSuccess) return e;
     void *args[] = {&ca};
