@@ -90,7 +90,7 @@ struct TileCfg {
     // P tile(s): 16 rows of TILE elements in 128-byte swizzled chunks of 64 (MQ: hi, then lo)
     static constexpr uint32_t P_TILE = 16u * ((TILE + 63) / 64 * 64) * 2;
     static constexpr uint32_t P_BYTES = (MQ ? 2u : 1u) * P_TILE;
-    // maxima and sums: per warp, or per 8-row group (the several-split kernel); RSL slots each
+    // maxima per warp; sums per warp, or per 8-row group (the several-split kernel); RSL slots each
     static constexpr int NRED = MQ ? NW : (TILE / 8 > NW ? TILE / 8 : NW);
     static constexpr int RSL = MQ ? 16 : 8;
     static constexpr uint32_t OFF_RED = OFF_Q + (QStage::EXTRA_BYTES + 15) / 16 * 16;   // [2][NRED][RSL] floats
@@ -379,7 +379,9 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
 
 // By block length with blk = split_len dividing TILE (and a multiple of 16):
 // block b serves the SPB = TILE / blk splits b·SPB .. b·SPB + SPB - 1, whose
-// rows [b·TILE, b·TILE + TILE) are one tile starting at row b·TILE. Cache
+// rows [b·TILE, b·TILE + TILE) are one tile starting at row b·TILE. Each split's
+// (mx, S, oc) is relative to the block's per-head maximum (one reference for the
+// block, as in the single-split kernel); the combine rescales them. Cache
 // rows of that tile at or past nkv (in the last block only; all within cap,
 // and rows past cap arrive as zeros) are read but never used: their scores
 // are masked and their V rows are set to zero in shared memory before P · V,
@@ -394,7 +396,7 @@ attn_split_partial_tile_ms(const __grid_constant__ CUtensorMap kmap, const __gri
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + Cfg::OFF_BAR);    // [0] K landed, [1] V landed
     volatile int *flags = reinterpret_cast<volatile int *>(bar + 2);     // [0] abort
-    float *red_m = reinterpret_cast<float *>(smem + Cfg::OFF_RED);      // [TILE / 8][8] group maxima
+    float *red_m = reinterpret_cast<float *>(smem + Cfg::OFF_RED);      // [NW][8] warp maxima
     float *red_l = red_m + Cfg::NRED * Cfg::RSL;                        // [TILE / 8][8] group sums
 
     const int hk = blockIdx.x, b = blockIdx.y, s = blockIdx.z;
@@ -508,31 +510,33 @@ attn_split_partial_tile_ms(const __grid_constant__ CUtensorMap kmap, const __gri
                 sc[j][e] = r < nv ? v : -INFINITY;
             }
     }
-    // ---- a4: each head's maximum per 8-row group, then per split ----
+    // ---- a4: each head's maximum over the block's rows, the reference of all of its
+    // splits (every split's p = 2^(s - M + OFF) with M >= its own maximum: a split far
+    // below M contributes equally little to the combined result), then each head's sum
+    // per 8-row group ----
+    {
+        float m = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < NS; ++j) {
-        float m = fmaxf(sc[j][0], sc[j][1]);
+        for (int j = 0; j < NS; ++j) m = fmaxf(m, fmaxf(sc[j][0], sc[j][1]));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        if (t == 0) red_m[(r0 / 8 + j) * 8 + g] = m;
+        if (t == 0) red_m[warp * 8 + g] = m;
     }
     __syncthreads();                          // the maxima are in; S is done, so Q is dead
+    float M = red_m[g];
+#pragma unroll
+    for (int w = 1; w < Cfg::NW; ++w) M = fmaxf(M, red_m[w * 8 + g]);
+    const float base = M - Cfg::OFF;          // M is finite: the block has rows before nv
     {
         uint8_t *pt = smem + Cfg::OFF_P;
 #pragma unroll
         for (int j = 0; j < NS; ++j) {
-            const int grp = r0 / 8 + j, first = grp / GPS * GPS;   // the split's first 8-row group
-            float M = red_m[first * 8 + g];
-            for (int k = 1; k < GPS; ++k) M = fmaxf(M, red_m[(first + k) * 8 + g]);
-            // a split with no row before nv has M = -inf and p = 0 throughout
-            const float base = M - Cfg::OFF;
-            const float p0 = M == -INFINITY ? 0.f : ex2(sc[j][0] - base);
-            const float p1 = M == -INFINITY ? 0.f : ex2(sc[j][1] - base);
+            const float p0 = ex2(sc[j][0] - base), p1 = ex2(sc[j][1] - base);
             store_p_pair<Cfg, KV>(pt, r0 + 8 * j, g, t, p0, p1);
             float l = p0 + p1;
             l += __shfl_xor_sync(0xffffffffu, l, 1);
             l += __shfl_xor_sync(0xffffffffu, l, 2);
-            if (t == 0) red_l[grp * 8 + g] = l;
+            if (t == 0) red_l[(r0 / 8 + j) * 8 + g] = l;
         }
     }
     bool vok = ok;
@@ -551,35 +555,44 @@ attn_split_partial_tile_ms(const __grid_constant__ CUtensorMap kmap, const __gri
     const int d0 = warp * Cfg::DW;
     const bool abort = flags[0] != 0;
     if (!abort) {
+        // one pass over the tile's k-steps, fully unrolled; after each split's
+        // KPS k-steps its accumulator is written out and cleared (the splits
+        // past nsplit hold P = 0 and are not written)
         const int KPS = blk / 16;             // k-steps per split
-        for (int j = 0; j < nsplit; ++j) {
-            const int sp = b * SPB + j;
-            float o[2][NO][4];
+        float o[NO][4];
 #pragma unroll
-            for (int e = 0; e < 2; ++e)
+        for (int jj = 0; jj < NO; ++jj)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[jj][i] = 0.f;
+        int left = KPS, j = 0;
+        float *dst = a.ws_o + (((size_t)s * heads + (size_t)hk * G + g) * P + (size_t)b * SPB) * HD + d0 + 2 * t;
+#pragma unroll
+        for (int kk = 0; kk < Cfg::KO; ++kk) {
+            tile_pv_step<Cfg, HD, KV>(smem, d0, lane, kk, o);
+            if (--left == 0) {
+                if (j < nsplit && g < G && b * SPB + j < P) {
+#pragma unroll
+                    for (int jj = 0; jj < NO; ++jj)
+                        *reinterpret_cast<float2 *>(dst + 8 * jj) =
+                            make_float2(o[jj][0] + o[jj][2], o[jj][1] + o[jj][3]);
+                }
 #pragma unroll
                 for (int jj = 0; jj < NO; ++jj)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) o[e][jj][i] = 0.f;
-            tile_pv<Cfg, HD, KV>(smem, d0, lane, j * KPS, (j + 1) * KPS, o);
-            if (g < G && sp < P) {
-                float *dst = a.ws_o + (((size_t)s * heads + (size_t)hk * G + g) * P + sp) * HD + d0 + 2 * t;
-#pragma unroll
-                for (int jj = 0; jj < NO; ++jj)
-                    *reinterpret_cast<float2 *>(dst + 8 * jj) =
-                        make_float2((o[0][jj][0] + o[1][jj][0]) + (o[0][jj][2] + o[1][jj][2]),
-                                    (o[0][jj][1] + o[1][jj][1]) + (o[0][jj][3] + o[1][jj][3]));
+                    for (int i = 0; i < 4; ++i) o[jj][i] = 0.f;
+                left = KPS;
+                ++j;
+                dst += HD;
             }
         }
-        // (mx, S) of every non-empty split: thread (j, head)
+        // (mx, S) of every non-empty split: thread (j, head); mx is the block's reference
         for (int i = tid; i < nsplit * 8; i += Cfg::THREADS) {
             const int j = i / 8, gg = i % 8, sp = b * SPB + j;
             if (gg < G && sp < P) {
-                float M = -INFINITY, L = 0.f;
-                for (int k = 0; k < GPS; ++k) M = fmaxf(M, red_m[(j * GPS + k) * 8 + gg]);
+                float Mh = red_m[gg], L = 0.f;
+                for (int w = 1; w < Cfg::NW; ++w) Mh = fmaxf(Mh, red_m[w * 8 + gg]);
                 for (int k = 0; k < GPS; ++k) L += red_l[(j * GPS + k) * 8 + gg];
-                a.ws_ml[((size_t)s * heads + (size_t)hk * G + gg) * P + sp] =
-                    make_float2(M == -INFINITY ? M : M - Cfg::OFF, L);
+                a.ws_ml[((size_t)s * heads + (size_t)hk * G + gg) * P + sp] = make_float2(Mh - Cfg::OFF, L);
             }
         }
     } else if (tid == 0) {

@@ -236,9 +236,12 @@ attn_status attn_decode_multi(const float *q, const void *k_cache, const void *v
  *     ml  at byte round_up(4 * n_seq * n_head * n_splits * head_dim, 256):
  *                                         [n_seq][n_head][n_splits][2] = (mx, S)
  * where oc is the unnormalised weighted V sum of the split, S its softmax
- * denominator and mx its running maximum, all relative to exp2(scores *
- * log2 e) (mx is in log2 units). An empty split has mx = -inf, S = 0 and its
- * oc is never read. Splits combine in any order: partials of disjoint row
+ * denominator and mx the reference they are scaled to (log2 units): with s a
+ * row's score times log2 e, oc = sum 2^(s - mx) v and S = sum 2^(s - mx) over
+ * the split's rows. mx is at or near the split's running maximum, or the
+ * maximum of the rows a kernel block shares among several splits (a split far
+ * below it then holds small or zero S and oc); 2^(s - mx) stays below 2^15. An
+ * empty split has mx = -inf, S = 0 and its oc is never read. Splits combine in any order: partials of disjoint row
  * ranges computed elsewhere (another device's shard of the rows, say) can be
  * laid side by side along the split axis and combined with n_splits = the
  * total split count.

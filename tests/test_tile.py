@@ -268,6 +268,21 @@ def test_several_splits_per_block_with_nan_past_nkv(pkg, hd, blk):
                n_splits=P, split_len=blk)
 
 
+@pytest.mark.parametrize("hd,blk", [(128, 16), (128, 32), (256, 32), (256, 48)])
+def test_several_splits_per_block_score_spread(pkg, hd, blk):
+    """The splits of a block share one reference maximum, the block's: with K x8
+    and a planted row several times larger, the other splits of that block sit
+    tens of log2 units below it (their p underflow where they do not matter),
+    and a block whose dominant row is in its last split reaches every earlier one."""
+    n_head, n_kv, cap = 16, 2, 1000
+    case = make_case(6150 + hd + blk, 1, n_head, n_kv, hd, cap, (999,), k_scale=8.0)
+    T = TILE[hd]
+    for row in (5, 130, 3 * T - 1):                  # a block's first split, a middle one, its last
+        case["k"][0, row] = (case["k"][0, row].astype(np.float32) * 4).astype(np.float16)
+    _check(pkg, case, n_head, n_kv, cap, "hd%d blk %d spread" % (hd, blk), hd=hd,
+           n_splits=-(-cap // blk), split_len=blk)
+
+
 @pytest.mark.parametrize("hd,blk", [(128, 32), (256, 32), (256, 64)])
 def test_several_splits_per_block_ragged_batch(pkg, hd, blk):
     n_head, n_kv, cap = 32, 8, 900
