@@ -111,8 +111,8 @@ def test_static_scratch_matches_oracle_twice(pkg, case_idx):
     _two_calls(pkg, CASES[case_idx], 0)
 
 
-@pytest.mark.parametrize("variant_name", ["TC", "TCGEN05", "TCGEN05_CLUSTER", "STABLE",
-                                          "TCGEN05|STABLE", "BF16"])
+@pytest.mark.parametrize("variant_name", ["TC", "TCGEN05", "TCGEN05_CLUSTER", "TC_TILE", "STABLE",
+                                          "TCGEN05|STABLE", "TC_TILE|STABLE", "BF16"])
 def test_static_scratch_every_variant_plans_like_ex(pkg, variant_name):
     """n_splits = 0 with an explicit kernel or flags: the static call must plan
     the split count attn_decode_ex plans for that variant (the cluster-fused
@@ -121,6 +121,8 @@ def test_static_scratch_every_variant_plans_like_ex(pkg, variant_name):
     names = {"TC": pkg.ATTN_VARIANT_TC, "TCGEN05": pkg.ATTN_VARIANT_TCGEN05,
              "TCGEN05_CLUSTER": pkg.ATTN_VARIANT_TCGEN05_CLUSTER, "STABLE": pkg.ATTN_KV_STABLE,
              "TCGEN05|STABLE": pkg.ATTN_VARIANT_TCGEN05 | pkg.ATTN_KV_STABLE,
+             "TC_TILE": pkg.ATTN_VARIANT_TC_TILE,
+             "TC_TILE|STABLE": pkg.ATTN_VARIANT_TC_TILE | pkg.ATTN_KV_STABLE,
              "BF16": pkg.ATTN_KV_BF16}
     variant = names[variant_name]
     _two_calls(pkg, CASES[0], variant, kv_dtype="bf16" if variant & pkg.ATTN_KV_BF16 else "f16")
