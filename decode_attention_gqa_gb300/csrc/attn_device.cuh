@@ -143,6 +143,25 @@ __device__ __forceinline__ void split_range(int64_t nkv, int sp, int n_splits, i
     hi = lo + chunk < nkv ? lo + chunk : nkv;
 }
 
+// split_range for the one-tile kernel (tile rows per block, count mode): a
+// chunk that would fill more than three quarters of a tile is rounded up to 16
+// rows only, so that a split count sized for two blocks per SM balances the
+// rows over the blocks (the 7b layer at full context: 76 splits of 108 -> 112
+// rows instead of 64 whole tiles on 256 blocks of 152 SMs); shorter chunks are
+// rounded up to whole tiles (few, full blocks for short contexts).
+__device__ __forceinline__ void split_range_tile(int64_t nkv, int sp, int n_splits, int split_len,
+                                                 int tile, int64_t &lo, int64_t &hi)
+{
+    if (split_len > 0) {
+        split_range(nkv, sp, n_splits, split_len, tile, lo, hi);
+        return;
+    }
+    int64_t chunk = (nkv + n_splits - 1) / n_splits;
+    chunk = 4 * chunk > 3 * (int64_t)tile ? (chunk + 15) / 16 * 16 : (chunk + tile - 1) / tile * tile;
+    lo = (int64_t)sp * chunk;
+    hi = lo + chunk < nkv ? lo + chunk : nkv;
+}
+
 // Row stride (floats) of a warp's published accumulators in the merge area:
 // 8 floats of padding put the rows of consecutive heads 8 banks apart, so
 // that the tensor-core fragments (lanes 4 apart hold the same dims of

@@ -46,6 +46,7 @@ struct KernelInfo {
     bool available;          // compiled for this (head_dim, group)
     int stages;              // pipeline stages (tiles in flight per block)
     int max_chunk;           // rows one block can take (0: any; the tcgen05 kernel: one tile)
+    bool balanced = false;   // count-mode chunks near a tile are rounded to 16 rows (one-tile kernel)
 };
 
 // Whether the one-tile kernel serves several block-length splits per block:

@@ -78,7 +78,8 @@ struct TileCfg {
     static constexpr int NO = DW / 8;                   // O n-tiles (8 dimensions each) per warp
     static constexpr int KO = TILE / 16;                // O k-steps
     static constexpr int NCH = HD / 64;                 // 128-byte column chunks per row
-    static constexpr int GRANULE = TILE;                // count-mode chunks are whole tiles
+    static constexpr int GRANULE = TILE;                // count-mode chunks: whole tiles, or 16 rows
+                                                        // near a tile (split_range_tile)
     static constexpr bool Q_REGS = KS <= 8 && !MQ;      // Q fragments held in registers
     using QStage = typename std::conditional<MQ, TcWarpMQ<HD, 16, NW, KV>, TcWarp<HD, G, NW, KV>>::type;
     static constexpr uint32_t Q_AREA = (MQ ? 2u : 1u) * QStage::QT_BYTES;   // Q tiles, before the scales
@@ -221,7 +222,7 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
     bool pos_ok;
     const int64_t nkv = rows_attended(a, s, sp == 0 && hk == 0 && tid == 0, &pos_ok);
     int64_t lo, hi;
-    split_range(nkv, sp, P, a.split_len, Cfg::GRANULE, lo, hi);
+    split_range_tile(nkv, sp, P, a.split_len, Cfg::TILE, lo, hi);
     if (lo >= hi) {
         if (stable) pdl_wait();               // the workspace may still be read by the previous grid
         if (tid < G) a.ws_ml[((size_t)s * heads + (size_t)hk * G + tid) * P + sp] = make_float2(-INFINITY, 0.f);
@@ -642,7 +643,7 @@ attn_split_partial_tile_mq(const __grid_constant__ CUtensorMap kmap, const __gri
     bool pos_ok;
     const int64_t nkv = rows_attended(a, s, sp == 0 && blockIdx.x == 0 && tid == 0, &pos_ok);
     int64_t lo, hi;
-    split_range(nkv, sp, P, a.split_len, Cfg::GRANULE, lo, hi);
+    split_range_tile(nkv, sp, P, a.split_len, Cfg::TILE, lo, hi);
     if (lo >= hi) {
         if (stable) pdl_wait();
         if (tid < 16) {

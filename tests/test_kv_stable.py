@@ -233,15 +233,23 @@ def _bench_configuration(pkg, name, L, n_q=1, variant=0):
     return P
 
 
+def torch_sm_count():
+    import torch
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
 def test_full_7b_bench_configuration(pkg):
-    # variant 0 runs this short call on the tcgen05 kernel: 8192 / 128 = 64 splits
-    assert _bench_configuration(pkg, "7b", L=4) == 64
+    # variant 0 runs this short call on the one-tile kernel: two blocks per SM, 76 splits
+    # of 108 -> 112 rows (152 SMs; ceil(8192 / 76) rounded to 16 rows near a tile)
+    P = _bench_configuration(pkg, "7b", L=4)
+    sms = torch_sm_count()
+    assert P == max(64, 2 * sms // 4) if 4 * -(-8192 // (2 * sms // 4)) > 3 * 128 else P == 64
     # the mma.sync kernel at its own split count (blocks of its three-tile ring)
     assert _bench_configuration(pkg, "7b", L=3, variant=pkg.ATTN_VARIANT_TC) == 43
 
 
 def test_full_long_bench_configuration(pkg):
-    # variant 0 runs the tcgen05 kernel at head_dim 256 too: 96-row tiles, ceil(8400 / 96) = 88
+    # variant 0 runs the one-tile kernel at head_dim 256 too: 96-row tiles, ceil(8400 / 96) = 88
     assert _bench_configuration(pkg, "long", L=3) == 88
     assert _bench_configuration(pkg, "long", L=2, variant=pkg.ATTN_VARIANT_TC) == 75
 

@@ -97,6 +97,24 @@ def test_block_split_boundaries(pkg, hd):
             assert_close(out.cpu().numpy(), ref, "hd%d block %d nkv=%d" % (hd, blk, nkv))
 
 
+def test_balanced_count_split_around_three_quarters_of_a_tile(pkg):
+    """By count, a chunk of more than three quarters of a tile is rounded up to
+    16 rows, a shorter one to a whole tile: with 76 splits at capacity 8192 the
+    rule switches between nkv = 7296 (96-row chunks -> 128) and 7297 (97 -> 112),
+    and again at 8513 (113 -> 128; capacity 8704 here). Rows past nkv are NaN."""
+    n_head, n_kv, hd, cap, P = 28, 4, 128, 8704, 76
+    v, Pp, _ = pkg.attn_plan_call(1, 1, n_head, n_kv, hd, 8192, 0, 0, 0)
+    assert v == VT and Pp == P                        # what variant 0 plans for the 7b layer
+    base = make_case(5350, 1, n_head, n_kv, hd, cap, (cap,))
+    for nkv in (1, 1000, 7296, 7297, 7300, 76 * 112, 76 * 112 + 1, 8192, 8600):
+        case = dict(base, positions=np.array([nkv - 1], np.int32))
+        case["k"] = base["k"].copy()
+        case["v"] = base["v"].copy()
+        case["k"][0, nkv:] = np.nan
+        case["v"][0, nkv:] = np.nan
+        _check(pkg, case, n_head, n_kv, cap, "balanced P=76 nkv=%d" % nkv, n_splits=P)
+
+
 def test_split_count_invariance_and_agreement_with_the_other_kernels(pkg):
     n_head, n_kv, cap = 32, 8, 3000
     case = make_case(5400, 2, n_head, n_kv, 128, cap, (3000, 1234))
@@ -343,10 +361,11 @@ def test_wide_tile_block_and_count_boundaries(pkg, G):
     n_head = G * n_kv
     base = make_case(6500 + G, 1, n_head, n_kv, hd, cap, (cap,))
     scale = 1 / math.sqrt(hd)
-    for P, blk in ((-(-cap // 128), 128), (-(-cap // 112), 112), (-(-cap // 97), 97), (9, 0), (11, 0)):
+    for P, blk in ((-(-cap // 128), 128), (-(-cap // 112), 112), (-(-cap // 97), 97), (9, 0), (10, 0), (11, 0)):
         v, Pp, _ = pkg.attn_plan_call(1, 1, n_head, n_kv, hd, cap, P, blk, VT)
         assert v == VT and Pp == P
-        edge = blk if blk else -(-(-(-cap // P)) // 128) * 128     # whole 128-row tiles
+        c = -(-cap // P)                                # by count: near a tile, 16-row chunks
+        edge = blk if blk else (-(-c // 16) * 16 if 4 * c > 3 * 128 else -(-c // 128) * 128)
         for nkv in (1, edge - 1, edge, edge + 1, 3 * edge + 7, cap - 1, cap):
             case = dict(base, positions=np.array([nkv - 1], np.int32))
             case["k"] = base["k"].copy()
