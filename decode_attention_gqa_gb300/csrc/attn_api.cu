@@ -163,8 +163,9 @@ int heuristic(int n_seq, int n_kv_head, int qgroups, int64_t cap, int sm_count,
     // tiles (the 7b layer: 76 splits of 112 rows on 304 blocks instead of 64
     // tiles on 256, 5.89 -> 5.73 us per layer; shorter contexts still run
     // whole tiles).
+    // The 128-row tiles at head_dim 256 (one block per SM) take one block per SM.
     if (ki.balanced && cap > 0 && sm_count > 0 && ki.max_chunk > 0) {
-        const int per_sm2 = ki.blocks_per_sm - 1 < 2 ? ki.blocks_per_sm - 1 : 2;
+        const int per_sm2 = ki.blocks_per_sm >= 3 ? 2 : ki.blocks_per_sm == 1 ? 1 : 0;
         const int64_t P2 = per_sm2 > 0 ? (int64_t)sm_count * per_sm2 / units : 0;
         const int64_t c2 = P2 > 0 ? (cap + P2 - 1) / P2 : 0;
         if (P2 > 0 && 4 * c2 > 3 * (int64_t)ki.max_chunk && c2 <= ki.max_chunk) P = P2;
@@ -219,6 +220,18 @@ bool one_tile_fits(int variant, int head_dim, int group, int n_q, int n_seq, int
 int auto_short_kernel(int head_dim, int group, int n_q, int n_seq, int n_kv_head, int64_t cap,
                       int sm_count, int n_splits, int split_len, bool kv_stable, attn::KernelInfo &ku)
 {
+    // head_dim 256 by count: where one block per SM makes chunks longer than the 96-row
+    // tile (and at most 128 rows), 128-row tiles with balanced chunks, one per SM (the
+    // long layer: 76 splits of 112 rows, 6.32 -> 6.00 us per layer against 88 tiles of
+    // 96 rows on 176 blocks)
+    if (n_q == 1 && head_dim == 256 && n_splits == 0 && split_len == 0 && cap > 0 && sm_count > 0) {
+        const int64_t P1 = (int64_t)sm_count / ((int64_t)n_seq * n_kv_head);
+        const int64_t c1 = P1 > 0 ? (cap + P1 - 1) / P1 : 0;
+        if (P1 > 0 && 4 * c1 > 3 * 128 && c1 <= 128 &&
+            one_tile_fits(attn::kVariantTileWide, head_dim, group, n_q, n_seq, n_kv_head, cap, sm_count, n_splits,
+                          split_len, kv_stable, ku))
+            return attn::kVariantTileWide;
+    }
     if ((n_q == 1 || head_dim == 128) &&
         one_tile_fits(attn::kVariantTile, head_dim, group, n_q, n_seq, n_kv_head, cap, sm_count, n_splits,
                       split_len, kv_stable, ku))

@@ -132,9 +132,14 @@ def test_split_heuristic_for_flagged_calls(lib):
     assert h(1, 64, 8, 128, 131072, 152, pkg.ATTN_KV_STABLE) == h(1, 64, 8, 128, 131072, 152, 0) == 38
     # a batch keeps its eight waves
     assert h(32, 32, 8, 128, 32768, 152, pkg.ATTN_KV_STABLE) == 10
-    # head_dim 256: variant 0 runs the tcgen05 kernel, 96-row tiles, ceil(8400 / 96) = 88
-    # splits; the mma.sync kernel already runs one block per SM
-    assert h(1, 16, 2, 256, 8400, 152, S) == h(1, 16, 2, 256, 8400, 152, 0) == 88
+    # head_dim 256: variant 0 runs the one-tile kernel; the mma.sync kernel already runs
+    # one block per SM
+    assert h(1, 16, 2, 256, 8400, 152, S) == h(1, 16, 2, 256, 8400, 152, 0) == 76
+    # ... with 128-row tiles, one block per SM: 152 / 2 = 76 splits of 111 -> 112 rows; at
+    # 148 SMs 74 splits of 114 -> 128; a shorter cache keeps the 96-row tiles
+    assert h(1, 16, 2, 256, 8400, 148, 0) == 74
+    assert h(1, 16, 2, 256, 6000, 152, 0) == 63
+    assert h(1, 16, 2, 256, 2048, 152, 0) == 22
     assert h(1, 16, 2, 256, 8400, 152, TC | S) == h(1, 16, 2, 256, 8400, 152, TC) == 75
     # several query rows: 4 rows x 7 heads = 28 pairs -> 2 query groups of 16 per KV
     # head; at one block per SM a block would hold 431 rows (not a short call), so
@@ -363,7 +368,8 @@ def test_tcgen05_choice_keeps_its_limits(lib):
             continue
         seen.add((hd, n_q > 1))
         assert hd in (128, 256)
-        assert P * tile[hd] >= cap
+        # the one-tile kernel may take 128-row tiles at head_dim 256 (one block per SM)
+        assert P * (128 if v == VT else tile[hd]) >= cap
         if v == VT:
             # 16 (row, head) slots per block; 3 blocks per SM at head_dim 128, 2 at 256
             assert n_q == 1 or hd == 128

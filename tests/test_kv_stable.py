@@ -249,8 +249,14 @@ def test_full_7b_bench_configuration(pkg):
 
 
 def test_full_long_bench_configuration(pkg):
-    # variant 0 runs the one-tile kernel at head_dim 256 too: 96-row tiles, ceil(8400 / 96) = 88
-    assert _bench_configuration(pkg, "long", L=3) == 88
+    # variant 0 runs the one-tile kernel at head_dim 256 too: 128-row tiles, one block per
+    # SM, 76 splits of 111 -> 112 rows on 152 SMs (whole 96-row tiles, 88, where one
+    # block per SM would leave chunks of 96 rows or fewer)
+    P = _bench_configuration(pkg, "long", L=3)
+    P1 = torch_sm_count() // 2
+    c1 = -(-8400 // P1)
+    assert P == (P1 if 96 < c1 <= 128 else 88)
+    assert _bench_configuration(pkg, "long", L=3, variant=pkg.ATTN_VARIANT_TC_TILE) == 88
     assert _bench_configuration(pkg, "long", L=2, variant=pkg.ATTN_VARIANT_TC) == 75
 
 

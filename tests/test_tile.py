@@ -215,8 +215,11 @@ def test_full_long_workload(pkg):
     lay = syn.make_layer(w)
     P = pkg.attn_split_heuristic_ex(1, 1, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0,
                                     VT | pkg.ATTN_KV_STABLE)
-    assert P * TILE[256] >= w.cap
-    _check(pkg, lay, w.n_head, w.n_kv_head, w.cap, "long", hd=w.head_dim, n_splits=P)
+    assert P * 128 >= w.cap                           # 96-row tiles, or 128-row ones
+    v, Pv, _ = pkg.attn_plan_call(1, 1, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0, 0, 0)
+    assert v == VT
+    for n in sorted({P, Pv, -(-w.cap // 96)}):
+        _check(pkg, lay, w.n_head, w.n_kv_head, w.cap, "long P=%d" % n, hd=w.head_dim, n_splits=n)
 
 
 def test_full_7b_workload(pkg):
