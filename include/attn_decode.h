@@ -106,12 +106,13 @@ typedef enum {
                                  head_dim 128 or 256 with one query row, head_dim 128 with
                                  several (16 (query row, head) pairs per block);
                                  ATTN_ERR_UNSUPPORTED otherwise. Every split must fit one tile
-                                 (ATTN_ERR_INVALID_ARG otherwise). By block length, for one
-                                 query row,
-                                 with split_len a multiple of 16 that divides T, one block serves
-                                 T / split_len consecutive splits from one tile (cache rows of
-                                 that tile past nkv are then read -- all below cap -- but never
-                                 used). */
+                                 (ATTN_ERR_INVALID_ARG otherwise). By count, a chunk
+                                 ceil(nkv / n_splits) of more than 3T/4 rows is rounded up to
+                                 16 rows, a shorter one to T. By block length, for one query
+                                 row, with split_len a multiple of 16 that divides T, one block
+                                 serves T / split_len consecutive splits from one tile (cache
+                                 rows of that tile past nkv are then read -- all below cap --
+                                 but never used). */
 
 /* Cache element type, OR'd into the variant argument: without it K and V are
    IEEE binary16 (f16); with it they are bfloat16 (1 sign, 8 exponent, 7
@@ -314,9 +315,15 @@ int attn_split_heuristic(int n_seq, int n_head, int n_kv_head, int head_dim, int
  * beside this call's and start their copies while it finishes, and a block
  * takes no more rows than its pipeline holds at once (3 tiles of 64 rows at
  * head_dim 128), so that all of its copies start before the previous kernel
- * ends. Returns 0 for an invalid shape or variant. This is the count-mode
- * plan; a call by block length (split_len > 0) with n_splits = 0 takes
- * P = ceil(cap / split_len) instead.
+ * ends. For the one-tile kernel with one query row the count is the one that
+ * gives each SM two blocks (one with its 128-row tiles at head_dim 256) where
+ * that makes splits of more than three quarters of a tile at full capacity --
+ * the kernel then rounds such chunks to 16 rows rather than to whole tiles, so
+ * the rows spread evenly over the blocks (76 splits of 112 rows for 28 / 4 heads
+ * at capacity 8192 on 152 SMs); else one whole tile per split. Returns 0 for an
+ * invalid shape or variant. This is the count-mode plan; a call by block
+ * length (split_len > 0) with n_splits = 0 takes P = ceil(cap / split_len)
+ * instead.
  */
 int attn_split_heuristic_ex(int n_seq, int n_q, int n_head, int n_kv_head, int head_dim,
                             int64_t cap, int sm_count, int variant);
@@ -329,12 +336,13 @@ int attn_split_heuristic_ex(int n_seq, int n_q, int n_head, int n_kv_head, int h
  * shape. ATTN_VARIANT_AUTO picks a one-tile kernel for a short call -- cap > 0
  * and the heuristic's splits, one tile each, in one wave of its blocks: the
  * one-tile mma.sync kernel (ATTN_VARIANT_TC_TILE; 3 blocks per SM at head_dim
- * 128, 2 at 256) for one query row at head_dim 128 or 256 and for several at
- * 128 (ceil(n_q * group / 16) blocks per split and KV head); else tcgen05 for
- * several query rows at head_dim 256 when n_q * group <= 16 (a KV head's (row,
- * head) pairs in one block, 1 block per SM) -- and otherwise the streaming
- * mma.sync tensor-core kernel (head_dim % 16 == 0) or the CUDA-core kernel.
- * With ATTN_KV_STABLE in
+ * 128, 2 at 256, or 1 with its 128-row tiles at head_dim 256 where one block per
+ * SM makes splits of 97..128 rows) for one query row at head_dim 128 or 256 and
+ * for several at 128 (ceil(n_q * group / 16) blocks per split and KV head);
+ * else tcgen05 for several query rows at head_dim 256 when n_q * group <= 16 (a
+ * KV head's (row, head) pairs in one block, 1 block per SM) -- and otherwise the
+ * streaming mma.sync tensor-core kernel (head_dim % 16 == 0) or the CUDA-core
+ * kernel. With ATTN_KV_STABLE in
  * variant the split count follows the flagged heuristic. With explicit splits
  * that leave a split longer than one tile, or too many blocks for one wave,
  * attn_decode_ex keeps the mma.sync kernel instead. Host only; sm_count <= 0
