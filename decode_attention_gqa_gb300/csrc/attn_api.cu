@@ -156,14 +156,11 @@ int heuristic(int n_seq, int n_kv_head, int qgroups, int64_t cap, int sm_count,
         const int64_t need = (cap + ki.max_chunk - 1) / ki.max_chunk;
         if (P < need) P = need;
     }
-    // The one-tile kernel's balanced chunks: where a count that gives each SM
-    // two blocks (one fewer than fit, leaving a slot for the next call's
-    // early blocks) makes chunks of more than three quarters of a tile at full
-    // capacity, take it: the device rounds such chunks to 16 rows, not to whole
-    // tiles (the 7b layer: 76 splits of 112 rows on 304 blocks instead of 64
-    // tiles on 256, 5.89 -> 5.73 us per layer; shorter contexts still run
-    // whole tiles).
-    // The 128-row tiles at head_dim 256 (one block per SM) take one block per SM.
+    // Balanced chunks (the one-tile kernel's 128-row tiles at head_dim 256, one
+    // block per SM): where a count that gives each SM one block makes chunks of
+    // more than three quarters of a tile at full capacity, take it; the device
+    // rounds such chunks to 16 rows, not to whole tiles (the long layer: 76
+    // splits of 112 rows on all 152 SMs). Shorter contexts run whole tiles.
     if (ki.balanced && cap > 0 && sm_count > 0 && ki.max_chunk > 0) {
         const int per_sm2 = ki.blocks_per_sm >= 3 ? 2 : ki.blocks_per_sm == 1 ? 1 : 0;
         const int64_t P2 = per_sm2 > 0 ? (int64_t)sm_count * per_sm2 / units : 0;

@@ -320,7 +320,10 @@ KernelInfo kernel_info_for_hd(int group, int variant, bool multi)
             const uint32_t smem = multi ? TileCfg<128, kMqHeads, __half, true>::SMEM_BYTES : C::SMEM_BYTES;
             k.blocks_per_sm = (int)(233472u / (smem + 1024u));
             k.max_chunk = C::TILE;
-            k.balanced = !multi;    // several query rows: measured slower with it (7.61 -> 7.72 us, 2 rows)
+            // balanced counts measured slower here: two query rows 7.61 -> 7.72 us; one row
+            // 5.89 -> 5.75 us at full context but 4.40 -> 4.72 / 3.67 -> 3.86 / 3.59 -> 3.74 us
+            // at contexts 2048 / 512 / 128 of the same capacity (more splits, all empty there)
+            k.balanced = false;
             k.available = true;
         }
         return k;

@@ -315,12 +315,12 @@ int attn_split_heuristic(int n_seq, int n_head, int n_kv_head, int head_dim, int
  * beside this call's and start their copies while it finishes, and a block
  * takes no more rows than its pipeline holds at once (3 tiles of 64 rows at
  * head_dim 128), so that all of its copies start before the previous kernel
- * ends. For the one-tile kernel with one query row the count is the one that
- * gives each SM two blocks (one with its 128-row tiles at head_dim 256) where
- * that makes splits of more than three quarters of a tile at full capacity --
- * the kernel then rounds such chunks to 16 rows rather than to whole tiles, so
- * the rows spread evenly over the blocks (76 splits of 112 rows for 28 / 4 heads
- * at capacity 8192 on 152 SMs); else one whole tile per split. Returns 0 for an
+ * ends. For the one-tile kernel's 128-row tiles at head_dim 256 the count is
+ * the one that gives each SM one block where that makes splits of more than
+ * 96 rows at full capacity -- the kernel then rounds such chunks to 16 rows
+ * rather than to whole tiles, so the rows spread evenly over the blocks (76
+ * splits of 112 rows for 16 / 2 heads at capacity 8400 on 152 SMs); otherwise
+ * the one-tile kernel takes one whole tile per split. Returns 0 for an
  * invalid shape or variant. This is the count-mode plan; a call by block
  * length (split_len > 0) with n_splits = 0 takes P = ceil(cap / split_len)
  * instead.

@@ -239,11 +239,8 @@ def torch_sm_count():
 
 
 def test_full_7b_bench_configuration(pkg):
-    # variant 0 runs this short call on the one-tile kernel: two blocks per SM, 76 splits
-    # of 108 -> 112 rows (152 SMs; ceil(8192 / 76) rounded to 16 rows near a tile)
-    P = _bench_configuration(pkg, "7b", L=4)
-    sms = torch_sm_count()
-    assert P == max(64, 2 * sms // 4) if 4 * -(-8192 // (2 * sms // 4)) > 3 * 128 else P == 64
+    # variant 0 runs this short call on the one-tile kernel: 8192 / 128 = 64 splits
+    assert _bench_configuration(pkg, "7b", L=4) == 64
     # the mma.sync kernel at its own split count (blocks of its three-tile ring)
     assert _bench_configuration(pkg, "7b", L=3, variant=pkg.ATTN_VARIANT_TC) == 43
 

@@ -103,8 +103,6 @@ def test_balanced_count_split_around_three_quarters_of_a_tile(pkg):
     rule switches between nkv = 7296 (96-row chunks -> 128) and 7297 (97 -> 112),
     and again at 8513 (113 -> 128; capacity 8704 here). Rows past nkv are NaN."""
     n_head, n_kv, hd, cap, P = 28, 4, 128, 8704, 76
-    v, Pp, _ = pkg.attn_plan_call(1, 1, n_head, n_kv, hd, 8192, 0, 0, 0)
-    assert v == VT and Pp == P                        # what variant 0 plans for the 7b layer
     base = make_case(5350, 1, n_head, n_kv, hd, cap, (cap,))
     for nkv in (1, 1000, 7296, 7297, 7300, 76 * 112, 76 * 112 + 1, 8192, 8600):
         case = dict(base, positions=np.array([nkv - 1], np.int32))
