@@ -156,11 +156,11 @@ int heuristic(int n_seq, int n_kv_head, int qgroups, int64_t cap, int sm_count,
         const int64_t need = (cap + ki.max_chunk - 1) / ki.max_chunk;
         if (P < need) P = need;
     }
-    // Balanced chunks (the one-tile kernel's 128-row tiles at head_dim 256, one
-    // block per SM): where a count that gives each SM one block makes chunks of
-    // more than three quarters of a tile at full capacity, take it; the device
-    // rounds such chunks to 16 rows, not to whole tiles (the long layer: 76
-    // splits of 112 rows on all 152 SMs). Shorter contexts run whole tiles.
+    // Balanced chunks (the one-tile kernel's wide tiles, one block per SM): where a
+    // count that gives each SM one block makes chunks of more than three quarters
+    // of a tile at full capacity, take it; the device rounds such chunks to 16
+    // rows, not to whole tiles (the 7b layer: 38 splits of 224 rows, the long
+    // layer: 76 of 112, on all 152 SMs). Shorter contexts run whole tiles.
     if (ki.balanced && cap > 0 && sm_count > 0 && ki.max_chunk > 0) {
         const int per_sm2 = ki.blocks_per_sm >= 3 ? 2 : ki.blocks_per_sm == 1 ? 1 : 0;
         const int64_t P2 = per_sm2 > 0 ? (int64_t)sm_count * per_sm2 / units : 0;
@@ -217,14 +217,16 @@ bool one_tile_fits(int variant, int head_dim, int group, int n_q, int n_seq, int
 int auto_short_kernel(int head_dim, int group, int n_q, int n_seq, int n_kv_head, int64_t cap,
                       int sm_count, int n_splits, int split_len, bool kv_stable, attn::KernelInfo &ku)
 {
-    // head_dim 256 by count: where one block per SM makes chunks longer than the 96-row
-    // tile (and at most 128 rows), 128-row tiles with balanced chunks, one per SM (the
-    // long layer: 76 splits of 112 rows, 6.32 -> 6.00 us per layer against 88 tiles of
-    // 96 rows on 176 blocks)
-    if (n_q == 1 && head_dim == 256 && n_splits == 0 && split_len == 0 && cap > 0 && sm_count > 0) {
+    // By count: where one block per SM makes chunks of more than three quarters of the
+    // wide tile (256 rows at head_dim 128, 128 at 256), the wide tile with balanced
+    // chunks, one block per SM (the 7b layer: 38 splits of 224 rows, 5.89 -> 5.51 us per
+    // layer at full context; the long layer: 76 splits of 112 rows, 6.32 -> 6.00 us)
+    if (n_q == 1 && (head_dim == 128 || head_dim == 256) && n_splits == 0 && split_len == 0 && cap > 0 &&
+        sm_count > 0) {
+        const int64_t wide = head_dim == 256 ? 128 : 256;      // the wide tile's rows
         const int64_t P1 = (int64_t)sm_count / ((int64_t)n_seq * n_kv_head);
         const int64_t c1 = P1 > 0 ? (cap + P1 - 1) / P1 : 0;
-        if (P1 > 0 && 4 * c1 > 3 * 128 && c1 <= 128 &&
+        if (P1 > 0 && 4 * c1 > 3 * wide && c1 <= wide &&
             one_tile_fits(attn::kVariantTileWide, head_dim, group, n_q, n_seq, n_kv_head, cap, sm_count, n_splits,
                           split_len, kv_stable, ku))
             return attn::kVariantTileWide;
@@ -233,8 +235,9 @@ int auto_short_kernel(int head_dim, int group, int n_q, int n_seq, int n_kv_head
         one_tile_fits(attn::kVariantTile, head_dim, group, n_q, n_seq, n_kv_head, cap, sm_count, n_splits,
                       split_len, kv_stable, ku))
         return attn::kVariantTile;
-    // splits of 97..128 rows at head_dim 256 (block length 128): 128-row tiles, one block per SM
-    if (n_q == 1 && head_dim == 256 &&
+    // splits longer than a tile (block length 128 at head_dim 256, 256 at 128): the wide
+    // tile, one block per SM
+    if (n_q == 1 &&
         one_tile_fits(attn::kVariantTileWide, head_dim, group, n_q, n_seq, n_kv_head, cap, sm_count, n_splits,
                       split_len, kv_stable, ku))
         return attn::kVariantTileWide;
@@ -336,7 +339,7 @@ attn_status finish_plan(DeviceState *ds, int n_seq, int n_head, int n_kv_head, i
     if (split_len > 0 && (int64_t)P * split_len < cap) return ATTN_ERR_INVALID_ARG;
     // the one-tile kernel at head_dim 256 takes splits longer than its 96-row tile
     // in 128-row tiles
-    if (pl.variant == attn::kVariantTile && head_dim == 256 && n_q == 1 &&
+    if (pl.variant == attn::kVariantTile && n_q == 1 &&
         (split_len > 0 ? split_len > pl.ki.max_chunk : (cap_known && (int64_t)P * pl.ki.max_chunk < cap))) {
         const attn::KernelInfo kw = kernel_info(head_dim, pl.group, attn::kVariantTileWide);
         if (kw.available) {

@@ -223,7 +223,7 @@ cudaError_t launch_group(const LaunchRequest &r)
                 if constexpr (HD == 128 || HD == 256) e = launch_partial_tile<HD, G, KV>(r);
                 else return cudaErrorInvalidValue;
             } else if (r.variant == kVariantTileWide) {
-                if constexpr (HD == 256) e = launch_partial_tile<HD, G, KV, true>(r);
+                if constexpr (HD == 128 || HD == 256) e = launch_partial_tile<HD, G, KV, true>(r);
                 else return cudaErrorInvalidValue;
             } else if (r.variant == kVariantTc) {
                 e = launch_partial<TcCfg<HD, G, KV>, HD, G, KV>(r);
@@ -329,7 +329,7 @@ KernelInfo kernel_info_for_hd(int group, int variant, bool multi)
         return k;
     }
     if (variant == kVariantTileWide) {
-        if constexpr (HD == 256) {
+        if constexpr (HD == 128 || HD == 256) {
             if (multi) return k;
             using C = TileCfg<HD, 8, __half, false, true>;
             k.tile_rows = C::TILE;

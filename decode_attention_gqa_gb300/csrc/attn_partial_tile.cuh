@@ -61,14 +61,14 @@ template <int HD, int G, typename KV, bool MQ = false, bool WIDE = false>
 struct TileCfg {
     static_assert(HD == 128 || HD == 256, "the one-tile kernel is built for head_dim 128 and 256");
     static_assert(!MQ || HD == 128, "several query rows: head_dim 128 (two blocks per SM would not fit at 256)");
-    static_assert(!WIDE || (HD == 256 && !MQ), "the wide tile: head_dim 256, one query row");
-    // rows per block: 96 at head_dim 256 so that two blocks fit an SM, or (WIDE) 128
-    // there for splits of 97..128 rows, one block per SM
-    static constexpr int TILE = HD == 256 && !WIDE ? 96 : 128;
-    static constexpr int MINB = HD == 256 ? (WIDE ? 1 : 2) : 3;   // resident blocks per SM
-    // warps: S rows and O dimensions split NW ways (8 warps at head_dim 128 were measured
-    // slower: each warp reads all of Q and P from shared memory, and more warps meet at
-    // each barrier)
+    static_assert(!WIDE || !MQ, "the wide tile: one query row");
+    // rows per block: 128 at head_dim 128 (three blocks per SM), 96 at 256 (two); the
+    // wide tile, one block per SM, takes 256 rows at head_dim 128 and 128 at 256
+    static constexpr int TILE = HD == 256 ? (WIDE ? 128 : 96) : (WIDE ? 256 : 128);
+    static constexpr int MINB = WIDE ? 1 : HD == 256 ? 2 : 3;   // resident blocks per SM
+    // warps: S rows and O dimensions split NW ways (8 warps were measured slower, on the
+    // 128-row tile and on both wide tiles: each warp reads all of Q and P from shared
+    // memory, and more warps meet at each barrier)
     static constexpr int NW = 4;
     static constexpr int THREADS = NW * 32;
     static constexpr int WR = TILE / NW;                // S rows per warp (32 or 24)
@@ -87,18 +87,20 @@ struct TileCfg {
     static constexpr uint32_t OFF_K = 0;
     static constexpr uint32_t OFF_V = TILE_BYTES;
     static constexpr uint32_t OFF_Q = 2 * TILE_BYTES;   // Q tile, then per-head scales
-    static constexpr uint32_t OFF_P = OFF_Q;            // P tile over the Q tile once S is done
-    // P tile(s): 16 rows of TILE elements in 128-byte swizzled chunks of 64 (MQ: hi, then lo)
+    // P tile(s): 16 rows of TILE elements in 128-byte swizzled chunks of 64 (MQ: hi, then lo),
+    // over the Q tile once S is done where they fit there, else after the scales
     static constexpr uint32_t P_TILE = 16u * ((TILE + 63) / 64 * 64) * 2;
     static constexpr uint32_t P_BYTES = (MQ ? 2u : 1u) * P_TILE;
+    static constexpr bool P_OVER_Q = P_BYTES <= Q_AREA;
+    static constexpr uint32_t OFF_P = P_OVER_Q ? OFF_Q : OFF_Q + (QStage::EXTRA_BYTES + 1023) / 1024 * 1024;
     // maxima per warp; sums per warp, or per 8-row group (the several-split kernel); RSL slots each
     static constexpr int NRED = MQ ? NW : (TILE / 8 > NW ? TILE / 8 : NW);
     static constexpr int RSL = MQ ? 16 : 8;
-    static constexpr uint32_t OFF_RED = OFF_Q + (QStage::EXTRA_BYTES + 15) / 16 * 16;   // [2][NRED][RSL] floats
+    static constexpr uint32_t OFF_RED = P_OVER_Q ? OFF_Q + (QStage::EXTRA_BYTES + 15) / 16 * 16
+                                                 : OFF_P + P_BYTES;                   // [2][NRED][RSL] floats
     static constexpr uint32_t OFF_BAR = OFF_RED + 2 * NRED * RSL * 4;                   // 2 mbarriers, flags
     static constexpr uint32_t SMEM_BYTES = OFF_BAR + 2 * 8 + 16 + 1024;                 // + alignment slack
     static constexpr float OFF = 7.f;                   // p headroom: p <= 2^OFF
-    static_assert(P_BYTES <= Q_AREA, "the P tile must not reach the per-head scales");
     static_assert(TILE % 32 == 0 && WR % 8 == 0 && DW % 16 == 0, "fragment shapes");
     static_assert((TILE * 128) % 1024 == 0, "swizzled chunks stay 1024-aligned");
     static_assert(MINB * (SMEM_BYTES + 1024) <= 233472u, "resident blocks per SM");

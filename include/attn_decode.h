@@ -100,9 +100,10 @@ typedef enum {
                                  registers (q and p as hi + lo pairs as above), S split by rows
                                  over four warps, one block-wide maximum, O = P·V split by head
                                  dimension over the warps (no merge of warp states). One tile of
-                                 T rows per block (T = 128; 96 at head_dim 256, or 128 there,
-                                 one block per SM, when a split needs 97..128 rows: block
-                                 lengths 97..128, or n_splits * 96 < cap <= n_splits * 128);
+                                 T rows per block (T = 128; 96 at head_dim 256) or, one block per
+                                 SM, a wide tile of W rows (W = 256 at head_dim 128, 128 at 256)
+                                 when a split needs more than T rows (block lengths T+1..W, or
+                                 n_splits * T < cap <= n_splits * W);
                                  head_dim 128 or 256 with one query row, head_dim 128 with
                                  several (16 (query row, head) pairs per block);
                                  ATTN_ERR_UNSUPPORTED otherwise. Every split must fit one tile
@@ -315,12 +316,13 @@ int attn_split_heuristic(int n_seq, int n_head, int n_kv_head, int head_dim, int
  * beside this call's and start their copies while it finishes, and a block
  * takes no more rows than its pipeline holds at once (3 tiles of 64 rows at
  * head_dim 128), so that all of its copies start before the previous kernel
- * ends. For the one-tile kernel's 128-row tiles at head_dim 256 the count is
- * the one that gives each SM one block where that makes splits of more than
- * 96 rows at full capacity -- the kernel then rounds such chunks to 16 rows
- * rather than to whole tiles, so the rows spread evenly over the blocks (76
- * splits of 112 rows for 16 / 2 heads at capacity 8400 on 152 SMs); otherwise
- * the one-tile kernel takes one whole tile per split. Returns 0 for an
+ * ends. For the one-tile kernel's wide tiles (256 rows at head_dim 128, 128
+ * at 256, one block per SM) the count is the one that gives each SM one block,
+ * where that makes splits of more than three quarters of the wide tile at full
+ * capacity -- the kernel then rounds such chunks to 16 rows rather than to
+ * whole tiles, so the rows spread evenly over the blocks (38 splits of 224 rows
+ * for 28 / 4 heads at capacity 8192, 76 of 112 for 16 / 2 heads at 8400, on
+ * 152 SMs); otherwise one whole (128- or 96-row) tile per split. Returns 0 for an
  * invalid shape or variant. This is the count-mode plan; a call by block
  * length (split_len > 0) with n_splits = 0 takes P = ceil(cap / split_len)
  * instead.
@@ -336,8 +338,8 @@ int attn_split_heuristic_ex(int n_seq, int n_q, int n_head, int n_kv_head, int h
  * shape. ATTN_VARIANT_AUTO picks a one-tile kernel for a short call -- cap > 0
  * and the heuristic's splits, one tile each, in one wave of its blocks: the
  * one-tile mma.sync kernel (ATTN_VARIANT_TC_TILE; 3 blocks per SM at head_dim
- * 128, 2 at 256, or 1 with its 128-row tiles at head_dim 256 where one block per
- * SM makes splits of 97..128 rows) for one query row at head_dim 128 or 256 and
+ * 128, 2 at 256, or 1 with its wide tiles where one block per SM makes splits
+ * longer than the plain tile) for one query row at head_dim 128 or 256 and
  * for several at 128 (ceil(n_q * group / 16) blocks per split and KV head);
  * else tcgen05 for several query rows at head_dim 256 when n_q * group <= 16 (a
  * KV head's (row, head) pairs in one block, 1 block per SM) -- and otherwise the

@@ -91,12 +91,14 @@ def test_split_heuristic_host_only(lib):
                                        pkg.ATTN_VARIANT_TCGEN05_CLUSTER) == 16
     # ... and the CUDA-core kernel's are 32-row warp slices: 40 rows -> 2 splits
     assert pkg.attn_split_heuristic_ex(1, 1, 8, 2, 128, 40, 152, pkg.ATTN_VARIANT_SIMT) == 2
-    # one sequence, 28/4 heads at 8192 rows: variant 0 is the one-tile kernel, one
-    # 128-row tile per split, 8192 / 128 = 64; the mma.sync kernel fills one wave,
-    # 4 x 64 blocks of 128 rows
-    assert pkg.attn_split_heuristic(1, 28, 4, 128, 8192, 152) == 64
+    # one sequence, 28/4 heads at 8192 rows: variant 0 is the one-tile kernel with its
+    # 256-row tiles, one block per SM: 152 / 4 = 38 splits of 216 -> 224 rows (more than
+    # three quarters of the tile); the mma.sync kernel fills one wave, 4 x 64 blocks of
+    # 128 rows; at 148 SMs 37 splits of 222 -> 224 rows; at 6000 rows one block per SM
+    # would make 158-row chunks, so 128-row tiles, ceil(6000 / 128) = 47
+    assert pkg.attn_split_heuristic(1, 28, 4, 128, 8192, 152) == 38
     assert pkg.attn_split_heuristic_ex(1, 1, 28, 4, 128, 8192, 152, pkg.ATTN_VARIANT_TC) == 64
-    assert pkg.attn_split_heuristic(1, 28, 4, 128, 8192, 148) == 64
+    assert pkg.attn_split_heuristic(1, 28, 4, 128, 8192, 148) == 37
     assert pkg.attn_split_heuristic(1, 28, 4, 128, 6000, 152) == 47
     # a batch aims at eight waves so ragged lengths still balance
     assert pkg.attn_split_heuristic(32, 32, 8, 128, 32768, 152) == 10
@@ -113,12 +115,12 @@ def test_split_heuristic_for_flagged_calls(lib):
         return pkg.attn_split_heuristic_ex(n_seq, n_q, n_head, n_kv, hd, cap, sms, variant)
     # the plain call and variant 0 agree; the element type does not change P
     assert h(1, 28, 4, 128, 8192, 152, 0) == pkg.attn_split_heuristic(1, 28, 4, 128, 8192, 152)
-    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_BF16) == 64
-    # variant 0 on this short call is the one-tile kernel, as is tcgen05: one 128-row
-    # tile per split
+    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_BF16) == 38
+    # variant 0 on this short call is the one-tile kernel (256-row tiles, 38 balanced
+    # splits); tcgen05 takes one 128-row tile per split
     S, TC, T5 = pkg.ATTN_KV_STABLE, pkg.ATTN_VARIANT_TC, pkg.ATTN_VARIANT_TCGEN05
-    assert h(1, 28, 4, 128, 8192, 152, S) == h(1, 28, 4, 128, 8192, 152, T5 | S) == 64
-    assert h(1, 28, 4, 128, 8192, 152, S | pkg.ATTN_KV_BF16) == 64
+    assert h(1, 28, 4, 128, 8192, 152, S) == 38 and h(1, 28, 4, 128, 8192, 152, T5 | S) == 64
+    assert h(1, 28, 4, 128, 8192, 152, S | pkg.ATTN_KV_BF16) == 38
     assert h(1, 28, 4, 128, 2048, 152, S) == 16
     # mma.sync kernel, early start, one sequence: one block per SM would give each
     # block 256 rows, more than its 3 x 64-row stage ring, so blocks of 192 rows: 4 x 43
@@ -301,7 +303,7 @@ int main(void) {
     if (attn_version() <= 0) return 1;
     if (strcmp(attn_status_string(ATTN_ERR_WORKSPACE), "ATTN_ERR_WORKSPACE") != 0) return 2;
     if (attn_workspace_size(1, 28, 128, 37) == 0) return 3;
-    if (attn_split_heuristic(1, 28, 4, 128, 8192, 152) != 64) return 4;
+    if (attn_split_heuristic(1, 28, 4, 128, 8192, 152) != 38) return 4;
     if (attn_split_heuristic_ex(1, 1, 28, 4, 128, 8192, 152, ATTN_KV_STABLE | ATTN_VARIANT_TC) != 43)
         return 5;
     if (attn_split_heuristic_ex(1, 1, 28, 4, 128, 8192, 152, ATTN_VARIANT_TCGEN05) != 64) return 10;
@@ -366,8 +368,9 @@ def test_tcgen05_choice_keeps_its_limits(lib):
             continue
         seen.add((hd, n_q > 1))
         assert hd in (128, 256)
-        # the one-tile kernel may take 128-row tiles at head_dim 256 (one block per SM)
-        assert P * (128 if v == VT else tile[hd]) >= cap
+        # the one-tile kernel may take its wide tiles (one block per SM): 256 rows at
+        # head_dim 128, 128 at 256
+        assert P * ((256 if hd == 128 else 128) if v == VT else tile[hd]) >= cap
         if v == VT:
             # 16 (row, head) slots per block; 3 blocks per SM at head_dim 128, 2 at 256
             assert n_q == 1 or hd == 128

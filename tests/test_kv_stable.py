@@ -239,8 +239,14 @@ def torch_sm_count():
 
 
 def test_full_7b_bench_configuration(pkg):
-    # variant 0 runs this short call on the one-tile kernel: 8192 / 128 = 64 splits
-    assert _bench_configuration(pkg, "7b", L=4) == 64
+    # variant 0 runs this short call on the one-tile kernel: 256-row tiles, one block per
+    # SM, 38 splits of 216 -> 224 rows on 152 SMs (128-row tiles, 64, where one block per
+    # SM would leave chunks of 192 rows or fewer)
+    P = _bench_configuration(pkg, "7b", L=4)
+    P1 = torch_sm_count() // 4
+    c1 = -(-8192 // P1)
+    assert P == (P1 if 192 < c1 <= 256 else 64)
+    assert _bench_configuration(pkg, "7b", L=3, variant=pkg.ATTN_VARIANT_TC_TILE) == 64
     # the mma.sync kernel at its own split count (blocks of its three-tile ring)
     assert _bench_configuration(pkg, "7b", L=3, variant=pkg.ATTN_VARIANT_TC) == 43
 

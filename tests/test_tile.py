@@ -234,9 +234,9 @@ def test_full_7b_workload(pkg):
 def test_arguments_that_leave_a_split_larger_than_a_tile(pkg):
     import torch
     case = to_device(make_case(6000, 1, 8, 2, 128, 1024, (1000,)))
-    bad = [dict(n_splits=7),                          # 7 * 128 < 1024
-           dict(n_splits=8, split_len=129),
-           dict(n_splits=4, split_len=256)]
+    bad = [dict(n_splits=3),                          # 3 * 256 < 1024 (256-row tiles at most)
+           dict(n_splits=4, split_len=257),
+           dict(n_splits=2, split_len=512)]
     for kw in bad:
         with pytest.raises(pkg.AttnError) as ei:
             run_decode(pkg, case, 8, 2, 128, 1024, 0.1, variant=VT, **kw)
@@ -353,20 +353,26 @@ def test_full_long_workload_block_32(pkg):
 
 # ---- splits of 97..128 rows at head_dim 256: 128-row tiles, one block per SM ----
 
-@pytest.mark.parametrize("G", [1, 5, 8])
-def test_wide_tile_block_and_count_boundaries(pkg, G):
-    """Block lengths 97..128 and split counts with 96 P < cap <= 128 P run
-    128-row tiles at head_dim 256; every nkv around the split edges, rows past
-    nkv NaN."""
-    hd, n_kv, cap = 256, 2, 1100
+@pytest.mark.parametrize("hd,G", [(256, 1), (256, 5), (256, 8), (128, 1), (128, 7), (128, 8)])
+def test_wide_tile_block_and_count_boundaries(pkg, hd, G):
+    """Splits longer than the tile run the wide tile, one block per SM: block
+    lengths 97..128 and split counts with 96 P < cap <= 128 P at head_dim 256
+    (128-row tiles), block lengths 129..256 and 128 P < cap <= 256 P at 128
+    (256-row tiles); every nkv around the split edges, rows past nkv NaN."""
+    n_kv, cap = 2, 1100
+    W = 128 if hd == 256 else 256                       # the wide tile's rows
     n_head = G * n_kv
-    base = make_case(6500 + G, 1, n_head, n_kv, hd, cap, (cap,))
+    base = make_case(6500 + G + hd, 1, n_head, n_kv, hd, cap, (cap,))
     scale = 1 / math.sqrt(hd)
-    for P, blk in ((-(-cap // 128), 128), (-(-cap // 112), 112), (-(-cap // 97), 97), (9, 0), (10, 0), (11, 0)):
+    if hd == 256:
+        cases = ((-(-cap // 128), 128), (-(-cap // 112), 112), (-(-cap // 97), 97), (9, 0), (10, 0), (11, 0))
+    else:
+        cases = ((-(-cap // 256), 256), (-(-cap // 200), 200), (-(-cap // 129), 129), (5, 0), (6, 0), (8, 0))
+    for P, blk in cases:
         v, Pp, _ = pkg.attn_plan_call(1, 1, n_head, n_kv, hd, cap, P, blk, VT)
         assert v == VT and Pp == P
         c = -(-cap // P)                                # by count: near a tile, 16-row chunks
-        edge = blk if blk else (-(-c // 16) * 16 if 4 * c > 3 * 128 else -(-c // 128) * 128)
+        edge = blk if blk else (-(-c // 16) * 16 if 4 * c > 3 * W else -(-c // W) * W)
         for nkv in (1, edge - 1, edge, edge + 1, 3 * edge + 7, cap - 1, cap):
             case = dict(base, positions=np.array([nkv - 1], np.int32))
             case["k"] = base["k"].copy()
@@ -414,6 +420,19 @@ def test_wide_tile_fused_append_and_bf16(pkg):
 def test_wide_tile_stable_chain(pkg):
     _chain(pkg, L=4, n_head=16, n_kv=2, hd=256, cap=2560, ctx=(2000,), P=20, blk=128,
            variant=VT, graph=True, replays=2, seed=6800)
+
+
+def test_full_7b_workload_on_256_row_tiles(pkg):
+    """What variant 0 plans for the 7b layer (256-row tiles, balanced splits),
+    at full capacity and shorter contexts, and block length 256."""
+    w = syn.WORKLOADS["7b"]
+    lay = syn.make_layer(w)
+    v, P, _ = pkg.attn_plan_call(1, 1, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0, 0, 0)
+    assert v == VT and P * 256 >= w.cap
+    for ctx in (w.cap, 7777, 2048, 129):
+        case = dict(lay, positions=np.array([ctx - 1], np.int32))
+        _check(pkg, case, w.n_head, w.n_kv_head, w.cap, "7b P=%d ctx %d" % (P, ctx), n_splits=P)
+    _check(pkg, lay, w.n_head, w.n_kv_head, w.cap, "7b blk 256", split_len=256)
 
 
 @pytest.mark.parametrize("blk", [64, 128])
