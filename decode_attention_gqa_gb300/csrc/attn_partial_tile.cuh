@@ -252,11 +252,11 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
 
     // a2, while the tile is in flight: the Q tile and the per-head scales
     if (stable) pdl_wait();
-    Cfg::QStage::template prepare<Cfg::THREADS>(smem + Cfg::OFF_Q, a, s, hk, 0, tid);
     // Fused append: the split ending at nkv holds the new row nkv - 1 as the
-    // tile's last row, which is in warp 3's S rows; warp 3 fetches it now (one
-    // 16-byte unit per lane) and writes it into both tiles and the cache once
-    // they have landed, before the barrier that precedes any read of V.
+    // tile's last row, which is in the last warp's S rows; that warp fetches it
+    // now (one 16-byte unit per lane, issued before q's loads so that both are in
+    // flight together) and writes each half into its tile and the cache once that
+    // tile has landed (V's before the barrier that precedes any read of V).
     constexpr int NU = HD / 8;                    // 16-byte units per row
     constexpr int NJ = 2 * NU / 32;               // units of the new K and V rows per lane
     static_assert(2 * NU % 32 == 0, "whole units per lane");
@@ -270,27 +270,29 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
             newrow[j] = ld_dep(reinterpret_cast<const uint4 *>((i < NU ? a.k_new : a.v_new) + src) + (i % NU));
         }
     }
+    Cfg::QStage::template prepare<Cfg::THREADS>(smem + Cfg::OFF_Q, a, s, hk, 0, tid);
     __syncthreads();
 
     const float inv = reinterpret_cast<const float *>(smem + Cfg::OFF_Q + Cfg::QStage::QT_BYTES)[lane >> 2];
     const int g = lane >> 2, t = lane & 3;
     bool ok = mbar_wait_bounded(bar + 0, 0);
     ok = __all_sync(0xffffffffu, ok);
-    if (ok && appending) {
-        const bool vl = __all_sync(0xffffffffu, mbar_wait_bounded(bar + 1, 0));
-        if (vl) {
-            const size_t dst = ((size_t)((int64_t)s * a.cap + nkv - 1) * a.n_kv_head + hk) * HD;
+    // the new row's K half into the K tile and the cache once K has landed (S reads
+    // it); its V half waits for V below, so that S does not
+    const size_t new_dst = ((size_t)((int64_t)s * a.cap + nkv - 1) * a.n_kv_head + hk) * HD;
+    auto put_new_row = [&](bool k_half) {
 #pragma unroll
-            for (int j = 0; j < NJ; ++j) {
-                const int i = lane + 32 * j;
-                uint8_t *tile = smem + (i < NU ? Cfg::OFF_K : Cfg::OFF_V);
-                *reinterpret_cast<uint4 *>(tile + tile_unit_offset<HD, TILE>(TILE - 1, i % NU)) = newrow[j];
-                reinterpret_cast<uint4 *>((i < NU ? a.k_w : a.v_w) + dst)[i % NU] = newrow[j];
+        for (int j = 0; j < NJ; ++j) {
+            const int i = lane + 32 * j;
+            if ((i < NU) == k_half) {
+                *reinterpret_cast<uint4 *>(smem + (k_half ? Cfg::OFF_K : Cfg::OFF_V) +
+                                           tile_unit_offset<HD, TILE>(TILE - 1, i % NU)) = newrow[j];
+                reinterpret_cast<uint4 *>((k_half ? a.k_w : a.v_w) + new_dst)[i % NU] = newrow[j];
             }
-            __syncwarp();
         }
-        ok = vl;
-    }
+        __syncwarp();
+    };
+    if (ok && appending) put_new_row(true);
     if (!ok && lane == 0) { flags[0] = 1; atomicOr(a.err, kErrPipelineTimeout); }
 
     // ---- a3: S for this warp's rows r0 .. r0 + WR - 1 ----
@@ -342,7 +344,8 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
         if (t == 0) red_l[warp * 8 + g] = lsum;
     }
     bool vok = ok;
-    if (vok && !appending) vok = __all_sync(0xffffffffu, mbar_wait_bounded(bar + 1, 0));
+    if (vok) vok = __all_sync(0xffffffffu, mbar_wait_bounded(bar + 1, 0));
+    if (vok && appending) put_new_row(false);
     if (ok && !vok && lane == 0) { flags[0] = 1; atomicOr(a.err, kErrPipelineTimeout); }
     __syncthreads();                          // P and the sums are in; every V wait is done
     // ---- a5: O = P · V for this warp's dimensions d0 .. d0 + DW - 1 ----
