@@ -145,10 +145,12 @@ __device__ __forceinline__ void split_range(int64_t nkv, int sp, int n_splits, i
 
 // split_range for the one-tile kernel (tile rows per block, count mode): a
 // chunk that would fill more than three quarters of a tile is rounded up to 16
-// rows only, so that a split count sized for two blocks per SM balances the
-// rows over the blocks (the 7b layer at full context: 76 splits of 108 -> 112
-// rows instead of 64 whole tiles on 256 blocks of 152 SMs); shorter chunks are
-// rounded up to whole tiles (few, full blocks for short contexts).
+// rows only, so that a split count sized for one block per SM balances the
+// rows over the blocks (the 7b layer at full context on 256-row tiles: 38
+// splits of 216 -> 224 rows on 152 SMs); shorter chunks are rounded up to whole
+// tiles (few, full blocks for short contexts), or, on the 256-row tile while
+// the context fits in four tiles, to half tiles, which that kernel runs on its
+// last 128 rows only (twice the blocks, each with the 128-row tile's chain).
 __device__ __forceinline__ void split_range_tile(int64_t nkv, int sp, int n_splits, int split_len,
                                                  int tile, int64_t &lo, int64_t &hi)
 {
@@ -157,7 +159,9 @@ __device__ __forceinline__ void split_range_tile(int64_t nkv, int sp, int n_spli
         return;
     }
     int64_t chunk = (nkv + n_splits - 1) / n_splits;
-    chunk = 4 * chunk > 3 * (int64_t)tile ? (chunk + 15) / 16 * 16 : (chunk + tile - 1) / tile * tile;
+    chunk = 4 * chunk > 3 * (int64_t)tile ? (chunk + 15) / 16 * 16
+          : tile >= 256 && nkv <= 4 * (int64_t)tile && 2 * chunk <= (int64_t)tile ? (int64_t)tile / 2
+          : (chunk + tile - 1) / tile * tile;
     lo = (int64_t)sp * chunk;
     hi = lo + chunk < nkv ? lo + chunk : nkv;
 }

@@ -35,6 +35,8 @@
 // writes each split's partial for its dimensions.
 #pragma once
 
+#include <type_traits>
+
 #include "attn_device.cuh"
 #include "attn_warp_tc.cuh"
 #include "attn_warp_tcmq.cuh"
@@ -110,10 +112,10 @@ struct TileCfg {
 // a3 for one warp: S = Q · Kᵀ over tile rows r0 .. r0 + WR - 1 (Q fragments in
 // registers, K by ldmatrix), even and odd k-steps in separate accumulators;
 // head g's score for row r0 + 8j + 2t + e is (c[.][j][e] + c[.][j][2 + e]).
-template <class Cfg, int HD, typename KV>
-__device__ __forceinline__ void tile_scores(const uint8_t *smem, int r0, int lane, float (&c)[2][Cfg::NS][4])
+template <class Cfg, int HD, typename KV, int NS = Cfg::NS>
+__device__ __forceinline__ void tile_scores(const uint8_t *smem, int r0, int lane, float (&c)[2][NS][4])
 {
-    constexpr int TILE = Cfg::TILE, NS = Cfg::NS, KS = Cfg::KS;
+    constexpr int TILE = Cfg::TILE, KS = Cfg::KS;
     const uint8_t *qt = smem + Cfg::OFF_Q;
     const int i8 = lane >> 3;
     uint32_t qa[Cfg::Q_REGS ? KS : 1][4];
@@ -295,20 +297,25 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
     if (ok && appending) put_new_row(true);
     if (!ok && lane == 0) { flags[0] = 1; atomicOr(a.err, kErrPipelineTimeout); }
 
-    // ---- a3: S for this warp's rows r0 .. r0 + WR - 1 ----
-    const int r0 = warp * Cfg::WR;
-    float sc[NS][2];                          // head g, rows r0 + 8j + 2t + {0, 1}
+    // a3 .. a6 for NSX S n-tiles per warp from tile row 16 K0 on: the whole tile
+    // (NSX = NS, K0 = 0), or, in the 256-row tile, its last 128 rows only when the
+    // split has no more (NSX = NS / 2, K0 = KO / 2: the chain of the 128-row tile)
+    auto rows_from = [&](auto nsx_c, auto k0_c) {
+    constexpr int NSX = decltype(nsx_c)::value, K0 = decltype(k0_c)::value;
+    // ---- a3: S for this warp's rows r0 .. r0 + 8 NSX - 1 ----
+    const int r0 = 16 * K0 + warp * 8 * NSX;
+    float sc[NSX][2];                         // head g, rows r0 + 8j + 2t + {0, 1}
     {
-        float c[2][NS][4];
+        float c[2][NSX][4];
 #pragma unroll
         for (int e = 0; e < 2; ++e)
 #pragma unroll
-            for (int j = 0; j < NS; ++j)
+            for (int j = 0; j < NSX; ++j)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) c[e][j][i] = 0.f;
-        if (ok) tile_scores<Cfg, HD, KV>(smem, r0, lane, c);
+        if (ok) tile_scores<Cfg, HD, KV, NSX>(smem, r0, lane, c);
 #pragma unroll
-        for (int j = 0; j < NS; ++j)
+        for (int j = 0; j < NSX; ++j)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int r = r0 + 8 * j + 2 * t + e;   // tile row
@@ -320,7 +327,7 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
     {
         float m = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < NS; ++j) m = fmaxf(m, fmaxf(sc[j][0], sc[j][1]));
+        for (int j = 0; j < NSX; ++j) m = fmaxf(m, fmaxf(sc[j][0], sc[j][1]));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
         if (t == 0) red_m[warp * 8 + g] = m;
@@ -334,7 +341,7 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
         float lsum = 0.f;
         uint8_t *pt = smem + Cfg::OFF_P;
 #pragma unroll
-        for (int j = 0; j < NS; ++j) {
+        for (int j = 0; j < NSX; ++j) {
             const float p0 = ex2(sc[j][0] - base), p1 = ex2(sc[j][1] - base);   // 0 at -inf
             lsum += p0 + p1;
             store_p_pair<Cfg, KV>(pt, r0 + 8 * j, g, t, p0, p1);
@@ -359,7 +366,11 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
             for (int j = 0; j < NO; ++j)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) o[e][j][i] = 0.f;
-        tile_pv<Cfg, HD, KV>(smem, d0, lane, 0, KO, o);
+#pragma unroll
+        for (int kk = K0; kk < KO; kk += 2) {
+            tile_pv_step<Cfg, HD, KV>(smem, d0, lane, kk, o[0]);
+            if (kk + 1 < KO) tile_pv_step<Cfg, HD, KV>(smem, d0, lane, kk + 1, o[1]);
+        }
         // ---- a6: oc of every head for these dimensions; (mx, S) per head ----
         if (g < G) {
             float *dst = a.ws_o + (((size_t)s * heads + (size_t)hk * G + g) * P + sp) * HD + d0 + 2 * t;
@@ -380,6 +391,13 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
         // wait (bounded) for both copies before leaving
         (void)mbar_wait_bounded(bar + 0, 0);
         (void)mbar_wait_bounded(bar + 1, 0);
+    }
+    };
+    if constexpr (TILE == 256) {
+        if (n <= TILE / 2) rows_from(std::integral_constant<int, NS / 2>{}, std::integral_constant<int, KO / 2>{});
+        else rows_from(std::integral_constant<int, NS>{}, std::integral_constant<int, 0>{});
+    } else {
+        rows_from(std::integral_constant<int, NS>{}, std::integral_constant<int, 0>{});
     }
 }
 

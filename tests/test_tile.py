@@ -424,12 +424,14 @@ def test_wide_tile_stable_chain(pkg):
 
 def test_full_7b_workload_on_256_row_tiles(pkg):
     """What variant 0 plans for the 7b layer (256-row tiles, balanced splits),
-    at full capacity and shorter contexts, and block length 256."""
+    at full capacity and shorter contexts -- whole 256-row tiles, and half tiles
+    (each block on its last 128 rows) while the context fits in four tiles --
+    and block length 256."""
     w = syn.WORKLOADS["7b"]
     lay = syn.make_layer(w)
     v, P, _ = pkg.attn_plan_call(1, 1, w.n_head, w.n_kv_head, w.head_dim, w.cap, 0, 0, 0)
     assert v == VT and P * 256 >= w.cap
-    for ctx in (w.cap, 7777, 2048, 129):
+    for ctx in (w.cap, 7777, 2048, 1025, 1024, 1023, 513, 512, 257, 256, 129, 128, 1):
         case = dict(lay, positions=np.array([ctx - 1], np.int32))
         _check(pkg, case, w.n_head, w.n_kv_head, w.cap, "7b P=%d ctx %d" % (P, ctx), n_splits=P)
     _check(pkg, lay, w.n_head, w.n_kv_head, w.cap, "7b blk 256", split_len=256)
