@@ -301,97 +301,97 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
     // (NSX = NS, K0 = 0), or, in the 256-row tile, its last 128 rows only when the
     // split has no more (NSX = NS / 2, K0 = KO / 2: the chain of the 128-row tile)
     auto rows_from = [&](auto nsx_c, auto k0_c) {
-    constexpr int NSX = decltype(nsx_c)::value, K0 = decltype(k0_c)::value;
-    // ---- a3: S for this warp's rows r0 .. r0 + 8 NSX - 1 ----
-    const int r0 = 16 * K0 + warp * 8 * NSX;
-    float sc[NSX][2];                         // head g, rows r0 + 8j + 2t + {0, 1}
-    {
-        float c[2][NSX][4];
+        constexpr int NSX = decltype(nsx_c)::value, K0 = decltype(k0_c)::value;
+        // ---- a3: S for this warp's rows r0 .. r0 + 8 NSX - 1 ----
+        const int r0 = 16 * K0 + warp * 8 * NSX;
+        float sc[NSX][2];                         // head g, rows r0 + 8j + 2t + {0, 1}
+        {
+            float c[2][NSX][4];
 #pragma unroll
-        for (int e = 0; e < 2; ++e)
+            for (int e = 0; e < 2; ++e)
+#pragma unroll
+                for (int j = 0; j < NSX; ++j)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) c[e][j][i] = 0.f;
+            if (ok) tile_scores<Cfg, HD, KV, NSX>(smem, r0, lane, c);
 #pragma unroll
             for (int j = 0; j < NSX; ++j)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) c[e][j][i] = 0.f;
-        if (ok) tile_scores<Cfg, HD, KV, NSX>(smem, r0, lane, c);
+                for (int e = 0; e < 2; ++e) {
+                    const int r = r0 + 8 * j + 2 * t + e;   // tile row
+                    const float v = ((c[0][j][e] + c[1][j][e]) + (c[0][j][2 + e] + c[1][j][2 + e])) * inv;
+                    sc[j][e] = r >= TILE - n ? v : -INFINITY;
+                }
+        }
+        // ---- a4: each head's maximum over the block ----
+        {
+            float m = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < NSX; ++j)
+            for (int j = 0; j < NSX; ++j) m = fmaxf(m, fmaxf(sc[j][0], sc[j][1]));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            if (t == 0) red_m[warp * 8 + g] = m;
+        }
+        __syncthreads();                          // the maxima are in; S is done, so Q is dead
+        float M = red_m[g];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int r = r0 + 8 * j + 2 * t + e;   // tile row
-                const float v = ((c[0][j][e] + c[1][j][e]) + (c[0][j][2 + e] + c[1][j][2 + e])) * inv;
-                sc[j][e] = r >= TILE - n ? v : -INFINITY;
+        for (int w = 1; w < Cfg::NW; ++w) M = fmaxf(M, red_m[w * 8 + g]);
+        const float base = M - Cfg::OFF;          // M is finite: the split has rows in every block
+        {
+            float lsum = 0.f;
+            uint8_t *pt = smem + Cfg::OFF_P;
+#pragma unroll
+            for (int j = 0; j < NSX; ++j) {
+                const float p0 = ex2(sc[j][0] - base), p1 = ex2(sc[j][1] - base);   // 0 at -inf
+                lsum += p0 + p1;
+                store_p_pair<Cfg, KV>(pt, r0 + 8 * j, g, t, p0, p1);
             }
-    }
-    // ---- a4: each head's maximum over the block ----
-    {
-        float m = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < NSX; ++j) m = fmaxf(m, fmaxf(sc[j][0], sc[j][1]));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        if (t == 0) red_m[warp * 8 + g] = m;
-    }
-    __syncthreads();                          // the maxima are in; S is done, so Q is dead
-    float M = red_m[g];
-#pragma unroll
-    for (int w = 1; w < Cfg::NW; ++w) M = fmaxf(M, red_m[w * 8 + g]);
-    const float base = M - Cfg::OFF;          // M is finite: the split has rows in every block
-    {
-        float lsum = 0.f;
-        uint8_t *pt = smem + Cfg::OFF_P;
-#pragma unroll
-        for (int j = 0; j < NSX; ++j) {
-            const float p0 = ex2(sc[j][0] - base), p1 = ex2(sc[j][1] - base);   // 0 at -inf
-            lsum += p0 + p1;
-            store_p_pair<Cfg, KV>(pt, r0 + 8 * j, g, t, p0, p1);
+            lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+            lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+            if (t == 0) red_l[warp * 8 + g] = lsum;
         }
-        lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
-        lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
-        if (t == 0) red_l[warp * 8 + g] = lsum;
-    }
-    bool vok = ok;
-    if (vok) vok = __all_sync(0xffffffffu, mbar_wait_bounded(bar + 1, 0));
-    if (vok && appending) put_new_row(false);
-    if (ok && !vok && lane == 0) { flags[0] = 1; atomicOr(a.err, kErrPipelineTimeout); }
-    __syncthreads();                          // P and the sums are in; every V wait is done
-    // ---- a5: O = P · V for this warp's dimensions d0 .. d0 + DW - 1 ----
-    const int d0 = warp * Cfg::DW;
-    const bool abort = flags[0] != 0;         // the same for every thread past the barrier
-    if (!abort) {
-        float o[2][NO][4];
+        bool vok = ok;
+        if (vok) vok = __all_sync(0xffffffffu, mbar_wait_bounded(bar + 1, 0));
+        if (vok && appending) put_new_row(false);
+        if (ok && !vok && lane == 0) { flags[0] = 1; atomicOr(a.err, kErrPipelineTimeout); }
+        __syncthreads();                          // P and the sums are in; every V wait is done
+        // ---- a5: O = P · V for this warp's dimensions d0 .. d0 + DW - 1 ----
+        const int d0 = warp * Cfg::DW;
+        const bool abort = flags[0] != 0;         // the same for every thread past the barrier
+        if (!abort) {
+            float o[2][NO][4];
 #pragma unroll
-        for (int e = 0; e < 2; ++e)
+            for (int e = 0; e < 2; ++e)
 #pragma unroll
-            for (int j = 0; j < NO; ++j)
+                for (int j = 0; j < NO; ++j)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) o[e][j][i] = 0.f;
+                    for (int i = 0; i < 4; ++i) o[e][j][i] = 0.f;
 #pragma unroll
-        for (int kk = K0; kk < KO; kk += 2) {
-            tile_pv_step<Cfg, HD, KV>(smem, d0, lane, kk, o[0]);
-            if (kk + 1 < KO) tile_pv_step<Cfg, HD, KV>(smem, d0, lane, kk + 1, o[1]);
+            for (int kk = K0; kk < KO; kk += 2) {
+                tile_pv_step<Cfg, HD, KV>(smem, d0, lane, kk, o[0]);
+                if (kk + 1 < KO) tile_pv_step<Cfg, HD, KV>(smem, d0, lane, kk + 1, o[1]);
+            }
+            // ---- a6: oc of every head for these dimensions; (mx, S) per head ----
+            if (g < G) {
+                float *dst = a.ws_o + (((size_t)s * heads + (size_t)hk * G + g) * P + sp) * HD + d0 + 2 * t;
+#pragma unroll
+                for (int j = 0; j < NO; ++j)
+                    *reinterpret_cast<float2 *>(dst + 8 * j) =
+                        make_float2((o[0][j][0] + o[1][j][0]) + (o[0][j][2] + o[1][j][2]),
+                                    (o[0][j][1] + o[1][j][1]) + (o[0][j][3] + o[1][j][3]));
+            }
+            if (warp == 0 && t == 0 && g < G) {
+                float L = 0.f;
+#pragma unroll
+                for (int w = 0; w < Cfg::NW; ++w) L += red_l[w * 8 + g];
+                a.ws_ml[((size_t)s * heads + (size_t)hk * G + g) * P + sp] = make_float2(base, L);
+            }
+        } else if (tid == 0) {
+            // nothing may still be writing shared memory when the block exits:
+            // wait (bounded) for both copies before leaving
+            (void)mbar_wait_bounded(bar + 0, 0);
+            (void)mbar_wait_bounded(bar + 1, 0);
         }
-        // ---- a6: oc of every head for these dimensions; (mx, S) per head ----
-        if (g < G) {
-            float *dst = a.ws_o + (((size_t)s * heads + (size_t)hk * G + g) * P + sp) * HD + d0 + 2 * t;
-#pragma unroll
-            for (int j = 0; j < NO; ++j)
-                *reinterpret_cast<float2 *>(dst + 8 * j) =
-                    make_float2((o[0][j][0] + o[1][j][0]) + (o[0][j][2] + o[1][j][2]),
-                                (o[0][j][1] + o[1][j][1]) + (o[0][j][3] + o[1][j][3]));
-        }
-        if (warp == 0 && t == 0 && g < G) {
-            float L = 0.f;
-#pragma unroll
-            for (int w = 0; w < Cfg::NW; ++w) L += red_l[w * 8 + g];
-            a.ws_ml[((size_t)s * heads + (size_t)hk * G + g) * P + sp] = make_float2(base, L);
-        }
-    } else if (tid == 0) {
-        // nothing may still be writing shared memory when the block exits:
-        // wait (bounded) for both copies before leaving
-        (void)mbar_wait_bounded(bar + 0, 0);
-        (void)mbar_wait_bounded(bar + 1, 0);
-    }
     };
     if constexpr (TILE == 256) {
         if (n <= TILE / 2) rows_from(std::integral_constant<int, NS / 2>{}, std::integral_constant<int, KO / 2>{});
