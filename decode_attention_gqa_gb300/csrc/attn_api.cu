@@ -220,9 +220,11 @@ int auto_short_kernel(int head_dim, int group, int n_q, int n_seq, int n_kv_head
     // By count: where one block per SM makes chunks of more than three quarters of the
     // wide tile (256 rows at head_dim 128, 128 at 256), the wide tile with balanced
     // chunks, one block per SM (the 7b layer: 38 splits of 224 rows, 5.89 -> 5.51 us per
-    // layer at full context; the long layer: 76 splits of 112 rows, 6.32 -> 6.00 us)
-    if (n_q == 1 && (head_dim == 128 || head_dim == 256) && n_splits == 0 && split_len == 0 && cap > 0 &&
-        sm_count > 0) {
+    // layer at full context; the long layer: 76 splits of 112 rows, 6.32 -> 6.00 us);
+    // several query rows too at head_dim 128 with one query group per KV head
+    const int qgroups1 = (n_q * group + attn::kMqHeadsPerBlock - 1) / attn::kMqHeadsPerBlock;
+    if ((n_q == 1 ? head_dim == 128 || head_dim == 256 : head_dim == 128 && qgroups1 == 1) && n_splits == 0 &&
+        split_len == 0 && cap > 0 && sm_count > 0) {
         const int64_t wide = head_dim == 256 ? 128 : 256;      // the wide tile's rows
         const int64_t P1 = (int64_t)sm_count / ((int64_t)n_seq * n_kv_head);
         const int64_t c1 = P1 > 0 ? (cap + P1 - 1) / P1 : 0;
@@ -237,7 +239,7 @@ int auto_short_kernel(int head_dim, int group, int n_q, int n_seq, int n_kv_head
         return attn::kVariantTile;
     // splits longer than a tile (block length 128 at head_dim 256, 256 at 128): the wide
     // tile, one block per SM
-    if (n_q == 1 &&
+    if ((n_q == 1 || head_dim == 128) &&
         one_tile_fits(attn::kVariantTileWide, head_dim, group, n_q, n_seq, n_kv_head, cap, sm_count, n_splits,
                       split_len, kv_stable, ku))
         return attn::kVariantTileWide;
@@ -339,7 +341,7 @@ attn_status finish_plan(DeviceState *ds, int n_seq, int n_head, int n_kv_head, i
     if (split_len > 0 && (int64_t)P * split_len < cap) return ATTN_ERR_INVALID_ARG;
     // the one-tile kernel at head_dim 256 takes splits longer than its 96-row tile
     // in 128-row tiles
-    if (pl.variant == attn::kVariantTile && n_q == 1 &&
+    if (pl.variant == attn::kVariantTile && (n_q == 1 || head_dim == 128) &&
         (split_len > 0 ? split_len > pl.ki.max_chunk : (cap_known && (int64_t)P * pl.ki.max_chunk < cap))) {
         const attn::KernelInfo kw = kernel_info(head_dim, pl.group, attn::kVariantTileWide);
         if (kw.available) {

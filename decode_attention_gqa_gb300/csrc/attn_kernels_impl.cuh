@@ -123,11 +123,12 @@ cudaError_t launch_partial_tile(const LaunchRequest &r)
 }
 
 // The one-tile mma.sync kernel for several causal query rows: 16 (row, head)
-// slots per block, grid (KV head x query group, split, sequence).
-template <int HD, typename KV>
+// slots per block, grid (KV head x query group, split, sequence); WIDE:
+// 256-row tiles, one block per SM.
+template <int HD, typename KV, bool WIDE = false>
 cudaError_t launch_partial_tile_mq(const LaunchRequest &r)
 {
-    using C = TileCfg<HD, kMqHeads, KV, true>;
+    using C = TileCfg<HD, kMqHeads, KV, true, WIDE>;
     alignas(64) CUtensorMap kmap, vmap;
     const int dt = kv_dtype_code<KV>();
     cudaError_t e = encode_kv_map4(&kmap, r.k_cache, r.n_seq, r.pa.cap, r.pa.n_kv_head, HD, 64, C::TILE, dt);
@@ -253,6 +254,9 @@ cudaError_t launch_for_hd(const LaunchRequest &r)
                 } else if (r.variant == kVariantTile) {
                     if constexpr (HD == 128) e = launch_partial_tile_mq<HD, KV>(r);
                     else return cudaErrorInvalidValue;
+                } else if (r.variant == kVariantTileWide) {
+                    if constexpr (HD == 128) e = launch_partial_tile_mq<HD, KV, true>(r);
+                    else return cudaErrorInvalidValue;
                 } else {
                     e = launch_partial<TcMqCfg<HD, KV>, HD, kMqHeads, KV>(r);
                 }
@@ -330,12 +334,13 @@ KernelInfo kernel_info_for_hd(int group, int variant, bool multi)
     }
     if (variant == kVariantTileWide) {
         if constexpr (HD == 128 || HD == 256) {
-            if (multi) return k;
+            if (multi && HD != 128) return k;   // several query rows: head_dim 128 only
             using C = TileCfg<HD, 8, __half, false, true>;
             k.tile_rows = C::TILE;
             k.granule = C::GRANULE;
             k.stages = 1;
-            k.blocks_per_sm = (int)(233472u / (C::SMEM_BYTES + 1024u));
+            const uint32_t smem = multi ? TileCfg<128, kMqHeads, __half, true, true>::SMEM_BYTES : C::SMEM_BYTES;
+            k.blocks_per_sm = (int)(233472u / (smem + 1024u));
             k.max_chunk = C::TILE;
             k.balanced = true;
             k.available = true;

@@ -63,7 +63,6 @@ template <int HD, int G, typename KV, bool MQ = false, bool WIDE = false>
 struct TileCfg {
     static_assert(HD == 128 || HD == 256, "the one-tile kernel is built for head_dim 128 and 256");
     static_assert(!MQ || HD == 128, "several query rows: head_dim 128 (two blocks per SM would not fit at 256)");
-    static_assert(!WIDE || !MQ, "the wide tile: one query row");
     // rows per block: 128 at head_dim 128 (three blocks per SM), 96 at 256 (two); the
     // wide tile, one block per SM, takes 256 rows at head_dim 128 and 128 at 256
     static constexpr int TILE = HD == 256 ? (WIDE ? 128 : 96) : (WIDE ? 256 : 128);
@@ -714,155 +713,166 @@ attn_split_partial_tile_mq(const __grid_constant__ CUtensorMap kmap, const __gri
     const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar + 0, 0));
     if (!ok && lane == 0) { flags[0] = 1; atomicOr(a.err, kErrPipelineTimeout); }
 
-    // ---- a3: S for rows r0 .. r0 + WR - 1, hi and lo q into one accumulator ----
-    const int r0 = warp * Cfg::WR;
-    float sc[NS][2][2];                       // [n-tile][slot g, g + 8][row 2t, 2t + 1]
-    {
-        float c[2][NS][4];
+    // a3 .. a6 for NSX S n-tiles per warp from tile row 16 K0 on: the whole tile, or,
+    // in the 256-row tile, its last 128 rows only when the split has no more
+    auto rows_from = [&](auto nsx_c, auto k0_c) {
+        constexpr int NSX = decltype(nsx_c)::value, K0 = decltype(k0_c)::value;
+        // ---- a3: S for rows r0 .. r0 + 8 NSX - 1, hi and lo q into one accumulator ----
+        const int r0 = 16 * K0 + warp * 8 * NSX;
+        float sc[NSX][2][2];                      // [n-tile][slot g, g + 8][row 2t, 2t + 1]
+        {
+            float c[2][NSX][4];
 #pragma unroll
-        for (int e = 0; e < 2; ++e)
+            for (int e = 0; e < 2; ++e)
 #pragma unroll
-            for (int j = 0; j < NS; ++j)
+                for (int j = 0; j < NSX; ++j)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) c[e][j][i] = 0.f;
-        if (ok) {
+                    for (int i = 0; i < 4; ++i) c[e][j][i] = 0.f;
+            if (ok) {
 #pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
-                uint32_t ah[4], al[4];
-                ldsm_a16<HD>(ah, qhi, kk, lane);
-                ldsm_a16<HD>(al, qlo, kk, lane);
+                for (int kk = 0; kk < KS; ++kk) {
+                    uint32_t ah[4], al[4];
+                    ldsm_a16<HD>(ah, qhi, kk, lane);
+                    ldsm_a16<HD>(al, qlo, kk, lane);
 #pragma unroll
-                for (int j = 0; j < NS; j += 2) {
-                    uint32_t b[4];
-                    const int krow = r0 + 8 * j + (i8 >> 1) * 8 + (lane & 7);
-                    ldsm_x4(b, smem + Cfg::OFF_K + tile_unit_offset<HD, TILE>(krow, 2 * kk + (i8 & 1)));
-                    mma_16816<KV>(c[kk & 1][j], ah, b[0], b[1]);
-                    mma_16816<KV>(c[kk & 1][j], al, b[0], b[1]);
-                    mma_16816<KV>(c[kk & 1][j + 1], ah, b[2], b[3]);
-                    mma_16816<KV>(c[kk & 1][j + 1], al, b[2], b[3]);
+                    for (int j = 0; j < NSX; j += 2) {
+                        uint32_t b[4];
+                        const int krow = r0 + 8 * j + (i8 >> 1) * 8 + (lane & 7);
+                        ldsm_x4(b, smem + Cfg::OFF_K + tile_unit_offset<HD, TILE>(krow, 2 * kk + (i8 & 1)));
+                        mma_16816<KV>(c[kk & 1][j], ah, b[0], b[1]);
+                        mma_16816<KV>(c[kk & 1][j], al, b[0], b[1]);
+                        mma_16816<KV>(c[kk & 1][j + 1], ah, b[2], b[3]);
+                        mma_16816<KV>(c[kk & 1][j + 1], al, b[2], b[3]);
+                    }
                 }
             }
+#pragma unroll
+            for (int j = 0; j < NSX; ++j)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = r0 + 8 * j + 2 * t + e;
+                    const int64_t row = hi - TILE + r;              // the cache row
+                    const bool in_split = r >= TILE - n;
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const float v = (c[0][j][2 * k + e] + c[1][j][2 * k + e]) * isc[k];
+                        sc[j][k][e] = in_split && row <= last[k] ? v : -INFINITY;
+                    }
+                }
         }
+        // ---- a4: each slot's maximum over the block ----
 #pragma unroll
-        for (int j = 0; j < NS; ++j)
+        for (int k = 0; k < 2; ++k) {
+            float m = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int r = r0 + 8 * j + 2 * t + e;
-                const int64_t row = hi - TILE + r;              // the cache row
-                const bool in_split = r >= TILE - n;
+            for (int j = 0; j < NSX; ++j) m = fmaxf(m, fmaxf(sc[j][k][0], sc[j][k][1]));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            if (t == 0) red_m[warp * 16 + g + 8 * k] = m;
+        }
+        __syncthreads();                          // the maxima are in; S is done, so the Q tiles are dead
+        float base[2];
+        bool none[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            float M = red_m[g + 8 * k];
+#pragma unroll
+            for (int w = 1; w < Cfg::NW; ++w) M = fmaxf(M, red_m[w * 16 + g + 8 * k]);
+            none[k] = M == -INFINITY;             // the slot sees no row of this split
+            base[k] = M - Cfg::OFF;
+        }
+        {
+            uint8_t *phi = smem + Cfg::OFF_P, *plo = phi + Cfg::P_TILE;
+            float lsum[2] = {0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < NSX; ++j) {
+                const int r = r0 + 8 * j;
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
-                    const float v = (c[0][j][2 * k + e] + c[1][j][2 * k + e]) * isc[k];
-                    sc[j][k][e] = in_split && row <= last[k] ? v : -INFINITY;
+                    const float p0 = none[k] ? 0.f : ex2(sc[j][k][0] - base[k]);
+                    const float p1 = none[k] ? 0.f : ex2(sc[j][k][1] - base[k]);
+                    lsum[k] += p0 + p1;
+                    const uint32_t hw = float2_to_kv2<KV>(p0, p1);
+                    const float2 f = kv2_to_float2<KV>(hw);
+                    const uint32_t lw = float2_to_kv2<KV>(p0 - f.x, p1 - f.y);
+                    const uint32_t off = tile_unit_offset<TILE, 16>(g + 8 * k, r >> 3) + 4 * t;
+                    *reinterpret_cast<uint32_t *>(phi + off) = hw;
+                    *reinterpret_cast<uint32_t *>(plo + off) = lw;
                 }
             }
-    }
-    // ---- a4: each slot's maximum over the block ----
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        float m = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < NS; ++j) m = fmaxf(m, fmaxf(sc[j][k][0], sc[j][k][1]));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        if (t == 0) red_m[warp * 16 + g + 8 * k] = m;
-    }
-    __syncthreads();                          // the maxima are in; S is done, so the Q tiles are dead
-    float base[2];
-    bool none[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        float M = red_m[g + 8 * k];
-#pragma unroll
-        for (int w = 1; w < Cfg::NW; ++w) M = fmaxf(M, red_m[w * 16 + g + 8 * k]);
-        none[k] = M == -INFINITY;             // the slot sees no row of this split
-        base[k] = M - Cfg::OFF;
-    }
-    {
-        uint8_t *phi = smem + Cfg::OFF_P, *plo = phi + Cfg::P_TILE;
-        float lsum[2] = {0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < NS; ++j) {
-            const int r = r0 + 8 * j;
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-                const float p0 = none[k] ? 0.f : ex2(sc[j][k][0] - base[k]);
-                const float p1 = none[k] ? 0.f : ex2(sc[j][k][1] - base[k]);
-                lsum[k] += p0 + p1;
-                const uint32_t hw = float2_to_kv2<KV>(p0, p1);
-                const float2 f = kv2_to_float2<KV>(hw);
-                const uint32_t lw = float2_to_kv2<KV>(p0 - f.x, p1 - f.y);
-                const uint32_t off = tile_unit_offset<TILE, 16>(g + 8 * k, r >> 3) + 4 * t;
-                *reinterpret_cast<uint32_t *>(phi + off) = hw;
-                *reinterpret_cast<uint32_t *>(plo + off) = lw;
+                float l = lsum[k];
+                l += __shfl_xor_sync(0xffffffffu, l, 1);
+                l += __shfl_xor_sync(0xffffffffu, l, 2);
+                if (t == 0) red_l[warp * 16 + g + 8 * k] = l;
             }
         }
+        bool vok = ok;
+        if (vok) vok = __all_sync(0xffffffffu, mbar_wait_bounded(bar + 1, 0));
+        if (ok && !vok && lane == 0) { flags[0] = 1; atomicOr(a.err, kErrPipelineTimeout); }
+        __syncthreads();                          // P and the sums are in; every V wait is done
+        // ---- a5: O = P · V for dimensions d0 .. d0 + DW - 1, hi and lo P into one accumulator ----
+        const int d0 = warp * Cfg::DW;
+        const bool abort = flags[0] != 0;
+        if (!abort) {
+            float o[2][NO][4];
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            float l = lsum[k];
-            l += __shfl_xor_sync(0xffffffffu, l, 1);
-            l += __shfl_xor_sync(0xffffffffu, l, 2);
-            if (t == 0) red_l[warp * 16 + g + 8 * k] = l;
-        }
-    }
-    bool vok = ok;
-    if (vok) vok = __all_sync(0xffffffffu, mbar_wait_bounded(bar + 1, 0));
-    if (ok && !vok && lane == 0) { flags[0] = 1; atomicOr(a.err, kErrPipelineTimeout); }
-    __syncthreads();                          // P and the sums are in; every V wait is done
-    // ---- a5: O = P · V for dimensions d0 .. d0 + DW - 1, hi and lo P into one accumulator ----
-    const int d0 = warp * Cfg::DW;
-    const bool abort = flags[0] != 0;
-    if (!abort) {
-        float o[2][NO][4];
+            for (int e = 0; e < 2; ++e)
 #pragma unroll
-        for (int e = 0; e < 2; ++e)
+                for (int j = 0; j < NO; ++j)
 #pragma unroll
-            for (int j = 0; j < NO; ++j)
+                    for (int i = 0; i < 4; ++i) o[e][j][i] = 0.f;
+            const uint8_t *phi = smem + Cfg::OFF_P, *plo = phi + Cfg::P_TILE;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) o[e][j][i] = 0.f;
-        const uint8_t *phi = smem + Cfg::OFF_P, *plo = phi + Cfg::P_TILE;
+            for (int kk = K0; kk < KO; ++kk) {
+                uint32_t ah[4], al[4];
+                ldsm_a16<TILE>(ah, phi, kk, lane);
+                ldsm_a16<TILE>(al, plo, kk, lane);
+                const int vrow = 16 * kk + (i8 & 1) * 8 + (lane & 7);
 #pragma unroll
-        for (int kk = 0; kk < KO; ++kk) {
-            uint32_t ah[4], al[4];
-            ldsm_a16<TILE>(ah, phi, kk, lane);
-            ldsm_a16<TILE>(al, plo, kk, lane);
-            const int vrow = 16 * kk + (i8 & 1) * 8 + (lane & 7);
-#pragma unroll
-            for (int j = 0; j < NO; j += 2) {
-                uint32_t b[4];
-                ldsm_x4_trans(b, smem + Cfg::OFF_V + tile_unit_offset<HD, TILE>(vrow, (d0 >> 3) + j + (i8 >> 1)));
-                mma_16816<KV>(o[kk & 1][j], ah, b[0], b[1]);
-                mma_16816<KV>(o[kk & 1][j], al, b[0], b[1]);
-                mma_16816<KV>(o[kk & 1][j + 1], ah, b[2], b[3]);
-                mma_16816<KV>(o[kk & 1][j + 1], al, b[2], b[3]);
+                for (int j = 0; j < NO; j += 2) {
+                    uint32_t b[4];
+                    ldsm_x4_trans(b, smem + Cfg::OFF_V + tile_unit_offset<HD, TILE>(vrow, (d0 >> 3) + j + (i8 >> 1)));
+                    mma_16816<KV>(o[kk & 1][j], ah, b[0], b[1]);
+                    mma_16816<KV>(o[kk & 1][j], al, b[0], b[1]);
+                    mma_16816<KV>(o[kk & 1][j + 1], ah, b[2], b[3]);
+                    mma_16816<KV>(o[kk & 1][j + 1], al, b[2], b[3]);
+                }
             }
-        }
-        // ---- a6: oc of both slots for these dimensions; (mx, S) per slot ----
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int hp = QS::slot_head(a, hk, qg, g + 8 * k);
-            if (hp < 0) continue;
-            float *dst = a.ws_o + (((size_t)s * heads + hp) * P + sp) * HD + d0 + 2 * t;
-#pragma unroll
-            for (int j = 0; j < NO; ++j)
-                *reinterpret_cast<float2 *>(dst + 8 * j) =
-                    make_float2(o[0][j][2 * k] + o[1][j][2 * k], o[0][j][2 * k + 1] + o[1][j][2 * k + 1]);
-        }
-        if (warp == 0 && t == 0) {
+            // ---- a6: oc of both slots for these dimensions; (mx, S) per slot ----
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 const int hp = QS::slot_head(a, hk, qg, g + 8 * k);
                 if (hp < 0) continue;
-                float L = 0.f;
+                float *dst = a.ws_o + (((size_t)s * heads + hp) * P + sp) * HD + d0 + 2 * t;
 #pragma unroll
-                for (int w = 0; w < Cfg::NW; ++w) L += red_l[w * 16 + g + 8 * k];
-                a.ws_ml[((size_t)s * heads + hp) * P + sp] =
-                    make_float2(none[k] ? -INFINITY : base[k], none[k] ? 0.f : L);
+                for (int j = 0; j < NO; ++j)
+                    *reinterpret_cast<float2 *>(dst + 8 * j) =
+                        make_float2(o[0][j][2 * k] + o[1][j][2 * k], o[0][j][2 * k + 1] + o[1][j][2 * k + 1]);
             }
+            if (warp == 0 && t == 0) {
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int hp = QS::slot_head(a, hk, qg, g + 8 * k);
+                    if (hp < 0) continue;
+                    float L = 0.f;
+#pragma unroll
+                    for (int w = 0; w < Cfg::NW; ++w) L += red_l[w * 16 + g + 8 * k];
+                    a.ws_ml[((size_t)s * heads + hp) * P + sp] =
+                        make_float2(none[k] ? -INFINITY : base[k], none[k] ? 0.f : L);
+                }
+            }
+        } else if (tid == 0) {
+            (void)mbar_wait_bounded(bar + 0, 0);
+            (void)mbar_wait_bounded(bar + 1, 0);
         }
-    } else if (tid == 0) {
-        (void)mbar_wait_bounded(bar + 0, 0);
-        (void)mbar_wait_bounded(bar + 1, 0);
+    };
+    if constexpr (TILE == 256) {
+        if (n <= TILE / 2) rows_from(std::integral_constant<int, NS / 2>{}, std::integral_constant<int, KO / 2>{});
+        else rows_from(std::integral_constant<int, NS>{}, std::integral_constant<int, 0>{});
+    } else {
+        rows_from(std::integral_constant<int, NS>{}, std::integral_constant<int, 0>{});
     }
 }
 

@@ -105,7 +105,7 @@ typedef enum {
                                  when a split needs more than T rows (block lengths T+1..W, or
                                  n_splits * T < cap <= n_splits * W);
                                  head_dim 128 or 256 with one query row, head_dim 128 with
-                                 several (16 (query row, head) pairs per block);
+                                 several (16 (query row, head) pairs per block, either tile);
                                  ATTN_ERR_UNSUPPORTED otherwise. Every split must fit one tile
                                  (ATTN_ERR_INVALID_ARG otherwise). By count, a chunk
                                  ceil(nkv / n_splits) of more than 3T/4 rows is rounded up to
@@ -339,8 +339,9 @@ int attn_split_heuristic_ex(int n_seq, int n_q, int n_head, int n_kv_head, int h
  * and the heuristic's splits, one tile each, in one wave of its blocks: the
  * one-tile mma.sync kernel (ATTN_VARIANT_TC_TILE; 3 blocks per SM at head_dim
  * 128, 2 at 256, or 1 with its wide tiles where one block per SM makes splits
- * longer than the plain tile) for one query row at head_dim 128 or 256 and
- * for several at 128 (ceil(n_q * group / 16) blocks per split and KV head);
+ * longer than the plain tile -- for several query rows with one 16-slot group
+ * per KV head) for one query row at head_dim 128 or 256 and for several at 128
+ * (ceil(n_q * group / 16) blocks per split and KV head);
  * else tcgen05 for several query rows at head_dim 256 when n_q * group <= 16 (a
  * KV head's (row, head) pairs in one block, 1 block per SM) -- and otherwise the
  * streaming mma.sync tensor-core kernel (head_dim % 16 == 0) or the CUDA-core

@@ -147,9 +147,10 @@ def test_split_heuristic_for_flagged_calls(lib):
     assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_STABLE, n_q=4) == 37
     # short: one 128-row tile per split on the one-tile kernel, 16 x 4 x 2 blocks
     assert h(1, 28, 4, 128, 2048, 152, pkg.ATTN_KV_STABLE, n_q=4) == 16
-    # 2 rows x 7 heads = 14 pairs: one group, so variant 0 runs the one-tile kernel with one
-    # 128-row tile per split; the streaming mma.sync kernel keeps its ring-sized blocks
-    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_STABLE, n_q=2) == 64
+    # 2 rows x 7 heads = 14 pairs: one group, so variant 0 runs the one-tile kernel with its
+    # 256-row tiles, 38 balanced splits; the streaming mma.sync kernel keeps its ring-sized
+    # blocks
+    assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_KV_STABLE, n_q=2) == 38
     assert h(1, 28, 4, 128, 8192, 152, TC | S, n_q=2) == 43
     assert h(1, 28, 4, 128, 8192, 152, pkg.ATTN_VARIANT_SIMT, n_q=2) == 0  # tensor cores only
     # the CUDA-core kernel has its own granule and residency

@@ -458,17 +458,20 @@ def test_several_query_rows_full_7b(pkg, n_q):
     lay = syn.make_layer(w)
     rng = np.random.Generator(np.random.PCG64([7007, n_q]))
     q = rng.standard_normal((1, n_q, w.n_head, w.head_dim), dtype=np.float32)
-    P = w.cap // TILE[128]
     scale = 1 / math.sqrt(w.head_dim)
-    for ctx in (w.cap, 3001):
-        pos = np.array([ctx - 1], np.int32)
-        dev = to_device(dict(lay, q=q, positions=pos))
-        out = torch.full_like(dev["q"], float("nan"))
-        pkg.attn_decode_multi(dev["q"], dev["k"], dev["v"], dev["positions"], out, 1, n_q, w.n_head,
-                              w.n_kv_head, w.head_dim, scale, w.cap, n_splits=P, variant=VT)
-        ref = oracle.attn_decode_multi(q, lay["k"], lay["v"], pos, n_q, w.n_head, w.n_kv_head,
-                                       w.head_dim, w.cap, scale, n_threads=8)
-        assert_close(out.cpu().numpy(), ref, "7b n_q=%d ctx %d" % (n_q, ctx))
+    # 128-row tiles (64 splits), and 256-row tiles (38 splits: balanced 224-row chunks at
+    # full context, whole tiles below 3/4 of a tile, half tiles -- each block on its last
+    # 128 rows -- while the context fits in four tiles)
+    for P in (w.cap // TILE[128], 38):
+        for ctx in (w.cap, 3001, 1000, 200, n_q):
+            pos = np.array([ctx - 1], np.int32)
+            dev = to_device(dict(lay, q=q, positions=pos))
+            out = torch.full_like(dev["q"], float("nan"))
+            pkg.attn_decode_multi(dev["q"], dev["k"], dev["v"], dev["positions"], out, 1, n_q, w.n_head,
+                                  w.n_kv_head, w.head_dim, scale, w.cap, n_splits=P, variant=VT)
+            ref = oracle.attn_decode_multi(q, lay["k"], lay["v"], pos, n_q, w.n_head, w.n_kv_head,
+                                           w.head_dim, w.cap, scale, n_threads=8)
+            assert_close(out.cpu().numpy(), ref, "7b n_q=%d P=%d ctx %d" % (n_q, P, ctx))
 
 
 @pytest.mark.parametrize("n_q,G", [(2, 8), (3, 5), (5, 4), (16, 1)])
