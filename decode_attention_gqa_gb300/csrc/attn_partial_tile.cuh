@@ -6,9 +6,10 @@
 // One block per (split sp, KV head hk, sequence s): the static grid of minfer
 // "10 · R4" §2.2 with the KV head in place of the query head, so the whole
 // group is served from one K/V read (Red Lite dev35 "Change"). The split is
-// one tile of TILE rows (128 at head_dim 128, 96 at 256), so the block sees
-// each row once and its softmax is one pass with a block-wide maximum (§2.1
-// with a single step). Four warps:
+// one tile of TILE rows (128 at head_dim 128, 96 at 256; the wide tiles, one
+// block per SM: 256 at 128, 128 at 256), so the block sees each row once and
+// its softmax is one pass with a block-wide maximum (§2.1 with a single step).
+// Four warps:
 //   1. TMA brings the TILE cache rows that end at hi, K and V on separate
 //      mbarriers (128-byte swizzled; rows in front of the sequence arrive as
 //      zeros, other rows outside the split are earlier rows of the same
@@ -27,12 +28,16 @@
 //      with the block's final accumulator for its dimensions.
 //   6. a6: each warp writes its dimensions of oc for every head; one thread
 //      per head writes (mx, S), S from the warps' partial sums.
+// A 256-row tile whose split holds at most 128 rows runs steps 3-6 on its last
+// 128 rows only (the 128-row tile's chain; both paths are compiled, the block
+// picks one from its row count).
 // By block length (Red Lite dev35 "Change": split sp covers [sp·blk, sp·blk +
 // blk)) with blk dividing the tile, a second kernel lets one block serve
-// SPB = TILE / blk consecutive splits from one tile: the maxima and sums are
-// taken per split (over 8-row groups through shared memory), O = P · V is
-// accumulated one split at a time over that split's k-steps, and every warp
-// writes each split's partial for its dimensions.
+// SPB = TILE / blk consecutive splits from one tile: one block-wide maximum as
+// every split's reference, the sums per split (over 8-row groups through
+// shared memory), O = P · V as one sweep over the tile's k-steps that writes
+// each split's accumulator at the split's end.
+// Several causal query rows: a third kernel serves 16 (query row, head) slots.
 #pragma once
 
 #include <type_traits>
