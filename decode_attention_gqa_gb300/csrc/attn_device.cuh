@@ -148,11 +148,11 @@ __device__ __forceinline__ void split_range(int64_t nkv, int sp, int n_splits, i
 // rows only, so that a split count sized for one block per SM balances the
 // rows over the blocks (the 7b layer at full context on 256-row tiles: 38
 // splits of 216 -> 224 rows on 152 SMs); shorter chunks are rounded up to whole
-// tiles (few, full blocks for short contexts), or, on the 256-row tile while
-// the context fits in four tiles, to half tiles, which that kernel runs on its
-// last 128 rows only (twice the blocks, each with the 128-row tile's chain).
+// tiles (few, full blocks for short contexts), or, on a wide tile (halves) while
+// the context fits in four tiles, to half tiles, which that kernel runs on the
+// tile's last half only (twice the blocks, each with half the chain).
 __device__ __forceinline__ void split_range_tile(int64_t nkv, int sp, int n_splits, int split_len,
-                                                 int tile, int64_t &lo, int64_t &hi)
+                                                 int tile, bool halves, int64_t &lo, int64_t &hi)
 {
     if (split_len > 0) {
         split_range(nkv, sp, n_splits, split_len, tile, lo, hi);
@@ -160,7 +160,7 @@ __device__ __forceinline__ void split_range_tile(int64_t nkv, int sp, int n_spli
     }
     int64_t chunk = (nkv + n_splits - 1) / n_splits;
     chunk = 4 * chunk > 3 * (int64_t)tile ? (chunk + 15) / 16 * 16
-          : tile >= 256 && nkv <= 4 * (int64_t)tile && 2 * chunk <= (int64_t)tile ? (int64_t)tile / 2
+          : halves && nkv <= 4 * (int64_t)tile && 2 * chunk <= (int64_t)tile ? (int64_t)tile / 2
           : (chunk + tile - 1) / tile * tile;
     lo = (int64_t)sp * chunk;
     hi = lo + chunk < nkv ? lo + chunk : nkv;

@@ -28,9 +28,9 @@
 //      with the block's final accumulator for its dimensions.
 //   6. a6: each warp writes its dimensions of oc for every head; one thread
 //      per head writes (mx, S), S from the warps' partial sums.
-// A 256-row tile whose split holds at most 128 rows runs steps 3-6 on its last
-// 128 rows only (the 128-row tile's chain; both paths are compiled, the block
-// picks one from its row count).
+// A wide tile whose split holds at most half its rows runs steps 3-6 on its
+// last half only (half the chain; both paths are compiled, the block picks one
+// from its row count).
 // By block length (Red Lite dev35 "Change": split sp covers [sp·blk, sp·blk +
 // blk)) with blk dividing the tile, a second kernel lets one block serve
 // SPB = TILE / blk consecutive splits from one tile: one block-wide maximum as
@@ -72,6 +72,7 @@ struct TileCfg {
     // wide tile, one block per SM, takes 256 rows at head_dim 128 and 128 at 256
     static constexpr int TILE = HD == 256 ? (WIDE ? 128 : 96) : (WIDE ? 256 : 128);
     static constexpr int MINB = WIDE ? 1 : HD == 256 ? 2 : 3;   // resident blocks per SM
+    static constexpr bool IS_WIDE = WIDE;               // half-tile splits run on the tile's last half
     // warps: S rows and O dimensions split NW ways (8 warps were measured slower, on the
     // 128-row tile and on both wide tiles: each warp reads all of Q and P from shared
     // memory, and more warps meet at each barrier)
@@ -230,7 +231,7 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
     bool pos_ok;
     const int64_t nkv = rows_attended(a, s, sp == 0 && hk == 0 && tid == 0, &pos_ok);
     int64_t lo, hi;
-    split_range_tile(nkv, sp, P, a.split_len, Cfg::TILE, lo, hi);
+    split_range_tile(nkv, sp, P, a.split_len, Cfg::TILE, Cfg::IS_WIDE, lo, hi);
     if (lo >= hi) {
         if (stable) pdl_wait();               // the workspace may still be read by the previous grid
         if (tid < G) a.ws_ml[((size_t)s * heads + (size_t)hk * G + tid) * P + sp] = make_float2(-INFINITY, 0.f);
@@ -302,8 +303,8 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
     if (!ok && lane == 0) { flags[0] = 1; atomicOr(a.err, kErrPipelineTimeout); }
 
     // a3 .. a6 for NSX S n-tiles per warp from tile row 16 K0 on: the whole tile
-    // (NSX = NS, K0 = 0), or, in the 256-row tile, its last 128 rows only when the
-    // split has no more (NSX = NS / 2, K0 = KO / 2: the chain of the 128-row tile)
+    // (NSX = NS, K0 = 0), or, in a wide tile, its last half only when the split has
+    // no more rows (NSX = NS / 2, K0 = KO / 2: half the chain)
     auto rows_from = [&](auto nsx_c, auto k0_c) {
         constexpr int NSX = decltype(nsx_c)::value, K0 = decltype(k0_c)::value;
         // ---- a3: S for this warp's rows r0 .. r0 + 8 NSX - 1 ----
@@ -397,7 +398,7 @@ attn_split_partial_tile(const __grid_constant__ CUtensorMap kmap, const __grid_c
             (void)mbar_wait_bounded(bar + 1, 0);
         }
     };
-    if constexpr (TILE == 256) {
+    if constexpr (Cfg::IS_WIDE) {
         if (n <= TILE / 2) rows_from(std::integral_constant<int, NS / 2>{}, std::integral_constant<int, KO / 2>{});
         else rows_from(std::integral_constant<int, NS>{}, std::integral_constant<int, 0>{});
     } else {
@@ -670,7 +671,7 @@ attn_split_partial_tile_mq(const __grid_constant__ CUtensorMap kmap, const __gri
     bool pos_ok;
     const int64_t nkv = rows_attended(a, s, sp == 0 && blockIdx.x == 0 && tid == 0, &pos_ok);
     int64_t lo, hi;
-    split_range_tile(nkv, sp, P, a.split_len, Cfg::TILE, lo, hi);
+    split_range_tile(nkv, sp, P, a.split_len, Cfg::TILE, Cfg::IS_WIDE, lo, hi);
     if (lo >= hi) {
         if (stable) pdl_wait();
         if (tid < 16) {
@@ -719,7 +720,7 @@ attn_split_partial_tile_mq(const __grid_constant__ CUtensorMap kmap, const __gri
     if (!ok && lane == 0) { flags[0] = 1; atomicOr(a.err, kErrPipelineTimeout); }
 
     // a3 .. a6 for NSX S n-tiles per warp from tile row 16 K0 on: the whole tile, or,
-    // in the 256-row tile, its last 128 rows only when the split has no more
+    // in a wide tile, its last half only when the split has no more rows
     auto rows_from = [&](auto nsx_c, auto k0_c) {
         constexpr int NSX = decltype(nsx_c)::value, K0 = decltype(k0_c)::value;
         // ---- a3: S for rows r0 .. r0 + 8 NSX - 1, hi and lo q into one accumulator ----
@@ -873,7 +874,7 @@ attn_split_partial_tile_mq(const __grid_constant__ CUtensorMap kmap, const __gri
             (void)mbar_wait_bounded(bar + 1, 0);
         }
     };
-    if constexpr (TILE == 256) {
+    if constexpr (Cfg::IS_WIDE) {
         if (n <= TILE / 2) rows_from(std::integral_constant<int, NS / 2>{}, std::integral_constant<int, KO / 2>{});
         else rows_from(std::integral_constant<int, NS>{}, std::integral_constant<int, 0>{});
     } else {

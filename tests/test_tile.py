@@ -218,6 +218,12 @@ def test_full_long_workload(pkg):
     assert v == VT
     for n in sorted({P, Pv, -(-w.cap // 96)}):
         _check(pkg, lay, w.n_head, w.n_kv_head, w.cap, "long P=%d" % n, hd=w.head_dim, n_splits=n)
+    # what variant 0 plans (128-row tiles) at shorter contexts: whole tiles, and half tiles --
+    # each block on its last 64 rows -- while the context fits in four tiles
+    for ctx in (2048, 513, 512, 300, 65, 64, 1):
+        case = dict(lay, positions=np.array([ctx - 1], np.int32))
+        _check(pkg, case, w.n_head, w.n_kv_head, w.cap, "long P=%d ctx %d" % (Pv, ctx), hd=w.head_dim,
+               n_splits=Pv)
 
 
 def test_full_7b_workload(pkg):
