@@ -654,7 +654,11 @@ def measure_one(args, rank, world, local):
                 if c == ctx_end or c > w.cap or c - 1 - (W + K) < 0:
                     continue
                 m = measure(plan, c)
-                sweep["ctx%d" % c] = {"us_per_layer": round(m["ms"] * 1e3 / (K * L), 3),
+                # the plan (kernel and split count) follows the capacity, not the
+                # context, so every point runs the headline's kernel
+                sweep["ctx%d" % c] = {"partial_variant": roofline["partial_variant"],
+                                      "n_splits": plan.P,
+                                      "us_per_layer": round(m["ms"] * 1e3 / (K * L), 3),
                                       "gbs": round(m["bytes"] / (m["ms"] * 1e-3) / 1e9, 1),
                                       "partial_us": round(m["partial_us"], 3),
                                       "combine_us": round(m["combine_us"], 3)}
